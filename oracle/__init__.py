@@ -1,0 +1,288 @@
+"""fp64 CPU oracle for TurboQuant-style KV-cache compression (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference arm of ``bench.py`` may import this package.  The
+product path (``libtq.so`` and ``decode_attention_tq_gb300``) never imports it
+and shares no code with it; this wrapper only marshals numpy arrays into the
+plain C functions of ``oracle.c``, where every step of the method is written
+out (see the header of ``oracle.c`` for the passages each function follows).
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``
+against closed forms, library routines, brute force or values printed on the
+pages; nothing in this oracle is "parity unpinned" except the conventions the
+pages leave open (bit order, seeds), which are self-consistent by construction.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (-O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Format(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "k_qjl", "qjl_m", "page_size", "num_kv_heads")]
+
+
+class _Layout(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("slab_bytes", "page_bytes", "k_norm", "k_gamma", "k_codes", "k_signs", "v_norm", "v_codes")] + [
+        (n, C.c_int32) for n in ("k_code_bytes", "k_sign_bytes", "v_code_bytes")
+    ]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = C.CDLL(_LIB_PATH)
+            P = C.c_void_p
+            i32, i64, dbl = C.c_int32, C.c_int64, C.c_double
+            lib.orc_half_to_double.argtypes = [C.c_uint16]
+            lib.orc_half_to_double.restype = dbl
+            lib.orc_lloyd_max_f64.argtypes = [C.c_int, P, P]
+            lib.orc_make_codebook.argtypes = [C.c_int, P, P]
+            lib.orc_quantize_scalar.argtypes = [C.c_int, P, dbl]
+            lib.orc_fwht.argtypes = [P, C.c_int]
+            lib.orc_fwht.restype = None
+            lib.orc_rotate.argtypes = [C.c_int, P, P, P]
+            lib.orc_rotate.restype = None
+            lib.orc_unrotate.argtypes = [C.c_int, P, P, P]
+            lib.orc_unrotate.restype = None
+            lib.orc_encode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int] + [P] * 12
+            lib.orc_decode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, dbl, dbl] + [P] * 6
+            lib.orc_pack_bits.argtypes = [C.c_int, C.c_int, P, P]
+            lib.orc_pack_bits.restype = None
+            lib.orc_unpack_bits.argtypes = [C.c_int, C.c_int, P, P]
+            lib.orc_unpack_bits.restype = None
+            lib.orc_page_layout.argtypes = [P, P]
+            lib.orc_encode.argtypes = [P, C.c_int, P, i64, P, P, i64, P, P, P, P, P, P, P]
+            lib.orc_decode.argtypes = [P, C.c_int, P, i64, P, i64, P, P, P, P]
+            lib.orc_attention.argtypes = [P, C.c_int, C.c_int, P, P, i64, P, C.c_int, P, P, P, P, C.c_int, P, P, P, P, P, P, C.c_int, P]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else C.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _fmt(f) -> _Format:
+    return _Format(int(f.head_dim), int(f.k_bits), int(f.v_bits), int(f.k_qjl), int(f.qjl_m), int(f.page_size), int(f.num_kv_heads))
+
+
+def _f16bits(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16:
+        return x.view(np.uint16)
+    if x.dtype == np.uint16:
+        return x
+    raise TypeError("expected float16 data")
+
+
+# ------------------------------------------------------------------ scalar --
+def half_to_double(bits: int) -> float:
+    return _load().orc_half_to_double(int(bits))
+
+
+def lloyd_max_f64(bits: int):
+    """fp64 Lloyd-Max centroids [2^b] and midpoints [2^b-1] for N(0,1)."""
+    c = np.zeros(256)
+    t = np.zeros(256)
+    it = _load().orc_lloyd_max_f64(bits, _ptr(c), _ptr(t))
+    if it < 0:
+        raise ValueError("bad bits")
+    L = 1 << bits
+    return c[:L].copy(), t[: L - 1].copy(), it
+
+
+def make_codebook(bits: int):
+    """The stored codebook: fp32 centroids [2^b] and fp32 midpoints [2^b-1]."""
+    L = 1 << bits
+    c = np.zeros(L, np.float32)
+    t = np.zeros(max(L - 1, 1), np.float32)
+    it = _load().orc_make_codebook(bits, _ptr(c), _ptr(t))
+    if it < 0:
+        raise ValueError("bad bits")
+    return c, t[: L - 1]
+
+
+def quantize_scalar(bits: int, midpoints, u: float) -> int:
+    m = _c(midpoints, np.float32)
+    return _load().orc_quantize_scalar(bits, _ptr(m), float(u))
+
+
+def fwht(x) -> np.ndarray:
+    y = _c(x, np.float64).copy()
+    _load().orc_fwht(_ptr(y), y.shape[-1])
+    return y
+
+
+def rotate(x, signs) -> np.ndarray:
+    x = _c(x, np.float64)
+    s = _c(signs, np.uint8)
+    y = np.zeros_like(x)
+    _load().orc_rotate(x.shape[-1], _ptr(s), _ptr(x), _ptr(y))
+    return y
+
+
+def unrotate(y, signs) -> np.ndarray:
+    y = _c(y, np.float64)
+    s = _c(signs, np.uint8)
+    x = np.zeros_like(y)
+    _load().orc_unrotate(y.shape[-1], _ptr(s), _ptr(y), _ptr(x))
+    return x
+
+
+# ------------------------------------------------------------------ vector --
+def encode_vector(x, bits, signs, centroids, midpoints, S=None, qjl_m=0):
+    """Encode one vector (fp64 values).  Returns a dict with norm, gamma, idx,
+    z, u, code_margin, sign_margin."""
+    x = _c(x, np.float64)
+    d = x.shape[0]
+    qjl = S is not None
+    m = int(qjl_m) if qjl else 0
+    idx = np.zeros(d, np.int32)
+    z = np.zeros(max(m, 1), np.uint8)
+    u = np.zeros(d)
+    cm = np.zeros(d)
+    sm = np.zeros(max(m, 1))
+    norm = C.c_double(0)
+    gamma = C.c_double(0)
+    Sa = _c(S, np.float32) if qjl else None
+    rc = _load().orc_encode_vector(
+        d, bits, int(qjl), m, _ptr(x), _ptr(_c(signs, np.uint8)), _ptr(_c(centroids, np.float32)),
+        _ptr(_c(midpoints, np.float32)), _ptr(Sa), C.byref(norm), C.byref(gamma), _ptr(idx), _ptr(z), _ptr(u), _ptr(cm), _ptr(sm),
+    )
+    if rc != 0:
+        raise ValueError(f"orc_encode_vector rc={rc}")
+    return dict(norm=norm.value, gamma=gamma.value, idx=idx, z=z[:m], u=u, code_margin=cm, sign_margin=sm[:m])
+
+
+def decode_vector(norm, idx, bits, signs, centroids, gamma=0.0, z=None, S=None, qjl_m=0):
+    idx = _c(idx, np.int32)
+    d = idx.shape[0]
+    qjl = S is not None
+    m = int(qjl_m) if qjl else 0
+    out = np.zeros(d)
+    za = _c(z, np.uint8) if qjl else None
+    Sa = _c(S, np.float32) if qjl else None
+    rc = _load().orc_decode_vector(
+        d, bits, int(qjl), m, float(norm), float(gamma), _ptr(idx), _ptr(za), _ptr(_c(signs, np.uint8)),
+        _ptr(_c(centroids, np.float32)), _ptr(Sa), _ptr(out),
+    )
+    if rc != 0:
+        raise ValueError(f"orc_decode_vector rc={rc}")
+    return out
+
+
+def pack_bits(vals, b: int) -> np.ndarray:
+    v = _c(vals, np.int32)
+    out = np.zeros((v.shape[0] * b + 7) // 8, np.uint8)
+    _load().orc_pack_bits(v.shape[0], b, _ptr(v), _ptr(out))
+    return out
+
+
+def unpack_bits(data, count: int, b: int) -> np.ndarray:
+    d = _c(data, np.uint8)
+    out = np.zeros(count, np.int32)
+    _load().orc_unpack_bits(count, b, _ptr(d), _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------------- paged --
+def page_layout(f) -> dict:
+    L = _Layout()
+    F = _fmt(f)
+    rc = _load().orc_page_layout(C.byref(F), C.byref(L))
+    if rc != 0:
+        raise ValueError("unsupported format for the oracle layout")
+    return {n: getattr(L, n) for n, _ in _Layout._fields_}
+
+
+def encode(f, kind: int, x, slot_mapping, pool, num_pages: int, signs, centroids, midpoints, S=None, diagnostics=False):
+    """Encode x [N,H,d] fp16 into ``pool`` (uint8, modified in place).
+    With ``diagnostics`` returns (rc, u, code_margin, sign_margin)."""
+    xb = _f16bits(x)
+    N = xb.shape[0]
+    H, d = int(f.num_kv_heads), int(f.head_dim)
+    m = int(f.qjl_m) if (kind == 0 and f.k_qjl) else 0
+    u = cm = sm = None
+    if diagnostics:
+        u = np.zeros((N, H, d))
+        cm = np.zeros((N, H, d))
+        sm = np.zeros((N, H, max(m, 1)))
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"]
+    F = _fmt(f)
+    rc = _load().orc_encode(
+        C.byref(F), kind, _ptr(xb), N, _ptr(_c(slot_mapping, np.int32)), _ptr(pool), int(num_pages), _ptr(_c(signs, np.uint8)),
+        _ptr(_c(centroids, np.float32)), _ptr(_c(midpoints, np.float32)), _ptr(None if S is None else _c(S, np.float32)),
+        _ptr(u), _ptr(cm), _ptr(sm),
+    )
+    if diagnostics:
+        return rc, u, cm, (sm[..., :m] if m else None)
+    return rc
+
+
+def decode(f, kind: int, pool, num_pages: int, slot_mapping, signs, centroids, S=None):
+    sl = _c(slot_mapping, np.int32)
+    N = sl.shape[0]
+    out = np.zeros((N, int(f.num_kv_heads), int(f.head_dim)))
+    F = _fmt(f)
+    rc = _load().orc_decode(
+        C.byref(F), kind, _ptr(pool), int(num_pages), _ptr(sl), N, _ptr(_c(signs, np.uint8)), _ptr(_c(centroids, np.float32)),
+        _ptr(None if S is None else _c(S, np.float32)), _ptr(out),
+    )
+    return rc, out
+
+
+def attention(f, q, pool, num_pages, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs, k_centroids, v_centroids,
+              S=None, heads=None):
+    """Exact-softmax decode attention over the compressed cache plus window.
+    q [B,Hq,d] fp16; k_win/v_win [B,Hkv,W,d] fp16 or None.  ``heads``: optional
+    list of b*Hq+qh; returns (rc, out) with out [B,Hq,d] or [len(heads),d]."""
+    qb = _f16bits(q)
+    B, Hq, d = qb.shape
+    bt = _c(block_tables, np.int32)
+    max_pages = bt.shape[1]
+    if k_win is None:
+        W = 0
+        kw = vw = wl = None
+    else:
+        kw = _f16bits(k_win)
+        vw = _f16bits(v_win)
+        W = kw.shape[2]
+        wl = _c(win_lens, np.int32)
+    hs = None if heads is None else _c(heads, np.int32)
+    n = B * Hq if hs is None else hs.shape[0]
+    out = np.zeros((n, d))
+    F = _fmt(f)
+    rc = _load().orc_attention(
+        C.byref(F), B, Hq, _ptr(qb), _ptr(pool), int(num_pages), _ptr(bt), max_pages, _ptr(_c(comp_lens, np.int32)), _ptr(kw), _ptr(vw),
+        _ptr(wl), W, _ptr(_c(k_signs, np.uint8)), _ptr(_c(v_signs, np.uint8)), _ptr(_c(k_centroids, np.float32)),
+        _ptr(_c(v_centroids, np.float32)), _ptr(None if S is None else _c(S, np.float32)), _ptr(hs), n, _ptr(out),
+    )
+    if hs is None:
+        out = out.reshape(B, Hq, d)
+    return rc, out

@@ -1,0 +1,558 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for TurboQuant-style KV-cache
+ * compression (encode, decode, and attention over a compressed paged cache).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline / reference arm may load this library.  The
+ * product path (libtq.so and its Python binding) never calls it, and it shares
+ * no code, header, table or constant generator with the CUDA path.
+ *
+ * Every step follows the pages, in their order, one vector at a time:
+ *
+ *   "TurboQuant Family Design Study for CPU and Browser WASM KV Caches"
+ *     - Capacity model (bytes per token 2*L*Hkv*d*s, M(T) with a W-token fp16
+ *       window)                                           -> orc_page_layout
+ *     - Why keys and values need different treatment (logit
+ *       l_i = q.k_i/sqrt(d), p = softmax(l), o = sum p_i v_i) -> orc_attention
+ *     - Placement relative to RoPE and attention (q.k = (Tq).(Tk) for an
+ *       orthogonal T)                                     -> attention algebra
+ *     - Dense and structured transform comparison (Rademacher signs then an
+ *       FWHT, per head, from a seed)                      -> fwht, rotate
+ *     - Packed format and complete bit accounting (section order inside a
+ *       fixed-token page, 16-byte alignment)              -> orc_page_layout
+ *   "From 0% to 100%: Debugging a KV Cache Compression Algorithm ..."
+ *     - Why this caught my eye (random rotation, then a precomputed Lloyd-Max
+ *       scalar quantizer per coordinate)                  -> orc_make_codebook
+ *     - The QJL detective story (Gaussian S, dequant scale sqrt(pi/2)/d,
+ *       unbiased inner products)                          -> qjl parts
+ *     - Round 2, Bug 4 (an all-zero block encodes to a true zero block)
+ *   aither-kvcache 2.4.0 README
+ *     - Algorithm (normalize, rotate, quantize, pack, store packed bytes plus
+ *       an fp32 norm; decoding reverses the steps)        -> encode/decode
+ *     - Zero-buffer fused attention (rotate q once, score in the rotated
+ *       domain, rotate back once)                         -> what the GPU does;
+ *       the oracle instead materializes every token and takes the exact
+ *       softmax, which is algebraically the same computation.
+ *
+ * Readings of points the pages leave open (each one is listed in the design doc):
+ *   - Codebook: Lloyd-Max for N(0,1), fp64 fixed-point iteration from a
+ *     symmetric start, symmetrized, then rounded to fp32.  Midpoints are the
+ *     fp64 averages of neighbouring fp64 centroids, rounded to fp32.
+ *   - u-domain: u = H (D . x) / ||x||, H the unnormalized Sylvester Hadamard
+ *     matrix, so ||u||^2 = d and each u_j is close to N(0,1).
+ *   - Quantizer: idx_j = #{k : t_k <= u_j} (ties go to the upper code).
+ *   - QJL: residual in the unit-sphere rotated domain, e = (u - c[idx])/sqrt(d),
+ *     gamma = ||e||, z_l = [(S e)_l >= 0]; dequant adds
+ *     sqrt(pi/2)/m * gamma * S^T (2z - 1).
+ *   - A zero vector stores n = 0, gamma = 0 and all codes / bits 0.
+ *   - Bitstreams are LSB-first: code j occupies bits [j*b, j*b+b), sign l is
+ *     bit l; byte k of the stream holds stream bits [8k, 8k+8).
+ *
+ * Build: gcc -O2 -std=c11 -fPIC -shared oracle.c -lm   (no fast-math)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_ARG (-1)
+#define ORC_ERR_RANGE (-2)
+
+#define ORC_PI 3.14159265358979323846
+
+typedef struct {
+  int32_t head_dim, k_bits, v_bits, k_qjl, qjl_m, page_size, num_kv_heads;
+} orc_format;
+
+typedef struct {
+  int64_t slab_bytes, page_bytes;
+  int64_t k_norm, k_gamma, k_codes, k_signs, v_norm, v_codes;
+  int32_t k_code_bytes, k_sign_bytes, v_code_bytes;
+} orc_layout;
+
+/* ------------------------------------------------------------------ fp16 -- */
+
+/* IEEE binary16 bit pattern -> exact double. */
+double orc_half_to_double(uint16_t h) {
+  int s = (h >> 15) & 1, e = (h >> 10) & 0x1f, m = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -24);
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp((double)(m | 0x400), e - 25);
+  return s ? -v : v;
+}
+
+/* ---------------------------------------------------------- Lloyd-Max ---- */
+
+static double std_normal_pdf(double x) { return exp(-0.5 * x * x) / sqrt(2.0 * ORC_PI); }
+/* Upper tail Q(x) = P(X > x), accurate in the far tail. */
+static double upper_tail(double x) { return 0.5 * erfc(x / sqrt(2.0)); }
+/* P(a < X < b) for X ~ N(0,1), written to avoid cancellation. */
+static double cell_probability(double a, double b) {
+  if (a >= 0.0) return upper_tail(a) - upper_tail(b);
+  if (b <= 0.0) return upper_tail(-b) - upper_tail(-a);
+  return 1.0 - upper_tail(b) - upper_tail(-a);
+}
+
+/*
+ * Lloyd-Max scalar quantizer for N(0,1) with 2^bits levels, in fp64.
+ * Fixed point: t_k = (c_k + c_{k+1})/2 and c_k = E[X | t_{k-1} < X < t_k]
+ *            = (phi(t_{k-1}) - phi(t_k)) / (Phi(t_k) - Phi(t_{k-1})).
+ * Returns the number of iterations used, or a negative error.
+ */
+int orc_lloyd_max_f64(int bits, double *c, double *t) {
+  if (bits < 1 || bits > 8) return ORC_ERR_ARG;
+  int L = 1 << bits;
+  for (int k = 0; k < L; k++) c[k] = (k - 0.5 * (L - 1)) * (6.0 / L);
+  int it;
+  for (it = 1; it <= 200000; it++) {
+    for (int k = 0; k + 1 < L; k++) t[k] = 0.5 * (c[k] + c[k + 1]);
+    double delta = 0.0;
+    for (int k = 0; k < L; k++) {
+      double a = (k == 0) ? -INFINITY : t[k - 1];
+      double b = (k == L - 1) ? INFINITY : t[k];
+      double pa = (k == 0) ? 0.0 : std_normal_pdf(a);
+      double pb = (k == L - 1) ? 0.0 : std_normal_pdf(b);
+      double ck = (pa - pb) / cell_probability(a, b);
+      double dd = fabs(ck - c[k]);
+      if (dd > delta) delta = dd;
+      c[k] = ck;
+    }
+    if (delta < 1e-15) break;
+  }
+  /* The start is symmetric, so the fixed point is too; remove rounding noise. */
+  for (int k = 0; k < L / 2; k++) {
+    double m = 0.5 * (c[L - 1 - k] - c[k]);
+    c[k] = -m;
+    c[L - 1 - k] = m;
+  }
+  for (int k = 0; k + 1 < L; k++) t[k] = 0.5 * (c[k] + c[k + 1]);
+  return it;
+}
+
+/* The stored codebook: fp32 centroids [2^b] and fp32 midpoints [2^b - 1]. */
+int orc_make_codebook(int bits, float *centroids, float *midpoints) {
+  double c[256], t[256];
+  int it = orc_lloyd_max_f64(bits, c, t);
+  if (it < 0) return it;
+  int L = 1 << bits;
+  for (int k = 0; k < L; k++) centroids[k] = (float)c[k];
+  for (int k = 0; k + 1 < L; k++) midpoints[k] = (float)t[k];
+  return it;
+}
+
+/* idx = #{k : t_k <= u}, t ascending (2^bits - 1 values). */
+int orc_quantize_scalar(int bits, const float *midpoints, double u) {
+  int L = 1 << bits, idx = 0;
+  for (int k = 0; k + 1 < L; k++)
+    if ((double)midpoints[k] <= u) idx++;
+  return idx;
+}
+
+/* ------------------------------------------------------------- rotation -- */
+
+static int is_pow2(int d) { return d >= 2 && (d & (d - 1)) == 0; }
+
+/* In-place unnormalized Walsh-Hadamard transform, Sylvester (natural) order:
+ * butterflies on pairs (i, i+h) for h = 1, 2, 4, ..., d/2. */
+void orc_fwht(double *x, int d) {
+  for (int h = 1; h < d; h <<= 1)
+    for (int i = 0; i < d; i += 2 * h)
+      for (int j = i; j < i + h; j++) {
+        double a = x[j], b = x[j + h];
+        x[j] = a + b;
+        x[j + h] = a - b;
+      }
+}
+
+/* sign_bit 1 means the coordinate is negated. */
+static double rademacher(const uint8_t *signs, int j) { return signs[j] ? -1.0 : 1.0; }
+
+/* Orthonormal structured rotation T x = H (D . x) / sqrt(d). */
+void orc_rotate(int d, const uint8_t *signs, const double *x, double *y) {
+  for (int j = 0; j < d; j++) y[j] = rademacher(signs, j) * x[j];
+  orc_fwht(y, d);
+  for (int j = 0; j < d; j++) y[j] /= sqrt((double)d);
+}
+
+/* Inverse: T^-1 y = D . (H y) / sqrt(d). */
+void orc_unrotate(int d, const uint8_t *signs, const double *y, double *x) {
+  for (int j = 0; j < d; j++) x[j] = y[j];
+  orc_fwht(x, d);
+  for (int j = 0; j < d; j++) x[j] = rademacher(signs, j) * x[j] / sqrt((double)d);
+}
+
+/* --------------------------------------------------------- one vector ---- */
+
+/*
+ * Encode one head vector x[d] (fp64 values of the fp16 input).
+ * Outputs: *norm = ||x||, *gamma = ||e|| (QJL only), idx[d], z[m] (QJL only).
+ * Optional diagnostics (may be NULL): u[d] (u-domain coordinates),
+ * code_margin[d] = min_k |u_j - t_k|, sign_margin[m] = |(S e)_l| / gamma.
+ */
+int orc_encode_vector(int d, int bits, int qjl, int m, const double *x, const uint8_t *signs,
+                      const float *centroids, const float *midpoints, const float *S,
+                      double *norm, double *gamma, int32_t *idx, uint8_t *z, double *u_out,
+                      double *code_margin, double *sign_margin) {
+  if (!is_pow2(d) || bits < 1 || bits > 8 || (qjl && m < 1)) return ORC_ERR_ARG;
+  int L = 1 << bits;
+  double *w = (double *)malloc(sizeof(double) * d);
+  double *e = (double *)malloc(sizeof(double) * d);
+  double ss = 0.0;
+  for (int j = 0; j < d; j++) ss += x[j] * x[j];
+  double n = sqrt(ss);
+  *norm = n;
+  if (qjl) *gamma = 0.0;
+  if (n == 0.0) { /* true zero block */
+    for (int j = 0; j < d; j++) {
+      idx[j] = 0;
+      if (u_out) u_out[j] = 0.0;
+      if (code_margin) code_margin[j] = 0.0;
+    }
+    if (qjl)
+      for (int l = 0; l < m; l++) {
+        z[l] = 0;
+        if (sign_margin) sign_margin[l] = 0.0;
+      }
+    free(w);
+    free(e);
+    return ORC_OK;
+  }
+  for (int j = 0; j < d; j++) w[j] = rademacher(signs, j) * x[j];
+  orc_fwht(w, d);
+  for (int j = 0; j < d; j++) {
+    double u = w[j] / n;
+    idx[j] = orc_quantize_scalar(bits, midpoints, u);
+    if (u_out) u_out[j] = u;
+    if (code_margin) {
+      double mg = INFINITY;
+      for (int k = 0; k + 1 < L; k++) {
+        double dd = fabs(u - (double)midpoints[k]);
+        if (dd < mg) mg = dd;
+      }
+      code_margin[j] = mg;
+    }
+    e[j] = (u - (double)centroids[idx[j]]) / sqrt((double)d);
+  }
+  if (qjl) {
+    double g2 = 0.0;
+    for (int j = 0; j < d; j++) g2 += e[j] * e[j];
+    double g = sqrt(g2);
+    *gamma = g;
+    for (int l = 0; l < m; l++) {
+      double p = 0.0;
+      for (int j = 0; j < d; j++) p += (double)S[(int64_t)l * d + j] * e[j];
+      z[l] = (p >= 0.0) ? 1 : 0;
+      if (sign_margin) sign_margin[l] = (g > 0.0) ? fabs(p) / g : 0.0;
+    }
+  }
+  free(w);
+  free(e);
+  return ORC_OK;
+}
+
+/*
+ * Decode one head vector:
+ *   y_hat = c[idx]/sqrt(d) + sqrt(pi/2)/m * gamma * S^T (2z - 1)   (QJL term optional)
+ *   x_hat = norm * D . (H y_hat) / sqrt(d)
+ */
+int orc_decode_vector(int d, int bits, int qjl, int m, double norm, double gamma, const int32_t *idx,
+                      const uint8_t *z, const uint8_t *signs, const float *centroids, const float *S,
+                      double *out) {
+  if (!is_pow2(d) || bits < 1 || bits > 8 || (qjl && m < 1)) return ORC_ERR_ARG;
+  double *y = (double *)malloc(sizeof(double) * d);
+  for (int j = 0; j < d; j++) y[j] = (double)centroids[idx[j]] / sqrt((double)d);
+  if (qjl) {
+    double scale = sqrt(ORC_PI / 2.0) / (double)m * gamma;
+    for (int j = 0; j < d; j++) {
+      double acc = 0.0;
+      for (int l = 0; l < m; l++) acc += (double)S[(int64_t)l * d + j] * (z[l] ? 1.0 : -1.0);
+      y[j] += scale * acc;
+    }
+  }
+  orc_fwht(y, d);
+  for (int j = 0; j < d; j++) out[j] = norm * rademacher(signs, j) * y[j] / sqrt((double)d);
+  free(y);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------ bitstreams -- */
+
+/* LSB-first: value j occupies stream bits [j*b, j*b + b). */
+void orc_pack_bits(int count, int b, const int32_t *vals, uint8_t *out) {
+  int nbytes = (count * b + 7) / 8;
+  memset(out, 0, (size_t)nbytes);
+  for (int j = 0; j < count; j++)
+    for (int i = 0; i < b; i++) {
+      int bit = j * b + i;
+      if ((vals[j] >> i) & 1) out[bit / 8] |= (uint8_t)(1u << (bit % 8));
+    }
+}
+
+void orc_unpack_bits(int count, int b, const uint8_t *in, int32_t *vals) {
+  for (int j = 0; j < count; j++) {
+    int v = 0;
+    for (int i = 0; i < b; i++) {
+      int bit = j * b + i;
+      v |= ((in[bit / 8] >> (bit % 8)) & 1) << i;
+    }
+    vals[j] = v;
+  }
+}
+
+/* ---------------------------------------------------------- page layout -- */
+
+static int64_t align16(int64_t x) { return (x + 15) / 16 * 16; }
+
+/*
+ * One pool per layer: [num_pages][num_kv_heads] head-slabs.  Inside a slab,
+ * the section order of the packed-format passage: K norms (fp32 [P]),
+ * K QJL gammas (fp32 [P], QJL only), K codes ([P][d*kb/8]), K sign bits
+ * ([P][m/8], QJL only), V norms (fp32 [P]), V codes ([P][d*vb/8]); every
+ * section starts on a 16-byte boundary and the slab is padded to 16 bytes.
+ */
+int orc_page_layout(const orc_format *f, orc_layout *L) {
+  if (!f || !L) return ORC_ERR_ARG;
+  if (!is_pow2(f->head_dim) || f->k_bits < 1 || f->k_bits > 8 || f->v_bits < 1 || f->v_bits > 8 ||
+      f->page_size < 1 || f->num_kv_heads < 1)
+    return ORC_ERR_ARG;
+  if ((f->head_dim * f->k_bits) % 8 || (f->head_dim * f->v_bits) % 8) return ORC_ERR_ARG;
+  if (f->k_qjl && (f->qjl_m < 8 || f->qjl_m % 8)) return ORC_ERR_ARG;
+  int64_t P = f->page_size, off = 0;
+  L->k_code_bytes = f->head_dim * f->k_bits / 8;
+  L->v_code_bytes = f->head_dim * f->v_bits / 8;
+  L->k_sign_bytes = f->k_qjl ? f->qjl_m / 8 : 0;
+  L->k_norm = off;
+  off = align16(off + 4 * P);
+  L->k_gamma = off;
+  if (f->k_qjl) off = align16(off + 4 * P);
+  L->k_codes = off;
+  off = align16(off + P * L->k_code_bytes);
+  L->k_signs = off;
+  if (f->k_qjl) off = align16(off + P * L->k_sign_bytes);
+  L->v_norm = off;
+  off = align16(off + 4 * P);
+  L->v_codes = off;
+  off = align16(off + P * L->v_code_bytes);
+  L->slab_bytes = off;
+  L->page_bytes = off * f->num_kv_heads;
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------ paged cache -- */
+
+static void put_f32(uint8_t *p, float v) { memcpy(p, &v, 4); }
+static float get_f32(const uint8_t *p) {
+  float v;
+  memcpy(&v, p, 4);
+  return v;
+}
+
+/*
+ * Encode N tokens x[N][H][d] (fp16 bits) of one kind (0 = K, 1 = V) into the
+ * pool at slots slot_mapping[n] = page * P + offset (negative slot: skipped).
+ * Diagnostics (nullable): u_out / code_margin [N][H][d], sign_margin [N][H][m].
+ */
+int orc_encode(const orc_format *f, int kind, const uint16_t *x, int64_t N, const int32_t *slot_mapping,
+               uint8_t *pool, int64_t num_pages, const uint8_t *signs, const float *centroids,
+               const float *midpoints, const float *S, double *u_out, double *code_margin,
+               double *sign_margin) {
+  orc_layout L;
+  if (orc_page_layout(f, &L) != ORC_OK) return ORC_ERR_ARG;
+  int d = f->head_dim, H = f->num_kv_heads, P = f->page_size;
+  int bits = kind == 0 ? f->k_bits : f->v_bits;
+  int qjl = (kind == 0) && f->k_qjl;
+  int m = qjl ? f->qjl_m : 0;
+  int code_bytes = kind == 0 ? L.k_code_bytes : L.v_code_bytes;
+  double *xv = (double *)malloc(sizeof(double) * d);
+  int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * d);
+  uint8_t *z = (uint8_t *)malloc((size_t)(m > 0 ? m : 1));
+  int32_t *zi = (int32_t *)malloc(sizeof(int32_t) * (m > 0 ? m : 1));
+  int rc = ORC_OK;
+  for (int64_t n = 0; n < N; n++) {
+    int64_t slot = slot_mapping[n];
+    if (slot < 0) continue;
+    if (slot >= num_pages * P) {
+      rc = ORC_ERR_RANGE;
+      continue;
+    }
+    int64_t page = slot / P, off = slot % P;
+    for (int h = 0; h < H; h++) {
+      const uint16_t *src = x + (n * H + h) * d;
+      for (int j = 0; j < d; j++) xv[j] = orc_half_to_double(src[j]);
+      double norm = 0.0, gamma = 0.0;
+      int64_t vh = n * H + h;
+      orc_encode_vector(d, bits, qjl, m, xv, signs, centroids, midpoints, S, &norm, &gamma, idx, z,
+                        u_out ? u_out + vh * d : NULL, code_margin ? code_margin + vh * d : NULL,
+                        sign_margin ? sign_margin + vh * m : NULL);
+      uint8_t *slab = pool + page * L.page_bytes + (int64_t)h * L.slab_bytes;
+      if (kind == 0) {
+        put_f32(slab + L.k_norm + 4 * off, (float)norm);
+        orc_pack_bits(d, bits, idx, slab + L.k_codes + off * code_bytes);
+        if (qjl) {
+          put_f32(slab + L.k_gamma + 4 * off, (float)gamma);
+          for (int l = 0; l < m; l++) zi[l] = z[l];
+          orc_pack_bits(m, 1, zi, slab + L.k_signs + off * L.k_sign_bytes);
+        }
+      } else {
+        put_f32(slab + L.v_norm + 4 * off, (float)norm);
+        orc_pack_bits(d, bits, idx, slab + L.v_codes + off * code_bytes);
+      }
+    }
+  }
+  free(xv);
+  free(idx);
+  free(z);
+  free(zi);
+  return rc;
+}
+
+/* Decode the token stored at `slot`, head h, of one kind, into out[d]. */
+static void decode_slot(const orc_format *f, const orc_layout *L, int kind, const uint8_t *pool,
+                        int64_t slot, int h, const uint8_t *signs, const float *centroids, const float *S,
+                        int32_t *idx, uint8_t *z, int32_t *zi, double *out) {
+  int d = f->head_dim, P = f->page_size;
+  int64_t page = slot / P, off = slot % P;
+  const uint8_t *slab = pool + page * L->page_bytes + (int64_t)h * L->slab_bytes;
+  if (kind == 0) {
+    int qjl = f->k_qjl, m = qjl ? f->qjl_m : 0;
+    double norm = get_f32(slab + L->k_norm + 4 * off);
+    orc_unpack_bits(d, f->k_bits, slab + L->k_codes + off * L->k_code_bytes, idx);
+    double gamma = 0.0;
+    if (qjl) {
+      gamma = get_f32(slab + L->k_gamma + 4 * off);
+      orc_unpack_bits(m, 1, slab + L->k_signs + off * L->k_sign_bytes, zi);
+      for (int l = 0; l < m; l++) z[l] = (uint8_t)zi[l];
+    }
+    orc_decode_vector(d, f->k_bits, qjl, m, norm, gamma, idx, z, signs, centroids, S, out);
+  } else {
+    double norm = get_f32(slab + L->v_norm + 4 * off);
+    orc_unpack_bits(d, f->v_bits, slab + L->v_codes + off * L->v_code_bytes, idx);
+    orc_decode_vector(d, f->v_bits, 0, 0, norm, 0.0, idx, NULL, signs, centroids, NULL, out);
+  }
+}
+
+/* Decode N slots of one kind into out[N][H][d] (fp64).  Negative slot: zeros. */
+int orc_decode(const orc_format *f, int kind, const uint8_t *pool, int64_t num_pages, const int32_t *slot_mapping,
+               int64_t N, const uint8_t *signs, const float *centroids, const float *S, double *out) {
+  orc_layout L;
+  if (orc_page_layout(f, &L) != ORC_OK) return ORC_ERR_ARG;
+  int d = f->head_dim, H = f->num_kv_heads, m = f->k_qjl ? f->qjl_m : 1;
+  int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * d);
+  uint8_t *z = (uint8_t *)malloc((size_t)m);
+  int32_t *zi = (int32_t *)malloc(sizeof(int32_t) * m);
+  int rc = ORC_OK;
+  for (int64_t n = 0; n < N; n++) {
+    int64_t slot = slot_mapping[n];
+    for (int h = 0; h < H; h++) {
+      double *o = out + (n * H + h) * d;
+      if (slot < 0 || slot >= num_pages * f->page_size) {
+        if (slot >= 0) rc = ORC_ERR_RANGE;
+        for (int j = 0; j < d; j++) o[j] = 0.0;
+        continue;
+      }
+      decode_slot(f, &L, kind, pool, slot, h, signs, centroids, S, idx, z, zi, o);
+    }
+  }
+  free(idx);
+  free(z);
+  free(zi);
+  return rc;
+}
+
+/*
+ * Decode-step attention over [compressed pages U fp16 window], exact softmax,
+ * in the "materialize every token, then attend" form:
+ *   l_i = q . k_hat_i / sqrt(d)      (window tokens use the raw fp16 k_i)
+ *   o   = sum_i softmax(l)_i v_hat_i (window tokens use the raw fp16 v_i)
+ * q: [B][Hq][d] fp16 bits; block_tables: [B][max_pages]; comp_lens[B] =
+ * compressed tokens (positions [0, comp_len)); k_win/v_win: [B][Hkv][W][d]
+ * fp16 bits with win_lens[B] valid tokens (may be NULL when W == 0).
+ * heads (nullable): list of b*Hq + qh to compute; out is [n_heads][d] then,
+ * else [B][Hq][d].  A block-table entry outside [0, num_pages) skips its page
+ * and makes the call return ORC_ERR_RANGE.  No token at all gives o = 0.
+ */
+int orc_attention(const orc_format *f, int B, int Hq, const uint16_t *q, const uint8_t *pool, int64_t num_pages,
+                  const int32_t *block_tables, int max_pages, const int32_t *comp_lens, const uint16_t *k_win,
+                  const uint16_t *v_win, const int32_t *win_lens, int W, const uint8_t *k_signs,
+                  const uint8_t *v_signs, const float *k_centroids, const float *v_centroids, const float *S,
+                  const int32_t *heads, int n_heads, double *out) {
+  orc_layout L;
+  if (orc_page_layout(f, &L) != ORC_OK) return ORC_ERR_ARG;
+  int d = f->head_dim, H = f->num_kv_heads, P = f->page_size;
+  if (B < 1 || Hq < 1 || Hq % H) return ORC_ERR_ARG;
+  int G = Hq / H, m = f->k_qjl ? f->qjl_m : 1;
+  int total = heads ? n_heads : B * Hq;
+  int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * d);
+  uint8_t *z = (uint8_t *)malloc((size_t)m);
+  int32_t *zi = (int32_t *)malloc(sizeof(int32_t) * m);
+  double *qv = (double *)malloc(sizeof(double) * d);
+  double *kh = (double *)malloc(sizeof(double) * d);
+  double *vh = (double *)malloc(sizeof(double) * d);
+  int rc = ORC_OK;
+  for (int t = 0; t < total; t++) {
+    int bq = heads ? heads[t] : t;
+    int b = bq / Hq, qh = bq % Hq, h = qh / G;
+    double *o = out + (int64_t)t * d;
+    for (int j = 0; j < d; j++) {
+      o[j] = 0.0;
+      qv[j] = orc_half_to_double(q[((int64_t)b * Hq + qh) * d + j]);
+    }
+    int comp = comp_lens[b], win = (W > 0 && win_lens) ? win_lens[b] : 0;
+    int ntok = comp + win;
+    if (ntok <= 0) continue;
+    /* pass 1: logits */
+    double *logit = (double *)malloc(sizeof(double) * ntok);
+    char *valid = (char *)malloc((size_t)ntok);
+    double mx = -INFINITY;
+    for (int i = 0; i < ntok; i++) {
+      valid[i] = 1;
+      if (i < comp) {
+        int32_t pg = block_tables[(int64_t)b * max_pages + i / P];
+        if (pg < 0 || pg >= num_pages) {
+          valid[i] = 0;
+          rc = ORC_ERR_RANGE;
+          continue;
+        }
+        decode_slot(f, &L, 0, pool, (int64_t)pg * P + i % P, h, k_signs, k_centroids, S, idx, z, zi, kh);
+      } else {
+        const uint16_t *kw = k_win + (((int64_t)b * H + h) * W + (i - comp)) * d;
+        for (int j = 0; j < d; j++) kh[j] = orc_half_to_double(kw[j]);
+      }
+      double s = 0.0;
+      for (int j = 0; j < d; j++) s += qv[j] * kh[j];
+      logit[i] = s / sqrt((double)d);
+      if (logit[i] > mx) mx = logit[i];
+    }
+    /* pass 2: softmax-weighted values */
+    double denom = 0.0;
+    for (int i = 0; i < ntok; i++) {
+      if (!valid[i]) continue;
+      double p = exp(logit[i] - mx);
+      denom += p;
+      if (i < comp) {
+        int32_t pg = block_tables[(int64_t)b * max_pages + i / P];
+        decode_slot(f, &L, 1, pool, (int64_t)pg * P + i % P, h, v_signs, v_centroids, NULL, idx, z, zi, vh);
+      } else {
+        const uint16_t *vw = v_win + (((int64_t)b * H + h) * W + (i - comp)) * d;
+        for (int j = 0; j < d; j++) vh[j] = orc_half_to_double(vw[j]);
+      }
+      for (int j = 0; j < d; j++) o[j] += p * vh[j];
+    }
+    if (denom > 0.0)
+      for (int j = 0; j < d; j++) o[j] /= denom;
+    free(logit);
+    free(valid);
+  }
+  free(idx);
+  free(z);
+  free(zi);
+  free(qv);
+  free(kh);
+  free(vh);
+  return rc;
+}
