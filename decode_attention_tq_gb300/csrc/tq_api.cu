@@ -1,0 +1,394 @@
+// tq_api.cu -- the C ABI of libtq.so: argument checks, layout, codebook,
+// decode-attention planning and kernel launches.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "tq_internal.cuh"
+
+using namespace tq;
+
+namespace {
+
+// ------------------------------------------------------------------ format --
+bool format_valid(const tq_format *f) {
+  if (!f) return false;
+  const int d = f->head_dim;
+  if (d < 2 || (d & (d - 1))) return false;
+  if (f->k_bits < 1 || f->k_bits > 8 || f->v_bits < 1 || f->v_bits > 8) return false;
+  if ((d * f->k_bits) % 8 || (d * f->v_bits) % 8) return false;
+  if (f->k_qjl != 0 && f->k_qjl != 1) return false;
+  if (f->k_qjl && (f->qjl_m < 8 || f->qjl_m % 8)) return false;
+  if (f->page_size < 1 || f->num_kv_heads < 1) return false;
+  return true;
+}
+
+bool bits_supported(int b) { return b >= 2 && b <= 4; }
+
+bool format_gpu_supported(const tq_format *f) {
+  return f->head_dim == kD && bits_supported(f->k_bits) && bits_supported(f->v_bits) &&
+         (!f->k_qjl || f->qjl_m == kM) && f->page_size % kTile == 0;
+}
+
+int64_t round16(int64_t x) { return (x + 15) & ~int64_t(15); }
+
+void compute_layout(const tq_format *f, tq_layout *L) {
+  const int64_t P = f->page_size;
+  L->k_code_bytes = f->head_dim * f->k_bits / 8;
+  L->v_code_bytes = f->head_dim * f->v_bits / 8;
+  L->k_sign_bytes = f->k_qjl ? f->qjl_m / 8 : 0;
+  int64_t cursor = 0;
+  L->k_norm = cursor;
+  cursor = round16(cursor + 4 * P);
+  L->k_gamma = cursor;
+  if (f->k_qjl) cursor = round16(cursor + 4 * P);
+  L->k_codes = cursor;
+  cursor = round16(cursor + P * L->k_code_bytes);
+  L->k_signs = cursor;
+  if (f->k_qjl) cursor = round16(cursor + P * L->k_sign_bytes);
+  L->v_norm = cursor;
+  cursor = round16(cursor + 4 * P);
+  L->v_codes = cursor;
+  cursor = round16(cursor + P * L->v_code_bytes);
+  L->slab_bytes = cursor;
+  L->page_bytes = cursor * f->num_kv_heads;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+tq_status sm_count(int *sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TQ_ERR_CUDA;
+  return TQ_OK;
+}
+
+// ---------------------------------------------------------------- codebook --
+// Gaussian Lloyd-Max by iterating the decision thresholds: each threshold
+// moves to the midpoint of the conditional means of its two neighbouring cells.
+double gauss_pdf(double x) { return exp(-0.5 * x * x) * 0.39894228040143267794; }
+double gauss_sf(double x) { return 0.5 * erfc(x * 0.70710678118654752440); }  // P(X > x)
+double cell_mean(double lo, double hi) {
+  const double flo = isinf(lo) ? 0.0 : gauss_pdf(lo), fhi = isinf(hi) ? 0.0 : gauss_pdf(hi);
+  double mass;
+  if (lo >= 0.0)
+    mass = gauss_sf(lo) - gauss_sf(hi);
+  else if (hi <= 0.0)
+    mass = gauss_sf(-hi) - gauss_sf(-lo);
+  else
+    mass = 1.0 - gauss_sf(hi) - gauss_sf(-lo);
+  return (flo - fhi) / mass;
+}
+
+void lloyd_max_thresholds(int bits, double *cent, double *thr) {
+  const int levels = 1 << bits;
+  for (int k = 0; k + 1 < levels; k++) thr[k] = 5.0 * ((k + 1.0) / levels - 0.5);
+  for (int iter = 0; iter < 400000; iter++) {
+    for (int k = 0; k < levels; k++) {
+      const double lo = k == 0 ? -INFINITY : thr[k - 1];
+      const double hi = k == levels - 1 ? INFINITY : thr[k];
+      cent[k] = cell_mean(lo, hi);
+    }
+    double moved = 0.0;
+    for (int k = 0; k + 1 < levels; k++) {
+      const double nt = 0.5 * (cent[k] + cent[k + 1]);
+      moved = fmax(moved, fabs(nt - thr[k]));
+      thr[k] = nt;
+    }
+    if (moved < 1e-15) break;
+  }
+  for (int k = 0; k < levels; k++) {
+    const double lo = k == 0 ? -INFINITY : thr[k - 1];
+    const double hi = k == levels - 1 ? INFINITY : thr[k];
+    cent[k] = cell_mean(lo, hi);
+  }
+  for (int k = 0; k < levels / 2; k++) {  // exact antisymmetry of a symmetric density
+    const double m = 0.5 * (cent[levels - 1 - k] - cent[k]);
+    cent[k] = -m;
+    cent[levels - 1 - k] = m;
+  }
+  for (int k = 0; k + 1 < levels; k++) thr[k] = 0.5 * (cent[k] + cent[k + 1]);
+}
+
+// ---------------------------------------------------------- attention plan --
+struct AttnPlan {
+  int G, NT, nw_launch, blocks;
+  size_t off_hdr, off_pre, off_clen, off_wlen, off_qrot, off_qs, off_qexp, off_segml, off_segacc, off_winml, off_winacc,
+      total;
+};
+
+constexpr int kMinTilesPerWarp = 16;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+cudaError_t main_kernel_call(const tq_format *f, const AttnArgs &a, int nt, bool query, int *bps, int blocks,
+                             cudaStream_t st) {
+  switch (f->k_bits) {
+    case 2: return attn_main_k2(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
+    case 3: return attn_main_k3(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
+    case 4: return attn_main_k4(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Occupancy of each main-kernel instance, per device (queried once).
+std::mutex g_occ_mu;
+int g_occ[64][3][3][2][2];  // [device][kb-2][vb-2][qjl][nt-1]; 0 = unknown
+
+tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int window, AttnPlan *p) {
+  const int H = f->num_kv_heads;
+  p->G = Hq / H;
+  p->NT = p->G <= 4 ? 1 : 2;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+  if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
+  int bps = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    int *slot = dev < 64 ? &g_occ[dev][f->k_bits - 2][f->v_bits - 2][f->k_qjl][p->NT - 1] : nullptr;
+    if (slot && *slot > 0) {
+      bps = *slot;
+    } else {
+      AttnArgs dummy;
+      memset(&dummy, 0, sizeof(dummy));
+      if (main_kernel_call(f, dummy, p->NT, true, &bps, 0, 0) != cudaSuccess) return TQ_ERR_CUDA;
+      if (bps < 1) bps = 1;
+      if (slot) *slot = bps;
+    }
+  }
+  const int64_t tiles_max = (int64_t)B * H * max_pages * (f->page_size / kTile);
+  int64_t warps = (tiles_max + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
+  const int64_t cap = (int64_t)sms * bps * kAttnWarps;
+  if (warps > cap) warps = cap;
+  if (warps < 1) warps = 1;
+  p->blocks = (int)((warps + kAttnWarps - 1) / kAttnWarps);
+  p->nw_launch = p->blocks * kAttnWarps;
+
+  const int64_t rows = (int64_t)B * Hq;
+  const int64_t slots = (int64_t)p->nw_launch + (int64_t)B * H;
+  size_t off = 0;
+  p->off_hdr = off;    off = align256(off + sizeof(AttnHeader));
+  p->off_pre = off;    off = align256(off + sizeof(int64_t) * (B + 1));
+  p->off_clen = off;   off = align256(off + sizeof(int32_t) * B);
+  p->off_wlen = off;   off = align256(off + sizeof(int32_t) * B);
+  p->off_qrot = off;   off = align256(off + sizeof(float) * rows * kD);
+  p->off_qs = off;     off = align256(off + (f->k_qjl ? sizeof(float) * rows * kM : 0));
+  p->off_qexp = off;   off = align256(off + sizeof(int32_t) * rows * 2);
+  p->off_segml = off;  off = align256(off + sizeof(float) * slots * p->G * 2);
+  p->off_segacc = off; off = align256(off + sizeof(float) * slots * p->G * kD);
+  p->off_winml = off;  off = align256(off + (window > 0 ? sizeof(float) * rows * 2 : 0));
+  p->off_winacc = off; off = align256(off + (window > 0 ? sizeof(float) * rows * kD : 0));
+  p->total = off;
+  return TQ_OK;
+}
+
+tq_status check_attn_shape(const tq_format *fmt, int B, int Hq, int max_pages, int window) {
+  if (!format_valid(fmt) || B < 1 || Hq < 1 || max_pages < 1 || window < 0) return TQ_ERR_INVALID_ARG;
+  if (Hq % fmt->num_kv_heads) return TQ_ERR_INVALID_ARG;
+  if (!format_gpu_supported(fmt) || Hq / fmt->num_kv_heads > 8) return TQ_ERR_UNSUPPORTED;
+  return TQ_OK;
+}
+
+}  // namespace
+
+// ================================================================== ABI ====
+extern "C" {
+
+const char *tq_status_string(tq_status s) {
+  switch (s) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_INVALID_ARG: return "invalid argument";
+    case TQ_ERR_UNSUPPORTED: return "unsupported format for the GPU kernels (need d=128, bits 2..4, m=128, page_size%16==0, G<=8)";
+    case TQ_ERR_CUDA: return "CUDA runtime error";
+    case TQ_ERR_DEVICE_FAULT: return "device-side data error (see err_word)";
+    case TQ_ERR_TIMEOUT: return "timeout";
+    case TQ_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+tq_status tq_make_codebook(int bits, float *centroids, float *midpoints) {
+  if (bits < 1 || bits > 8 || !centroids || (bits > 0 && !midpoints)) return TQ_ERR_INVALID_ARG;
+  double c[256], t[256];
+  lloyd_max_thresholds(bits, c, t);
+  const int levels = 1 << bits;
+  for (int k = 0; k < levels; k++) centroids[k] = (float)c[k];
+  for (int k = 0; k + 1 < levels; k++) midpoints[k] = (float)t[k];
+  return TQ_OK;
+}
+
+tq_status tq_page_layout(const tq_format *fmt, tq_layout *out) {
+  if (!format_valid(fmt) || !out) return TQ_ERR_INVALID_ARG;
+  compute_layout(fmt, out);
+  return TQ_OK;
+}
+
+tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n_tokens, const int32_t *slot_mapping,
+                    void *page_pool, int64_t num_pages, const uint8_t *signs, const float *codebook, const float *S,
+                    int32_t *err_word, void *stream) {
+  if (!format_valid(fmt) || (kind != TQ_KIND_K && kind != TQ_KIND_V) || n_tokens < 0 || num_pages < 1)
+    return TQ_ERR_INVALID_ARG;
+  if (!format_gpu_supported(fmt)) return TQ_ERR_UNSUPPORTED;
+  const bool qjl = kind == TQ_KIND_K && fmt->k_qjl;
+  if (!x_f16 || !slot_mapping || !page_pool || !signs || !codebook || (qjl && !S)) return TQ_ERR_INVALID_ARG;
+  if (!aligned(x_f16, 16) || !aligned(page_pool, 16) || !aligned(slot_mapping, 4) || !aligned(codebook, 4) ||
+      (qjl && !aligned(S, 16)))
+    return TQ_ERR_INVALID_ARG;
+  if (n_tokens == 0) return TQ_OK;
+  tq_layout L;
+  compute_layout(fmt, &L);
+  EncodeArgs a;
+  a.x = static_cast<const __half *>(x_f16);
+  a.n_tokens = n_tokens;
+  a.H = fmt->num_kv_heads;
+  a.P = fmt->page_size;
+  a.slot_mapping = slot_mapping;
+  a.pool = static_cast<uint8_t *>(page_pool);
+  a.num_pages = num_pages;
+  a.page_bytes = L.page_bytes;
+  a.slab_bytes = L.slab_bytes;
+  a.norm_off = kind == TQ_KIND_K ? L.k_norm : L.v_norm;
+  a.codes_off = kind == TQ_KIND_K ? L.k_codes : L.v_codes;
+  a.gamma_off = L.k_gamma;
+  a.signs_off = L.k_signs;
+  a.code_bytes = kind == TQ_KIND_K ? L.k_code_bytes : L.v_code_bytes;
+  a.signs = signs;
+  a.codebook = codebook;
+  a.S = S;
+  a.err_word = err_word;
+  int sms = 0;
+  if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
+  const int bits = kind == TQ_KIND_K ? fmt->k_bits : fmt->v_bits;
+  return launch_encode(a, bits, qjl, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64_t num_pages,
+                    const int32_t *slot_mapping, int64_t n_tokens, const uint8_t *signs, const float *codebook,
+                    const float *S, float *out, int32_t *err_word, void *stream) {
+  if (!format_valid(fmt) || (kind != TQ_KIND_K && kind != TQ_KIND_V) || n_tokens < 0 || num_pages < 1)
+    return TQ_ERR_INVALID_ARG;
+  if (!format_gpu_supported(fmt)) return TQ_ERR_UNSUPPORTED;
+  const bool qjl = kind == TQ_KIND_K && fmt->k_qjl;
+  if (!page_pool || !slot_mapping || !signs || !codebook || !out || (qjl && !S)) return TQ_ERR_INVALID_ARG;
+  if (!aligned(page_pool, 16) || !aligned(out, 16) || (qjl && !aligned(S, 16))) return TQ_ERR_INVALID_ARG;
+  if (n_tokens == 0) return TQ_OK;
+  tq_layout L;
+  compute_layout(fmt, &L);
+  DecodeArgs a;
+  a.pool = static_cast<const uint8_t *>(page_pool);
+  a.n_tokens = n_tokens;
+  a.H = fmt->num_kv_heads;
+  a.P = fmt->page_size;
+  a.slot_mapping = slot_mapping;
+  a.num_pages = num_pages;
+  a.page_bytes = L.page_bytes;
+  a.slab_bytes = L.slab_bytes;
+  a.norm_off = kind == TQ_KIND_K ? L.k_norm : L.v_norm;
+  a.codes_off = kind == TQ_KIND_K ? L.k_codes : L.v_codes;
+  a.gamma_off = L.k_gamma;
+  a.signs_off = L.k_signs;
+  a.code_bytes = kind == TQ_KIND_K ? L.k_code_bytes : L.v_code_bytes;
+  a.signs = signs;
+  a.codebook = codebook;
+  a.S = S;
+  a.out = out;
+  a.err_word = err_word;
+  int sms = 0;
+  if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
+  const int bits = kind == TQ_KIND_K ? fmt->k_bits : fmt->v_bits;
+  return launch_decode(a, bits, qjl, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_decode_attn_workspace_size(const tq_format *fmt, int batch, int num_q_heads, int max_pages, int window,
+                                        size_t *bytes) {
+  if (!bytes) return TQ_ERR_INVALID_ARG;
+  tq_status s = check_attn_shape(fmt, batch, num_q_heads, max_pages, window);
+  if (s != TQ_OK) return s;
+  AttnPlan p;
+  s = plan_attention(fmt, batch, num_q_heads, max_pages, window, &p);
+  if (s != TQ_OK) return s;
+  *bytes = p.total;
+  return TQ_OK;
+}
+
+tq_status tq_decode_attn(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16, const void *page_pool,
+                         int64_t num_pages, const int32_t *block_tables, int max_pages, const int32_t *comp_lens,
+                         const void *k_win_f16, const void *v_win_f16, const int32_t *win_lens, int window,
+                         const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
+                         const float *v_codebook, const float *S, float *out, void *workspace, size_t workspace_bytes,
+                         int32_t *err_word, void *stream) {
+  tq_status s = check_attn_shape(fmt, batch, num_q_heads, max_pages, window);
+  if (s != TQ_OK) return s;
+  if (num_pages < 1 || !q_f16 || !page_pool || !block_tables || !comp_lens || !k_signs || !v_signs || !k_codebook ||
+      !v_codebook || !out || !workspace || (fmt->k_qjl && !S))
+    return TQ_ERR_INVALID_ARG;
+  if (window > 0 && (!k_win_f16 || !v_win_f16 || !win_lens)) return TQ_ERR_INVALID_ARG;
+  if (!aligned(q_f16, 8) || !aligned(page_pool, 16) || !aligned(workspace, 256) || !aligned(out, 4) ||
+      (fmt->k_qjl && !aligned(S, 16)) || (window > 0 && (!aligned(k_win_f16, 8) || !aligned(v_win_f16, 8))))
+    return TQ_ERR_INVALID_ARG;
+  AttnPlan p;
+  s = plan_attention(fmt, batch, num_q_heads, max_pages, window, &p);
+  if (s != TQ_OK) return s;
+  if (workspace_bytes < p.total) return TQ_ERR_WORKSPACE;
+
+  tq_layout L;
+  compute_layout(fmt, &L);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.pool = static_cast<const uint8_t *>(page_pool);
+  a.num_pages = num_pages;
+  a.page_bytes = L.page_bytes;
+  a.slab_bytes = L.slab_bytes;
+  a.k_norm_o = L.k_norm;
+  a.k_gamma_o = L.k_gamma;
+  a.k_codes_o = L.k_codes;
+  a.k_signs_o = L.k_signs;
+  a.v_norm_o = L.v_norm;
+  a.v_codes_o = L.v_codes;
+  a.k_code_bytes = L.k_code_bytes;
+  a.v_code_bytes = L.v_code_bytes;
+  a.B = batch;
+  a.Hq = num_q_heads;
+  a.H = fmt->num_kv_heads;
+  a.G = p.G;
+  a.P = fmt->page_size;
+  a.max_pages = max_pages;
+  a.window = window;
+  a.block_tables = block_tables;
+  a.comp_lens = comp_lens;
+  a.q = static_cast<const __half *>(q_f16);
+  a.k_win = static_cast<const __half *>(k_win_f16);
+  a.v_win = static_cast<const __half *>(v_win_f16);
+  a.win_lens = win_lens;
+  a.k_signs = k_signs;
+  a.v_signs = v_signs;
+  a.k_cb = k_codebook;
+  a.v_cb = v_codebook;
+  a.S = S;
+  a.out = out;
+  a.err_word = err_word;
+  a.hdr = reinterpret_cast<AttnHeader *>(ws + p.off_hdr);
+  a.pre = reinterpret_cast<int64_t *>(ws + p.off_pre);
+  a.clen = reinterpret_cast<int32_t *>(ws + p.off_clen);
+  a.wlen = reinterpret_cast<int32_t *>(ws + p.off_wlen);
+  a.q_rot = reinterpret_cast<float *>(ws + p.off_qrot);
+  a.q_s = reinterpret_cast<float *>(ws + p.off_qs);
+  a.q_exp = reinterpret_cast<int32_t *>(ws + p.off_qexp);
+  a.seg_ml = reinterpret_cast<float *>(ws + p.off_segml);
+  a.seg_acc = reinterpret_cast<float *>(ws + p.off_segacc);
+  a.win_ml = reinterpret_cast<float *>(ws + p.off_winml);
+  a.win_acc = reinterpret_cast<float *>(ws + p.off_winacc);
+  a.nw_launch = p.nw_launch;
+  a.min_tiles = kMinTilesPerWarp;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_attn_prep(a, fmt->k_qjl != 0, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (main_kernel_call(fmt, a, p.NT, false, nullptr, p.blocks, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (window > 0 && launch_attn_window(a, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (launch_attn_merge(a, st) != cudaSuccess) return TQ_ERR_CUDA;
+  return TQ_OK;
+}
+
+}  // extern "C"

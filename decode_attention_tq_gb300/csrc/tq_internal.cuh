@@ -1,0 +1,100 @@
+// tq_internal.cuh -- argument blocks and launcher declarations shared by the
+// libtq translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+
+struct EncodeArgs {
+  const __half *x;
+  int64_t n_tokens;
+  int H, P;
+  const int32_t *slot_mapping;
+  uint8_t *pool;
+  int64_t num_pages, page_bytes, slab_bytes;
+  int64_t norm_off, codes_off, gamma_off, signs_off;
+  int code_bytes;
+  const uint8_t *signs;
+  const float *codebook;
+  const float *S;
+  int32_t *err_word;
+};
+
+struct DecodeArgs {
+  const uint8_t *pool;
+  int64_t n_tokens;
+  int H, P;
+  const int32_t *slot_mapping;
+  int64_t num_pages, page_bytes, slab_bytes;
+  int64_t norm_off, codes_off, gamma_off, signs_off;
+  int code_bytes;
+  const uint8_t *signs;
+  const float *codebook;
+  const float *S;
+  float *out;
+  int32_t *err_word;
+};
+
+// Workspace header written by the prep kernel and read by the others.
+struct AttnHeader {
+  int64_t total_tiles;  // sum over (b, h) of ceil(comp_len / 16)
+  int64_t active_warps; // warps that own a non-empty tile range
+};
+
+struct AttnArgs {
+  // cache
+  const uint8_t *pool;
+  int64_t num_pages, page_bytes, slab_bytes;
+  int64_t k_norm_o, k_gamma_o, k_codes_o, k_signs_o, v_norm_o, v_codes_o;  // section offsets in a slab
+  int k_code_bytes, v_code_bytes;
+  int B, Hq, H, G, P, max_pages, window;
+  const int32_t *block_tables;
+  const int32_t *comp_lens;
+  const __half *q;
+  const __half *k_win;
+  const __half *v_win;
+  const int32_t *win_lens;
+  const uint8_t *k_signs, *v_signs;
+  const float *k_cb, *v_cb;
+  const float *S;
+  float *out;
+  int32_t *err_word;
+  // workspace sections
+  AttnHeader *hdr;
+  int64_t *pre;      // [B + 1] prefix sums of tiles per sequence
+  int32_t *clen;     // [B] clamped compressed lengths
+  int32_t *wlen;     // [B] clamped window lengths
+  float *q_rot;      // [B][Hq][d]
+  float *q_s;        // [B][Hq][m]
+  int32_t *q_exp;    // [B][Hq][2] power-of-two exponents for the fp16 operands
+  float *seg_ml;     // [slots][G][2]  (max in log2 units, sum)
+  float *seg_acc;    // [slots][G][d]  rotated-domain value accumulator
+  float *win_ml;     // [B][Hq][2]
+  float *win_acc;    // [B][Hq][d]
+  int nw_launch;     // warps launched for the main kernel
+  int min_tiles;     // fewest tiles a warp is given
+};
+
+cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
+
+// Decode attention pieces (tq_attn_aux.cu and tq_attn_k*.cu).
+cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st);
+cudaError_t launch_attn_window(const AttnArgs &a, cudaStream_t st);
+cudaError_t launch_attn_merge(const AttnArgs &a, cudaStream_t st);
+// Main split-KV kernel: returns its per-SM occupancy through *blocks_per_sm
+// when `query_only`, else launches `blocks` CTAs.
+cudaError_t attn_main_k2(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                         int blocks, cudaStream_t st);
+cudaError_t attn_main_k3(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                         int blocks, cudaStream_t st);
+cudaError_t attn_main_k4(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                         int blocks, cudaStream_t st);
+
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
+
+}  // namespace tq

@@ -1,0 +1,186 @@
+"""Python binding of libtq.so (ctypes): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: it checks tensor dtypes/devices, turns tensors into raw
+pointers and the current CUDA stream into a handle, calls the library and
+raises ``TQError`` on a non-OK status.  If libtq.so has not been built the
+first call raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtq.so")
+
+TQ_KIND_K = 0
+TQ_KIND_V = 1
+TQ_DEVERR_SLOT_RANGE = 0x1
+TQ_DEVERR_PAGE_RANGE = 0x2
+TQ_DEVERR_LENGTH = 0x4
+
+STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_CUDA", 4: "TQ_ERR_DEVICE_FAULT",
+          5: "TQ_ERR_TIMEOUT", 6: "TQ_ERR_WORKSPACE"}
+
+
+class TQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({tq_status_string(status)})")
+
+
+class tq_format(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "k_qjl", "qjl_m", "page_size", "num_kv_heads")]
+
+
+class tq_layout(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("slab_bytes", "page_bytes", "k_norm", "k_gamma", "k_codes", "k_signs", "v_norm", "v_codes")] + [
+        (n, C.c_int32) for n in ("k_code_bytes", "k_sign_bytes", "v_code_bytes")
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library():
+    """Load libtq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libtq.so not found at {LIB_PATH}: build it with decode_attention_tq_gb300.build.build()")
+            lib = C.CDLL(LIB_PATH)
+            P, i32, i64, sz = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
+            lib.tq_status_string.argtypes = [C.c_int]
+            lib.tq_status_string.restype = C.c_char_p
+            lib.tq_make_codebook.argtypes = [C.c_int, P, P]
+            lib.tq_page_layout.argtypes = [P, P]
+            lib.tq_encode.argtypes = [P, i32, P, i64, P, P, i64, P, P, P, P, P]
+            lib.tq_decode.argtypes = [P, i32, P, i64, P, i64, P, P, P, P, P, P]
+            lib.tq_decode_attn_workspace_size.argtypes = [P, i32, i32, i32, i32, C.POINTER(sz)]
+            lib.tq_decode_attn.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P]
+            for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn"):
+                getattr(lib, f).restype = C.c_int
+            _lib = lib
+    return _lib
+
+
+def _fmt(f) -> tq_format:
+    if isinstance(f, tq_format):
+        return f
+    g = (lambda k: f[k]) if isinstance(f, dict) else (lambda k: getattr(f, k))
+    return tq_format(*(int(g(n)) for n, _ in tq_format._fields_))
+
+
+def _dev_ptr(t, dtype=None, name="tensor", allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise TQError(rc, where)
+
+
+# ------------------------------------------------------------------- host --
+def tq_status_string(status: int) -> str:
+    return load_library().tq_status_string(int(status)).decode()
+
+
+def tq_make_codebook(bits: int):
+    """Lloyd-Max N(0,1) codebook: (centroids fp32 [2^b], midpoints fp32 [2^b-1])."""
+    L = 1 << bits
+    c = np.zeros(L, np.float32)
+    t = np.zeros(max(L - 1, 1), np.float32)
+    _check(load_library().tq_make_codebook(int(bits), c.ctypes.data, t.ctypes.data), "tq_make_codebook")
+    return c, t[: L - 1]
+
+
+def tq_page_layout(fmt) -> dict:
+    L = tq_layout()
+    F = _fmt(fmt)
+    _check(load_library().tq_page_layout(C.byref(F), C.byref(L)), "tq_page_layout")
+    return {n: getattr(L, n) for n, _ in tq_layout._fields_}
+
+
+def device_codebook(bits: int, device="cuda") -> torch.Tensor:
+    """centroids || midpoints as the fp32 device array the kernels take."""
+    c, t = tq_make_codebook(bits)
+    return torch.from_numpy(np.concatenate([c, t])).to(device)
+
+
+# ----------------------------------------------------------------- device --
+def tq_encode(fmt, kind: int, x, slot_mapping, page_pool, num_pages: int, signs, codebook, S=None, err_word=None, stream=None):
+    F = _fmt(fmt)
+    rc = load_library().tq_encode(
+        C.byref(F), int(kind), _dev_ptr(x, torch.float16, "x"), int(x.shape[0]), _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
+        _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(signs, torch.uint8, "signs"),
+        _dev_ptr(codebook, torch.float32, "codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
+        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+    )
+    _check(rc, "tq_encode")
+
+
+def tq_decode(fmt, kind: int, page_pool, num_pages: int, slot_mapping, signs, codebook, S=None, out=None, err_word=None, stream=None):
+    F = _fmt(fmt)
+    n = int(slot_mapping.shape[0])
+    if out is None:
+        out = torch.empty((n, F.num_kv_heads, F.head_dim), dtype=torch.float32, device=slot_mapping.device)
+    rc = load_library().tq_decode(
+        C.byref(F), int(kind), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
+        n, _dev_ptr(signs, torch.uint8, "signs"), _dev_ptr(codebook, torch.float32, "codebook"),
+        _dev_ptr(S, torch.float32, "S", allow_none=True), _dev_ptr(out, torch.float32, "out"),
+        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+    )
+    _check(rc, "tq_decode")
+    return out
+
+
+def tq_decode_attn_workspace_size(fmt, batch: int, num_q_heads: int, max_pages: int, window: int) -> int:
+    F = _fmt(fmt)
+    n = C.c_size_t(0)
+    _check(load_library().tq_decode_attn_workspace_size(C.byref(F), int(batch), int(num_q_heads), int(max_pages), int(window), C.byref(n)),
+           "tq_decode_attn_workspace_size")
+    return int(n.value)
+
+
+def tq_decode_attn(fmt, q, page_pool, num_pages: int, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs,
+                   k_codebook, v_codebook, S, out, workspace, err_word=None, stream=None):
+    F = _fmt(fmt)
+    B, Hq, _ = q.shape
+    window = 0 if k_win is None else int(k_win.shape[2])
+    rc = load_library().tq_decode_attn(
+        C.byref(F), int(B), int(Hq), _dev_ptr(q, torch.float16, "q"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
+        _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]), _dev_ptr(comp_lens, torch.int32, "comp_lens"),
+        _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True),
+        _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), window, _dev_ptr(k_signs, torch.uint8, "k_signs"),
+        _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
+        _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
+        _dev_ptr(out, torch.float32, "out"), _dev_ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()),
+        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+    )
+    _check(rc, "tq_decode_attn")
+    return out

@@ -1,0 +1,176 @@
+/*
+ * tq.h -- C ABI of libtq.so: TurboQuant-style compressed KV cache on one
+ * NVIDIA GB300 (sm_103a).  Encode (append) head vectors into a paged cache and
+ * run fused decode attention directly on the packed pages.
+ *
+ * Conventions for every entry point
+ *   - All device memory is allocated by the caller; the library allocates
+ *     nothing and keeps no state between calls.
+ *   - Device pointers must be valid on the CUDA device that is current on the
+ *     calling thread.  Work is enqueued asynchronously on `stream` (a
+ *     cudaStream_t; NULL means the legacy default stream).  Host pointers are
+ *     read before the call returns.
+ *   - No exception crosses the ABI.  Each call returns a tq_status.  Argument
+ *     errors are detected on the host before anything is launched, and then
+ *     nothing is launched.  TQ_ERR_CUDA reports a failed launch
+ *     (cudaGetLastError after the launch).
+ *   - Data errors that only the device can see (a slot or a block-table entry
+ *     outside the pool, a length larger than its buffer) never trap: the
+ *     kernel skips the offending token/page and ORs a TQ_DEVERR_* bit into
+ *     the caller's optional int32 *err_word (device memory, may be NULL).
+ *   - Nothing waits on the device: there are no spin-waits in any kernel.
+ *
+ * Format (tq_format): d = head_dim, b_K / b_V = bits per coordinate of the
+ * Lloyd-Max codes, optional 1-bit QJL residual sketch of length m on keys,
+ * P = page_size tokens per page, H = num_kv_heads.  The GPU kernels support
+ * d = 128, b in {2, 3, 4}, m = 128, P a multiple of 16; other shapes return
+ * TQ_ERR_UNSUPPORTED.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,   /* a null pointer, a negative size, inconsistent shapes */
+  TQ_ERR_UNSUPPORTED = 2,   /* a valid format the GPU kernels do not implement    */
+  TQ_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed               */
+  TQ_ERR_DEVICE_FAULT = 4,  /* reserved: reported through err_word instead         */
+  TQ_ERR_TIMEOUT = 5,       /* reserved: no kernel waits on another               */
+  TQ_ERR_WORKSPACE = 6      /* the workspace passed is smaller than required       */
+} tq_status;
+
+/* Which stream of the cache a call works on. */
+enum { TQ_KIND_K = 0, TQ_KIND_V = 1 };
+
+/* Bits ORed into *err_word by the kernels. */
+#define TQ_DEVERR_SLOT_RANGE 0x1   /* slot_mapping[n] >= num_pages * page_size          */
+#define TQ_DEVERR_PAGE_RANGE 0x2   /* block_tables entry outside [0, num_pages)         */
+#define TQ_DEVERR_LENGTH 0x4       /* comp_lens[b] > max_pages*P, win_lens[b] > window, or a negative length */
+
+typedef struct {
+  int32_t head_dim;     /* d                                                   */
+  int32_t k_bits;       /* b_K, Lloyd-Max bits per key coordinate              */
+  int32_t v_bits;       /* b_V, Lloyd-Max bits per value coordinate            */
+  int32_t k_qjl;        /* 1: keys also store the QJL sign sketch and gamma    */
+  int32_t qjl_m;        /* m, number of QJL sign bits per key                  */
+  int32_t page_size;    /* P, tokens per page                                  */
+  int32_t num_kv_heads; /* H, KV heads per layer                               */
+} tq_format;
+
+/* Byte layout of one page (one pool per layer = [num_pages][H] head-slabs).
+ * Section offsets are relative to the start of a head-slab; each section
+ * starts on a 16-byte boundary.  Section order follows the page format of
+ * "TurboQuant Family Design Study for CPU and Browser WASM KV Caches",
+ * section 'Packed format and complete bit accounting': K norms fp32 [P],
+ * K QJL gammas fp32 [P] (QJL only), K codes [P][d*b_K/8], K sign bits
+ * [P][m/8] (QJL only), V norms fp32 [P], V codes [P][d*b_V/8].  Codes are an
+ * LSB-first bitstream (code j at bits [j*b, j*b+b)); sign bit l is bit l. */
+typedef struct {
+  int64_t slab_bytes, page_bytes;
+  int64_t k_norm, k_gamma, k_codes, k_signs, v_norm, v_codes;
+  int32_t k_code_bytes, k_sign_bytes, v_code_bytes; /* per token */
+} tq_layout;
+
+/* Human-readable text for a status (static storage). */
+const char *tq_status_string(tq_status s);
+
+/*
+ * Lloyd-Max scalar quantizer for N(0, 1) with 2^bits levels (host only).
+ * The precomputed Gaussian codebook of "From 0% to 100%: Debugging a KV Cache
+ * Compression Algorithm on a 16GB MacBook", section 'Why this caught my eye',
+ * applied to the unit-variance rotated coordinates.  fp64 fixed-point
+ * iteration, rounded to fp32.  centroids: host float[2^bits], ascending;
+ * midpoints: host float[2^bits - 1], ascending (decision thresholds).
+ * bits in [1, 8].  The device codebook the other calls take is the
+ * concatenation centroids || midpoints (2^(b+1) - 1 floats).
+ */
+tq_status tq_make_codebook(int bits, float *centroids, float *midpoints);
+
+/* Page layout of a format (host only); see tq_layout. */
+tq_status tq_page_layout(const tq_format *fmt, tq_layout *out);
+
+/*
+ * Encode (append) N tokens of one kind into the paged cache: for each head
+ * vector x, n = ||x||, u = H (D . x) / n (signs D, unnormalized Sylvester
+ * Hadamard H), code_j = #{k : t_k <= u_j}, then for keys with QJL:
+ * e = (u - c[code]) / sqrt(d), gamma = ||e||, bit_l = [(S e)_l >= 0].
+ * Follows the aither-kvcache README, section 'Algorithm', with the
+ * structured rotation of the design study's 'Dense and structured transform
+ * comparison' and the QJL sketch of the debugging post's 'The QJL detective
+ * story'.  An all-zero vector stores n = 0, gamma = 0, all codes/bits 0.
+ *   x_f16        device fp16 [N][H][d]
+ *   slot_mapping device int32 [N]; token n goes to page slot/P, offset slot%P;
+ *                a negative slot skips the token
+ *   page_pool    device bytes [num_pages * page_bytes], 16-byte aligned
+ *   signs        device uint8 [d], 1 = negate coordinate (the kind's D)
+ *   codebook     device fp32 [2^b + 2^b - 1] for this kind's b
+ *   S            device fp32 [m][d] row-major (keys with QJL), else NULL
+ *   err_word     device int32 or NULL (TQ_DEVERR_SLOT_RANGE)
+ */
+tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n_tokens,
+                    const int32_t *slot_mapping, void *page_pool, int64_t num_pages,
+                    const uint8_t *signs, const float *codebook, const float *S, int32_t *err_word,
+                    void *stream);
+
+/*
+ * Decode N slots of one kind back to vectors (tests and offline use; never on
+ * the attention path, which reads the packed pages directly):
+ *   x_hat = n * D . (H y) / sqrt(d),
+ *   y = c[code] / sqrt(d) + sqrt(pi/2)/m * gamma * S^T (2 bits - 1) (QJL keys).
+ *   out  device fp32 [N][H][d].  A negative slot gives zeros.
+ */
+tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64_t num_pages,
+                    const int32_t *slot_mapping, int64_t n_tokens, const uint8_t *signs,
+                    const float *codebook, const float *S, float *out, int32_t *err_word, void *stream);
+
+/*
+ * Bytes of device workspace tq_decode_attn needs for these sizes on the
+ * current device (depends on its SM count).  Host only.
+ */
+tq_status tq_decode_attn_workspace_size(const tq_format *fmt, int batch, int num_q_heads, int max_pages,
+                                        int window, size_t *bytes);
+
+/*
+ * One decode step of attention over [compressed pages U fp16 recent window]:
+ *   l_i = q . k_i / sqrt(d),  o = sum_i softmax(l)_i v_i
+ * ("TurboQuant Family Design Study ...", section 'Why keys and values need
+ * different treatment'), computed as in the aither-kvcache README section
+ * 'Zero-buffer fused attention': q is rotated once into the key basis
+ * (q.k = (Tq).(Tk), design study 'Placement relative to RoPE and attention'),
+ * each compressed key is scored from its codes through the centroids plus the
+ * QJL correction, values are accumulated in the rotated domain and rotated
+ * back once per head.  No decoded copy of the cache is ever written.
+ *   q_f16        device fp16 [B][Hq][d]; Hq = G * H (GQA, G <= 8)
+ *   block_tables device int32 [B][max_pages]: logical page -> pool page
+ *   comp_lens    device int32 [B]: compressed tokens (positions [0, comp_len))
+ *   k_win_f16, v_win_f16  device fp16 [B][H][window][d] raw recent tokens,
+ *                win_lens device int32 [B] valid window tokens (order free);
+ *                all three may be NULL when window == 0
+ *   k_signs, v_signs      device uint8 [d]; k_codebook, v_codebook as in
+ *                tq_encode; S device fp32 [m][d] when fmt->k_qjl, else NULL
+ *   out          device fp32 [B][Hq][d]; a head with no token at all gives 0
+ *   workspace    device scratch of at least tq_decode_attn_workspace_size()
+ *                bytes, 256-byte aligned; overwritten by every call, so calls
+ *                that overlap on the GPU need separate workspaces
+ *   err_word     device int32 or NULL (TQ_DEVERR_PAGE_RANGE / _LENGTH)
+ */
+tq_status tq_decode_attn(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                         const void *page_pool, int64_t num_pages, const int32_t *block_tables,
+                         int max_pages, const int32_t *comp_lens, const void *k_win_f16,
+                         const void *v_win_f16, const int32_t *win_lens, int window,
+                         const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
+                         const float *v_codebook, const float *S, float *out, void *workspace,
+                         size_t workspace_bytes, int32_t *err_word, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -1,0 +1,183 @@
+"""GPU parity of libtq against the fp64 oracle, through the C ABI.
+
+Encode: codes and sign bits bit-exact except where the oracle's fp64
+coordinate lies within 1e-4 of a decision boundary; fp32 norms / gammas to
+1e-6 relative; untouched bytes identical.  Decode: fp32 reconstruction to
+1e-5 of the vector's max.  Attention: max |o - o_ref| / max |o_ref| <= 2e-3
+per (sequence, query head), the tolerance the benchmark spec's target states.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tq_inputs as ti
+from tq_testlib import REL_ATTN, Scenario, compare_encoded, gpu_attention, rel_err
+
+pytestmark = pytest.mark.gpu
+
+tq = pytest.importorskip("decode_attention_tq_gb300")
+
+
+def _encode_case(fmt, kind, N, seed, zero_rows=(), neg_slots=()):
+    d, H, P = fmt.head_dim, fmt.num_kv_heads, fmt.page_size
+    num_pages = (N + P - 1) // P + 2
+    lay = oracle.page_layout(fmt)
+    x = ti.kv_history(1, N, H, d, seed, kind)[0].numpy()  # [N, H, d]
+    for zr in zero_rows:
+        x[zr] = 0
+    perm = np.random.default_rng(seed).permutation(num_pages * P)[:N].astype(np.int32)
+    for ns in neg_slots:
+        perm[ns] = -1
+    signs = ti.sign_bits(ti.SEED_SIGNS_K if kind == 0 else ti.SEED_SIGNS_V, d)
+    bits = fmt.k_bits if kind == 0 else fmt.v_bits
+    c, t = oracle.make_codebook(bits)
+    S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if (kind == 0 and fmt.k_qjl) else None
+    pool_ref = np.full(num_pages * lay["page_bytes"], 0x5A, np.uint8)
+    rc, u, cm, sm = oracle.encode(fmt, kind, x, perm, pool_ref, num_pages, signs, c, t, S, diagnostics=True)
+    assert rc == 0
+    pool = torch.full((num_pages * lay["page_bytes"],), 0x5A, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tq.tq_encode(fmt, kind, torch.from_numpy(x).cuda(), torch.from_numpy(perm).cuda(), pool, num_pages,
+                 torch.from_numpy(signs).cuda(), tq.device_codebook(bits), None if S is None else torch.from_numpy(S).cuda(), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return pool.cpu().numpy(), pool_ref, lay, perm, cm, sm, x, signs, c, S, num_pages
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("kind,qjl", [(0, 0), (0, 1), (1, 0)])
+def test_encode_matches_oracle(bits, kind, qjl):
+    fmt = ti.Format(128, bits, bits, qjl, 128, 64, 4)
+    N = 333  # several pages and a ragged tail
+    pool, pool_ref, lay, slots, cm, sm, *_ = _encode_case(fmt, kind, N, seed=bits + 10 * kind + 100 * qjl,
+                                                          zero_rows=(5, 200), neg_slots=(17,))
+    st = compare_encoded(pool, pool_ref, lay, fmt, kind, slots, cm, sm)
+    print("encode", bits, kind, qjl, st)
+
+
+@pytest.mark.parametrize("bits,kind,qjl", [(2, 0, 1), (3, 1, 0), (4, 0, 0), (4, 0, 1)])
+def test_decode_matches_oracle(bits, kind, qjl):
+    fmt = ti.Format(128, bits, bits, qjl, 128, 32, 2)
+    N = 150
+    pool, pool_ref, lay, slots, cm, sm, x, signs, c, S, num_pages = _encode_case(fmt, kind, N, seed=7)
+    # the GPU decodes the oracle's pages
+    out = tq.tq_decode(fmt, kind, torch.from_numpy(pool_ref).cuda(), num_pages, torch.from_numpy(slots).cuda(),
+                       torch.from_numpy(signs).cuda(), tq.device_codebook(bits), None if S is None else torch.from_numpy(S).cuda())
+    torch.cuda.synchronize()
+    rc, ref = oracle.decode(fmt, kind, pool_ref, num_pages, slots, signs, c, S)
+    assert rc == 0
+    e = rel_err(out.cpu().numpy(), ref)
+    assert e.max() < 1e-5, e.max()
+    # the zero vector decodes to exact zeros on both sides
+    z = np.all(x == 0, axis=-1)
+    assert np.all(out.cpu().numpy()[z] == 0)
+
+
+ATTN_CASES = {
+    # name: (fmt, B, Hq, comp_lens, W, win_lens)
+    "k4v4_g4_t2048": (ti.Format(128, 4, 4, 0, 128, 64, 8), 1, 32, [2048], 0, [0]),
+    "k3qjl_v4_g8_w": (ti.Format(128, 3, 4, 1, 128, 64, 2), 2, 16, [1000, 333], 128, [128, 77]),
+    "k2qjl_v2_p128_w": (ti.Format(128, 2, 2, 1, 128, 128, 2), 2, 8, [700, 129], 64, [64, 64]),
+    "k4v4_ragged_w": (ti.Format(128, 4, 4, 0, 128, 64, 4), 3, 16, [1, 640, 97], 16, [16, 5, 0]),
+    "k4v3_g2": (ti.Format(128, 4, 3, 0, 128, 32, 3), 2, 6, [300, 47], 0, [0, 0]),
+    "k2v4_g1": (ti.Format(128, 2, 4, 0, 128, 16, 4), 1, 4, [175], 8, [3]),
+    "window_only": (ti.Format(128, 4, 4, 0, 128, 64, 2), 2, 8, [0, 0], 40, [40, 13]),
+    "empty_seq": (ti.Format(128, 3, 3, 1, 128, 64, 2), 3, 8, [0, 200, 0], 8, [0, 8, 5]),
+}
+
+
+@pytest.mark.parametrize("name", list(ATTN_CASES))
+def test_attention_matches_oracle(name):
+    fmt, B, Hq, comp, W, wl = ATTN_CASES[name]
+    sc = Scenario(fmt, B, Hq, comp, W, wl, layer=3)
+    dev = sc.device_inputs()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_attention(sc, dev, err=err)
+    rc, ref = sc.oracle_attention()
+    assert rc == 0 and int(err.item()) == 0
+    e = rel_err(out, ref)
+    print(name, "max rel err", float(e.max()))
+    # heads with no token at all are exactly zero on both sides
+    assert np.all(np.isfinite(out))
+    assert e.max() <= REL_ATTN, e.max()
+
+
+def test_attention_end_to_end_gpu_encode():
+    """GPU encode -> GPU attention against oracle encode -> oracle attention."""
+    fmt = ti.Format(128, 3, 4, 1, 128, 64, 4)
+    B, Hq, comp, W, wl = 2, 16, [900, 450], 32, [32, 20]
+    sc = Scenario(fmt, B, Hq, comp, W, wl, layer=5)
+    dev = sc.device_inputs()
+    pool = torch.full_like(dev["pool"], 0xA5)
+    for b in range(B):
+        c = comp[b]
+        sl = torch.from_numpy(sc.slots[b]).cuda()
+        tq.tq_encode(fmt, 0, torch.from_numpy(np.ascontiguousarray(sc.K[b, :c])).cuda(), sl, pool, sc.num_pages, dev["ks"], dev["kcb"], dev["S"])
+        tq.tq_encode(fmt, 1, torch.from_numpy(np.ascontiguousarray(sc.V[b, :c])).cuda(), sl, pool, sc.num_pages, dev["vs"], dev["vcb"])
+    dev["pool"] = pool
+    out = gpu_attention(sc, dev)
+    rc, ref = sc.oracle_attention()
+    e = rel_err(out, ref)
+    print("end-to-end max rel err", float(e.max()))
+    assert e.max() <= REL_ATTN
+
+
+def test_bad_page_is_skipped_and_flagged():
+    fmt = ti.Format(128, 4, 4, 0, 128, 64, 2)
+    sc = Scenario(fmt, 2, 4, [300, 130], 0, [0, 0], layer=1)
+    dev = sc.device_inputs()
+    bt = sc.bt.copy()
+    bt[0, 2] = sc.num_pages + 7
+    bt[1, 0] = -3
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_attention(sc, dev, err=err, bt=torch.from_numpy(bt).cuda())
+    assert int(err.item()) & tq.TQ_DEVERR_PAGE_RANGE
+    rc, ref = sc.oracle_attention(bt=bt)
+    assert rc == -2  # the oracle skips the same pages
+    assert rel_err(out, ref).max() <= REL_ATTN
+
+
+def test_length_errors_are_clamped_and_flagged():
+    fmt = ti.Format(128, 4, 4, 0, 128, 64, 2)
+    sc = Scenario(fmt, 2, 4, [128, 64], 8, [8, 4], layer=2)
+    dev = sc.device_inputs()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    comp = torch.tensor([10_000, 64], dtype=torch.int32, device="cuda")  # beyond max_pages * P
+    out = gpu_attention(sc, dev, err=err, comp=comp)
+    assert int(err.item()) & tq.TQ_DEVERR_LENGTH
+    rc, ref = sc.oracle_attention(comp=np.array([sc.max_pages * 64, 64], np.int32))
+    assert rel_err(out, ref).max() <= REL_ATTN
+
+
+def test_encode_slot_out_of_range_flagged():
+    fmt = ti.Format(128, 4, 4, 0, 128, 64, 1)
+    x = torch.randn(4, 1, 128, device="cuda").half()
+    pool = torch.zeros(2 * tq.tq_page_layout(fmt)["page_bytes"], dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.tensor([0, 1, 128, 5], dtype=torch.int32, device="cuda")
+    tq.tq_encode(fmt, 1, x, slots, pool, 2, torch.zeros(128, dtype=torch.uint8, device="cuda"), tq.device_codebook(4), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == tq.TQ_DEVERR_SLOT_RANGE
+
+
+def test_host_argument_errors():
+    fmt = ti.Format(128, 4, 4, 0, 128, 64, 2)
+    q = torch.zeros(1, 4, 128, dtype=torch.float16, device="cuda")
+    with pytest.raises(tq.TQError) as ei:
+        tq.tq_decode_attn_workspace_size(ti.Format(64, 4, 4, 0, 128, 64, 2), 1, 4, 4, 0)
+    assert ei.value.status == 2
+    with pytest.raises(tq.TQError) as ei:
+        tq.tq_decode_attn_workspace_size(fmt, 1, 3, 4, 0)  # Hq not a multiple of H
+    assert ei.value.status == 1
+    ws_need = tq.tq_decode_attn_workspace_size(fmt, 1, 4, 4, 0)
+    small = torch.empty(ws_need - 256, dtype=torch.uint8, device="cuda")
+    z = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cb = tq.device_codebook(4)
+    s = torch.zeros(128, dtype=torch.uint8, device="cuda")
+    pool = torch.zeros(4 * tq.tq_page_layout(fmt)["page_bytes"], dtype=torch.uint8, device="cuda")
+    out = torch.empty(1, 4, 128, device="cuda")
+    bt = torch.zeros(1, 4, dtype=torch.int32, device="cuda")
+    with pytest.raises(tq.TQError) as ei:
+        tq.tq_decode_attn(fmt, q, pool, 4, bt, z, None, None, None, s, s, cb, cb, None, out, small)
+    assert ei.value.status == 6

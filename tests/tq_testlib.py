@@ -1,0 +1,174 @@
+"""Shared helpers of the parity tests: scenario construction with the seeded
+generators, oracle runs, and field-wise comparison of packed pools."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import tq_inputs as ti
+
+EXEMPT = 1e-4     # codes / sign bits may differ only this close to a decision boundary
+REL_ATTN = 2e-3   # attention outputs: max |o - o_ref| / max |o_ref| per (b, q head)
+REL_NORM = 1e-6   # stored fp32 norms and gammas
+
+
+def unpack_field(pool: np.ndarray, lay: dict, fmt, kind: int, slots: np.ndarray):
+    """Fields of the given slots (all heads): norm, gamma, codes [.., d], signs [.., m]."""
+    P, H, d = fmt.page_size, fmt.num_kv_heads, fmt.head_dim
+    bits = fmt.k_bits if kind == 0 else fmt.v_bits
+    qjl = kind == 0 and fmt.k_qjl
+    m = fmt.qjl_m
+    cb = lay["k_code_bytes"] if kind == 0 else lay["v_code_bytes"]
+    n = len(slots)
+    norm = np.zeros((n, H), np.float32)
+    gamma = np.zeros((n, H), np.float32)
+    codes = np.zeros((n, H, d), np.int64)
+    signs = np.zeros((n, H, m), np.int64)
+    for i, s in enumerate(slots):
+        page, off = divmod(int(s), P)
+        for h in range(H):
+            base = page * lay["page_bytes"] + h * lay["slab_bytes"]
+            no = lay["k_norm"] if kind == 0 else lay["v_norm"]
+            co = lay["k_codes"] if kind == 0 else lay["v_codes"]
+            norm[i, h] = pool[base + no + 4 * off: base + no + 4 * off + 4].view(np.float32)[0]
+            raw = pool[base + co + off * cb: base + co + (off + 1) * cb]
+            bitsarr = np.unpackbits(raw, bitorder="little").reshape(d, bits)
+            codes[i, h] = (bitsarr * (1 << np.arange(bits))).sum(1)
+            if qjl:
+                gamma[i, h] = pool[base + lay["k_gamma"] + 4 * off: base + lay["k_gamma"] + 4 * off + 4].view(np.float32)[0]
+                sraw = pool[base + lay["k_signs"] + off * (m // 8): base + lay["k_signs"] + (off + 1) * (m // 8)]
+                signs[i, h] = np.unpackbits(sraw, bitorder="little")[:m]
+    return norm, gamma, codes, signs
+
+
+def written_mask(pool_len: int, lay: dict, fmt, kind: int, slots) -> np.ndarray:
+    """Boolean mask of the pool bytes an encode of `slots` may write."""
+    P, H = fmt.page_size, fmt.num_kv_heads
+    mask = np.zeros(pool_len, bool)
+    qjl = kind == 0 and fmt.k_qjl
+    cb = lay["k_code_bytes"] if kind == 0 else lay["v_code_bytes"]
+    for s in slots:
+        if s < 0:
+            continue
+        page, off = divmod(int(s), P)
+        for h in range(H):
+            base = page * lay["page_bytes"] + h * lay["slab_bytes"]
+            no = lay["k_norm"] if kind == 0 else lay["v_norm"]
+            co = lay["k_codes"] if kind == 0 else lay["v_codes"]
+            mask[base + no + 4 * off: base + no + 4 * off + 4] = True
+            mask[base + co + off * cb: base + co + (off + 1) * cb] = True
+            if qjl:
+                mask[base + lay["k_gamma"] + 4 * off: base + lay["k_gamma"] + 4 * off + 4] = True
+                sb = fmt.qjl_m // 8
+                mask[base + lay["k_signs"] + off * sb: base + lay["k_signs"] + (off + 1) * sb] = True
+    return mask
+
+
+def compare_encoded(pool_gpu, pool_ref, lay, fmt, kind, slots, code_margin, sign_margin):
+    """Field-wise parity of an encode.  Returns a dict of statistics; raises
+    AssertionError on any difference the tolerance rules do not allow.
+    code_margin [N, H, d] and sign_margin [N, H, m] are the oracle's fp64
+    distances to the nearest decision boundary (unit-variance domain)."""
+    slots = np.asarray(slots)
+    live = slots >= 0
+    ls = slots[live]
+    ng, gg, cg, sg = unpack_field(pool_gpu, lay, fmt, kind, ls)
+    nr, gr, cr, sr = unpack_field(pool_ref, lay, fmt, kind, ls)
+    cm = code_margin[live]
+    # norms / gammas: fp32 fields, relative tolerance
+    assert np.all(np.abs(ng - nr) <= REL_NORM * np.abs(nr) + 1e-30), np.max(np.abs(ng - nr) / np.maximum(np.abs(nr), 1e-30))
+    code_diff = cg != cr
+    assert np.all(cm[code_diff] < EXEMPT), "code mismatch outside the boundary exemption"
+    stats = dict(codes=cg.size, code_mismatch=int(code_diff.sum()), code_exempt=int((cm < EXEMPT).sum()))
+    if kind == 0 and fmt.k_qjl:
+        vec_same = ~code_diff.any(-1)  # sign bits are compared where all codes agree
+        sm = sign_margin[live]
+        gdiff = np.abs(gg - gr)
+        assert np.all(gdiff[vec_same] <= 1e-5 * np.abs(gr[vec_same]) + 1e-30), np.max(gdiff[vec_same])
+        sdiff = (sg != sr) & vec_same[..., None]
+        assert np.all(sm[sdiff] < EXEMPT), "sign-bit mismatch outside the boundary exemption"
+        stats.update(signs=int(vec_same.sum()) * fmt.qjl_m, sign_mismatch=int(sdiff.sum()),
+                     sign_exempt=int((sm[vec_same] < EXEMPT).sum()), vectors_skipped_for_signs=int((~vec_same).sum()))
+    # bytes the encode must not touch are identical (both pools start from the same canary)
+    mask = written_mask(len(pool_ref), lay, fmt, kind, slots)
+    assert np.array_equal(pool_gpu[~mask], pool_ref[~mask]), "bytes outside the written fields changed"
+    return stats
+
+
+def rel_err(out, ref):
+    """max_i |o_i - ref_i| / max_i |ref_i| per row (last axis)."""
+    out = np.asarray(out, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.abs(ref).max(-1)
+    num = np.abs(out - ref).max(-1)
+    return np.where(den > 0, num / np.where(den > 0, den, 1), num)
+
+
+class Scenario:
+    """A decode-attention case: K/V generated with the seeded recipe, encoded by
+    the oracle into permuted pages, plus query and window."""
+
+    def __init__(self, fmt, B, Hq, comp_lens, W, win_lens, layer=0, extra_pages=3, max_pages=None):
+        d, H, P = fmt.head_dim, fmt.num_kv_heads, fmt.page_size
+        self.fmt, self.B, self.Hq, self.W = fmt, B, Hq, W
+        self.comp = np.array(comp_lens, np.int32)
+        self.wl = np.array(win_lens, np.int32)
+        need = max(1, max((c + P - 1) // P for c in comp_lens))
+        self.max_pages = max_pages or need
+        self.num_pages = B * self.max_pages + extra_pages
+        perm = ti.page_permutation(self.num_pages).numpy()
+        self.bt = perm[: B * self.max_pages].reshape(B, self.max_pages).astype(np.int32)
+        self.lay = oracle.page_layout(fmt)
+        self.pool = np.full(self.num_pages * self.lay["page_bytes"], 0xA5, np.uint8)
+        T = max(int(self.comp.max()) + W, 1)
+        self.K = ti.kv_history(B, T, H, d, layer, 0).numpy()
+        self.V = ti.kv_history(B, T, H, d, layer, 1).numpy()
+        self.ks, self.vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
+        self.kc, self.kt = oracle.make_codebook(fmt.k_bits)
+        self.vc, self.vt = oracle.make_codebook(fmt.v_bits)
+        self.S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if fmt.k_qjl else None
+        self.kwin = np.zeros((B, H, max(W, 1), d), np.float16)
+        self.vwin = np.zeros((B, H, max(W, 1), d), np.float16)
+        self.slots = []
+        for b in range(B):
+            c = int(self.comp[b])
+            sl = np.array([self.bt[b, i // P] * P + i % P for i in range(c)], np.int32)
+            self.slots.append(sl)
+            if c:
+                assert oracle.encode(fmt, 0, self.K[b, :c], sl, self.pool, self.num_pages, self.ks, self.kc, self.kt, self.S) == 0
+                assert oracle.encode(fmt, 1, self.V[b, :c], sl, self.pool, self.num_pages, self.vs, self.vc, self.vt) == 0
+            n = int(self.wl[b]) if W else 0
+            self.kwin[b, :, :n] = self.K[b, c:c + n].transpose(1, 0, 2)
+            self.vwin[b, :, :n] = self.V[b, c:c + n].transpose(1, 0, 2)
+        self.q = ti.query(B, Hq, d).numpy()
+
+    def oracle_attention(self, heads=None, bt=None, comp=None):
+        return oracle.attention(self.fmt, self.q, self.pool, self.num_pages, self.bt if bt is None else bt,
+                                self.comp if comp is None else comp, self.kwin if self.W else None, self.vwin if self.W else None,
+                                self.wl, self.ks, self.vs, self.kc, self.vc, self.S, heads=heads)
+
+    def device_inputs(self, dev="cuda"):
+        import decode_attention_tq_gb300 as tq
+
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        return dict(
+            q=t(self.q), pool=t(self.pool), bt=t(self.bt), comp=t(self.comp),
+            kwin=t(self.kwin) if self.W else None, vwin=t(self.vwin) if self.W else None, wl=t(self.wl) if self.W else None,
+            ks=t(self.ks), vs=t(self.vs), kcb=tq.device_codebook(self.fmt.k_bits, dev), vcb=tq.device_codebook(self.fmt.v_bits, dev),
+            S=t(self.S) if self.S is not None else None,
+        )
+
+
+def gpu_attention(sc: Scenario, dev_in: dict, err=None, bt=None, comp=None):
+    import decode_attention_tq_gb300 as tq
+
+    out = torch.full((sc.B, sc.Hq, sc.fmt.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tq.tq_decode_attn_workspace_size(sc.fmt, sc.B, sc.Hq, sc.max_pages, sc.W), dtype=torch.uint8, device="cuda")
+    tq.tq_decode_attn(sc.fmt, dev_in["q"], dev_in["pool"], sc.num_pages, dev_in["bt"] if bt is None else bt,
+                      dev_in["comp"] if comp is None else comp, dev_in["kwin"], dev_in["vwin"], dev_in["wl"], dev_in["ks"], dev_in["vs"],
+                      dev_in["kcb"], dev_in["vcb"], dev_in["S"], out, ws, err_word=err)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
