@@ -1,0 +1,581 @@
+#!/usr/bin/env python
+"""Benchmark of the compressed-KV hot path on GB300.
+
+Default workload (N=1): Llama-3-8B-shaped decode, 32 layers, batch 16,
+32 query / 8 KV heads, d = 128, context 32768 per sequence (32640 compressed
+4-bit K / 4-bit V tokens in 64-token pages with a random page permutation,
+plus a 128-token fp16 window).  One step = for every layer: append one token
+per sequence into the packed pages (tq_encode of K and V) and one decode
+attention over the whole cache (tq_decode_attn).  The 32 layers' caches
+(18.5 GB) are resident in HBM before timing; the working set is far larger
+than L2, so no flush is needed between iterations.
+
+Printed JSON line: metric = cached tokens scored per second (B * L * T per
+step); plus HBM GB/s of the step, the roofline of the dominant kernel (the
+split-KV attention kernel, timed in place with CUDA events), bulk-encode
+throughput (32 layers x 8 heads x 65536 tokens, K and V, six formats), the
+end-to-end number through the public API with host buffers, the CPU oracle
+baseline, clocks and the kernel-launch count.
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import tq_inputs as ti  # noqa: E402
+
+METRIC = "compressed-KV decode attn: cached tokens scored/s & HBM GB/s; encode vecs/s"
+UNIT = "tokens/s"
+
+
+# ------------------------------------------------------------------ utils --
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def nvml_index(cuda_index: int) -> int:
+    """nvidia-smi index of a CUDA device (CUDA_VISIBLE_DEVICES may remap)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p for p in vis.split(",") if p.strip()]
+    if parts and cuda_index < len(parts) and parts[cuda_index].strip().isdigit():
+        return int(parts[cuda_index])
+    return cuda_index
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def per_token_head_bytes(fmt) -> dict:
+    from decode_attention_tq_gb300 import tq_page_layout
+
+    L = tq_page_layout(fmt)
+    k = 4 + L["k_code_bytes"] + (4 + L["k_sign_bytes"] if fmt.k_qjl else 0)
+    v = 4 + L["v_code_bytes"]
+    return {"k": k, "v": v, "page_bytes": L["page_bytes"]}
+
+
+# ----------------------------------------------------------- decode bench --
+class DecodeBench:
+    """A resident multi-layer compressed cache and its decode step."""
+
+    def __init__(self, wl: ti.DecodeWorkload, device: str):
+        import decode_attention_tq_gb300 as tq
+
+        self.tq = tq
+        self.wl = wl
+        f = wl.fmt
+        self.fmt = f
+        B, Hq, H, d, P, W, T = wl.batch, wl.q_heads, wl.kv_heads, f.head_dim, f.page_size, wl.window, wl.context
+        comp = wl.comp_tokens
+        self.B, self.Hq, self.H, self.W, self.T, self.comp = B, Hq, H, W, T, comp
+        self.pages_per_seq = wl.pages_per_seq
+        self.num_pages = B * self.pages_per_seq + 1
+        perm = ti.page_permutation(self.num_pages).to(device)
+        self.bt = perm[: B * self.pages_per_seq].reshape(B, self.pages_per_seq).contiguous()
+        pos = torch.arange(comp, device=device)
+        slots = self.bt[:, pos // P] * P + (pos % P)[None, :]
+        self.comp_lens = torch.full((B,), comp, dtype=torch.int32, device=device)
+        self.win_lens = torch.full((B,), wl.win_tokens, dtype=torch.int32, device=device)
+        self.append_slots = slots[:, comp - 1].to(torch.int32).contiguous()
+        self.ks = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_K, d)).to(device)
+        self.vs = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_V, d)).to(device)
+        self.kcb = tq.device_codebook(f.k_bits, device)
+        self.vcb = tq.device_codebook(f.v_bits, device)
+        self.S = torch.from_numpy(ti.gaussian_matrix(ti.SEED_QJL, f.qjl_m, d)).to(device) if f.k_qjl else None
+        page_bytes = tq.tq_page_layout(f)["page_bytes"]
+        flat_slots = slots.reshape(-1).to(torch.int32).contiguous()
+        self.layers = []
+        for layer in range(wl.layers):
+            pool = torch.zeros(self.num_pages * page_bytes, dtype=torch.uint8, device=device)
+            ent = {"pool": pool}
+            for kind, name in ((0, "k"), (1, "v")):
+                x = ti.kv_history(B, T, H, d, layer, kind, device=device)
+                flat = x[:, :comp].reshape(B * comp, H, d).contiguous()
+                tq.tq_encode(f, kind, flat, flat_slots, pool, self.num_pages, self.ks if kind == 0 else self.vs,
+                             self.kcb if kind == 0 else self.vcb, self.S if kind == 0 else None)
+                del flat
+                ent[name + "win"] = x[:, comp:].permute(0, 2, 1, 3).contiguous() if W else None
+                ent[name + "new"] = x[:, comp - 1].contiguous()  # the token each step re-appends
+                del x
+            ent["q"] = ti.query(B, Hq, d, device=device, seed=ti.SEED_QUERY + 7919 * layer)
+            ent["out"] = torch.empty(B, Hq, d, dtype=torch.float32, device=device)
+            self.layers.append(ent)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()  # generation temporaries go back to the driver
+        self.ws = torch.empty(tq.tq_decode_attn_workspace_size(f, B, Hq, self.pages_per_seq, W), dtype=torch.uint8, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        bph = per_token_head_bytes(f)
+        self.main_bytes = B * H * comp * (bph["k"] + bph["v"]) + B * self.pages_per_seq * 4  # per layer launch
+        self.window_bytes = B * H * wl.win_tokens * d * 2 * 2
+        self.step_bytes = wl.layers * (self.main_bytes + self.window_bytes + B * Hq * d * (2 + 4))
+        self.launches_per_step = wl.layers * (2 + 3 + (1 if W else 0))
+
+    def step(self, events=None):
+        tq, f = self.tq, self.fmt
+        for i, L in enumerate(self.layers):
+            tq.tq_encode(f, 0, L["knew"], self.append_slots, L["pool"], self.num_pages, self.ks, self.kcb, self.S, err_word=self.err)
+            tq.tq_encode(f, 1, L["vnew"], self.append_slots, L["pool"], self.num_pages, self.vs, self.vcb, None, err_word=self.err)
+            args = (f, L["q"], L["pool"], self.num_pages, self.bt, self.comp_lens, L["kwin"], L["vwin"], self.win_lens if self.W else None,
+                    self.ks, self.vs, self.kcb, self.vcb, self.S, L["out"], self.ws)
+            if events is None:
+                tq.tq_decode_attn(*args, err_word=self.err)
+            else:
+                tq.tq_decode_attn_timed(*args, events[i][0], events[i][1], err_word=self.err)
+
+
+def time_steps(fn, steps: int, warmup: int, barrier):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1) / steps  # ms per step
+
+
+def run_decode(args, device, barrier, reduce_max, rank, world):
+    wl = {w.name: w for w in ti.DECODE_WORKLOADS}[args.workload]
+    if args.layers:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, layers=args.layers, name=f"{wl.name}(first {args.layers} layers)")
+    t0 = time.time()
+    bench = DecodeBench(wl, device)
+    setup_s = time.time() - t0
+
+    # graph-captured step (launch-bound pieces replay without host overhead)
+    bench.step()
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            bench.step()
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            bench.step()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else bench.step
+
+    with ClockSampler(nvml_index(torch.cuda.current_device())) as clk:
+        ms = time_steps(run, args.steps, args.warmup, barrier)
+    ms = reduce_max(ms)
+    clocks = clk.summary()
+
+    # dominant kernel in place: eager steps with events around the main kernel
+    nl = wl.layers
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
+    for a, b in evs:  # torch creates the CUDA event on its first record
+        a.record()
+        b.record()
+    durs = []
+    for _ in range(max(1, min(args.steps, 5))):
+        bench.step(events=evs)
+        torch.cuda.synchronize()
+        durs.extend(a.elapsed_time(b) for a, b in evs)
+    main_ms = statistics.mean(durs)
+    err = int(bench.err.item())
+
+    peak, peak_kind = measured_peaks()
+    achieved = bench.main_bytes / (main_ms * 1e-3) / 1e9
+    traffic = load_traffic("attn_main", wl.name)
+
+    tokens_per_step = wl.batch * wl.layers * wl.context
+    value = world * tokens_per_step / (ms * 1e-3)
+    res = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8 codes / fp16 operands / f32 accumulate",
+        "data": "synthetic (Student-t nu=3 + 4 outlier channels x20, RoPE keys, seeded)",
+        "config": {
+            "workload": wl.name, "layers": wl.layers, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
+            "head_dim": wl.fmt.head_dim, "context": wl.context, "window": wl.window, "page_size": wl.fmt.page_size,
+            "k_bits": wl.fmt.k_bits, "v_bits": wl.fmt.v_bits, "k_qjl": wl.fmt.k_qjl, "step": "per layer: append 1 token/seq + decode attention",
+            "l2": "working set (cache %.1f GB) >> L2; no flush" % (bench.step_bytes / 1e9), "cuda_graph": graph is not None,
+        },
+        "hbm_gbs": bench.step_bytes / (ms * 1e-3) / 1e9,
+        "token_heads_per_s": value * wl.kv_heads,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attn_main_kernel", "bytes_per_launch": bench.main_bytes, "ms_per_launch": main_ms,
+                     "peak_source": peak_kind},
+        "gpu_launches": bench.launches_per_step * args.steps,
+        "clocks": clocks,
+        "setup_s": setup_s,
+        "err_word": err,
+    }
+    return res, bench
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (same hash)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[f"{kernel}:{workload}"]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_attention_tq_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------- encode bench --
+def run_encode(args, device):
+    """Bulk encode: 32 layers x 8 heads x 65536 tokens of K and V into 64-token
+    pages, for b in {2,3,4} and keys with / without QJL (m = 128)."""
+    import decode_attention_tq_gb300 as tq
+
+    wl = ti.BULK_ENCODE_64K
+    layers = wl.layers if not args.quick else 4
+    H, d, N, P = wl.kv_heads, 128, wl.tokens, wl.page_size
+    xs = []
+    for layer in range(layers):
+        xs.append((ti.kv_history(1, N, H, d, layer, 0, device=device)[0].contiguous(),
+                   ti.kv_history(1, N, H, d, layer, 1, device=device)[0].contiguous()))
+    num_pages = N // P
+    perm = ti.page_permutation(num_pages).to(device)
+    pos = torch.arange(N, device=device)
+    slots = (perm[pos // P] * P + pos % P).to(torch.int32).contiguous()
+    ks = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_K, d)).to(device)
+    vs = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_V, d)).to(device)
+    S = torch.from_numpy(ti.gaussian_matrix(ti.SEED_QJL, wl.qjl_m, d)).to(device)
+    out = {}
+    peak, _ = measured_peaks()
+    for b in wl.bits:
+        for qjl in wl.qjl_options:
+            fmt = ti.Format(d, b, b, qjl, wl.qjl_m, P, H)
+            lay = tq.tq_page_layout(fmt)
+            pools = [torch.zeros(num_pages * lay["page_bytes"], dtype=torch.uint8, device=device) for _ in range(layers)]
+            kcb = tq.device_codebook(b, device)
+
+            def run():
+                for layer in range(layers):
+                    tq.tq_encode(fmt, 0, xs[layer][0], slots, pools[layer], num_pages, ks, kcb, S if qjl else None)
+                    tq.tq_encode(fmt, 1, xs[layer][1], slots, pools[layer], num_pages, vs, kcb, None)
+
+            reps = max(2, args.steps // 3)
+            ms = time_steps(run, reps, 2, lambda: None)
+            vecs = 2 * layers * N * H
+            bph = per_token_head_bytes(fmt)
+            algo = layers * N * H * (2 * 256 + bph["k"] + bph["v"])
+            out[f"b{b}_qjl{qjl}"] = {"vectors_per_s": vecs / (ms * 1e-3), "ms_per_run": ms, "gbs": algo / (ms * 1e-3) / 1e9,
+                                     "frac_hbm": algo / (ms * 1e-3) / 1e9 / peak, "gpu_launches": 2 * layers * reps}
+            del pools
+    del xs
+    torch.cuda.empty_cache()
+    return {"workload": wl.name + ("" if layers == wl.layers else f"(first {layers} layers)"), "per_format": out,
+            "vectors_per_run": 2 * layers * N * H}
+
+
+# ------------------------------------------------------------------- e2e --
+def run_e2e(args, bench: DecodeBench):
+    """Same step through the public API with host buffers: every step copies
+    each layer's query and appended K/V token from pinned host memory and
+    reads each layer's output back, inside the timed region."""
+    host_q = [L["q"].cpu().pin_memory() for L in bench.layers]
+    host_k = [L["knew"].cpu().pin_memory() for L in bench.layers]
+    host_v = [L["vnew"].cpu().pin_memory() for L in bench.layers]
+    host_o = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in bench.layers]
+    h2d = sum(t.numel() * t.element_size() for t in host_q + host_k + host_v)
+    d2h = sum(t.numel() * t.element_size() for t in host_o)
+
+    def step():
+        for i, L in enumerate(bench.layers):
+            L["q"].copy_(host_q[i], non_blocking=True)
+            L["knew"].copy_(host_k[i], non_blocking=True)
+            L["vnew"].copy_(host_v[i], non_blocking=True)
+        bench.step()
+        for i, L in enumerate(bench.layers):
+            host_o[i].copy_(L["out"], non_blocking=True)
+
+    ms = time_steps(step, args.steps, args.warmup, lambda: None)
+    value = bench.wl.batch * bench.wl.layers * bench.wl.context / (ms * 1e-3)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+# --------------------------------------------------------------- oracle --
+def oracle_sample_setup(wl: ti.DecodeWorkload, n_seq: int, device: str | None):
+    """Host-side pages of `n_seq` sequences of layer 0, encoded by the oracle."""
+    import oracle
+
+    f = wl.fmt
+    H, d, P, W, T, comp = wl.kv_heads, f.head_dim, f.page_size, wl.window, wl.context, wl.comp_tokens
+    gen_dev = device if device else "cpu"
+    K = ti.kv_history(n_seq, T, H, d, 0, 0, device=gen_dev).cpu().numpy()
+    V = ti.kv_history(n_seq, T, H, d, 0, 1, device=gen_dev).cpu().numpy()
+    pps = wl.pages_per_seq
+    num_pages = n_seq * pps
+    bt = np.arange(num_pages, dtype=np.int32).reshape(n_seq, pps)
+    lay = oracle.page_layout(f)
+    pool = np.zeros(num_pages * lay["page_bytes"], np.uint8)
+    ks, vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
+    kc, kt = oracle.make_codebook(f.k_bits)
+    vc, vt = oracle.make_codebook(f.v_bits)
+    S = ti.gaussian_matrix(ti.SEED_QJL, f.qjl_m, d) if f.k_qjl else None
+    jobs = []
+    for b in range(n_seq):
+        sl = (bt[b, np.arange(comp) // P] * P + np.arange(comp) % P).astype(np.int32)
+        jobs.append((0, np.ascontiguousarray(K[b, :comp]), sl, ks, kc, kt, S))
+        jobs.append((1, np.ascontiguousarray(V[b, :comp]), sl, vs, vc, vt, None))
+    with cf.ThreadPoolExecutor(max_workers=min(len(jobs), host_cores())) as ex:
+        rcs = list(ex.map(lambda j: oracle.encode(f, j[0], j[1], j[2], pool, num_pages, *j[3:]), jobs))
+    assert all(rc == 0 for rc in rcs)
+    kwin = np.ascontiguousarray(K[:, comp:].transpose(0, 2, 1, 3)) if W else None
+    vwin = np.ascontiguousarray(V[:, comp:].transpose(0, 2, 1, 3)) if W else None
+    q = ti.query(n_seq, wl.q_heads, d).numpy()
+    return dict(f=f, q=q, pool=pool, num_pages=num_pages, bt=bt, comp=np.full(n_seq, comp, np.int32), kwin=kwin, vwin=vwin,
+                wl=np.full(n_seq, wl.win_tokens, np.int32), ks=ks, vs=vs, kc=kc, vc=vc, S=S)
+
+
+def oracle_time(s, heads, cores):
+    """Oracle decode attention for the listed (b*Hq + qh) rows on `cores` threads."""
+    import oracle
+
+    chunks = [heads[i::cores] for i in range(cores) if heads[i::cores]]
+
+    def work(hs):
+        return oracle.attention(s["f"], s["q"], s["pool"], s["num_pages"], s["bt"], s["comp"], s["kwin"], s["vwin"], s["wl"], s["ks"],
+                                s["vs"], s["kc"], s["vc"], s["S"], heads=np.array(hs, np.int32))
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+        list(ex.map(work, chunks))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl: ti.DecodeWorkload, device, target_cpu_s: float = 15.0):
+    """The oracle as it stands, on a bounded sample: whole sequences (all query
+    heads) of layer 0, about `target_cpu_s` seconds of CPU work."""
+    cores = host_cores()
+    Hq = wl.q_heads
+    n_seq = 2
+    s = oracle_sample_setup(wl, n_seq, device)
+    probe = oracle_time(s, [0], 1)  # one query head on one core
+    n_heads = int(max(1, min(Hq * n_seq, target_cpu_s / max(probe, 1e-3))))
+    heads = list(range(n_heads))
+    dt = oracle_time(s, heads, cores)
+    tokens = wl.context * n_heads / Hq  # a sequence-token counts once per layer, all heads included
+    return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"layer 0: {n_heads} (sequence, query head) rows of {Hq} heads per sequence at context {wl.context}, "
+                      f"= {n_heads / Hq:.2f} sequence-layers; {dt:.2f} s wall on {cores} threads"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle, timed on the host cores."""
+    wl = {w.name: w for w in ti.DECODE_WORKLOADS}[args.workload]
+    if rank != 0:
+        return None
+    cores = host_cores()
+    dev = "cuda" if torch.cuda.is_available() else None
+    s = oracle_sample_setup(wl, 1, dev)
+    Hq = wl.q_heads
+    probe = oracle_time(s, [0], 1)
+    budget = max(2.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))  # seconds per step
+    n_heads = int(max(1, min(Hq, budget * cores / max(probe, 1e-3))))
+    heads = list(range(n_heads))
+    for _ in range(args.warmup):
+        oracle_time(s, heads, cores)
+    times = [oracle_time(s, heads, cores) for _ in range(args.steps)]
+    dt = sum(times) / len(times)
+    value = wl.context * n_heads / Hq / dt
+    sample = f"layer 0, sequence 0, {n_heads} of {Hq} query heads at context {wl.context} per step; {cores} threads"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same recipe)", "config": {"workload": wl.name, "reference": "fp64 CPU oracle (no reference implementation exists)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--workload", default=ti.LLAMA3_8B_T32K.name, choices=[w.name for w in ti.DECODE_WORKLOADS])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-encode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="fewer encode layers (development)")
+    ap.add_argument("--layers", type=int, default=0, help="decode layers (profiling a small case; 0 = the workload's)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "tq" else args.warmup
+
+    world, rank, local = dist_info()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        if pg:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --impl tq needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+    def barrier():
+        if pg:
+            pg.barrier()
+
+    def reduce_max(x):
+        if not pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    res, bench = run_decode(args, device, barrier, reduce_max, rank, world)
+    if not args.no_e2e:
+        e2e = run_e2e(args, bench)
+        e2e_ms = reduce_max(e2e["ms_per_step"])
+        e2e["value"] = world * bench.wl.batch * bench.wl.layers * bench.wl.context / (e2e_ms * 1e-3)
+        res["e2e"] = e2e
+    del bench
+    torch.cuda.empty_cache()
+    if not args.no_encode:
+        res["encode"] = run_encode(args, device)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        wl = {w.name: w for w in ti.DECODE_WORKLOADS}[args.workload]
+        res["cpu_baseline"] = cpu_baseline(wl, device)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

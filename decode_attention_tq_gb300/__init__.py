@@ -15,6 +15,7 @@ from .tq import (  # noqa: F401
     load_library,
     tq_decode,
     tq_decode_attn,
+    tq_decode_attn_timed,
     tq_decode_attn_workspace_size,
     tq_encode,
     tq_make_codebook,

@@ -312,12 +312,13 @@ tq_status tq_decode_attn_workspace_size(const tq_format *fmt, int batch, int num
   return TQ_OK;
 }
 
-tq_status tq_decode_attn(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16, const void *page_pool,
-                         int64_t num_pages, const int32_t *block_tables, int max_pages, const int32_t *comp_lens,
-                         const void *k_win_f16, const void *v_win_f16, const int32_t *win_lens, int window,
-                         const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
-                         const float *v_codebook, const float *S, float *out, void *workspace, size_t workspace_bytes,
-                         int32_t *err_word, void *stream) {
+static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                                  const void *page_pool, int64_t num_pages, const int32_t *block_tables, int max_pages,
+                                  const int32_t *comp_lens, const void *k_win_f16, const void *v_win_f16,
+                                  const int32_t *win_lens, int window, const uint8_t *k_signs, const uint8_t *v_signs,
+                                  const float *k_codebook, const float *v_codebook, const float *S, float *out,
+                                  void *workspace, size_t workspace_bytes, int32_t *err_word, cudaEvent_t ev_begin,
+                                  cudaEvent_t ev_end, void *stream) {
   tq_status s = check_attn_shape(fmt, batch, num_q_heads, max_pages, window);
   if (s != TQ_OK) return s;
   if (num_pages < 1 || !q_f16 || !page_pool || !block_tables || !comp_lens || !k_signs || !v_signs || !k_codebook ||
@@ -325,7 +326,7 @@ tq_status tq_decode_attn(const tq_format *fmt, int batch, int num_q_heads, const
     return TQ_ERR_INVALID_ARG;
   if (window > 0 && (!k_win_f16 || !v_win_f16 || !win_lens)) return TQ_ERR_INVALID_ARG;
   if (!aligned(q_f16, 8) || !aligned(page_pool, 16) || !aligned(workspace, 256) || !aligned(out, 4) ||
-      (fmt->k_qjl && !aligned(S, 16)) || (window > 0 && (!aligned(k_win_f16, 8) || !aligned(v_win_f16, 8))))
+      (fmt->k_qjl && !aligned(S, 16)) || (window > 0 && (!aligned(k_win_f16, 16) || !aligned(v_win_f16, 16))))
     return TQ_ERR_INVALID_ARG;
   AttnPlan p;
   s = plan_attention(fmt, batch, num_q_heads, max_pages, window, &p);
@@ -385,10 +386,36 @@ tq_status tq_decode_attn(const tq_format *fmt, int batch, int num_q_heads, const
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_attn_prep(a, fmt->k_qjl != 0, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (ev_begin && cudaEventRecord(ev_begin, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (main_kernel_call(fmt, a, p.NT, false, nullptr, p.blocks, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (ev_end && cudaEventRecord(ev_end, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (window > 0 && launch_attn_window(a, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (launch_attn_merge(a, st) != cudaSuccess) return TQ_ERR_CUDA;
   return TQ_OK;
+}
+
+tq_status tq_decode_attn(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16, const void *page_pool,
+                         int64_t num_pages, const int32_t *block_tables, int max_pages, const int32_t *comp_lens,
+                         const void *k_win_f16, const void *v_win_f16, const int32_t *win_lens, int window,
+                         const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
+                         const float *v_codebook, const float *S, float *out, void *workspace, size_t workspace_bytes,
+                         int32_t *err_word, void *stream) {
+  return decode_attn_impl(fmt, batch, num_q_heads, q_f16, page_pool, num_pages, block_tables, max_pages, comp_lens,
+                          k_win_f16, v_win_f16, win_lens, window, k_signs, v_signs, k_codebook, v_codebook, S, out,
+                          workspace, workspace_bytes, err_word, nullptr, nullptr, stream);
+}
+
+tq_status tq_decode_attn_timed(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                               const void *page_pool, int64_t num_pages, const int32_t *block_tables, int max_pages,
+                               const int32_t *comp_lens, const void *k_win_f16, const void *v_win_f16,
+                               const int32_t *win_lens, int window, const uint8_t *k_signs, const uint8_t *v_signs,
+                               const float *k_codebook, const float *v_codebook, const float *S, float *out,
+                               void *workspace, size_t workspace_bytes, int32_t *err_word, void *main_begin_event,
+                               void *main_end_event, void *stream) {
+  return decode_attn_impl(fmt, batch, num_q_heads, q_f16, page_pool, num_pages, block_tables, max_pages, comp_lens,
+                          k_win_f16, v_win_f16, win_lens, window, k_signs, v_signs, k_codebook, v_codebook, S, out,
+                          workspace, workspace_bytes, err_word, static_cast<cudaEvent_t>(main_begin_event),
+                          static_cast<cudaEvent_t>(main_end_event), stream);
 }
 
 }  // extern "C"

@@ -99,71 +99,141 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
   }
 }
 
-// One block per (b, kv head); thread j owns output coordinate j.  Scores and
-// probabilities of a chunk of up to 128 window tokens go through shared memory.
-__global__ void __launch_bounds__(128) attn_window_kernel(const AttnArgs a) {
+// One block (256 threads) per (b, kv head) over the raw fp16 window, in
+// chunks of 128 tokens: (1) scores, two threads per token (64 coordinates
+// each, 16-byte loads); (2) per-head max / exp / sum with warp reductions;
+// (3) values, thread = (coordinate pair, head group) streaming half2 rows.
+__global__ void __launch_bounds__(256) attn_window_kernel(const AttnArgs a) {
   __shared__ float s_q[8][kD];
   __shared__ float s_p[8][128];
   __shared__ float s_mu[8], s_l[8], s_alpha[8];
   const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
-  const int j = threadIdx.x, warp = j >> 5, lane = j & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
   const int wl = a.wlen[b];
-  for (int g = 0; g < G; g++) s_q[g][j] = __half2float(a.q[((int64_t)b * a.Hq + h * G + g) * kD + j]);
-  if (j < G) {
-    s_mu[j] = -INFINITY;
-    s_l[j] = 0.f;
+  for (int i = tid; i < G * kD; i += 256) s_q[i / kD][i % kD] = __half2float(a.q[((int64_t)b * a.Hq + h * G) * kD + i]);
+  if (tid < G) {
+    s_mu[tid] = -INFINITY;
+    s_l[tid] = 0.f;
   }
-  float acc[8];
-#pragma unroll
-  for (int g = 0; g < 8; g++) acc[g] = 0.f;
+  const int cpair = tid & 63, hg = tid >> 6;  // value phase: coordinates 2*cpair, 2*cpair+1; heads hg, hg+4
+  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
   __syncthreads();
   const float sscale = kLog2e * 0.08838834764831845f;  // log2(e)/sqrt(d)
   const __half *kbase = a.k_win + ((int64_t)b * a.H + h) * a.window * kD;
   const __half *vbase = a.v_win + ((int64_t)b * a.H + h) * a.window * kD;
   for (int c0 = 0; c0 < wl; c0 += 128) {
     const int n = min(128, wl - c0);
-    for (int i = warp; i < n; i += 4) {
-      const uint2 raw = *reinterpret_cast<const uint2 *>(kbase + (int64_t)(c0 + i) * kD + 4 * lane);
-      const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-      const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-      for (int g = 0; g < G; g++) {
-        float d = f01.x * s_q[g][4 * lane] + f01.y * s_q[g][4 * lane + 1] + f23.x * s_q[g][4 * lane + 2] +
-                  f23.y * s_q[g][4 * lane + 3];
-        d = warp_sum_xor(d, 31);
-        if (lane == 0) s_p[g][i] = d * sscale;
+    {  // (1) scores
+      const int i = tid >> 1, half = tid & 1;
+      float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (i < n) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(kbase + (int64_t)(c0 + i) * kD + 64 * half);
+        uint4 raw[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) raw[k] = src[k];
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+            const int c = 64 * half + 8 * k + 2 * e;
+#pragma unroll
+            for (int g = 0; g < 8; g++)
+              if (g < G) part[g] = fmaf(f.x, s_q[g][c], fmaf(f.y, s_q[g][c + 1], part[g]));
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < 8; g++) {
+        const float tot = part[g] + __shfl_xor_sync(0xffffffffu, part[g], 1);
+        if (g < G && half == 0 && i < n) s_p[g][i] = tot * sscale;
       }
     }
     __syncthreads();
-    if (j < G) {
-      float m = s_mu[j];
-      for (int i = 0; i < n; i++) m = fmaxf(m, s_p[j][i]);
-      const float alpha = exp2f(s_mu[j] - m);
-      float l = s_l[j] * alpha;
-      for (int i = 0; i < n; i++) {
-        const float p = exp2f(s_p[j][i] - m);
-        s_p[j][i] = p;
-        l += p;
+    for (int g = warp; g < G; g += 8) {  // (2) softmax statistics, one warp per head
+      float v[4], m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int i = lane + 32 * k;
+        v[k] = i < n ? s_p[g][i] : -INFINITY;
+        m = fmaxf(m, v[k]);
       }
-      s_mu[j] = m;
-      s_l[j] = l;
-      s_alpha[j] = alpha;
+      m = warp_max_xor(m, 31);
+      const float mnew = fmaxf(s_mu[g], m);
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int i = lane + 32 * k;
+        const float p = i < n ? exp2f(v[k] - mnew) : 0.f;
+        if (i < n) s_p[g][i] = p;
+        sum += p;
+      }
+      sum = warp_sum_xor(sum, 31);
+      if (lane == 0) {
+        const float alpha = exp2f(s_mu[g] - mnew);
+        s_alpha[g] = alpha;
+        s_l[g] = s_l[g] * alpha + sum;
+        s_mu[g] = mnew;
+      }
     }
     __syncthreads();
-    for (int g = 0; g < G; g++) acc[g] *= s_alpha[g];
-    for (int i = 0; i < n; i++) {
-      const float v = __half2float(vbase[(int64_t)(c0 + i) * kD + j]);
-      for (int g = 0; g < G; g++) acc[g] = fmaf(s_p[g][i], v, acc[g]);
+    {  // (3) values
+#pragma unroll
+      for (int gi = 0; gi < 2; gi++) {
+        const int g = hg + 4 * gi;
+        if (g < G) {
+          acc[gi][0] *= s_alpha[g];
+          acc[gi][1] *= s_alpha[g];
+        }
+      }
+      const __half2 *vrow = reinterpret_cast<const __half2 *>(vbase + (int64_t)c0 * kD) + cpair;
+      int i = 0;
+      for (; i + 8 <= n; i += 8) {
+        __half2 vv[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) vv[k] = vrow[(i + k) * (kD / 2)];
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          const float2 f = __half22float2(vv[k]);
+#pragma unroll
+          for (int gi = 0; gi < 2; gi++) {
+            const int g = hg + 4 * gi;
+            if (g < G) {
+              const float p = s_p[g][i + k];
+              acc[gi][0] = fmaf(p, f.x, acc[gi][0]);
+              acc[gi][1] = fmaf(p, f.y, acc[gi][1]);
+            }
+          }
+        }
+      }
+      for (; i < n; i++) {
+        const float2 f = __half22float2(vrow[i * (kD / 2)]);
+#pragma unroll
+        for (int gi = 0; gi < 2; gi++) {
+          const int g = hg + 4 * gi;
+          if (g < G) {
+            const float p = s_p[g][i];
+            acc[gi][0] = fmaf(p, f.x, acc[gi][0]);
+            acc[gi][1] = fmaf(p, f.y, acc[gi][1]);
+          }
+        }
+      }
     }
     __syncthreads();
   }
-  for (int g = 0; g < G; g++) {
-    const int64_t row = (int64_t)b * a.Hq + h * G + g;
-    if (j == 0) {
-      a.win_ml[row * 2] = s_mu[g];
-      a.win_ml[row * 2 + 1] = s_l[g];
+#pragma unroll
+  for (int gi = 0; gi < 2; gi++) {
+    const int g = hg + 4 * gi;
+    if (g < G) {
+      const int64_t row = (int64_t)b * a.Hq + h * G + g;
+      if (cpair == 0) {
+        a.win_ml[row * 2] = s_mu[g];
+        a.win_ml[row * 2 + 1] = s_l[g];
+      }
+      *reinterpret_cast<float2 *>(a.win_acc + row * kD + 2 * cpair) = make_float2(acc[gi][0], acc[gi][1]);
     }
-    a.win_acc[row * kD + j] = acc[g];
   }
 }
 
@@ -240,7 +310,7 @@ cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
 }
 
 cudaError_t launch_attn_window(const AttnArgs &a, cudaStream_t st) {
-  attn_window_kernel<<<(unsigned)((int64_t)a.B * a.H), 128, 0, st>>>(a);
+  attn_window_kernel<<<(unsigned)((int64_t)a.B * a.H), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -9,7 +9,7 @@
 // accumulator) per piece into slot w + (b*H + h), which is unique because both
 // w and the unit index grow monotonically along the list.
 //
-// Per tile (16 tokens, one (b, h)) a warp does, on the tensor cores
+// Per tile (16 tokens of one (b, h)) a warp runs, on the tensor cores
 // (mma.sync m16n8k16, fp16 operands, fp32 accumulation):
 //   scores[16 x 2G] = Kcodes[16 x 128] * Qrot[128 x 2G]
 //     A: centroid of each code pair from a shared-memory table (fp16 hi and lo
@@ -19,10 +19,13 @@
 //        exact in fp16;
 //   online softmax in fp32 (log2 domain);
 //   acc[128 x 2G] += Vcodes^T[128 x 16] * W[16 x 2G], W = p_i * n_i / nu
-//        (nu = running max value norm) split hi/lo over the columns.
-// Thread (r = lane/4, t = lane%4) of the MMA layout owns head 4*nt + t of
-// n-tile nt, tokens r and r+8 of a tile for the scores, and output
-// coordinates 16r..16r+15 of the value accumulator.
+//        (nu = running max value norm) split hi/lo over the columns; the
+//        value table maps a pair of codes to a pair of centroids, so the codes
+//        of the two tokens an A register pairs are interleaved and looked up
+//        once.
+// Thread (r = lane/4, t = lane%4) owns head 4*nt + t of n-tile nt, tokens r
+// and r+8 of a tile for the scores, and output coordinates 16r..16r+15 of the
+// value accumulator.
 #pragma once
 
 #include "tq_internal.cuh"
@@ -31,7 +34,7 @@ namespace tq {
 
 template <int KB, int VB, bool QJL>
 struct TileRegs {
-  uint32_t k0[KB], k1[KB];  // key code slice (coords 32t..32t+31) of tokens r, r+8
+  uint32_t k0[KB], k1[KB];  // key code slice t (coords 32t..32t+31) of tokens r, r+8
   float nk0, nk1;           // key norms of tokens r, r+8
   float g0, g1;             // QJL gammas
   uint32_t s0, s1;          // QJL sign word t of tokens r, r+8
@@ -40,33 +43,61 @@ struct TileRegs {
   bool ok0, ok1;            // token r / r+8 is a live compressed token
 };
 
-// Code pair p (coordinates 32t+2p, 32t+2p+1) of a key slice.
-template <int KB>
-__device__ __forceinline__ uint32_t key_pair(const uint32_t (&w)[KB], int p) {
-  if constexpr (KB == 4) {
-    return (w[p >> 2] >> ((p & 3) * 8)) & 0xFFu;
-  } else if constexpr (KB == 2) {
-    return (w[p >> 3] >> ((p & 7) * 4)) & 0xFu;
+// `width` bits at compile-time bit `pos` of the 64-bit (hi:lo), moved to bit
+// SH and ORed with `base` (table base and lane slot; the fields never overlap).
+template <int SH>
+__device__ __forceinline__ uint32_t field_at(uint32_t lo, uint32_t hi, int pos, int width, uint32_t base) {
+  const uint32_t mask = ((1u << width) - 1u) << SH;
+  uint32_t x;
+  if (pos + width <= 32) {
+    x = pos >= SH ? (lo >> (pos - SH)) : (lo << (SH - pos));
+  } else if (pos >= 32) {
+    x = (pos - 32) >= SH ? (hi >> (pos - 32 - SH)) : (hi << (SH - (pos - 32)));
   } else {
-    const int bit = 6 * p, wi = bit >> 5, sh = bit & 31;
-    if (sh <= 26) return (w[wi] >> sh) & 63u;
-    return __funnelshift_r(w[wi], w[wi + 1], sh) & 63u;
+    x = __funnelshift_r(lo, hi, pos) << SH;
   }
+  return (x & mask) | base;
 }
 
-// Code pair mt (coordinates 16r+2mt, 16r+2mt+1) of a value slice.
-template <int VB>
-__device__ __forceinline__ uint32_t value_pair(uint32_t lo, uint32_t hi, int mt) {
-  constexpr uint32_t mask = (1u << (2 * VB)) - 1u;
-  const int bit = 2 * VB * mt;
-  if (bit + 2 * VB <= 32) return (lo >> bit) & mask;
-  if (bit >= 32) return (hi >> (bit - 32)) & mask;
-  return __funnelshift_r(lo, hi, bit) & mask;
+// Shared address of the key-table entry of code pair p (coordinates 32t+2p,
+// 32t+2p+1): table base | pair code << 8 | lane * 8.
+template <int KB>
+__device__ __forceinline__ uint32_t key_addr(const uint32_t (&w)[KB], int p, uint32_t laneK) {
+  if constexpr (KB == 4) {
+    // byte p of the slice into bits 8..15; bytes 0, 2, 3 from laneK
+    return __byte_perm(w[p >> 2], laneK, 0x7604 | ((p & 3) << 4));
+  } else {
+    const int bit = 2 * KB * p, wi = bit >> 5;
+    return field_at<8>(w[wi], (wi + 1 < KB) ? w[wi + 1] : 0u, bit & 31, 2 * KB, laneK);
+  }
 }
 
 // +-1 fp16 pair from sign bits p and p+16 of a word (bit set -> +1).
 __device__ __forceinline__ uint32_t sign_pair(uint32_t w, int p) {
   return 0xBC00BC00u ^ ((w << (15 - p)) & 0x80008000u);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Ask the TMA engine to stage a page slab in L2 (no registers, no smem).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 template <int NB>
@@ -83,23 +114,15 @@ __device__ __forceinline__ void ldg_words(const uint8_t *p, uint32_t (&w)[NB]) {
   }
 }
 
+// Registers of one 16-token tile at offset o0 of a page slab; `live` is the
+// number of leading tokens of the tile that are compressed tokens (0 for a
+// page outside the pool).
 template <int KB, int VB, bool QJL>
-__device__ __forceinline__ void load_tile(const AttnArgs &a, int b, int h, int64_t j, int clen, int r, int t,
+__device__ __forceinline__ void load_tile(const AttnArgs &a, const uint8_t *slab, int o0, int live, int r, int t,
                                           TileRegs<KB, VB, QJL> &R) {
   constexpr int KCB = 16 * KB, VCB = 16 * VB;
-  const int tpp = a.P >> 4;
-  const int64_t pidx = j / tpp;
-  const int o0 = (int)(j - pidx * tpp) * 16;
-  int32_t page = __ldg(a.block_tables + (int64_t)b * a.max_pages + pidx);
-  const bool pok = page >= 0 && (int64_t)page < a.num_pages;
-  if (!pok) {
-    if (r == 0 && t == 0) report(a.err_word, TQ_DEVERR_PAGE_RANGE);
-    page = 0;
-  }
-  const uint8_t *slab = a.pool + (int64_t)page * a.page_bytes + (int64_t)h * a.slab_bytes;
-  const int64_t tok0 = j * 16;
-  R.ok0 = pok && (tok0 + r < clen);
-  R.ok1 = pok && (tok0 + r + 8 < clen);
+  R.ok0 = r < live;
+  R.ok1 = r + 8 < live;
   const uint8_t *kc = slab + a.k_codes_o + t * 4 * KB;
   ldg_words<KB>(kc + (o0 + r) * KCB, R.k0);
   ldg_words<KB>(kc + (o0 + r + 8) * KCB, R.k1);
@@ -141,14 +164,72 @@ __device__ __forceinline__ void load_tile(const AttnArgs &a, int b, int h, int64
   }
 }
 
+// Walks the tiles of one segment page by page, without divisions.
+struct TileCursor {
+  const uint8_t *pool;
+  const int32_t *btrow;
+  int64_t num_pages, page_bytes, slab_off;  // slab_off = h * slab_bytes
+  int P, pidx, o0, tok0, clen;
+  const uint8_t *slab;
+  bool page_ok;
+
+  __device__ __forceinline__ void enter_page(int32_t *err_word, bool reporter) {
+    int32_t page = __ldg(btrow + pidx);
+    page_ok = page >= 0 && (int64_t)page < num_pages;
+    if (!page_ok) {
+      if (reporter) report(err_word, TQ_DEVERR_PAGE_RANGE);
+      page = 0;
+    }
+    slab = pool + (int64_t)page * page_bytes + slab_off;
+  }
+  __device__ __forceinline__ const uint8_t *slab_of(int pi) const {
+    const int32_t page = __ldg(btrow + pi);
+    return (page >= 0 && (int64_t)page < num_pages) ? pool + (int64_t)page * page_bytes + slab_off : nullptr;
+  }
+  __device__ __forceinline__ int live() const { return page_ok ? clen - tok0 : 0; }
+  __device__ __forceinline__ bool advance() {  // true when a new page starts
+    tok0 += 16;
+    o0 += 16;
+    if (o0 == P) {
+      o0 = 0;
+      ++pidx;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Keep two tiles of registers in flight per warp (1) or one (0).
+#ifndef TQ_TILE_DOUBLE_BUFFER
+#define TQ_TILE_DOUBLE_BUFFER 0
+#endif
+
+// Pages of a segment staged in L2 ahead of the page being read.
+#ifndef TQ_L2_PREFETCH
+#define TQ_L2_PREFETCH 1
+#endif
+
+// Shared-memory placement of the two centroid tables.  The value table
+// ([EV][32] 4-byte entries, 128-byte rows) starts on a 32 KB boundary and the
+// key table ([EK][32] 8-byte (hi, lo) entries, 256-byte rows) on a 64 KB
+// boundary, so an entry address is (table base | pair code << row shift |
+// lane slot) and one prmt / lop3 builds it.  The allocation covers the worst
+// alignment slack.
+constexpr uint32_t kValTableAlign = 32768, kKeyTableAlign = 65536;
+constexpr size_t kAttnSmemBytes = 196608;
+
 template <int KB, int VB, bool QJL, int NT>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnArgs a) {
   constexpr int EK = 1 << (2 * KB), EV = 1 << (2 * VB);
+  static_assert(EV * 128 <= (int)kValTableAlign && EK * 256 <= (int)kKeyTableAlign, "table sizes");
   extern __shared__ __align__(16) uint8_t smem[];
-  uint2 *lutK = reinterpret_cast<uint2 *>(smem);            // [EK][32] (hi, lo) x256
-  uint32_t *lutV = reinterpret_cast<uint32_t *>(lutK + EK * 32);  // [EV][32] x256
+  const uint32_t smem_s = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t lutV_s = (smem_s + kValTableAlign - 1) & ~(kValTableAlign - 1);
+  const uint32_t lutK_s = (lutV_s + kValTableAlign + kKeyTableAlign - 1) & ~(kKeyTableAlign - 1);
+  uint32_t *lutV = reinterpret_cast<uint32_t *>(smem + (lutV_s - smem_s));  // [EV][32]
+  uint2 *lutK = reinterpret_cast<uint2 *>(smem + (lutK_s - smem_s));        // [EK][32] (hi, lo)
 
-  // Bank-private centroid-pair tables: entry e of lane l lives in bank l.
+  // Bank-private centroid-pair tables: lane l reads its own copy in bank l.
   for (int i = threadIdx.x; i < EK * 32; i += blockDim.x) {
     const int e = i >> 5;
     __half h0, l0, h1, l1;
@@ -169,9 +250,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
   if (wg >= NW) return;
   const int64_t ts = T * wg / NW, te = T * (wg + 1) / NW;
   if (ts >= te) return;
-  const uint2 *lutK_l = lutK + lane;
-  const uint32_t *lutV_l = lutV + lane;
+  const uint32_t laneK = lutK_s | ((uint32_t)lane * 8u);
+  const uint32_t laneV = lutV_s | ((uint32_t)lane * 4u);
   const int H = a.H, G = a.G, Hq = a.Hq;
+  const int tpp = a.P >> 4;
+  const uint32_t slab_bytes = (uint32_t)a.slab_bytes;
 
   // locate the first tile: largest b with H * pre[b] <= ts
   int b = 0;
@@ -183,14 +266,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
     }
     b = lo;
   }
-  int64_t tb = a.pre[b + 1] - a.pre[b];
+  int tb = (int)(a.pre[b + 1] - a.pre[b]);
   int h = (int)((ts - H * a.pre[b]) / tb);
-  int64_t j = (ts - H * a.pre[b]) - (int64_t)h * tb;
+  int j = (int)((ts - H * a.pre[b]) - (int64_t)h * tb);
   int64_t pos = ts;
 
   while (pos < te) {
-    const int64_t seg_tiles = min(te - pos, tb - j);
-    const int clen = a.clen[b];
+    const int seg_tiles = (int)min(te - pos, (int64_t)(tb - j));
 
     // ---- segment setup: query operands for the G heads of (b, h)
     uint32_t qb[NT][8][2];
@@ -220,19 +302,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
         const int es = gval ? a.q_exp[qrow * 2 + 1] : 0;
         const float ss = ldexpf(1.0f, es);
         const float *qs = a.q_s + qrow * kM + 32 * t;
-        float v[32];
-#pragma unroll
-        for (int k4 = 0; k4 < 8; k4++) {
-          const float4 f = gval ? *reinterpret_cast<const float4 *>(qs + 4 * k4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[4 * k4] = f.x * ss; v[4 * k4 + 1] = f.y * ss; v[4 * k4 + 2] = f.z * ss; v[4 * k4 + 3] = f.w * ss;
-        }
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
+          // b0 pairs sign bits (2kk, 2kk+16), b1 pairs (2kk+1, 2kk+17) of word t
+          const float v0 = gval ? qs[2 * kk] * ss : 0.f, v1 = gval ? qs[2 * kk + 16] * ss : 0.f;
+          const float v2 = gval ? qs[2 * kk + 1] * ss : 0.f, v3 = gval ? qs[2 * kk + 17] * ss : 0.f;
           __half h0, l0, h1, l1, h2, l2, h3, l3;
-          split_half(v[2 * kk], h0, l0);
-          split_half(v[2 * kk + 16], h1, l1);
-          split_half(v[2 * kk + 1], h2, l2);
-          split_half(v[2 * kk + 17], h3, l3);
+          split_half(v0, h0, l0);
+          split_half(v1, h1, l1);
+          split_half(v2, h2, l2);
+          split_half(v3, h3, l3);
           sb[nt][kk][0] = lo_part ? pack_half2_raw(l0, l1) : pack_half2_raw(h0, h1);
           sb[nt][kk][1] = lo_part ? pack_half2_raw(l2, l3) : pack_half2_raw(h2, h3);
         }
@@ -264,98 +343,187 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
     }
     float nu = 0.f;
 
-    TileRegs<KB, VB, QJL> cur, nxt;
-    load_tile<KB, VB, QJL>(a, b, h, j, clen, r, t, cur);
-    for (int64_t k = 0; k < seg_tiles; k++) {
-      if (k + 1 < seg_tiles) load_tile<KB, VB, QJL>(a, b, h, j + k + 1, clen, r, t, nxt);
-      if (__any_sync(0xffffffffu, cur.ok0 || cur.ok1)) {
-        // ---- scores
-        float sk[NT][4], sq[NT][4];
+    TileCursor cur;
+    cur.pool = a.pool;
+    cur.btrow = a.block_tables + (int64_t)b * a.max_pages;
+    cur.num_pages = a.num_pages;
+    cur.page_bytes = a.page_bytes;
+    cur.slab_off = (int64_t)h * a.slab_bytes;
+    cur.P = a.P;
+    cur.pidx = j / tpp;
+    cur.o0 = (j - cur.pidx * tpp) * 16;
+    cur.tok0 = j * 16;
+    cur.clen = a.clen[b];
+    const int last_page = (j + seg_tiles - 1) / tpp;
+    if (TQ_L2_PREFETCH > 0 && lane == 0) {  // stage the first pages of the segment in L2
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-          for (int i = 0; i < 4; i++) { sk[nt][i] = 0.f; sq[nt][i] = 0.f; }
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          const uint2 L00 = lutK_l[key_pair<KB>(cur.k0, 2 * kk) << 5];
-          const uint2 L10 = lutK_l[key_pair<KB>(cur.k1, 2 * kk) << 5];
-          const uint2 L01 = lutK_l[key_pair<KB>(cur.k0, 2 * kk + 1) << 5];
-          const uint2 L11 = lutK_l[key_pair<KB>(cur.k1, 2 * kk + 1) << 5];
-#pragma unroll
-          for (int nt = 0; nt < NT; nt++) {
-            mma_16816(sk[nt], L00.x, L10.x, L01.x, L11.x, qb[nt][kk][0], qb[nt][kk][1]);
-            mma_16816(sk[nt], L00.y, L10.y, L01.y, L11.y, qb[nt][kk][0], qb[nt][kk][1]);
-          }
-          if constexpr (QJL) {
-            const uint32_t a0 = sign_pair(cur.s0, 2 * kk), a1 = sign_pair(cur.s1, 2 * kk);
-            const uint32_t a2 = sign_pair(cur.s0, 2 * kk + 1), a3 = sign_pair(cur.s1, 2 * kk + 1);
-#pragma unroll
-            for (int nt = 0; nt < NT; nt++) mma_16816(sq[nt], a0, a1, a2, a3, sb[nt][kk][0], sb[nt][kk][1]);
-          }
+      for (int d = 0; d <= TQ_L2_PREFETCH; d++)
+        if (cur.pidx + d <= last_page) {
+          const uint8_t *sp = cur.slab_of(cur.pidx + d);
+          if (sp) prefetch_l2(sp, slab_bytes);
         }
-        // ---- online softmax (log2 domain) and value weights
-        float vn0 = cur.ok0 ? cur.nv0 : 0.f, vn1 = cur.ok1 ? cur.nv1 : 0.f;
-        const float tnu = warp_max_xor(fmaxf(vn0, vn1), 4 | 8 | 16);
-        const float nu_new = fmaxf(nu, tnu);
-        const float nu_ratio = nu_new > 0.f ? nu / nu_new : 1.f;
-        const float inv_nu = nu_new > 0.f ? kWeightScale / nu_new : 0.f;
-        nu = nu_new;
-        uint32_t wb[NT][2];
-        bool rescale = false;
-        float beta[NT];
+    }
+    cur.enter_page(a.err_word, lane == 0);
+
+    auto process = [&](const TileRegs<KB, VB, QJL> &R) {
+      if (!__any_sync(0xffffffffu, R.ok0)) return;  // token 0 of a tile is live iff any is
+      // ---- scores: hi-part, lo-part and QJL chains run independently
+      float sk[NT][4], sl[NT][4], sq[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int i = 0; i < 4; i++) { sk[nt][i] = 0.f; sl[nt][i] = 0.f; sq[nt][i] = 0.f; }
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) {
+        const uint2 L00 = lds64(key_addr<KB>(R.k0, 2 * kk, laneK));
+        const uint2 L10 = lds64(key_addr<KB>(R.k1, 2 * kk, laneK));
+        const uint2 L01 = lds64(key_addr<KB>(R.k0, 2 * kk + 1, laneK));
+        const uint2 L11 = lds64(key_addr<KB>(R.k1, 2 * kk + 1, laneK));
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) {
-          float l0 = (sk[nt][0] + sk[nt][1]) * cK[nt];
-          float l1 = (sk[nt][2] + sk[nt][3]) * cK[nt];
-          if constexpr (QJL) {
-            l0 = fmaf(cur.g0 * (sq[nt][0] + sq[nt][1]), cQ[nt], l0);
-            l1 = fmaf(cur.g1 * (sq[nt][2] + sq[nt][3]), cQ[nt], l1);
-          }
-          l0 = cur.ok0 ? cur.nk0 * l0 : -INFINITY;
-          l1 = cur.ok1 ? cur.nk1 * l1 : -INFINITY;
-          const float tmax = warp_max_xor(fmaxf(l0, l1), 4 | 8 | 16);
-          const float mnew = fmaxf(mu[nt], tmax);
-          const float alpha = exp2f(mu[nt] - mnew);
-          const float p0 = exp2f(l0 - mnew), p1 = exp2f(l1 - mnew);
-          lsum[nt] = fmaf(lsum[nt], alpha, p0 + p1);
-          mu[nt] = mnew;
-          beta[nt] = alpha * nu_ratio;
-          rescale |= beta[nt] != 1.f;
-          const float w0 = p0 * vn0 * inv_nu, w1 = p1 * vn1 * inv_nu;
-          __half wh0, wl0, wh1, wl1;
-          split_half(w0, wh0, wl0);
-          split_half(w1, wh1, wl1);
-          const uint32_t Wh = pack_half2_raw(wh0, wh1), Wl = pack_half2_raw(wl0, wl1);
-          const int src0 = 4 * (2 * t) + (r >> 1), src1 = src0 + 4;
-          const uint32_t h0 = __shfl_sync(0xffffffffu, Wh, src0), q0 = __shfl_sync(0xffffffffu, Wl, src0);
-          const uint32_t h1 = __shfl_sync(0xffffffffu, Wh, src1), q1 = __shfl_sync(0xffffffffu, Wl, src1);
-          const uint32_t x0 = (r & 1) ? q0 : h0, x1 = (r & 1) ? q1 : h1;
-          wb[nt][0] = __byte_perm(x0, x1, 0x5410);
-          wb[nt][1] = __byte_perm(x0, x1, 0x7632);
+          mma_16816(sk[nt], L00.x, L10.x, L01.x, L11.x, qb[nt][kk][0], qb[nt][kk][1]);
+          mma_16816(sl[nt], L00.y, L10.y, L01.y, L11.y, qb[nt][kk][0], qb[nt][kk][1]);
         }
-        if (__any_sync(0xffffffffu, rescale)) {
+        if constexpr (QJL) {
+          const uint32_t a0 = sign_pair(R.s0, 2 * kk), a1 = sign_pair(R.s1, 2 * kk);
+          const uint32_t a2 = sign_pair(R.s0, 2 * kk + 1), a3 = sign_pair(R.s1, 2 * kk + 1);
 #pragma unroll
-          for (int mt = 0; mt < 8; mt++)
-#pragma unroll
-            for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-              for (int i = 0; i < 4; i++) acc[mt][nt][i] *= beta[nt];
-        }
-        // ---- values
-#pragma unroll
-        for (int mt = 0; mt < 8; mt++) {
-          const uint32_t V0 = lutV_l[value_pair<VB>(cur.vlo[0], cur.vhi[0], mt) << 5];
-          const uint32_t V1 = lutV_l[value_pair<VB>(cur.vlo[1], cur.vhi[1], mt) << 5];
-          const uint32_t V2 = lutV_l[value_pair<VB>(cur.vlo[2], cur.vhi[2], mt) << 5];
-          const uint32_t V3 = lutV_l[value_pair<VB>(cur.vlo[3], cur.vhi[3], mt) << 5];
-          const uint32_t a0 = __byte_perm(V0, V1, 0x5410), a1 = __byte_perm(V0, V1, 0x7632);
-          const uint32_t a2 = __byte_perm(V2, V3, 0x5410), a3 = __byte_perm(V2, V3, 0x7632);
-#pragma unroll
-          for (int nt = 0; nt < NT; nt++) mma_16816(acc[mt][nt], a0, a1, a2, a3, wb[nt][0], wb[nt][1]);
+          for (int nt = 0; nt < NT; nt++) mma_16816(sq[nt], a0, a1, a2, a3, sb[nt][kk][0], sb[nt][kk][1]);
         }
       }
-      cur = nxt;
+      // ---- online softmax (log2 domain) and value weights
+      const float vn0 = R.ok0 ? R.nv0 : 0.f, vn1 = R.ok1 ? R.nv1 : 0.f;
+      const float tnu = warp_max_xor(fmaxf(vn0, vn1), 4 | 8 | 16);
+      const float nu_new = fmaxf(nu, tnu);
+      const float rcp_nu = nu_new > 0.f ? __frcp_rn(nu_new) : 0.f;
+      const float nu_ratio = nu_new > 0.f ? nu * rcp_nu : 1.f;
+      const float inv_nu = kWeightScale * rcp_nu;
+      nu = nu_new;
+      uint32_t wb[NT][2];
+      bool rescale = false;
+      float beta[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++) {
+        float l0 = ((sk[nt][0] + sk[nt][1]) + (sl[nt][0] + sl[nt][1])) * cK[nt];
+        float l1 = ((sk[nt][2] + sk[nt][3]) + (sl[nt][2] + sl[nt][3])) * cK[nt];
+        if constexpr (QJL) {
+          l0 = fmaf(R.g0 * (sq[nt][0] + sq[nt][1]), cQ[nt], l0);
+          l1 = fmaf(R.g1 * (sq[nt][2] + sq[nt][3]), cQ[nt], l1);
+        }
+        l0 = R.ok0 ? R.nk0 * l0 : -INFINITY;
+        l1 = R.ok1 ? R.nk1 * l1 : -INFINITY;
+        const float tmax = warp_max_xor(fmaxf(l0, l1), 4 | 8 | 16);
+        const float mnew = fmaxf(mu[nt], tmax);
+        const float alpha = fast_exp2(mu[nt] - mnew);
+        const float p0 = fast_exp2(l0 - mnew), p1 = fast_exp2(l1 - mnew);
+        lsum[nt] = fmaf(lsum[nt], alpha, p0 + p1);
+        mu[nt] = mnew;
+        beta[nt] = alpha * nu_ratio;
+        rescale |= beta[nt] != 1.f;
+        const float w0 = p0 * vn0 * inv_nu, w1 = p1 * vn1 * inv_nu;
+        __half wh0, wl0, wh1, wl1;
+        split_half(w0, wh0, wl0);
+        split_half(w1, wh1, wl1);
+        const uint32_t Wh = pack_half2_raw(wh0, wh1), Wl = pack_half2_raw(wl0, wl1);
+        // B operand column r = (head 4nt + r/2, hi or lo): weights of tokens
+        // 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) from the lanes that own them
+        const int src0 = 4 * (2 * t) + (r >> 1), src1 = src0 + 4;
+        const uint32_t h0 = __shfl_sync(0xffffffffu, Wh, src0), q0 = __shfl_sync(0xffffffffu, Wl, src0);
+        const uint32_t h1 = __shfl_sync(0xffffffffu, Wh, src1), q1 = __shfl_sync(0xffffffffu, Wl, src1);
+        const uint32_t x0 = (r & 1) ? q0 : h0, x1 = (r & 1) ? q1 : h1;
+        wb[nt][0] = __byte_perm(x0, x1, 0x5410);
+        wb[nt][1] = __byte_perm(x0, x1, 0x7632);
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) acc[mt][nt][i] *= beta[nt];
+      }
+      // ---- values: interleave the codes of the token pairs (2t, 2t+1) and
+      // (2t+8, 2t+9) at each coordinate; one lookup gives an A register.
+      // Row r of m-tile mt is coordinate 16r+2mt, row r+8 is 16r+2mt+1.
+      uint32_t ev[2][2][2];  // [token pair][even/odd coordinate][word]
+#pragma unroll
+      for (int tp = 0; tp < 2; tp++) {
+#pragma unroll
+        for (int wi = 0; wi < 2; wi++) {
+          const uint32_t wa = wi ? R.vhi[2 * tp] : R.vlo[2 * tp];
+          const uint32_t wz = wi ? R.vhi[2 * tp + 1] : R.vlo[2 * tp + 1];
+          if constexpr (VB == 4) {
+            ev[tp][0][wi] = (wa & 0x0F0F0F0Fu) | ((wz << 4) & 0xF0F0F0F0u);  // byte k: coordinate 2k
+            ev[tp][1][wi] = ((wa >> 4) & 0x0F0F0F0Fu) | (wz & 0xF0F0F0F0u);  // byte k: coordinate 2k+1
+          } else if constexpr (VB == 2) {
+            ev[tp][0][wi] = (wa & 0x33333333u) | ((wz << 2) & 0xCCCCCCCCu);  // nibble k: coordinate 2k
+            ev[tp][1][wi] = ((wa >> 2) & 0x33333333u) | (wz & 0xCCCCCCCCu);  // nibble k: coordinate 2k+1
+          } else {
+            ev[tp][0][wi] = 0u;
+            ev[tp][1][wi] = 0u;
+          }
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; mt++) {
+        uint32_t av[4];  // (tokens 2t,2t+1 | 2t+8,2t+9) x (coordinate 16r+2mt | 16r+2mt+1)
+#pragma unroll
+        for (int tp = 0; tp < 2; tp++) {
+#pragma unroll
+          for (int eo = 0; eo < 2; eo++) {
+            uint32_t addr;
+            if constexpr (VB == 4) {
+              addr = field_at<7>(ev[tp][eo][mt >> 2], 0u, 8 * (mt & 3), 8, laneV);
+            } else if constexpr (VB == 2) {
+              addr = field_at<7>(ev[tp][eo][0], 0u, 4 * mt, 4, laneV);
+            } else {  // 3-bit: gather the two codes of coordinate 16r+2mt+eo
+              const int p3 = 3 * (2 * mt + eo);
+              addr = field_at<7>(R.vlo[2 * tp], R.vhi[2 * tp], p3, 3, laneV) |
+                     field_at<10>(R.vlo[2 * tp + 1], R.vhi[2 * tp + 1], p3, 3, 0u);
+            }
+            av[2 * tp + eo] = lds32(addr);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) mma_16816(acc[mt][nt], av[0], av[1], av[2], av[3], wb[nt][0], wb[nt][1]);
+      }
+    };
+
+    // next tile position: stage the page TQ_L2_PREFETCH ahead whenever a page starts
+    auto step_cursor = [&]() {
+      if (cur.advance()) {
+        cur.enter_page(a.err_word, lane == 0);
+        if (TQ_L2_PREFETCH > 0 && lane == 0 && cur.pidx + TQ_L2_PREFETCH <= last_page) {
+          const uint8_t *sp = cur.slab_of(cur.pidx + TQ_L2_PREFETCH);
+          if (sp) prefetch_l2(sp, slab_bytes);
+        }
+      }
+    };
+
+#if TQ_TILE_DOUBLE_BUFFER
+    // the next tile's loads are in flight while this one is computed
+    TileRegs<KB, VB, QJL> ra, rb;
+    load_tile<KB, VB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, ra);
+    int k = 0;
+    for (; k + 2 <= seg_tiles; k += 2) {
+      step_cursor();
+      load_tile<KB, VB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, rb);
+      process(ra);
+      if (k + 2 < seg_tiles) {
+        step_cursor();
+        load_tile<KB, VB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, ra);
+      }
+      process(rb);
     }
+    if (k < seg_tiles) process(ra);
+#else
+    for (int k = 0; k < seg_tiles; k++) {
+      TileRegs<KB, VB, QJL> ra;
+      load_tile<KB, VB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, ra);
+      process(ra);
+      if (k + 1 < seg_tiles) step_cursor();
+    }
+#endif
 
     // ---- segment partial: slot = warp + unit
     const int64_t slot = wg + (int64_t)b * H + h;
@@ -388,7 +556,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
       if (++h == H) {
         h = 0;
         do { ++b; } while (a.pre[b + 1] == a.pre[b]);
-        tb = a.pre[b + 1] - a.pre[b];
+        tb = (int)(a.pre[b + 1] - a.pre[b]);
       }
     }
   }
@@ -396,13 +564,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
 
 template <int KB, int VB, bool QJL, int NT>
 cudaError_t attn_main_launch_t(const AttnArgs &a, bool query_only, int *blocks_per_sm, int blocks, cudaStream_t st) {
-  constexpr int EK = 1 << (2 * KB), EV = 1 << (2 * VB);
-  constexpr size_t smem = (size_t)EK * 32 * 8 + (size_t)EV * 32 * 4;
   auto kern = attn_main_kernel<KB, VB, QJL, NT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static unsigned long long done = 0;
+  cudaError_t e = set_smem_once(kern, (int)kAttnSmemBytes, done);
   if (e != cudaSuccess) return e;
-  if (query_only) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kern, kAttnThreads, smem);
-  kern<<<blocks, kAttnThreads, smem, st>>>(a);
+  if (query_only) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kern, kAttnThreads, kAttnSmemBytes);
+  kern<<<blocks, kAttnThreads, kAttnSmemBytes, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -321,7 +321,8 @@ template <int BITS, bool QJL>
 static cudaError_t launch_encode_t(const EncodeArgs &a, int sms, cudaStream_t st) {
   const size_t smem = QJL ? (size_t)kM * kD * sizeof(float) : 0;
   if (QJL) {
-    cudaError_t e = cudaFuncSetAttribute(encode_kernel<BITS, QJL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static unsigned long long done = 0;
+    cudaError_t e = set_smem_once(encode_kernel<BITS, QJL>, (int)smem, done);
     if (e != cudaSuccess) return e;
   }
   const int64_t quads = a.n_tokens * a.H;
@@ -337,7 +338,8 @@ template <int BITS, bool QJL>
 static cudaError_t launch_decode_t(const DecodeArgs &a, int sms, cudaStream_t st) {
   const size_t smem = QJL ? (size_t)kM * kD * sizeof(float) : 0;
   if (QJL) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<BITS, QJL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static unsigned long long done = 0;
+    cudaError_t e = set_smem_once(decode_kernel<BITS, QJL>, (int)smem, done);
     if (e != cudaSuccess) return e;
   }
   const int64_t quads = a.n_tokens * a.H;

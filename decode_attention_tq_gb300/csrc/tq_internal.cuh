@@ -94,7 +94,25 @@ cudaError_t attn_main_k3(const AttnArgs &a, int v_bits, bool qjl, int nt, bool q
 cudaError_t attn_main_k4(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
                          int blocks, cudaStream_t st);
 
-constexpr int kAttnThreads = 256;
+// Set a kernel's dynamic shared-memory limit once per device (never inside a
+// stream capture after the first call on that device).
+template <typename K>
+cudaError_t set_smem_once(K kernel, int bytes, unsigned long long &done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
+  return e;
+}
+
+// Threads per CTA of the main attention kernel (one CTA per SM).
+#ifndef TQ_ATTN_THREADS
+#define TQ_ATTN_THREADS 512
+#endif
+constexpr int kAttnThreads = TQ_ATTN_THREADS;
 constexpr int kAttnWarps = kAttnThreads / 32;
 
 }  // namespace tq

@@ -65,7 +65,9 @@ def load_library():
             lib.tq_decode.argtypes = [P, i32, P, i64, P, i64, P, P, P, P, P, P]
             lib.tq_decode_attn_workspace_size.argtypes = [P, i32, i32, i32, i32, C.POINTER(sz)]
             lib.tq_decode_attn.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P]
-            for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn"):
+            lib.tq_decode_attn_timed.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P, P, P]
+            for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn",
+                      "tq_decode_attn_timed"):
                 getattr(lib, f).restype = C.c_int
             _lib = lib
     return _lib
@@ -169,10 +171,32 @@ def tq_decode_attn_workspace_size(fmt, batch: int, num_q_heads: int, max_pages: 
 
 def tq_decode_attn(fmt, q, page_pool, num_pages: int, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs,
                    k_codebook, v_codebook, S, out, workspace, err_word=None, stream=None):
+    return _decode_attn(fmt, q, page_pool, num_pages, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs,
+                        k_codebook, v_codebook, S, out, workspace, err_word, stream, None)
+
+
+def tq_decode_attn_timed(fmt, q, page_pool, num_pages: int, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs,
+                         k_codebook, v_codebook, S, out, workspace, main_begin, main_end, err_word=None, stream=None):
+    """tq_decode_attn that also records torch.cuda.Event objects around the split-KV main kernel."""
+    return _decode_attn(fmt, q, page_pool, num_pages, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs,
+                        k_codebook, v_codebook, S, out, workspace, err_word, stream, (main_begin, main_end))
+
+
+def _event(ev):
+    if ev is None:
+        return None
+    return C.c_void_p(ev.cuda_event if hasattr(ev, "cuda_event") else int(ev))
+
+
+def _decode_attn(fmt, q, page_pool, num_pages, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs,
+                 k_codebook, v_codebook, S, out, workspace, err_word, stream, events):
     F = _fmt(fmt)
     B, Hq, _ = q.shape
     window = 0 if k_win is None else int(k_win.shape[2])
-    rc = load_library().tq_decode_attn(
+    lib = load_library()
+    fn = lib.tq_decode_attn if events is None else lib.tq_decode_attn_timed
+    extra = () if events is None else (_event(events[0]), _event(events[1]))
+    rc = fn(
         C.byref(F), int(B), int(Hq), _dev_ptr(q, torch.float16, "q"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
         _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]), _dev_ptr(comp_lens, torch.int32, "comp_lens"),
         _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True),
@@ -180,7 +204,7 @@ def tq_decode_attn(fmt, q, page_pool, num_pages: int, block_tables, comp_lens, k
         _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
         _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
         _dev_ptr(out, torch.float32, "out"), _dev_ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()),
-        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), *extra, _stream(stream),
     )
-    _check(rc, "tq_decode_attn")
+    _check(rc, "tq_decode_attn" if events is None else "tq_decode_attn_timed")
     return out

@@ -169,6 +169,21 @@ tq_status tq_decode_attn(const tq_format *fmt, int batch, int num_q_heads, const
                          const float *v_codebook, const float *S, float *out, void *workspace,
                          size_t workspace_bytes, int32_t *err_word, void *stream);
 
+/*
+ * tq_decode_attn, and additionally records two caller-created CUDA events
+ * (cudaEvent_t, may be NULL) on `stream` immediately before and after the
+ * split-KV main kernel, so a caller can time the dominant kernel in place
+ * with cudaEventElapsedTime.  Same arguments, results and errors otherwise.
+ */
+tq_status tq_decode_attn_timed(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                               const void *page_pool, int64_t num_pages, const int32_t *block_tables,
+                               int max_pages, const int32_t *comp_lens, const void *k_win_f16,
+                               const void *v_win_f16, const int32_t *win_lens, int window,
+                               const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
+                               const float *v_codebook, const float *S, float *out, void *workspace,
+                               size_t workspace_bytes, int32_t *err_word, void *main_begin_event,
+                               void *main_end_event, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
