@@ -196,7 +196,7 @@ class DecodeBench:
         self.main_bytes = B * H * comp * (bph["k"] + bph["v"]) + B * self.pages_per_seq * 4  # per layer launch
         self.window_bytes = B * H * wl.win_tokens * d * 2 * 2
         self.step_bytes = wl.layers * (self.main_bytes + self.window_bytes + B * Hq * d * (2 + 4))
-        self.launches_per_step = wl.layers * (2 + 3 + (1 if W else 0))
+        self.launches_per_step = wl.layers * (2 + 3)  # 2 appends + prep (with window chunks), main, merge
 
     def step(self, events=None):
         tq, f = self.tq, self.fmt
@@ -458,21 +458,25 @@ def oracle_time(s, heads, cores):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(wl: ti.DecodeWorkload, device, target_cpu_s: float = 15.0):
+def cpu_baseline(wl: ti.DecodeWorkload, device, target_cpu_s: float = 20.0):
     """The oracle as it stands, on a bounded sample: whole sequences (all query
-    heads) of layer 0, about `target_cpu_s` seconds of CPU work."""
+    heads) of layer 0, sized to about `target_cpu_s` seconds of CPU work."""
     cores = host_cores()
     Hq = wl.q_heads
-    n_seq = 2
-    s = oracle_sample_setup(wl, n_seq, device)
+    s = oracle_sample_setup(wl, 1, device)
     probe = oracle_time(s, [0], 1)  # one query head on one core
-    n_heads = int(max(1, min(Hq * n_seq, target_cpu_s / max(probe, 1e-3))))
+    rows = int(max(1, target_cpu_s / max(probe, 1e-3)))
+    n_seq = int(min(wl.batch, 8, max(1, -(-rows // Hq))))
+    if n_seq > 1:
+        s = oracle_sample_setup(wl, n_seq, device)
+    n_heads = int(min(rows, Hq * n_seq))
     heads = list(range(n_heads))
     dt = oracle_time(s, heads, cores)
     tokens = wl.context * n_heads / Hq  # a sequence-token counts once per layer, all heads included
     return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"layer 0: {n_heads} (sequence, query head) rows of {Hq} heads per sequence at context {wl.context}, "
-                      f"= {n_heads / Hq:.2f} sequence-layers; {dt:.2f} s wall on {cores} threads"}
+                      f"= {n_heads / Hq:.2f} sequence-layers; {dt:.2f} s wall on {cores} threads "
+                      f"(~{n_heads * probe:.0f} s of CPU work)"}
 
 
 def run_reference(args, rank, world):

@@ -118,7 +118,7 @@ struct AttnPlan {
       total;
 };
 
-constexpr int kMinTilesPerWarp = 16;
+constexpr int kMinTilesPerWarp = 4;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -159,11 +159,12 @@ tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int w
   }
   const int64_t tiles_max = (int64_t)B * H * max_pages * (f->page_size / kTile);
   int64_t warps = (tiles_max + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
-  const int64_t cap = (int64_t)sms * bps * kAttnWarps;
+  const int wpb = attn_warps(p->NT, f->k_qjl != 0);
+  const int64_t cap = (int64_t)sms * bps * wpb;
   if (warps > cap) warps = cap;
   if (warps < 1) warps = 1;
-  p->blocks = (int)((warps + kAttnWarps - 1) / kAttnWarps);
-  p->nw_launch = p->blocks * kAttnWarps;
+  p->blocks = (int)((warps + wpb - 1) / wpb);
+  p->nw_launch = p->blocks * wpb;
 
   const int64_t rows = (int64_t)B * Hq;
   const int64_t slots = (int64_t)p->nw_launch + (int64_t)B * H;
@@ -177,8 +178,9 @@ tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int w
   p->off_qexp = off;   off = align256(off + sizeof(int32_t) * rows * 2);
   p->off_segml = off;  off = align256(off + sizeof(float) * slots * p->G * 2);
   p->off_segacc = off; off = align256(off + sizeof(float) * slots * p->G * kD);
-  p->off_winml = off;  off = align256(off + (window > 0 ? sizeof(float) * rows * 2 : 0));
-  p->off_winacc = off; off = align256(off + (window > 0 ? sizeof(float) * rows * kD : 0));
+  const int64_t nch = (window + kWinChunk - 1) / kWinChunk;
+  p->off_winml = off;  off = align256(off + sizeof(float) * rows * nch * 2);
+  p->off_winacc = off; off = align256(off + sizeof(float) * rows * nch * kD);
   p->total = off;
   return TQ_OK;
 }
@@ -389,7 +391,6 @@ static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_hea
   if (ev_begin && cudaEventRecord(ev_begin, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (main_kernel_call(fmt, a, p.NT, false, nullptr, p.blocks, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, st) != cudaSuccess) return TQ_ERR_CUDA;
-  if (window > 0 && launch_attn_window(a, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (launch_attn_merge(a, st) != cudaSuccess) return TQ_ERR_CUDA;
   return TQ_OK;
 }

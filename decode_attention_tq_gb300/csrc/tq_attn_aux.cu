@@ -1,32 +1,34 @@
 // tq_attn_aux.cu -- the small kernels around the split-KV main kernel:
-//   prep   : rotate each query once into the key basis (q_rot = H (D_K . q)/sqrt(d)),
-//            project it for the QJL term (q_s = S q_rot), choose power-of-two
-//            operand scales, clamp the lengths and build the tile prefix sums;
-//   window : attention partial over the raw fp16 recent-token window;
-//   merge  : log-sum-exp merge of all partials of a (sequence, query head),
-//            one inverse rotation of the value accumulator (D_V . H acc / d),
-//            plus the window part, normalised.
+//   prep   : (one launch, three kinds of block) tile prefix sums and clamped
+//            lengths; each query rotated once into the key basis
+//            (q_rot = H (D_K . q)/sqrt(d)), projected for the QJL term
+//            (q_s = S q_rot), with power-of-two operand scales; and
+//            attention partials over the raw fp16 recent-token window, one
+//            per 32-token chunk;
+//   merge  : log-sum-exp merge of the compressed partials of a (sequence,
+//            query head), one inverse rotation of their value accumulator
+//            (D_V . H acc / d), then the window partials, normalised.
 #include "tq_internal.cuh"
 
 namespace tq {
 
-__global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool qjl) {
-  __shared__ float s_q[4][kD];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    const int64_t cap = (int64_t)a.max_pages * a.P;
-    int64_t acc = 0;
-    a.pre[0] = 0;
-    for (int b = 0; b < a.B; b++) {
+// Block 0, warp 0: clamped lengths and tile prefix sums, 32 sequences at a
+// time (a warp scan), then the header the main and merge kernels read.
+__device__ void prep_lengths(const AttnArgs &a, int lane) {
+  const int64_t cap = (int64_t)a.max_pages * a.P;
+  int64_t carry = 0;
+  if (lane == 0) a.pre[0] = 0;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    const int b = b0 + lane;
+    int64_t tiles = 0;
+    if (b < a.B) {
       int64_t c = a.comp_lens[b];
       if (c < 0 || c > cap) {
         report(a.err_word, TQ_DEVERR_LENGTH);
         c = c < 0 ? 0 : cap;
       }
       a.clen[b] = (int32_t)c;
-      acc += (c + kTile - 1) / kTile;
-      a.pre[b + 1] = acc;
+      tiles = (c + kTile - 1) / kTile;
       int32_t wl = 0;
       if (a.window > 0 && a.win_lens) {
         wl = a.win_lens[b];
@@ -37,15 +39,26 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
       }
       a.wlen[b] = wl;
     }
-    const int64_t total = acc * a.H;
+    int64_t inc = tiles;  // inclusive scan over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (b < a.B) a.pre[b + 1] = carry + inc;
+    carry += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (lane == 0) {
+    const int64_t total = carry * a.H;
     int64_t nw = (total + a.min_tiles - 1) / a.min_tiles;
     if (nw > a.nw_launch) nw = a.nw_launch;
     a.hdr->total_tiles = total;
     a.hdr->active_warps = total > 0 ? nw : 0;
   }
+}
 
-  const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // b * Hq + qh
-  if (row >= (int64_t)a.B * a.Hq) return;
+// One warp per query row: rotation, QJL projection, operand exponents.
+__device__ void prep_query(const AttnArgs &a, bool qjl, int64_t row, int lane, float *s_q) {
   // lane holds coordinates 4*lane .. 4*lane+3
   const uint2 raw = *reinterpret_cast<const uint2 *>(a.q + row * kD + 4 * lane);
   const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
@@ -70,7 +83,7 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
   int es = 0;
   if (qjl) {
 #pragma unroll
-    for (int i = 0; i < 4; i++) s_q[warp][4 * lane + i] = x[i];
+    for (int i = 0; i < 4; i++) s_q[4 * lane + i] = x[i];
     __syncwarp();
     float ys[4];
     float my = 0.f;
@@ -81,10 +94,10 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
 #pragma unroll 8
       for (int k = 0; k < kD / 4; k++) {
         const float4 s = __ldg(srow + k);
-        acc = fmaf(s.x, s_q[warp][4 * k], acc);
-        acc = fmaf(s.y, s_q[warp][4 * k + 1], acc);
-        acc = fmaf(s.z, s_q[warp][4 * k + 2], acc);
-        acc = fmaf(s.w, s_q[warp][4 * k + 3], acc);
+        acc = fmaf(s.x, s_q[4 * k], acc);
+        acc = fmaf(s.y, s_q[4 * k + 1], acc);
+        acc = fmaf(s.z, s_q[4 * k + 2], acc);
+        acc = fmaf(s.w, s_q[4 * k + 3], acc);
       }
       ys[i] = acc;
       my = fmaxf(my, fabsf(acc));
@@ -99,142 +112,95 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
   }
 }
 
-// One block (256 threads) per (b, kv head) over the raw fp16 window, in
-// chunks of 128 tokens: (1) scores, two threads per token (64 coordinates
-// each, 16-byte loads); (2) per-head max / exp / sum with warp reductions;
-// (3) values, thread = (coordinate pair, head group) streaming half2 rows.
-__global__ void __launch_bounds__(256) attn_window_kernel(const AttnArgs a) {
-  __shared__ float s_q[8][kD];
-  __shared__ float s_p[8][128];
-  __shared__ float s_mu[8], s_l[8], s_alpha[8];
-  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+// Attention partial of the G query heads of (b, h) over window chunk c
+// (tokens 32c .. 32c+31 of the raw fp16 window), 128 threads:
+// (1) scores, four threads per token (32 coordinates each);
+// (2) per-head max / exp / sum, one warp per head, lane = token;
+// (3) values, thread = coordinate.
+__device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float (*s_q)[kD], float (*s_p)[kWinChunk]) {
+  const int b = (int)(unit / a.H), h = (int)(unit % a.H);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
-  const int wl = a.wlen[b];
-  for (int i = tid; i < G * kD; i += 256) s_q[i / kD][i % kD] = __half2float(a.q[((int64_t)b * a.Hq + h * G) * kD + i]);
-  if (tid < G) {
-    s_mu[tid] = -INFINITY;
-    s_l[tid] = 0.f;
-  }
-  const int cpair = tid & 63, hg = tid >> 6;  // value phase: coordinates 2*cpair, 2*cpair+1; heads hg, hg+4
-  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  int wl = a.win_lens ? a.win_lens[b] : 0;  // clamped here as in prep_lengths (which reports)
+  wl = wl < 0 ? 0 : (wl > a.window ? a.window : wl);
+  const int t0 = c * kWinChunk;
+  const int n = min(kWinChunk, wl - t0);
+  if (n <= 0) return;  // block-uniform
+  for (int i = tid; i < G * kD; i += blockDim.x) s_q[i / kD][i % kD] = __half2float(a.q[((int64_t)b * a.Hq + h * G) * kD + i]);
   __syncthreads();
-  const float sscale = kLog2e * 0.08838834764831845f;  // log2(e)/sqrt(d)
-  const __half *kbase = a.k_win + ((int64_t)b * a.H + h) * a.window * kD;
-  const __half *vbase = a.v_win + ((int64_t)b * a.H + h) * a.window * kD;
-  for (int c0 = 0; c0 < wl; c0 += 128) {
-    const int n = min(128, wl - c0);
-    {  // (1) scores
-      const int i = tid >> 1, half = tid & 1;
-      float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (i < n) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(kbase + (int64_t)(c0 + i) * kD + 64 * half);
-        uint4 raw[8];
+  const __half *kbase = a.k_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
+  const __half *vbase = a.v_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
+  {  // (1) scores
+    const int i = tid >> 2, part = tid & 3;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (i < n) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(kbase + (int64_t)i * kD + 32 * part);
+      uint4 raw[4];
 #pragma unroll
-        for (int k = 0; k < 8; k++) raw[k] = src[k];
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-          const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-#pragma unroll
-          for (int e = 0; e < 4; e++) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-            const int c = 64 * half + 8 * k + 2 * e;
-#pragma unroll
-            for (int g = 0; g < 8; g++)
-              if (g < G) part[g] = fmaf(f.x, s_q[g][c], fmaf(f.y, s_q[g][c + 1], part[g]));
-          }
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < 8; g++) {
-        const float tot = part[g] + __shfl_xor_sync(0xffffffffu, part[g], 1);
-        if (g < G && half == 0 && i < n) s_p[g][i] = tot * sscale;
-      }
-    }
-    __syncthreads();
-    for (int g = warp; g < G; g += 8) {  // (2) softmax statistics, one warp per head
-      float v[4], m = -INFINITY;
+      for (int k = 0; k < 4; k++) raw[k] = src[k];
 #pragma unroll
       for (int k = 0; k < 4; k++) {
-        const int i = lane + 32 * k;
-        v[k] = i < n ? s_p[g][i] : -INFINITY;
-        m = fmaxf(m, v[k]);
-      }
-      m = warp_max_xor(m, 31);
-      const float mnew = fmaxf(s_mu[g], m);
-      float sum = 0.f;
+        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        const int i = lane + 32 * k;
-        const float p = i < n ? exp2f(v[k] - mnew) : 0.f;
-        if (i < n) s_p[g][i] = p;
-        sum += p;
-      }
-      sum = warp_sum_xor(sum, 31);
-      if (lane == 0) {
-        const float alpha = exp2f(s_mu[g] - mnew);
-        s_alpha[g] = alpha;
-        s_l[g] = s_l[g] * alpha + sum;
-        s_mu[g] = mnew;
-      }
-    }
-    __syncthreads();
-    {  // (3) values
+        for (int e = 0; e < 4; e++) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+          const int cc = 32 * part + 8 * k + 2 * e;
 #pragma unroll
-      for (int gi = 0; gi < 2; gi++) {
-        const int g = hg + 4 * gi;
-        if (g < G) {
-          acc[gi][0] *= s_alpha[g];
-          acc[gi][1] *= s_alpha[g];
-        }
-      }
-      const __half2 *vrow = reinterpret_cast<const __half2 *>(vbase + (int64_t)c0 * kD) + cpair;
-      int i = 0;
-      for (; i + 8 <= n; i += 8) {
-        __half2 vv[8];
-#pragma unroll
-        for (int k = 0; k < 8; k++) vv[k] = vrow[(i + k) * (kD / 2)];
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-          const float2 f = __half22float2(vv[k]);
-#pragma unroll
-          for (int gi = 0; gi < 2; gi++) {
-            const int g = hg + 4 * gi;
-            if (g < G) {
-              const float p = s_p[g][i + k];
-              acc[gi][0] = fmaf(p, f.x, acc[gi][0]);
-              acc[gi][1] = fmaf(p, f.y, acc[gi][1]);
-            }
-          }
-        }
-      }
-      for (; i < n; i++) {
-        const float2 f = __half22float2(vrow[i * (kD / 2)]);
-#pragma unroll
-        for (int gi = 0; gi < 2; gi++) {
-          const int g = hg + 4 * gi;
-          if (g < G) {
-            const float p = s_p[g][i];
-            acc[gi][0] = fmaf(p, f.x, acc[gi][0]);
-            acc[gi][1] = fmaf(p, f.y, acc[gi][1]);
-          }
+          for (int g = 0; g < 8; g++)
+            if (g < G) acc[g] = fmaf(f.x, s_q[g][cc], fmaf(f.y, s_q[g][cc + 1], acc[g]));
         }
       }
     }
-    __syncthreads();
-  }
+    const float sscale = kLog2e * 0.08838834764831845f;  // log2(e)/sqrt(d)
 #pragma unroll
-  for (int gi = 0; gi < 2; gi++) {
-    const int g = hg + 4 * gi;
-    if (g < G) {
-      const int64_t row = (int64_t)b * a.Hq + h * G + g;
-      if (cpair == 0) {
-        a.win_ml[row * 2] = s_mu[g];
-        a.win_ml[row * 2 + 1] = s_l[g];
-      }
-      *reinterpret_cast<float2 *>(a.win_acc + row * kD + 2 * cpair) = make_float2(acc[gi][0], acc[gi][1]);
+    for (int g = 0; g < 8; g++) {
+      float v = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (g < G && part == 0 && i < n) s_p[g][i] = v * sscale;
     }
   }
+  __syncthreads();
+  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
+  for (int g = warp; g < G; g += 4) {  // (2) softmax statistics of the chunk
+    const float v = lane < n ? s_p[g][lane] : -INFINITY;
+    const float m = warp_max_xor(v, 31);
+    const float p = lane < n ? exp2f(v - m) : 0.f;
+    s_p[g][lane] = p;
+    const float l = warp_sum_xor(p, 31);
+    if (lane == 0) {
+      const int64_t part = ((int64_t)b * a.Hq + h * G + g) * nch + c;
+      a.win_ml[part * 2] = m;
+      a.win_ml[part * 2 + 1] = l;
+    }
+  }
+  __syncthreads();
+  {  // (3) values
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < n; i++) {
+      const float v = __half2float(vbase[(int64_t)i * kD + tid]);
+#pragma unroll
+      for (int g = 0; g < 8; g++)
+        if (g < G) acc[g] = fmaf(s_p[g][i], v, acc[g]);
+    }
+#pragma unroll
+    for (int g = 0; g < 8; g++)
+      if (g < G) a.win_acc[(((int64_t)b * a.Hq + h * G + g) * nch + c) * kD + tid] = acc[g];
+  }
+}
+
+__global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool qjl, int row_blocks) {
+  __shared__ float s_q[8][kD];
+  __shared__ float s_p[8][kWinChunk];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x >= row_blocks) {  // window chunk blocks
+    const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
+    const int64_t k = blockIdx.x - row_blocks;
+    prep_window(a, k / nch, (int)(k % nch), s_q, s_p);
+    return;
+  }
+  if (blockIdx.x == 0 && warp == 0) prep_lengths(a, lane);
+  const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // b * Hq + qh
+  if (row < (int64_t)a.B * a.Hq) prep_query(a, qjl, row, lane, s_q[warp]);
 }
 
 // Warp that owns tile x: largest w in [0, NW) with floor(T*w/NW) <= x.
@@ -243,8 +209,67 @@ __device__ __forceinline__ int64_t tile_owner(int64_t x, int64_t T, int64_t NW) 
   return w < NW - 1 ? w : NW - 1;
 }
 
+__device__ __forceinline__ float block_max128(float v, float *s_red) {
+  v = warp_max_xor(v, 31);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  const float r = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ float block_sum128(float v, float *s_red) {
+  v = warp_sum_xor(v, 31);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  const float r = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
+  __syncthreads();
+  return r;
+}
+
+// Online log-sum-exp merge of n partials (max, sum, accumulator column j),
+// up to 128 at a time: their (max, sum) pairs are read in parallel, the
+// accumulator columns with independent loads.
+template <class ML, class ACC>
+__device__ __forceinline__ void merge_partials(int64_t n, ML ml, ACC acc_of, float &M, float &L, float &A, float *s_w,
+                                               float *s_red) {
+  const int j = threadIdx.x;
+  for (int64_t c0 = 0; c0 < n; c0 += 128) {
+    const int64_t k = c0 + j;
+    float m = -INFINITY, l = 0.f;
+    if (k < n) {
+      const float2 v = ml(k);
+      m = v.x;
+      l = v.y;
+    }
+    const float Mn = fmaxf(M, block_max128(m, s_red));
+    if (Mn == -INFINITY) continue;  // block-uniform
+    const float w = m == -INFINITY ? 0.f : exp2f(m - Mn);
+    s_w[j] = w;
+    const float lsum = block_sum128(l * w, s_red);  // also publishes s_w
+    const float sold = exp2f(M - Mn);
+    A *= sold;
+    L = L * sold + lsum;
+    M = Mn;
+    const int cn = (int)min((int64_t)128, n - c0);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int i = 0;
+    for (; i + 4 <= cn; i += 4) {
+      a0 = fmaf(s_w[i], acc_of(c0 + i)[j], a0);
+      a1 = fmaf(s_w[i + 1], acc_of(c0 + i + 1)[j], a1);
+      a2 = fmaf(s_w[i + 2], acc_of(c0 + i + 2)[j], a2);
+      a3 = fmaf(s_w[i + 3], acc_of(c0 + i + 3)[j], a3);
+    }
+    for (; i < cn; i++) a0 = fmaf(s_w[i], acc_of(c0 + i)[j], a0);
+    A += (a0 + a1) + (a2 + a3);
+    __syncthreads();  // s_w is rewritten by the next chunk
+  }
+}
+
 __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
   __shared__ float s_x[kD];
+  __shared__ float s_w[128];
+  __shared__ float s_red[4];
   const int64_t row = blockIdx.x;  // b * Hq + qh
   const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
   const int h = qh / a.G, g = qh % a.G;
@@ -256,18 +281,15 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
     const int64_t o = a.H * a.pre[b] + h * tb;
     const int64_t w0 = tile_owner(o, T, NW), w1 = tile_owner(o + tb - 1, T, NW);
     const int64_t unit = (int64_t)b * a.H + h;
-    for (int64_t w = w0; w <= w1; w++) {
-      if (T * w / NW >= T * (w + 1) / NW) continue;  // empty range
-      const int64_t base = (w + unit) * a.G + g;
-      const float ms = a.seg_ml[base * 2], ls = a.seg_ml[base * 2 + 1];
-      const float As = a.seg_acc[base * kD + j];
-      const float mn = fmaxf(mu, ms);
-      if (mn == -INFINITY) continue;
-      const float sa = exp2f(mu - mn), sb = exp2f(ms - mn);
-      l = l * sa + ls * sb;
-      A = A * sa + As * sb;
-      mu = mn;
-    }
+    merge_partials(
+        w1 - w0 + 1,
+        [&](int64_t k) {
+          const int64_t w = w0 + k;
+          if (T * w / NW >= T * (w + 1) / NW) return make_float2(-INFINITY, 0.f);  // empty range
+          const int64_t base = (w + unit) * a.G + g;
+          return make_float2(a.seg_ml[base * 2], a.seg_ml[base * 2 + 1]);
+        },
+        [&](int64_t k) { return a.seg_acc + ((w0 + k + unit) * a.G + g) * kD; }, mu, l, A, s_w, s_red);
   }
   // inverse rotation of the rotated-domain accumulator: D_V . (H A) / d
   float x = A;
@@ -286,31 +308,24 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
   }
   x = (a.v_signs[j] ? -x : x) * (1.0f / (float)kD);
 
-  float mw = -INFINITY, lw = 0.f, Aw = 0.f;
-  if (a.window > 0 && a.wlen[b] > 0) {
-    mw = a.win_ml[row * 2];
-    lw = a.win_ml[row * 2 + 1];
-    Aw = a.win_acc[row * kD + j];
+  // window partials (raw domain): merged onto the compressed part
+  float M = mu, Lt = l, At = x;
+  if (a.window > 0) {
+    const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
+    const int wl = a.wlen[b];
+    const int64_t n = (wl + kWinChunk - 1) / kWinChunk;
+    merge_partials(
+        n, [&](int64_t k) { return make_float2(a.win_ml[(row * nch + k) * 2], a.win_ml[(row * nch + k) * 2 + 1]); },
+        [&](int64_t k) { return a.win_acc + (row * nch + k) * kD; }, M, Lt, At, s_w, s_red);
   }
-  const float M = fmaxf(mu, mw);
-  float o = 0.f;
-  if (M != -INFINITY) {
-    const float sc = exp2f(mu - M), sw = exp2f(mw - M);
-    const float den = l * sc + lw * sw;
-    o = den > 0.f ? (x * sc + Aw * sw) / den : 0.f;
-  }
-  a.out[row * kD + j] = o;
+  a.out[row * kD + j] = (M != -INFINITY && Lt > 0.f) ? At / Lt : 0.f;
 }
 
 cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
   const int64_t rows = (int64_t)a.B * a.Hq;
-  const unsigned blocks = (unsigned)((rows + 3) / 4);
-  attn_prep_kernel<<<blocks, 128, 0, st>>>(a, qjl);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_attn_window(const AttnArgs &a, cudaStream_t st) {
-  attn_window_kernel<<<(unsigned)((int64_t)a.B * a.H), 256, 0, st>>>(a);
+  const int64_t row_blocks = (rows + 3) / 4;
+  const int64_t win_blocks = a.window > 0 ? (int64_t)a.B * a.H * ((a.window + kWinChunk - 1) / kWinChunk) : 0;
+  attn_prep_kernel<<<(unsigned)(row_blocks + win_blocks), 128, 0, st>>>(a, qjl, (int)row_blocks);
   return cudaGetLastError();
 }
 

@@ -12,9 +12,11 @@
 // Per tile (16 tokens of one (b, h)) a warp runs, on the tensor cores
 // (mma.sync m16n8k16, fp16 operands, fp32 accumulation):
 //   scores[16 x 2G] = Kcodes[16 x 128] * Qrot[128 x 2G]
-//     A: centroid of each code pair from a shared-memory table (fp16 hi and lo
-//        parts, two MMAs); B: the rotated query, hi/lo split over the 2G
-//        columns, so the product is exact to ~2^-22;
+//     A: centroids of each code pair from a shared-memory table, split into
+//        fp16 hi and lo parts that fill rows g and g+8 of one MMA (8 tokens
+//        per MMA, so one 8-byte table read gives two A registers);
+//        B: the rotated query, hi/lo split over the 2G columns, so the
+//        product is exact to ~2^-22;
 //   QJL (keys): + signs[16 x 128] * (S q_rot)[128 x 2G], the +-1 operands are
 //        exact in fp16;
 //   online softmax in fp32 (log2 domain);
@@ -32,15 +34,20 @@
 
 namespace tq {
 
-template <int KB, int VB, bool QJL>
-struct TileRegs {
+// Registers of one 16-token tile, key half and value half (loaded apart so
+// that the keys of the next tile can be in flight while a tile is scored).
+template <int KB, bool QJL>
+struct KeyRegs {
   uint32_t k0[KB], k1[KB];  // key code slice t (coords 32t..32t+31) of tokens r, r+8
   float nk0, nk1;           // key norms of tokens r, r+8
   float g0, g1;             // QJL gammas
   uint32_t s0, s1;          // QJL sign word t of tokens r, r+8
+  bool ok0, ok1;            // token r / r+8 is a live compressed token
+};
+template <int VB>
+struct ValRegs {
   float nv0, nv1;           // value norms of tokens r, r+8
   uint32_t vlo[4], vhi[4];  // value code bits of coords 16r..16r+15 of tokens 2t, 2t+1, 2t+8, 2t+9
-  bool ok0, ok1;            // token r / r+8 is a live compressed token
 };
 
 // `width` bits at compile-time bit `pos` of the 64-bit (hi:lo), moved to bit
@@ -59,8 +66,8 @@ __device__ __forceinline__ uint32_t field_at(uint32_t lo, uint32_t hi, int pos, 
   return (x & mask) | base;
 }
 
-// Shared address of the key-table entry of code pair p (coordinates 32t+2p,
-// 32t+2p+1): table base | pair code << 8 | lane * 8.
+// Shared-memory offset of the key-table entry of code pair p (coordinates
+// 32t+2p, 32t+2p+1): table offset | pair code << 8 | lane * 8.
 template <int KB>
 __device__ __forceinline__ uint32_t key_addr(const uint32_t (&w)[KB], int p, uint32_t laneK) {
   if constexpr (KB == 4) {
@@ -83,18 +90,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
 // Ask the TMA engine to stage a page slab in L2 (no registers, no smem).
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -114,13 +109,13 @@ __device__ __forceinline__ void ldg_words(const uint8_t *p, uint32_t (&w)[NB]) {
   }
 }
 
-// Registers of one 16-token tile at offset o0 of a page slab; `live` is the
-// number of leading tokens of the tile that are compressed tokens (0 for a
-// page outside the pool).
-template <int KB, int VB, bool QJL>
-__device__ __forceinline__ void load_tile(const AttnArgs &a, const uint8_t *slab, int o0, int live, int r, int t,
-                                          TileRegs<KB, VB, QJL> &R) {
-  constexpr int KCB = 16 * KB, VCB = 16 * VB;
+// Key registers of the 16-token tile at offset o0 of a page slab; `live` is
+// the number of leading tokens of the tile that are compressed tokens (0 for
+// a page outside the pool).
+template <int KB, bool QJL>
+__device__ __forceinline__ void load_keys(const AttnArgs &a, const uint8_t *slab, int o0, int live, int r, int t,
+                                          KeyRegs<KB, QJL> &R) {
+  constexpr int KCB = 16 * KB;
   R.ok0 = r < live;
   R.ok1 = r + 8 < live;
   const uint8_t *kc = slab + a.k_codes_o + t * 4 * KB;
@@ -137,6 +132,13 @@ __device__ __forceinline__ void load_tile(const AttnArgs &a, const uint8_t *slab
     R.s0 = __ldg(ks + r * (kM / 32));
     R.s1 = __ldg(ks + (r + 8) * (kM / 32));
   }
+}
+
+// Value registers of the same tile.
+template <int VB>
+__device__ __forceinline__ void load_values(const AttnArgs &a, const uint8_t *slab, int o0, int r, int t,
+                                            ValRegs<VB> &R) {
+  constexpr int VCB = 16 * VB;
   const float *vn = reinterpret_cast<const float *>(slab + a.v_norm_o) + o0;
   R.nv0 = __ldg(vn + r);
   R.nv1 = __ldg(vn + r + 8);
@@ -199,9 +201,11 @@ struct TileCursor {
   }
 };
 
-// Keep two tiles of registers in flight per warp (1) or one (0).
-#ifndef TQ_TILE_DOUBLE_BUFFER
-#define TQ_TILE_DOUBLE_BUFFER 0
+// Register pipeline over tiles: 0 = load a tile, then compute it; 1 = the
+// whole next tile in flight while one is computed; 2 = the next tile's keys
+// in flight, a tile's values loaded as its keys are scored.
+#ifndef TQ_TILE_PIPELINE
+#define TQ_TILE_PIPELINE 0
 #endif
 
 // Pages of a segment staged in L2 ahead of the page being read.
@@ -209,25 +213,28 @@ struct TileCursor {
 #define TQ_L2_PREFETCH 1
 #endif
 
-// Shared-memory placement of the two centroid tables.  The value table
-// ([EV][32] 4-byte entries, 128-byte rows) starts on a 32 KB boundary and the
-// key table ([EK][32] 8-byte (hi, lo) entries, 256-byte rows) on a 64 KB
-// boundary, so an entry address is (table base | pair code << row shift |
-// lane slot) and one prmt / lop3 builds it.  The allocation covers the worst
-// alignment slack.
-constexpr uint32_t kValTableAlign = 32768, kKeyTableAlign = 65536;
-constexpr size_t kAttnSmemBytes = 196608;
+// Shared-memory placement of the two centroid tables, as offsets from the
+// start of dynamic shared memory: the value table ([EV] rows of 256 bytes,
+// lane l's 4-byte entry at 4l) at 0 and the key table ([EK] rows of 256 bytes,
+// lane l's 8-byte (hi, lo) entry at 8l) at 64 KB.  An entry offset is then
+// (table offset | pair code << 8 | lane slot), one prmt / lop3, and each lane
+// reads its own bank.
+constexpr uint32_t kValTableOff = 0, kKeyTableOff = 65536;
+template <int KB>
+constexpr size_t attn_smem_bytes() {
+  return kKeyTableOff + (size_t(1) << (2 * KB)) * 256;
+}
 
 template <int KB, int VB, bool QJL, int NT>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(const AttnArgs a) {
   constexpr int EK = 1 << (2 * KB), EV = 1 << (2 * VB);
-  static_assert(EV * 128 <= (int)kValTableAlign && EK * 256 <= (int)kKeyTableAlign, "table sizes");
+  static_assert(EV * 256 <= (int)kKeyTableOff, "table sizes");
   extern __shared__ __align__(16) uint8_t smem[];
-  const uint32_t smem_s = (uint32_t)__cvta_generic_to_shared(smem);
-  const uint32_t lutV_s = (smem_s + kValTableAlign - 1) & ~(kValTableAlign - 1);
-  const uint32_t lutK_s = (lutV_s + kValTableAlign + kKeyTableAlign - 1) & ~(kKeyTableAlign - 1);
-  uint32_t *lutV = reinterpret_cast<uint32_t *>(smem + (lutV_s - smem_s));  // [EV][32]
-  uint2 *lutK = reinterpret_cast<uint2 *>(smem + (lutK_s - smem_s));        // [EK][32] (hi, lo)
+  uint32_t *lutV = reinterpret_cast<uint32_t *>(smem + kValTableOff);  // [EV][64], lanes in the first 32
+  uint2 *lutK = reinterpret_cast<uint2 *>(smem + kKeyTableOff);        // [EK][32] (hi, lo)
+  // table reads at a byte offset from the start of dynamic shared memory
+  auto lut64 = [&](uint32_t off) { return *reinterpret_cast<const uint2 *>(smem + off); };
+  auto lut32 = [&](uint32_t off) { return *reinterpret_cast<const uint32_t *>(smem + off); };
 
   // Bank-private centroid-pair tables: lane l reads its own copy in bank l.
   for (int i = threadIdx.x; i < EK * 32; i += blockDim.x) {
@@ -239,19 +246,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
   }
   for (int i = threadIdx.x; i < EV * 32; i += blockDim.x) {
     const int e = i >> 5;
-    lutV[i] = pack_half2(__ldg(a.v_cb + (e & ((1 << VB) - 1))) * kCentScale, __ldg(a.v_cb + (e >> VB)) * kCentScale);
+    lutV[e * 64 + (i & 31)] =
+        pack_half2(__ldg(a.v_cb + (e & ((1 << VB) - 1))) * kCentScale, __ldg(a.v_cb + (e >> VB)) * kCentScale);
   }
   __syncthreads();
 
   const int lane = threadIdx.x & 31, r = lane >> 2, t = lane & 3;
-  const int64_t wg = (int64_t)blockIdx.x * kAttnWarps + (threadIdx.x >> 5);
+  const int64_t wg = (int64_t)blockIdx.x * attn_warps(NT, QJL) + (threadIdx.x >> 5);
   const int64_t T = a.hdr->total_tiles;
   const int64_t NW = a.hdr->active_warps;
   if (wg >= NW) return;
   const int64_t ts = T * wg / NW, te = T * (wg + 1) / NW;
   if (ts >= te) return;
-  const uint32_t laneK = lutK_s | ((uint32_t)lane * 8u);
-  const uint32_t laneV = lutV_s | ((uint32_t)lane * 4u);
+  const uint32_t laneK = kKeyTableOff | ((uint32_t)lane * 8u);
+  const uint32_t laneV = kValTableOff | ((uint32_t)lane * 4u);
   const int H = a.H, G = a.G, Hq = a.Hq;
   const int tpp = a.P >> 4;
   const uint32_t slab_bytes = (uint32_t)a.slab_bytes;
@@ -365,24 +373,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
     }
     cur.enter_page(a.err_word, lane == 0);
 
-    auto process = [&](const TileRegs<KB, VB, QJL> &R) {
+    auto process = [&](const KeyRegs<KB, QJL> &R, const ValRegs<VB> &V) {
       if (!__any_sync(0xffffffffu, R.ok0)) return;  // token 0 of a tile is live iff any is
-      // ---- scores: hi-part, lo-part and QJL chains run independently
-      float sk[NT][4], sl[NT][4], sq[NT][4];
+      // ---- scores: tokens 0-7, tokens 8-15 and QJL chains run independently.
+      // sa rows r / r+8 = token r hi / lo part; sb likewise for token r+8.
+      float sa[NT][4], sbk[NT][4], sq[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-        for (int i = 0; i < 4; i++) { sk[nt][i] = 0.f; sl[nt][i] = 0.f; sq[nt][i] = 0.f; }
+        for (int i = 0; i < 4; i++) { sa[nt][i] = 0.f; sbk[nt][i] = 0.f; sq[nt][i] = 0.f; }
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) {
-        const uint2 L00 = lds64(key_addr<KB>(R.k0, 2 * kk, laneK));
-        const uint2 L10 = lds64(key_addr<KB>(R.k1, 2 * kk, laneK));
-        const uint2 L01 = lds64(key_addr<KB>(R.k0, 2 * kk + 1, laneK));
-        const uint2 L11 = lds64(key_addr<KB>(R.k1, 2 * kk + 1, laneK));
+        const uint2 L00 = lut64(key_addr<KB>(R.k0, 2 * kk, laneK));
+        const uint2 L01 = lut64(key_addr<KB>(R.k0, 2 * kk + 1, laneK));
+        const uint2 L10 = lut64(key_addr<KB>(R.k1, 2 * kk, laneK));
+        const uint2 L11 = lut64(key_addr<KB>(R.k1, 2 * kk + 1, laneK));
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) {
-          mma_16816(sk[nt], L00.x, L10.x, L01.x, L11.x, qb[nt][kk][0], qb[nt][kk][1]);
-          mma_16816(sl[nt], L00.y, L10.y, L01.y, L11.y, qb[nt][kk][0], qb[nt][kk][1]);
+          mma_16816(sa[nt], L00.x, L00.y, L01.x, L01.y, qb[nt][kk][0], qb[nt][kk][1]);
+          mma_16816(sbk[nt], L10.x, L10.y, L11.x, L11.y, qb[nt][kk][0], qb[nt][kk][1]);
         }
         if constexpr (QJL) {
           const uint32_t a0 = sign_pair(R.s0, 2 * kk), a1 = sign_pair(R.s1, 2 * kk);
@@ -392,7 +401,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
         }
       }
       // ---- online softmax (log2 domain) and value weights
-      const float vn0 = R.ok0 ? R.nv0 : 0.f, vn1 = R.ok1 ? R.nv1 : 0.f;
+      const float vn0 = R.ok0 ? V.nv0 : 0.f, vn1 = R.ok1 ? V.nv1 : 0.f;
       const float tnu = warp_max_xor(fmaxf(vn0, vn1), 4 | 8 | 16);
       const float nu_new = fmaxf(nu, tnu);
       const float rcp_nu = nu_new > 0.f ? __frcp_rn(nu_new) : 0.f;
@@ -404,8 +413,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
       float beta[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; nt++) {
-        float l0 = ((sk[nt][0] + sk[nt][1]) + (sl[nt][0] + sl[nt][1])) * cK[nt];
-        float l1 = ((sk[nt][2] + sk[nt][3]) + (sl[nt][2] + sl[nt][3])) * cK[nt];
+        float l0 = ((sa[nt][0] + sa[nt][1]) + (sa[nt][2] + sa[nt][3])) * cK[nt];
+        float l1 = ((sbk[nt][0] + sbk[nt][1]) + (sbk[nt][2] + sbk[nt][3])) * cK[nt];
         if constexpr (QJL) {
           l0 = fmaf(R.g0 * (sq[nt][0] + sq[nt][1]), cQ[nt], l0);
           l1 = fmaf(R.g1 * (sq[nt][2] + sq[nt][3]), cQ[nt], l1);
@@ -445,13 +454,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
       // ---- values: interleave the codes of the token pairs (2t, 2t+1) and
       // (2t+8, 2t+9) at each coordinate; one lookup gives an A register.
       // Row r of m-tile mt is coordinate 16r+2mt, row r+8 is 16r+2mt+1.
+      // Table offset = pair code << 8 | lane * 4.
       uint32_t ev[2][2][2];  // [token pair][even/odd coordinate][word]
 #pragma unroll
       for (int tp = 0; tp < 2; tp++) {
 #pragma unroll
         for (int wi = 0; wi < 2; wi++) {
-          const uint32_t wa = wi ? R.vhi[2 * tp] : R.vlo[2 * tp];
-          const uint32_t wz = wi ? R.vhi[2 * tp + 1] : R.vlo[2 * tp + 1];
+          const uint32_t wa = wi ? V.vhi[2 * tp] : V.vlo[2 * tp];
+          const uint32_t wz = wi ? V.vhi[2 * tp + 1] : V.vlo[2 * tp + 1];
           if constexpr (VB == 4) {
             ev[tp][0][wi] = (wa & 0x0F0F0F0Fu) | ((wz << 4) & 0xF0F0F0F0u);  // byte k: coordinate 2k
             ev[tp][1][wi] = ((wa >> 4) & 0x0F0F0F0Fu) | (wz & 0xF0F0F0F0u);  // byte k: coordinate 2k+1
@@ -473,15 +483,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
           for (int eo = 0; eo < 2; eo++) {
             uint32_t addr;
             if constexpr (VB == 4) {
-              addr = field_at<7>(ev[tp][eo][mt >> 2], 0u, 8 * (mt & 3), 8, laneV);
+              addr = __byte_perm(ev[tp][eo][mt >> 2], laneV, 0x7604 | ((mt & 3) << 4));
             } else if constexpr (VB == 2) {
-              addr = field_at<7>(ev[tp][eo][0], 0u, 4 * mt, 4, laneV);
+              addr = field_at<8>(ev[tp][eo][0], 0u, 4 * mt, 4, laneV);
             } else {  // 3-bit: gather the two codes of coordinate 16r+2mt+eo
               const int p3 = 3 * (2 * mt + eo);
-              addr = field_at<7>(R.vlo[2 * tp], R.vhi[2 * tp], p3, 3, laneV) |
-                     field_at<10>(R.vlo[2 * tp + 1], R.vhi[2 * tp + 1], p3, 3, 0u);
+              addr = field_at<8>(V.vlo[2 * tp], V.vhi[2 * tp], p3, 3, laneV) |
+                     field_at<11>(V.vlo[2 * tp + 1], V.vhi[2 * tp + 1], p3, 3, 0u);
             }
-            av[2 * tp + eo] = lds32(addr);
+            av[2 * tp + eo] = lut32(addr);
           }
         }
 #pragma unroll
@@ -500,27 +510,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
       }
     };
 
-#if TQ_TILE_DOUBLE_BUFFER
+    using KR = KeyRegs<KB, QJL>;
+    using VR = ValRegs<VB>;
+    auto keys = [&](KR &R) { load_keys<KB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, R); };
+    auto vals = [&](VR &R) { load_values<VB>(a, cur.slab, cur.o0, r, t, R); };
+#if TQ_TILE_PIPELINE == 2
+    // keys one tile ahead (ping-pong ka / kb), values at the tile itself
+    KR ka, kb;
+    VR v;
+    keys(ka);
+    for (int k = 0;;) {
+      vals(v);
+      if (k + 1 < seg_tiles) {
+        step_cursor();
+        keys(kb);
+      }
+      process(ka, v);
+      if (++k == seg_tiles) break;
+      vals(v);
+      if (k + 1 < seg_tiles) {
+        step_cursor();
+        keys(ka);
+      }
+      process(kb, v);
+      if (++k == seg_tiles) break;
+    }
+#elif TQ_TILE_PIPELINE == 1
     // the next tile's loads are in flight while this one is computed
-    TileRegs<KB, VB, QJL> ra, rb;
-    load_tile<KB, VB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, ra);
+    KR ka, kb;
+    VR va, vb;
+    keys(ka);
+    vals(va);
     int k = 0;
     for (; k + 2 <= seg_tiles; k += 2) {
       step_cursor();
-      load_tile<KB, VB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, rb);
-      process(ra);
+      keys(kb);
+      vals(vb);
+      process(ka, va);
       if (k + 2 < seg_tiles) {
         step_cursor();
-        load_tile<KB, VB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, ra);
+        keys(ka);
+        vals(va);
       }
-      process(rb);
+      process(kb, vb);
     }
-    if (k < seg_tiles) process(ra);
+    if (k < seg_tiles) process(ka, va);
 #else
     for (int k = 0; k < seg_tiles; k++) {
-      TileRegs<KB, VB, QJL> ra;
-      load_tile<KB, VB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, ra);
-      process(ra);
+      KR ka;
+      VR va;
+      keys(ka);
+      vals(va);
+      process(ka, va);
       if (k + 1 < seg_tiles) step_cursor();
     }
 #endif
@@ -565,11 +606,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_main_kernel(const AttnAr
 template <int KB, int VB, bool QJL, int NT>
 cudaError_t attn_main_launch_t(const AttnArgs &a, bool query_only, int *blocks_per_sm, int blocks, cudaStream_t st) {
   auto kern = attn_main_kernel<KB, VB, QJL, NT>;
+  constexpr size_t smem_bytes = attn_smem_bytes<KB>();
   static unsigned long long done = 0;
-  cudaError_t e = set_smem_once(kern, (int)kAttnSmemBytes, done);
+  cudaError_t e = set_smem_once(kern, (int)smem_bytes, done);
   if (e != cudaSuccess) return e;
-  if (query_only) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kern, kAttnThreads, kAttnSmemBytes);
-  kern<<<blocks, kAttnThreads, kAttnSmemBytes, st>>>(a);
+  if (query_only) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kern, attn_threads(NT, QJL), smem_bytes);
+  kern<<<blocks, attn_threads(NT, QJL), smem_bytes, st>>>(a);
   return cudaGetLastError();
 }
 

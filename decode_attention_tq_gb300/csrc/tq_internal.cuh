@@ -72,8 +72,8 @@ struct AttnArgs {
   int32_t *q_exp;    // [B][Hq][2] power-of-two exponents for the fp16 operands
   float *seg_ml;     // [slots][G][2]  (max in log2 units, sum)
   float *seg_acc;    // [slots][G][d]  rotated-domain value accumulator
-  float *win_ml;     // [B][Hq][2]
-  float *win_acc;    // [B][Hq][d]
+  float *win_ml;     // [B][Hq][window chunks][2]
+  float *win_acc;    // [B][Hq][window chunks][d]  raw-domain window accumulators
   int nw_launch;     // warps launched for the main kernel
   int min_tiles;     // fewest tiles a warp is given
 };
@@ -82,8 +82,8 @@ cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, int sms, cuda
 cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
 
 // Decode attention pieces (tq_attn_aux.cu and tq_attn_k*.cu).
+constexpr int kWinChunk = 32;  // window tokens per window partial
 cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st);
-cudaError_t launch_attn_window(const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_attn_merge(const AttnArgs &a, cudaStream_t st);
 // Main split-KV kernel: returns its per-SM occupancy through *blocks_per_sm
 // when `query_only`, else launches `blocks` CTAs.
@@ -108,11 +108,22 @@ cudaError_t set_smem_once(K kernel, int bytes, unsigned long long &done_mask) {
   return e;
 }
 
-// Threads per CTA of the main attention kernel (one CTA per SM).
+// Threads per CTA of the main attention kernel (one CTA per SM), by the
+// number of 8-column n-tiles (NT = 1 for up to 4 query heads per kv head, 2
+// for up to 8) and QJL: the register file is shared out as 65536 / threads,
+// and the NT = 2 accumulators (and QJL operands) need more per thread.
 #ifndef TQ_ATTN_THREADS
 #define TQ_ATTN_THREADS 512
 #endif
-constexpr int kAttnThreads = TQ_ATTN_THREADS;
-constexpr int kAttnWarps = kAttnThreads / 32;
+#ifndef TQ_ATTN_THREADS_NT2
+#define TQ_ATTN_THREADS_NT2 384
+#endif
+#ifndef TQ_ATTN_THREADS_NT2_QJL
+#define TQ_ATTN_THREADS_NT2_QJL 256
+#endif
+__host__ __device__ constexpr int attn_threads(int nt, bool qjl) {
+  return nt == 1 ? TQ_ATTN_THREADS : (qjl ? TQ_ATTN_THREADS_NT2_QJL : TQ_ATTN_THREADS_NT2);
+}
+__host__ __device__ constexpr int attn_warps(int nt, bool qjl) { return attn_threads(nt, qjl) / 32; }
 
 }  // namespace tq
