@@ -15,12 +15,12 @@ namespace {
 bool format_valid(const tq_format *f) {
   if (!f) return false;
   const int d = f->head_dim;
-  if (d < 2 || (d & (d - 1))) return false;
+  if (d < 16 || (d & (d - 1))) return false;
   if (f->k_bits < 1 || f->k_bits > 8 || f->v_bits < 1 || f->v_bits > 8) return false;
   if ((d * f->k_bits) % 8 || (d * f->v_bits) % 8) return false;
   if (f->k_qjl != 0 && f->k_qjl != 1) return false;
   if (f->k_qjl && (f->qjl_m < 8 || f->qjl_m % 8)) return false;
-  if (f->page_size < 1 || f->num_kv_heads < 1) return false;
+  if (f->page_size < 16 || f->page_size % 16 || f->num_kv_heads < 1) return false;
   return true;
 }
 
@@ -255,6 +255,7 @@ tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n
   a.gamma_off = L.k_gamma;
   a.signs_off = L.k_signs;
   a.code_bytes = kind == TQ_KIND_K ? L.k_code_bytes : L.v_code_bytes;
+  a.grouped = kind == TQ_KIND_V;
   a.signs = signs;
   a.codebook = codebook;
   a.S = S;
@@ -291,6 +292,7 @@ tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64
   a.gamma_off = L.k_gamma;
   a.signs_off = L.k_signs;
   a.code_bytes = kind == TQ_KIND_K ? L.k_code_bytes : L.v_code_bytes;
+  a.grouped = kind == TQ_KIND_V;
   a.signs = signs;
   a.codebook = codebook;
   a.S = S;

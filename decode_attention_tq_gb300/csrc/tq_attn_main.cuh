@@ -142,27 +142,25 @@ __device__ __forceinline__ void load_values(const AttnArgs &a, const uint8_t *sl
   const float *vn = reinterpret_cast<const float *>(slab + a.v_norm_o) + o0;
   R.nv0 = __ldg(vn + r);
   R.nv1 = __ldg(vn + r + 8);
-  const uint8_t *vc = slab + a.v_codes_o;
-  const int vt[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+  // chunk r (coordinates 16r..16r+15) of tokens 2t, 2t+1, 2t+8, 2t+9: one
+  // contiguous run of 4 * 2VB bytes in the grouped value-code section
+  const uint8_t *vc = slab + a.v_codes_o + (int64_t)o0 * VCB + r * (16 * 2 * VB) + t * (4 * 2 * VB);
+  if constexpr (VB == 4) {
+    const uint4 x0 = __ldg(reinterpret_cast<const uint4 *>(vc)), x1 = __ldg(reinterpret_cast<const uint4 *>(vc) + 1);
+    R.vlo[0] = x0.x; R.vhi[0] = x0.y; R.vlo[1] = x0.z; R.vhi[1] = x0.w;
+    R.vlo[2] = x1.x; R.vhi[2] = x1.y; R.vlo[3] = x1.z; R.vhi[3] = x1.w;
+  } else if constexpr (VB == 2) {
+    const uint4 x0 = __ldg(reinterpret_cast<const uint4 *>(vc));
+    R.vlo[0] = x0.x; R.vlo[1] = x0.y; R.vlo[2] = x0.z; R.vlo[3] = x0.w;
 #pragma unroll
-  for (int i = 0; i < 4; i++) {
-    const uint8_t *row = vc + (o0 + vt[i]) * VCB;
-    if constexpr (VB == 4) {
-      const uint2 v = __ldg(reinterpret_cast<const uint2 *>(row + 8 * r));
-      R.vlo[i] = v.x;
-      R.vhi[i] = v.y;
-    } else if constexpr (VB == 2) {
-      R.vlo[i] = __ldg(reinterpret_cast<const uint32_t *>(row + 4 * r));
-      R.vhi[i] = 0u;
-    } else {
-      // 48 bits starting at byte 6r: two aligned words, then shift by 0 or 16
-      const int w0 = (6 * r) >> 2;
-      const uint32_t x0 = __ldg(reinterpret_cast<const uint32_t *>(row) + w0);
-      const uint32_t x1 = __ldg(reinterpret_cast<const uint32_t *>(row) + w0 + 1);
-      const int sh = ((6 * r) & 3) * 8;
-      R.vlo[i] = __funnelshift_r(x0, x1, sh);
-      R.vhi[i] = x1 >> sh;
-    }
+    for (int i = 0; i < 4; i++) R.vhi[i] = 0u;
+  } else {  // four 6-byte chunks in 24 bytes (8-byte aligned)
+    const uint2 x0 = __ldg(reinterpret_cast<const uint2 *>(vc)), x1 = __ldg(reinterpret_cast<const uint2 *>(vc) + 1),
+                x2 = __ldg(reinterpret_cast<const uint2 *>(vc) + 2);
+    R.vlo[0] = x0.x;                                  R.vhi[0] = x0.y & 0xFFFFu;
+    R.vlo[1] = __byte_perm(x0.y, x1.x, 0x5432);       R.vhi[1] = x1.x >> 16;
+    R.vlo[2] = x1.y;                                  R.vhi[2] = x2.x & 0xFFFFu;
+    R.vlo[3] = __byte_perm(x2.x, x2.y, 0x5432);       R.vhi[3] = x2.y >> 16;
   }
 }
 

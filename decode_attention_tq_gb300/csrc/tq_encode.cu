@@ -49,6 +49,47 @@ __device__ __forceinline__ void store_codes(uint8_t *p, const uint32_t (&w)[BITS
   }
 }
 
+// The same 4*BITS bytes (chunks 2q and 2q+1 of a token) in a grouped
+// value-code section (value_chunk_offset).
+template <int BITS>
+__device__ __forceinline__ void store_codes_grouped(uint8_t *sec, int64_t off, int q, const uint32_t (&w)[BITS]) {
+  uint8_t *c0 = sec + value_chunk_offset(off, 2 * q, BITS);
+  uint8_t *c1 = sec + value_chunk_offset(off, 2 * q + 1, BITS);
+  if constexpr (BITS == 4) {
+    *reinterpret_cast<uint2 *>(c0) = make_uint2(w[0], w[1]);
+    *reinterpret_cast<uint2 *>(c1) = make_uint2(w[2], w[3]);
+  } else if constexpr (BITS == 2) {
+    *reinterpret_cast<uint32_t *>(c0) = w[0];
+    *reinterpret_cast<uint32_t *>(c1) = w[1];
+  } else {  // 6-byte chunks on 2-byte boundaries
+    uint16_t *h0 = reinterpret_cast<uint16_t *>(c0), *h1 = reinterpret_cast<uint16_t *>(c1);
+    h0[0] = (uint16_t)w[0];
+    h0[1] = (uint16_t)(w[0] >> 16);
+    h0[2] = (uint16_t)w[1];
+    h1[0] = (uint16_t)(w[1] >> 16);
+    h1[1] = (uint16_t)w[2];
+    h1[2] = (uint16_t)(w[2] >> 16);
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ void load_codes_grouped(const uint8_t *sec, int64_t off, int q, uint32_t (&w)[BITS]) {
+  const uint8_t *c0 = sec + value_chunk_offset(off, 2 * q, BITS);
+  const uint8_t *c1 = sec + value_chunk_offset(off, 2 * q + 1, BITS);
+  if constexpr (BITS == 4) {
+    const uint2 x = *reinterpret_cast<const uint2 *>(c0), y = *reinterpret_cast<const uint2 *>(c1);
+    w[0] = x.x; w[1] = x.y; w[2] = y.x; w[3] = y.y;
+  } else if constexpr (BITS == 2) {
+    w[0] = *reinterpret_cast<const uint32_t *>(c0);
+    w[1] = *reinterpret_cast<const uint32_t *>(c1);
+  } else {
+    const uint16_t *h0 = reinterpret_cast<const uint16_t *>(c0), *h1 = reinterpret_cast<const uint16_t *>(c1);
+    w[0] = (uint32_t)h0[0] | ((uint32_t)h0[1] << 16);
+    w[1] = (uint32_t)h0[2] | ((uint32_t)h1[0] << 16);
+    w[2] = (uint32_t)h1[1] | ((uint32_t)h1[2] << 16);
+  }
+}
+
 template <int BITS>
 __device__ __forceinline__ void load_codes(const uint8_t *p, uint32_t (&w)[BITS]) {
   if constexpr (BITS == 4) {
@@ -160,7 +201,10 @@ __global__ void __launch_bounds__(256) encode_kernel(const EncodeArgs a) {
     const int64_t off = ok ? slot % a.P : 0;
     uint8_t *slab = a.pool + page * a.page_bytes + (int64_t)h * a.slab_bytes;
     if (ok) {
-      store_codes<BITS>(slab + a.codes_off + off * a.code_bytes + q * 4 * BITS, w);
+      if (a.grouped)
+        store_codes_grouped<BITS>(slab + a.codes_off, off, q, w);
+      else
+        store_codes<BITS>(slab + a.codes_off + off * a.code_bytes + q * 4 * BITS, w);
       if (q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nrm;
     }
 
@@ -268,7 +312,10 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
     const uint8_t *slab = a.pool + page * a.page_bytes + (int64_t)h * a.slab_bytes;
 
     uint32_t w[BITS];
-    load_codes<BITS>(slab + a.codes_off + off * a.code_bytes + q * 4 * BITS, w);
+    if (a.grouped)
+      load_codes_grouped<BITS>(slab + a.codes_off, off, q, w);
+    else
+      load_codes<BITS>(slab + a.codes_off + off * a.code_bytes + q * 4 * BITS, w);
     const float nrm = reinterpret_cast<const float *>(slab + a.norm_off)[off];
     int idx[32];
     unpack_codes<BITS>(w, idx);

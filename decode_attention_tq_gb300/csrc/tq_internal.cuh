@@ -17,6 +17,7 @@ struct EncodeArgs {
   int64_t num_pages, page_bytes, slab_bytes;
   int64_t norm_off, codes_off, gamma_off, signs_off;
   int code_bytes;
+  bool grouped;  // value-code stream: 16-token groups, chunk-major (value_chunk_offset)
   const uint8_t *signs;
   const float *codebook;
   const float *S;
@@ -31,12 +32,26 @@ struct DecodeArgs {
   int64_t num_pages, page_bytes, slab_bytes;
   int64_t norm_off, codes_off, gamma_off, signs_off;
   int code_bytes;
+  bool grouped;
   const uint8_t *signs;
   const float *codebook;
   const float *S;
   float *out;
   int32_t *err_word;
 };
+
+// The value-code section keeps each token's LSB-first bitstream in chunks of
+// 16 coordinates (2*bits bytes) and stores a group of 16 tokens chunk by
+// chunk; inside a chunk row the tokens of the group sit in the order
+// 0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15, so that one thread of the
+// attention kernel finds chunk r of the tokens it multiplies (2t, 2t+1,
+// 2t+8, 2t+9) in one contiguous run.  Offset of chunk r of the token at page
+// offset `off`, from the start of the section:
+__host__ __device__ __forceinline__ int64_t value_chunk_offset(int64_t off, int r, int bits) {
+  const int i = (int)(off & 15);
+  const int slot = 4 * ((i & 7) >> 1) + 2 * (i >> 3) + (i & 1);
+  return (off >> 4) * (2 * kD * bits) + (int64_t)r * (16 * 2 * bits) + slot * (2 * bits);  // group = 16 * kD * bits / 8 bytes
+}
 
 // Workspace header written by the prep kernel and read by the others.
 struct AttnHeader {

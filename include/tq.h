@@ -22,9 +22,10 @@
  *
  * Format (tq_format): d = head_dim, b_K / b_V = bits per coordinate of the
  * Lloyd-Max codes, optional 1-bit QJL residual sketch of length m on keys,
- * P = page_size tokens per page, H = num_kv_heads.  The GPU kernels support
- * d = 128, b in {2, 3, 4}, m = 128, P a multiple of 16; other shapes return
- * TQ_ERR_UNSUPPORTED.
+ * P = page_size tokens per page, H = num_kv_heads.  A valid format has d a
+ * power of two and a multiple of 16 and P a multiple of 16 (pages hold whole
+ * 16-token groups).  The GPU kernels support d = 128, b in {2, 3, 4},
+ * m = 128; other valid shapes return TQ_ERR_UNSUPPORTED.
  */
 #ifndef TQ_H_
 #define TQ_H_
@@ -70,8 +71,18 @@ typedef struct {
  * "TurboQuant Family Design Study for CPU and Browser WASM KV Caches",
  * section 'Packed format and complete bit accounting': K norms fp32 [P],
  * K QJL gammas fp32 [P] (QJL only), K codes [P][d*b_K/8], K sign bits
- * [P][m/8] (QJL only), V norms fp32 [P], V codes [P][d*b_V/8].  Codes are an
- * LSB-first bitstream (code j at bits [j*b, j*b+b)); sign bit l is bit l. */
+ * [P][m/8] (QJL only), V norms fp32 [P], V codes (P*d*b_V/8 bytes, grouped
+ * as below).  Codes are an LSB-first bitstream per token (code j at bits
+ * [j*b, j*b+b)); sign bit l is bit l.  Token t of a page is at offset t of
+ * every per-token section, except in the V codes section: there each token's
+ * bitstream is cut into d/16 chunks of 16 coordinates (2*b_V bytes), and a
+ * group of 16 tokens (offsets 16g .. 16g+15) is stored chunk by chunk: chunk r
+ * of the token at offset 16g+i sits at byte
+ *   g*16*(d*b_V/8) + r*16*(2*b_V) + s(i)*(2*b_V),
+ *   s(i) = 4*((i mod 8) div 2) + 2*(i div 8) + (i mod 2)
+ * (tokens in the order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15), so that the
+ * attention kernel reads chunk r of the four tokens one thread multiplies in
+ * one contiguous load. */
 typedef struct {
   int64_t slab_bytes, page_bytes;
   int64_t k_norm, k_gamma, k_codes, k_signs, v_norm, v_codes;

@@ -47,6 +47,11 @@
  *   - A zero vector stores n = 0, gamma = 0 and all codes / bits 0.
  *   - Bitstreams are LSB-first: code j occupies bits [j*b, j*b+b), sign l is
  *     bit l; byte k of the stream holds stream bits [8k, 8k+8).
+ *   - Page body: the passage's section order, each section 16-byte aligned,
+ *     pages of a multiple of 16 tokens and d a multiple of 16.  The value
+ *     code stream keeps each token's bitstream whole in 16-coordinate chunks
+ *     (2*b bytes) but stores a group of 16 tokens chunk by chunk, tokens in
+ *     the order 0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15 (v_chunk_pos).
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared oracle.c -lm   (no fast-math)
  */
@@ -309,16 +314,39 @@ void orc_unpack_bits(int count, int b, const uint8_t *in, int32_t *vals) {
 static int64_t align16(int64_t x) { return (x + 15) / 16 * 16; }
 
 /*
+ * Byte position, inside the value-code section, of chunk r (coordinates
+ * 16r .. 16r+15, i.e. bytes 2*vb*r .. 2*vb*r + 2*vb - 1 of the token's
+ * bitstream) of the token at page offset `off`: groups of 16 tokens, inside a
+ * group chunk-major, token i at slot 4*((i mod 8) div 2) + 2*(i div 8) + (i mod 2).
+ */
+static int64_t v_chunk_pos(int64_t off, int r, int d, int vb) {
+  int64_t grp = off / 16;
+  int i = (int)(off % 16);
+  int slot = 4 * ((i % 8) / 2) + 2 * (i / 8) + (i % 2);
+  int64_t token_bytes = (int64_t)d * vb / 8, chunk_bytes = 2 * vb;
+  return grp * 16 * token_bytes + (int64_t)r * 16 * chunk_bytes + (int64_t)slot * chunk_bytes;
+}
+
+static void put_v_codes(uint8_t *section, int64_t off, int d, int vb, const uint8_t *stream) {
+  for (int r = 0; r < d / 16; r++) memcpy(section + v_chunk_pos(off, r, d, vb), stream + 2 * vb * r, (size_t)(2 * vb));
+}
+
+static void get_v_codes(const uint8_t *section, int64_t off, int d, int vb, uint8_t *stream) {
+  for (int r = 0; r < d / 16; r++) memcpy(stream + 2 * vb * r, section + v_chunk_pos(off, r, d, vb), (size_t)(2 * vb));
+}
+
+/*
  * One pool per layer: [num_pages][num_kv_heads] head-slabs.  Inside a slab,
  * the section order of the packed-format passage: K norms (fp32 [P]),
  * K QJL gammas (fp32 [P], QJL only), K codes ([P][d*kb/8]), K sign bits
- * ([P][m/8], QJL only), V norms (fp32 [P]), V codes ([P][d*vb/8]); every
- * section starts on a 16-byte boundary and the slab is padded to 16 bytes.
+ * ([P][m/8], QJL only), V norms (fp32 [P]), V codes (P*d*vb/8 bytes in
+ * 16-token groups, see v_chunk_pos); every section starts on a 16-byte
+ * boundary and the slab is padded to 16 bytes.  P and d are multiples of 16.
  */
 int orc_page_layout(const orc_format *f, orc_layout *L) {
   if (!f || !L) return ORC_ERR_ARG;
-  if (!is_pow2(f->head_dim) || f->k_bits < 1 || f->k_bits > 8 || f->v_bits < 1 || f->v_bits > 8 ||
-      f->page_size < 1 || f->num_kv_heads < 1)
+  if (!is_pow2(f->head_dim) || f->head_dim % 16 || f->k_bits < 1 || f->k_bits > 8 || f->v_bits < 1 ||
+      f->v_bits > 8 || f->page_size < 16 || f->page_size % 16 || f->num_kv_heads < 1)
     return ORC_ERR_ARG;
   if ((f->head_dim * f->k_bits) % 8 || (f->head_dim * f->v_bits) % 8) return ORC_ERR_ARG;
   if (f->k_qjl && (f->qjl_m < 8 || f->qjl_m % 8)) return ORC_ERR_ARG;
@@ -372,6 +400,7 @@ int orc_encode(const orc_format *f, int kind, const uint16_t *x, int64_t N, cons
   int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * d);
   uint8_t *z = (uint8_t *)malloc((size_t)(m > 0 ? m : 1));
   int32_t *zi = (int32_t *)malloc(sizeof(int32_t) * (m > 0 ? m : 1));
+  uint8_t *stream = (uint8_t *)malloc((size_t)code_bytes);
   int rc = ORC_OK;
   for (int64_t n = 0; n < N; n++) {
     int64_t slot = slot_mapping[n];
@@ -400,10 +429,12 @@ int orc_encode(const orc_format *f, int kind, const uint16_t *x, int64_t N, cons
         }
       } else {
         put_f32(slab + L.v_norm + 4 * off, (float)norm);
-        orc_pack_bits(d, bits, idx, slab + L.v_codes + off * code_bytes);
+        orc_pack_bits(d, bits, idx, stream);
+        put_v_codes(slab + L.v_codes, off, d, bits, stream);
       }
     }
   }
+  free(stream);
   free(xv);
   free(idx);
   free(z);
@@ -431,7 +462,9 @@ static void decode_slot(const orc_format *f, const orc_layout *L, int kind, cons
     orc_decode_vector(d, f->k_bits, qjl, m, norm, gamma, idx, z, signs, centroids, S, out);
   } else {
     double norm = get_f32(slab + L->v_norm + 4 * off);
-    orc_unpack_bits(d, f->v_bits, slab + L->v_codes + off * L->v_code_bytes, idx);
+    uint8_t stream[L->v_code_bytes];
+    get_v_codes(slab + L->v_codes, off, d, f->v_bits, stream);
+    orc_unpack_bits(d, f->v_bits, stream, idx);
     orc_decode_vector(d, f->v_bits, 0, 0, norm, 0.0, idx, NULL, signs, centroids, NULL, out);
   }
 }

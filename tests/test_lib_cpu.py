@@ -46,7 +46,7 @@ def test_codebook_equals_oracle(lib, bits):
 
 
 @pytest.mark.parametrize("fmt", [ti.Format(128, b, v, q, 128, P, H) for b in (2, 3, 4) for v in (2, 4) for q in (0, 1) for P in (16, 64, 128)
-                                 for H in (1, 8)] + [ti.Format(64, 3, 5, 1, 24, 7, 3), ti.Format(8, 1, 2, 0, 8, 3, 1)])
+                                 for H in (1, 8)] + [ti.Format(64, 3, 5, 1, 24, 48, 3), ti.Format(16, 1, 2, 0, 8, 16, 1)])
 def test_layout_equals_oracle(lib, fmt):
     from decode_attention_tq_gb300 import tq_page_layout
 
@@ -79,7 +79,9 @@ def test_host_validation_before_any_launch(lib):
     # a valid format the kernels do not implement
     assert lib.tq_encode(C.byref(_F(head_dim=64)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 2
     assert lib.tq_encode(C.byref(_F(k_bits=5)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 2
-    assert lib.tq_encode(C.byref(_F(page_size=24)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 2
+    assert lib.tq_encode(C.byref(_F(qjl_m=64, k_qjl=1)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, dummy, None, None) == 2
+    # pages are whole 16-token groups
+    assert lib.tq_encode(C.byref(_F(page_size=24)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
     # bad kind, negative count, missing S for QJL keys, misaligned input
     assert lib.tq_encode(C.byref(f), 2, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
     assert lib.tq_encode(C.byref(f), 0, dummy, -1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1

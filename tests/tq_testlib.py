@@ -15,6 +15,20 @@ REL_ATTN = 2e-3   # attention outputs: max |o - o_ref| / max |o_ref| per (b, q h
 REL_NORM = 1e-6   # stored fp32 norms and gammas
 
 
+def value_chunk_pos(off: int, r: int, d: int, vb: int) -> int:
+    """Byte position in the value-code section of chunk r (coordinates
+    16r..16r+15) of the token at page offset `off`: 16-token groups stored
+    chunk by chunk, tokens in the order 0,1,8,9,2,3,10,11,..."""
+    g, i = divmod(off, 16)
+    slot = 4 * ((i % 8) // 2) + 2 * (i // 8) + (i % 2)
+    return g * 16 * (d * vb // 8) + r * 16 * (2 * vb) + slot * (2 * vb)
+
+
+def value_code_bytes(section: np.ndarray, off: int, d: int, vb: int) -> np.ndarray:
+    """The token's LSB-first code bitstream, gathered from a grouped section."""
+    return np.concatenate([section[value_chunk_pos(off, r, d, vb): value_chunk_pos(off, r, d, vb) + 2 * vb] for r in range(d // 16)])
+
+
 def unpack_field(pool: np.ndarray, lay: dict, fmt, kind: int, slots: np.ndarray):
     """Fields of the given slots (all heads): norm, gamma, codes [.., d], signs [.., m]."""
     P, H, d = fmt.page_size, fmt.num_kv_heads, fmt.head_dim
@@ -34,7 +48,10 @@ def unpack_field(pool: np.ndarray, lay: dict, fmt, kind: int, slots: np.ndarray)
             no = lay["k_norm"] if kind == 0 else lay["v_norm"]
             co = lay["k_codes"] if kind == 0 else lay["v_codes"]
             norm[i, h] = pool[base + no + 4 * off: base + no + 4 * off + 4].view(np.float32)[0]
-            raw = pool[base + co + off * cb: base + co + (off + 1) * cb]
+            if kind == 0:
+                raw = pool[base + co + off * cb: base + co + (off + 1) * cb]
+            else:
+                raw = value_code_bytes(pool[base + co: base + co + P * cb], off, d, bits)
             bitsarr = np.unpackbits(raw, bitorder="little").reshape(d, bits)
             codes[i, h] = (bitsarr * (1 << np.arange(bits))).sum(1)
             if qjl:
@@ -59,7 +76,13 @@ def written_mask(pool_len: int, lay: dict, fmt, kind: int, slots) -> np.ndarray:
             no = lay["k_norm"] if kind == 0 else lay["v_norm"]
             co = lay["k_codes"] if kind == 0 else lay["v_codes"]
             mask[base + no + 4 * off: base + no + 4 * off + 4] = True
-            mask[base + co + off * cb: base + co + (off + 1) * cb] = True
+            if kind == 0:
+                mask[base + co + off * cb: base + co + (off + 1) * cb] = True
+            else:
+                d, vb = fmt.head_dim, fmt.v_bits
+                for r in range(d // 16):
+                    pos = base + co + value_chunk_pos(off, r, d, vb)
+                    mask[pos: pos + 2 * vb] = True
             if qjl:
                 mask[base + lay["k_gamma"] + 4 * off: base + lay["k_gamma"] + 4 * off + 4] = True
                 sb = fmt.qjl_m // 8
