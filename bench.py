@@ -358,6 +358,8 @@ def run_encode(args, device):
     peak, _ = measured_peaks()
     for b in wl.bits:
         for qjl in wl.qjl_options:
+            if args.encode_formats and f"b{b}_qjl{qjl}" not in args.encode_formats.split(","):
+                continue
             fmt = ti.Format(d, b, b, qjl, wl.qjl_m, P, H)
             lay = tq.tq_page_layout(fmt)
             pools = [torch.zeros(num_pages * lay["page_bytes"], dtype=torch.uint8, device=device) for _ in range(layers)]
@@ -521,6 +523,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--quick", action="store_true", help="fewer encode layers (development)")
     ap.add_argument("--layers", type=int, default=0, help="decode layers (profiling a small case; 0 = the workload's)")
+    ap.add_argument("--encode-only", action="store_true", help="run only the bulk-encode part (profiling)")
+    ap.add_argument("--encode-formats", default="", help="comma list such as b4_qjl1 (default: all six)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "tq" else args.warmup
 
@@ -561,6 +565,13 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         return float(t.item())
 
+    if args.encode_only:
+        if rank == 0:
+            print(json.dumps({"encode": run_encode(args, device)}), flush=True)
+        if pg:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
     res, bench = run_decode(args, device, barrier, reduce_max, rank, world)
     if not args.no_e2e:
         e2e = run_e2e(args, bench)
