@@ -10,11 +10,13 @@ from .tq import (  # noqa: F401
     TQ_DEVERR_SLOT_RANGE,
     TQ_KIND_K,
     TQ_KIND_V,
+    TQ_STATIC_SCRATCH_BYTES,
     TQError,
     device_codebook,
     load_library,
     tq_decode,
     tq_decode_attn,
+    tq_decode_attn_static,
     tq_decode_attn_timed,
     tq_decode_attn_workspace_size,
     tq_encode,

@@ -206,6 +206,7 @@ const char *tq_status_string(tq_status s) {
     case TQ_ERR_DEVICE_FAULT: return "device-side data error (see err_word)";
     case TQ_ERR_TIMEOUT: return "timeout";
     case TQ_ERR_WORKSPACE: return "workspace too small";
+    case TQ_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the static buffer of tq_decode_attn_static holds";
   }
   return "unknown status";
 }

@@ -1,0 +1,59 @@
+// tq_attn_static.cu -- tq_decode_attn_static: decode attention whose scratch
+// is a fixed device array in the library image instead of a caller
+// workspace, for callers that have no allocator to draw a workspace from
+// (a plug-in handed bare tensor pointers by its host framework, or a loop
+// that must not enter any allocator).  Nothing here allocates: the array is
+// part of the loaded module, its address is looked up once per device, and
+// the call then runs the ordinary tq_decode_attn on it.
+#include <mutex>
+
+#include "tq.h"
+#include "tq_internal.cuh"
+
+namespace {
+
+constexpr size_t kScratchBytes = TQ_STATIC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+// The scratch: every call on a device uses this one buffer (calls must not
+// overlap in time).  No word of it needs to start at zero.
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+std::mutex g_setup_mu;
+void *g_scratch_ptr[kMaxDevices];  // device address of g_scratch, per device; null until set up
+
+// Set-up, once per device, with that device current.
+tq_status scratch_address(void **ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return TQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_setup_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" tq_status tq_decode_attn_static(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                                           const void *page_pool, int64_t num_pages, const int32_t *block_tables,
+                                           int max_pages, const int32_t *comp_lens, const void *k_win_f16,
+                                           const void *v_win_f16, const int32_t *win_lens, int window,
+                                           const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
+                                           const float *v_codebook, const float *S, float *out, int32_t *err_word,
+                                           void *stream) {
+  size_t need = 0;
+  tq_status s = tq_decode_attn_workspace_size(fmt, batch, num_q_heads, max_pages, window, &need);
+  if (s != TQ_OK) return s;
+  if (need > kScratchBytes) return TQ_ERR_SCRATCH_LIMIT;
+  void *scratch = nullptr;
+  s = scratch_address(&scratch);
+  if (s != TQ_OK) return s;
+  return tq_decode_attn(fmt, batch, num_q_heads, q_f16, page_pool, num_pages, block_tables, max_pages, comp_lens,
+                        k_win_f16, v_win_f16, win_lens, window, k_signs, v_signs, k_codebook, v_codebook, S, out,
+                        scratch, kScratchBytes, err_word, stream);
+}

@@ -25,7 +25,8 @@ TQ_DEVERR_PAGE_RANGE = 0x2
 TQ_DEVERR_LENGTH = 0x4
 
 STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_CUDA", 4: "TQ_ERR_DEVICE_FAULT",
-          5: "TQ_ERR_TIMEOUT", 6: "TQ_ERR_WORKSPACE"}
+          5: "TQ_ERR_TIMEOUT", 6: "TQ_ERR_WORKSPACE", 7: "TQ_ERR_SCRATCH_LIMIT"}
+TQ_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class TQError(RuntimeError):
@@ -66,8 +67,9 @@ def load_library():
             lib.tq_decode_attn_workspace_size.argtypes = [P, i32, i32, i32, i32, C.POINTER(sz)]
             lib.tq_decode_attn.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P]
             lib.tq_decode_attn_timed.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P, P, P]
+            lib.tq_decode_attn_static.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, P]
             for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn",
-                      "tq_decode_attn_timed"):
+                      "tq_decode_attn_timed", "tq_decode_attn_static"):
                 getattr(lib, f).restype = C.c_int
             _lib = lib
     return _lib
@@ -180,6 +182,25 @@ def tq_decode_attn_timed(fmt, q, page_pool, num_pages: int, block_tables, comp_l
     """tq_decode_attn that also records torch.cuda.Event objects around the split-KV main kernel."""
     return _decode_attn(fmt, q, page_pool, num_pages, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs,
                         k_codebook, v_codebook, S, out, workspace, err_word, stream, (main_begin, main_end))
+
+
+def tq_decode_attn_static(fmt, q, page_pool, num_pages: int, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs,
+                          k_codebook, v_codebook, S, out, err_word=None, stream=None):
+    """tq_decode_attn on the library's fixed scratch buffer: no workspace, no allocation."""
+    F = _fmt(fmt)
+    B, Hq, _ = q.shape
+    window = 0 if k_win is None else int(k_win.shape[2])
+    rc = load_library().tq_decode_attn_static(
+        C.byref(F), int(B), int(Hq), _dev_ptr(q, torch.float16, "q"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
+        _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]), _dev_ptr(comp_lens, torch.int32, "comp_lens"),
+        _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True),
+        _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), window, _dev_ptr(k_signs, torch.uint8, "k_signs"),
+        _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
+        _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
+        _dev_ptr(out, torch.float32, "out"), _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+    )
+    _check(rc, "tq_decode_attn_static")
+    return out
 
 
 def _event(ev):

@@ -44,7 +44,9 @@ typedef enum {
   TQ_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed               */
   TQ_ERR_DEVICE_FAULT = 4,  /* reserved: reported through err_word instead         */
   TQ_ERR_TIMEOUT = 5,       /* reserved: no kernel waits on another               */
-  TQ_ERR_WORKSPACE = 6      /* the workspace passed is smaller than required       */
+  TQ_ERR_WORKSPACE = 6,     /* the workspace passed is smaller than required       */
+  TQ_ERR_SCRATCH_LIMIT = 7  /* tq_decode_attn_static: the shape needs more scratch
+                               than its fixed buffer (TQ_STATIC_SCRATCH_BYTES)    */
 } tq_status;
 
 /* Which stream of the cache a call works on. */
@@ -194,6 +196,37 @@ tq_status tq_decode_attn_timed(const tq_format *fmt, int batch, int num_q_heads,
                                const float *v_codebook, const float *S, float *out, void *workspace,
                                size_t workspace_bytes, int32_t *err_word, void *main_begin_event,
                                void *main_end_event, void *stream);
+
+/*
+ * tq_decode_attn without a workspace argument: the library's own scratch is
+ * one fixed device buffer of TQ_STATIC_SCRATCH_BYTES per device, a static
+ * array in the library image, so this call allocates nothing at all.  The
+ * pages have no counterpart; it exists for callers that cannot hand over a
+ * workspace: a plug-in that only receives tensor pointers from its host
+ * framework and has no handle on that framework's allocator, or a loop that
+ * must not call into any allocator.
+ *   - Arguments, layouts, results and device-side errors are those of
+ *     tq_decode_attn, minus workspace / workspace_bytes.
+ *   - The first call on a device (that device current) looks up the
+ *     buffer's address with cudaGetSymbolAddress; make that first call
+ *     before any stream capture.  A failed look-up returns TQ_ERR_CUDA.
+ *   - A shape whose tq_decode_attn_workspace_size exceeds
+ *     TQ_STATIC_SCRATCH_BYTES returns TQ_ERR_SCRATCH_LIMIT before anything
+ *     is launched (16 MiB covers, e.g., B 16 x 32/8 heads at 32K context).
+ *   - Nothing in the buffer has to start at zero: every call writes each
+ *     scratch word it later reads.
+ *   - All calls on one device share the buffer: two calls whose work
+ *     overlaps in time (different streams, or threads without ordering)
+ *     race and corrupt each other's results.  Order them on one stream.
+ */
+#define TQ_STATIC_SCRATCH_BYTES (16u << 20)
+tq_status tq_decode_attn_static(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                                const void *page_pool, int64_t num_pages, const int32_t *block_tables,
+                                int max_pages, const int32_t *comp_lens, const void *k_win_f16,
+                                const void *v_win_f16, const int32_t *win_lens, int window,
+                                const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
+                                const float *v_codebook, const float *S, float *out, int32_t *err_word,
+                                void *stream);
 
 #ifdef __cplusplus
 }
