@@ -61,14 +61,20 @@ __device__ __forceinline__ void store_codes_grouped(uint8_t *sec, int64_t off, i
   } else if constexpr (BITS == 2) {
     *reinterpret_cast<uint32_t *>(c0) = w[0];
     *reinterpret_cast<uint32_t *>(c1) = w[1];
-  } else {  // 6-byte chunks on 2-byte boundaries
-    uint16_t *h0 = reinterpret_cast<uint16_t *>(c0), *h1 = reinterpret_cast<uint16_t *>(c1);
-    h0[0] = (uint16_t)w[0];
-    h0[1] = (uint16_t)(w[0] >> 16);
-    h0[2] = (uint16_t)w[1];
-    h1[0] = (uint16_t)(w[1] >> 16);
-    h1[1] = (uint16_t)w[2];
-    h1[2] = (uint16_t)(w[2] >> 16);
+  } else {  // 6-byte chunks: 4-byte aligned for even offsets, 2 bytes past that for odd ones
+    const uint32_t lo0 = w[0], hi0 = w[1] & 0xFFFFu;                   // chunk 2q: bytes 0..5
+    const uint32_t lo1 = __byte_perm(w[1], w[2], 0x5432), hi1 = w[2] >> 16;  // chunk 2q+1: bytes 6..11
+    if ((off & 1) == 0) {
+      *reinterpret_cast<uint32_t *>(c0) = lo0;
+      *reinterpret_cast<uint16_t *>(c0 + 4) = (uint16_t)hi0;
+      *reinterpret_cast<uint32_t *>(c1) = lo1;
+      *reinterpret_cast<uint16_t *>(c1 + 4) = (uint16_t)hi1;
+    } else {
+      *reinterpret_cast<uint16_t *>(c0) = (uint16_t)lo0;
+      *reinterpret_cast<uint32_t *>(c0 + 2) = (lo0 >> 16) | (hi0 << 16);
+      *reinterpret_cast<uint16_t *>(c1) = (uint16_t)lo1;
+      *reinterpret_cast<uint32_t *>(c1 + 2) = (lo1 >> 16) | (hi1 << 16);
+    }
   }
 }
 
@@ -128,9 +134,16 @@ __device__ __forceinline__ void fwht_quad(float (&x)[32], int q) {
   fwht_xlane<32>(x, 2, (q & 2) != 0);
 }
 
+// QJL matrix for the encode projection on the tensor cores: S split into
+// fp16 hi and lo parts, one 16-byte cell per (row l, lane slice t, k-step ks)
+// holding S[l][32t+4ks .. 32t+4ks+3] as {hi pair, hi pair, lo pair, lo pair};
+// the cell position inside its 128-byte row is XOR-swizzled by (t, l&1) so
+// the 8 lanes of each load phase read 8 different bank groups.
+__device__ __forceinline__ int sq_cell(int l, int t, int ks) { return (l * 4 + t) * 8 + (ks ^ (t + 4 * (l & 1))); }
+
 template <int BITS, bool QJL>
 __global__ void __launch_bounds__(256) encode_kernel(const EncodeArgs a) {
-  extern __shared__ float s_S[];  // [m][d] swizzled, QJL only
+  extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells, QJL only
   __shared__ float s_cent[16];
   __shared__ float s_mid[16];
   __shared__ uint32_t s_dsign[4];
@@ -144,7 +157,15 @@ __global__ void __launch_bounds__(256) encode_kernel(const EncodeArgs a) {
     s_dsign[tid] = w;
   }
   if constexpr (QJL) {
-    for (int i = tid; i < kM * kD; i += blockDim.x) s_S[s_swz(i / kD, i % kD)] = a.S[i];
+    __half *sh = reinterpret_cast<__half *>(s_Sq);
+    for (int i = tid; i < kM * kD; i += blockDim.x) {
+      const int l = i / kD, j = i % kD;
+      __half hi, lo;
+      split_half(a.S[i], hi, lo);
+      const int cell = sq_cell(l, j >> 5, (j & 31) >> 2);
+      sh[cell * 8 + (j & 3)] = hi;
+      sh[cell * 8 + 4 + (j & 3)] = lo;
+    }
   }
   __syncthreads();
 
@@ -217,48 +238,46 @@ __global__ void __launch_bounds__(256) encode_kernel(const EncodeArgs a) {
       g2 += __shfl_xor_sync(0xffffffffu, g2, 1);
       g2 += __shfl_xor_sync(0xffffffffu, g2, 2);
       const float gamma = zero ? 0.f : sqrtf(g2) * 0.08838834764831845f;
-      uint32_t word = 0u;
-#pragma unroll 1
-      for (int c = 0; c < 4; c++) {
-        // rows l = 32k + 8c + i, partial index p = 8k + i
-        float part[32];
+      // (S e)_l on the tensor cores: rows g / g+8 of the A operand are the fp16
+      // hi / lo parts of this quad's residual (vector g of the warp), B is
+      // S hi then S lo, so the fp32 sum misses only the lo*lo term (~2^-22).
+      // k-indices 2t, 2t+1 | 2t+8, 2t+9 of step ks are coordinates
+      // 32t+4ks+{0,1} | +{2,3}: every lane supplies its own slice.
+      uint32_t A[8][4];
 #pragma unroll
-        for (int p = 0; p < 32; p++) {
-          const int l = 32 * (p >> 3) + 8 * c + (p & 7);
-          float acc = 0.f;
-#pragma unroll
-          for (int i4 = 0; i4 < 8; i4++) {
-            const float4 sv = *reinterpret_cast<const float4 *>(&s_S[l * kD + 32 * q + ((4 * i4) ^ (8 * q))]);
-            acc = fmaf(sv.x, x[4 * i4 + 0], acc);
-            acc = fmaf(sv.y, x[4 * i4 + 1], acc);
-            acc = fmaf(sv.z, x[4 * i4 + 2], acc);
-            acc = fmaf(sv.w, x[4 * i4 + 3], acc);
-          }
-          part[p] = acc;
-        }
-        // reduce-scatter over the quad: stage 1 keeps k in {b, b+2}, stage 2 keeps k = q
-        const int bq = q & 1, aq = q >> 1;
-        float r1[16];
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          // keep groups k = bq and k = bq + 2; send k = 1-bq and k = 3-bq
-          const float keep0 = bq ? part[8 + i] : part[i];
-          const float keep1 = bq ? part[24 + i] : part[16 + i];
-          const float send0 = bq ? part[i] : part[8 + i];
-          const float send1 = bq ? part[16 + i] : part[24 + i];
-          r1[i] = keep0 + __shfl_xor_sync(0xffffffffu, send0, 1);
-          r1[8 + i] = keep1 + __shfl_xor_sync(0xffffffffu, send1, 1);
-        }
-        uint32_t byte = 0u;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          const float keep = aq ? r1[8 + i] : r1[i];
-          const float send = aq ? r1[i] : r1[8 + i];
-          const float tot = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-          byte |= (tot >= 0.f ? 1u : 0u) << i;
-        }
-        word |= byte << (8 * c);
+      for (int ks = 0; ks < 8; ks++) {
+        __half h0, l0, h1, l1, h2, l2, h3, l3;
+        split_half(x[4 * ks + 0], h0, l0);
+        split_half(x[4 * ks + 1], h1, l1);
+        split_half(x[4 * ks + 2], h2, l2);
+        split_half(x[4 * ks + 3], h3, l3);
+        A[ks][0] = pack_half2_raw(h0, h1);
+        A[ks][1] = pack_half2_raw(l0, l1);
+        A[ks][2] = pack_half2_raw(h2, h3);
+        A[ks][3] = pack_half2_raw(l2, l3);
       }
+      uint32_t words[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int nt = 0; nt < 16; nt++) {  // outputs l = 8nt .. 8nt+7; this lane gets 8nt+2q, 8nt+2q+1
+        float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f};
+        const int l = 8 * nt + quad_in_warp;
+#pragma unroll
+        for (int ks = 0; ks < 8; ks++) {
+          const uint4 sv = s_Sq[sq_cell(l, q, ks)];
+          mma_16816(dh, A[ks][0], A[ks][1], A[ks][2], A[ks][3], sv.x, sv.y);
+          mma_16816(dl, A[ks][0], A[ks][1], A[ks][2], A[ks][3], sv.z, sv.w);
+        }
+        const float p0 = (dh[0] + dh[2]) + (dl[0] + dl[2]);
+        const float p1 = (dh[1] + dh[3]) + (dl[1] + dl[3]);
+        const int bit = 8 * (nt & 3) + 2 * q;
+        words[nt >> 2] |= ((p0 >= 0.f ? 1u : 0u) << bit) | ((p1 >= 0.f ? 1u : 0u) << (bit + 1));
+      }
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        words[k] |= __shfl_xor_sync(0xffffffffu, words[k], 1);
+        words[k] |= __shfl_xor_sync(0xffffffffu, words[k], 2);
+      }
+      uint32_t word = q == 0 ? words[0] : q == 1 ? words[1] : q == 2 ? words[2] : words[3];
       if (zero) word = 0u;
       if (ok) {
         reinterpret_cast<uint32_t *>(slab + a.signs_off + off * (kM / 8))[q] = word;
