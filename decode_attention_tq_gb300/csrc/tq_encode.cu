@@ -141,16 +141,47 @@ __device__ __forceinline__ void fwht_quad(float (&x)[32], int q) {
 // the 8 lanes of each load phase read 8 different bank groups.
 __device__ __forceinline__ int sq_cell(int l, int t, int ks) { return (l * 4 + t) * 8 + (ks ^ (t + 4 * (l & 1))); }
 
+// Quantizer lookup.  Bucket k = 48 + round(4u) covers 4u in [k-48.5, k-47.5]
+// (both ends closed); since |u| <= sqrt(d) (||u||^2 = d), k stays in [2, 94].
+// Entry k = (number of thresholds below the bucket, the single threshold
+// inside it or +inf), so idx = #{t <= u} = base + [u >= thr] exactly, as long
+// as no bucket holds two thresholds (checked when the table is built; the
+// binary search is used otherwise).
+constexpr int kQBuckets = 96;
+constexpr float kQMagic = 12582912.0f + 48.0f;  // 1.5 * 2^23: the integer part lands in the low mantissa bits
+
+__device__ __forceinline__ int quant_bucket(float u) {
+  return __float_as_int(fmaf(u, 4.0f, kQMagic)) - __float_as_int(12582912.0f);
+}
+
 template <int BITS, bool QJL>
-__global__ void __launch_bounds__(256) encode_kernel(const EncodeArgs a) {
+__global__ void __launch_bounds__(256, QJL ? 2 : 3) encode_kernel(const EncodeArgs a) {
   extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells, QJL only
   __shared__ float s_cent[16];
   __shared__ float s_mid[16];
   __shared__ uint32_t s_dsign[4];
+  __shared__ uint2 s_qlut[kQBuckets];
+  __shared__ float2 s_qcen[kQBuckets];  // centroids of codes base and base+1 (QJL residual)
+  __shared__ int s_lut_bad;
   constexpr int L = 1 << BITS;
   const int tid = threadIdx.x;
   if (tid < L) s_cent[tid] = a.codebook[tid];
   if (tid < L - 1) s_mid[tid] = a.codebook[L + tid];
+  if (tid == 0) s_lut_bad = 0;
+  __syncthreads();
+  if (tid < kQBuckets) {
+    const float lo = ((float)(tid - 48) - 0.5f) * 0.25f, hi = ((float)(tid - 48) + 0.5f) * 0.25f;
+    int base = 0, inside = 0;
+    float thr = __int_as_float(0x7f800000);  // +inf
+    for (int k = 0; k < L - 1; k++) {
+      const float t = a.codebook[L + k];
+      if (t < lo) base++;
+      else if (t <= hi) { thr = t; inside++; }
+    }
+    if (inside > 1 || (tid == 0 && base > 0) || (tid == kQBuckets - 1 && inside + base < L - 1)) atomicOr(&s_lut_bad, 1);
+    s_qlut[tid] = make_uint2((uint32_t)base, __float_as_uint(thr));
+    s_qcen[tid] = make_float2(a.codebook[base], a.codebook[base + 1 < L ? base + 1 : base]);
+  }
   if (tid < 4) {
     uint32_t w = 0;
     for (int j = 0; j < 32; j++) w |= (a.signs[32 * tid + j] ? 1u : 0u) << j;
@@ -175,13 +206,22 @@ __global__ void __launch_bounds__(256) encode_kernel(const EncodeArgs a) {
   const int64_t NH = a.n_tokens * a.H;
   const uint32_t dsign = s_dsign[q];
   const int64_t pool_slots = a.num_pages * (int64_t)a.P;
+  const bool lut_bad = s_lut_bad != 0;
+  const bool small = NH <= 0x7fffffff;
 
   for (int64_t vb = (int64_t)warp * 8; vb < NH; vb += nwarps * 8) {
     const int64_t v = vb + quad_in_warp;
     const bool in_range = v < NH;
     const int64_t vv = in_range ? v : NH - 1;
-    const int64_t n = vv / a.H;
-    const int h = (int)(vv % a.H);
+    int64_t n;
+    int h;
+    if (small) {  // 32-bit division for the common sizes
+      n = (uint32_t)vv / (uint32_t)a.H;
+      h = (int)((uint32_t)vv - (uint32_t)n * (uint32_t)a.H);
+    } else {
+      n = vv / a.H;
+      h = (int)(vv % a.H);
+    }
     const int64_t slot = a.slot_mapping[n];
     bool ok = in_range && slot >= 0;
     if (ok && slot >= pool_slots) {
@@ -205,15 +245,30 @@ __global__ void __launch_bounds__(256) encode_kernel(const EncodeArgs a) {
     const float inv = zero ? 0.f : 1.0f / nrm;
 
     int idx[32];
+    if (!lut_bad) {
 #pragma unroll
-    for (int j = 0; j < 32; j++) {
-      const float u = x[j] * inv;
-      int k = 0;
+      for (int j = 0; j < 32; j++) {
+        const float u = x[j] * inv;
+        const int b = quant_bucket(u);
+        const uint2 e = s_qlut[b];
+        const bool up = u >= __uint_as_float(e.y);
+        idx[j] = zero ? 0 : (int)e.x + (up ? 1 : 0);
+        if constexpr (QJL) {
+          const float2 c = s_qcen[b];
+          x[j] = u - (zero ? s_cent[0] : (up ? c.y : c.x));  // residual in u units
+        }
+      }
+    } else {
 #pragma unroll
-      for (int s = L / 2; s >= 1; s >>= 1)
-        if (u >= s_mid[k + s - 1]) k += s;
-      idx[j] = zero ? 0 : k;
-      x[j] = u - s_cent[idx[j]];  // residual in u units (QJL only)
+      for (int j = 0; j < 32; j++) {
+        const float u = x[j] * inv;
+        int k = 0;
+#pragma unroll
+        for (int s = L / 2; s >= 1; s >>= 1)
+          if (u >= s_mid[k + s - 1]) k += s;
+        idx[j] = zero ? 0 : k;
+        x[j] = u - s_cent[idx[j]];  // residual in u units (QJL only)
+      }
     }
     uint32_t w[BITS];
     pack_codes<BITS>(idx, w);
