@@ -18,7 +18,11 @@
  *     outside the pool, a length larger than its buffer) never trap: the
  *     kernel skips the offending token/page and ORs a TQ_DEVERR_* bit into
  *     the caller's optional int32 *err_word (device memory, may be NULL).
- *   - Nothing waits on the device: there are no spin-waits in any kernel.
+ *   - No kernel waits on another, and the default build has no wait inside
+ *     a kernel.  A build with the bulk-copy staging option of the attention
+ *     kernel (TQ_TMA_STAGING=1) has one: a warp waiting for its own copies
+ *     into shared memory, which gives up after about 0.5 s, sets
+ *     TQ_DEVERR_TIMEOUT and returns.
  *
  * Format (tq_format): d = head_dim, b_K / b_V = bits per coordinate of the
  * Lloyd-Max codes, optional 1-bit QJL residual sketch of length m on keys,
@@ -56,6 +60,7 @@ enum { TQ_KIND_K = 0, TQ_KIND_V = 1 };
 #define TQ_DEVERR_SLOT_RANGE 0x1   /* slot_mapping[n] >= num_pages * page_size          */
 #define TQ_DEVERR_PAGE_RANGE 0x2   /* block_tables entry outside [0, num_pages)         */
 #define TQ_DEVERR_LENGTH 0x4       /* comp_lens[b] > max_pages*P, win_lens[b] > window, or a negative length */
+#define TQ_DEVERR_TIMEOUT 0x8      /* a staging wait in the attention kernel gave up after ~0.5 s: outputs invalid */
 
 typedef struct {
   int32_t head_dim;     /* d                                                   */
