@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 #pragma unroll
         for (int i = 0; i < 4; i++) acc[mt][nt][i] = 0.f;
     }
-    float nu = 0.f;
+    float nu = 0.f, inv_nu = 0.f;
 
     TileCursor cur;
     cur.pool = a.pool;
@@ -549,17 +549,14 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
           for (int nt = 0; nt < NT; nt++) mma_16816(sq[nt], a0, a1, a2, a3, sb[nt][kk][0], sb[nt][kk][1]);
         }
       }
-      // ---- online softmax (log2 domain) and value weights
+      // ---- online softmax (log2 domain) and value weights, relative to the
+      // running (mu, nu).  They are moved (warp reductions, accumulator
+      // rescale) only when a live token would exceed the weight bound: a logit
+      // above mu + kLazyLog2 or a value norm above kLazyNu * nu.  Weights then
+      // stay below 2^kLazyLog2 * kLazyNu, which kWeightScale keeps inside fp16.
       const float vn0 = R.ok0 ? V.nv0 : 0.f, vn1 = R.ok1 ? V.nv1 : 0.f;
-      const float tnu = warp_max_xor(fmaxf(vn0, vn1), 4 | 8 | 16);
-      const float nu_new = fmaxf(nu, tnu);
-      const float rcp_nu = nu_new > 0.f ? __frcp_rn(nu_new) : 0.f;
-      const float nu_ratio = nu_new > 0.f ? nu * rcp_nu : 1.f;
-      const float inv_nu = kWeightScale * rcp_nu;
-      nu = nu_new;
-      uint32_t wb[NT][2];
-      bool rescale = false;
-      float beta[NT];
+      float lg0[NT], lg1[NT];
+      bool big = vn0 > kLazyNu * nu || vn1 > kLazyNu * nu;
 #pragma unroll
       for (int nt = 0; nt < NT; nt++) {
         float l0 = ((sa[nt][0] + sa[nt][1]) + (sa[nt][2] + sa[nt][3])) * cK[nt];
@@ -568,16 +565,37 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
           l0 = fmaf(R.g0 * (sq[nt][0] + sq[nt][1]), cQ[nt], l0);
           l1 = fmaf(R.g1 * (sq[nt][2] + sq[nt][3]), cQ[nt], l1);
         }
-        l0 = R.ok0 ? R.nk0 * l0 : -INFINITY;
-        l1 = R.ok1 ? R.nk1 * l1 : -INFINITY;
-        const float tmax = warp_max_xor(fmaxf(l0, l1), 4 | 8 | 16);
-        const float mnew = fmaxf(mu[nt], tmax);
-        const float alpha = fast_exp2(mu[nt] - mnew);
-        const float p0 = fast_exp2(l0 - mnew), p1 = fast_exp2(l1 - mnew);
-        lsum[nt] = fmaf(lsum[nt], alpha, p0 + p1);
-        mu[nt] = mnew;
-        beta[nt] = alpha * nu_ratio;
-        rescale |= beta[nt] != 1.f;
+        lg0[nt] = R.ok0 ? R.nk0 * l0 : -INFINITY;
+        lg1[nt] = R.ok1 ? R.nk1 * l1 : -INFINITY;
+        big |= fmaxf(lg0[nt], lg1[nt]) > mu[nt] + kLazyLog2;
+      }
+      if (__any_sync(0xffffffffu, big)) {
+        const float tnu = warp_max_xor(fmaxf(vn0, vn1), 4 | 8 | 16);
+        const float nu_new = fmaxf(nu, tnu);
+        const float nu_ratio = nu_new > 0.f ? nu / nu_new : 1.f;
+        inv_nu = nu_new > 0.f ? kWeightScale / nu_new : 0.f;
+        nu = nu_new;
+        float beta[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+          const float mnew = fmaxf(mu[nt], warp_max_xor(fmaxf(lg0[nt], lg1[nt]), 4 | 8 | 16));
+          const float alpha = mnew == -INFINITY ? 1.f : fast_exp2(mu[nt] - mnew);
+          lsum[nt] *= alpha;
+          mu[nt] = mnew;
+          beta[nt] = alpha * nu_ratio;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) acc[mt][nt][i] *= beta[nt];
+      }
+      uint32_t wb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++) {
+        const float p0 = fast_exp2(lg0[nt] - mu[nt]), p1 = fast_exp2(lg1[nt] - mu[nt]);
+        lsum[nt] += p0 + p1;
         const float w0 = p0 * vn0 * inv_nu, w1 = p1 * vn1 * inv_nu;
         __half wh0, wl0, wh1, wl1;
         split_half(w0, wh0, wl0);
@@ -591,14 +609,6 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         const uint32_t x0 = (r & 1) ? q0 : h0, x1 = (r & 1) ? q1 : h1;
         wb[nt][0] = __byte_perm(x0, x1, 0x5410);
         wb[nt][1] = __byte_perm(x0, x1, 0x7632);
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int mt = 0; mt < 8; mt++)
-#pragma unroll
-          for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-            for (int i = 0; i < 4; i++) acc[mt][nt][i] *= beta[nt];
       }
       // ---- values: interleave the codes of the token pairs (2t, 2t+1) and
       // (2t+8, 2t+9) at each coordinate; one lookup gives an A register.

@@ -14,9 +14,13 @@ constexpr int kTile = 16;     // tokens per attention tile (one mma M / K tile)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Power-of-two scales that keep fp16 MMA operands away from overflow and
-// subnormals: centroids are stored x256, attention weights x16384.
+// subnormals: centroids are stored x256, attention weights x64.
 constexpr float kCentScale = 256.0f;
-constexpr float kWeightScale = 16384.0f;
+constexpr float kWeightScale = 64.0f;
+// Lazy softmax bounds of the attention kernel: weights p * n / nu stay below
+// 2^kLazyLog2 * kLazyNu = 512, so 512 * kWeightScale = 32768 fits in fp16.
+constexpr float kLazyLog2 = 8.0f;
+constexpr float kLazyNu = 2.0f;
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
