@@ -130,6 +130,11 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float (*s_q)
   __syncthreads();
   const __half *kbase = a.k_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
   const __half *vbase = a.v_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
+  // this thread's coordinate of every value row, loaded up front so the
+  // loads are in flight during the score phase
+  __half vrow[kWinChunk];
+#pragma unroll
+  for (int i = 0; i < kWinChunk; i++) vrow[i] = i < n ? vbase[(int64_t)i * kD + tid] : __float2half(0.f);
   {  // (1) scores
     const int i = tid >> 2, part = tid & 3;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -174,10 +179,11 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float (*s_q)
     }
   }
   __syncthreads();
-  {  // (3) values
+  {  // (3) values (s_p is 0 past n)
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int i = 0; i < n; i++) {
-      const float v = __half2float(vbase[(int64_t)i * kD + tid]);
+#pragma unroll
+    for (int i = 0; i < kWinChunk; i++) {
+      const float v = __half2float(vrow[i]);
 #pragma unroll
       for (int g = 0; g < 8; g++)
         if (g < G) acc[g] = fmaf(s_p[g][i], v, acc[g]);
@@ -228,40 +234,41 @@ __device__ __forceinline__ float block_sum128(float v, float *s_red) {
 }
 
 // Online log-sum-exp merge of n partials (max, sum, accumulator column j),
-// up to 128 at a time: their (max, sum) pairs are read in parallel, the
-// accumulator columns with independent loads.
+// 32 at a time: the accumulator columns of a chunk are loaded into registers
+// together with the (max, sum) pairs, so a chunk costs one memory latency.
 template <class ML, class ACC>
 __device__ __forceinline__ void merge_partials(int64_t n, ML ml, ACC acc_of, float &M, float &L, float &A, float *s_w,
                                                float *s_red) {
+  constexpr int kChunk = 32;
   const int j = threadIdx.x;
-  for (int64_t c0 = 0; c0 < n; c0 += 128) {
-    const int64_t k = c0 + j;
+  for (int64_t c0 = 0; c0 < n; c0 += kChunk) {
+    const int cn = (int)min((int64_t)kChunk, n - c0);
+    float av[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; i++) av[i] = i < cn ? acc_of(c0 + i)[j] : 0.f;
     float m = -INFINITY, l = 0.f;
-    if (k < n) {
-      const float2 v = ml(k);
+    if (j < cn) {
+      const float2 v = ml(c0 + j);
       m = v.x;
       l = v.y;
     }
     const float Mn = fmaxf(M, block_max128(m, s_red));
     if (Mn == -INFINITY) continue;  // block-uniform
     const float w = m == -INFINITY ? 0.f : exp2f(m - Mn);
-    s_w[j] = w;
+    if (j < kChunk) s_w[j] = w;
     const float lsum = block_sum128(l * w, s_red);  // also publishes s_w
     const float sold = exp2f(M - Mn);
-    A *= sold;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kChunk; i += 4) {
+      a0 = fmaf(s_w[i], av[i], a0);
+      a1 = fmaf(s_w[i + 1], av[i + 1], a1);
+      a2 = fmaf(s_w[i + 2], av[i + 2], a2);
+      a3 = fmaf(s_w[i + 3], av[i + 3], a3);
+    }
+    A = A * sold + ((a0 + a1) + (a2 + a3));
     L = L * sold + lsum;
     M = Mn;
-    const int cn = (int)min((int64_t)128, n - c0);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int i = 0;
-    for (; i + 4 <= cn; i += 4) {
-      a0 = fmaf(s_w[i], acc_of(c0 + i)[j], a0);
-      a1 = fmaf(s_w[i + 1], acc_of(c0 + i + 1)[j], a1);
-      a2 = fmaf(s_w[i + 2], acc_of(c0 + i + 2)[j], a2);
-      a3 = fmaf(s_w[i + 3], acc_of(c0 + i + 3)[j], a3);
-    }
-    for (; i < cn; i++) a0 = fmaf(s_w[i], acc_of(c0 + i)[j], a0);
-    A += (a0 + a1) + (a2 + a3);
     __syncthreads();  // s_w is rewritten by the next chunk
   }
 }
