@@ -168,24 +168,23 @@ __global__ void __launch_bounds__(256, QJL ? 2 : 3) encode_kernel(const EncodeAr
   if (tid < L) s_cent[tid] = a.codebook[tid];
   if (tid < L - 1) s_mid[tid] = a.codebook[L + tid];
   if (tid == 0) s_lut_bad = 0;
+  if (tid < kD) {  // sign words: one load per coordinate, packed by a ballot
+    const uint32_t w = __ballot_sync(0xffffffffu, a.signs[tid] != 0);
+    if ((tid & 31) == 0) s_dsign[tid >> 5] = w;
+  }
   __syncthreads();
   if (tid < kQBuckets) {
     const float lo = ((float)(tid - 48) - 0.5f) * 0.25f, hi = ((float)(tid - 48) + 0.5f) * 0.25f;
     int base = 0, inside = 0;
     float thr = __int_as_float(0x7f800000);  // +inf
     for (int k = 0; k < L - 1; k++) {
-      const float t = a.codebook[L + k];
+      const float t = s_mid[k];
       if (t < lo) base++;
       else if (t <= hi) { thr = t; inside++; }
     }
     if (inside > 1 || (tid == 0 && base > 0) || (tid == kQBuckets - 1 && inside + base < L - 1)) atomicOr(&s_lut_bad, 1);
     s_qlut[tid] = make_uint2((uint32_t)base, __float_as_uint(thr));
-    s_qcen[tid] = make_float2(a.codebook[base], a.codebook[base + 1 < L ? base + 1 : base]);
-  }
-  if (tid < 4) {
-    uint32_t w = 0;
-    for (int j = 0; j < 32; j++) w |= (a.signs[32 * tid + j] ? 1u : 0u) << j;
-    s_dsign[tid] = w;
+    s_qcen[tid] = make_float2(s_cent[base], s_cent[base + 1 < L ? base + 1 : base]);
   }
   if constexpr (QJL) {
     __half *sh = reinterpret_cast<__half *>(s_Sq);
