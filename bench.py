@@ -54,6 +54,22 @@ def dist_info():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest x over all ranks (the step time the job is charged with);
+    x itself when there is no process group."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job rate of N independent replicas: every rank processes the same
+    units, the job takes as long as its slowest rank."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -276,7 +292,7 @@ def run_decode(args, device, barrier, reduce_max, rank, world):
     traffic = load_traffic("attn_main", wl.name)
 
     tokens_per_step = wl.batch * wl.layers * wl.context
-    value = world * tokens_per_step / (ms * 1e-3)
+    value = job_throughput(tokens_per_step, ms, world)
     res = {
         "metric": METRIC,
         "value": value,
@@ -559,11 +575,7 @@ def main():
             pg.barrier()
 
     def reduce_max(x):
-        if not pg:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(x, pg, device)
 
     if args.encode_only:
         if rank == 0:
@@ -576,7 +588,7 @@ def main():
     if not args.no_e2e:
         e2e = run_e2e(args, bench)
         e2e_ms = reduce_max(e2e["ms_per_step"])
-        e2e["value"] = world * bench.wl.batch * bench.wl.layers * bench.wl.context / (e2e_ms * 1e-3)
+        e2e["value"] = job_throughput(bench.wl.batch * bench.wl.layers * bench.wl.context, e2e_ms, world)
         res["e2e"] = e2e
     del bench
     torch.cuda.empty_cache()
