@@ -154,8 +154,27 @@ __device__ __forceinline__ int quant_bucket(float u) {
   return __float_as_int(fmaf(u, 4.0f, kQMagic)) - __float_as_int(12582912.0f);
 }
 
+// Encode layout.  A warp encodes 8 vectors; thread (g, t) = (lane/4, lane%4)
+// holds vector g at coordinates 32c + 8t + i (block c = 0..3, i = 0..7).
+// With i = 32c + b the Sylvester matrix factors as H_128 = H_4 (x) H_32, so
+// the transform is one tensor-core product per block (z = x_c H_32, rows of
+// the A operand are (vector g, block 2m) and (vector g, block 2m+1)) and a
+// 4-point butterfly across the blocks a thread already holds.  The k and n
+// indices of the MMA are permuted so that a thread's operand words are its
+// own loaded fp16 pairs and its outputs are again coordinates 8t .. 8t+7.
+//   k (per k-step ks): 2t+e -> 8t+4ks+e, 2t+8+e -> 8t+4ks+2+e
+//   n (per n-tile nt): 8nt+2t'+e -> 8t'+2nt+e
+__device__ __forceinline__ uint32_t had_pair(int i0, int i1, int j) {
+  // fp16 pair (H32[i0][j], H32[i1][j]) of the unnormalized Sylvester matrix
+  const uint32_t s0 = (uint32_t)(__popc(i0 & j) & 1) << 15, s1 = (uint32_t)(__popc(i1 & j) & 1) << 31;
+  return 0x3C003C00u | s0 | s1;
+}
+
+#ifndef TQ_ENCODE_MIN_BLOCKS
+#define TQ_ENCODE_MIN_BLOCKS 3
+#endif
 template <int BITS, bool QJL>
-__global__ void __launch_bounds__(256, QJL ? 2 : 3) encode_kernel(const EncodeArgs a) {
+__global__ void __launch_bounds__(256, QJL ? 2 : TQ_ENCODE_MIN_BLOCKS) encode_kernel(const EncodeArgs a) {
   extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells, QJL only
   __shared__ float s_cent[16];
   __shared__ float s_mid[16];
@@ -187,12 +206,14 @@ __global__ void __launch_bounds__(256, QJL ? 2 : 3) encode_kernel(const EncodeAr
     s_qcen[tid] = make_float2(s_cent[base], s_cent[base + 1 < L ? base + 1 : base]);
   }
   if constexpr (QJL) {
+    // cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
+    // coordinates thread t contributes at k-step ks of the projection
     __half *sh = reinterpret_cast<__half *>(s_Sq);
     for (int i = tid; i < kM * kD; i += blockDim.x) {
       const int l = i / kD, j = i % kD;
       __half hi, lo;
       split_half(a.S[i], hi, lo);
-      const int cell = sq_cell(l, j >> 5, (j & 31) >> 2);
+      const int cell = sq_cell(l, (j & 31) >> 3, 2 * (j >> 5) + ((j >> 2) & 1));
       sh[cell * 8 + (j & 3)] = hi;
       sh[cell * 8 + 4 + (j & 3)] = lo;
     }
@@ -203,10 +224,27 @@ __global__ void __launch_bounds__(256, QJL ? 2 : 3) encode_kernel(const EncodeAr
   const int warp = (blockIdx.x * blockDim.x + tid) >> 5;
   const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / 32;
   const int64_t NH = a.n_tokens * a.H;
-  const uint32_t dsign = s_dsign[q];
   const int64_t pool_slots = a.num_pages * (int64_t)a.P;
   const bool lut_bad = s_lut_bad != 0;
   const bool small = NH <= 0x7fffffff;
+  // sign masks of this thread's fp16 pairs (coordinates 32c + 8q + 2p, +1)
+  uint32_t smask[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; c++) {
+    const uint32_t byte = (s_dsign[c] >> (8 * q)) & 0xFFu;
+#pragma unroll
+    for (int p = 0; p < 4; p++) smask[c][p] = ((byte >> (2 * p)) & 1u) << 15 | ((byte >> (2 * p + 1)) & 1u) << 31;
+  }
+  // B fragments of H_32 (k and n permuted as above), constant over the loop
+  uint32_t hb[2][4][2];
+#pragma unroll
+  for (int ks = 0; ks < 2; ks++)
+#pragma unroll
+    for (int nt = 0; nt < 4; nt++) {
+      const int j = 8 * (quad_in_warp >> 1) + 2 * nt + (quad_in_warp & 1);  // permuted column of n = 8nt + g
+      hb[ks][nt][0] = had_pair(8 * q + 4 * ks, 8 * q + 4 * ks + 1, j);
+      hb[ks][nt][1] = had_pair(8 * q + 4 * ks + 2, 8 * q + 4 * ks + 3, j);
+    }
 
   for (int64_t vb = (int64_t)warp * 8; vb < NH; vb += nwarps * 8) {
     const int64_t v = vb + quad_in_warp;
@@ -228,19 +266,49 @@ __global__ void __launch_bounds__(256, QJL ? 2 : 3) encode_kernel(const EncodeAr
       ok = false;
     }
 
-    float x[32];
-    load_slice_f16(a.x + vv * kD + 32 * q, x);
+    // fp16 pairs of coordinates 32c + 8q + 2p, +1, sign-flipped by D
+    uint32_t xw[4][4];
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; j++) ss = fmaf(x[j], x[j], ss);
+    for (int c = 0; c < 4; c++) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(a.x + vv * kD + 32 * c + 8 * q);
+      const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int p = 0; p < 4; p++) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r4[p]));
+        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+        xw[c][p] = r4[p] ^ smask[c][p];
+      }
+    }
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
     const float nrm = sqrtf(ss);
     const bool zero = !(nrm > 0.f);
 
+    // z = x_c H_32 on the tensor cores, then the H_4 butterfly over blocks
+    float z[4][8];
 #pragma unroll
-    for (int j = 0; j < 32; j++) x[j] = ((dsign >> j) & 1u) ? -x[j] : x[j];
-    fwht_quad(x, q);
+    for (int mt = 0; mt < 2; mt++)
+#pragma unroll
+      for (int nt = 0; nt < 4; nt++) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(d, xw[2 * mt][0], xw[2 * mt + 1][0], xw[2 * mt][1], xw[2 * mt + 1][1], hb[0][nt][0], hb[0][nt][1]);
+        mma_16816(d, xw[2 * mt][2], xw[2 * mt + 1][2], xw[2 * mt][3], xw[2 * mt + 1][3], hb[1][nt][0], hb[1][nt][1]);
+        z[2 * mt][2 * nt] = d[0];
+        z[2 * mt][2 * nt + 1] = d[1];
+        z[2 * mt + 1][2 * nt] = d[2];
+        z[2 * mt + 1][2 * nt + 1] = d[3];
+      }
+    float x[32];  // x[8c + i]: coordinate 32c + 8q + i of H (D . x)
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const float s01 = z[0][i] + z[1][i], d01 = z[0][i] - z[1][i];
+      const float s23 = z[2][i] + z[3][i], d23 = z[2][i] - z[3][i];
+      x[i] = s01 + s23;
+      x[8 + i] = d01 + d23;
+      x[16 + i] = s01 - s23;
+      x[24 + i] = d01 - d23;
+    }
     const float inv = zero ? 0.f : 1.0f / nrm;
 
     int idx[32];
@@ -269,17 +337,44 @@ __global__ void __launch_bounds__(256, QJL ? 2 : 3) encode_kernel(const EncodeAr
         x[j] = u - s_cent[idx[j]];  // residual in u units (QJL only)
       }
     }
-    uint32_t w[BITS];
-    pack_codes<BITS>(idx, w);
 
     const int64_t page = ok ? slot / a.P : 0;
     const int64_t off = ok ? slot % a.P : 0;
     uint8_t *slab = a.pool + page * a.page_bytes + (int64_t)h * a.slab_bytes;
     if (ok) {
-      if (a.grouped)
-        store_codes_grouped<BITS>(slab + a.codes_off, off, q, w);
-      else
-        store_codes<BITS>(slab + a.codes_off + off * a.code_bytes + q * 4 * BITS, w);
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        // codes of coordinates 32c + 8q .. +7: 8 * BITS bits, LSB first
+        uint32_t w = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; i++) w |= (uint32_t)idx[8 * c + i] << (BITS * i);
+        uint8_t *dst = a.grouped ? slab + a.codes_off + value_chunk_offset(off, 2 * c + (q >> 1), BITS) + (q & 1) * BITS
+                                 : slab + a.codes_off + off * a.code_bytes + c * 4 * BITS + q * BITS;
+        if constexpr (BITS == 4) {
+          *reinterpret_cast<uint32_t *>(dst) = w;
+        } else if constexpr (BITS == 2) {
+          *reinterpret_cast<uint16_t *>(dst) = (uint16_t)w;
+        } else if (!a.grouped) {
+          // the quad's 4 x 3 bytes are 12 contiguous bytes: lanes 0..2 write
+          // one aligned word each, taking the neighbour's bytes by a shuffle
+          const uint32_t wn = __shfl_down_sync(0xfu << (lane & ~3), w, 1, 4);
+          if (q < 3) *reinterpret_cast<uint32_t *>(dst - q * BITS + 4 * q) = (w >> (8 * q)) | (wn << (24 - 8 * q));
+        } else {
+          // a 6-byte chunk is lanes (2k, 2k+1): the even lane writes it,
+          // 4-byte aligned for even page offsets, 2 bytes past that for odd
+          const uint32_t wn = __shfl_xor_sync(0xfu << (lane & ~3), w, 1);
+          if ((q & 1) == 0) {
+            const uint32_t lo = w | (wn << 24), hi = wn >> 8;  // 48 bits: lo (4 bytes) then hi (2 bytes)
+            if ((off & 1) == 0) {
+              *reinterpret_cast<uint32_t *>(dst) = lo;
+              *reinterpret_cast<uint16_t *>(dst + 4) = (uint16_t)hi;
+            } else {
+              *reinterpret_cast<uint16_t *>(dst) = (uint16_t)lo;
+              *reinterpret_cast<uint32_t *>(dst + 2) = (lo >> 16) | (hi << 16);
+            }
+          }
+        }
+      }
       if (q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nrm;
     }
 
@@ -295,8 +390,8 @@ __global__ void __launch_bounds__(256, QJL ? 2 : 3) encode_kernel(const EncodeAr
       // (S e)_l on the tensor cores: rows g / g+8 of the A operand are the fp16
       // hi / lo parts of this quad's residual (vector g of the warp), B is
       // S hi then S lo, so the fp32 sum misses only the lo*lo term (~2^-22).
-      // k-indices 2t, 2t+1 | 2t+8, 2t+9 of step ks are coordinates
-      // 32t+4ks+{0,1} | +{2,3}: every lane supplies its own slice.
+      // k-indices 2t, 2t+1 | 2t+8, 2t+9 of step ks are the coordinates
+      // 32(ks/2) + 8t + 4(ks%2) + {0,1} | +{2,3}: x[4ks .. 4ks+3] of this lane.
       uint32_t A[8][4];
 #pragma unroll
       for (int ks = 0; ks < 8; ks++) {
