@@ -189,6 +189,11 @@ class DecodeBench:
         page_bytes = tq.tq_page_layout(f)["page_bytes"]
         flat_slots = slots.reshape(-1).to(torch.int32).contiguous()
         self.layers = []
+        # per-step inputs and outputs of all layers in three contiguous device
+        # buffers (q, the appended K and V token, out), so one copy moves them
+        nq, nkv = B * Hq * d, B * H * d  # per layer: [q | new K | new V]
+        self.io_in = torch.empty((wl.layers, nq + 2 * nkv), dtype=torch.float16, device=device)
+        self.io_out = torch.empty((wl.layers, B * Hq * d), dtype=torch.float32, device=device)
         for layer in range(wl.layers):
             pool = torch.zeros(self.num_pages * page_bytes, dtype=torch.uint8, device=device)
             ent = {"pool": pool}
@@ -199,10 +204,13 @@ class DecodeBench:
                              self.kcb if kind == 0 else self.vcb, self.S if kind == 0 else None)
                 del flat
                 ent[name + "win"] = x[:, comp:].permute(0, 2, 1, 3).contiguous() if W else None
-                ent[name + "new"] = x[:, comp - 1].contiguous()  # the token each step re-appends
+                new = self.io_in[layer, nq + kind * nkv: nq + (kind + 1) * nkv].view(B, H, d)
+                new.copy_(x[:, comp - 1])  # the token each step re-appends
+                ent[name + "new"] = new
                 del x
-            ent["q"] = ti.query(B, Hq, d, device=device, seed=ti.SEED_QUERY + 7919 * layer)
-            ent["out"] = torch.empty(B, Hq, d, dtype=torch.float32, device=device)
+            ent["q"] = self.io_in[layer, :nq].view(B, Hq, d)
+            ent["q"].copy_(ti.query(B, Hq, d, device=device, seed=ti.SEED_QUERY + 7919 * layer))
+            ent["out"] = self.io_out[layer].view(B, Hq, d)
             self.layers.append(ent)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()  # generation temporaries go back to the driver
@@ -339,14 +347,21 @@ def load_traffic(kernel: str, workload: str):
     return rec.get("dram_bytes_per_launch")
 
 
+# Sources the split-KV main attention kernel is compiled from: a change in
+# any of them invalidates its recorded DRAM traffic.
+ATTN_MAIN_SOURCES = ("tq_attn_main.cuh", "tq_attn_k2.cu", "tq_attn_k3.cu", "tq_attn_k4.cu", "tq_internal.cuh", "tq_device.cuh")
+
+
 def kernel_source_hash() -> str:
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_tq_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
+    for n in ATTN_MAIN_SOURCES:
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "tq.h"), "rb") as f:
+        h.update(b"tq.h" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -401,29 +416,40 @@ def run_encode(args, device):
 
 
 # ------------------------------------------------------------------- e2e --
-def run_e2e(args, bench: DecodeBench):
+def run_e2e(args, bench: DecodeBench, graph: bool = True):
     """Same step through the public API with host buffers: every step copies
-    each layer's query and appended K/V token from pinned host memory and
-    reads each layer's output back, inside the timed region."""
-    host_q = [L["q"].cpu().pin_memory() for L in bench.layers]
-    host_k = [L["knew"].cpu().pin_memory() for L in bench.layers]
-    host_v = [L["vnew"].cpu().pin_memory() for L in bench.layers]
-    host_o = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in bench.layers]
-    h2d = sum(t.numel() * t.element_size() for t in host_q + host_k + host_v)
-    d2h = sum(t.numel() * t.element_size() for t in host_o)
+    all layers' queries and appended K/V tokens from pinned host memory (one
+    copy) and reads all layers' outputs back (one copy), inside the timed
+    region.  Like the device-resident step it is replayed as a CUDA graph."""
+    host_in = bench.io_in.cpu().pin_memory()
+    host_out = torch.empty_like(bench.io_out, device="cpu").pin_memory()
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = host_out.numel() * host_out.element_size()
 
     def step():
-        for i, L in enumerate(bench.layers):
-            L["q"].copy_(host_q[i], non_blocking=True)
-            L["knew"].copy_(host_k[i], non_blocking=True)
-            L["vnew"].copy_(host_v[i], non_blocking=True)
+        bench.io_in.copy_(host_in, non_blocking=True)
         bench.step()
-        for i, L in enumerate(bench.layers):
-            host_o[i].copy_(L["out"], non_blocking=True)
+        host_out.copy_(bench.io_out, non_blocking=True)
 
-    ms = time_steps(step, args.steps, args.warmup, lambda: None)
+    run = step
+    if graph:
+        step()
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        torch.cuda.synchronize()
+        run = g.replay
+    ms = time_steps(run, args.steps, args.warmup, lambda: None)
     value = bench.wl.batch * bench.wl.layers * bench.wl.context / (ms * 1e-3)
-    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+    out_ok = bool(torch.isfinite(host_out).all())
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "cuda_graph": graph, "outputs_finite": out_ok}
 
 
 # --------------------------------------------------------------- oracle --
@@ -586,7 +612,7 @@ def main():
         return
     res, bench = run_decode(args, device, barrier, reduce_max, rank, world)
     if not args.no_e2e:
-        e2e = run_e2e(args, bench)
+        e2e = run_e2e(args, bench, graph=not args.no_graph)
         e2e_ms = reduce_max(e2e["ms_per_step"])
         e2e["value"] = job_throughput(bench.wl.batch * bench.wl.layers * bench.wl.context, e2e_ms, world)
         res["e2e"] = e2e
