@@ -117,7 +117,12 @@ __device__ void prep_query(const AttnArgs &a, bool qjl, int64_t row, int lane, f
 // (1) scores, four threads per token (32 coordinates each);
 // (2) per-head max / exp / sum, one warp per head, lane = token;
 // (3) values, thread = coordinate.
-__device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float (*s_q)[kD], float (*s_p)[kWinChunk]) {
+// Window queries in shared memory: head g, coordinate c at g * kQRow +
+// (c / 32) * 34 + c % 32, so the four 32-coordinate parts read by the four
+// threads of a token start in different banks (and stay 8-byte aligned).
+constexpr int kQPart = 34, kQRow = 4 * kQPart;
+
+__device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, float (*s_p)[kWinChunk]) {
   const int b = (int)(unit / a.H), h = (int)(unit % a.H);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
@@ -126,7 +131,8 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float (*s_q)
   const int t0 = c * kWinChunk;
   const int n = min(kWinChunk, wl - t0);
   if (n <= 0) return;  // block-uniform
-  for (int i = tid; i < G * kD; i += blockDim.x) s_q[i / kD][i % kD] = __half2float(a.q[((int64_t)b * a.Hq + h * G) * kD + i]);
+  for (int i = tid; i < G * kD; i += blockDim.x)
+    s_q[(i / kD) * kQRow + ((i % kD) >> 5) * kQPart + (i & 31)] = __half2float(a.q[((int64_t)b * a.Hq + h * G) * kD + i]);
   __syncthreads();
   const __half *kbase = a.k_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
   const __half *vbase = a.v_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
@@ -152,7 +158,10 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float (*s_q)
           const int cc = 32 * part + 8 * k + 2 * e;
 #pragma unroll
           for (int g = 0; g < 8; g++)
-            if (g < G) acc[g] = fmaf(f.x, s_q[g][cc], fmaf(f.y, s_q[g][cc + 1], acc[g]));
+            if (g < G) {
+              const float2 qq = *reinterpret_cast<const float2 *>(s_q + g * kQRow + part * kQPart + (cc & 31));
+              acc[g] = fmaf(f.x, qq.x, fmaf(f.y, qq.y, acc[g]));
+            }
         }
       }
     }
@@ -195,7 +204,7 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float (*s_q)
 }
 
 __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool qjl, int row_blocks) {
-  __shared__ float s_q[8][kD];
+  __shared__ __align__(16) float s_q[8 * kQRow];
   __shared__ float s_p[8][kWinChunk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (blockIdx.x >= row_blocks) {  // window chunk blocks
@@ -206,7 +215,7 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
   }
   if (blockIdx.x == 0 && warp == 0) prep_lengths(a, lane);
   const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // b * Hq + qh
-  if (row < (int64_t)a.B * a.Hq) prep_query(a, qjl, row, lane, s_q[warp]);
+  if (row < (int64_t)a.B * a.Hq) prep_query(a, qjl, row, lane, s_q + warp * kQRow);
 }
 
 // Warp that owns tile x: largest w in [0, NW) with floor(T*w/NW) <= x.
@@ -284,6 +293,18 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
   const int64_t T = a.hdr->total_tiles, NW = a.hdr->active_warps;
   float mu = -INFINITY, l = 0.f, A = 0.f;
   const int64_t tb = a.pre[b + 1] - a.pre[b];
+  // the window partials do not depend on the compressed merge: their loads
+  // are issued first (up to kWinPre chunks; longer windows read them later)
+  constexpr int kWinPre = 8;
+  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
+  const int64_t nwin = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
+  float wacc[kWinPre];
+  float2 wml = make_float2(-INFINITY, 0.f);
+  if (nwin <= kWinPre) {
+#pragma unroll
+    for (int i = 0; i < kWinPre; i++) wacc[i] = i < nwin ? a.win_acc[(row * nch + i) * kD + j] : 0.f;
+    if (j < nwin) wml = make_float2(a.win_ml[(row * nch + j) * 2], a.win_ml[(row * nch + j) * 2 + 1]);
+  }
   if (tb > 0 && NW > 0) {
     const int64_t o = a.H * a.pre[b] + h * tb;
     const int64_t w0 = tile_owner(o, T, NW), w1 = tile_owner(o + tb - 1, T, NW);
@@ -317,12 +338,21 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
 
   // window partials (raw domain): merged onto the compressed part
   float M = mu, Lt = l, At = x;
-  if (a.window > 0) {
-    const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
-    const int wl = a.wlen[b];
-    const int64_t n = (wl + kWinChunk - 1) / kWinChunk;
+  if (nwin > 0 && nwin <= kWinPre) {
+    const float Mn = fmaxf(M, block_max128(wml.x, s_red));
+    const float w = wml.x == -INFINITY ? 0.f : exp2f(wml.x - Mn);
+    if (j < kWinPre) s_w[j] = w;
+    const float lsum = block_sum128(wml.y * w, s_red);  // also publishes s_w
+    const float sold = exp2f(M - Mn);
+    float aw = 0.f;
+#pragma unroll
+    for (int i = 0; i < kWinPre; i++) aw = fmaf(s_w[i], wacc[i], aw);
+    At = At * sold + aw;
+    Lt = Lt * sold + lsum;
+    M = Mn;
+  } else if (nwin > kWinPre) {
     merge_partials(
-        n, [&](int64_t k) { return make_float2(a.win_ml[(row * nch + k) * 2], a.win_ml[(row * nch + k) * 2 + 1]); },
+        nwin, [&](int64_t k) { return make_float2(a.win_ml[(row * nch + k) * 2], a.win_ml[(row * nch + k) * 2 + 1]); },
         [&](int64_t k) { return a.win_acc + (row * nch + k) * kD; }, M, Lt, At, s_w, s_red);
   }
   a.out[row * kD + j] = (M != -INFINITY && Lt > 0.f) ? At / Lt : 0.f;
