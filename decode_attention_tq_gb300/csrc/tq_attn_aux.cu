@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
         w1 - w0 + 1,
         [&](int64_t k) {
           const int64_t w = w0 + k;
-          if (T * w / NW >= T * (w + 1) / NW) return make_float2(-INFINITY, 0.f);  // empty range
+          // a warp's range can only be empty when there are fewer tiles than warps
+          if (T < NW && T * w / NW >= T * (w + 1) / NW) return make_float2(-INFINITY, 0.f);
           const int64_t base = (w + unit) * a.G + g;
           return make_float2(a.seg_ml[base * 2], a.seg_ml[base * 2 + 1]);
         },
