@@ -371,10 +371,20 @@ template <int KB>
 __host__ __device__ constexpr uint32_t attn_stage_off() {
   return kKeyTableOff + (uint32_t(1) << (2 * KB)) * 256;
 }
-// Per warp: two stages, then two 8-byte mbarriers.
+// Stages of the per-warp ring (TQ_TMA_STAGING=1).
+#ifndef TQ_TMA_STAGES
+#define TQ_TMA_STAGES 2
+#endif
+constexpr int kStages = TQ_TMA_STAGES;
+// Per warp: kStages stages of (tile, 16-byte slot holding the tile's live
+// token count), then kStages 8-byte mbarriers, padded to 16 bytes.
+template <int KB, int VB, bool QJL>
+__host__ __device__ constexpr uint32_t attn_stage_stride() {
+  return Stage<KB, VB, QJL>::bytes + 16;
+}
 template <int KB, int VB, bool QJL>
 __host__ __device__ constexpr uint32_t attn_warp_stage_bytes() {
-  return 2 * Stage<KB, VB, QJL>::bytes + 16;
+  return (kStages * attn_stage_stride<KB, VB, QJL>() + 8 * kStages + 15) / 16 * 16;
 }
 template <int KB, int VB, bool QJL, int NT>
 constexpr size_t attn_smem_bytes() {
@@ -419,17 +429,18 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 #if TQ_TMA_STAGING
   using SL = Stage<KB, VB, QJL>;
   const uint32_t wst_off = attn_stage_off<KB>() + (threadIdx.x >> 5) * attn_warp_stage_bytes<KB, VB, QJL>();
-  const uint8_t *wst = smem + wst_off;  // this warp's two stages
+  constexpr uint32_t kStride = attn_stage_stride<KB, VB, QJL>();
+  uint8_t *wst = smem + wst_off;  // this warp's ring
   const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(smem) + wst_off;
-  const uint32_t bar0 = wst_s + 2 * SL::bytes;
+  const uint32_t bar0 = wst_s + kStages * kStride;
   if (lane == 0) {
-    mbar_init(bar0, 1);
-    mbar_init(bar0 + 8, 1);
+#pragma unroll
+    for (int i = 0; i < kStages; i++) mbar_init(bar0 + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");  // visible to the bulk-copy unit
     fence_proxy_async_smem();
   }
   __syncwarp();
-  uint32_t gk = 0;  // tiles this warp has consumed: stage gk & 1, phase parity (gk >> 1) & 1
+  uint32_t gk = 0;  // tiles this warp has consumed: stage gk % kStages, phase parity (gk / kStages) & 1
 #endif
   const int H = a.H, G = a.G, Hq = a.Hq;
   const int tpp = a.P >> 4;
@@ -695,13 +706,13 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
     using VR = ValRegs<VB>;
 #if TQ_TMA_STAGING
     // Lane 0 copies the tile under the cursor into stage s (or, for a page
-    // outside the pool, only arrives so the phase still completes).
-    int live_s0 = 0, live_s1 = 0;
+    // outside the pool, only arrives so the phase still completes) and notes
+    // the tile's live token count in the stage's slot.
     auto issue = [&](uint32_t s) {
       const int live = cur.live();
-      if (s) live_s1 = live; else live_s0 = live;
       if (lane == 0) {
-        const uint32_t bar = bar0 + 8 * s, dst = wst_s + s * SL::bytes;
+        const uint32_t bar = bar0 + 8 * s, dst = wst_s + s * kStride;
+        *reinterpret_cast<int *>(wst + s * kStride + SL::bytes) = live;
         if (cur.page_ok) {
           mbar_arrive_expect_tx(bar, SL::bytes);
           bulk_g2s(dst + SL::kc, cur.slab + a.k_codes_o + (int64_t)cur.o0 * (16 * KB), 16 * 16 * KB, bar);
@@ -717,26 +728,33 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         }
       }
     };
-    __syncwarp();  // stage gk & 1 was last read two tiles ago
+    // prologue: the first kStages - 1 tiles of the segment; their stages were
+    // last read at least one tile ago
+    const int ahead = kStages - 1 < seg_tiles ? kStages - 1 : seg_tiles;
+    __syncwarp();
     if (lane == 0) fence_proxy_async_smem();
-    issue(gk & 1);
+    for (int i = 0; i < ahead; i++) {
+      if (i) step_cursor();
+      issue((gk + i) % kStages);
+    }
     for (int k = 0; k < seg_tiles; k++, gk++) {
-      const uint32_t s = gk & 1;
-      if (k + 1 < seg_tiles) {  // the other stage was read by the previous tile, now finished
+      const uint32_t s = gk % kStages;
+      if (k + kStages - 1 < seg_tiles) {  // the stage of tile k - 1, now finished
         step_cursor();
         __syncwarp();
         if (lane == 0) fence_proxy_async_smem();
-        issue(s ^ 1);
+        issue((gk + kStages - 1) % kStages);
       }
-      if (!mbar_wait_bounded(bar0 + 8 * s, (gk >> 1) & 1)) {
+      if (!mbar_wait_bounded(bar0 + 8 * s, (gk / kStages) & 1)) {
         if (lane == 0) report(a.err_word, TQ_DEVERR_TIMEOUT);
-        if (k + 1 < seg_tiles) mbar_wait_bounded(bar0 + 8 * (s ^ 1), ((gk + 1) >> 1) & 1);  // own copy in flight
+        for (int i = 1; i < kStages; i++)  // own copies still in flight
+          if (k + i < seg_tiles) mbar_wait_bounded(bar0 + 8 * ((gk + i) % kStages), ((gk + i) / kStages) & 1);
         return;
       }
-      const uint8_t *st = wst + s * SL::bytes;
+      const uint8_t *st = wst + s * kStride;
       KR ka;
       VR va;
-      lds_keys<KB, VB, QJL>(st, s ? live_s1 : live_s0, r, t, ka);
+      lds_keys<KB, VB, QJL>(st, *reinterpret_cast<const int *>(st + SL::bytes), r, t, ka);
       lds_values<KB, VB, QJL>(st, r, t, va);
       process(ka, va);
     }

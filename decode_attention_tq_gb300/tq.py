@@ -16,7 +16,8 @@ import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtq.so")
+# the in-tree build; TQ_LIBRARY may name another build of the same sources
+LIB_PATH = os.environ.get("TQ_LIBRARY") or os.path.join(_HERE, "libtq.so")
 
 TQ_KIND_K = 0
 TQ_KIND_V = 1
