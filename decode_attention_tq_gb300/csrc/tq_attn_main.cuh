@@ -367,9 +367,15 @@ struct TileCursor {
 // (table offset | pair code << 8 | lane slot), one prmt / lop3, and each lane
 // reads its own bank.
 constexpr uint32_t kValTableOff = 0, kKeyTableOff = 65536;
+// 2-bit keys use a key table indexed by a code byte (two pairs, 128 KB);
+// builds with the staging ring keep the pair-indexed table to leave room.
+template <int KB>
+__host__ __device__ constexpr bool byte_keys() {
+  return KB == 2 && !TQ_TMA_STAGING;
+}
 template <int KB>
 __host__ __device__ constexpr uint32_t attn_stage_off() {
-  return kKeyTableOff + (uint32_t(1) << (2 * KB)) * 256;
+  return kKeyTableOff + (byte_keys<KB>() ? 2u * 256 * 256 : (uint32_t(1) << (2 * KB)) * 256);
 }
 // Stages of the per-warp ring (TQ_TMA_STAGING=1).
 #ifndef TQ_TMA_STAGES
@@ -395,6 +401,7 @@ template <int KB, int VB, bool QJL, int NT>
 __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(const AttnArgs a) {
   constexpr int EK = 1 << (2 * KB), EV = 1 << (2 * VB);
   static_assert(EV * 256 <= (int)kKeyTableOff, "table sizes");
+  static_assert(attn_stage_off<KB>() <= 232448, "tables above the shared-memory limit");
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t *lutV = reinterpret_cast<uint32_t *>(smem + kValTableOff);  // [EV][64], lanes in the first 32
   uint2 *lutK = reinterpret_cast<uint2 *>(smem + kKeyTableOff);        // [EK][32] (hi, lo)
@@ -403,17 +410,34 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   auto lut32 = [&](uint32_t off) { return *reinterpret_cast<const uint32_t *>(smem + off); };
 
   // Bank-private centroid-pair tables: lane l reads its own copy in bank l.
-  for (int i = threadIdx.x; i < EK * 32; i += blockDim.x) {
-    const int e = i >> 5;
+  auto key_pair = [&](int e) {  // (hi pair, lo pair) of the code pair e
     __half h0, l0, h1, l1;
     split_half(__ldg(a.k_cb + (e & ((1 << KB) - 1))) * kCentScale, h0, l0);
     split_half(__ldg(a.k_cb + (e >> KB)) * kCentScale, h1, l1);
-    lutK[i] = make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(l0, l1));
+    return make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(l0, l1));
+  };
+  auto val_pair = [&](int e) {
+    return pack_half2(__ldg(a.v_cb + (e & ((1 << VB) - 1))) * kCentScale, __ldg(a.v_cb + (e >> VB)) * kCentScale);
+  };
+  if constexpr (byte_keys<KB>()) {
+    // 2-bit keys: indexed by a code byte (two pairs), entry halves 64 KB apart
+    for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
+      const int e = i >> 5;
+      lutK[i] = key_pair(e & 15);
+      lutK[i + 256 * 32] = key_pair(e >> 4);
+    }
+  } else {
+    for (int i = threadIdx.x; i < EK * 32; i += blockDim.x) lutK[i] = key_pair(i >> 5);
   }
-  for (int i = threadIdx.x; i < EV * 32; i += blockDim.x) {
-    const int e = i >> 5;
-    lutV[e * 64 + (i & 31)] =
-        pack_half2(__ldg(a.v_cb + (e & ((1 << VB) - 1))) * kCentScale, __ldg(a.v_cb + (e >> VB)) * kCentScale);
+  if constexpr (VB == 2) {
+    // 2-bit values: indexed by a byte of the interleaved codes (two coordinates)
+    uint2 *lutV2 = reinterpret_cast<uint2 *>(smem + kValTableOff);
+    for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
+      const int e = i >> 5;
+      lutV2[i] = make_uint2(val_pair(e & 15), val_pair(e >> 4));
+    }
+  } else {
+    for (int i = threadIdx.x; i < EV * 32; i += blockDim.x) lutV[(i >> 5) * 64 + (i & 31)] = val_pair(i >> 5);
   }
   __syncthreads();
 
@@ -425,7 +449,7 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   const int64_t ts = T * wg / NW, te = T * (wg + 1) / NW;
   if (ts >= te) return;
   const uint32_t laneK = kKeyTableOff | ((uint32_t)lane * 8u);
-  const uint32_t laneV = kValTableOff | ((uint32_t)lane * 4u);
+  const uint32_t laneV = kValTableOff | ((uint32_t)lane * (VB == 2 ? 8u : 4u));
 #if TQ_TMA_STAGING
   using SL = Stage<KB, VB, QJL>;
   const uint32_t wst_off = attn_stage_off<KB>() + (threadIdx.x >> 5) * attn_warp_stage_bytes<KB, VB, QJL>();
@@ -566,10 +590,20 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         for (int i = 0; i < 4; i++) { sa[nt][i] = 0.f; sbk[nt][i] = 0.f; sq[nt][i] = 0.f; }
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) {
-        const uint2 L00 = lut64(key_addr<KB>(R.k0, 2 * kk, laneK));
-        const uint2 L01 = lut64(key_addr<KB>(R.k0, 2 * kk + 1, laneK));
-        const uint2 L10 = lut64(key_addr<KB>(R.k1, 2 * kk, laneK));
-        const uint2 L11 = lut64(key_addr<KB>(R.k1, 2 * kk + 1, laneK));
+        uint2 L00, L01, L10, L11;
+        if constexpr (byte_keys<KB>()) {  // byte kk = pairs 2kk (low nibble), 2kk+1: one address, halves 64 KB apart
+          const uint32_t a0 = __byte_perm(R.k0[kk >> 2], laneK, 0x7604 | ((kk & 3) << 4));
+          const uint32_t a1 = __byte_perm(R.k1[kk >> 2], laneK, 0x7604 | ((kk & 3) << 4));
+          L00 = lut64(a0);
+          L01 = lut64(a0 + 65536);
+          L10 = lut64(a1);
+          L11 = lut64(a1 + 65536);
+        } else {
+          L00 = lut64(key_addr<KB>(R.k0, 2 * kk, laneK));
+          L01 = lut64(key_addr<KB>(R.k0, 2 * kk + 1, laneK));
+          L10 = lut64(key_addr<KB>(R.k1, 2 * kk, laneK));
+          L11 = lut64(key_addr<KB>(R.k1, 2 * kk + 1, laneK));
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) {
           mma_16816(sa[nt], L00.x, L00.y, L01.x, L01.y, qb[nt][kk][0], qb[nt][kk][1]);
@@ -666,6 +700,27 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
           }
         }
       }
+      if constexpr (VB == 2) {
+        // byte m of ev[tp][eo] holds the pairs of coordinates 4m + eo and
+        // 4m + 2 + eo, i.e. m-tiles 2m and 2m+1: one 8-byte read serves both
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+          uint32_t av0[4], av1[4];
+#pragma unroll
+          for (int tp = 0; tp < 2; tp++)
+#pragma unroll
+            for (int eo = 0; eo < 2; eo++) {
+              const uint2 pr = lut64(__byte_perm(ev[tp][eo][0], laneV, 0x7604 | (m << 4)));
+              av0[2 * tp + eo] = pr.x;
+              av1[2 * tp + eo] = pr.y;
+            }
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) {
+            mma_16816(acc[2 * m][nt], av0[0], av0[1], av0[2], av0[3], wb[nt][0], wb[nt][1]);
+            mma_16816(acc[2 * m + 1][nt], av1[0], av1[1], av1[2], av1[3], wb[nt][0], wb[nt][1]);
+          }
+        }
+      } else {
 #pragma unroll
       for (int mt = 0; mt < 8; mt++) {
         uint32_t av[4];  // (tokens 2t,2t+1 | 2t+8,2t+9) x (coordinate 16r+2mt | 16r+2mt+1)
@@ -688,6 +743,7 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         }
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) mma_16816(acc[mt][nt], av[0], av[1], av[2], av[3], wb[nt][0], wb[nt][1]);
+      }
       }
     };
 
