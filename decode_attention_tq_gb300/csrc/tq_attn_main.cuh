@@ -21,7 +21,8 @@
 //        exact in fp16;
 //   online softmax in fp32 (log2 domain);
 //   acc[128 x 2G] += Vcodes^T[128 x 16] * W[16 x 2G], W = p_i * n_i / nu
-//        (nu = running max value norm) split hi/lo over the columns; the
+//        (nu = running max value norm) in fp16 in the even columns (the odd
+//        ones, the query's lo columns on the key side, are zero here); the
 //        value table maps a pair of codes to a pair of centroids, so the codes
 //        of the two tokens an A register pairs are interleaved and looked up
 //        once.
@@ -664,16 +665,13 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         const float p0 = fast_exp2(lg0[nt] - mu[nt]), p1 = fast_exp2(lg1[nt] - mu[nt]);
         lsum[nt] += p0 + p1;
         const float w0 = p0 * vn0 * inv_nu, w1 = p1 * vn1 * inv_nu;
-        __half wh0, wl0, wh1, wl1;
-        split_half(w0, wh0, wl0);
-        split_half(w1, wh1, wl1);
-        const uint32_t Wh = pack_half2_raw(wh0, wh1), Wl = pack_half2_raw(wl0, wl1);
-        // B operand column r = (head 4nt + r/2, hi or lo): weights of tokens
+        // B operand column r = (head 4nt + r/2, even r only): weights of tokens
         // 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) from the lanes that own them
+        const uint32_t Wh = pack_half2(w0, w1);
         const int src0 = 4 * (2 * t) + (r >> 1), src1 = src0 + 4;
-        const uint32_t h0 = __shfl_sync(0xffffffffu, Wh, src0), q0 = __shfl_sync(0xffffffffu, Wl, src0);
-        const uint32_t h1 = __shfl_sync(0xffffffffu, Wh, src1), q1 = __shfl_sync(0xffffffffu, Wl, src1);
-        const uint32_t x0 = (r & 1) ? q0 : h0, x1 = (r & 1) ? q1 : h1;
+        const uint32_t h0 = __shfl_sync(0xffffffffu, Wh, src0);
+        const uint32_t h1 = __shfl_sync(0xffffffffu, Wh, src1);
+        const uint32_t x0 = (r & 1) ? 0u : h0, x1 = (r & 1) ? 0u : h1;
         wb[nt][0] = __byte_perm(x0, x1, 0x5410);
         wb[nt][1] = __byte_perm(x0, x1, 0x7632);
       }
