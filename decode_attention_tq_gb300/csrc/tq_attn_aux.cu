@@ -122,6 +122,8 @@ __device__ void prep_query(const AttnArgs &a, bool qjl, int64_t row, int lane, f
 // threads of a token start in different banks (and stay 8-byte aligned).
 constexpr int kQPart = 34, kQRow = 4 * kQPart;
 
+// GM: 4 or 8, the largest head count the unrolled loops cover (G <= GM).
+template <int GM>
 __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, float (*s_p)[kWinChunk]) {
   const int b = (int)(unit / a.H), h = (int)(unit % a.H);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -131,24 +133,29 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
   const int t0 = c * kWinChunk;
   const int n = min(kWinChunk, wl - t0);
   if (n <= 0) return;  // block-uniform
-  for (int i = tid; i < G * kD; i += blockDim.x)
-    s_q[(i / kD) * kQRow + ((i % kD) >> 5) * kQPart + (i & 31)] = __half2float(a.q[((int64_t)b * a.Hq + h * G) * kD + i]);
-  __syncthreads();
   const __half *kbase = a.k_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
   const __half *vbase = a.v_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
-  // this thread's coordinate of every value row, loaded up front so the
-  // loads are in flight during the score phase
+  // every load of the block is issued before the first barrier: this
+  // thread's key row part (token tid/4, coordinates 32 (tid%4) ..) and its
+  // coordinate of every value row
+  const int i = tid >> 2, part = tid & 3;
+  uint4 raw[4] = {};
+  if (i < n) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(kbase + (int64_t)i * kD + 32 * part);
+#pragma unroll
+    for (int k = 0; k < 4; k++) raw[k] = src[k];
+  }
   __half vrow[kWinChunk];
 #pragma unroll
-  for (int i = 0; i < kWinChunk; i++) vrow[i] = i < n ? vbase[(int64_t)i * kD + tid] : __float2half(0.f);
+  for (int k = 0; k < kWinChunk; k++) vrow[k] = k < n ? vbase[(int64_t)k * kD + tid] : __float2half(0.f);
+  for (int e = tid; e < G * kD; e += blockDim.x)
+    s_q[(e / kD) * kQRow + ((e % kD) >> 5) * kQPart + (e & 31)] = __half2float(a.q[((int64_t)b * a.Hq + h * G) * kD + e]);
+  __syncthreads();
   {  // (1) scores
-    const int i = tid >> 2, part = tid & 3;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (i < n) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(kbase + (int64_t)i * kD + 32 * part);
-      uint4 raw[4];
+    float acc[GM];
 #pragma unroll
-      for (int k = 0; k < 4; k++) raw[k] = src[k];
+    for (int g = 0; g < GM; g++) acc[g] = 0.f;
+    if (i < n) {
 #pragma unroll
       for (int k = 0; k < 4; k++) {
         const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
@@ -157,7 +164,7 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
           const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
           const int cc = 32 * part + 8 * k + 2 * e;
 #pragma unroll
-          for (int g = 0; g < 8; g++)
+          for (int g = 0; g < GM; g++)
             if (g < G) {
               const float2 qq = *reinterpret_cast<const float2 *>(s_q + g * kQRow + part * kQPart + (cc & 31));
               acc[g] = fmaf(f.x, qq.x, fmaf(f.y, qq.y, acc[g]));
@@ -167,7 +174,7 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
     }
     const float sscale = kLog2e * 0.08838834764831845f;  // log2(e)/sqrt(d)
 #pragma unroll
-    for (int g = 0; g < 8; g++) {
+    for (int g = 0; g < GM; g++) {
       float v = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], 1);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       if (g < G && part == 0 && i < n) s_p[g][i] = v * sscale;
@@ -189,16 +196,18 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
   }
   __syncthreads();
   {  // (3) values (s_p is 0 past n)
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float acc[GM];
 #pragma unroll
-    for (int i = 0; i < kWinChunk; i++) {
-      const float v = __half2float(vrow[i]);
+    for (int g = 0; g < GM; g++) acc[g] = 0.f;
 #pragma unroll
-      for (int g = 0; g < 8; g++)
-        if (g < G) acc[g] = fmaf(s_p[g][i], v, acc[g]);
+    for (int k = 0; k < kWinChunk; k++) {
+      const float v = __half2float(vrow[k]);
+#pragma unroll
+      for (int g = 0; g < GM; g++)
+        if (g < G) acc[g] = fmaf(s_p[g][k], v, acc[g]);
     }
 #pragma unroll
-    for (int g = 0; g < 8; g++)
+    for (int g = 0; g < GM; g++)
       if (g < G) a.win_acc[(((int64_t)b * a.Hq + h * G + g) * nch + c) * kD + tid] = acc[g];
   }
 }
@@ -210,7 +219,10 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
   if (blockIdx.x >= row_blocks) {  // window chunk blocks
     const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
     const int64_t k = blockIdx.x - row_blocks;
-    prep_window(a, k / nch, (int)(k % nch), s_q, s_p);
+    if (a.G <= 4)
+      prep_window<4>(a, k / nch, (int)(k % nch), s_q, s_p);
+    else
+      prep_window<8>(a, k / nch, (int)(k % nch), s_q, s_p);
     return;
   }
   if (blockIdx.x == 0 && warp == 0) prep_lengths(a, lane);
@@ -220,7 +232,8 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
 
 // Warp that owns tile x: largest w in [0, NW) with floor(T*w/NW) <= x.
 __device__ __forceinline__ int64_t tile_owner(int64_t x, int64_t T, int64_t NW) {
-  const int64_t w = (NW * (x + 1) + T - 1) / T - 1;
+  const int64_t num = NW * (x + 1) + T - 1;
+  const int64_t w = (num <= 0xffffffffll ? (int64_t)((uint32_t)num / (uint32_t)T) : num / T) - 1;  // 32-bit when it fits
   return w < NW - 1 ? w : NW - 1;
 }
 
