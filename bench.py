@@ -5,7 +5,7 @@ Default workload (N=1): Llama-3-8B-shaped decode, 32 layers, batch 16,
 32 query / 8 KV heads, d = 128, context 32768 per sequence (32640 compressed
 4-bit K / 4-bit V tokens in 64-token pages with a random page permutation,
 plus a 128-token fp16 window).  One step = for every layer: append one token
-per sequence into the packed pages (tq_encode of K and V) and one decode
+per sequence into the packed pages (tq_encode_kv) and one decode
 attention over the whole cache (tq_decode_attn).  The 32 layers' caches
 (18.5 GB) are resident in HBM before timing; the working set is far larger
 than L2, so no flush is needed between iterations.
@@ -220,13 +220,14 @@ class DecodeBench:
         self.main_bytes = B * H * comp * (bph["k"] + bph["v"]) + B * self.pages_per_seq * 4  # per layer launch
         self.window_bytes = B * H * wl.win_tokens * d * 2 * 2
         self.step_bytes = wl.layers * (self.main_bytes + self.window_bytes + B * Hq * d * (2 + 4))
-        self.launches_per_step = wl.layers * (2 + 3)  # 2 appends + prep (with window chunks), main, merge
+        appends = 1 if (f.k_bits == f.v_bits and not f.k_qjl) else 2  # tq_encode_kv: one joint launch or K then V
+        self.launches_per_step = wl.layers * (appends + 3)  # appends + prep (with window chunks), main, merge
 
     def step(self, events=None):
         tq, f = self.tq, self.fmt
         for i, L in enumerate(self.layers):
-            tq.tq_encode(f, 0, L["knew"], self.append_slots, L["pool"], self.num_pages, self.ks, self.kcb, self.S, err_word=self.err)
-            tq.tq_encode(f, 1, L["vnew"], self.append_slots, L["pool"], self.num_pages, self.vs, self.vcb, None, err_word=self.err)
+            tq.tq_encode_kv(f, L["knew"], L["vnew"], self.append_slots, L["pool"], self.num_pages, self.ks, self.vs, self.kcb,
+                            self.vcb, self.S, err_word=self.err)
             args = (f, L["q"], L["pool"], self.num_pages, self.bt, self.comp_lens, L["kwin"], L["vwin"], self.win_lens if self.W else None,
                     self.ks, self.vs, self.kcb, self.vcb, self.S, L["out"], self.ws)
             if events is None:

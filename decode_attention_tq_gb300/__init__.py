@@ -20,6 +20,7 @@ from .tq import (  # noqa: F401
     tq_decode_attn_timed,
     tq_decode_attn_workspace_size,
     tq_encode,
+    tq_encode_kv,
     tq_make_codebook,
     tq_page_layout,
     tq_status_string,

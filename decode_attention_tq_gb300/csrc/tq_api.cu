@@ -227,9 +227,9 @@ tq_status tq_page_layout(const tq_format *fmt, tq_layout *out) {
   return TQ_OK;
 }
 
-tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n_tokens, const int32_t *slot_mapping,
-                    void *page_pool, int64_t num_pages, const uint8_t *signs, const float *codebook, const float *S,
-                    int32_t *err_word, void *stream) {
+static tq_status encode_args(const tq_format *fmt, int kind, const void *x_f16, int64_t n_tokens,
+                             const int32_t *slot_mapping, void *page_pool, int64_t num_pages, const uint8_t *signs,
+                             const float *codebook, const float *S, int32_t *err_word, EncodeArgs *a) {
   if (!format_valid(fmt) || (kind != TQ_KIND_K && kind != TQ_KIND_V) || n_tokens < 0 || num_pages < 1)
     return TQ_ERR_INVALID_ARG;
   if (!format_gpu_supported(fmt)) return TQ_ERR_UNSUPPORTED;
@@ -238,33 +238,63 @@ tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n
   if (!aligned(x_f16, 16) || !aligned(page_pool, 16) || !aligned(slot_mapping, 4) || !aligned(codebook, 4) ||
       (qjl && !aligned(S, 16)))
     return TQ_ERR_INVALID_ARG;
-  if (n_tokens == 0) return TQ_OK;
   tq_layout L;
   compute_layout(fmt, &L);
+  a->x = static_cast<const __half *>(x_f16);
+  a->n_tokens = n_tokens;
+  a->H = fmt->num_kv_heads;
+  a->P = fmt->page_size;
+  a->slot_mapping = slot_mapping;
+  a->pool = static_cast<uint8_t *>(page_pool);
+  a->num_pages = num_pages;
+  a->page_bytes = L.page_bytes;
+  a->slab_bytes = L.slab_bytes;
+  a->norm_off = kind == TQ_KIND_K ? L.k_norm : L.v_norm;
+  a->codes_off = kind == TQ_KIND_K ? L.k_codes : L.v_codes;
+  a->gamma_off = L.k_gamma;
+  a->signs_off = L.k_signs;
+  a->code_bytes = kind == TQ_KIND_K ? L.k_code_bytes : L.v_code_bytes;
+  a->grouped = kind == TQ_KIND_V;
+  a->signs = signs;
+  a->codebook = codebook;
+  a->S = S;
+  a->err_word = err_word;
+  return TQ_OK;
+}
+
+tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n_tokens, const int32_t *slot_mapping,
+                    void *page_pool, int64_t num_pages, const uint8_t *signs, const float *codebook, const float *S,
+                    int32_t *err_word, void *stream) {
   EncodeArgs a;
-  a.x = static_cast<const __half *>(x_f16);
-  a.n_tokens = n_tokens;
-  a.H = fmt->num_kv_heads;
-  a.P = fmt->page_size;
-  a.slot_mapping = slot_mapping;
-  a.pool = static_cast<uint8_t *>(page_pool);
-  a.num_pages = num_pages;
-  a.page_bytes = L.page_bytes;
-  a.slab_bytes = L.slab_bytes;
-  a.norm_off = kind == TQ_KIND_K ? L.k_norm : L.v_norm;
-  a.codes_off = kind == TQ_KIND_K ? L.k_codes : L.v_codes;
-  a.gamma_off = L.k_gamma;
-  a.signs_off = L.k_signs;
-  a.code_bytes = kind == TQ_KIND_K ? L.k_code_bytes : L.v_code_bytes;
-  a.grouped = kind == TQ_KIND_V;
-  a.signs = signs;
-  a.codebook = codebook;
-  a.S = S;
-  a.err_word = err_word;
+  tq_status s = encode_args(fmt, kind, x_f16, n_tokens, slot_mapping, page_pool, num_pages, signs, codebook, S, err_word, &a);
+  if (s != TQ_OK) return s;
+  if (n_tokens == 0) return TQ_OK;
   int sms = 0;
   if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
   const int bits = kind == TQ_KIND_K ? fmt->k_bits : fmt->v_bits;
+  const bool qjl = kind == TQ_KIND_K && fmt->k_qjl;
   return launch_encode(a, bits, qjl, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_encode_kv(const tq_format *fmt, const void *k_f16, const void *v_f16, int64_t n_tokens,
+                       const int32_t *slot_mapping, void *page_pool, int64_t num_pages, const uint8_t *k_signs,
+                       const uint8_t *v_signs, const float *k_codebook, const float *v_codebook, const float *S,
+                       int32_t *err_word, void *stream) {
+  EncodeArgs ka, va;
+  tq_status s = encode_args(fmt, TQ_KIND_K, k_f16, n_tokens, slot_mapping, page_pool, num_pages, k_signs, k_codebook, S,
+                            err_word, &ka);
+  if (s != TQ_OK) return s;
+  s = encode_args(fmt, TQ_KIND_V, v_f16, n_tokens, slot_mapping, page_pool, num_pages, v_signs, v_codebook, nullptr,
+                  err_word, &va);
+  if (s != TQ_OK) return s;
+  if (n_tokens == 0) return TQ_OK;
+  int sms = 0;
+  if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fmt->k_bits == fmt->v_bits && !fmt->k_qjl)
+    return launch_encode_kv(ka, va, fmt->k_bits, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  if (launch_encode(ka, fmt->k_bits, fmt->k_qjl != 0, sms, st) != cudaSuccess) return TQ_ERR_CUDA;
+  return launch_encode(va, fmt->v_bits, false, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64_t num_pages,

@@ -174,7 +174,7 @@ __device__ __forceinline__ uint32_t had_pair(int i0, int i1, int j) {
 #define TQ_ENCODE_MIN_BLOCKS 3
 #endif
 template <int BITS, bool QJL>
-__global__ void __launch_bounds__(256, QJL ? 2 : TQ_ENCODE_MIN_BLOCKS) encode_kernel(const EncodeArgs a) {
+__device__ __forceinline__ void encode_body(const EncodeArgs &a) {
   extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells, QJL only
   __shared__ float s_cent[16];
   __shared__ float s_mid[16];
@@ -437,6 +437,21 @@ __global__ void __launch_bounds__(256, QJL ? 2 : TQ_ENCODE_MIN_BLOCKS) encode_ke
 }
 
 template <int BITS, bool QJL>
+__global__ void __launch_bounds__(256, QJL ? 2 : TQ_ENCODE_MIN_BLOCKS) encode_kernel(const EncodeArgs a) {
+  encode_body<BITS, QJL>(a);
+}
+
+// Keys and values of the same tokens in one launch (same bits, keys without
+// QJL): blockIdx.y selects the kind.
+template <int BITS>
+__global__ void __launch_bounds__(256, TQ_ENCODE_MIN_BLOCKS) encode_kv_kernel(const EncodeArgs ka, const EncodeArgs va) {
+  if (blockIdx.y == 0)
+    encode_body<BITS, false>(ka);
+  else
+    encode_body<BITS, false>(va);
+}
+
+template <int BITS, bool QJL>
 __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
   extern __shared__ float s_S[];
   __shared__ float s_cent[16];
@@ -563,6 +578,22 @@ static cudaError_t launch_decode_t(const DecodeArgs &a, int sms, cudaStream_t st
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   decode_kernel<BITS, QJL><<<(unsigned)blocks, 256, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_kv(const EncodeArgs &ka, const EncodeArgs &va, int bits, int sms, cudaStream_t st) {
+  const int64_t quads = ka.n_tokens * ka.H;
+  int64_t blocks = (quads + 63) / 64;
+  const int64_t cap = (int64_t)sms * 4;  // two kinds share the machine
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const dim3 grid((unsigned)blocks, 2);
+  switch (bits) {
+    case 2: encode_kv_kernel<2><<<grid, 256, 0, st>>>(ka, va); break;
+    case 3: encode_kv_kernel<3><<<grid, 256, 0, st>>>(ka, va); break;
+    case 4: encode_kv_kernel<4><<<grid, 256, 0, st>>>(ka, va); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

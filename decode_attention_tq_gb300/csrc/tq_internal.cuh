@@ -94,6 +94,7 @@ struct AttnArgs {
 };
 
 cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
+cudaError_t launch_encode_kv(const EncodeArgs &ka, const EncodeArgs &va, int bits, int sms, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
 
 // Decode attention pieces (tq_attn_aux.cu and tq_attn_k*.cu).

@@ -65,12 +65,13 @@ def load_library():
             lib.tq_make_codebook.argtypes = [C.c_int, P, P]
             lib.tq_page_layout.argtypes = [P, P]
             lib.tq_encode.argtypes = [P, i32, P, i64, P, P, i64, P, P, P, P, P]
+            lib.tq_encode_kv.argtypes = [P, P, P, i64, P, P, i64, P, P, P, P, P, P, P]
             lib.tq_decode.argtypes = [P, i32, P, i64, P, i64, P, P, P, P, P, P]
             lib.tq_decode_attn_workspace_size.argtypes = [P, i32, i32, i32, i32, C.POINTER(sz)]
             lib.tq_decode_attn.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P]
             lib.tq_decode_attn_timed.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P, P, P]
             lib.tq_decode_attn_static.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, P]
-            for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn",
+            for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_encode_kv", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn",
                       "tq_decode_attn_timed", "tq_decode_attn_static"):
                 getattr(lib, f).restype = C.c_int
             _lib = lib
@@ -148,6 +149,22 @@ def tq_encode(fmt, kind: int, x, slot_mapping, page_pool, num_pages: int, signs,
         _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
     )
     _check(rc, "tq_encode")
+
+
+def tq_encode_kv(fmt, k, v, slot_mapping, page_pool, num_pages: int, k_signs, v_signs, k_codebook, v_codebook, S=None,
+                 err_word=None, stream=None):
+    F = _fmt(fmt)
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError("tq_encode_kv: k and v must have the same shape")
+    rc = load_library().tq_encode_kv(
+        C.byref(F), _dev_ptr(k, torch.float16, "k"), _dev_ptr(v, torch.float16, "v"), int(k.shape[0]),
+        _dev_ptr(slot_mapping, torch.int32, "slot_mapping"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
+        _dev_ptr(k_signs, torch.uint8, "k_signs"), _dev_ptr(v_signs, torch.uint8, "v_signs"),
+        _dev_ptr(k_codebook, torch.float32, "k_codebook"), _dev_ptr(v_codebook, torch.float32, "v_codebook"),
+        _dev_ptr(S, torch.float32, "S", allow_none=True), _dev_ptr(err_word, torch.int32, "err_word", allow_none=True),
+        _stream(stream),
+    )
+    _check(rc, "tq_encode_kv")
 
 
 def tq_decode(fmt, kind: int, page_pool, num_pages: int, slot_mapping, signs, codebook, S=None, out=None, err_word=None, stream=None):

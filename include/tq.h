@@ -138,6 +138,25 @@ tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n
                     void *stream);
 
 /*
+ * Append N tokens' keys and values in one call: the same result as
+ * tq_encode(K, k_f16, ...) followed by tq_encode(V, v_f16, ...) with the same
+ * slot_mapping (byte-identical pages).  A decode step appends both kinds of
+ * the new token at once (aither-kvcache README, section 'Algorithm': keys and
+ * values are compressed alike, each with its own rotation and codebook).
+ * When k_bits == v_bits and keys carry no QJL sketch this is one kernel
+ * launch; otherwise it is two launches, in this order, on `stream`.
+ *   k_f16, v_f16          device fp16 [N][H][d]
+ *   k_signs, v_signs      device uint8 [d] (the kinds' D)
+ *   k_codebook/v_codebook device fp32 codebooks for k_bits / v_bits
+ *   S                     device fp32 [m][d] when fmt->k_qjl, else NULL
+ * Argument rules and errors are those of tq_encode for each kind.
+ */
+tq_status tq_encode_kv(const tq_format *fmt, const void *k_f16, const void *v_f16, int64_t n_tokens,
+                       const int32_t *slot_mapping, void *page_pool, int64_t num_pages, const uint8_t *k_signs,
+                       const uint8_t *v_signs, const float *k_codebook, const float *v_codebook, const float *S,
+                       int32_t *err_word, void *stream);
+
+/*
  * Decode N slots of one kind back to vectors (tests and offline use; never on
  * the attention path, which reads the packed pages directly):
  *   x_hat = n * D . (H y) / sqrt(d),

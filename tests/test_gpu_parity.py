@@ -123,6 +123,48 @@ def test_attention_end_to_end_gpu_encode():
     assert e.max() <= REL_ATTN
 
 
+@pytest.mark.parametrize("kb,vb,qjl", [(2, 2, 0), (3, 3, 0), (4, 4, 0), (4, 4, 1), (3, 4, 1), (2, 4, 0)])
+def test_encode_kv_matches_two_encodes(kb, vb, qjl):
+    """The joint K+V append writes exactly the bytes of two single-kind appends."""
+    fmt = ti.Format(128, kb, vb, qjl, 128, 64, 4)
+    d, H, P = fmt.head_dim, fmt.num_kv_heads, fmt.page_size
+    N = 301
+    num_pages = (N + P - 1) // P + 2
+    lay = oracle.page_layout(fmt)
+    k = ti.kv_history(1, N, H, d, 7 + kb, 0)[0].cuda()
+    v = ti.kv_history(1, N, H, d, 7 + vb, 1)[0].cuda()
+    k[3] = 0
+    v[250] = 0
+    perm = np.random.default_rng(kb * 10 + vb).permutation(num_pages * P)[:N].astype(np.int32)
+    perm[40] = -1
+    sl = torch.from_numpy(perm).cuda()
+    ks = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_K, d)).cuda()
+    vs = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_V, d)).cuda()
+    S = torch.from_numpy(ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d)).cuda() if qjl else None
+    kcb, vcb = tq.device_codebook(kb), tq.device_codebook(vb)
+    two = torch.full((num_pages * lay["page_bytes"],), 0x3C, dtype=torch.uint8, device="cuda")
+    one = two.clone()
+    tq.tq_encode(fmt, 0, k, sl, two, num_pages, ks, kcb, S)
+    tq.tq_encode(fmt, 1, v, sl, two, num_pages, vs, vcb)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tq.tq_encode_kv(fmt, k, v, sl, one, num_pages, ks, vs, kcb, vcb, S, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(one, two)
+    # an out-of-range slot is skipped and flagged, the other tokens still land
+    bad = sl.clone()
+    bad[0] = num_pages * P
+    three = torch.full_like(one, 0x3C)
+    tq.tq_encode_kv(fmt, k, v, bad, three, num_pages, ks, vs, kcb, vcb, S, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == tq.TQ_DEVERR_SLOT_RANGE
+    page, off = int(perm[0]) // P, int(perm[0]) % P
+    assert not torch.equal(three, one)
+    mask = torch.ones_like(one, dtype=torch.bool)
+    mask[page * lay["page_bytes"]:(page + 1) * lay["page_bytes"]] = False
+    assert torch.equal(three[mask], one[mask])
+
+
 def test_bad_page_is_skipped_and_flagged():
     fmt = ti.Format(128, 4, 4, 0, 128, 64, 2)
     sc = Scenario(fmt, 2, 4, [300, 130], 0, [0, 0], layer=1)
