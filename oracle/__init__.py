@@ -286,3 +286,66 @@ def attention(f, q, pool, num_pages, block_tables, comp_lens, k_win, v_win, win_
     if hs is None:
         out = out.reshape(B, Hq, d)
     return rc, out
+
+
+def append_window(f, k_new, v_new, k_win, v_win, win_lens, win_head, comp_lens, block_tables, pool, num_pages,
+                  k_signs, v_signs, k_codebook, v_codebook, S=None):
+    """One decode step's append into a cache made of compressed pages plus an
+    fp16 recent window kept as a ring of W slots per sequence.
+
+    Follows "TurboQuant Family Design Study for CPU and Browser WASM KV
+    Caches": 'Packed format and complete bit accounting' (the most recent W
+    tokens stay fp16 for K and V), 'Append cost and memory-bandwidth
+    tradeoffs' (the append runs once per generated token, per layer and kv
+    head: rotate, quantize, pack, store) and 'Paging, lifecycle, and cache
+    identity' (fixed-size pages filled in order).  Per sequence b:
+
+    * W == 0: the new token is encoded at compressed position comp_lens[b];
+    * window not full (win_lens[b] < W): the new token goes to ring slot
+      win_lens[b] and win_lens[b] grows by one (win_head stays 0);
+    * window full: the oldest token, at ring slot win_head[b], is encoded at
+      compressed position comp_lens[b], the new token takes its ring slot,
+      win_head[b] advances by one modulo W.
+
+    Compressed position c lives in physical page block_tables[b][c // P] at
+    offset c % P; those pages are allocated by the caller.  A position whose
+    page index reaches the table width or whose entry lies outside
+    [0, num_pages) leaves that sequence untouched and is reported.
+
+    k_new, v_new [B, H, d] fp16; k_win, v_win [B, H, W, d] fp16 (or None for
+    W == 0); counters int32 [B]; all but the inputs are updated in place.
+    Returns the list of sequences that were skipped.
+    """
+    B, H, d = k_new.shape
+    P = int(f.page_size)
+    W = 0 if k_win is None else int(k_win.shape[2])
+    kc, kt = k_codebook
+    vc, vt = v_codebook
+    skipped = []
+    for b in range(B):
+        if W > 0 and win_lens[b] < W:
+            k_win[b, :, win_lens[b]] = k_new[b]
+            v_win[b, :, win_lens[b]] = v_new[b]
+            win_lens[b] += 1
+            continue
+        c = int(comp_lens[b])
+        pi = c // P
+        page = int(block_tables[b, pi]) if pi < block_tables.shape[1] else -1
+        if page < 0 or page >= num_pages:
+            skipped.append(b)
+            continue
+        slot = np.array([page * P + c % P], np.int32)
+        if W == 0:
+            k_out, v_out = k_new[b], v_new[b]
+        else:
+            i = int(win_head[b])
+            k_out, v_out = k_win[b, :, i].copy(), v_win[b, :, i].copy()
+            k_win[b, :, i] = k_new[b]
+            v_win[b, :, i] = v_new[b]
+            win_head[b] = (i + 1) % W
+        rc = encode(f, 0, k_out[None], slot, pool, num_pages, k_signs, kc, kt, S)
+        assert rc == 0
+        rc = encode(f, 1, v_out[None], slot, pool, num_pages, v_signs, vc, vt, None)
+        assert rc == 0
+        comp_lens[b] += 1
+    return skipped
