@@ -21,6 +21,8 @@ from .tq import (  # noqa: F401
     tq_decode_attn_workspace_size,
     tq_encode,
     tq_encode_kv,
+    tq_append_window,
+    tq_append_window_workspace_size,
     tq_make_codebook,
     tq_page_layout,
     tq_status_string,

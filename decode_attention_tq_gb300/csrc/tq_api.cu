@@ -276,6 +276,18 @@ tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n
   return launch_encode(a, bits, qjl, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
+// K then V of one append: one launch when both kinds share a bit width and
+// keys carry no QJL sketch, else two.
+static tq_status launch_kv(const tq_format *fmt, const EncodeArgs &ka, const EncodeArgs &va, void *stream) {
+  int sms = 0;
+  if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fmt->k_bits == fmt->v_bits && !fmt->k_qjl)
+    return launch_encode_kv(ka, va, fmt->k_bits, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  if (launch_encode(ka, fmt->k_bits, fmt->k_qjl != 0, sms, st) != cudaSuccess) return TQ_ERR_CUDA;
+  return launch_encode(va, fmt->v_bits, false, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 tq_status tq_encode_kv(const tq_format *fmt, const void *k_f16, const void *v_f16, int64_t n_tokens,
                        const int32_t *slot_mapping, void *page_pool, int64_t num_pages, const uint8_t *k_signs,
                        const uint8_t *v_signs, const float *k_codebook, const float *v_codebook, const float *S,
@@ -288,13 +300,70 @@ tq_status tq_encode_kv(const tq_format *fmt, const void *k_f16, const void *v_f1
                   err_word, &va);
   if (s != TQ_OK) return s;
   if (n_tokens == 0) return TQ_OK;
-  int sms = 0;
-  if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (fmt->k_bits == fmt->v_bits && !fmt->k_qjl)
-    return launch_encode_kv(ka, va, fmt->k_bits, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
-  if (launch_encode(ka, fmt->k_bits, fmt->k_qjl != 0, sms, st) != cudaSuccess) return TQ_ERR_CUDA;
-  return launch_encode(va, fmt->v_bits, false, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_kv(fmt, ka, va, stream);
+}
+
+
+
+tq_status tq_append_window_workspace_size(const tq_format *fmt, int batch, size_t *bytes) {
+  if (!bytes || !format_valid(fmt) || batch < 0) return TQ_ERR_INVALID_ARG;
+  const size_t stage = (size_t)batch * fmt->num_kv_heads * fmt->head_dim * 2;
+  *bytes = 2 * align256(stage) + align256((size_t)batch * 4);
+  return TQ_OK;
+}
+
+tq_status tq_append_window(const tq_format *fmt, int batch, const void *k_new_f16, const void *v_new_f16,
+                           void *k_win_f16, void *v_win_f16, int window, int32_t *win_lens, int32_t *win_head,
+                           int32_t *comp_lens, const int32_t *block_tables, int max_pages, void *page_pool,
+                           int64_t num_pages, const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
+                           const float *v_codebook, const float *S, void *workspace, size_t workspace_bytes,
+                           int32_t *err_word, void *stream) {
+  if (!format_valid(fmt) || batch < 0 || window < 0 || max_pages < 1 || num_pages < 1) return TQ_ERR_INVALID_ARG;
+  if (!format_gpu_supported(fmt)) return TQ_ERR_UNSUPPORTED;
+  if (num_pages > INT32_MAX / fmt->page_size) return TQ_ERR_UNSUPPORTED;  // page slots are int32
+  if (!k_new_f16 || !v_new_f16 || !comp_lens || !block_tables || !workspace) return TQ_ERR_INVALID_ARG;
+  if (window > 0 && (!k_win_f16 || !v_win_f16 || !win_lens || !win_head)) return TQ_ERR_INVALID_ARG;
+  if (!aligned(k_new_f16, 16) || !aligned(v_new_f16, 16) || !aligned(workspace, 256) || !aligned(comp_lens, 4) ||
+      !aligned(block_tables, 4) || (window > 0 && (!aligned(k_win_f16, 16) || !aligned(v_win_f16, 16) ||
+                                                   !aligned(win_lens, 4) || !aligned(win_head, 4))))
+    return TQ_ERR_INVALID_ARG;
+  size_t need = 0;
+  tq_append_window_workspace_size(fmt, batch, &need);
+  if (workspace_bytes < need) return TQ_ERR_INVALID_ARG;
+  if (batch == 0) return TQ_OK;
+
+  const size_t stage = align256((size_t)batch * fmt->num_kv_heads * fmt->head_dim * 2);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  RollArgs r;
+  r.k_new = static_cast<const __half *>(k_new_f16);
+  r.v_new = static_cast<const __half *>(v_new_f16);
+  r.k_win = static_cast<__half *>(k_win_f16);
+  r.v_win = static_cast<__half *>(v_win_f16);
+  r.B = batch;
+  r.H = fmt->num_kv_heads;
+  r.W = window;
+  r.P = fmt->page_size;
+  r.max_pages = max_pages;
+  r.num_pages = num_pages;
+  r.win_lens = win_lens;
+  r.win_head = win_head;
+  r.comp_lens = comp_lens;
+  r.block_tables = block_tables;
+  r.stage_k = reinterpret_cast<__half *>(ws);
+  r.stage_v = reinterpret_cast<__half *>(ws + stage);
+  r.stage_slots = reinterpret_cast<int32_t *>(ws + 2 * stage);
+  r.err_word = err_word;
+  // the staged tokens (slot -1 where nothing left the window) go into the
+  // pages; their arguments are checked before anything is launched
+  EncodeArgs ka, va;
+  tq_status s = encode_args(fmt, TQ_KIND_K, r.stage_k, batch, r.stage_slots, page_pool, num_pages, k_signs, k_codebook,
+                            S, err_word, &ka);
+  if (s != TQ_OK) return s;
+  s = encode_args(fmt, TQ_KIND_V, r.stage_v, batch, r.stage_slots, page_pool, num_pages, v_signs, v_codebook, nullptr,
+                  err_word, &va);
+  if (s != TQ_OK) return s;
+  if (launch_window_roll(r, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TQ_ERR_CUDA;
+  return launch_kv(fmt, ka, va, stream);
 }
 
 tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64_t num_pages,

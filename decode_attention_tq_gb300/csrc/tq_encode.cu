@@ -283,7 +283,11 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
     const float nrm = sqrtf(ss);
-    const bool zero = !(nrm > 0.f);
+    // A NaN or infinite coordinate (finite fp16 vectors cannot overflow ss)
+    // stores the norm as computed and a zero block, and never reaches the
+    // quantizer's bucket table with a NaN.
+    const bool bad = !(ss <= 3.0e38f);
+    const bool zero = !(nrm > 0.f) || bad;
 
     // z = x_c H_32 on the tensor cores, then the H_4 butterfly over blocks
     float z[4][8];
@@ -308,6 +312,10 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
       x[8 + i] = d01 + d23;
       x[16 + i] = s01 - s23;
       x[24 + i] = d01 - d23;
+    }
+    if (bad) {
+#pragma unroll
+      for (int j = 0; j < 32; j++) x[j] = 0.f;
     }
     const float inv = zero ? 0.f : 1.0f / nrm;
 

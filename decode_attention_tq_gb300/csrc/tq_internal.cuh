@@ -24,6 +24,19 @@ struct EncodeArgs {
   int32_t *err_word;
 };
 
+// Per-step window roll (tq_append_window): see tq_append.cu.
+struct RollArgs {
+  const __half *k_new, *v_new;  // [B][H][d]
+  __half *k_win, *v_win;        // [B][H][W][d] (W > 0)
+  int B, H, W, P, max_pages;
+  int64_t num_pages;
+  int32_t *win_lens, *win_head, *comp_lens;  // [B], updated in place
+  const int32_t *block_tables;               // [B][max_pages]
+  __half *stage_k, *stage_v;                 // [B][H][d] tokens to encode
+  int32_t *stage_slots;                      // [B] their page slots, -1: none
+  int32_t *err_word;
+};
+
 struct DecodeArgs {
   const uint8_t *pool;
   int64_t n_tokens;
@@ -94,6 +107,7 @@ struct AttnArgs {
 };
 
 cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
+cudaError_t launch_window_roll(const RollArgs &a, cudaStream_t st);
 cudaError_t launch_encode_kv(const EncodeArgs &ka, const EncodeArgs &va, int bits, int sms, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
 

@@ -66,12 +66,14 @@ def load_library():
             lib.tq_page_layout.argtypes = [P, P]
             lib.tq_encode.argtypes = [P, i32, P, i64, P, P, i64, P, P, P, P, P]
             lib.tq_encode_kv.argtypes = [P, P, P, i64, P, P, i64, P, P, P, P, P, P, P]
+            lib.tq_append_window_workspace_size.argtypes = [P, i32, C.POINTER(sz)]
+            lib.tq_append_window.argtypes = [P, i32, P, P, P, P, i32, P, P, P, P, i32, P, i64, P, P, P, P, P, P, sz, P, P]
             lib.tq_decode.argtypes = [P, i32, P, i64, P, i64, P, P, P, P, P, P]
             lib.tq_decode_attn_workspace_size.argtypes = [P, i32, i32, i32, i32, C.POINTER(sz)]
             lib.tq_decode_attn.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P]
             lib.tq_decode_attn_timed.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P, P, P]
             lib.tq_decode_attn_static.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, P]
-            for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_encode_kv", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn",
+            for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_encode_kv", "tq_append_window_workspace_size", "tq_append_window", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn",
                       "tq_decode_attn_timed", "tq_decode_attn_static"):
                 getattr(lib, f).restype = C.c_int
             _lib = lib
@@ -165,6 +167,36 @@ def tq_encode_kv(fmt, k, v, slot_mapping, page_pool, num_pages: int, k_signs, v_
         _stream(stream),
     )
     _check(rc, "tq_encode_kv")
+
+
+def tq_append_window_workspace_size(fmt, batch: int) -> int:
+    F = _fmt(fmt)
+    n = C.c_size_t(0)
+    _check(load_library().tq_append_window_workspace_size(C.byref(F), int(batch), C.byref(n)), "tq_append_window_workspace_size")
+    return int(n.value)
+
+
+def tq_append_window(fmt, k_new, v_new, k_win, v_win, win_lens, win_head, comp_lens, block_tables, page_pool, num_pages: int,
+                     k_signs, v_signs, k_codebook, v_codebook, S=None, workspace=None, err_word=None, stream=None):
+    """One decode step's append: new token into the fp16 ring window, the token
+    leaving it into the pages (counters updated on the device)."""
+    F = _fmt(fmt)
+    B = int(k_new.shape[0])
+    W = 0 if k_win is None else int(k_win.shape[2])
+    if workspace is None:
+        workspace = torch.empty(tq_append_window_workspace_size(F, B), dtype=torch.uint8, device=k_new.device)
+    rc = load_library().tq_append_window(
+        C.byref(F), B, _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
+        _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True), W,
+        _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), _dev_ptr(win_head, torch.int32, "win_head", allow_none=True),
+        _dev_ptr(comp_lens, torch.int32, "comp_lens"), _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
+        _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(k_signs, torch.uint8, "k_signs"),
+        _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
+        _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
+        _dev_ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()),
+        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+    )
+    _check(rc, "tq_append_window")
 
 
 def tq_decode(fmt, kind: int, page_pool, num_pages: int, slot_mapping, signs, codebook, S=None, out=None, err_word=None, stream=None):

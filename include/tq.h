@@ -157,6 +157,55 @@ tq_status tq_encode_kv(const tq_format *fmt, const void *k_f16, const void *v_f1
                        int32_t *err_word, void *stream);
 
 /*
+ * Bytes of device workspace tq_append_window needs for `batch` sequences
+ * (staging for the tokens that leave the window).  Host only.
+ */
+tq_status tq_append_window_workspace_size(const tq_format *fmt, int batch, size_t *bytes);
+
+/*
+ * One decode step's append for `batch` sequences, for a cache of compressed
+ * pages plus an fp16 recent window of `window` tokens kept as a ring per
+ * sequence.  Follows "TurboQuant Family Design Study for CPU and Browser WASM
+ * KV Caches": 'Packed format and complete bit accounting' (the last W tokens
+ * stay fp16 for K and V), 'Append cost and memory-bandwidth tradeoffs' (the
+ * append runs once per generated token) and 'Paging, lifecycle, and cache
+ * identity' (fixed pages filled in order).  Per sequence b:
+ *   window == 0: the new token is encoded at compressed position comp_lens[b];
+ *   win_lens[b] < window: the new token goes to ring slot win_lens[b], which
+ *     then grows by one (win_head[b] stays 0 until the ring is full);
+ *   otherwise: the token in ring slot win_head[b] (the oldest) is encoded at
+ *     compressed position comp_lens[b], the new token takes that ring slot and
+ *     win_head[b] advances by one modulo the window.
+ * Compressed position c goes to physical page block_tables[b][c / P], offset
+ * c % P: the caller allocates the page before the append that needs it.
+ * Afterwards tq_decode_attn with the updated counters sees the new token
+ * (attention does not depend on the order of the window's tokens).
+ *   k_new_f16, v_new_f16  device fp16 [batch][H][d], the new token
+ *   k_win_f16, v_win_f16  device fp16 [batch][H][window][d], updated in place
+ *                         (NULL when window == 0)
+ *   win_lens, win_head    device int32 [batch], updated in place (NULL when
+ *                         window == 0)
+ *   comp_lens             device int32 [batch], updated in place
+ *   block_tables          device int32 [batch][max_pages]
+ *   signs, codebooks, S   as for tq_encode_kv
+ *   workspace             device, >= tq_append_window_workspace_size bytes,
+ *                         256-byte aligned; its contents need no setup
+ * All counters are read and written on the device, so a step can be replayed
+ * from a CUDA graph.  Two or three kernel launches on `stream`: the window
+ * roll, then the append of the tokens that left the window (one launch when
+ * k_bits == v_bits without QJL).  Host argument errors return before any
+ * launch.  A negative or out-of-range counter (TQ_DEVERR_LENGTH), or a block
+ * table entry outside [0, num_pages) (TQ_DEVERR_PAGE_RANGE), leaves that
+ * sequence untouched and sets the bit in err_word.
+ */
+tq_status tq_append_window(const tq_format *fmt, int batch, const void *k_new_f16, const void *v_new_f16,
+                           void *k_win_f16, void *v_win_f16, int window, int32_t *win_lens, int32_t *win_head,
+                           int32_t *comp_lens, const int32_t *block_tables, int max_pages, void *page_pool,
+                           int64_t num_pages, const uint8_t *k_signs, const uint8_t *v_signs, const float *k_codebook,
+                           const float *v_codebook, const float *S, void *workspace, size_t workspace_bytes,
+                           int32_t *err_word, void *stream);
+
+/*
  * Decode N slots of one kind back to vectors (tests and offline use; never on
  * the attention path, which reads the packed pages directly):
  *   x_hat = n * D . (H y) / sqrt(d),

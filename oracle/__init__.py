@@ -289,7 +289,7 @@ def attention(f, q, pool, num_pages, block_tables, comp_lens, k_win, v_win, win_
 
 
 def append_window(f, k_new, v_new, k_win, v_win, win_lens, win_head, comp_lens, block_tables, pool, num_pages,
-                  k_signs, v_signs, k_codebook, v_codebook, S=None):
+                  k_signs, v_signs, k_codebook, v_codebook, S=None, evicted=None):
     """One decode step's append into a cache made of compressed pages plus an
     fp16 recent window kept as a ring of W slots per sequence.
 
@@ -314,7 +314,9 @@ def append_window(f, k_new, v_new, k_win, v_win, win_lens, win_head, comp_lens, 
 
     k_new, v_new [B, H, d] fp16; k_win, v_win [B, H, W, d] fp16 (or None for
     W == 0); counters int32 [B]; all but the inputs are updated in place.
-    Returns the list of sequences that were skipped.
+    Returns the list of sequences that were skipped.  With a list as
+    ``evicted``, each token written to the pages is appended to it as
+    (b, slot, k [H, d], v [H, d]).
     """
     B, H, d = k_new.shape
     P = int(f.page_size)
@@ -343,6 +345,8 @@ def append_window(f, k_new, v_new, k_win, v_win, win_lens, win_head, comp_lens, 
             k_win[b, :, i] = k_new[b]
             v_win[b, :, i] = v_new[b]
             win_head[b] = (i + 1) % W
+        if evicted is not None:
+            evicted.append((b, int(slot[0]), np.array(k_out), np.array(v_out)))
         rc = encode(f, 0, k_out[None], slot, pool, num_pages, k_signs, kc, kt, S)
         assert rc == 0
         rc = encode(f, 1, v_out[None], slot, pool, num_pages, v_signs, vc, vt, None)

@@ -223,3 +223,106 @@ def test_host_argument_errors():
     with pytest.raises(tq.TQError) as ei:
         tq.tq_decode_attn(fmt, q, pool, 4, bt, z, None, None, None, s, s, cb, cb, None, out, small)
     assert ei.value.status == 6
+
+
+@pytest.mark.parametrize("kb,vb,qjl,W", [(4, 4, 0, 8), (3, 4, 1, 8), (2, 2, 1, 5), (4, 4, 0, 0)])
+def test_append_window_matches_oracle(kb, vb, qjl, W):
+    """Window roll plus encode of the leaving token, from mixed initial states
+    (empty, partial, full at several ring heads, a missing page), stepped on
+    both sides: windows and counters identical, pages field by field."""
+    fmt = ti.Format(128, kb, vb, qjl, 128, 16, 4)
+    d, H, P = fmt.head_dim, fmt.num_kv_heads, fmt.page_size
+    B, steps = 5, 30
+    rng = np.random.default_rng(kb * 100 + vb * 10 + W)
+    max_pages = 8
+    num_pages = B * max_pages + 2
+    bt = rng.permutation(num_pages)[: B * max_pages].astype(np.int32).reshape(B, max_pages)
+    bt[4, 2] = -1  # sequence 4 runs out of pages at compressed position 32
+    comp = np.array([0, 5, 7, 16, 20], np.int32)
+    lens = np.array([0, 3, W, W, W], np.int32) if W else None
+    head = np.array([0, 0, 5 % max(W, 1), 0, 2 % max(W, 1)], np.int32) if W else None
+    kw = (rng.standard_normal((B, H, W, d)) * 3).astype(np.float16) if W else None
+    vw = (rng.standard_normal((B, H, W, d)) * 3).astype(np.float16) if W else None
+    K = ti.kv_history(steps, B, H, d, 3, 0).numpy()  # [steps, B, H, d]
+    V = ti.kv_history(steps, B, H, d, 3, 1).numpy()
+    lay = oracle.page_layout(fmt)
+    pool_ref = np.full(num_pages * lay["page_bytes"], 0x5A, np.uint8)
+    kcb, vcb = oracle.make_codebook(kb), oracle.make_codebook(vb)
+    ks, vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
+    S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if qjl else None
+
+    dev = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    g_kw, g_vw, g_lens, g_head, g_comp, g_bt = dev(kw), dev(vw), dev(lens), dev(head), dev(comp), dev(bt)
+    g_pool = torch.full((pool_ref.size,), 0x5A, dtype=torch.uint8, device="cuda")
+    g_ks, g_vs, g_S = dev(ks), dev(vs), dev(S)
+    ws = torch.empty(tq.tq_append_window_workspace_size(fmt, B), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    evicted, skipped_any = [], set()
+    for t in range(steps):
+        tq.tq_append_window(fmt, dev(K[t]), dev(V[t]), g_kw, g_vw, g_lens, g_head, g_comp, g_bt, g_pool, num_pages, g_ks, g_vs,
+                            tq.device_codebook(kb), tq.device_codebook(vb), g_S, workspace=ws, err_word=err)
+        sk = oracle.append_window(fmt, K[t], V[t], kw, vw, lens, head, comp, bt, pool_ref, num_pages, ks, vs, kcb, vcb, S,
+                                  evicted=evicted)
+        skipped_any |= set(sk)
+    torch.cuda.synchronize()
+    assert skipped_any == {4}
+    assert int(err.item()) == tq.TQ_DEVERR_PAGE_RANGE
+    assert np.array_equal(g_comp.cpu().numpy(), comp)
+    if W:
+        assert np.array_equal(g_lens.cpu().numpy(), lens) and np.array_equal(g_head.cpu().numpy(), head)
+        assert np.array_equal(g_kw.cpu().numpy(), kw) and np.array_equal(g_vw.cpu().numpy(), vw)
+    # pages: the evicted tokens, field by field against a direct oracle encode
+    pool = g_pool.cpu().numpy()
+    slots = np.array([e[1] for e in evicted], np.int32)
+    assert len(slots) > 0
+    from tq_testlib import written_mask
+    for kind, bits in ((0, kb), (1, vb)):
+        X = np.stack([e[2 + kind] for e in evicted])
+        scratch = np.zeros_like(pool_ref)
+        rc, _, cm, sm = oracle.encode(fmt, kind, X, slots, scratch, num_pages, ks if kind == 0 else vs,
+                                      *(kcb if kind == 0 else vcb), S if kind == 0 else None, diagnostics=True)
+        assert rc == 0
+        other = written_mask(len(pool_ref), lay, fmt, 1 - kind, slots)
+        pg = pool.copy()
+        pg[other] = pool_ref[other]  # the other kind is checked in its own pass
+        compare_encoded(pg, pool_ref, lay, fmt, kind, slots, cm, sm)
+
+
+@pytest.mark.parametrize("kind,qjl", [(0, 1), (1, 0)])
+def test_encode_non_finite_vector_is_a_zero_block(kind, qjl):
+    """A head vector with an infinite or NaN coordinate is stored as a zero
+    block (codes, signs and gamma 0) with its non-finite norm; the other
+    vectors are unaffected."""
+    from tq_testlib import unpack_field
+    fmt = ti.Format(128, 4, 4, qjl, 128, 64, 4)
+    d, H = fmt.head_dim, fmt.num_kv_heads
+    N = 24
+    lay = oracle.page_layout(fmt)
+    x = ti.kv_history(1, N, H, d, 2, kind)[0].clone()
+    bad = [(3, 1), (7, 2), (9, 0)]
+    x[3, 1, 5] = float("inf")
+    x[7, 2, :] = float("nan")
+    x[9, 0, 0] = float("-inf")
+    slots = torch.arange(N, dtype=torch.int32)
+    signs = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_K if kind == 0 else ti.SEED_SIGNS_V, d)).cuda()
+    S = torch.from_numpy(ti.gaussian_matrix(ti.SEED_QJL, 128, d)).cuda() if qjl else None
+    pools = []
+    for xs in (x, torch.where(torch.isfinite(x), x, torch.zeros_like(x))):
+        pool = torch.full((2 * lay["page_bytes"],), 0x77, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        tq.tq_encode(fmt, kind, xs.cuda(), slots.cuda(), pool, 2, signs, tq.device_codebook(4), S, err_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        pools.append(pool.cpu().numpy())
+    n, g, c, s = unpack_field(pools[0], lay, fmt, kind, slots.numpy())
+    n2, g2, c2, s2 = unpack_field(pools[1], lay, fmt, kind, slots.numpy())
+    good = np.ones((N, H), bool)
+    for t, h in bad:
+        good[t, h] = False
+        assert not np.isfinite(n[t, h])
+        assert np.all(c[t, h] == 0)
+        if qjl:
+            assert g[t, h] == 0 and np.all(s[t, h] == 0)
+    assert np.array_equal(n[good], n2[good]) and np.array_equal(c[good], c2[good])
+    if qjl:
+        assert np.array_equal(g[good], g2[good]) and np.array_equal(s[good], s2[good])
