@@ -5,8 +5,11 @@ Default workload (N=1): Llama-3-8B-shaped decode, 32 layers, batch 16,
 32 query / 8 KV heads, d = 128, context 32768 per sequence (32640 compressed
 4-bit K / 4-bit V tokens in 64-token pages with a random page permutation,
 plus a 128-token fp16 window).  One step = for every layer: append one token
-per sequence into the packed pages (tq_encode_kv) and one decode
-attention over the whole cache (tq_decode_attn).  The 32 layers' caches
+per sequence (tq_append_window: the new token enters the fp16 ring window and
+the oldest window token is encoded into the packed pages) and one decode
+attention over the whole cache (tq_decode_attn).  The context therefore grows
+by one token per step; the metric counts the starting context (the run adds
+well under 1 % to it).  The 32 layers' caches
 (18.5 GB) are resident in HBM before timing; the working set is far larger
 than L2, so no flush is needed between iterations.
 
@@ -162,7 +165,9 @@ def per_token_head_bytes(fmt) -> dict:
 class DecodeBench:
     """A resident multi-layer compressed cache and its decode step."""
 
-    def __init__(self, wl: ti.DecodeWorkload, device: str):
+    def __init__(self, wl: ti.DecodeWorkload, device: str, spare_tokens: int = 0):
+        """`spare_tokens`: compressed positions beyond the context that steps
+        may append (their pages are allocated in the block tables)."""
         import decode_attention_tq_gb300 as tq
 
         self.tq = tq
@@ -172,7 +177,7 @@ class DecodeBench:
         B, Hq, H, d, P, W, T = wl.batch, wl.q_heads, wl.kv_heads, f.head_dim, f.page_size, wl.window, wl.context
         comp = wl.comp_tokens
         self.B, self.Hq, self.H, self.W, self.T, self.comp = B, Hq, H, W, T, comp
-        self.pages_per_seq = wl.pages_per_seq
+        self.pages_per_seq = wl.pages_per_seq + (spare_tokens + P - 1) // P
         self.num_pages = B * self.pages_per_seq + 1
         perm = ti.page_permutation(self.num_pages).to(device)
         self.bt = perm[: B * self.pages_per_seq].reshape(B, self.pages_per_seq).contiguous()
@@ -180,7 +185,6 @@ class DecodeBench:
         slots = self.bt[:, pos // P] * P + (pos % P)[None, :]
         self.comp_lens = torch.full((B,), comp, dtype=torch.int32, device=device)
         self.win_lens = torch.full((B,), wl.win_tokens, dtype=torch.int32, device=device)
-        self.append_slots = slots[:, comp - 1].to(torch.int32).contiguous()
         self.ks = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_K, d)).to(device)
         self.vs = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_V, d)).to(device)
         self.kcb = tq.device_codebook(f.k_bits, device)
@@ -205,30 +209,36 @@ class DecodeBench:
                 del flat
                 ent[name + "win"] = x[:, comp:].permute(0, 2, 1, 3).contiguous() if W else None
                 new = self.io_in[layer, nq + kind * nkv: nq + (kind + 1) * nkv].view(B, H, d)
-                new.copy_(x[:, comp - 1])  # the token each step re-appends
+                new.copy_(x[:, comp - 1])  # the token each step appends
                 ent[name + "new"] = new
                 del x
             ent["q"] = self.io_in[layer, :nq].view(B, Hq, d)
             ent["q"].copy_(ti.query(B, Hq, d, device=device, seed=ti.SEED_QUERY + 7919 * layer))
             ent["out"] = self.io_out[layer].view(B, Hq, d)
+            # per-layer cache counters, advanced on the device by each append
+            ent["comp"] = self.comp_lens.clone()
+            ent["wlen"] = self.win_lens.clone() if W else None
+            ent["whead"] = torch.zeros(B, dtype=torch.int32, device=device) if W else None
             self.layers.append(ent)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()  # generation temporaries go back to the driver
         self.ws = torch.empty(tq.tq_decode_attn_workspace_size(f, B, Hq, self.pages_per_seq, W), dtype=torch.uint8, device=device)
+        self.ws_append = torch.empty(tq.tq_append_window_workspace_size(f, B), dtype=torch.uint8, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         bph = per_token_head_bytes(f)
         self.main_bytes = B * H * comp * (bph["k"] + bph["v"]) + B * self.pages_per_seq * 4  # per layer launch
         self.window_bytes = B * H * wl.win_tokens * d * 2 * 2
         self.step_bytes = wl.layers * (self.main_bytes + self.window_bytes + B * Hq * d * (2 + 4))
-        appends = 1 if (f.k_bits == f.v_bits and not f.k_qjl) else 2  # tq_encode_kv: one joint launch or K then V
-        self.launches_per_step = wl.layers * (appends + 3)  # appends + prep (with window chunks), main, merge
+        appends = 1 if (f.k_bits == f.v_bits and not f.k_qjl) else 2  # one joint K+V encode launch, or K then V
+        self.launches_per_step = wl.layers * (1 + appends + 3)  # window roll, encode, prep (with window chunks), main, merge
 
     def step(self, events=None):
         tq, f = self.tq, self.fmt
         for i, L in enumerate(self.layers):
-            tq.tq_encode_kv(f, L["knew"], L["vnew"], self.append_slots, L["pool"], self.num_pages, self.ks, self.vs, self.kcb,
-                            self.vcb, self.S, err_word=self.err)
-            args = (f, L["q"], L["pool"], self.num_pages, self.bt, self.comp_lens, L["kwin"], L["vwin"], self.win_lens if self.W else None,
+            tq.tq_append_window(f, L["knew"], L["vnew"], L["kwin"], L["vwin"], L["wlen"], L["whead"], L["comp"], self.bt, L["pool"],
+                                self.num_pages, self.ks, self.vs, self.kcb, self.vcb, self.S, workspace=self.ws_append,
+                                err_word=self.err)
+            args = (f, L["q"], L["pool"], self.num_pages, self.bt, L["comp"], L["kwin"], L["vwin"], L["wlen"],
                     self.ks, self.vs, self.kcb, self.vcb, self.S, L["out"], self.ws)
             if events is None:
                 tq.tq_decode_attn(*args, err_word=self.err)
@@ -258,7 +268,9 @@ def run_decode(args, device, barrier, reduce_max, rank, world):
 
         wl = dataclasses.replace(wl, layers=args.layers, name=f"{wl.name}(first {args.layers} layers)")
     t0 = time.time()
-    bench = DecodeBench(wl, device)
+    # every step appends one compressed token per sequence: room for all the
+    # steps this run makes (both timed arms, warm-ups, captures, event steps)
+    bench = DecodeBench(wl, device, spare_tokens=2 * (args.steps + args.warmup) + 32)
     setup_s = time.time() - t0
 
     # graph-captured step (launch-bound pieces replay without host overhead)
