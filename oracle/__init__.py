@@ -15,6 +15,7 @@ pages leave open (bit order, seeds), which are self-consistent by construction.
 from __future__ import annotations
 
 import ctypes as C
+import math
 import os
 import subprocess
 import threading
@@ -38,7 +39,8 @@ def build(force: bool = False) -> str:
 
 
 class _Format(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "k_qjl", "qjl_m", "page_size", "num_kv_heads")]
+    _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "k_qjl", "qjl_m", "page_size", "num_kv_heads",
+                                         "norm_correct")] + [("qjl_scale", C.c_float)]
 
 
 class _Layout(C.Structure):
@@ -66,8 +68,8 @@ def _load():
             lib.orc_rotate.restype = None
             lib.orc_unrotate.argtypes = [C.c_int, P, P, P]
             lib.orc_unrotate.restype = None
-            lib.orc_encode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int] + [P] * 12
-            lib.orc_decode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, dbl, dbl] + [P] * 6
+            lib.orc_encode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int] + [P] * 12 + [C.c_int, dbl]
+            lib.orc_decode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, dbl, dbl] + [P] * 6 + [dbl]
             lib.orc_pack_bits.argtypes = [C.c_int, C.c_int, P, P]
             lib.orc_pack_bits.restype = None
             lib.orc_unpack_bits.argtypes = [C.c_int, C.c_int, P, P]
@@ -89,7 +91,8 @@ def _c(a, dtype):
 
 
 def _fmt(f) -> _Format:
-    return _Format(int(f.head_dim), int(f.k_bits), int(f.v_bits), int(f.k_qjl), int(f.qjl_m), int(f.page_size), int(f.num_kv_heads))
+    return _Format(int(f.head_dim), int(f.k_bits), int(f.v_bits), int(f.k_qjl), int(f.qjl_m), int(f.page_size), int(f.num_kv_heads),
+                   int(getattr(f, "norm_correct", 0)), float(getattr(f, "qjl_scale", 0.0)))
 
 
 def _f16bits(x) -> np.ndarray:
@@ -156,9 +159,15 @@ def unrotate(y, signs) -> np.ndarray:
 
 
 # ------------------------------------------------------------------ vector --
-def encode_vector(x, bits, signs, centroids, midpoints, S=None, qjl_m=0):
+def qjl_coef(qjl_m: int, qjl_scale: float = 0.0) -> float:
+    """Factor of gamma S^T (2z - 1) in y_hat: qjl_scale, else the paper's sqrt(pi/2)/m."""
+    return float(qjl_scale) if qjl_scale > 0 else math.sqrt(math.pi / 2) / qjl_m
+
+
+def encode_vector(x, bits, signs, centroids, midpoints, S=None, qjl_m=0, norm_correct=0, qjl_scale=0.0):
     """Encode one vector (fp64 values).  Returns a dict with norm, gamma, idx,
-    z, u, code_margin, sign_margin."""
+    z, u, code_margin, sign_margin.  With norm_correct the returned norm is
+    ||x|| / ||y_hat|| (y_hat with the QJL factor of qjl_coef)."""
     x = _c(x, np.float64)
     d = x.shape[0]
     qjl = S is not None
@@ -174,13 +183,14 @@ def encode_vector(x, bits, signs, centroids, midpoints, S=None, qjl_m=0):
     rc = _load().orc_encode_vector(
         d, bits, int(qjl), m, _ptr(x), _ptr(_c(signs, np.uint8)), _ptr(_c(centroids, np.float32)),
         _ptr(_c(midpoints, np.float32)), _ptr(Sa), C.byref(norm), C.byref(gamma), _ptr(idx), _ptr(z), _ptr(u), _ptr(cm), _ptr(sm),
+        int(norm_correct), qjl_coef(m, qjl_scale) if qjl else 0.0,
     )
     if rc != 0:
         raise ValueError(f"orc_encode_vector rc={rc}")
     return dict(norm=norm.value, gamma=gamma.value, idx=idx, z=z[:m], u=u, code_margin=cm, sign_margin=sm[:m])
 
 
-def decode_vector(norm, idx, bits, signs, centroids, gamma=0.0, z=None, S=None, qjl_m=0):
+def decode_vector(norm, idx, bits, signs, centroids, gamma=0.0, z=None, S=None, qjl_m=0, qjl_scale=0.0):
     idx = _c(idx, np.int32)
     d = idx.shape[0]
     qjl = S is not None
@@ -190,7 +200,7 @@ def decode_vector(norm, idx, bits, signs, centroids, gamma=0.0, z=None, S=None, 
     Sa = _c(S, np.float32) if qjl else None
     rc = _load().orc_decode_vector(
         d, bits, int(qjl), m, float(norm), float(gamma), _ptr(idx), _ptr(za), _ptr(_c(signs, np.uint8)),
-        _ptr(_c(centroids, np.float32)), _ptr(Sa), _ptr(out),
+        _ptr(_c(centroids, np.float32)), _ptr(Sa), _ptr(out), qjl_coef(m, qjl_scale) if qjl else 0.0,
     )
     if rc != 0:
         raise ValueError(f"orc_decode_vector rc={rc}")

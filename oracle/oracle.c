@@ -68,7 +68,17 @@
 
 typedef struct {
   int32_t head_dim, k_bits, v_bits, k_qjl, qjl_m, page_size, num_kv_heads;
+  int32_t norm_correct; /* store n / ||y_hat|| (Bug 3 of the debugging post) */
+  float qjl_scale;      /* factor of gamma S^T (2z - 1); 0: sqrt(pi/2) / m   */
 } orc_format;
+
+/* The QJL dequantization factor: the paper's sqrt(pi/2)/m for a Gaussian S
+ * ("The QJL detective story"), or the format's own (an orthogonal S takes
+ * sqrt(pi/2)/sqrt(d), times a shrinkage as in 'Testing it with an
+ * ablation'). */
+static double orc_qjl_coef(const orc_format *f) {
+  return f->qjl_scale > 0.0f ? (double)f->qjl_scale : sqrt(ORC_PI / 2.0) / (double)f->qjl_m;
+}
 
 typedef struct {
   int64_t slab_bytes, page_bytes;
@@ -193,16 +203,25 @@ void orc_unrotate(int d, const uint8_t *signs, const double *y, double *x) {
 
 /* --------------------------------------------------------- one vector ---- */
 
+int orc_decode_vector(int d, int bits, int qjl, int m, double norm, double gamma, const int32_t *idx,
+                      const uint8_t *z, const uint8_t *signs, const float *centroids, const float *S,
+                      double *out, double qjl_coef);
+
 /*
  * Encode one head vector x[d] (fp64 values of the fp16 input).
  * Outputs: *norm = ||x||, *gamma = ||e|| (QJL only), idx[d], z[m] (QJL only).
+ * With norm_correct, *norm = ||x|| / ||y_hat|| instead, y_hat being the
+ * unit-domain reconstruction of orc_decode_vector with factor qjl_coef, so
+ * that the decoded vector has norm ||x|| ("From 0% to 100% ...", section
+ * 'Round 2: the llama.cpp bug hunt', Bug 3: store original_norm /
+ * reconstruction_norm).
  * Optional diagnostics (may be NULL): u[d] (u-domain coordinates),
  * code_margin[d] = min_k |u_j - t_k|, sign_margin[m] = |(S e)_l| / gamma.
  */
 int orc_encode_vector(int d, int bits, int qjl, int m, const double *x, const uint8_t *signs,
                       const float *centroids, const float *midpoints, const float *S,
                       double *norm, double *gamma, int32_t *idx, uint8_t *z, double *u_out,
-                      double *code_margin, double *sign_margin) {
+                      double *code_margin, double *sign_margin, int norm_correct, double qjl_coef) {
   if (!is_pow2(d) || bits < 1 || bits > 8 || (qjl && m < 1)) return ORC_ERR_ARG;
   int L = 1 << bits;
   double *w = (double *)malloc(sizeof(double) * d);
@@ -255,6 +274,14 @@ int orc_encode_vector(int d, int bits, int qjl, int m, const double *x, const ui
       if (sign_margin) sign_margin[l] = (g > 0.0) ? fabs(p) / g : 0.0;
     }
   }
+  if (norm_correct) {
+    /* ||decode(norm = 1)|| = ||y_hat|| (H / sqrt(d) and the signs are orthogonal) */
+    double *r = w;
+    orc_decode_vector(d, bits, qjl, m, 1.0, qjl ? *gamma : 0.0, idx, z, signs, centroids, S, r, qjl_coef);
+    double r2 = 0.0;
+    for (int j = 0; j < d; j++) r2 += r[j] * r[j];
+    if (r2 > 0.0) *norm = n / sqrt(r2);
+  }
   free(w);
   free(e);
   return ORC_OK;
@@ -262,17 +289,18 @@ int orc_encode_vector(int d, int bits, int qjl, int m, const double *x, const ui
 
 /*
  * Decode one head vector:
- *   y_hat = c[idx]/sqrt(d) + sqrt(pi/2)/m * gamma * S^T (2z - 1)   (QJL term optional)
+ *   y_hat = c[idx]/sqrt(d) + qjl_coef * gamma * S^T (2z - 1)   (QJL term optional;
+ *           qjl_coef = sqrt(pi/2)/m in the paper's estimator)
  *   x_hat = norm * D . (H y_hat) / sqrt(d)
  */
 int orc_decode_vector(int d, int bits, int qjl, int m, double norm, double gamma, const int32_t *idx,
                       const uint8_t *z, const uint8_t *signs, const float *centroids, const float *S,
-                      double *out) {
+                      double *out, double qjl_coef) {
   if (!is_pow2(d) || bits < 1 || bits > 8 || (qjl && m < 1)) return ORC_ERR_ARG;
   double *y = (double *)malloc(sizeof(double) * d);
   for (int j = 0; j < d; j++) y[j] = (double)centroids[idx[j]] / sqrt((double)d);
   if (qjl) {
-    double scale = sqrt(ORC_PI / 2.0) / (double)m * gamma;
+    double scale = qjl_coef * gamma;
     for (int j = 0; j < d; j++) {
       double acc = 0.0;
       for (int l = 0; l < m; l++) acc += (double)S[(int64_t)l * d + j] * (z[l] ? 1.0 : -1.0);
@@ -417,7 +445,7 @@ int orc_encode(const orc_format *f, int kind, const uint16_t *x, int64_t N, cons
       int64_t vh = n * H + h;
       orc_encode_vector(d, bits, qjl, m, xv, signs, centroids, midpoints, S, &norm, &gamma, idx, z,
                         u_out ? u_out + vh * d : NULL, code_margin ? code_margin + vh * d : NULL,
-                        sign_margin ? sign_margin + vh * m : NULL);
+                        sign_margin ? sign_margin + vh * m : NULL, f->norm_correct, orc_qjl_coef(f));
       uint8_t *slab = pool + page * L.page_bytes + (int64_t)h * L.slab_bytes;
       if (kind == 0) {
         put_f32(slab + L.k_norm + 4 * off, (float)norm);
@@ -459,13 +487,13 @@ static void decode_slot(const orc_format *f, const orc_layout *L, int kind, cons
       orc_unpack_bits(m, 1, slab + L->k_signs + off * L->k_sign_bytes, zi);
       for (int l = 0; l < m; l++) z[l] = (uint8_t)zi[l];
     }
-    orc_decode_vector(d, f->k_bits, qjl, m, norm, gamma, idx, z, signs, centroids, S, out);
+    orc_decode_vector(d, f->k_bits, qjl, m, norm, gamma, idx, z, signs, centroids, S, out, orc_qjl_coef(f));
   } else {
     double norm = get_f32(slab + L->v_norm + 4 * off);
     uint8_t stream[L->v_code_bytes];
     get_v_codes(slab + L->v_codes, off, d, f->v_bits, stream);
     orc_unpack_bits(d, f->v_bits, stream, idx);
-    orc_decode_vector(d, f->v_bits, 0, 0, norm, 0.0, idx, NULL, signs, centroids, NULL, out);
+    orc_decode_vector(d, f->v_bits, 0, 0, norm, 0.0, idx, NULL, signs, centroids, NULL, out, 0.0);
   }
 }
 

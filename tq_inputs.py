@@ -135,7 +135,7 @@ def page_permutation(num_pages: int, seed: int = SEED_PAGES) -> torch.Tensor:
 
 @dataclasses.dataclass(frozen=True)
 class Format:
-    """Cache format (plain integers, mirrored by the C structs on both sides)."""
+    """Cache format (plain numbers, mirrored by the C structs on both sides)."""
 
     head_dim: int = 128
     k_bits: int = 4
@@ -144,6 +144,8 @@ class Format:
     qjl_m: int = 128
     page_size: int = 64
     num_kv_heads: int = 8
+    norm_correct: int = 0
+    qjl_scale: float = 0.0
 
 
 @dataclasses.dataclass(frozen=True)
@@ -194,3 +196,13 @@ BULK_ENCODE_64K = EncodeWorkload("bulk_encode_l32_h8_t65536", 32, 8, 65536, (2, 
 LONG_CTX_T128K = DecodeWorkload("long_ctx_l32_b4_h32x8_t131072_k2qjl_v2_w256", 32, 4, 32, Format(128, 2, 2, 1, 128, 128, 8), 131072, 256)
 
 DECODE_WORKLOADS = (SINGLE_LAYER_T2K, QWEN25_3B_T16K, LLAMA3_8B_T32K, LONG_CTX_T128K)
+
+
+def orthogonal_matrix(seed: int, m: int, d: int) -> np.ndarray:
+    """fp32 [m, d] with orthonormal rows (m <= d): the Q factor of the QR
+    decomposition of gaussian_matrix(seed, d, m), signs fixed so that R has a
+    positive diagonal (a Haar-distributed draw)."""
+    g = gaussian_matrix(seed, d, m).astype(np.float64)
+    q, r = np.linalg.qr(g)
+    q = q * np.sign(np.diag(r))[None, :]
+    return np.ascontiguousarray(q.T).astype(np.float32)
