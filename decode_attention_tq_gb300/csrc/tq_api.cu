@@ -21,7 +21,14 @@ bool format_valid(const tq_format *f) {
   if (f->k_qjl != 0 && f->k_qjl != 1) return false;
   if (f->k_qjl && (f->qjl_m < 8 || f->qjl_m % 8)) return false;
   if (f->page_size < 16 || f->page_size % 16 || f->num_kv_heads < 1) return false;
+  if (f->norm_correct != 0 && f->norm_correct != 1) return false;
+  if (!(f->qjl_scale >= 0.0f) || !isfinite(f->qjl_scale)) return false;
   return true;
+}
+
+// Factor of gamma * S^T (2z - 1) in y_hat: the format's, else sqrt(pi/2)/m.
+float qjl_coef(const tq_format *f) {
+  return f->qjl_scale > 0.0f ? f->qjl_scale : (float)(1.2533141373155003 / (double)f->qjl_m);
 }
 
 bool bits_supported(int b) { return b >= 2 && b <= 4; }
@@ -234,6 +241,7 @@ static tq_status encode_args(const tq_format *fmt, int kind, const void *x_f16, 
     return TQ_ERR_INVALID_ARG;
   if (!format_gpu_supported(fmt)) return TQ_ERR_UNSUPPORTED;
   const bool qjl = kind == TQ_KIND_K && fmt->k_qjl;
+  if (qjl && fmt->norm_correct) return TQ_ERR_UNSUPPORTED;  // would need S^T z per key in the encode
   if (!x_f16 || !slot_mapping || !page_pool || !signs || !codebook || (qjl && !S)) return TQ_ERR_INVALID_ARG;
   if (!aligned(x_f16, 16) || !aligned(page_pool, 16) || !aligned(slot_mapping, 4) || !aligned(codebook, 4) ||
       (qjl && !aligned(S, 16)))
@@ -255,6 +263,7 @@ static tq_status encode_args(const tq_format *fmt, int kind, const void *x_f16, 
   a->signs_off = L.k_signs;
   a->code_bytes = kind == TQ_KIND_K ? L.k_code_bytes : L.v_code_bytes;
   a->grouped = kind == TQ_KIND_V;
+  a->norm_correct = fmt->norm_correct != 0;
   a->signs = signs;
   a->codebook = codebook;
   a->S = S;
@@ -396,6 +405,7 @@ tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64
   a.signs = signs;
   a.codebook = codebook;
   a.S = S;
+  a.qjl_coef = qjl_coef(fmt);
   a.out = out;
   a.err_word = err_word;
   int sms = 0;
@@ -472,6 +482,7 @@ static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_hea
   a.k_cb = k_codebook;
   a.v_cb = v_codebook;
   a.S = S;
+  a.qjl_coef = qjl_coef(fmt);
   a.out = out;
   a.err_word = err_word;
   a.hdr = reinterpret_cast<AttnHeader *>(ws + p.off_hdr);

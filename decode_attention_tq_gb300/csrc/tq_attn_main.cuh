@@ -538,8 +538,8 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
       cK[nt] = ldexpf(kLog2e / (float)kD, -(eq + 8));
       if constexpr (QJL) {
         const int es = a.q_exp[orow * 2 + 1];
-        // sqrt(pi/2) / (m sqrt(d))
-        cQ[nt] = ldexpf(kLog2e * 1.2533141373155003f / ((float)kM * 11.313708498984761f), -es);
+        // qjl_coef / sqrt(d) (qjl_coef = sqrt(pi/2) / m for the paper's Gaussian S)
+        cQ[nt] = ldexpf(kLog2e * a.qjl_coef / 11.313708498984761f, -es);
       } else {
         cQ[nt] = 0.f;
       }

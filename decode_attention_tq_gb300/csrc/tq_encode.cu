@@ -346,6 +346,21 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
       }
     }
 
+    // Norm correction (no QJL): store n / ||y_hat|| with y_hat = c[idx] / sqrt(d),
+    // i.e. n sqrt(d) / ||c[idx]||, so that the reconstruction keeps ||x||.
+    float nstore = nrm;
+    if (!QJL && a.norm_correct) {
+      float c2 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; j++) {
+        const float cj = s_cent[idx[j]];
+        c2 = fmaf(cj, cj, c2);
+      }
+      c2 += __shfl_xor_sync(0xffffffffu, c2, 1);
+      c2 += __shfl_xor_sync(0xffffffffu, c2, 2);
+      nstore = (zero || !(c2 > 0.f)) ? nrm : nrm * 11.313708498984761f / sqrtf(c2);
+    }
+
     const int64_t page = ok ? slot / a.P : 0;
     const int64_t off = ok ? slot % a.P : 0;
     uint8_t *slab = a.pool + page * a.page_bytes + (int64_t)h * a.slab_bytes;
@@ -383,7 +398,7 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
           }
         }
       }
-      if (q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nrm;
+      if (q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nstore;
     }
 
     if constexpr (QJL) {
@@ -483,8 +498,9 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
   const int64_t NH = a.n_tokens * a.H;
   const uint32_t dsign = s_dsign[q];
   const int64_t pool_slots = a.num_pages * (int64_t)a.P;
-  // sqrt(d) * sqrt(pi/2) / m: the QJL term in u units
-  const float kq = 11.313708498984761f * 1.2533141373155003f / (float)kM;
+  // sqrt(d) * qjl_coef: the QJL term in u units (qjl_coef = sqrt(pi/2) / m
+  // for the paper's Gaussian S)
+  const float kq = 11.313708498984761f * a.qjl_coef;
 
   for (int64_t vb = (int64_t)warp * 8; vb < NH; vb += nwarps * 8) {
     const int64_t v = vb + quad_in_warp;

@@ -18,6 +18,7 @@ struct EncodeArgs {
   int64_t norm_off, codes_off, gamma_off, signs_off;
   int code_bytes;
   bool grouped;  // value-code stream: 16-token groups, chunk-major (value_chunk_offset)
+  bool norm_correct;  // store n / ||y_hat|| (no QJL)
   const uint8_t *signs;
   const float *codebook;
   const float *S;
@@ -49,6 +50,7 @@ struct DecodeArgs {
   const uint8_t *signs;
   const float *codebook;
   const float *S;
+  float qjl_coef;  // factor of gamma * S^T (2z - 1) in y_hat
   float *out;
   int32_t *err_word;
 };
@@ -88,6 +90,7 @@ struct AttnArgs {
   const uint8_t *k_signs, *v_signs;
   const float *k_cb, *v_cb;
   const float *S;
+  float qjl_coef;  // factor of gamma * S^T (2z - 1) in y_hat
   float *out;
   int32_t *err_word;
   // workspace sections

@@ -38,7 +38,8 @@ class TQError(RuntimeError):
 
 
 class tq_format(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "k_qjl", "qjl_m", "page_size", "num_kv_heads")]
+    _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "k_qjl", "qjl_m", "page_size", "num_kv_heads",
+                                         "norm_correct")] + [("qjl_scale", C.c_float)]
 
 
 class tq_layout(C.Structure):
@@ -83,8 +84,8 @@ def load_library():
 def _fmt(f) -> tq_format:
     if isinstance(f, tq_format):
         return f
-    g = (lambda k: f[k]) if isinstance(f, dict) else (lambda k: getattr(f, k))
-    return tq_format(*(int(g(n)) for n, _ in tq_format._fields_))
+    g = (lambda k: f.get(k, 0)) if isinstance(f, dict) else (lambda k: getattr(f, k, 0))
+    return tq_format(*(float(g(n)) if t is C.c_float else int(g(n)) for n, t in tq_format._fields_))
 
 
 def _dev_ptr(t, dtype=None, name="tensor", allow_none=False):

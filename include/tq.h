@@ -70,6 +70,17 @@ typedef struct {
   int32_t qjl_m;        /* m, number of QJL sign bits per key                  */
   int32_t page_size;    /* P, tokens per page                                  */
   int32_t num_kv_heads; /* H, KV heads per layer                               */
+  /* Variants of "From 0% to 100%: Debugging a KV Cache Compression
+   * Algorithm ...", sections 'The QJL detective story', 'Testing it with an
+   * ablation' and 'Round 2: the llama.cpp bug hunt' (Bug 3).  A zeroed
+   * field keeps the paper's estimator. */
+  int32_t norm_correct; /* 1: store n / ||y_hat|| instead of n, so that the
+                           reconstruction keeps the input's norm (on the GPU:
+                           not for keys with QJL)                           */
+  float qjl_scale;      /* factor of gamma * S^T (2z - 1) in y_hat; 0 means
+                           sqrt(pi/2)/m (Gaussian S).  An orthogonal S takes
+                           sqrt(pi/2)/sqrt(d); a shrinkage a in (0, 1]
+                           multiplies either (2/pi is the MMSE choice)      */
 } tq_format;
 
 /* Byte layout of one page (one pool per layer = [num_pages][H] head-slabs).

@@ -6,6 +6,8 @@ coordinate lies within 1e-4 of a decision boundary; fp32 norms / gammas to
 1e-5 of the vector's max.  Attention: max |o - o_ref| / max |o_ref| <= 2e-3
 per (sequence, query head), the tolerance the benchmark spec's target states.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -32,7 +34,9 @@ def _encode_case(fmt, kind, N, seed, zero_rows=(), neg_slots=()):
     signs = ti.sign_bits(ti.SEED_SIGNS_K if kind == 0 else ti.SEED_SIGNS_V, d)
     bits = fmt.k_bits if kind == 0 else fmt.v_bits
     c, t = oracle.make_codebook(bits)
-    S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if (kind == 0 and fmt.k_qjl) else None
+    S = None
+    if kind == 0 and fmt.k_qjl:
+        S = (ti.orthogonal_matrix if fmt.qjl_scale > 0 else ti.gaussian_matrix)(ti.SEED_QJL, fmt.qjl_m, d)
     pool_ref = np.full(num_pages * lay["page_bytes"], 0x5A, np.uint8)
     rc, u, cm, sm = oracle.encode(fmt, kind, x, perm, pool_ref, num_pages, signs, c, t, S, diagnostics=True)
     assert rc == 0
@@ -74,6 +78,30 @@ def test_decode_matches_oracle(bits, kind, qjl):
     assert np.all(out.cpu().numpy()[z] == 0)
 
 
+ORTH_SHRINK = 0.7 * math.sqrt(math.pi / 2) / math.sqrt(128)  # orthogonal S, 0.7 damping
+
+
+@pytest.mark.parametrize("bits,kind", [(4, 0), (3, 1), (2, 0)])
+def test_encode_norm_correction_matches_oracle(bits, kind):
+    fmt = ti.Format(128, bits, bits, 0, 128, 64, 4, norm_correct=1)
+    pool, pool_ref, lay, slots, cm, sm, *_ = _encode_case(fmt, kind, 200, seed=bits + 50, zero_rows=(9,), neg_slots=(3,))
+    st = compare_encoded(pool, pool_ref, lay, fmt, kind, slots, cm, sm)
+    print("norm-corrected encode", bits, kind, st)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_decode_orthogonal_qjl_factor_matches_oracle(bits):
+    fmt = ti.Format(128, bits, bits, 1, 128, 32, 2, qjl_scale=ORTH_SHRINK)
+    pool, pool_ref, lay, slots, cm, sm, x, signs, c, S, num_pages = _encode_case(fmt, 0, 120, seed=bits + 70)
+    out = tq.tq_decode(fmt, 0, torch.from_numpy(pool_ref).cuda(), num_pages, torch.from_numpy(slots).cuda(),
+                       torch.from_numpy(signs).cuda(), tq.device_codebook(bits), torch.from_numpy(S).cuda())
+    torch.cuda.synchronize()
+    rc, ref = oracle.decode(fmt, 0, pool_ref, num_pages, slots, signs, c, S)
+    assert rc == 0
+    e = rel_err(out.cpu().numpy(), ref)
+    assert e.max() < 1e-5, e.max()
+
+
 ATTN_CASES = {
     # name: (fmt, B, Hq, comp_lens, W, win_lens)
     "k4v4_g4_t2048": (ti.Format(128, 4, 4, 0, 128, 64, 8), 1, 32, [2048], 0, [0]),
@@ -84,6 +112,8 @@ ATTN_CASES = {
     "k2v4_g1": (ti.Format(128, 2, 4, 0, 128, 16, 4), 1, 4, [175], 8, [3]),
     "window_only": (ti.Format(128, 4, 4, 0, 128, 64, 2), 2, 8, [0, 0], 40, [40, 13]),
     "empty_seq": (ti.Format(128, 3, 3, 1, 128, 64, 2), 3, 8, [0, 200, 0], 8, [0, 8, 5]),
+    "k3qjl_orth_shrink_v4_w": (ti.Format(128, 3, 4, 1, 128, 64, 2, qjl_scale=ORTH_SHRINK), 2, 8, [900, 257], 32, [32, 9]),
+    "k4v4_norm_corrected": (ti.Format(128, 4, 4, 0, 128, 64, 4, norm_correct=1), 2, 16, [500, 64], 16, [16, 3]),
 }
 
 

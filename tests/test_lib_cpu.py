@@ -87,6 +87,20 @@ def test_host_validation_before_any_launch(lib):
     assert lib.tq_encode(C.byref(f), 0, dummy, -1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
     assert lib.tq_encode(C.byref(_F(k_qjl=1)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
     assert lib.tq_encode(C.byref(f), 0, P(4098), 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
+    # format variants: norm correction and the QJL factor are validated; the
+    # GPU encode of QJL keys has no norm correction
+    assert lib.tq_encode(C.byref(_F(norm_correct=2)), 1, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
+    assert lib.tq_encode(C.byref(_F(qjl_scale=-1.0)), 1, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
+    assert lib.tq_encode(C.byref(_F(qjl_scale=float("nan"))), 1, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
+    assert lib.tq_encode(C.byref(_F(k_qjl=1, norm_correct=1)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, dummy, None, None) == 2
+    assert lib.tq_encode(C.byref(_F(k_qjl=1, norm_correct=1)), 1, dummy, 0, dummy, dummy, 1, dummy, dummy, None, None, None) == 0
+    # append: window buffers and counters are required with a window
+    assert lib.tq_append_window(C.byref(f), 2, dummy, dummy, None, None, 8, None, None, dummy, dummy, 4, dummy, 4, dummy, dummy,
+                                dummy, dummy, None, dummy, 1 << 20, None, None) == 1
+    assert lib.tq_append_window(C.byref(f), 2, dummy, dummy, None, None, 0, None, None, dummy, dummy, 4, dummy, 4, dummy, dummy,
+                                dummy, dummy, None, dummy, 16, None, None) == 1  # workspace too small
+    n_ws = C.c_size_t(0)
+    assert lib.tq_append_window_workspace_size(C.byref(f), 2, C.byref(n_ws)) == 0 and n_ws.value >= 2 * 2 * 8 * 128 * 2
     # zero tokens is a no-op success without touching the device
     assert lib.tq_encode(C.byref(f), 1, dummy, 0, dummy, dummy, 1, dummy, dummy, None, None, None) == 0
     assert lib.tq_decode(C.byref(f), 1, dummy, 1, dummy, 0, dummy, dummy, None, dummy, None, None) == 0

@@ -152,7 +152,14 @@ class Scenario:
         self.ks, self.vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
         self.kc, self.kt = oracle.make_codebook(fmt.k_bits)
         self.vc, self.vt = oracle.make_codebook(fmt.v_bits)
-        self.S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if fmt.k_qjl else None
+        # a format with its own QJL factor is exercised with an orthogonal S
+        # (the variant that factor exists for); else the paper's Gaussian S
+        if not fmt.k_qjl:
+            self.S = None
+        elif getattr(fmt, "qjl_scale", 0.0) > 0:
+            self.S = ti.orthogonal_matrix(ti.SEED_QJL, fmt.qjl_m, d)
+        else:
+            self.S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d)
         self.kwin = np.zeros((B, H, max(W, 1), d), np.float16)
         self.vwin = np.zeros((B, H, max(W, 1), d), np.float16)
         self.slots = []
