@@ -439,7 +439,7 @@ static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_hea
       !v_codebook || !out || !workspace || (fmt->k_qjl && !S))
     return TQ_ERR_INVALID_ARG;
   if (window > 0 && (!k_win_f16 || !v_win_f16 || !win_lens)) return TQ_ERR_INVALID_ARG;
-  if (!aligned(q_f16, 8) || !aligned(page_pool, 16) || !aligned(workspace, 256) || !aligned(out, 4) ||
+  if (!aligned(q_f16, 8) || !aligned(page_pool, 32) || !aligned(workspace, 256) || !aligned(out, 4) ||
       (fmt->k_qjl && !aligned(S, 16)) || (window > 0 && (!aligned(k_win_f16, 16) || !aligned(v_win_f16, 16))))
     return TQ_ERR_INVALID_ARG;
   AttnPlan p;

@@ -162,6 +162,13 @@ __device__ __forceinline__ float ldna(const float *p) {
   asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
+// 32 bytes in one request (32-byte aligned address): every 32-byte sector a
+// warp touches is then read whole by one request, not half by each of two.
+__device__ __forceinline__ void ldna32B(const void *p, uint32_t (&w)[8]) {
+  asm("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+      : "l"(p));
+}
 template <int NB>
 __device__ __forceinline__ void ldg_words(const uint8_t *p, uint32_t (&w)[NB]) {
   if constexpr (NB == 4) {
@@ -213,9 +220,12 @@ __device__ __forceinline__ void load_values(const AttnArgs &a, const uint8_t *sl
   // contiguous run of 4 * 2VB bytes in the grouped value-code section
   const uint8_t *vc = slab + a.v_codes_o + (int64_t)o0 * VCB + r * (16 * 2 * VB) + t * (4 * 2 * VB);
   if constexpr (VB == 4) {
-    const uint4 x0 = ldna(reinterpret_cast<const uint4 *>(vc)), x1 = ldna(reinterpret_cast<const uint4 *>(vc) + 1);
-    R.vlo[0] = x0.x; R.vhi[0] = x0.y; R.vlo[1] = x0.z; R.vhi[1] = x0.w;
-    R.vlo[2] = x1.x; R.vhi[2] = x1.y; R.vlo[3] = x1.z; R.vhi[3] = x1.w;
+    // 32-byte aligned: sections are multiples of 64 bytes for P % 16 == 0 and
+    // the pool is 32-byte aligned
+    uint32_t w[8];
+    ldna32B(vc, w);
+    R.vlo[0] = w[0]; R.vhi[0] = w[1]; R.vlo[1] = w[2]; R.vhi[1] = w[3];
+    R.vlo[2] = w[4]; R.vhi[2] = w[5]; R.vlo[3] = w[6]; R.vhi[3] = w[7];
   } else if constexpr (VB == 2) {
     const uint4 x0 = ldna(reinterpret_cast<const uint4 *>(vc));
     R.vlo[0] = x0.x; R.vlo[1] = x0.y; R.vlo[2] = x0.z; R.vlo[3] = x0.w;

@@ -245,6 +245,8 @@ tq_status tq_decode_attn_workspace_size(const tq_format *fmt, int batch, int num
  * QJL correction, values are accumulated in the rotated domain and rotated
  * back once per head.  No decoded copy of the cache is ever written.
  *   q_f16        device fp16 [B][Hq][d]; Hq = G * H (GQA, G <= 8)
+ *   page_pool    as for tq_encode, but 32-byte aligned (the kernel reads
+ *                32-byte runs of value codes in single requests)
  *   block_tables device int32 [B][max_pages]: logical page -> pool page
  *   comp_lens    device int32 [B]: compressed tokens (positions [0, comp_len))
  *   k_win_f16, v_win_f16  device fp16 [B][H][window][d] raw recent tokens,
