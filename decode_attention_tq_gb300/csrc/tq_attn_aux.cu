@@ -215,6 +215,7 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
 __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool qjl, int row_blocks) {
   __shared__ __align__(16) float s_q[8 * kQRow];
   __shared__ float s_p[8][kWinChunk];
+  griddep_launch_dependents();  // the main kernel may start building its tables
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (blockIdx.x >= row_blocks) {  // window chunk blocks
     const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
@@ -299,6 +300,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
   __shared__ float s_x[kD];
   __shared__ float s_w[128];
   __shared__ float s_red[4];
+  griddep_wait();  // the main kernel's partials
   const int64_t row = blockIdx.x;  // b * Hq + qh
   const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
   const int h = qh / a.G, g = qh % a.G;
@@ -381,7 +383,8 @@ cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
 }
 
 cudaError_t launch_attn_merge(const AttnArgs &a, cudaStream_t st) {
-  attn_merge_kernel<<<(unsigned)((int64_t)a.B * a.Hq), 128, 0, st>>>(a);
+  const cudaError_t e = launch_maybe_dependent(attn_merge_kernel, dim3((unsigned)((int64_t)a.B * a.Hq)), dim3(128), 0, st, a.pdl, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

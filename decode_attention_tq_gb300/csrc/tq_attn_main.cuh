@@ -451,6 +451,11 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
     for (int i = threadIdx.x; i < EV * 32; i += blockDim.x) lutV[(i >> 5) * 64 + (i & 31)] = val_pair(i >> 5);
   }
   __syncthreads();
+  // Up to here only the codebooks were read; launched as a dependent of the
+  // prep kernel, the table build above overlaps it.  Its outputs (tile
+  // counts, rotated queries) are read below.
+  griddep_wait();
+  griddep_launch_dependents();
 
   const int lane = threadIdx.x & 31, r = lane >> 2, t = lane & 3;
   const int64_t wg = (int64_t)blockIdx.x * attn_warps(NT, QJL) + (threadIdx.x >> 5);
@@ -925,8 +930,7 @@ cudaError_t attn_main_launch_t(const AttnArgs &a, bool query_only, int *blocks_p
   cudaError_t e = set_smem_once(kern, (int)smem_bytes, done);
   if (e != cudaSuccess) return e;
   if (query_only) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kern, attn_threads(NT, QJL), smem_bytes);
-  kern<<<blocks, attn_threads(NT, QJL), smem_bytes, st>>>(a);
-  return cudaGetLastError();
+  return launch_maybe_dependent(kern, dim3(blocks), dim3(attn_threads(NT, QJL)), smem_bytes, st, a.pdl, a);
 }
 
 template <int KB>

@@ -47,6 +47,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Programmatic dependent launch: a kernel launched as a dependent may start
+// while the previous kernel on the stream runs; griddep_wait() blocks until
+// that kernel has completed and its writes are visible (a no-op for a normal
+// launch).  griddep_launch_dependents() lets the next dependent kernel start.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void report(int32_t *err_word, int32_t bit) {
   if (err_word) atomicOr(err_word, bit);
 }

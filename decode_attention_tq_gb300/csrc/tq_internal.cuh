@@ -2,6 +2,8 @@
 // libtq translation units.
 #pragma once
 
+#include <utility>
+
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
@@ -107,10 +109,30 @@ struct AttnArgs {
   float *win_acc;    // [B][Hq][window chunks][d]  raw-domain window accumulators
   int nw_launch;     // warps launched for the main kernel
   int min_tiles;     // fewest tiles a warp is given
+  bool pdl;          // host: launch main and merge as programmatic dependents
 };
 
 cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
 cudaError_t launch_window_roll(const RollArgs &a, cudaStream_t st);
+
+// Launch `kern` on `st`, as a programmatic dependent of the previous kernel on
+// the stream when `dependent` (the kernel must call griddep_wait() before it
+// reads that kernel's outputs).
+template <typename... P, typename... A>
+cudaError_t launch_maybe_dependent(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                   bool dependent, A &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
 cudaError_t launch_encode_kv(const EncodeArgs &ka, const EncodeArgs &va, int bits, int sms, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
 
