@@ -13,6 +13,7 @@ from .tq import (  # noqa: F401
     TQ_STATIC_SCRATCH_BYTES,
     TQError,
     device_codebook,
+    kind_codebook,
     load_library,
     tq_decode,
     tq_decode_attn,

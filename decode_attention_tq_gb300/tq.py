@@ -39,7 +39,7 @@ class TQError(RuntimeError):
 
 class tq_format(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "k_qjl", "qjl_m", "page_size", "num_kv_heads",
-                                         "norm_correct")] + [("qjl_scale", C.c_float)]
+                                         "norm_correct")] + [("qjl_scale", C.c_float), ("k_mixed", C.c_int32)]
 
 
 class tq_layout(C.Structure):
@@ -140,6 +140,15 @@ def device_codebook(bits: int, device="cuda") -> torch.Tensor:
     """centroids || midpoints as the fp32 device array the kernels take."""
     c, t = tq_make_codebook(bits)
     return torch.from_numpy(np.concatenate([c, t])).to(device)
+
+
+def kind_codebook(fmt, kind: int, device="cuda") -> torch.Tensor:
+    """The device codebook of one kind of `fmt`: device_codebook(bits), or for
+    mixed-rate keys device_codebook(k_bits + 1) followed by device_codebook(k_bits)."""
+    F = _fmt(fmt)
+    if kind == TQ_KIND_K and F.k_mixed:
+        return torch.cat([device_codebook(F.k_bits + 1, device), device_codebook(F.k_bits, device)])
+    return device_codebook(F.k_bits if kind == TQ_KIND_K else F.v_bits, device)
 
 
 # ----------------------------------------------------------------- device --

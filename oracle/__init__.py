@@ -40,7 +40,7 @@ def build(force: bool = False) -> str:
 
 class _Format(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "k_qjl", "qjl_m", "page_size", "num_kv_heads",
-                                         "norm_correct")] + [("qjl_scale", C.c_float)]
+                                         "norm_correct")] + [("qjl_scale", C.c_float), ("k_mixed", C.c_int32)]
 
 
 class _Layout(C.Structure):
@@ -68,8 +68,8 @@ def _load():
             lib.orc_rotate.restype = None
             lib.orc_unrotate.argtypes = [C.c_int, P, P, P]
             lib.orc_unrotate.restype = None
-            lib.orc_encode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int] + [P] * 12 + [C.c_int, dbl]
-            lib.orc_decode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, dbl, dbl] + [P] * 6 + [dbl]
+            lib.orc_encode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int] + [P] * 12 + [C.c_int, dbl, C.c_int, P, P]
+            lib.orc_decode_vector.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, dbl, dbl] + [P] * 6 + [dbl, C.c_int, P]
             lib.orc_pack_bits.argtypes = [C.c_int, C.c_int, P, P]
             lib.orc_pack_bits.restype = None
             lib.orc_unpack_bits.argtypes = [C.c_int, C.c_int, P, P]
@@ -92,7 +92,7 @@ def _c(a, dtype):
 
 def _fmt(f) -> _Format:
     return _Format(int(f.head_dim), int(f.k_bits), int(f.v_bits), int(f.k_qjl), int(f.qjl_m), int(f.page_size), int(f.num_kv_heads),
-                   int(getattr(f, "norm_correct", 0)), float(getattr(f, "qjl_scale", 0.0)))
+                   int(getattr(f, "norm_correct", 0)), float(getattr(f, "qjl_scale", 0.0)), int(getattr(f, "k_mixed", 0)))
 
 
 def _f16bits(x) -> np.ndarray:
@@ -118,6 +118,18 @@ def lloyd_max_f64(bits: int):
         raise ValueError("bad bits")
     L = 1 << bits
     return c[:L].copy(), t[: L - 1].copy(), it
+
+
+def kind_codebook(f, kind: int):
+    """(centroids, midpoints) a kind of format f is encoded with: one
+    codebook, or for mixed-rate keys the k_bits + 1 codebook followed by the
+    k_bits one (the layout of the device codebooks)."""
+    bits = int(f.k_bits if kind == 0 else f.v_bits)
+    if kind == 0 and int(getattr(f, "k_mixed", 0)):
+        ch, th = make_codebook(bits + 1)
+        cl, tl = make_codebook(bits)
+        return np.concatenate([ch, cl]).astype(np.float32), np.concatenate([th, tl]).astype(np.float32)
+    return make_codebook(bits)
 
 
 def make_codebook(bits: int):
@@ -164,10 +176,12 @@ def qjl_coef(qjl_m: int, qjl_scale: float = 0.0) -> float:
     return float(qjl_scale) if qjl_scale > 0 else math.sqrt(math.pi / 2) / qjl_m
 
 
-def encode_vector(x, bits, signs, centroids, midpoints, S=None, qjl_m=0, norm_correct=0, qjl_scale=0.0):
+def encode_vector(x, bits, signs, centroids, midpoints, S=None, qjl_m=0, norm_correct=0, qjl_scale=0.0, lo_codebook=None):
     """Encode one vector (fp64 values).  Returns a dict with norm, gamma, idx,
     z, u, code_margin, sign_margin.  With norm_correct the returned norm is
-    ||x|| / ||y_hat|| (y_hat with the QJL factor of qjl_coef)."""
+    ||x|| / ||y_hat|| (y_hat with the QJL factor of qjl_coef).  With
+    lo_codebook = (centroids, midpoints) of bits - 1 the vector is mixed-rate:
+    high channels ((j mod 16) < 8) use `bits`, the others bits - 1."""
     x = _c(x, np.float64)
     d = x.shape[0]
     qjl = S is not None
@@ -183,14 +197,16 @@ def encode_vector(x, bits, signs, centroids, midpoints, S=None, qjl_m=0, norm_co
     rc = _load().orc_encode_vector(
         d, bits, int(qjl), m, _ptr(x), _ptr(_c(signs, np.uint8)), _ptr(_c(centroids, np.float32)),
         _ptr(_c(midpoints, np.float32)), _ptr(Sa), C.byref(norm), C.byref(gamma), _ptr(idx), _ptr(z), _ptr(u), _ptr(cm), _ptr(sm),
-        int(norm_correct), qjl_coef(m, qjl_scale) if qjl else 0.0,
+        int(norm_correct), qjl_coef(m, qjl_scale) if qjl else 0.0, int(lo_codebook is not None),
+        _ptr(None if lo_codebook is None else _c(lo_codebook[0], np.float32)),
+        _ptr(None if lo_codebook is None else _c(lo_codebook[1], np.float32)),
     )
     if rc != 0:
         raise ValueError(f"orc_encode_vector rc={rc}")
     return dict(norm=norm.value, gamma=gamma.value, idx=idx, z=z[:m], u=u, code_margin=cm, sign_margin=sm[:m])
 
 
-def decode_vector(norm, idx, bits, signs, centroids, gamma=0.0, z=None, S=None, qjl_m=0, qjl_scale=0.0):
+def decode_vector(norm, idx, bits, signs, centroids, gamma=0.0, z=None, S=None, qjl_m=0, qjl_scale=0.0, lo_centroids=None):
     idx = _c(idx, np.int32)
     d = idx.shape[0]
     qjl = S is not None
@@ -201,6 +217,7 @@ def decode_vector(norm, idx, bits, signs, centroids, gamma=0.0, z=None, S=None, 
     rc = _load().orc_decode_vector(
         d, bits, int(qjl), m, float(norm), float(gamma), _ptr(idx), _ptr(za), _ptr(_c(signs, np.uint8)),
         _ptr(_c(centroids, np.float32)), _ptr(Sa), _ptr(out), qjl_coef(m, qjl_scale) if qjl else 0.0,
+        int(lo_centroids is not None), _ptr(None if lo_centroids is None else _c(lo_centroids, np.float32)),
     )
     if rc != 0:
         raise ValueError(f"orc_decode_vector rc={rc}")

@@ -70,7 +70,16 @@ typedef struct {
   int32_t head_dim, k_bits, v_bits, k_qjl, qjl_m, page_size, num_kv_heads;
   int32_t norm_correct; /* store n / ||y_hat|| (Bug 3 of the debugging post) */
   float qjl_scale;      /* factor of gamma S^T (2z - 1); 0: sqrt(pi/2) / m   */
+  int32_t k_mixed;      /* keys at a fractional rate: b+1 bits on half the channels */
 } orc_format;
+
+/* Mixed-channel rates ("TurboQuant Family Design Study ...", 'Packed format
+ * and complete bit accounting': 3.5 bits per channel = 64 channels at 4 bits
+ * and 64 at 3; 2.5 = 64 at 3 and 64 at 2).  Which half carries the extra bit
+ * is not fixed by the page; here channel j is a high channel when
+ * (j mod 16) < 8.  A mixed code stream holds the high channels' codes first,
+ * then the low channels', each in channel order and LSB-first. */
+static int is_high_channel(int j) { return (j & 15) < 8; }
 
 /* The QJL dequantization factor: the paper's sqrt(pi/2)/m for a Gaussian S
  * ("The QJL detective story"), or the format's own (an orthogonal S takes
@@ -205,7 +214,7 @@ void orc_unrotate(int d, const uint8_t *signs, const double *y, double *x) {
 
 int orc_decode_vector(int d, int bits, int qjl, int m, double norm, double gamma, const int32_t *idx,
                       const uint8_t *z, const uint8_t *signs, const float *centroids, const float *S,
-                      double *out, double qjl_coef);
+                      double *out, double qjl_coef, int mixed, const float *lo_centroids);
 
 /*
  * Encode one head vector x[d] (fp64 values of the fp16 input).
@@ -221,9 +230,9 @@ int orc_decode_vector(int d, int bits, int qjl, int m, double norm, double gamma
 int orc_encode_vector(int d, int bits, int qjl, int m, const double *x, const uint8_t *signs,
                       const float *centroids, const float *midpoints, const float *S,
                       double *norm, double *gamma, int32_t *idx, uint8_t *z, double *u_out,
-                      double *code_margin, double *sign_margin, int norm_correct, double qjl_coef) {
-  if (!is_pow2(d) || bits < 1 || bits > 8 || (qjl && m < 1)) return ORC_ERR_ARG;
-  int L = 1 << bits;
+                      double *code_margin, double *sign_margin, int norm_correct, double qjl_coef,
+                      int mixed, const float *lo_centroids, const float *lo_midpoints) {
+  if (!is_pow2(d) || bits < 1 || bits > 8 || (qjl && m < 1) || (mixed && bits < 2)) return ORC_ERR_ARG;
   double *w = (double *)malloc(sizeof(double) * d);
   double *e = (double *)malloc(sizeof(double) * d);
   double ss = 0.0;
@@ -249,18 +258,23 @@ int orc_encode_vector(int d, int bits, int qjl, int m, const double *x, const ui
   for (int j = 0; j < d; j++) w[j] = rademacher(signs, j) * x[j];
   orc_fwht(w, d);
   for (int j = 0; j < d; j++) {
+    /* this channel's width and codebook: `bits` on high channels of a mixed
+       kind (and on every channel otherwise), bits - 1 on its low channels */
+    const int lo = mixed && !is_high_channel(j);
+    const int bj = lo ? bits - 1 : bits, Lj = 1 << bj;
+    const float *cj = lo ? lo_centroids : centroids, *tj = lo ? lo_midpoints : midpoints;
     double u = w[j] / n;
-    idx[j] = orc_quantize_scalar(bits, midpoints, u);
+    idx[j] = orc_quantize_scalar(bj, tj, u);
     if (u_out) u_out[j] = u;
     if (code_margin) {
       double mg = INFINITY;
-      for (int k = 0; k + 1 < L; k++) {
-        double dd = fabs(u - (double)midpoints[k]);
+      for (int k = 0; k + 1 < Lj; k++) {
+        double dd = fabs(u - (double)tj[k]);
         if (dd < mg) mg = dd;
       }
       code_margin[j] = mg;
     }
-    e[j] = (u - (double)centroids[idx[j]]) / sqrt((double)d);
+    e[j] = (u - (double)cj[idx[j]]) / sqrt((double)d);
   }
   if (qjl) {
     double g2 = 0.0;
@@ -277,7 +291,8 @@ int orc_encode_vector(int d, int bits, int qjl, int m, const double *x, const ui
   if (norm_correct) {
     /* ||decode(norm = 1)|| = ||y_hat|| (H / sqrt(d) and the signs are orthogonal) */
     double *r = w;
-    orc_decode_vector(d, bits, qjl, m, 1.0, qjl ? *gamma : 0.0, idx, z, signs, centroids, S, r, qjl_coef);
+    orc_decode_vector(d, bits, qjl, m, 1.0, qjl ? *gamma : 0.0, idx, z, signs, centroids, S, r, qjl_coef, mixed,
+                      lo_centroids);
     double r2 = 0.0;
     for (int j = 0; j < d; j++) r2 += r[j] * r[j];
     if (r2 > 0.0) *norm = n / sqrt(r2);
@@ -295,10 +310,11 @@ int orc_encode_vector(int d, int bits, int qjl, int m, const double *x, const ui
  */
 int orc_decode_vector(int d, int bits, int qjl, int m, double norm, double gamma, const int32_t *idx,
                       const uint8_t *z, const uint8_t *signs, const float *centroids, const float *S,
-                      double *out, double qjl_coef) {
+                      double *out, double qjl_coef, int mixed, const float *lo_centroids) {
   if (!is_pow2(d) || bits < 1 || bits > 8 || (qjl && m < 1)) return ORC_ERR_ARG;
   double *y = (double *)malloc(sizeof(double) * d);
-  for (int j = 0; j < d; j++) y[j] = (double)centroids[idx[j]] / sqrt((double)d);
+  for (int j = 0; j < d; j++)
+    y[j] = (double)((mixed && !is_high_channel(j)) ? lo_centroids : centroids)[idx[j]] / sqrt((double)d);
   if (qjl) {
     double scale = qjl_coef * gamma;
     for (int j = 0; j < d; j++) {
@@ -339,6 +355,36 @@ void orc_unpack_bits(int count, int b, const uint8_t *in, int32_t *vals) {
 
 /* ---------------------------------------------------------- page layout -- */
 
+/* One vector's code stream: LSB-first codes of every channel at `bits` bits,
+ * or for a mixed kind the high channels' codes at `bits` bits followed by the
+ * low channels' at bits - 1 (see is_high_channel). */
+static void pack_codes(int d, int bits, int mixed, const int32_t *idx, uint8_t *out) {
+  if (!mixed) {
+    orc_pack_bits(d, bits, idx, out);
+    return;
+  }
+  int32_t hi[d / 2], lo[d / 2];
+  int nh = 0, nl = 0;
+  for (int j = 0; j < d; j++) {
+    if (is_high_channel(j)) hi[nh++] = idx[j];
+    else lo[nl++] = idx[j];
+  }
+  orc_pack_bits(nh, bits, hi, out);
+  orc_pack_bits(nl, bits - 1, lo, out + nh * bits / 8);
+}
+
+static void unpack_codes(int d, int bits, int mixed, const uint8_t *in, int32_t *idx) {
+  if (!mixed) {
+    orc_unpack_bits(d, bits, in, idx);
+    return;
+  }
+  int32_t hi[d / 2], lo[d / 2];
+  orc_unpack_bits(d / 2, bits, in, hi);
+  orc_unpack_bits(d / 2, bits - 1, in + (d / 2) * bits / 8, lo);
+  int nh = 0, nl = 0;
+  for (int j = 0; j < d; j++) idx[j] = is_high_channel(j) ? hi[nh++] : lo[nl++];
+}
+
 static int64_t align16(int64_t x) { return (x + 15) / 16 * 16; }
 
 /*
@@ -378,8 +424,11 @@ int orc_page_layout(const orc_format *f, orc_layout *L) {
     return ORC_ERR_ARG;
   if ((f->head_dim * f->k_bits) % 8 || (f->head_dim * f->v_bits) % 8) return ORC_ERR_ARG;
   if (f->k_qjl && (f->qjl_m < 8 || f->qjl_m % 8)) return ORC_ERR_ARG;
+  if (f->k_mixed != 0 && f->k_mixed != 1) return ORC_ERR_ARG;
+  if (f->k_mixed && f->k_bits + 1 > 8) return ORC_ERR_ARG;
   int64_t P = f->page_size, off = 0;
-  L->k_code_bytes = f->head_dim * f->k_bits / 8;
+  /* mixed keys: d/2 channels at k_bits + 1 and d/2 at k_bits */
+  L->k_code_bytes = f->k_mixed ? (f->head_dim / 2) * (2 * f->k_bits + 1) / 8 : f->head_dim * f->k_bits / 8;
   L->v_code_bytes = f->head_dim * f->v_bits / 8;
   L->k_sign_bytes = f->k_qjl ? f->qjl_m / 8 : 0;
   L->k_norm = off;
@@ -420,7 +469,12 @@ int orc_encode(const orc_format *f, int kind, const uint16_t *x, int64_t N, cons
   orc_layout L;
   if (orc_page_layout(f, &L) != ORC_OK) return ORC_ERR_ARG;
   int d = f->head_dim, H = f->num_kv_heads, P = f->page_size;
-  int bits = kind == 0 ? f->k_bits : f->v_bits;
+  /* mixed keys: `centroids` / `midpoints` hold the k_bits + 1 codebook, then
+     the k_bits one (the layout of the device codebooks) */
+  int mixed = kind == 0 && f->k_mixed;
+  int bits = kind == 0 ? f->k_bits + mixed : f->v_bits;
+  const float *lo_c = mixed ? centroids + (1 << bits) : NULL;
+  const float *lo_t = mixed ? midpoints + (1 << bits) - 1 : NULL;
   int qjl = (kind == 0) && f->k_qjl;
   int m = qjl ? f->qjl_m : 0;
   int code_bytes = kind == 0 ? L.k_code_bytes : L.v_code_bytes;
@@ -445,11 +499,12 @@ int orc_encode(const orc_format *f, int kind, const uint16_t *x, int64_t N, cons
       int64_t vh = n * H + h;
       orc_encode_vector(d, bits, qjl, m, xv, signs, centroids, midpoints, S, &norm, &gamma, idx, z,
                         u_out ? u_out + vh * d : NULL, code_margin ? code_margin + vh * d : NULL,
-                        sign_margin ? sign_margin + vh * m : NULL, f->norm_correct, orc_qjl_coef(f));
+                        sign_margin ? sign_margin + vh * m : NULL, f->norm_correct, orc_qjl_coef(f), mixed, lo_c,
+                        lo_t);
       uint8_t *slab = pool + page * L.page_bytes + (int64_t)h * L.slab_bytes;
       if (kind == 0) {
         put_f32(slab + L.k_norm + 4 * off, (float)norm);
-        orc_pack_bits(d, bits, idx, slab + L.k_codes + off * code_bytes);
+        pack_codes(d, bits, mixed, idx, slab + L.k_codes + off * code_bytes);
         if (qjl) {
           put_f32(slab + L.k_gamma + 4 * off, (float)gamma);
           for (int l = 0; l < m; l++) zi[l] = z[l];
@@ -479,21 +534,23 @@ static void decode_slot(const orc_format *f, const orc_layout *L, int kind, cons
   const uint8_t *slab = pool + page * L->page_bytes + (int64_t)h * L->slab_bytes;
   if (kind == 0) {
     int qjl = f->k_qjl, m = qjl ? f->qjl_m : 0;
+    int mixed = f->k_mixed, bits = f->k_bits + mixed;
     double norm = get_f32(slab + L->k_norm + 4 * off);
-    orc_unpack_bits(d, f->k_bits, slab + L->k_codes + off * L->k_code_bytes, idx);
+    unpack_codes(d, bits, mixed, slab + L->k_codes + off * L->k_code_bytes, idx);
     double gamma = 0.0;
     if (qjl) {
       gamma = get_f32(slab + L->k_gamma + 4 * off);
       orc_unpack_bits(m, 1, slab + L->k_signs + off * L->k_sign_bytes, zi);
       for (int l = 0; l < m; l++) z[l] = (uint8_t)zi[l];
     }
-    orc_decode_vector(d, f->k_bits, qjl, m, norm, gamma, idx, z, signs, centroids, S, out, orc_qjl_coef(f));
+    orc_decode_vector(d, bits, qjl, m, norm, gamma, idx, z, signs, centroids, S, out, orc_qjl_coef(f), mixed,
+                      mixed ? centroids + (1 << bits) : NULL);
   } else {
     double norm = get_f32(slab + L->v_norm + 4 * off);
     uint8_t stream[L->v_code_bytes];
     get_v_codes(slab + L->v_codes, off, d, f->v_bits, stream);
     orc_unpack_bits(d, f->v_bits, stream, idx);
-    orc_decode_vector(d, f->v_bits, 0, 0, norm, 0.0, idx, NULL, signs, centroids, NULL, out, 0.0);
+    orc_decode_vector(d, f->v_bits, 0, 0, norm, 0.0, idx, NULL, signs, centroids, NULL, out, 0.0, 0, NULL);
   }
 }
 

@@ -146,6 +146,7 @@ class Format:
     num_kv_heads: int = 8
     norm_correct: int = 0
     qjl_scale: float = 0.0
+    k_mixed: int = 0
 
 
 @dataclasses.dataclass(frozen=True)
