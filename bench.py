@@ -187,8 +187,8 @@ class DecodeBench:
         self.win_lens = torch.full((B,), wl.win_tokens, dtype=torch.int32, device=device)
         self.ks = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_K, d)).to(device)
         self.vs = torch.from_numpy(ti.sign_bits(ti.SEED_SIGNS_V, d)).to(device)
-        self.kcb = tq.device_codebook(f.k_bits, device)
-        self.vcb = tq.device_codebook(f.v_bits, device)
+        self.kcb = tq.kind_codebook(f, 0, device)
+        self.vcb = tq.kind_codebook(f, 1, device)
         self.S = torch.from_numpy(ti.gaussian_matrix(ti.SEED_QJL, f.qjl_m, d)).to(device) if f.k_qjl else None
         page_bytes = tq.tq_page_layout(f)["page_bytes"]
         flat_slots = slots.reshape(-1).to(torch.int32).contiguous()
@@ -229,7 +229,7 @@ class DecodeBench:
         self.main_bytes = B * H * comp * (bph["k"] + bph["v"]) + B * self.pages_per_seq * 4  # per layer launch
         self.window_bytes = B * H * wl.win_tokens * d * 2 * 2
         self.step_bytes = wl.layers * (self.main_bytes + self.window_bytes + B * Hq * d * (2 + 4))
-        appends = 1 if (f.k_bits == f.v_bits and not f.k_qjl) else 2  # one joint K+V encode launch, or K then V
+        appends = 1 if (f.k_bits == f.v_bits and not f.k_qjl and not f.k_mixed) else 2  # one joint K+V encode launch, or K then V
         self.launches_per_step = wl.layers * (1 + appends + 3)  # window roll, encode, prep (with window chunks), main, merge
 
     def step(self, events=None):
@@ -330,7 +330,7 @@ def run_decode(args, device, barrier, reduce_max, rank, world):
         "config": {
             "workload": wl.name, "layers": wl.layers, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
             "head_dim": wl.fmt.head_dim, "context": wl.context, "window": wl.window, "page_size": wl.fmt.page_size,
-            "k_bits": wl.fmt.k_bits, "v_bits": wl.fmt.v_bits, "k_qjl": wl.fmt.k_qjl, "step": "per layer: append 1 token/seq + decode attention",
+            "k_bits": wl.fmt.k_bits + 0.5 * wl.fmt.k_mixed, "v_bits": wl.fmt.v_bits, "k_qjl": wl.fmt.k_qjl, "step": "per layer: append 1 token/seq + decode attention",
             "l2": "working set (cache %.1f GB) >> L2; no flush" % (bench.step_bytes / 1e9), "cuda_graph": graph is not None,
         },
         "hbm_gbs": bench.step_bytes / (ms * 1e-3) / 1e9,
@@ -481,8 +481,8 @@ def oracle_sample_setup(wl: ti.DecodeWorkload, n_seq: int, device: str | None):
     lay = oracle.page_layout(f)
     pool = np.zeros(num_pages * lay["page_bytes"], np.uint8)
     ks, vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
-    kc, kt = oracle.make_codebook(f.k_bits)
-    vc, vt = oracle.make_codebook(f.v_bits)
+    kc, kt = oracle.kind_codebook(f, 0)
+    vc, vt = oracle.kind_codebook(f, 1)
     S = ti.gaussian_matrix(ti.SEED_QJL, f.qjl_m, d) if f.k_qjl else None
     jobs = []
     for b in range(n_seq):

@@ -22,6 +22,8 @@ bool format_valid(const tq_format *f) {
   if (f->k_qjl && (f->qjl_m < 8 || f->qjl_m % 8)) return false;
   if (f->page_size < 16 || f->page_size % 16 || f->num_kv_heads < 1) return false;
   if (f->norm_correct != 0 && f->norm_correct != 1) return false;
+  if (f->k_mixed != 0 && f->k_mixed != 1) return false;
+  if (f->k_mixed && f->k_bits + 1 > 8) return false;
   if (!(f->qjl_scale >= 0.0f) || !isfinite(f->qjl_scale)) return false;
   return true;
 }
@@ -34,7 +36,8 @@ float qjl_coef(const tq_format *f) {
 bool bits_supported(int b) { return b >= 2 && b <= 4; }
 
 bool format_gpu_supported(const tq_format *f) {
-  return f->head_dim == kD && bits_supported(f->k_bits) && bits_supported(f->v_bits) &&
+  return f->head_dim == kD && bits_supported(f->k_bits) && bits_supported(f->k_bits + f->k_mixed) &&
+         bits_supported(f->v_bits) &&
          (!f->k_qjl || f->qjl_m == kM) && f->page_size % kTile == 0;
 }
 
@@ -42,7 +45,8 @@ int64_t round16(int64_t x) { return (x + 15) & ~int64_t(15); }
 
 void compute_layout(const tq_format *f, tq_layout *L) {
   const int64_t P = f->page_size;
-  L->k_code_bytes = f->head_dim * f->k_bits / 8;
+  // mixed keys: d/2 channels at k_bits + 1 and d/2 at k_bits
+  L->k_code_bytes = f->k_mixed ? (f->head_dim / 2) * (2 * f->k_bits + 1) / 8 : f->head_dim * f->k_bits / 8;
   L->v_code_bytes = f->head_dim * f->v_bits / 8;
   L->k_sign_bytes = f->k_qjl ? f->qjl_m / 8 : 0;
   int64_t cursor = 0;
@@ -131,6 +135,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 cudaError_t main_kernel_call(const tq_format *f, const AttnArgs &a, int nt, bool query, int *bps, int blocks,
                              cudaStream_t st) {
+  if (f->k_mixed) {
+    switch (f->k_bits) {
+      case 2: return attn_main_k23(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
+      case 3: return attn_main_k34(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (f->k_bits) {
     case 2: return attn_main_k2(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
     case 3: return attn_main_k3(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
@@ -141,7 +152,7 @@ cudaError_t main_kernel_call(const tq_format *f, const AttnArgs &a, int nt, bool
 
 // Occupancy of each main-kernel instance, per device (queried once).
 std::mutex g_occ_mu;
-int g_occ[64][3][3][2][2];  // [device][kb-2][vb-2][qjl][nt-1]; 0 = unknown
+int g_occ[64][5][3][2][2];  // [device][key widths][vb-2][qjl][nt-1]; 0 = unknown
 
 tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int window, AttnPlan *p) {
   const int H = f->num_kv_heads;
@@ -153,7 +164,8 @@ tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int w
   int bps = 0;
   {
     std::lock_guard<std::mutex> lk(g_occ_mu);
-    int *slot = dev < 64 ? &g_occ[dev][f->k_bits - 2][f->v_bits - 2][f->k_qjl][p->NT - 1] : nullptr;
+    const int kw = f->k_mixed ? 3 + (f->k_bits - 2) : f->k_bits - 2;  // 2, 3, 4, then 2.5, 3.5
+    int *slot = dev < 64 ? &g_occ[dev][kw][f->v_bits - 2][f->k_qjl][p->NT - 1] : nullptr;
     if (slot && *slot > 0) {
       bps = *slot;
     } else {
@@ -280,21 +292,24 @@ tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n
   if (n_tokens == 0) return TQ_OK;
   int sms = 0;
   if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
-  const int bits = kind == TQ_KIND_K ? fmt->k_bits : fmt->v_bits;
+  const bool mixed = kind == TQ_KIND_K && fmt->k_mixed;  // width below: the high channels'
+  const int bits = kind == TQ_KIND_K ? fmt->k_bits + (mixed ? 1 : 0) : fmt->v_bits;
   const bool qjl = kind == TQ_KIND_K && fmt->k_qjl;
-  return launch_encode(a, bits, qjl, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_encode(a, bits, qjl, mixed, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK
+                                                                                                    : TQ_ERR_CUDA;
 }
 
-// K then V of one append: one launch when both kinds share a bit width and
-// keys carry no QJL sketch, else two.
+// K then V of one append: one launch when both kinds share a uniform bit
+// width and keys carry no QJL sketch, else two.
 static tq_status launch_kv(const tq_format *fmt, const EncodeArgs &ka, const EncodeArgs &va, void *stream) {
   int sms = 0;
   if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (fmt->k_bits == fmt->v_bits && !fmt->k_qjl)
+  if (fmt->k_bits == fmt->v_bits && !fmt->k_qjl && !fmt->k_mixed)
     return launch_encode_kv(ka, va, fmt->k_bits, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
-  if (launch_encode(ka, fmt->k_bits, fmt->k_qjl != 0, sms, st) != cudaSuccess) return TQ_ERR_CUDA;
-  return launch_encode(va, fmt->v_bits, false, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  if (launch_encode(ka, fmt->k_bits + fmt->k_mixed, fmt->k_qjl != 0, fmt->k_mixed != 0, sms, st) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  return launch_encode(va, fmt->v_bits, false, false, sms, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 tq_status tq_encode_kv(const tq_format *fmt, const void *k_f16, const void *v_f16, int64_t n_tokens,
@@ -410,8 +425,10 @@ tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64
   a.err_word = err_word;
   int sms = 0;
   if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
-  const int bits = kind == TQ_KIND_K ? fmt->k_bits : fmt->v_bits;
-  return launch_decode(a, bits, qjl, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  const bool mixed = kind == TQ_KIND_K && fmt->k_mixed;
+  const int bits = kind == TQ_KIND_K ? fmt->k_bits + (mixed ? 1 : 0) : fmt->v_bits;
+  return launch_decode(a, bits, qjl, mixed, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK
+                                                                                                    : TQ_ERR_CUDA;
 }
 
 tq_status tq_decode_attn_workspace_size(const tq_format *fmt, int batch, int num_q_heads, int max_pages, int window,

@@ -35,11 +35,27 @@
 
 namespace tq {
 
+// Key code widths.  KB = 2, 3, 4: every channel at KB bits.  KB = 34 or 23:
+// mixed-rate keys ("TurboQuant Family Design Study ...", 'Packed format and
+// complete bit accounting': 3.5 and 2.5 bits per channel), KB % 10 bits on
+// the channels j with (j mod 16) < 8 and KB / 10 on the others; a token's
+// stream holds the high channels' codes, then the low ones'.  Lane t's 32
+// channels 32t..32t+31 are 16 of each: high codes 16t..16t+15 and low codes
+// 16t..16t+15 of the two streams, used by the k-steps kk with (kk mod 4) < 2
+// and >= 2 respectively.
+__host__ __device__ constexpr bool kb_mixed(int KB) { return KB > 8; }
+__host__ __device__ constexpr int kb_hi(int KB) { return KB > 8 ? KB % 10 : KB; }
+__host__ __device__ constexpr int kb_lo(int KB) { return KB > 8 ? KB / 10 : KB; }
+__host__ __device__ constexpr int key_words(int KB) { return KB > 8 ? 4 : KB; }  // code registers per slice
+__host__ __device__ constexpr int key_token_bytes(int KB) { return KB > 8 ? 8 * (kb_hi(KB) + kb_lo(KB)) : 16 * KB; }
+
 // Registers of one 16-token tile, key half and value half (loaded apart so
 // that the keys of the next tile can be in flight while a tile is scored).
 template <int KB, bool QJL>
 struct KeyRegs {
-  uint32_t k0[KB], k1[KB];  // key code slice t (coords 32t..32t+31) of tokens r, r+8
+  // key code slice t (coords 32t..32t+31) of tokens r, r+8; mixed keys: high
+  // codes in words 0-1, low codes in words 2-3
+  uint32_t k0[key_words(KB)], k1[key_words(KB)];
   float nk0, nk1;           // key norms of tokens r, r+8
   float g0, g1;             // QJL gammas
   uint32_t s0, s1;          // QJL sign word t of tokens r, r+8
@@ -78,6 +94,14 @@ __device__ __forceinline__ uint32_t key_addr(const uint32_t (&w)[KB], int p, uin
     const int bit = 2 * KB * p, wi = bit >> 5;
     return field_at<8>(w[wi], (wi + 1 < KB) ? w[wi + 1] : 0u, bit & 31, 2 * KB, laneK);
   }
+}
+
+// Table offset of code pair p (codes 2p, 2p+1) of a 16-code stream slice of
+// BITS-bit codes held in (w1:w0): base | pair code << 8.
+template <int BITS>
+__device__ __forceinline__ uint32_t mixed_pair_addr(uint32_t w0, uint32_t w1, int p, uint32_t base) {
+  if constexpr (BITS == 4) return __byte_perm(p < 4 ? w0 : w1, base, 0x7604 | ((p & 3) << 4));
+  else return field_at<8>(w0, w1, 2 * BITS * p, 2 * BITS, base);
 }
 
 // +-1 fp16 pair from sign bits p and p+16 of a word (bit set -> +1).
@@ -183,18 +207,53 @@ __device__ __forceinline__ void ldg_words(const uint8_t *p, uint32_t (&w)[NB]) {
   }
 }
 
+// 16 codes of BITS bits starting at byte `off` of a token's key stream (the
+// stream starts 8-byte aligned; `off` is a multiple of 8 for 4-bit codes, of
+// 4 for 2-bit codes and even for 3-bit codes), as bits 0.. of (w0, w1).
+template <int BITS>
+__device__ __forceinline__ void load_codes16(const uint8_t *tok, int off, uint32_t &w0, uint32_t &w1) {
+  if constexpr (BITS == 4) {
+    const uint2 v = ldna(reinterpret_cast<const uint2 *>(tok + off));
+    w0 = v.x;
+    w1 = v.y;
+  } else if constexpr (BITS == 2) {
+    w0 = ldna(reinterpret_cast<const uint32_t *>(tok + off));
+    w1 = 0u;
+  } else {  // 6 bytes at an even offset: the two aligned words around them
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(tok + (off & ~3));
+    const uint32_t a0 = ldna(p), a1 = ldna(p + 1);
+    const int sh = (off & 3) * 8;
+    w0 = __funnelshift_r(a0, a1, sh);
+    w1 = a1 >> sh;
+  }
+}
+
+// Lane t's mixed-rate key slice of one token.
+template <int KB>
+__device__ __forceinline__ void load_mixed_slice(const uint8_t *tok, int t, uint32_t (&w)[4]) {
+  constexpr int HB = kb_hi(KB), LB = kb_lo(KB);
+  load_codes16<HB>(tok, 2 * HB * t, w[0], w[1]);
+  load_codes16<LB>(tok, 8 * HB + 2 * LB * t, w[2], w[3]);
+}
+
 // Key registers of the 16-token tile at offset o0 of a page slab; `live` is
 // the number of leading tokens of the tile that are compressed tokens (0 for
 // a page outside the pool).
 template <int KB, bool QJL>
 __device__ __forceinline__ void load_keys(const AttnArgs &a, const uint8_t *slab, int o0, int live, int r, int t,
                                           KeyRegs<KB, QJL> &R) {
-  constexpr int KCB = 16 * KB;
+  constexpr int KCB = key_token_bytes(KB);
   R.ok0 = r < live;
   R.ok1 = r + 8 < live;
-  const uint8_t *kc = slab + a.k_codes_o + t * 4 * KB;
-  ldg_words<KB>(kc + (o0 + r) * KCB, R.k0);
-  ldg_words<KB>(kc + (o0 + r + 8) * KCB, R.k1);
+  if constexpr (kb_mixed(KB)) {
+    const uint8_t *kc = slab + a.k_codes_o;
+    load_mixed_slice<KB>(kc + (o0 + r) * KCB, t, R.k0);
+    load_mixed_slice<KB>(kc + (o0 + r + 8) * KCB, t, R.k1);
+  } else {
+    const uint8_t *kc = slab + a.k_codes_o + t * 4 * KB;
+    ldg_words<KB>(kc + (o0 + r) * KCB, R.k0);
+    ldg_words<KB>(kc + (o0 + r + 8) * KCB, R.k1);
+  }
   const float *kn = reinterpret_cast<const float *>(slab + a.k_norm_o) + o0;
   R.nk0 = ldna(kn + r);
   R.nk1 = ldna(kn + r + 8);
@@ -386,7 +445,13 @@ __host__ __device__ constexpr bool byte_keys() {
 }
 template <int KB>
 __host__ __device__ constexpr uint32_t attn_stage_off() {
-  return kKeyTableOff + (byte_keys<KB>() ? 2u * 256 * 256 : (uint32_t(1) << (2 * KB)) * 256);
+  return kKeyTableOff + (kb_mixed(KB) ? ((uint32_t(1) << (2 * kb_hi(KB))) + (uint32_t(1) << (2 * kb_lo(KB)))) * 256
+                         : byte_keys<KB>() ? 2u * 256 * 256 : (uint32_t(1) << (2 * KB)) * 256);
+}
+// Mixed keys: the low channels' pair table follows the high channels' one.
+template <int KB>
+__host__ __device__ constexpr uint32_t key_lo_table_off() {
+  return kKeyTableOff + (uint32_t(1) << (2 * kb_hi(KB))) * 256;
 }
 // Stages of the per-warp ring (TQ_TMA_STAGING=1).
 #ifndef TQ_TMA_STAGES
@@ -410,7 +475,7 @@ constexpr size_t attn_smem_bytes() {
 
 template <int KB, int VB, bool QJL, int NT>
 __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(const AttnArgs a) {
-  constexpr int EK = 1 << (2 * KB), EV = 1 << (2 * VB);
+  constexpr int EK = 1 << (2 * kb_hi(KB)), EV = 1 << (2 * VB);
   static_assert(EV * 256 <= (int)kKeyTableOff, "table sizes");
   static_assert(attn_stage_off<KB>() <= 232448, "tables above the shared-memory limit");
   extern __shared__ __align__(16) uint8_t smem[];
@@ -421,12 +486,14 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   auto lut32 = [&](uint32_t off) { return *reinterpret_cast<const uint32_t *>(smem + off); };
 
   // Bank-private centroid-pair tables: lane l reads its own copy in bank l.
-  auto key_pair = [&](int e) {  // (hi pair, lo pair) of the code pair e
+  // (hi pair, lo pair) of the code pair e of a `bits`-bit codebook cb
+  auto key_pair_of = [&](const float *cb, int bits, int e) {
     __half h0, l0, h1, l1;
-    split_half(__ldg(a.k_cb + (e & ((1 << KB) - 1))) * kCentScale, h0, l0);
-    split_half(__ldg(a.k_cb + (e >> KB)) * kCentScale, h1, l1);
+    split_half(__ldg(cb + (e & ((1 << bits) - 1))) * kCentScale, h0, l0);
+    split_half(__ldg(cb + (e >> bits)) * kCentScale, h1, l1);
     return make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(l0, l1));
   };
+  auto key_pair = [&](int e) { return key_pair_of(a.k_cb, kb_hi(KB), e); };
   auto val_pair = [&](int e) {
     return pack_half2(__ldg(a.v_cb + (e & ((1 << VB) - 1))) * kCentScale, __ldg(a.v_cb + (e >> VB)) * kCentScale);
   };
@@ -439,6 +506,13 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
     }
   } else {
     for (int i = threadIdx.x; i < EK * 32; i += blockDim.x) lutK[i] = key_pair(i >> 5);
+  }
+  if constexpr (kb_mixed(KB)) {
+    // low channels: the k_bits codebook follows the (k_bits + 1) one
+    constexpr int HB = kb_hi(KB), LB = kb_lo(KB), EL = 1 << (2 * LB);
+    const float *cb_lo = a.k_cb + (2 << HB) - 1;
+    uint2 *lutKL = reinterpret_cast<uint2 *>(smem + key_lo_table_off<KB>());
+    for (int i = threadIdx.x; i < EL * 32; i += blockDim.x) lutKL[i] = key_pair_of(cb_lo, LB, i >> 5);
   }
   if constexpr (VB == 2) {
     // 2-bit values: indexed by a byte of the interleaved codes (two coordinates)
@@ -465,8 +539,10 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   const int64_t ts = T * wg / NW, te = T * (wg + 1) / NW;
   if (ts >= te) return;
   const uint32_t laneK = kKeyTableOff | ((uint32_t)lane * 8u);
+  const uint32_t laneKL = key_lo_table_off<KB>() | ((uint32_t)lane * 8u);  // mixed keys: low-channel table
   const uint32_t laneV = kValTableOff | ((uint32_t)lane * (VB == 2 ? 8u : 4u));
 #if TQ_TMA_STAGING
+  static_assert(!kb_mixed(KB), "the staging ring carries uniform key widths only");
   using SL = Stage<KB, VB, QJL>;
   const uint32_t wst_off = attn_stage_off<KB>() + (threadIdx.x >> 5) * attn_warp_stage_bytes<KB, VB, QJL>();
   constexpr uint32_t kStride = attn_stage_stride<KB, VB, QJL>();
@@ -607,7 +683,22 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) {
         uint2 L00, L01, L10, L11;
-        if constexpr (byte_keys<KB>()) {  // byte kk = pairs 2kk (low nibble), 2kk+1: one address, halves 64 KB apart
+        if constexpr (kb_mixed(KB)) {
+          // channels 32t + 4kk .. +3 are the 4-code group g of the lane's
+          // high stream when kk mod 4 < 2, of its low stream otherwise
+          const int g = (kk & 1) + 2 * (kk >> 2);
+          if ((kk & 2) == 0) {
+            L00 = lut64(mixed_pair_addr<kb_hi(KB)>(R.k0[0], R.k0[1], 2 * g, laneK));
+            L01 = lut64(mixed_pair_addr<kb_hi(KB)>(R.k0[0], R.k0[1], 2 * g + 1, laneK));
+            L10 = lut64(mixed_pair_addr<kb_hi(KB)>(R.k1[0], R.k1[1], 2 * g, laneK));
+            L11 = lut64(mixed_pair_addr<kb_hi(KB)>(R.k1[0], R.k1[1], 2 * g + 1, laneK));
+          } else {
+            L00 = lut64(mixed_pair_addr<kb_lo(KB)>(R.k0[2], R.k0[3], 2 * g, laneKL));
+            L01 = lut64(mixed_pair_addr<kb_lo(KB)>(R.k0[2], R.k0[3], 2 * g + 1, laneKL));
+            L10 = lut64(mixed_pair_addr<kb_lo(KB)>(R.k1[2], R.k1[3], 2 * g, laneKL));
+            L11 = lut64(mixed_pair_addr<kb_lo(KB)>(R.k1[2], R.k1[3], 2 * g + 1, laneKL));
+          }
+        } else if constexpr (byte_keys<KB>()) {  // byte kk = pairs 2kk (low nibble), 2kk+1: one address, halves 64 KB apart
           const uint32_t a0 = __byte_perm(R.k0[kk >> 2], laneK, 0x7604 | ((kk & 3) << 4));
           const uint32_t a1 = __byte_perm(R.k1[kk >> 2], laneK, 0x7604 | ((kk & 3) << 4));
           L00 = lut64(a0);

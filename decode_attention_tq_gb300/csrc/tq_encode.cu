@@ -173,37 +173,51 @@ __device__ __forceinline__ uint32_t had_pair(int i0, int i1, int j) {
 #ifndef TQ_ENCODE_MIN_BLOCKS
 #define TQ_ENCODE_MIN_BLOCKS 3
 #endif
-template <int BITS, bool QJL>
+// MIXED (keys at a fractional rate): BITS is the width of the high channels
+// (j mod 16 < 8), BITS - 1 that of the others; the codebook argument holds
+// the BITS-bit device codebook, then the (BITS - 1)-bit one.  The quad lanes
+// q = 0, 2 hold high channels (32c + 8q + i), q = 1, 3 low ones, so each lane
+// quantizes with one codebook set: set 0 (high) or set 1 (low).
+template <int BITS, bool QJL, bool MIXED = false>
 __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
+  constexpr int NSET = MIXED ? 2 : 1;
   extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells, QJL only
-  __shared__ float s_cent[16];
-  __shared__ float s_mid[16];
+  __shared__ float s_cent[NSET * 16];
+  __shared__ float s_mid[NSET * 16];
   __shared__ uint32_t s_dsign[4];
-  __shared__ uint2 s_qlut[kQBuckets];
-  __shared__ float2 s_qcen[kQBuckets];  // centroids of codes base and base+1 (QJL residual)
-  __shared__ int s_lut_bad;
+  __shared__ uint2 s_qlut[NSET * kQBuckets];
+  __shared__ float2 s_qcen[NSET * kQBuckets];  // centroids of codes base and base+1 (QJL residual)
+  __shared__ int s_lut_bad;                    // bit per set
   constexpr int L = 1 << BITS;
   const int tid = threadIdx.x;
   if (tid < L) s_cent[tid] = a.codebook[tid];
   if (tid < L - 1) s_mid[tid] = a.codebook[L + tid];
+  if constexpr (MIXED) {
+    const float *cb_lo = a.codebook + 2 * L - 1;
+    if (tid < L / 2) s_cent[16 + tid] = cb_lo[tid];
+    if (tid < L / 2 - 1) s_mid[16 + tid] = cb_lo[L / 2 + tid];
+  }
   if (tid == 0) s_lut_bad = 0;
   if (tid < kD) {  // sign words: one load per coordinate, packed by a ballot
     const uint32_t w = __ballot_sync(0xffffffffu, a.signs[tid] != 0);
     if ((tid & 31) == 0) s_dsign[tid >> 5] = w;
   }
   __syncthreads();
-  if (tid < kQBuckets) {
-    const float lo = ((float)(tid - 48) - 0.5f) * 0.25f, hi = ((float)(tid - 48) + 0.5f) * 0.25f;
+  if ((tid & 127) < kQBuckets && (tid >> 7) < NSET) {
+    const int set = tid >> 7, bk = tid & 127, Ls = set ? L / 2 : L;
+    const float *mid = s_mid + 16 * set, *cen = s_cent + 16 * set;
+    const float lo = ((float)(bk - 48) - 0.5f) * 0.25f, hi = ((float)(bk - 48) + 0.5f) * 0.25f;
     int base = 0, inside = 0;
     float thr = __int_as_float(0x7f800000);  // +inf
-    for (int k = 0; k < L - 1; k++) {
-      const float t = s_mid[k];
+    for (int k = 0; k < Ls - 1; k++) {
+      const float t = mid[k];
       if (t < lo) base++;
       else if (t <= hi) { thr = t; inside++; }
     }
-    if (inside > 1 || (tid == 0 && base > 0) || (tid == kQBuckets - 1 && inside + base < L - 1)) atomicOr(&s_lut_bad, 1);
-    s_qlut[tid] = make_uint2((uint32_t)base, __float_as_uint(thr));
-    s_qcen[tid] = make_float2(s_cent[base], s_cent[base + 1 < L ? base + 1 : base]);
+    if (inside > 1 || (bk == 0 && base > 0) || (bk == kQBuckets - 1 && inside + base < Ls - 1))
+      atomicOr(&s_lut_bad, 1 << set);
+    s_qlut[set * kQBuckets + bk] = make_uint2((uint32_t)base, __float_as_uint(thr));
+    s_qcen[set * kQBuckets + bk] = make_float2(cen[base], cen[base + 1 < Ls ? base + 1 : base]);
   }
   if constexpr (QJL) {
     // cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
@@ -225,7 +239,12 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
   const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / 32;
   const int64_t NH = a.n_tokens * a.H;
   const int64_t pool_slots = a.num_pages * (int64_t)a.P;
-  const bool lut_bad = s_lut_bad != 0;
+  // this lane's codebook set (mixed keys: odd quad lanes hold low channels)
+  const int set = MIXED ? (q & 1) : 0;
+  const float *cent = s_cent + 16 * set, *midp = s_mid + 16 * set;
+  const uint2 *qlut = s_qlut + set * kQBuckets;
+  const float2 *qcen = s_qcen + set * kQBuckets;
+  const bool lut_bad = (s_lut_bad >> set) & 1;
   const bool small = NH <= 0x7fffffff;
   // sign masks of this thread's fp16 pairs (coordinates 32c + 8q + 2p, +1)
   uint32_t smask[4][4];
@@ -325,12 +344,12 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
       for (int j = 0; j < 32; j++) {
         const float u = x[j] * inv;
         const int b = quant_bucket(u);
-        const uint2 e = s_qlut[b];
+        const uint2 e = qlut[b];
         const bool up = u >= __uint_as_float(e.y);
         idx[j] = zero ? 0 : (int)e.x + (up ? 1 : 0);
         if constexpr (QJL) {
-          const float2 c = s_qcen[b];
-          x[j] = u - (zero ? s_cent[0] : (up ? c.y : c.x));  // residual in u units
+          const float2 c = qcen[b];
+          x[j] = u - (zero ? cent[0] : (up ? c.y : c.x));  // residual in u units
         }
       }
     } else {
@@ -338,11 +357,11 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
       for (int j = 0; j < 32; j++) {
         const float u = x[j] * inv;
         int k = 0;
-#pragma unroll
-        for (int s = L / 2; s >= 1; s >>= 1)
-          if (u >= s_mid[k + s - 1]) k += s;
+        const int Lq = set ? L / 2 : L;
+        for (int s = Lq / 2; s >= 1; s >>= 1)
+          if (u >= midp[k + s - 1]) k += s;
         idx[j] = zero ? 0 : k;
-        x[j] = u - s_cent[idx[j]];  // residual in u units (QJL only)
+        x[j] = u - cent[idx[j]];  // residual in u units (QJL only)
       }
     }
 
@@ -353,7 +372,7 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
       float c2 = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; j++) {
-        const float cj = s_cent[idx[j]];
+        const float cj = cent[idx[j]];
         c2 = fmaf(cj, cj, c2);
       }
       c2 += __shfl_xor_sync(0xffffffffu, c2, 1);
@@ -364,7 +383,31 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
     const int64_t page = ok ? slot / a.P : 0;
     const int64_t off = ok ? slot % a.P : 0;
     uint8_t *slab = a.pool + page * a.page_bytes + (int64_t)h * a.slab_bytes;
-    if (ok) {
+    if (MIXED && ok) {
+      // high stream (channels j mod 16 < 8) at BITS bits, then the low stream
+      // at BITS - 1: this lane's 8 codes of block c are group 2c + q/2 of its
+      // stream
+      const int W = set ? BITS - 1 : BITS;
+      uint8_t *tok = slab + a.codes_off + off * a.code_bytes;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        uint32_t w = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; i++) w |= (uint32_t)idx[8 * c + i] << (W * i);
+        const int g = 2 * c + (q >> 1);
+        uint8_t *dst = set ? tok + 8 * BITS + g * (BITS - 1) : tok + g * BITS;
+        if (W == 4) {
+          *reinterpret_cast<uint32_t *>(dst) = w;
+        } else if (W == 2) {
+          *reinterpret_cast<uint16_t *>(dst) = (uint16_t)w;
+        } else {
+          dst[0] = (uint8_t)w;
+          dst[1] = (uint8_t)(w >> 8);
+          dst[2] = (uint8_t)(w >> 16);
+        }
+      }
+      if (q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nstore;
+    } else if (ok) {
 #pragma unroll
       for (int c = 0; c < 4; c++) {
         // codes of coordinates 32c + 8q .. +7: 8 * BITS bits, LSB first
@@ -459,9 +502,9 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a) {
   }
 }
 
-template <int BITS, bool QJL>
+template <int BITS, bool QJL, bool MIXED = false>
 __global__ void __launch_bounds__(256, QJL ? 2 : TQ_ENCODE_MIN_BLOCKS) encode_kernel(const EncodeArgs a) {
-  encode_body<BITS, QJL>(a);
+  encode_body<BITS, QJL, MIXED>(a);
 }
 
 // Keys and values of the same tokens in one launch (same bits, keys without
@@ -474,14 +517,24 @@ __global__ void __launch_bounds__(256, TQ_ENCODE_MIN_BLOCKS) encode_kv_kernel(co
     encode_body<BITS, false>(va);
 }
 
-template <int BITS, bool QJL>
+// 16 codes of W bits from byte `off` of a key stream, as a 64-bit value.
+__device__ __forceinline__ uint64_t codes16_bytes(const uint8_t *tok, int off, int W) {
+  uint64_t v = 0;
+  for (int k = 0; k < 2 * W; k++) v |= (uint64_t)tok[off + k] << (8 * k);
+  return v;
+}
+
+// MIXED: keys at a fractional rate, BITS on the high channels (j mod 16 < 8)
+// and BITS - 1 on the others (as in encode_body).
+template <int BITS, bool QJL, bool MIXED = false>
 __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
   extern __shared__ float s_S[];
-  __shared__ float s_cent[16];
+  __shared__ float s_cent[MIXED ? 32 : 16];
   __shared__ uint32_t s_dsign[4];
   constexpr int L = 1 << BITS;
   const int tid = threadIdx.x;
   if (tid < L) s_cent[tid] = a.codebook[tid];
+  if (MIXED && tid < L / 2) s_cent[16 + tid] = a.codebook[2 * L - 1 + tid];
   if (tid < 4) {
     uint32_t w = 0;
     for (int j = 0; j < 32; j++) w |= (a.signs[32 * tid + j] ? 1u : 0u) << j;
@@ -518,17 +571,31 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
     const int64_t off = ok ? slot % a.P : 0;
     const uint8_t *slab = a.pool + page * a.page_bytes + (int64_t)h * a.slab_bytes;
 
-    uint32_t w[BITS];
-    if (a.grouped)
-      load_codes_grouped<BITS>(slab + a.codes_off, off, q, w);
-    else
-      load_codes<BITS>(slab + a.codes_off + off * a.code_bytes + q * 4 * BITS, w);
     const float nrm = reinterpret_cast<const float *>(slab + a.norm_off)[off];
-    int idx[32];
-    unpack_codes<BITS>(w, idx);
     float y[32];
+    if constexpr (MIXED) {
+      // lane q's channels 32q..32q+31: codes 16q..16q+15 of the high stream
+      // (channels with j mod 16 < 8) and of the low stream
+      const uint8_t *tok = slab + a.codes_off + off * a.code_bytes;
+      const uint64_t hv = codes16_bytes(tok, 2 * BITS * q, BITS);
+      const uint64_t lv = codes16_bytes(tok, 8 * BITS + 2 * (BITS - 1) * q, BITS - 1);
 #pragma unroll
-    for (int j = 0; j < 32; j++) y[j] = s_cent[idx[j]];
+      for (int j = 0; j < 32; j++) {
+        const int k = 8 * (j >> 4) + (j & 7);
+        y[j] = (j & 15) < 8 ? s_cent[(int)((hv >> (BITS * k)) & ((1u << BITS) - 1))]
+                            : s_cent[16 + (int)((lv >> ((BITS - 1) * k)) & ((1u << (BITS - 1)) - 1))];
+      }
+    } else {
+      uint32_t w[BITS];
+      if (a.grouped)
+        load_codes_grouped<BITS>(slab + a.codes_off, off, q, w);
+      else
+        load_codes<BITS>(slab + a.codes_off + off * a.code_bytes + q * 4 * BITS, w);
+      int idx[32];
+      unpack_codes<BITS>(w, idx);
+#pragma unroll
+      for (int j = 0; j < 32; j++) y[j] = s_cent[idx[j]];
+    }
     if constexpr (QJL) {
       const float gamma = reinterpret_cast<const float *>(slab + a.gamma_off)[off];
       const uint4 sb = *reinterpret_cast<const uint4 *>(slab + a.signs_off + off * (kM / 8));
@@ -571,12 +638,12 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
 }
 
 // ----------------------------------------------------------------- launch --
-template <int BITS, bool QJL>
+template <int BITS, bool QJL, bool MIXED = false>
 static cudaError_t launch_encode_t(const EncodeArgs &a, int sms, cudaStream_t st) {
   const size_t smem = QJL ? (size_t)kM * kD * sizeof(float) : 0;
   if (QJL) {
     static unsigned long long done = 0;
-    cudaError_t e = set_smem_once(encode_kernel<BITS, QJL>, (int)smem, done);
+    cudaError_t e = set_smem_once(encode_kernel<BITS, QJL, MIXED>, (int)smem, done);
     if (e != cudaSuccess) return e;
   }
   const int64_t quads = a.n_tokens * a.H;
@@ -584,16 +651,16 @@ static cudaError_t launch_encode_t(const EncodeArgs &a, int sms, cudaStream_t st
   const int64_t cap = (int64_t)sms * (QJL ? 3 : 8);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  encode_kernel<BITS, QJL><<<(unsigned)blocks, 256, smem, st>>>(a);
+  encode_kernel<BITS, QJL, MIXED><<<(unsigned)blocks, 256, smem, st>>>(a);
   return cudaGetLastError();
 }
 
-template <int BITS, bool QJL>
+template <int BITS, bool QJL, bool MIXED = false>
 static cudaError_t launch_decode_t(const DecodeArgs &a, int sms, cudaStream_t st) {
   const size_t smem = QJL ? (size_t)kM * kD * sizeof(float) : 0;
   if (QJL) {
     static unsigned long long done = 0;
-    cudaError_t e = set_smem_once(decode_kernel<BITS, QJL>, (int)smem, done);
+    cudaError_t e = set_smem_once(decode_kernel<BITS, QJL, MIXED>, (int)smem, done);
     if (e != cudaSuccess) return e;
   }
   const int64_t quads = a.n_tokens * a.H;
@@ -601,7 +668,7 @@ static cudaError_t launch_decode_t(const DecodeArgs &a, int sms, cudaStream_t st
   const int64_t cap = (int64_t)sms * (QJL ? 3 : 8);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  decode_kernel<BITS, QJL><<<(unsigned)blocks, 256, smem, st>>>(a);
+  decode_kernel<BITS, QJL, MIXED><<<(unsigned)blocks, 256, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -621,7 +688,17 @@ cudaError_t launch_encode_kv(const EncodeArgs &ka, const EncodeArgs &va, int bit
   return cudaGetLastError();
 }
 
-cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st) {
+// bits: the code width; for mixed-rate keys the high channels' width
+cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, bool mixed, int sms, cudaStream_t st) {
+  if (mixed) {
+    switch (bits * 2 + (qjl ? 1 : 0)) {
+      case 6: return launch_encode_t<3, false, true>(a, sms, st);
+      case 7: return launch_encode_t<3, true, true>(a, sms, st);
+      case 8: return launch_encode_t<4, false, true>(a, sms, st);
+      case 9: return launch_encode_t<4, true, true>(a, sms, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (bits * 2 + (qjl ? 1 : 0)) {
     case 4: return launch_encode_t<2, false>(a, sms, st);
     case 5: return launch_encode_t<2, true>(a, sms, st);
@@ -633,7 +710,16 @@ cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, int sms, cuda
   }
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, bool mixed, int sms, cudaStream_t st) {
+  if (mixed) {
+    switch (bits * 2 + (qjl ? 1 : 0)) {
+      case 6: return launch_decode_t<3, false, true>(a, sms, st);
+      case 7: return launch_decode_t<3, true, true>(a, sms, st);
+      case 8: return launch_decode_t<4, false, true>(a, sms, st);
+      case 9: return launch_decode_t<4, true, true>(a, sms, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (bits * 2 + (qjl ? 1 : 0)) {
     case 4: return launch_decode_t<2, false>(a, sms, st);
     case 5: return launch_decode_t<2, true>(a, sms, st);

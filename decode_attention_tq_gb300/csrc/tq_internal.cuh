@@ -112,7 +112,7 @@ struct AttnArgs {
   bool pdl;          // host: launch main and merge as programmatic dependents
 };
 
-cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
+cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, bool mixed, int sms, cudaStream_t st);
 cudaError_t launch_window_roll(const RollArgs &a, cudaStream_t st);
 
 // Launch `kern` on `st`, as a programmatic dependent of the previous kernel on
@@ -134,7 +134,7 @@ cudaError_t launch_maybe_dependent(void (*kern)(P...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
 }
 cudaError_t launch_encode_kv(const EncodeArgs &ka, const EncodeArgs &va, int bits, int sms, cudaStream_t st);
-cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, int sms, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, bool mixed, int sms, cudaStream_t st);
 
 // Decode attention pieces (tq_attn_aux.cu and tq_attn_k*.cu).
 constexpr int kWinChunk = 32;  // window tokens per window partial
@@ -147,6 +147,10 @@ cudaError_t attn_main_k2(const AttnArgs &a, int v_bits, bool qjl, int nt, bool q
 cudaError_t attn_main_k3(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
                          int blocks, cudaStream_t st);
 cudaError_t attn_main_k4(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                         int blocks, cudaStream_t st);
+cudaError_t attn_main_k34(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                         int blocks, cudaStream_t st);
+cudaError_t attn_main_k23(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
                          int blocks, cudaStream_t st);
 
 // Set a kernel's dynamic shared-memory limit once per device (never inside a

@@ -81,6 +81,16 @@ typedef struct {
                            sqrt(pi/2)/m (Gaussian S).  An orthogonal S takes
                            sqrt(pi/2)/sqrt(d); a shrinkage a in (0, 1]
                            multiplies either (2/pi is the MMSE choice)      */
+  int32_t k_mixed;      /* 1: keys at the fractional rate k_bits + 1/2: the
+                           channels j with (j mod 16) < 8 take k_bits + 1
+                           bits, the others k_bits ("TurboQuant Family Design
+                           Study ...", 'Packed format and complete bit
+                           accounting': 3.5 = 64 x 4 + 64 x 3 bits, 2.5 =
+                           64 x 3 + 64 x 2).  A key's code stream holds the
+                           high channels' codes first, then the low ones',
+                           each LSB-first in channel order; the key codebook
+                           argument is then the device codebook of k_bits + 1
+                           followed by that of k_bits                        */
 } tq_format;
 
 /* Byte layout of one page (one pool per layer = [num_pages][H] head-slabs).

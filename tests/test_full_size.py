@@ -35,8 +35,7 @@ def _check_encode_samples(fmt, kind, x_dev, slots_dev, pool_host, num_pages, pic
     x = x_dev[pick].cpu().numpy()
     slots = slots_dev[pick].cpu().numpy().astype(np.int32)
     signs = ti.sign_bits(ti.SEED_SIGNS_K if kind == 0 else ti.SEED_SIGNS_V, d)
-    bits = fmt.k_bits if kind == 0 else fmt.v_bits
-    c, t = oracle.make_codebook(bits)
+    c, t = oracle.kind_codebook(fmt, kind)
     S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if (kind == 0 and fmt.k_qjl) else None
     ref = pool_host.copy()
     rc, _, cm, sm = oracle.encode(fmt, kind, x, slots, ref, num_pages, signs, c, t, S, diagnostics=True)
@@ -68,8 +67,8 @@ def test_decode_workload_full_size(wl):
     # sampled rows through the oracle, on the very same pool / window / query
     pool = L["pool"].cpu().numpy()
     rows = sorted({0, Hq - 1, (B - 1) * Hq, B * Hq - 1, (B // 2) * Hq + Hq // 2 + 1})
-    kc, _ = oracle.make_codebook(f.k_bits)
-    vc, _ = oracle.make_codebook(f.v_bits)
+    kc, _ = oracle.kind_codebook(f, 0)
+    vc, _ = oracle.kind_codebook(f, 1)
     S = b.S.cpu().numpy() if b.S is not None else None
     rc, ref = oracle.attention(f, L["q"].cpu().numpy(), pool, b.num_pages, b.bt.cpu().numpy(), b.comp_lens.cpu().numpy(),
                                L["kwin"].cpu().numpy() if b.W else None, L["vwin"].cpu().numpy() if b.W else None,

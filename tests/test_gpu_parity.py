@@ -33,7 +33,7 @@ def _encode_case(fmt, kind, N, seed, zero_rows=(), neg_slots=()):
         perm[ns] = -1
     signs = ti.sign_bits(ti.SEED_SIGNS_K if kind == 0 else ti.SEED_SIGNS_V, d)
     bits = fmt.k_bits if kind == 0 else fmt.v_bits
-    c, t = oracle.make_codebook(bits)
+    c, t = oracle.kind_codebook(fmt, kind)
     S = None
     if kind == 0 and fmt.k_qjl:
         S = (ti.orthogonal_matrix if fmt.qjl_scale > 0 else ti.gaussian_matrix)(ti.SEED_QJL, fmt.qjl_m, d)
@@ -43,7 +43,7 @@ def _encode_case(fmt, kind, N, seed, zero_rows=(), neg_slots=()):
     pool = torch.full((num_pages * lay["page_bytes"],), 0x5A, dtype=torch.uint8, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     tq.tq_encode(fmt, kind, torch.from_numpy(x).cuda(), torch.from_numpy(perm).cuda(), pool, num_pages,
-                 torch.from_numpy(signs).cuda(), tq.device_codebook(bits), None if S is None else torch.from_numpy(S).cuda(), err_word=err)
+                 torch.from_numpy(signs).cuda(), tq.kind_codebook(fmt, kind), None if S is None else torch.from_numpy(S).cuda(), err_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     return pool.cpu().numpy(), pool_ref, lay, perm, cm, sm, x, signs, c, S, num_pages
@@ -67,7 +67,7 @@ def test_decode_matches_oracle(bits, kind, qjl):
     pool, pool_ref, lay, slots, cm, sm, x, signs, c, S, num_pages = _encode_case(fmt, kind, N, seed=7)
     # the GPU decodes the oracle's pages
     out = tq.tq_decode(fmt, kind, torch.from_numpy(pool_ref).cuda(), num_pages, torch.from_numpy(slots).cuda(),
-                       torch.from_numpy(signs).cuda(), tq.device_codebook(bits), None if S is None else torch.from_numpy(S).cuda())
+                       torch.from_numpy(signs).cuda(), tq.kind_codebook(fmt, kind), None if S is None else torch.from_numpy(S).cuda())
     torch.cuda.synchronize()
     rc, ref = oracle.decode(fmt, kind, pool_ref, num_pages, slots, signs, c, S)
     assert rc == 0
@@ -79,6 +79,28 @@ def test_decode_matches_oracle(bits, kind, qjl):
 
 
 ORTH_SHRINK = 0.7 * math.sqrt(math.pi / 2) / math.sqrt(128)  # orthogonal S, 0.7 damping
+
+
+@pytest.mark.parametrize("b,qjl,nc", [(3, 0, 0), (2, 0, 0), (3, 1, 0), (2, 1, 0), (3, 0, 1)])
+def test_encode_mixed_keys_matches_oracle(b, qjl, nc):
+    """Keys at 3.5 / 2.5 bits per channel (b+1 bits on j mod 16 < 8, b on the rest)."""
+    fmt = ti.Format(128, b, 4, qjl, 128, 64, 4, norm_correct=nc, k_mixed=1)
+    pool, pool_ref, lay, slots, cm, sm, *_ = _encode_case(fmt, 0, 300, seed=b + 20 * qjl + 7 * nc, zero_rows=(4,), neg_slots=(11,))
+    st = compare_encoded(pool, pool_ref, lay, fmt, 0, slots, cm, sm)
+    print("mixed encode", b, qjl, nc, st)
+
+
+@pytest.mark.parametrize("b,qjl", [(3, 1), (2, 0)])
+def test_decode_mixed_keys_matches_oracle(b, qjl):
+    fmt = ti.Format(128, b, 4, qjl, 128, 32, 2, k_mixed=1)
+    pool, pool_ref, lay, slots, cm, sm, x, signs, c, S, num_pages = _encode_case(fmt, 0, 100, seed=b + 90)
+    out = tq.tq_decode(fmt, 0, torch.from_numpy(pool_ref).cuda(), num_pages, torch.from_numpy(slots).cuda(),
+                       torch.from_numpy(signs).cuda(), tq.kind_codebook(fmt, 0), None if S is None else torch.from_numpy(S).cuda())
+    torch.cuda.synchronize()
+    rc, ref = oracle.decode(fmt, 0, pool_ref, num_pages, slots, signs, c, S)
+    assert rc == 0
+    e = rel_err(out.cpu().numpy(), ref)
+    assert e.max() < 1e-5, e.max()
 
 
 @pytest.mark.parametrize("bits,kind", [(4, 0), (3, 1), (2, 0)])
@@ -114,6 +136,10 @@ ATTN_CASES = {
     "empty_seq": (ti.Format(128, 3, 3, 1, 128, 64, 2), 3, 8, [0, 200, 0], 8, [0, 8, 5]),
     "k3qjl_orth_shrink_v4_w": (ti.Format(128, 3, 4, 1, 128, 64, 2, qjl_scale=ORTH_SHRINK), 2, 8, [900, 257], 32, [32, 9]),
     "k4v4_norm_corrected": (ti.Format(128, 4, 4, 0, 128, 64, 4, norm_correct=1), 2, 16, [500, 64], 16, [16, 3]),
+    "k35v4_w": (ti.Format(128, 3, 4, 0, 128, 64, 4, k_mixed=1), 2, 16, [777, 130], 32, [32, 11]),
+    "k25qjl_v2_g8": (ti.Format(128, 2, 2, 1, 128, 64, 2, k_mixed=1), 2, 16, [600, 97], 16, [16, 16]),
+    "k35qjl_v3_ragged": (ti.Format(128, 3, 3, 1, 128, 32, 4, k_mixed=1), 3, 16, [1, 333, 64], 8, [0, 8, 2]),
+    "k25v4_p16": (ti.Format(128, 2, 4, 0, 128, 16, 8, k_mixed=1), 1, 32, [250], 0, [0]),
 }
 
 
@@ -255,12 +281,12 @@ def test_host_argument_errors():
     assert ei.value.status == 6
 
 
-@pytest.mark.parametrize("kb,vb,qjl,W", [(4, 4, 0, 8), (3, 4, 1, 8), (2, 2, 1, 5), (4, 4, 0, 0)])
-def test_append_window_matches_oracle(kb, vb, qjl, W):
+@pytest.mark.parametrize("kb,vb,qjl,W,kmix", [(4, 4, 0, 8, 0), (3, 4, 1, 8, 0), (2, 2, 1, 5, 0), (4, 4, 0, 0, 0), (3, 4, 0, 8, 1)])
+def test_append_window_matches_oracle(kb, vb, qjl, W, kmix):
     """Window roll plus encode of the leaving token, from mixed initial states
     (empty, partial, full at several ring heads, a missing page), stepped on
     both sides: windows and counters identical, pages field by field."""
-    fmt = ti.Format(128, kb, vb, qjl, 128, 16, 4)
+    fmt = ti.Format(128, kb, vb, qjl, 128, 16, 4, k_mixed=kmix)
     d, H, P = fmt.head_dim, fmt.num_kv_heads, fmt.page_size
     B, steps = 5, 30
     rng = np.random.default_rng(kb * 100 + vb * 10 + W)
@@ -277,7 +303,7 @@ def test_append_window_matches_oracle(kb, vb, qjl, W):
     V = ti.kv_history(steps, B, H, d, 3, 1).numpy()
     lay = oracle.page_layout(fmt)
     pool_ref = np.full(num_pages * lay["page_bytes"], 0x5A, np.uint8)
-    kcb, vcb = oracle.make_codebook(kb), oracle.make_codebook(vb)
+    kcb, vcb = oracle.kind_codebook(fmt, 0), oracle.kind_codebook(fmt, 1)
     ks, vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
     S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if qjl else None
 
@@ -290,7 +316,7 @@ def test_append_window_matches_oracle(kb, vb, qjl, W):
     evicted, skipped_any = [], set()
     for t in range(steps):
         tq.tq_append_window(fmt, dev(K[t]), dev(V[t]), g_kw, g_vw, g_lens, g_head, g_comp, g_bt, g_pool, num_pages, g_ks, g_vs,
-                            tq.device_codebook(kb), tq.device_codebook(vb), g_S, workspace=ws, err_word=err)
+                            tq.kind_codebook(fmt, 0), tq.kind_codebook(fmt, 1), g_S, workspace=ws, err_word=err)
         sk = oracle.append_window(fmt, K[t], V[t], kw, vw, lens, head, comp, bt, pool_ref, num_pages, ks, vs, kcb, vcb, S,
                                   evicted=evicted)
         skipped_any |= set(sk)

@@ -46,7 +46,8 @@ def test_codebook_equals_oracle(lib, bits):
 
 
 @pytest.mark.parametrize("fmt", [ti.Format(128, b, v, q, 128, P, H) for b in (2, 3, 4) for v in (2, 4) for q in (0, 1) for P in (16, 64, 128)
-                                 for H in (1, 8)] + [ti.Format(64, 3, 5, 1, 24, 48, 3), ti.Format(16, 1, 2, 0, 8, 16, 1)])
+                                 for H in (1, 8)] + [ti.Format(64, 3, 5, 1, 24, 48, 3), ti.Format(16, 1, 2, 0, 8, 16, 1)]
+                         + [ti.Format(128, b, 4, q, 128, 64, 8, k_mixed=1) for b in (1, 2, 3, 7) for q in (0, 1)])
 def test_layout_equals_oracle(lib, fmt):
     from decode_attention_tq_gb300 import tq_page_layout
 
@@ -94,6 +95,11 @@ def test_host_validation_before_any_launch(lib):
     assert lib.tq_encode(C.byref(_F(qjl_scale=float("nan"))), 1, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
     assert lib.tq_encode(C.byref(_F(k_qjl=1, norm_correct=1)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, dummy, None, None) == 2
     assert lib.tq_encode(C.byref(_F(k_qjl=1, norm_correct=1)), 1, dummy, 0, dummy, dummy, 1, dummy, dummy, None, None, None) == 0
+    # mixed-rate keys: 3.5 and 2.5 bits run on the GPU, 4.5 does not; 8.5 is not a format
+    assert lib.tq_encode(C.byref(_F(k_bits=4, k_mixed=1)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 2
+    assert lib.tq_encode(C.byref(_F(k_bits=8, k_mixed=1)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
+    assert lib.tq_encode(C.byref(_F(k_mixed=3)), 0, dummy, 1, dummy, dummy, 1, dummy, dummy, None, None, None) == 1
+    assert lib.tq_encode(C.byref(_F(k_bits=3, k_mixed=1)), 0, dummy, 0, dummy, dummy, 1, dummy, dummy, None, None, None) == 0
     # append: window buffers and counters are required with a window
     assert lib.tq_append_window(C.byref(f), 2, dummy, dummy, None, None, 8, None, None, dummy, dummy, 4, dummy, 4, dummy, dummy,
                                 dummy, dummy, None, dummy, 1 << 20, None, None) == 1

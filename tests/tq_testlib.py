@@ -52,13 +52,30 @@ def unpack_field(pool: np.ndarray, lay: dict, fmt, kind: int, slots: np.ndarray)
                 raw = pool[base + co + off * cb: base + co + (off + 1) * cb]
             else:
                 raw = value_code_bytes(pool[base + co: base + co + P * cb], off, d, bits)
-            bitsarr = np.unpackbits(raw, bitorder="little").reshape(d, bits)
-            codes[i, h] = (bitsarr * (1 << np.arange(bits))).sum(1)
+            if kind == 0 and getattr(fmt, "k_mixed", 0):
+                codes[i, h] = mixed_key_codes(raw, d, bits)
+            else:
+                bitsarr = np.unpackbits(raw, bitorder="little").reshape(d, bits)
+                codes[i, h] = (bitsarr * (1 << np.arange(bits))).sum(1)
             if qjl:
                 gamma[i, h] = pool[base + lay["k_gamma"] + 4 * off: base + lay["k_gamma"] + 4 * off + 4].view(np.float32)[0]
                 sraw = pool[base + lay["k_signs"] + off * (m // 8): base + lay["k_signs"] + (off + 1) * (m // 8)]
                 signs[i, h] = np.unpackbits(sraw, bitorder="little")[:m]
     return norm, gamma, codes, signs
+
+
+def mixed_key_codes(raw: np.ndarray, d: int, b: int) -> np.ndarray:
+    """Per-channel codes of a mixed-rate key stream: the channels j with
+    (j mod 16) < 8 at b+1 bits first, then the others at b bits."""
+    bits = np.unpackbits(raw, bitorder="little")
+    nh = d // 2
+    hi = (bits[: nh * (b + 1)].reshape(nh, b + 1) * (1 << np.arange(b + 1))).sum(1)
+    lo = (bits[nh * (b + 1): nh * (2 * b + 1)].reshape(nh, b) * (1 << np.arange(b))).sum(1)
+    high = (np.arange(d) % 16) < 8
+    out = np.zeros(d, np.int64)
+    out[high] = hi
+    out[~high] = lo
+    return out
 
 
 def written_mask(pool_len: int, lay: dict, fmt, kind: int, slots) -> np.ndarray:
@@ -150,7 +167,7 @@ class Scenario:
         self.K = ti.kv_history(B, T, H, d, layer, 0).numpy()
         self.V = ti.kv_history(B, T, H, d, layer, 1).numpy()
         self.ks, self.vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
-        self.kc, self.kt = oracle.make_codebook(fmt.k_bits)
+        self.kc, self.kt = oracle.kind_codebook(fmt, 0)
         self.vc, self.vt = oracle.make_codebook(fmt.v_bits)
         # a format with its own QJL factor is exercised with an orthogonal S
         # (the variant that factor exists for); else the paper's Gaussian S
@@ -187,7 +204,7 @@ class Scenario:
         return dict(
             q=t(self.q), pool=t(self.pool), bt=t(self.bt), comp=t(self.comp),
             kwin=t(self.kwin) if self.W else None, vwin=t(self.vwin) if self.W else None, wl=t(self.wl) if self.W else None,
-            ks=t(self.ks), vs=t(self.vs), kcb=tq.device_codebook(self.fmt.k_bits, dev), vcb=tq.device_codebook(self.fmt.v_bits, dev),
+            ks=t(self.ks), vs=t(self.vs), kcb=tq.kind_codebook(self.fmt, 0, dev), vcb=tq.device_codebook(self.fmt.v_bits, dev),
             S=t(self.S) if self.S is not None else None,
         )
 

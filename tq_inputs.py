@@ -196,7 +196,13 @@ LLAMA3_8B_T32K = DecodeWorkload("llama-3-8b_l32_b16_h32x8_t32768_k4v4_w128", 32,
 BULK_ENCODE_64K = EncodeWorkload("bulk_encode_l32_h8_t65536", 32, 8, 65536, (2, 3, 4), (0, 1), 128, 64)
 LONG_CTX_T128K = DecodeWorkload("long_ctx_l32_b4_h32x8_t131072_k2qjl_v2_w256", 32, 4, 32, Format(128, 2, 2, 1, 128, 128, 8), 131072, 256)
 
-DECODE_WORKLOADS = (SINGLE_LAYER_T2K, QWEN25_3B_T16K, LLAMA3_8B_T32K, LONG_CTX_T128K)
+# The design study's recommended first product mode ('Packed format and
+# complete bit accounting': keys 3.5 bits per channel, values 3.0, last 128
+# tokens fp16) at the Llama-3-8B decode shape.
+LLAMA3_8B_T32K_K35V3 = DecodeWorkload("llama-3-8b_l32_b16_h32x8_t32768_k35v3_w128", 32, 16, 32,
+                                      Format(128, 3, 3, 0, 128, 64, 8, k_mixed=1), 32768, 128)
+
+DECODE_WORKLOADS = (SINGLE_LAYER_T2K, QWEN25_3B_T16K, LLAMA3_8B_T32K, LONG_CTX_T128K, LLAMA3_8B_T32K_K35V3)
 
 
 def orthogonal_matrix(seed: int, m: int, d: int) -> np.ndarray:
