@@ -229,8 +229,7 @@ class DecodeBench:
         self.main_bytes = B * H * comp * (bph["k"] + bph["v"]) + B * self.pages_per_seq * 4  # per layer launch
         self.window_bytes = B * H * wl.win_tokens * d * 2 * 2
         self.step_bytes = wl.layers * (self.main_bytes + self.window_bytes + B * Hq * d * (2 + 4))
-        appends = 1 if (f.k_bits == f.v_bits and not f.k_qjl and not f.k_mixed) else 2  # one joint K+V encode launch, or K then V
-        self.launches_per_step = wl.layers * (1 + appends + 3)  # window roll, encode, prep (with window chunks), main, merge
+        self.launches_per_step = wl.layers * 4  # append (roll + K and V encode), prep (with window chunks), main, merge
 
     def step(self, events=None):
         tq, f = self.tq, self.fmt

@@ -386,8 +386,12 @@ tq_status tq_append_window(const tq_format *fmt, int batch, const void *k_new_f1
   s = encode_args(fmt, TQ_KIND_V, r.stage_v, batch, r.stage_slots, page_pool, num_pages, v_signs, v_codebook, nullptr,
                   err_word, &va);
   if (s != TQ_OK) return s;
-  if (launch_window_roll(r, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TQ_ERR_CUDA;
-  return launch_kv(fmt, ka, va, stream);
+  int sms = 0;
+  if (sm_count(&sms) != TQ_OK) return TQ_ERR_CUDA;
+  return launch_append(r, ka, va, fmt->k_bits + fmt->k_mixed, fmt->k_qjl != 0, fmt->k_mixed != 0, fmt->v_bits, sms,
+                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? TQ_OK
+             : TQ_ERR_CUDA;
 }
 
 tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64_t num_pages,

@@ -1,506 +1,10 @@
-// tq_encode.cu -- encode (append) kernel and the decode (reconstruct) kernel.
-//
-// Work split: four consecutive lanes (a "quad") own one head vector; lane q
-// holds coordinates 32q..32q+31, so the Walsh-Hadamard butterflies with
-// h = 1..16 run in registers and h = 32, 64 are two shuffle stages.  With 32
-// coordinates per lane the packed codes of a lane are exactly b 32-bit words
-// for every b, so packing is thread-local and each lane writes its own slice.
-#include "tq_internal.cuh"
+// tq_encode.cu -- encode (append) kernels and the decode (reconstruct)
+// kernel.  The encode body lives in tq_encode_body.cuh.  Decode: four
+// consecutive lanes (a "quad") own one head vector, lane q holds coordinates
+// 32q..32q+31; its codes are b 32-bit words of one stream for every b.
+#include "tq_encode_body.cuh"
 
 namespace tq {
-
-// QJL matrix S [m][d] staged in shared memory with columns XOR-swizzled by
-// lane slice so the four lanes of a quad read different banks.
-__device__ __forceinline__ int s_swz(int l, int j) { return l * kD + (j ^ ((j >> 5) << 3)); }
-
-template <int BITS>
-__device__ __forceinline__ void pack_codes(const int (&idx)[32], uint32_t (&w)[BITS]) {
-#pragma unroll
-  for (int k = 0; k < BITS; k++) w[k] = 0u;
-#pragma unroll
-  for (int j = 0; j < 32; j++) {
-    const int bit = j * BITS, wi = bit >> 5, sh = bit & 31;
-    w[wi] |= (uint32_t)idx[j] << sh;
-    if (sh + BITS > 32) w[wi + 1] |= (uint32_t)idx[j] >> (32 - sh);
-  }
-}
-
-template <int BITS>
-__device__ __forceinline__ void unpack_codes(const uint32_t (&w)[BITS], int (&idx)[32]) {
-  constexpr uint32_t mask = (1u << BITS) - 1u;
-#pragma unroll
-  for (int j = 0; j < 32; j++) {
-    const int bit = j * BITS, wi = bit >> 5, sh = bit & 31;
-    uint32_t v = w[wi] >> sh;
-    if (sh + BITS > 32) v |= w[wi + 1] << (32 - sh);
-    idx[j] = (int)(v & mask);
-  }
-}
-
-template <int BITS>
-__device__ __forceinline__ void store_codes(uint8_t *p, const uint32_t (&w)[BITS]) {
-  if constexpr (BITS == 4) {
-    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-  } else if constexpr (BITS == 2) {
-    *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
-  } else {
-#pragma unroll
-    for (int k = 0; k < BITS; k++) reinterpret_cast<uint32_t *>(p)[k] = w[k];
-  }
-}
-
-// The same 4*BITS bytes (chunks 2q and 2q+1 of a token) in a grouped
-// value-code section (value_chunk_offset).
-template <int BITS>
-__device__ __forceinline__ void store_codes_grouped(uint8_t *sec, int64_t off, int q, const uint32_t (&w)[BITS]) {
-  uint8_t *c0 = sec + value_chunk_offset(off, 2 * q, BITS);
-  uint8_t *c1 = sec + value_chunk_offset(off, 2 * q + 1, BITS);
-  if constexpr (BITS == 4) {
-    *reinterpret_cast<uint2 *>(c0) = make_uint2(w[0], w[1]);
-    *reinterpret_cast<uint2 *>(c1) = make_uint2(w[2], w[3]);
-  } else if constexpr (BITS == 2) {
-    *reinterpret_cast<uint32_t *>(c0) = w[0];
-    *reinterpret_cast<uint32_t *>(c1) = w[1];
-  } else {  // 6-byte chunks: 4-byte aligned for even offsets, 2 bytes past that for odd ones
-    const uint32_t lo0 = w[0], hi0 = w[1] & 0xFFFFu;                   // chunk 2q: bytes 0..5
-    const uint32_t lo1 = __byte_perm(w[1], w[2], 0x5432), hi1 = w[2] >> 16;  // chunk 2q+1: bytes 6..11
-    if ((off & 1) == 0) {
-      *reinterpret_cast<uint32_t *>(c0) = lo0;
-      *reinterpret_cast<uint16_t *>(c0 + 4) = (uint16_t)hi0;
-      *reinterpret_cast<uint32_t *>(c1) = lo1;
-      *reinterpret_cast<uint16_t *>(c1 + 4) = (uint16_t)hi1;
-    } else {
-      *reinterpret_cast<uint16_t *>(c0) = (uint16_t)lo0;
-      *reinterpret_cast<uint32_t *>(c0 + 2) = (lo0 >> 16) | (hi0 << 16);
-      *reinterpret_cast<uint16_t *>(c1) = (uint16_t)lo1;
-      *reinterpret_cast<uint32_t *>(c1 + 2) = (lo1 >> 16) | (hi1 << 16);
-    }
-  }
-}
-
-template <int BITS>
-__device__ __forceinline__ void load_codes_grouped(const uint8_t *sec, int64_t off, int q, uint32_t (&w)[BITS]) {
-  const uint8_t *c0 = sec + value_chunk_offset(off, 2 * q, BITS);
-  const uint8_t *c1 = sec + value_chunk_offset(off, 2 * q + 1, BITS);
-  if constexpr (BITS == 4) {
-    const uint2 x = *reinterpret_cast<const uint2 *>(c0), y = *reinterpret_cast<const uint2 *>(c1);
-    w[0] = x.x; w[1] = x.y; w[2] = y.x; w[3] = y.y;
-  } else if constexpr (BITS == 2) {
-    w[0] = *reinterpret_cast<const uint32_t *>(c0);
-    w[1] = *reinterpret_cast<const uint32_t *>(c1);
-  } else {
-    const uint16_t *h0 = reinterpret_cast<const uint16_t *>(c0), *h1 = reinterpret_cast<const uint16_t *>(c1);
-    w[0] = (uint32_t)h0[0] | ((uint32_t)h0[1] << 16);
-    w[1] = (uint32_t)h0[2] | ((uint32_t)h1[0] << 16);
-    w[2] = (uint32_t)h1[1] | ((uint32_t)h1[2] << 16);
-  }
-}
-
-template <int BITS>
-__device__ __forceinline__ void load_codes(const uint8_t *p, uint32_t (&w)[BITS]) {
-  if constexpr (BITS == 4) {
-    uint4 v = *reinterpret_cast<const uint4 *>(p);
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  } else if constexpr (BITS == 2) {
-    uint2 v = *reinterpret_cast<const uint2 *>(p);
-    w[0] = v.x; w[1] = v.y;
-  } else {
-#pragma unroll
-    for (int k = 0; k < BITS; k++) w[k] = reinterpret_cast<const uint32_t *>(p)[k];
-  }
-}
-
-// 32 fp16 -> fp32 of this lane's slice.
-__device__ __forceinline__ void load_slice_f16(const __half *src, float (&x)[32]) {
-  const uint4 *p = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-  for (int k = 0; k < 4; k++) {
-    uint4 v = p[k];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
-      float2 f = __half22float2(h);
-      x[8 * k + 2 * i] = f.x;
-      x[8 * k + 2 * i + 1] = f.y;
-    }
-  }
-}
-
-// Unnormalized WHT of a 128-vector spread over a quad (lane slice q).
-__device__ __forceinline__ void fwht_quad(float (&x)[32], int q) {
-  fwht_local<32>(x);
-  fwht_xlane<32>(x, 1, (q & 1) != 0);
-  fwht_xlane<32>(x, 2, (q & 2) != 0);
-}
-
-// QJL matrix for the encode projection on the tensor cores: S split into
-// fp16 hi and lo parts, one 16-byte cell per (row l, lane slice t, k-step ks)
-// holding S[l][32t+4ks .. 32t+4ks+3] as {hi pair, hi pair, lo pair, lo pair};
-// the cell position inside its 128-byte row is XOR-swizzled by (t, l&1) so
-// the 8 lanes of each load phase read 8 different bank groups.
-__device__ __forceinline__ int sq_cell(int l, int t, int ks) { return (l * 4 + t) * 8 + (ks ^ (t + 4 * (l & 1))); }
-
-// Quantizer lookup.  Bucket k = 48 + round(4u) covers 4u in [k-48.5, k-47.5]
-// (both ends closed); since |u| <= sqrt(d) (||u||^2 = d), k stays in [2, 94].
-// Entry k = (number of thresholds below the bucket, the single threshold
-// inside it or +inf), so idx = #{t <= u} = base + [u >= thr] exactly, as long
-// as no bucket holds two thresholds (checked when the table is built; the
-// binary search is used otherwise).
-constexpr int kQBuckets = 96;
-constexpr float kQMagic = 12582912.0f + 48.0f;  // 1.5 * 2^23: the integer part lands in the low mantissa bits
-
-__device__ __forceinline__ int quant_bucket(float u) {
-  return __float_as_int(fmaf(u, 4.0f, kQMagic)) - __float_as_int(12582912.0f);
-}
-
-// Encode layout.  A warp encodes 8 vectors; thread (g, t) = (lane/4, lane%4)
-// holds vector g at coordinates 32c + 8t + i (block c = 0..3, i = 0..7).
-// With i = 32c + b the Sylvester matrix factors as H_128 = H_4 (x) H_32, so
-// the transform is one tensor-core product per block (z = x_c H_32, rows of
-// the A operand are (vector g, block 2m) and (vector g, block 2m+1)) and a
-// 4-point butterfly across the blocks a thread already holds.  The k and n
-// indices of the MMA are permuted so that a thread's operand words are its
-// own loaded fp16 pairs and its outputs are again coordinates 8t .. 8t+7.
-//   k (per k-step ks): 2t+e -> 8t+4ks+e, 2t+8+e -> 8t+4ks+2+e
-//   n (per n-tile nt): 8nt+2t'+e -> 8t'+2nt+e
-__device__ __forceinline__ uint32_t had_pair(int i0, int i1, int j) {
-  // fp16 pair (H32[i0][j], H32[i1][j]) of the unnormalized Sylvester matrix
-  const uint32_t s0 = (uint32_t)(__popc(i0 & j) & 1) << 15, s1 = (uint32_t)(__popc(i1 & j) & 1) << 31;
-  return 0x3C003C00u | s0 | s1;
-}
-
-#ifndef TQ_ENCODE_MIN_BLOCKS
-#define TQ_ENCODE_MIN_BLOCKS 3
-#endif
-// MIXED (keys at a fractional rate): BITS is the width of the high channels
-// (j mod 16 < 8), BITS - 1 that of the others; the codebook argument holds
-// the BITS-bit device codebook, then the (BITS - 1)-bit one.  The quad lanes
-// q = 0, 2 hold high channels (32c + 8q + i), q = 1, 3 low ones, so each lane
-// quantizes with one codebook set: set 0 (high) or set 1 (low).
-template <int BITS, bool QJL, bool MIXED = false>
-__device__ __forceinline__ void encode_body(const EncodeArgs &a) {
-  constexpr int NSET = MIXED ? 2 : 1;
-  extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells, QJL only
-  __shared__ float s_cent[NSET * 16];
-  __shared__ float s_mid[NSET * 16];
-  __shared__ uint32_t s_dsign[4];
-  __shared__ uint2 s_qlut[NSET * kQBuckets];
-  __shared__ float2 s_qcen[NSET * kQBuckets];  // centroids of codes base and base+1 (QJL residual)
-  __shared__ int s_lut_bad;                    // bit per set
-  constexpr int L = 1 << BITS;
-  const int tid = threadIdx.x;
-  if (tid < L) s_cent[tid] = a.codebook[tid];
-  if (tid < L - 1) s_mid[tid] = a.codebook[L + tid];
-  if constexpr (MIXED) {
-    const float *cb_lo = a.codebook + 2 * L - 1;
-    if (tid < L / 2) s_cent[16 + tid] = cb_lo[tid];
-    if (tid < L / 2 - 1) s_mid[16 + tid] = cb_lo[L / 2 + tid];
-  }
-  if (tid == 0) s_lut_bad = 0;
-  if (tid < kD) {  // sign words: one load per coordinate, packed by a ballot
-    const uint32_t w = __ballot_sync(0xffffffffu, a.signs[tid] != 0);
-    if ((tid & 31) == 0) s_dsign[tid >> 5] = w;
-  }
-  __syncthreads();
-  if ((tid & 127) < kQBuckets && (tid >> 7) < NSET) {
-    const int set = tid >> 7, bk = tid & 127, Ls = set ? L / 2 : L;
-    const float *mid = s_mid + 16 * set, *cen = s_cent + 16 * set;
-    const float lo = ((float)(bk - 48) - 0.5f) * 0.25f, hi = ((float)(bk - 48) + 0.5f) * 0.25f;
-    int base = 0, inside = 0;
-    float thr = __int_as_float(0x7f800000);  // +inf
-    for (int k = 0; k < Ls - 1; k++) {
-      const float t = mid[k];
-      if (t < lo) base++;
-      else if (t <= hi) { thr = t; inside++; }
-    }
-    if (inside > 1 || (bk == 0 && base > 0) || (bk == kQBuckets - 1 && inside + base < Ls - 1))
-      atomicOr(&s_lut_bad, 1 << set);
-    s_qlut[set * kQBuckets + bk] = make_uint2((uint32_t)base, __float_as_uint(thr));
-    s_qcen[set * kQBuckets + bk] = make_float2(cen[base], cen[base + 1 < Ls ? base + 1 : base]);
-  }
-  if constexpr (QJL) {
-    // cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
-    // coordinates thread t contributes at k-step ks of the projection
-    __half *sh = reinterpret_cast<__half *>(s_Sq);
-    for (int i = tid; i < kM * kD; i += blockDim.x) {
-      const int l = i / kD, j = i % kD;
-      __half hi, lo;
-      split_half(a.S[i], hi, lo);
-      const int cell = sq_cell(l, (j & 31) >> 3, 2 * (j >> 5) + ((j >> 2) & 1));
-      sh[cell * 8 + (j & 3)] = hi;
-      sh[cell * 8 + 4 + (j & 3)] = lo;
-    }
-  }
-  __syncthreads();
-
-  const int lane = tid & 31, q = lane & 3, quad_in_warp = lane >> 2;
-  const int warp = (blockIdx.x * blockDim.x + tid) >> 5;
-  const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / 32;
-  const int64_t NH = a.n_tokens * a.H;
-  const int64_t pool_slots = a.num_pages * (int64_t)a.P;
-  // this lane's codebook set (mixed keys: odd quad lanes hold low channels)
-  const int set = MIXED ? (q & 1) : 0;
-  const float *cent = s_cent + 16 * set, *midp = s_mid + 16 * set;
-  const uint2 *qlut = s_qlut + set * kQBuckets;
-  const float2 *qcen = s_qcen + set * kQBuckets;
-  const bool lut_bad = (s_lut_bad >> set) & 1;
-  const bool small = NH <= 0x7fffffff;
-  // sign masks of this thread's fp16 pairs (coordinates 32c + 8q + 2p, +1)
-  uint32_t smask[4][4];
-#pragma unroll
-  for (int c = 0; c < 4; c++) {
-    const uint32_t byte = (s_dsign[c] >> (8 * q)) & 0xFFu;
-#pragma unroll
-    for (int p = 0; p < 4; p++) smask[c][p] = ((byte >> (2 * p)) & 1u) << 15 | ((byte >> (2 * p + 1)) & 1u) << 31;
-  }
-  // B fragments of H_32 (k and n permuted as above), constant over the loop
-  uint32_t hb[2][4][2];
-#pragma unroll
-  for (int ks = 0; ks < 2; ks++)
-#pragma unroll
-    for (int nt = 0; nt < 4; nt++) {
-      const int j = 8 * (quad_in_warp >> 1) + 2 * nt + (quad_in_warp & 1);  // permuted column of n = 8nt + g
-      hb[ks][nt][0] = had_pair(8 * q + 4 * ks, 8 * q + 4 * ks + 1, j);
-      hb[ks][nt][1] = had_pair(8 * q + 4 * ks + 2, 8 * q + 4 * ks + 3, j);
-    }
-
-  for (int64_t vb = (int64_t)warp * 8; vb < NH; vb += nwarps * 8) {
-    const int64_t v = vb + quad_in_warp;
-    const bool in_range = v < NH;
-    const int64_t vv = in_range ? v : NH - 1;
-    int64_t n;
-    int h;
-    if (small) {  // 32-bit division for the common sizes
-      n = (uint32_t)vv / (uint32_t)a.H;
-      h = (int)((uint32_t)vv - (uint32_t)n * (uint32_t)a.H);
-    } else {
-      n = vv / a.H;
-      h = (int)(vv % a.H);
-    }
-    const int64_t slot = a.slot_mapping[n];
-    bool ok = in_range && slot >= 0;
-    if (ok && slot >= pool_slots) {
-      if (q == 0) report(a.err_word, TQ_DEVERR_SLOT_RANGE);
-      ok = false;
-    }
-
-    // fp16 pairs of coordinates 32c + 8q + 2p, +1, sign-flipped by D
-    uint32_t xw[4][4];
-    float ss = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; c++) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(a.x + vv * kD + 32 * c + 8 * q);
-      const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int p = 0; p < 4; p++) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r4[p]));
-        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-        xw[c][p] = r4[p] ^ smask[c][p];
-      }
-    }
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    const float nrm = sqrtf(ss);
-    // A NaN or infinite coordinate (finite fp16 vectors cannot overflow ss)
-    // stores the norm as computed and a zero block, and never reaches the
-    // quantizer's bucket table with a NaN.
-    const bool bad = !(ss <= 3.0e38f);
-    const bool zero = !(nrm > 0.f) || bad;
-
-    // z = x_c H_32 on the tensor cores, then the H_4 butterfly over blocks
-    float z[4][8];
-#pragma unroll
-    for (int mt = 0; mt < 2; mt++)
-#pragma unroll
-      for (int nt = 0; nt < 4; nt++) {
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(d, xw[2 * mt][0], xw[2 * mt + 1][0], xw[2 * mt][1], xw[2 * mt + 1][1], hb[0][nt][0], hb[0][nt][1]);
-        mma_16816(d, xw[2 * mt][2], xw[2 * mt + 1][2], xw[2 * mt][3], xw[2 * mt + 1][3], hb[1][nt][0], hb[1][nt][1]);
-        z[2 * mt][2 * nt] = d[0];
-        z[2 * mt][2 * nt + 1] = d[1];
-        z[2 * mt + 1][2 * nt] = d[2];
-        z[2 * mt + 1][2 * nt + 1] = d[3];
-      }
-    float x[32];  // x[8c + i]: coordinate 32c + 8q + i of H (D . x)
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      const float s01 = z[0][i] + z[1][i], d01 = z[0][i] - z[1][i];
-      const float s23 = z[2][i] + z[3][i], d23 = z[2][i] - z[3][i];
-      x[i] = s01 + s23;
-      x[8 + i] = d01 + d23;
-      x[16 + i] = s01 - s23;
-      x[24 + i] = d01 - d23;
-    }
-    if (bad) {
-#pragma unroll
-      for (int j = 0; j < 32; j++) x[j] = 0.f;
-    }
-    const float inv = zero ? 0.f : 1.0f / nrm;
-
-    int idx[32];
-    if (!lut_bad) {
-#pragma unroll
-      for (int j = 0; j < 32; j++) {
-        const float u = x[j] * inv;
-        const int b = quant_bucket(u);
-        const uint2 e = qlut[b];
-        const bool up = u >= __uint_as_float(e.y);
-        idx[j] = zero ? 0 : (int)e.x + (up ? 1 : 0);
-        if constexpr (QJL) {
-          const float2 c = qcen[b];
-          x[j] = u - (zero ? cent[0] : (up ? c.y : c.x));  // residual in u units
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; j++) {
-        const float u = x[j] * inv;
-        int k = 0;
-        const int Lq = set ? L / 2 : L;
-        for (int s = Lq / 2; s >= 1; s >>= 1)
-          if (u >= midp[k + s - 1]) k += s;
-        idx[j] = zero ? 0 : k;
-        x[j] = u - cent[idx[j]];  // residual in u units (QJL only)
-      }
-    }
-
-    // Norm correction (no QJL): store n / ||y_hat|| with y_hat = c[idx] / sqrt(d),
-    // i.e. n sqrt(d) / ||c[idx]||, so that the reconstruction keeps ||x||.
-    float nstore = nrm;
-    if (!QJL && a.norm_correct) {
-      float c2 = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; j++) {
-        const float cj = cent[idx[j]];
-        c2 = fmaf(cj, cj, c2);
-      }
-      c2 += __shfl_xor_sync(0xffffffffu, c2, 1);
-      c2 += __shfl_xor_sync(0xffffffffu, c2, 2);
-      nstore = (zero || !(c2 > 0.f)) ? nrm : nrm * 11.313708498984761f / sqrtf(c2);
-    }
-
-    const int64_t page = ok ? slot / a.P : 0;
-    const int64_t off = ok ? slot % a.P : 0;
-    uint8_t *slab = a.pool + page * a.page_bytes + (int64_t)h * a.slab_bytes;
-    if (MIXED && ok) {
-      // high stream (channels j mod 16 < 8) at BITS bits, then the low stream
-      // at BITS - 1: this lane's 8 codes of block c are group 2c + q/2 of its
-      // stream
-      const int W = set ? BITS - 1 : BITS;
-      uint8_t *tok = slab + a.codes_off + off * a.code_bytes;
-#pragma unroll
-      for (int c = 0; c < 4; c++) {
-        uint32_t w = 0u;
-#pragma unroll
-        for (int i = 0; i < 8; i++) w |= (uint32_t)idx[8 * c + i] << (W * i);
-        const int g = 2 * c + (q >> 1);
-        uint8_t *dst = set ? tok + 8 * BITS + g * (BITS - 1) : tok + g * BITS;
-        if (W == 4) {
-          *reinterpret_cast<uint32_t *>(dst) = w;
-        } else if (W == 2) {
-          *reinterpret_cast<uint16_t *>(dst) = (uint16_t)w;
-        } else {
-          dst[0] = (uint8_t)w;
-          dst[1] = (uint8_t)(w >> 8);
-          dst[2] = (uint8_t)(w >> 16);
-        }
-      }
-      if (q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nstore;
-    } else if (ok) {
-#pragma unroll
-      for (int c = 0; c < 4; c++) {
-        // codes of coordinates 32c + 8q .. +7: 8 * BITS bits, LSB first
-        uint32_t w = 0u;
-#pragma unroll
-        for (int i = 0; i < 8; i++) w |= (uint32_t)idx[8 * c + i] << (BITS * i);
-        uint8_t *dst = a.grouped ? slab + a.codes_off + value_chunk_offset(off, 2 * c + (q >> 1), BITS) + (q & 1) * BITS
-                                 : slab + a.codes_off + off * a.code_bytes + c * 4 * BITS + q * BITS;
-        if constexpr (BITS == 4) {
-          *reinterpret_cast<uint32_t *>(dst) = w;
-        } else if constexpr (BITS == 2) {
-          *reinterpret_cast<uint16_t *>(dst) = (uint16_t)w;
-        } else if (!a.grouped) {
-          // the quad's 4 x 3 bytes are 12 contiguous bytes: lanes 0..2 write
-          // one aligned word each, taking the neighbour's bytes by a shuffle
-          const uint32_t wn = __shfl_down_sync(0xfu << (lane & ~3), w, 1, 4);
-          if (q < 3) *reinterpret_cast<uint32_t *>(dst - q * BITS + 4 * q) = (w >> (8 * q)) | (wn << (24 - 8 * q));
-        } else {
-          // a 6-byte chunk is lanes (2k, 2k+1): the even lane writes it,
-          // 4-byte aligned for even page offsets, 2 bytes past that for odd
-          const uint32_t wn = __shfl_xor_sync(0xfu << (lane & ~3), w, 1);
-          if ((q & 1) == 0) {
-            const uint32_t lo = w | (wn << 24), hi = wn >> 8;  // 48 bits: lo (4 bytes) then hi (2 bytes)
-            if ((off & 1) == 0) {
-              *reinterpret_cast<uint32_t *>(dst) = lo;
-              *reinterpret_cast<uint16_t *>(dst + 4) = (uint16_t)hi;
-            } else {
-              *reinterpret_cast<uint16_t *>(dst) = (uint16_t)lo;
-              *reinterpret_cast<uint32_t *>(dst + 2) = (lo >> 16) | (hi << 16);
-            }
-          }
-        }
-      }
-      if (q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nstore;
-    }
-
-    if constexpr (QJL) {
-      // gamma = ||u - c|| / sqrt(d); the sign of (S e)_l does not depend on the
-      // positive factor 1/sqrt(d), so the projection uses u - c directly.
-      float g2 = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; j++) g2 = fmaf(x[j], x[j], g2);
-      g2 += __shfl_xor_sync(0xffffffffu, g2, 1);
-      g2 += __shfl_xor_sync(0xffffffffu, g2, 2);
-      const float gamma = zero ? 0.f : sqrtf(g2) * 0.08838834764831845f;
-      // (S e)_l on the tensor cores: rows g / g+8 of the A operand are the fp16
-      // hi / lo parts of this quad's residual (vector g of the warp), B is
-      // S hi then S lo, so the fp32 sum misses only the lo*lo term (~2^-22).
-      // k-indices 2t, 2t+1 | 2t+8, 2t+9 of step ks are the coordinates
-      // 32(ks/2) + 8t + 4(ks%2) + {0,1} | +{2,3}: x[4ks .. 4ks+3] of this lane.
-      uint32_t A[8][4];
-#pragma unroll
-      for (int ks = 0; ks < 8; ks++) {
-        __half h0, l0, h1, l1, h2, l2, h3, l3;
-        split_half(x[4 * ks + 0], h0, l0);
-        split_half(x[4 * ks + 1], h1, l1);
-        split_half(x[4 * ks + 2], h2, l2);
-        split_half(x[4 * ks + 3], h3, l3);
-        A[ks][0] = pack_half2_raw(h0, h1);
-        A[ks][1] = pack_half2_raw(l0, l1);
-        A[ks][2] = pack_half2_raw(h2, h3);
-        A[ks][3] = pack_half2_raw(l2, l3);
-      }
-      uint32_t words[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int nt = 0; nt < 16; nt++) {  // outputs l = 8nt .. 8nt+7; this lane gets 8nt+2q, 8nt+2q+1
-        float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f};
-        const int l = 8 * nt + quad_in_warp;
-#pragma unroll
-        for (int ks = 0; ks < 8; ks++) {
-          const uint4 sv = s_Sq[sq_cell(l, q, ks)];
-          mma_16816(dh, A[ks][0], A[ks][1], A[ks][2], A[ks][3], sv.x, sv.y);
-          mma_16816(dl, A[ks][0], A[ks][1], A[ks][2], A[ks][3], sv.z, sv.w);
-        }
-        const float p0 = (dh[0] + dh[2]) + (dl[0] + dl[2]);
-        const float p1 = (dh[1] + dh[3]) + (dl[1] + dl[3]);
-        const int bit = 8 * (nt & 3) + 2 * q;
-        words[nt >> 2] |= ((p0 >= 0.f ? 1u : 0u) << bit) | ((p1 >= 0.f ? 1u : 0u) << (bit + 1));
-      }
-#pragma unroll
-      for (int k = 0; k < 4; k++) {
-        words[k] |= __shfl_xor_sync(0xffffffffu, words[k], 1);
-        words[k] |= __shfl_xor_sync(0xffffffffu, words[k], 2);
-      }
-      uint32_t word = q == 0 ? words[0] : q == 1 ? words[1] : q == 2 ? words[2] : words[3];
-      if (zero) word = 0u;
-      if (ok) {
-        reinterpret_cast<uint32_t *>(slab + a.signs_off + off * (kM / 8))[q] = word;
-        if (q == 0) reinterpret_cast<float *>(slab + a.gamma_off)[off] = gamma;
-      }
-    }
-  }
-}
 
 template <int BITS, bool QJL, bool MIXED = false>
 __global__ void __launch_bounds__(256, QJL ? 2 : TQ_ENCODE_MIN_BLOCKS) encode_kernel(const EncodeArgs a) {

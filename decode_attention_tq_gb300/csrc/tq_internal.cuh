@@ -27,7 +27,7 @@ struct EncodeArgs {
   int32_t *err_word;
 };
 
-// Per-step window roll (tq_append_window): see tq_append.cu.
+// Per-step append (tq_append_window): see tq_append.cu.
 struct RollArgs {
   const __half *k_new, *v_new;  // [B][H][d]
   __half *k_win, *v_win;        // [B][H][W][d] (W > 0)
@@ -113,7 +113,10 @@ struct AttnArgs {
 };
 
 cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, bool mixed, int sms, cudaStream_t st);
-cudaError_t launch_window_roll(const RollArgs &a, cudaStream_t st);
+// One launch: window roll, encode of the staged keys and values, counters.
+// k_bits is the key code width (the high channels' width for mixed keys).
+cudaError_t launch_append(const RollArgs &r, const EncodeArgs &ka, const EncodeArgs &va, int k_bits, bool k_qjl,
+                          bool k_mixed, int v_bits, int sms, cudaStream_t st);
 
 // Launch `kern` on `st`, as a programmatic dependent of the previous kernel on
 // the stream when `dependent` (the kernel must call griddep_wait() before it

@@ -212,10 +212,10 @@ tq_status tq_append_window_workspace_size(const tq_format *fmt, int batch, size_
  *   workspace             device, >= tq_append_window_workspace_size bytes,
  *                         256-byte aligned; its contents need no setup
  * All counters are read and written on the device, so a step can be replayed
- * from a CUDA graph.  Two or three kernel launches on `stream`: the window
- * roll, then the append of the tokens that left the window (one launch when
- * k_bits == v_bits without QJL).  Host argument errors return before any
- * launch.  A negative or out-of-range counter (TQ_DEVERR_LENGTH), or a block
+ * from a CUDA graph.  One kernel launch on `stream`: each block rolls the
+ * windows of a group of sequences, encodes the keys and values that left
+ * them and then advances their counters.  Host argument errors return before
+ * any launch.  A negative or out-of-range counter (TQ_DEVERR_LENGTH), or a block
  * table entry outside [0, num_pages) (TQ_DEVERR_PAGE_RANGE), leaves that
  * sequence untouched and sets the bit in err_word.
  */
