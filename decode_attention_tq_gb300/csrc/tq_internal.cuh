@@ -183,8 +183,11 @@ cudaError_t set_smem_once(K kernel, int bytes, unsigned long long &done_mask) {
 #ifndef TQ_ATTN_THREADS_NT2_QJL
 #define TQ_ATTN_THREADS_NT2_QJL 256
 #endif
+#ifndef TQ_ATTN_THREADS_QJL
+#define TQ_ATTN_THREADS_QJL 512
+#endif
 __host__ __device__ constexpr int attn_threads(int nt, bool qjl) {
-  return nt == 1 ? TQ_ATTN_THREADS : (qjl ? TQ_ATTN_THREADS_NT2_QJL : TQ_ATTN_THREADS_NT2);
+  return nt == 1 ? (qjl ? TQ_ATTN_THREADS_QJL : TQ_ATTN_THREADS) : (qjl ? TQ_ATTN_THREADS_NT2_QJL : TQ_ATTN_THREADS_NT2);
 }
 __host__ __device__ constexpr int attn_warps(int nt, bool qjl) { return attn_threads(nt, qjl) / 32; }
 
