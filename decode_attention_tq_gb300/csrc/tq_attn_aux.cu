@@ -85,23 +85,26 @@ __device__ void prep_query(const AttnArgs &a, bool qjl, int64_t row, int lane, f
 #pragma unroll
     for (int i = 0; i < 4; i++) s_q[4 * lane + i] = x[i];
     __syncwarp();
-    float ys[4];
+    // rows 4 lane .. 4 lane + 3 of S side by side, so that 16 loads are in
+    // flight per step instead of 4 rows one after another
+    float ys[4] = {0.f, 0.f, 0.f, 0.f};
+    const float4 *srow = reinterpret_cast<const float4 *>(a.S + (int64_t)(4 * lane) * kD);
+#pragma unroll 4
+    for (int k = 0; k < kD / 4; k++) {
+      float4 sv[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) sv[i] = __ldg(srow + i * (kD / 4) + k);
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        ys[i] = fmaf(sv[i].x, s_q[4 * k], ys[i]);
+        ys[i] = fmaf(sv[i].y, s_q[4 * k + 1], ys[i]);
+        ys[i] = fmaf(sv[i].z, s_q[4 * k + 2], ys[i]);
+        ys[i] = fmaf(sv[i].w, s_q[4 * k + 3], ys[i]);
+      }
+    }
     float my = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float4 *srow = reinterpret_cast<const float4 *>(a.S + (int64_t)(4 * lane + i) * kD);
-      float acc = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < kD / 4; k++) {
-        const float4 s = __ldg(srow + k);
-        acc = fmaf(s.x, s_q[4 * k], acc);
-        acc = fmaf(s.y, s_q[4 * k + 1], acc);
-        acc = fmaf(s.z, s_q[4 * k + 2], acc);
-        acc = fmaf(s.w, s_q[4 * k + 3], acc);
-      }
-      ys[i] = acc;
-      my = fmaxf(my, fabsf(acc));
-    }
+    for (int i = 0; i < 4; i++) my = fmaxf(my, fabsf(ys[i]));
     *reinterpret_cast<float4 *>(a.q_s + row * kM + 4 * lane) = make_float4(ys[0], ys[1], ys[2], ys[3]);
     my = warp_max_xor(my, 31);
     es = my > 0.f ? 12 - ilogbf(my) : 0;

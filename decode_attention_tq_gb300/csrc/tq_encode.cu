@@ -45,7 +45,23 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
     s_dsign[tid] = w;
   }
   if constexpr (QJL) {
-    for (int i = tid; i < kM * kD; i += blockDim.x) s_S[s_swz(i / kD, i % kD)] = a.S[i];
+    // float4 loads, four per thread in flight; the swizzle keeps groups of
+    // four columns together
+    constexpr int N4 = kM * kD / 4;
+    const float4 *S4 = reinterpret_cast<const float4 *>(a.S);
+    for (int i0 = tid; i0 < N4; i0 += 4 * blockDim.x) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i4 = i0 + u * blockDim.x;
+        v[u] = i4 < N4 ? __ldg(S4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i4 = i0 + u * blockDim.x;
+        if (i4 < N4) *reinterpret_cast<float4 *>(&s_S[s_swz((4 * i4) / kD, (4 * i4) % kD)]) = v[u];
+      }
+    }
   }
   __syncthreads();
 

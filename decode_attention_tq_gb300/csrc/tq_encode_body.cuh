@@ -224,14 +224,33 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 =
   if constexpr (QJL) {
     // cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
     // coordinates thread t contributes at k-step ks of the projection
-    __half *sh = reinterpret_cast<__half *>(s_Sq);
-    for (int i = tid; i < kM * kD; i += blockDim.x) {
-      const int l = i / kD, j = i % kD;
-      __half hi, lo;
-      split_half(a.S[i], hi, lo);
-      const int cell = sq_cell(l, (j & 31) >> 3, 2 * (j >> 5) + ((j >> 2) & 1));
-      sh[cell * 8 + (j & 3)] = hi;
-      sh[cell * 8 + 4 + (j & 3)] = lo;
+    // four consecutive coordinates share a cell: float4 loads, four per
+    // thread in flight, and one 8-byte store each for the hi and lo halves
+    constexpr int N4 = kM * kD / 4;
+    const float4 *S4 = reinterpret_cast<const float4 *>(a.S);
+    uint2 *cells = reinterpret_cast<uint2 *>(s_Sq);
+    for (int i0 = tid; i0 < N4; i0 += 4 * blockDim.x) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i4 = i0 + u * blockDim.x;
+        v[u] = i4 < N4 ? __ldg(S4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i4 = i0 + u * blockDim.x;
+        if (i4 < N4) {
+          const int l = (4 * i4) / kD, j = (4 * i4) % kD;
+          __half h0, l0, h1, l1, h2, l2, h3, l3;
+          split_half(v[u].x, h0, l0);
+          split_half(v[u].y, h1, l1);
+          split_half(v[u].z, h2, l2);
+          split_half(v[u].w, h3, l3);
+          const int cell = sq_cell(l, (j & 31) >> 3, 2 * (j >> 5) + ((j >> 2) & 1));
+          cells[2 * cell] = make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(h2, h3));
+          cells[2 * cell + 1] = make_uint2(pack_half2_raw(l0, l1), pack_half2_raw(l2, l3));
+        }
+      }
     }
   }
   __syncthreads();
