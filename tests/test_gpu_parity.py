@@ -140,6 +140,13 @@ ATTN_CASES = {
     "k25qjl_v2_g8": (ti.Format(128, 2, 2, 1, 128, 64, 2, k_mixed=1), 2, 16, [600, 97], 16, [16, 16]),
     "k35qjl_v3_ragged": (ti.Format(128, 3, 3, 1, 128, 32, 4, k_mixed=1), 3, 16, [1, 333, 64], 8, [0, 8, 2]),
     "k25v4_p16": (ti.Format(128, 2, 4, 0, 128, 16, 8, k_mixed=1), 1, 32, [250], 0, [0]),
+    # windows longer than 8 chunks of 32 (the merge's second window path)
+    "k4v4_w300": (ti.Format(128, 4, 4, 0, 128, 64, 2), 2, 8, [410, 0], 300, [300, 259]),
+    # GQA groups that are not powers of two (partly filled MMA columns)
+    "k3v4_g3": (ti.Format(128, 3, 4, 0, 128, 64, 3), 2, 9, [333, 700], 16, [16, 1]),
+    "k4qjl_v2_g7": (ti.Format(128, 4, 2, 1, 128, 64, 2), 1, 14, [515], 32, [20]),
+    # a page of 48 tokens (three tiles per page) and many short sequences
+    "k4v4_p48_b24": (ti.Format(128, 4, 4, 0, 128, 48, 2), 24, 4, [int(x) for x in (np.arange(24) * 37) % 211], 8, [int(x) for x in np.arange(24) % 9]),
 }
 
 
