@@ -367,10 +367,10 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 =
         const int b = quant_bucket(u);
         const uint2 e = qlut[b];
         const bool up = u >= __uint_as_float(e.y);
-        idx[j] = zero ? 0 : (int)e.x + (up ? 1 : 0);
+        idx[j] = (int)e.x + (up ? 1 : 0);  // a zero vector's codes are cleared when packed
         if constexpr (QJL) {
           const float2 c = qcen[b];
-          x[j] = u - (zero ? cent[0] : (up ? c.y : c.x));  // residual in u units
+          x[j] = u - (up ? c.y : c.x);  // residual in u units (unused for a zero vector: gamma, bits 0)
         }
       }
     } else {
@@ -415,6 +415,7 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 =
         uint32_t w = 0u;
 #pragma unroll
         for (int i = 0; i < 8; i++) w |= (uint32_t)idx[8 * c + i] << (W * i);
+        if (zero) w = 0u;
         const int g = 2 * c + (q >> 1);
         uint8_t *dst = set ? tok + 8 * BITS + g * (BITS - 1) : tok + g * BITS;
         if (W == 4) {
@@ -434,7 +435,8 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 =
         // codes of coordinates 32c + 8q .. +7: 8 * BITS bits, LSB first
         uint32_t w = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; i++) w |= (uint32_t)idx[8 * c + i] << (BITS * i);
+        for (int i = 0; i < 8; i++) w += (uint32_t)idx[8 * c + i] << (BITS * i);  // disjoint fields: + is |
+        if (zero) w = 0u;
         uint8_t *dst = a.grouped ? slab + a.codes_off + value_chunk_offset(off, 2 * c + (q >> 1), BITS) + (q & 1) * BITS
                                  : slab + a.codes_off + off * a.code_bytes + c * 4 * BITS + q * BITS;
         if constexpr (BITS == 4) {
