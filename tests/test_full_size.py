@@ -50,43 +50,44 @@ def test_decode_workload_full_size(wl):
     import bench
     import decode_attention_tq_gb300 as tq
 
-    one = dataclasses.replace(wl, layers=1)
-    b = bench.DecodeBench(one, "cuda")
-    L = b.layers[0]
+    two = dataclasses.replace(wl, layers=min(wl.layers, 2))  # at least two layers, as the benchmark builds them
+    b = bench.DecodeBench(two, "cuda")
     f = b.fmt
     B, Hq, H, d = b.B, b.Hq, b.H, f.head_dim
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
-    tq.tq_decode_attn(f, L["q"], L["pool"], b.num_pages, b.bt, b.comp_lens, L["kwin"], L["vwin"], b.win_lens if b.W else None,
-                      b.ks, b.vs, b.kcb, b.vcb, b.S, out, b.ws, err_word=err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    got = out.cpu().numpy()
-    assert np.isfinite(got).all()
-
-    # sampled rows through the oracle, on the very same pool / window / query
-    pool = L["pool"].cpu().numpy()
-    rows = sorted({0, Hq - 1, (B - 1) * Hq, B * Hq - 1, (B // 2) * Hq + Hq // 2 + 1})
     kc, _ = oracle.kind_codebook(f, 0)
     vc, _ = oracle.kind_codebook(f, 1)
     S = b.S.cpu().numpy() if b.S is not None else None
-    rc, ref = oracle.attention(f, L["q"].cpu().numpy(), pool, b.num_pages, b.bt.cpu().numpy(), b.comp_lens.cpu().numpy(),
-                               L["kwin"].cpu().numpy() if b.W else None, L["vwin"].cpu().numpy() if b.W else None,
-                               b.win_lens.cpu().numpy(), b.ks.cpu().numpy(), b.vs.cpu().numpy(), kc, vc, S, heads=rows)
-    assert rc == 0
-    e = rel_err(got.reshape(B * Hq, d)[rows], ref)
-    assert e.max() <= REL_ATTN, (wl.name, e)
+    for li, L in enumerate(b.layers):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
+        tq.tq_decode_attn(f, L["q"], L["pool"], b.num_pages, b.bt, b.comp_lens, L["kwin"], L["vwin"], b.win_lens if b.W else None,
+                          b.ks, b.vs, b.kcb, b.vcb, b.S, out, b.ws, err_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        got = out.cpu().numpy()
+        assert np.isfinite(got).all()
 
-    # sampled tokens of the cache the benchmark built, re-encoded by the oracle
-    rng = np.random.default_rng(5)
-    comp, P = b.comp, f.page_size
-    slots_all = b.bt[:, torch.arange(comp, device="cuda") // P] * P + (torch.arange(comp, device="cuda") % P)[None, :]
-    for kind in (0, 1):
-        x = ti.kv_history(B, wl.context, H, d, 0, kind, device="cuda")[:, :comp]  # [B, comp, H, d]
-        for bb in sorted({0, B - 1}):
-            pick = _sample_positions(comp, P, rng)
-            _check_encode_samples(f, kind, x[bb], slots_all[bb].to(torch.int32), pool, b.num_pages, pick, f"{wl.name} b{bb}")
-        del x
+        # sampled rows through the oracle, on the very same pool / window / query
+        pool = L["pool"].cpu().numpy()
+        rows = sorted({0, Hq - 1, (B - 1) * Hq, B * Hq - 1, (B // 2) * Hq + Hq // 2 + 1 + li})
+        rc, ref = oracle.attention(f, L["q"].cpu().numpy(), pool, b.num_pages, b.bt.cpu().numpy(), b.comp_lens.cpu().numpy(),
+                                   L["kwin"].cpu().numpy() if b.W else None, L["vwin"].cpu().numpy() if b.W else None,
+                                   b.win_lens.cpu().numpy(), b.ks.cpu().numpy(), b.vs.cpu().numpy(), kc, vc, S, heads=rows)
+        assert rc == 0
+        e = rel_err(got.reshape(B * Hq, d)[rows], ref)
+        assert e.max() <= REL_ATTN, (wl.name, li, e)
+
+        # sampled tokens of this layer's cache, re-encoded by the oracle
+        rng = np.random.default_rng(5 + li)
+        comp, P = b.comp, f.page_size
+        slots_all = b.bt[:, torch.arange(comp, device="cuda") // P] * P + (torch.arange(comp, device="cuda") % P)[None, :]
+        for kind in (0, 1):
+            x = ti.kv_history(B, wl.context, H, d, li, kind, device="cuda")[:, :comp]  # [B, comp, H, d]
+            for bb in sorted({0, B - 1}):
+                pick = _sample_positions(comp, P, rng)
+                _check_encode_samples(f, kind, x[bb], slots_all[bb].to(torch.int32), pool, b.num_pages, pick,
+                                      f"{wl.name} layer {li} b{bb}")
+            del x
     del b
     torch.cuda.empty_cache()
 
