@@ -28,8 +28,9 @@
  * Lloyd-Max codes, optional 1-bit QJL residual sketch of length m on keys,
  * P = page_size tokens per page, H = num_kv_heads.  A valid format has d a
  * power of two and a multiple of 16 and P a multiple of 16 (pages hold whole
- * 16-token groups).  The GPU kernels support d = 128, b in {2, 3, 4},
- * m = 128; other valid shapes return TQ_ERR_UNSUPPORTED.
+ * 16-token groups).  The GPU kernels support d = 128, b in {2, 3, 4} (mixed
+ * keys: k_bits in {2, 3}, i.e. 2.5 and 3.5 bits), m = 128, and no norm
+ * correction on QJL keys; other valid shapes return TQ_ERR_UNSUPPORTED.
  */
 #ifndef TQ_H_
 #define TQ_H_
@@ -164,8 +165,9 @@ tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n
  * slot_mapping (byte-identical pages).  A decode step appends both kinds of
  * the new token at once (aither-kvcache README, section 'Algorithm': keys and
  * values are compressed alike, each with its own rotation and codebook).
- * When k_bits == v_bits and keys carry no QJL sketch this is one kernel
- * launch; otherwise it is two launches, in this order, on `stream`.
+ * When k_bits == v_bits, keys carry no QJL sketch and are not mixed-rate,
+ * this is one kernel launch; otherwise it is two launches, in this order, on
+ * `stream`.
  *   k_f16, v_f16          device fp16 [N][H][d]
  *   k_signs, v_signs      device uint8 [d] (the kinds' D)
  *   k_codebook/v_codebook device fp32 codebooks for k_bits / v_bits
