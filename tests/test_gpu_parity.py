@@ -389,3 +389,40 @@ def test_encode_non_finite_vector_is_a_zero_block(kind, qjl):
     assert np.array_equal(n[good], n2[good]) and np.array_equal(c[good], c2[good])
     if qjl:
         assert np.array_equal(g[good], g2[good]) and np.array_equal(s[good], s2[good])
+
+
+def _random_attention_cases(n=24, seed=2024):
+    """Seeded random formats and shapes: every key width (uniform and mixed),
+    value width, QJL on/off, page sizes, GQA groups 1..8, ragged lengths,
+    windows from none to several chunks."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        kmix = int(rng.random() < 0.3)
+        kb = int(rng.choice([2, 3])) if kmix else int(rng.choice([2, 3, 4]))
+        vb = int(rng.choice([2, 3, 4]))
+        qjl = int(rng.random() < 0.4)
+        P = int(rng.choice([16, 32, 48, 64, 128]))
+        H = int(rng.choice([1, 2, 4]))
+        G = int(rng.integers(1, 9))
+        B = int(rng.integers(1, 5))
+        W = int(rng.choice([0, 8, 40, 100]))
+        comp = [int(x) for x in rng.integers(0, 700, B)]
+        wl = [int(rng.integers(0, W + 1)) for _ in range(B)]
+        fmt = ti.Format(128, kb, vb, qjl, 128, P, H, k_mixed=kmix)
+        cases.append((f"r{i}_k{kb}{'m' if kmix else ''}v{vb}q{qjl}_p{P}_h{H}g{G}_b{B}_w{W}", fmt, B, H * G, comp, W, wl))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_attention_cases(), ids=lambda c: c[0])
+def test_attention_random_formats_match_oracle(case):
+    name, fmt, B, Hq, comp, W, wl = case
+    sc = Scenario(fmt, B, Hq, comp, W, wl, layer=7)
+    dev = sc.device_inputs()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_attention(sc, dev, err=err)
+    rc, ref = sc.oracle_attention()
+    assert rc == 0 and int(err.item()) == 0
+    e = rel_err(out, ref)
+    assert np.all(np.isfinite(out))
+    assert e.max() <= REL_ATTN, (name, e.max())
