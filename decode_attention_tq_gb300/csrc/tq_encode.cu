@@ -6,8 +6,15 @@
 
 namespace tq {
 
+// Blocks per SM: 2 with QJL (S cells in shared memory), else 3 for 4-bit and
+// 4 for 2- and 3-bit codes (measured: 3-bit +6 %, 2-bit +2 % at 4 blocks).
+template <int BITS, bool QJL>
+constexpr int encode_min_blocks() {
+  return QJL ? 2 : (BITS == 4 ? TQ_ENCODE_MIN_BLOCKS : 4);
+}
+
 template <int BITS, bool QJL, bool MIXED = false>
-__global__ void __launch_bounds__(256, QJL ? 2 : TQ_ENCODE_MIN_BLOCKS) encode_kernel(const EncodeArgs a) {
+__global__ void __launch_bounds__(256, encode_min_blocks<BITS, QJL>()) encode_kernel(const EncodeArgs a) {
   encode_body<BITS, QJL, MIXED>(a);
 }
 
