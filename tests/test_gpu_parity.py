@@ -426,3 +426,29 @@ def test_attention_random_formats_match_oracle(case):
     e = rel_err(out, ref)
     assert np.all(np.isfinite(out))
     assert e.max() <= REL_ATTN, (name, e.max())
+
+
+def _random_encode_cases(n=16, seed=77):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        kind = int(rng.integers(0, 2))
+        kmix = int(kind == 0 and rng.random() < 0.35)
+        bits = int(rng.choice([2, 3])) if kmix else int(rng.choice([2, 3, 4]))
+        qjl = int(kind == 0 and rng.random() < 0.5)
+        nc = int(rng.random() < 0.25 and not qjl)
+        P = int(rng.choice([16, 32, 48, 64, 128]))
+        H = int(rng.choice([1, 2, 3, 8]))
+        N = int(rng.integers(1, 400))
+        fmt = ti.Format(128, bits, bits, qjl, 128, P, H, norm_correct=nc, k_mixed=kmix)
+        out.append((f"e{i}_kind{kind}_b{bits}{'m' if kmix else ''}_q{qjl}_nc{nc}_p{P}_h{H}_n{N}", fmt, kind, N, 1000 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", _random_encode_cases(), ids=lambda c: c[0])
+def test_encode_random_formats_match_oracle(case):
+    name, fmt, kind, N, seed = case
+    zero = (N // 2,) if N > 2 else ()
+    neg = (N - 1,) if N > 3 else ()
+    pool, pool_ref, lay, slots, cm, sm, *_ = _encode_case(fmt, kind, N, seed=seed, zero_rows=zero, neg_slots=neg)
+    compare_encoded(pool, pool_ref, lay, fmt, kind, slots, cm, sm)
