@@ -642,11 +642,17 @@ def main():
     device = f"cuda:{local}"
     import __graft_entry__
 
-    __graft_entry__.build()
-
     def barrier():
         if pg:
             pg.barrier()
+
+    # one rank per node compiles (the others would race on the same objects);
+    # the rest find the library up to date after the barrier
+    if local == 0:
+        __graft_entry__.build()
+    barrier()
+    if local != 0:
+        __graft_entry__.build()
 
     def reduce_max(x):
         return max_over_ranks(x, pg, device)
