@@ -20,15 +20,18 @@
 //   QJL (keys): + signs[16 x 128] * (S q_rot)[128 x 2G], the +-1 operands are
 //        exact in fp16;
 //   online softmax in fp32 (log2 domain);
-//   acc[128 x 2G] += Vcodes^T[128 x 16] * W[16 x 2G], W = p_i * n_i / nu
-//        (nu = running max value norm) in fp16 in the even columns (the odd
-//        ones, the query's lo columns on the key side, are zero here); the
-//        value table maps a pair of codes to a pair of centroids, so the codes
-//        of the two tokens an A register pairs are interleaved and looked up
-//        once.
-// Thread (r = lane/4, t = lane%4) owns head 4*nt + t of n-tile nt, tokens r
-// and r+8 of a tile for the scores, and output coordinates 16r..16r+15 of the
-// value accumulator.
+//   acc[128 x G] += Vcodes^T[128 x 16] * W[16 x G], W = p_i * n_i / nu
+//        (nu = running max value norm) in fp16.  One MMA takes 8 tokens and
+//        two coordinate halves: its K index is (half h, token i), column
+//        4h + g of B holds head g's weights in the rows of half h and zeros
+//        in the other's, so the 8 columns carry 2 x 4 useful outputs and the
+//        accumulator needs no register for a zero column.  The value table
+//        maps a pair of codes to a pair of centroids, so the codes of the two
+//        tokens an A register pairs are interleaved and looked up once.
+// Thread (r = lane/4, t = lane%4) owns head 4*nt + t of n-tile nt and tokens r
+// and r+8 of a tile for the scores; for the values it reads the codes of
+// coordinates 16r..16r+15 and accumulates heads 4nt + 2(t&1), 4nt + 2(t&1) + 1
+// at coordinates 16r + 4mt + 2(t>>1) + {0, 1}, mt = 0..3.
 #pragma once
 
 #include "tq_internal.cuh"
@@ -412,10 +415,17 @@ struct TileCursor {
 
 // Register pipeline over tiles: 0 = load a tile, then compute it; 1 = the
 // whole next tile in flight while one is computed; 2 = the next tile's keys
-// in flight, a tile's values loaded as its keys are scored.
+// in flight, a tile's values loaded as its keys are scored.  Default: 2 for
+// uniform key widths, 0 for mixed ones (measured at the Llama-3-8B decode
+// shape, 32K context: K4/V4 141.3 us with 2 against 146.4 with 0; K3.5/V3
+// 188.4 against 169.0).
 #ifndef TQ_TILE_PIPELINE
-#define TQ_TILE_PIPELINE 0
+#define TQ_TILE_PIPELINE -1
 #endif
+template <int KB>
+__host__ __device__ constexpr int tile_pipeline() {
+  return TQ_TILE_PIPELINE >= 0 ? TQ_TILE_PIPELINE : (kb_mixed(KB) ? 0 : 2);
+}
 
 // Tile operands: 1 = bulk copies into a two-stage shared-memory ring per warp
 // (the next tile in flight while one is computed), 0 = loads into registers.
@@ -637,13 +647,13 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
     }
 
     float mu[NT], lsum[NT];
-    float acc[8][NT][4];
+    float acc[4][NT][4];  // value accumulator m-tiles (see the file header)
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
       mu[nt] = -INFINITY;
       lsum[nt] = 0.f;
 #pragma unroll
-      for (int mt = 0; mt < 8; mt++)
+      for (int mt = 0; mt < 4; mt++)
 #pragma unroll
         for (int i = 0; i < 4; i++) acc[mt][nt][i] = 0.f;
     }
@@ -758,33 +768,45 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
           mu[nt] = mnew;
           beta[nt] = alpha * nu_ratio;
         }
+        // accumulator columns hold heads 4nt + 2(t&1) (i = 0, 2) and
+        // 4nt + 2(t&1) + 1 (i = 1, 3): their factors from the lanes owning them
+        const int l0 = (lane & ~3) | (2 * (t & 1));
 #pragma unroll
-        for (int mt = 0; mt < 8; mt++)
+        for (int nt = 0; nt < NT; nt++) {
+          const float bA = __shfl_sync(0xffffffffu, beta[nt], l0), bB = __shfl_sync(0xffffffffu, beta[nt], l0 + 1);
 #pragma unroll
-          for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-            for (int i = 0; i < 4; i++) acc[mt][nt][i] *= beta[nt];
+          for (int mt = 0; mt < 4; mt++) {
+            acc[mt][nt][0] *= bA;
+            acc[mt][nt][1] *= bB;
+            acc[mt][nt][2] *= bA;
+            acc[mt][nt][3] *= bB;
+          }
+        }
       }
-      uint32_t wb[NT][2];
+      // wb[nt][s]: B operand of the value MMAs of token group s
+      uint32_t wb[NT][2][2];
 #pragma unroll
       for (int nt = 0; nt < NT; nt++) {
         const float p0 = fast_exp2(lg0[nt] - mu[nt]), p1 = fast_exp2(lg1[nt] - mu[nt]);
         lsum[nt] += p0 + p1;
         const float w0 = p0 * vn0 * inv_nu, w1 = p1 * vn1 * inv_nu;
-        // B operand column r = (head 4nt + r/2, even r only): weights of tokens
-        // 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) from the lanes that own them
-        const uint32_t Wh = pack_half2(w0, w1);
-        const int src0 = 4 * (2 * t) + (r >> 1), src1 = src0 + 4;
+        const uint32_t Wh = pack_half2(w0, w1);  // (token r, token r+8) of head 4nt + t
+        // column r = (coordinate half r/4, head 4nt + r%4): the weights of
+        // tokens 8s + 2t, 8s + 2t + 1 in the rows of half r/4, zeros in the
+        // other half's rows; the lanes (2t, r%4), (2t+1, r%4) own them
+        const int src0 = 4 * (2 * t) + (r & 3), src1 = src0 + 4;
         const uint32_t h0 = __shfl_sync(0xffffffffu, Wh, src0);
         const uint32_t h1 = __shfl_sync(0xffffffffu, Wh, src1);
-        const uint32_t x0 = (r & 1) ? 0u : h0, x1 = (r & 1) ? 0u : h1;
-        wb[nt][0] = __byte_perm(x0, x1, 0x5410);
-        wb[nt][1] = __byte_perm(x0, x1, 0x7632);
+        const uint32_t e0 = __byte_perm(h0, h1, 0x5410), e1 = __byte_perm(h0, h1, 0x7632);
+        const bool half0 = r < 4;
+        wb[nt][0][0] = half0 ? e0 : 0u;
+        wb[nt][0][1] = half0 ? 0u : e0;
+        wb[nt][1][0] = half0 ? e1 : 0u;
+        wb[nt][1][1] = half0 ? 0u : e1;
       }
       // ---- values: interleave the codes of the token pairs (2t, 2t+1) and
       // (2t+8, 2t+9) at each coordinate; one lookup gives an A register.
-      // Row r of m-tile mt is coordinate 16r+2mt, row r+8 is 16r+2mt+1.
-      // Table offset = pair code << 8 | lane * 4.
+      // Table offset = pair code << 8 | lane slot.
       uint32_t ev[2][2][2];  // [token pair][even/odd coordinate][word]
 #pragma unroll
       for (int tp = 0; tp < 2; tp++) {
@@ -804,50 +826,38 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
           }
         }
       }
-      if constexpr (VB == 2) {
-        // byte m of ev[tp][eo] holds the pairs of coordinates 4m + eo and
-        // 4m + 2 + eo, i.e. m-tiles 2m and 2m+1: one 8-byte read serves both
+      // token group s (tokens 8s + 2t, 8s + 2t + 1 in this lane's A
+      // registers), m-tile mt: A rows r / r+8 of half h are coordinates
+      // 16r + 4mt + 2h / 16r + 4mt + 2h + 1, so av[q] is coordinate 16r + 4mt + q
 #pragma unroll
-        for (int m = 0; m < 4; m++) {
-          uint32_t av0[4], av1[4];
+      for (int s = 0; s < 2; s++) {
 #pragma unroll
-          for (int tp = 0; tp < 2; tp++)
+        for (int mt = 0; mt < 4; mt++) {
+          uint32_t av[4];
+          if constexpr (VB == 2) {
+            // byte mt of ev[s][eo]: coordinates 4mt + eo and 4mt + 2 + eo
+            const uint2 pe = lut64(__byte_perm(ev[s][0][0], laneV, 0x7604 | (mt << 4)));
+            const uint2 po = lut64(__byte_perm(ev[s][1][0], laneV, 0x7604 | (mt << 4)));
+            av[0] = pe.x; av[1] = po.x; av[2] = pe.y; av[3] = po.y;
+          } else {
 #pragma unroll
-            for (int eo = 0; eo < 2; eo++) {
-              const uint2 pr = lut64(__byte_perm(ev[tp][eo][0], laneV, 0x7604 | (m << 4)));
-              av0[2 * tp + eo] = pr.x;
-              av1[2 * tp + eo] = pr.y;
+            for (int q = 0; q < 4; q++) {
+              uint32_t addr;
+              if constexpr (VB == 4) {
+                // byte k of ev[s][eo][wi] is coordinate 8wi + 2k + eo
+                addr = __byte_perm(ev[s][q & 1][mt >> 1], laneV, 0x7604 | ((2 * (mt & 1) + (q >> 1)) << 4));
+              } else {  // 3-bit: gather the two codes of coordinate 16r + 4mt + q
+                const int p3 = 3 * (4 * mt + q);
+                addr = field_at<8>(V.vlo[2 * s], V.vhi[2 * s], p3, 3, laneV) |
+                       field_at<11>(V.vlo[2 * s + 1], V.vhi[2 * s + 1], p3, 3, 0u);
+              }
+              av[q] = lut32(addr);
             }
-#pragma unroll
-          for (int nt = 0; nt < NT; nt++) {
-            mma_16816(acc[2 * m][nt], av0[0], av0[1], av0[2], av0[3], wb[nt][0], wb[nt][1]);
-            mma_16816(acc[2 * m + 1][nt], av1[0], av1[1], av1[2], av1[3], wb[nt][0], wb[nt][1]);
           }
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++)
+            mma_16816(acc[mt][nt], av[0], av[1], av[2], av[3], wb[nt][s][0], wb[nt][s][1]);
         }
-      } else {
-#pragma unroll
-      for (int mt = 0; mt < 8; mt++) {
-        uint32_t av[4];  // (tokens 2t,2t+1 | 2t+8,2t+9) x (coordinate 16r+2mt | 16r+2mt+1)
-#pragma unroll
-        for (int tp = 0; tp < 2; tp++) {
-#pragma unroll
-          for (int eo = 0; eo < 2; eo++) {
-            uint32_t addr;
-            if constexpr (VB == 4) {
-              addr = __byte_perm(ev[tp][eo][mt >> 2], laneV, 0x7604 | ((mt & 3) << 4));
-            } else if constexpr (VB == 2) {
-              addr = field_at<8>(ev[tp][eo][0], 0u, 4 * mt, 4, laneV);
-            } else {  // 3-bit: gather the two codes of coordinate 16r+2mt+eo
-              const int p3 = 3 * (2 * mt + eo);
-              addr = field_at<8>(V.vlo[2 * tp], V.vhi[2 * tp], p3, 3, laneV) |
-                     field_at<11>(V.vlo[2 * tp + 1], V.vhi[2 * tp + 1], p3, 3, 0u);
-            }
-            av[2 * tp + eo] = lut32(addr);
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++) mma_16816(acc[mt][nt], av[0], av[1], av[2], av[3], wb[nt][0], wb[nt][1]);
-      }
       }
     };
 
@@ -921,57 +931,57 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 #else
     auto keys = [&](KR &R) { load_keys<KB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, R); };
     auto vals = [&](VR &R) { load_values<VB>(a, cur.slab, cur.o0, r, t, R); };
-#if TQ_TILE_PIPELINE == 2
-    // keys one tile ahead (ping-pong ka / kb), values at the tile itself
-    KR ka, kb;
-    VR v;
-    keys(ka);
-    for (int k = 0;;) {
-      vals(v);
-      if (k + 1 < seg_tiles) {
-        step_cursor();
-        keys(kb);
+    if constexpr (tile_pipeline<KB>() == 2) {
+      // keys one tile ahead (ping-pong ka / kb), values at the tile itself
+      KR ka, kb;
+      VR v;
+      keys(ka);
+      for (int k = 0;;) {
+        vals(v);
+        if (k + 1 < seg_tiles) {
+          step_cursor();
+          keys(kb);
+        }
+        process(ka, v);
+        if (++k == seg_tiles) break;
+        vals(v);
+        if (k + 1 < seg_tiles) {
+          step_cursor();
+          keys(ka);
+        }
+        process(kb, v);
+        if (++k == seg_tiles) break;
       }
-      process(ka, v);
-      if (++k == seg_tiles) break;
-      vals(v);
-      if (k + 1 < seg_tiles) {
-        step_cursor();
-        keys(ka);
-      }
-      process(kb, v);
-      if (++k == seg_tiles) break;
-    }
-#elif TQ_TILE_PIPELINE == 1
-    // the next tile's loads are in flight while this one is computed
-    KR ka, kb;
-    VR va, vb;
-    keys(ka);
-    vals(va);
-    int k = 0;
-    for (; k + 2 <= seg_tiles; k += 2) {
-      step_cursor();
-      keys(kb);
-      vals(vb);
-      process(ka, va);
-      if (k + 2 < seg_tiles) {
-        step_cursor();
-        keys(ka);
-        vals(va);
-      }
-      process(kb, vb);
-    }
-    if (k < seg_tiles) process(ka, va);
-#else
-    for (int k = 0; k < seg_tiles; k++) {
-      KR ka;
-      VR va;
+    } else if constexpr (tile_pipeline<KB>() == 1) {
+      // the next tile's loads are in flight while this one is computed
+      KR ka, kb;
+      VR va, vb;
       keys(ka);
       vals(va);
-      process(ka, va);
-      if (k + 1 < seg_tiles) step_cursor();
+      int k = 0;
+      for (; k + 2 <= seg_tiles; k += 2) {
+        step_cursor();
+        keys(kb);
+        vals(vb);
+        process(ka, va);
+        if (k + 2 < seg_tiles) {
+          step_cursor();
+          keys(ka);
+          vals(va);
+        }
+        process(kb, vb);
+      }
+      if (k < seg_tiles) process(ka, va);
+    } else {
+      for (int k = 0; k < seg_tiles; k++) {
+        KR ka;
+        VR va;
+        keys(ka);
+        vals(va);
+        process(ka, va);
+        if (k + 1 < seg_tiles) step_cursor();
+      }
     }
-#endif
 
 #endif
 
@@ -981,22 +991,22 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
       const float ltot = warp_sum_xor(lsum[nt], 4 | 8 | 16);
-      const int g = 4 * nt + t;
-      if (g < G) {
-        const int64_t base = slot * G + g;
-        if (r == 0) {
-          a.seg_ml[base * 2] = mu[nt];
-          a.seg_ml[base * 2 + 1] = ltot;
-        }
-        float o[16];
+      const int g = 4 * nt + t;  // this lane's softmax state
+      if (g < G && r == 0) {
+        a.seg_ml[(slot * G + g) * 2] = mu[nt];
+        a.seg_ml[(slot * G + g) * 2 + 1] = ltot;
+      }
+      // this lane's accumulator: heads gA, gA + 1 at coordinates
+      // 16r + 4mt + 2(t>>1) + {0, 1}
+      const int gA = 4 * nt + 2 * (t & 1);
 #pragma unroll
-        for (int mt = 0; mt < 8; mt++) {
-          o[2 * mt] = (acc[mt][nt][0] + acc[mt][nt][1]) * vscale;
-          o[2 * mt + 1] = (acc[mt][nt][2] + acc[mt][nt][3]) * vscale;
-        }
-        float4 *dst = reinterpret_cast<float4 *>(a.seg_acc + base * kD + 16 * r);
+      for (int hh = 0; hh < 2; hh++) {
+        if (gA + hh < G) {
+          float *dst = a.seg_acc + (slot * G + gA + hh) * kD + 16 * r + 2 * (t >> 1);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; k4++) dst[k4] = make_float4(o[4 * k4], o[4 * k4 + 1], o[4 * k4 + 2], o[4 * k4 + 3]);
+          for (int mt = 0; mt < 4; mt++)
+            *reinterpret_cast<float2 *>(dst + 4 * mt) = make_float2(acc[mt][nt][hh] * vscale, acc[mt][nt][hh + 2] * vscale);
+        }
       }
     }
 
