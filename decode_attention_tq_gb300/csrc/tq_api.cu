@@ -331,8 +331,7 @@ tq_status tq_encode_kv(const tq_format *fmt, const void *k_f16, const void *v_f1
 
 tq_status tq_append_window_workspace_size(const tq_format *fmt, int batch, size_t *bytes) {
   if (!bytes || !format_valid(fmt) || batch < 0) return TQ_ERR_INVALID_ARG;
-  const size_t stage = (size_t)batch * fmt->num_kv_heads * fmt->head_dim * 2;
-  *bytes = 2 * align256(stage) + align256((size_t)batch * 4);
+  *bytes = 0;  // the append stages its tokens in shared memory
   return TQ_OK;
 }
 
@@ -345,19 +344,17 @@ tq_status tq_append_window(const tq_format *fmt, int batch, const void *k_new_f1
   if (!format_valid(fmt) || batch < 0 || window < 0 || max_pages < 1 || num_pages < 1) return TQ_ERR_INVALID_ARG;
   if (!format_gpu_supported(fmt)) return TQ_ERR_UNSUPPORTED;
   if (num_pages > INT32_MAX / fmt->page_size) return TQ_ERR_UNSUPPORTED;  // page slots are int32
-  if (!k_new_f16 || !v_new_f16 || !comp_lens || !block_tables || !workspace) return TQ_ERR_INVALID_ARG;
+  if (fmt->num_kv_heads > 128) return TQ_ERR_UNSUPPORTED;                 // a sequence's tokens in one block
+  if (!k_new_f16 || !v_new_f16 || !comp_lens || !block_tables) return TQ_ERR_INVALID_ARG;
   if (window > 0 && (!k_win_f16 || !v_win_f16 || !win_lens || !win_head)) return TQ_ERR_INVALID_ARG;
-  if (!aligned(k_new_f16, 16) || !aligned(v_new_f16, 16) || !aligned(workspace, 256) || !aligned(comp_lens, 4) ||
+  if (!aligned(k_new_f16, 16) || !aligned(v_new_f16, 16) || !aligned(comp_lens, 4) ||
       !aligned(block_tables, 4) || (window > 0 && (!aligned(k_win_f16, 16) || !aligned(v_win_f16, 16) ||
                                                    !aligned(win_lens, 4) || !aligned(win_head, 4))))
     return TQ_ERR_INVALID_ARG;
-  size_t need = 0;
-  tq_append_window_workspace_size(fmt, batch, &need);
-  if (workspace_bytes < need) return TQ_ERR_INVALID_ARG;
+  (void)workspace;  // no device workspace (tq_append_window_workspace_size is 0)
+  (void)workspace_bytes;
   if (batch == 0) return TQ_OK;
 
-  const size_t stage = align256((size_t)batch * fmt->num_kv_heads * fmt->head_dim * 2);
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
   RollArgs r;
   r.k_new = static_cast<const __half *>(k_new_f16);
   r.v_new = static_cast<const __half *>(v_new_f16);
@@ -373,17 +370,15 @@ tq_status tq_append_window(const tq_format *fmt, int batch, const void *k_new_f1
   r.win_head = win_head;
   r.comp_lens = comp_lens;
   r.block_tables = block_tables;
-  r.stage_k = reinterpret_cast<__half *>(ws);
-  r.stage_v = reinterpret_cast<__half *>(ws + stage);
-  r.stage_slots = reinterpret_cast<int32_t *>(ws + 2 * stage);
   r.err_word = err_word;
-  // the staged tokens (slot -1 where nothing left the window) go into the
-  // pages; their arguments are checked before anything is launched
+  // the encodes of the tokens that leave the windows (their inputs and page
+  // slots are set by the kernel, in shared memory); the arguments are checked
+  // before anything is launched
   EncodeArgs ka, va;
-  tq_status s = encode_args(fmt, TQ_KIND_K, r.stage_k, batch, r.stage_slots, page_pool, num_pages, k_signs, k_codebook,
-                            S, err_word, &ka);
+  tq_status s = encode_args(fmt, TQ_KIND_K, r.k_new, batch, comp_lens, page_pool, num_pages, k_signs, k_codebook, S,
+                            err_word, &ka);
   if (s != TQ_OK) return s;
-  s = encode_args(fmt, TQ_KIND_V, r.stage_v, batch, r.stage_slots, page_pool, num_pages, v_signs, v_codebook, nullptr,
+  s = encode_args(fmt, TQ_KIND_V, r.v_new, batch, comp_lens, page_pool, num_pages, v_signs, v_codebook, nullptr,
                   err_word, &va);
   if (s != TQ_OK) return s;
   int sms = 0;

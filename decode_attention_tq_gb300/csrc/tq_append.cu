@@ -12,12 +12,19 @@
 //     at compressed position comp_lens[b] and the new token takes its slot;
 //   * W == 0: the new token itself is encoded.
 //
-// A block owns a group of sequences and does everything for them: it reads
-// their counters, copies the tokens that leave into a staging buffer, writes
-// the new tokens into the rings, encodes the staged keys, then the staged
-// values (each kind with its own format), and last writes the counters.  No
-// other block touches these sequences, so one launch needs no cross-block
-// ordering.
+// A block owns a group of sequences and does everything for them, in three
+// phases separated by block barriers, so that one launch needs no
+// cross-block ordering and each phase waits on at most one memory latency:
+//   1. loads that depend on nothing: the sequences' counters, their new
+//      tokens (into shared memory), both kinds' codebooks and sign flips (and
+//      the QJL matrix);
+//   2. the action of each sequence from its counters; side by side, the block
+//      table entry of the compressed position it writes and the ring slot of
+//      the token that leaves (copied into shared memory); the quantizer
+//      tables are built meanwhile;
+//   3. the new tokens into the rings (every leaving token has been read),
+//      the counters, and the two encodes from shared memory at once: keys on
+//      warps 0-3, values on warps 4-7.
 #include "tq_encode_body.cuh"
 
 namespace tq {
@@ -26,6 +33,10 @@ namespace {
 
 constexpr int kChunks = kD / 8;    // 16-byte chunks per head vector
 constexpr int kMaxSeqPerBlock = 32;
+constexpr int kAppendThreads = 256;
+// Vectors per kind a block holds: at most 64 sequence-heads, or one sequence
+// of up to 128 heads (the largest head count tq_append_window accepts).
+constexpr int kAppendMaxVecs = 128;
 
 __device__ __forceinline__ void copy16(__half *dst, const __half *src) {
   *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
@@ -33,19 +44,52 @@ __device__ __forceinline__ void copy16(__half *dst, const __half *src) {
 
 enum : int { kSkip = 0, kFill = 1, kEvict = 2 };
 
+// Dynamic shared memory of a block: the QJL matrix cells (keys with a sketch)
+// at its start, then the new tokens and, with a window, the tokens that leave
+// it, each as [kind K, V][sequence][head][d] fp16.
+__host__ __device__ constexpr size_t append_cells_bytes(bool kqjl) { return kqjl ? (size_t)kM * kD * 4 : 0; }
+__host__ __device__ constexpr size_t append_smem_bytes(bool kqjl, int vecs, bool window) {
+  return append_cells_bytes(kqjl) + (size_t)(window ? 2 : 1) * 2 * vecs * kD * sizeof(__half);
+}
+
 template <int KBITS, bool KQJL, bool KMIX, int VBITS>
-__global__ void __launch_bounds__(256) append_kernel(const RollArgs r, const EncodeArgs ka, const EncodeArgs va,
-                                                     int seq_per_block) {
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const RollArgs r, const EncodeArgs ka,
+                                                                const EncodeArgs va, int seq_per_block) {
+  __shared__ EncodeTables<KMIX> tk;
+  __shared__ EncodeTables<false> tv;
   __shared__ int s_len[kMaxSeqPerBlock], s_head[kMaxSeqPerBlock], s_comp[kMaxSeqPerBlock], s_act[kMaxSeqPerBlock];
+  __shared__ int32_t s_slot[kMaxSeqPerBlock];
+  extern __shared__ __align__(16) uint8_t smem[];
   const int s0 = blockIdx.x * seq_per_block;
   const int ns = min(seq_per_block, r.B - s0);
   const int tid = threadIdx.x;
   const int W = r.W, H = r.H, P = r.P;
+  const int nsh = ns * H;                 // vectors per kind
+  const int nchunk = 2 * nsh * kChunks;   // 16-byte chunks of one token per (sequence, head, kind)
+  const int64_t win_h = (int64_t)W * kD;  // head stride inside a sequence's window
+  __half *s_new = reinterpret_cast<__half *>(smem + append_cells_bytes(KQJL));
+  __half *s_old = s_new + 2 * nsh * kD;
 
-  // 1. what each sequence does, from its counters
+  // 1. counters, new tokens, tables
   if (tid < ns) {
     const int b = s0 + tid;
-    const int len = W > 0 ? r.win_lens[b] : 0, head = W > 0 ? r.win_head[b] : 0, comp = r.comp_lens[b];
+    s_len[tid] = W > 0 ? r.win_lens[b] : 0;
+    s_head[tid] = W > 0 ? r.win_head[b] : 0;
+    s_comp[tid] = r.comp_lens[b];
+  }
+  for (int i = tid; i < nchunk; i += blockDim.x) {
+    const int kind = i >= nsh * kChunks, c = kind ? i - nsh * kChunks : i;
+    copy16(s_new + kind * nsh * kD + c * 8, (kind ? r.v_new : r.k_new) + (int64_t)s0 * H * kD + c * 8);
+  }
+  if (tid < kD) encode_tables_load<KBITS, KMIX>(tk, ka, tid);
+  else if (tid < 2 * kD) encode_tables_load<VBITS, false>(tv, va, tid - kD);
+  if constexpr (KQJL) encode_s_cells_load(ka);
+  __syncthreads();
+
+  // 2. actions, pages and leaving tokens, quantizer tables
+  if (tid < ns) {
+    const int b = s0 + tid;
+    const int len = s_len[tid], head = s_head[tid], comp = s_comp[tid];
     int act = kSkip, slot = -1;
     if (comp < 0 || (W > 0 && (len < 0 || len > W || head < 0 || head >= W))) {
       report(r.err_word, TQ_DEVERR_LENGTH);
@@ -61,56 +105,37 @@ __global__ void __launch_bounds__(256) append_kernel(const RollArgs r, const Enc
         slot = (int32_t)(page * P + comp % P);
       }
     }
-    s_len[tid] = len;
-    s_head[tid] = head;
-    s_comp[tid] = comp;
     s_act[tid] = act;
-    r.stage_slots[b] = slot;
+    s_slot[tid] = slot;
   }
+  if (W > 0) {
+    // a full ring with valid counters gives up its oldest token (whether its
+    // page turns out valid is decided above; an unused copy is harmless)
+    for (int i = tid; i < nchunk; i += blockDim.x) {
+      const int kind = i >= nsh * kChunks, c = kind ? i - nsh * kChunks : i;
+      const int sl = c / (H * kChunks), h = (c / kChunks) % H, e = (c % kChunks) * 8;
+      const int head = s_head[sl];
+      if (s_len[sl] != W || head < 0 || head >= W || s_comp[sl] < 0) continue;
+      const int64_t vec = (int64_t)(s0 + sl) * H + h;
+      copy16(s_old + kind * nsh * kD + c * 8, (kind ? r.v_win : r.k_win) + vec * win_h + (int64_t)head * kD + e);
+    }
+  }
+  encode_tables_build<KBITS, KMIX>(tk);
+  encode_tables_build<VBITS, false>(tv);
   __syncthreads();
 
-  // 2. stage the tokens that leave (or, without a window, the new ones); 3.
-  // after every thread has read the ring slots, write the new tokens
-  const int per_seq = 2 * H * kChunks;
-  const int64_t win_h = (int64_t)W * kD;  // head stride inside a sequence's window
-  for (int i = tid; i < ns * per_seq; i += blockDim.x) {
-    const int sl = i / per_seq, c = i % per_seq, kind = c >= H * kChunks, cc = kind ? c - H * kChunks : c;
-    const int h = cc / kChunks, e = (cc % kChunks) * 8;
-    if (s_act[sl] != kEvict) continue;
-    const int64_t vec = (int64_t)(s0 + sl) * H + h;
-    const __half *src = W == 0 ? (kind ? r.v_new : r.k_new) + vec * kD + e
-                               : (kind ? r.v_win : r.k_win) + vec * win_h + (int64_t)s_head[sl] * kD + e;
-    copy16((kind ? r.stage_v : r.stage_k) + vec * kD + e, src);
-  }
-  __syncthreads();
+  // 3. rings, counters, encodes (slot -1: nothing to encode for that sequence)
   if (W > 0) {
-    for (int i = tid; i < ns * per_seq; i += blockDim.x) {
-      const int sl = i / per_seq, c = i % per_seq, kind = c >= H * kChunks, cc = kind ? c - H * kChunks : c;
-      const int h = cc / kChunks, e = (cc % kChunks) * 8;
+    for (int i = tid; i < nchunk; i += blockDim.x) {
+      const int kind = i >= nsh * kChunks, c = kind ? i - nsh * kChunks : i;
+      const int sl = c / (H * kChunks), h = (c / kChunks) % H, e = (c % kChunks) * 8;
       const int act = s_act[sl];
       if (act == kSkip) continue;
       const int ring = act == kFill ? s_len[sl] : s_head[sl];
       const int64_t vec = (int64_t)(s0 + sl) * H + h;
-      copy16((kind ? r.v_win : r.k_win) + vec * win_h + (int64_t)ring * kD + e, (kind ? r.v_new : r.k_new) + vec * kD + e);
+      copy16((kind ? r.v_win : r.k_win) + vec * win_h + (int64_t)ring * kD + e, s_new + kind * nsh * kD + c * 8);
     }
   }
-
-  // 4. encode this block's staged keys, then values (slot -1: nothing staged)
-  const int64_t warp = tid >> 5, nwarps = blockDim.x >> 5;
-  EncodeArgs kl = ka;
-  kl.x = r.stage_k + (int64_t)s0 * H * kD;
-  kl.n_tokens = ns;
-  kl.slot_mapping = r.stage_slots + s0;
-  encode_body<KBITS, KQJL, KMIX>(kl, warp, nwarps);
-  __syncthreads();  // the two bodies may share their tables
-  EncodeArgs vl = va;
-  vl.x = r.stage_v + (int64_t)s0 * H * kD;
-  vl.n_tokens = ns;
-  vl.slot_mapping = r.stage_slots + s0;
-  encode_body<VBITS, false, false>(vl, warp, nwarps);
-
-  // 5. the counters, after every thread of the block has used them
-  __syncthreads();
   if (tid < ns) {
     const int b = s0 + tid, act = s_act[tid];
     if (act == kFill) {
@@ -120,25 +145,39 @@ __global__ void __launch_bounds__(256) append_kernel(const RollArgs r, const Enc
       r.comp_lens[b] = s_comp[tid] + 1;
     }
   }
+  const int warp = tid >> 5;
+  const __half *x = W > 0 ? s_old : s_new;  // the tokens to encode, [kind][sequence][head][d]
+  if (warp < 4) {
+    EncodeArgs kl = ka;
+    kl.x = x;
+    kl.n_tokens = ns;
+    kl.slot_mapping = s_slot;
+    encode_loop<KBITS, KQJL, KMIX>(tk, kl, warp, 4);
+  } else {
+    EncodeArgs vl = va;
+    vl.x = x + nsh * kD;
+    vl.n_tokens = ns;
+    vl.slot_mapping = s_slot;
+    encode_loop<VBITS, false, false>(tv, vl, warp - 4, 4);
+  }
 }
 
 template <int KBITS, bool KQJL, bool KMIX, int VBITS>
 cudaError_t launch_append_t(const RollArgs &r, const EncodeArgs &ka, const EncodeArgs &va, int sms, cudaStream_t st) {
   auto kern = append_kernel<KBITS, KQJL, KMIX, VBITS>;
-  const size_t smem = KQJL ? (size_t)kM * kD * sizeof(float) : 0;  // S cells of the key sketch
-  if (KQJL) {
-    static unsigned long long done = 0;
-    const cudaError_t e = set_smem_once(kern, (int)smem, done);
-    if (e != cudaSuccess) return e;
-  }
   // Sequences per block: as few as keep the grid about one wave of the
-  // machine (each block runs its copies and both encodes one after another)
+  // machine (a block's phases wait on memory latency, not on throughput)
   int spb = (r.B + sms - 1) / (sms > 0 ? sms : 1);
   const int cap = r.H >= 64 ? 1 : (64 / r.H < kMaxSeqPerBlock ? 64 / r.H : kMaxSeqPerBlock);
   if (spb > cap) spb = cap;
   if (spb < 1) spb = 1;
   const int blocks = (r.B + spb - 1) / spb;
-  kern<<<blocks, 256, smem, st>>>(r, ka, va, spb);
+  const size_t smem = append_smem_bytes(KQJL, spb * r.H, r.W > 0);
+  if (smem > append_smem_bytes(KQJL, kAppendMaxVecs, true)) return cudaErrorInvalidValue;
+  static unsigned long long done = 0;
+  const cudaError_t e = set_smem_once(kern, (int)append_smem_bytes(KQJL, kAppendMaxVecs, true), done);
+  if (e != cudaSuccess) return e;
+  kern<<<blocks, kAppendThreads, smem, st>>>(r, ka, va, spb);
   return cudaGetLastError();
 }
 

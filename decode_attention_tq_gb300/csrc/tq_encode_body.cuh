@@ -178,36 +178,84 @@ __device__ __forceinline__ uint32_t had_pair(int i0, int i1, int j) {
 // the BITS-bit device codebook, then the (BITS - 1)-bit one.  The quad lanes
 // q = 0, 2 hold high channels (32c + 8q + i), q = 1, 3 low ones, so each lane
 // quantizes with one codebook set: set 0 (high) or set 1 (low).
-// Warps [warp0, warp0 + nwarps) of the grid share the vectors (a grid-stride
-// loop); the default is every warp of the grid.
-template <int BITS, bool QJL, bool MIXED = false>
-__device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 = -1, int64_t nwarps_in = 0) {
-  constexpr int NSET = MIXED ? 2 : 1;
-  extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells, QJL only
-  __shared__ float s_cent[NSET * 16];
-  __shared__ float s_mid[NSET * 16];
-  __shared__ uint32_t s_dsign[4];
-  __shared__ uint2 s_qlut[NSET * kQBuckets];
-  __shared__ float2 s_qcen[NSET * kQBuckets];  // centroids of codes base and base+1 (QJL residual)
-  __shared__ int s_lut_bad;                    // bit per set
+//
+// The encode runs in three parts: encode_tables_load (global loads of the
+// codebook and sign flips into shared memory, plus the QJL matrix cells),
+// then after a block barrier encode_tables_build (the quantizer's bucket
+// table), then after another barrier encode_loop (the vectors).  A kernel
+// that encodes two kinds keeps two table sets and overlaps their loads.
+template <bool MIXED>
+struct EncodeTables {
+  static constexpr int NSET = MIXED ? 2 : 1;
+  float cent[NSET * 16];
+  float mid[NSET * 16];
+  uint32_t dsign[4];
+  uint2 qlut[NSET * kQBuckets];
+  float2 qcen[NSET * kQBuckets];  // centroids of codes base and base+1 (QJL residual)
+  int lut_bad;                    // bit per set
+};
+
+// Table loads by the 128 threads i = 0..127 (whole warps) of a block.
+template <int BITS, bool MIXED>
+__device__ __forceinline__ void encode_tables_load(EncodeTables<MIXED> &T, const EncodeArgs &a, int i) {
   constexpr int L = 1 << BITS;
-  const int tid = threadIdx.x;
-  if (tid < L) s_cent[tid] = a.codebook[tid];
-  if (tid < L - 1) s_mid[tid] = a.codebook[L + tid];
+  if (i < L) T.cent[i] = a.codebook[i];
+  if (i < L - 1) T.mid[i] = a.codebook[L + i];
   if constexpr (MIXED) {
     const float *cb_lo = a.codebook + 2 * L - 1;
-    if (tid < L / 2) s_cent[16 + tid] = cb_lo[tid];
-    if (tid < L / 2 - 1) s_mid[16 + tid] = cb_lo[L / 2 + tid];
+    if (i < L / 2) T.cent[16 + i] = cb_lo[i];
+    if (i < L / 2 - 1) T.mid[16 + i] = cb_lo[L / 2 + i];
   }
-  if (tid == 0) s_lut_bad = 0;
-  if (tid < kD) {  // sign words: one load per coordinate, packed by a ballot
-    const uint32_t w = __ballot_sync(0xffffffffu, a.signs[tid] != 0);
-    if ((tid & 31) == 0) s_dsign[tid >> 5] = w;
+  if (i == 0) T.lut_bad = 0;
+  // sign words: one load per coordinate, packed by a ballot
+  const uint32_t w = __ballot_sync(0xffffffffu, a.signs[i] != 0);
+  if ((i & 31) == 0) T.dsign[i >> 5] = w;
+}
+
+// QJL: the matrix S staged as fp16 hi/lo cells in dynamic shared memory, by
+// every thread of the block.
+__device__ __forceinline__ void encode_s_cells_load(const EncodeArgs &a) {
+  extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells
+  // cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
+  // coordinates thread t contributes at k-step ks of the projection
+  // four consecutive coordinates share a cell: float4 loads, four per
+  // thread in flight, and one 8-byte store each for the hi and lo halves
+  constexpr int N4 = kM * kD / 4;
+  const int tid = threadIdx.x;
+  const float4 *S4 = reinterpret_cast<const float4 *>(a.S);
+  uint2 *cells = reinterpret_cast<uint2 *>(s_Sq);
+  for (int i0 = tid; i0 < N4; i0 += 4 * blockDim.x) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int i4 = i0 + u * blockDim.x;
+      v[u] = i4 < N4 ? __ldg(S4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int i4 = i0 + u * blockDim.x;
+      if (i4 < N4) {
+        const int l = (4 * i4) / kD, j = (4 * i4) % kD;
+        __half h0, l0, h1, l1, h2, l2, h3, l3;
+        split_half(v[u].x, h0, l0);
+        split_half(v[u].y, h1, l1);
+        split_half(v[u].z, h2, l2);
+        split_half(v[u].w, h3, l3);
+        const int cell = sq_cell(l, (j & 31) >> 3, 2 * (j >> 5) + ((j >> 2) & 1));
+        cells[2 * cell] = make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(h2, h3));
+        cells[2 * cell + 1] = make_uint2(pack_half2_raw(l0, l1), pack_half2_raw(l2, l3));
+      }
+    }
   }
-  __syncthreads();
-  if ((tid & 127) < kQBuckets && (tid >> 7) < NSET) {
-    const int set = tid >> 7, bk = tid & 127, Ls = set ? L / 2 : L;
-    const float *mid = s_mid + 16 * set, *cen = s_cent + 16 * set;
+}
+
+// Quantizer bucket table from the loaded codebook (every thread of the block).
+template <int BITS, bool MIXED>
+__device__ __forceinline__ void encode_tables_build(EncodeTables<MIXED> &T) {
+  constexpr int L = 1 << BITS;
+  for (int e = threadIdx.x; e < EncodeTables<MIXED>::NSET * kQBuckets; e += blockDim.x) {
+    const int set = e / kQBuckets, bk = e % kQBuckets, Ls = set ? L / 2 : L;
+    const float *mid = T.mid + 16 * set, *cen = T.cent + 16 * set;
     const float lo = ((float)(bk - 48) - 0.5f) * 0.25f, hi = ((float)(bk - 48) + 0.5f) * 0.25f;
     int base = 0, inside = 0;
     float thr = __int_as_float(0x7f800000);  // +inf
@@ -217,44 +265,21 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 =
       else if (t <= hi) { thr = t; inside++; }
     }
     if (inside > 1 || (bk == 0 && base > 0) || (bk == kQBuckets - 1 && inside + base < Ls - 1))
-      atomicOr(&s_lut_bad, 1 << set);
-    s_qlut[set * kQBuckets + bk] = make_uint2((uint32_t)base, __float_as_uint(thr));
-    s_qcen[set * kQBuckets + bk] = make_float2(cen[base], cen[base + 1 < Ls ? base + 1 : base]);
+      atomicOr(&T.lut_bad, 1 << set);
+    T.qlut[set * kQBuckets + bk] = make_uint2((uint32_t)base, __float_as_uint(thr));
+    T.qcen[set * kQBuckets + bk] = make_float2(cen[base], cen[base + 1 < Ls ? base + 1 : base]);
   }
-  if constexpr (QJL) {
-    // cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
-    // coordinates thread t contributes at k-step ks of the projection
-    // four consecutive coordinates share a cell: float4 loads, four per
-    // thread in flight, and one 8-byte store each for the hi and lo halves
-    constexpr int N4 = kM * kD / 4;
-    const float4 *S4 = reinterpret_cast<const float4 *>(a.S);
-    uint2 *cells = reinterpret_cast<uint2 *>(s_Sq);
-    for (int i0 = tid; i0 < N4; i0 += 4 * blockDim.x) {
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int i4 = i0 + u * blockDim.x;
-        v[u] = i4 < N4 ? __ldg(S4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int i4 = i0 + u * blockDim.x;
-        if (i4 < N4) {
-          const int l = (4 * i4) / kD, j = (4 * i4) % kD;
-          __half h0, l0, h1, l1, h2, l2, h3, l3;
-          split_half(v[u].x, h0, l0);
-          split_half(v[u].y, h1, l1);
-          split_half(v[u].z, h2, l2);
-          split_half(v[u].w, h3, l3);
-          const int cell = sq_cell(l, (j & 31) >> 3, 2 * (j >> 5) + ((j >> 2) & 1));
-          cells[2 * cell] = make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(h2, h3));
-          cells[2 * cell + 1] = make_uint2(pack_half2_raw(l0, l1), pack_half2_raw(l2, l3));
-        }
-      }
-    }
-  }
-  __syncthreads();
+}
 
+// The vectors [n_tokens][H] of a.x (global or shared memory), 8 per warp and
+// step: warps [warp0, warp0 + nwarps) of the grid share them (a grid-stride
+// loop); the default is every warp of the grid.
+template <int BITS, bool QJL, bool MIXED = false>
+__device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const EncodeArgs &a, int64_t warp0 = -1,
+                                            int64_t nwarps_in = 0) {
+  extern __shared__ __align__(16) uint4 s_Sq[];  // QJL only
+  constexpr int L = 1 << BITS;
+  const int tid = threadIdx.x;
   const int lane = tid & 31, q = lane & 3, quad_in_warp = lane >> 2;
   const int64_t warp = warp0 >= 0 ? warp0 : (int64_t)((blockIdx.x * blockDim.x + tid) >> 5);
   const int64_t nwarps = warp0 >= 0 ? nwarps_in : (int64_t)gridDim.x * blockDim.x / 32;
@@ -262,16 +287,16 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 =
   const int64_t pool_slots = a.num_pages * (int64_t)a.P;
   // this lane's codebook set (mixed keys: odd quad lanes hold low channels)
   const int set = MIXED ? (q & 1) : 0;
-  const float *cent = s_cent + 16 * set, *midp = s_mid + 16 * set;
-  const uint2 *qlut = s_qlut + set * kQBuckets;
-  const float2 *qcen = s_qcen + set * kQBuckets;
-  const bool lut_bad = (s_lut_bad >> set) & 1;
+  const float *cent = T.cent + 16 * set, *midp = T.mid + 16 * set;
+  const uint2 *qlut = T.qlut + set * kQBuckets;
+  const float2 *qcen = T.qcen + set * kQBuckets;
+  const bool lut_bad = (T.lut_bad >> set) & 1;
   const bool small = NH <= 0x7fffffff;
   // sign masks of this thread's fp16 pairs (coordinates 32c + 8q + 2p, +1)
   uint32_t smask[4][4];
 #pragma unroll
   for (int c = 0; c < 4; c++) {
-    const uint32_t byte = (s_dsign[c] >> (8 * q)) & 0xFFu;
+    const uint32_t byte = (T.dsign[c] >> (8 * q)) & 0xFFu;
 #pragma unroll
     for (int p = 0; p < 4; p++) smask[c][p] = ((byte >> (2 * p)) & 1u) << 15 | ((byte >> (2 * p + 1)) & 1u) << 31;
   }
@@ -523,6 +548,19 @@ __device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 =
       }
     }
   }
+}
+
+
+// Load, build and loop in one call (kernels that encode one kind).
+template <int BITS, bool QJL, bool MIXED = false>
+__device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 = -1, int64_t nwarps_in = 0) {
+  __shared__ EncodeTables<MIXED> T;
+  if (threadIdx.x < kD) encode_tables_load<BITS, MIXED>(T, a, threadIdx.x);
+  if constexpr (QJL) encode_s_cells_load(a);
+  __syncthreads();
+  encode_tables_build<BITS, MIXED>(T);
+  __syncthreads();
+  encode_loop<BITS, QJL, MIXED>(T, a, warp0, nwarps_in);
 }
 
 }  // namespace tq

@@ -35,8 +35,6 @@ struct RollArgs {
   int64_t num_pages;
   int32_t *win_lens, *win_head, *comp_lens;  // [B], updated in place
   const int32_t *block_tables;               // [B][max_pages]
-  __half *stage_k, *stage_v;                 // [B][H][d] tokens to encode
-  int32_t *stage_slots;                      // [B] their page slots, -1: none
   int32_t *err_word;
 };
 

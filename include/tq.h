@@ -180,8 +180,10 @@ tq_status tq_encode_kv(const tq_format *fmt, const void *k_f16, const void *v_f1
                        int32_t *err_word, void *stream);
 
 /*
- * Bytes of device workspace tq_append_window needs for `batch` sequences
- * (staging for the tokens that leave the window).  Host only.
+ * Bytes of device workspace tq_append_window needs for `batch` sequences:
+ * 0 (the tokens that leave the window are staged in shared memory).  Kept so
+ * that callers size the workspace the same way as for tq_decode_attn.  Host
+ * only.
  */
 tq_status tq_append_window_workspace_size(const tq_format *fmt, int batch, size_t *bytes);
 
@@ -211,13 +213,14 @@ tq_status tq_append_window_workspace_size(const tq_format *fmt, int batch, size_
  *   comp_lens             device int32 [batch], updated in place
  *   block_tables          device int32 [batch][max_pages]
  *   signs, codebooks, S   as for tq_encode_kv
- *   workspace             device, >= tq_append_window_workspace_size bytes,
- *                         256-byte aligned; its contents need no setup
+ *   workspace             device, tq_append_window_workspace_size bytes (0:
+ *                         may be NULL)
  * All counters are read and written on the device, so a step can be replayed
  * from a CUDA graph.  One kernel launch on `stream`: each block rolls the
  * windows of a group of sequences, encodes the keys and values that left
  * them and then advances their counters.  Host argument errors return before
- * any launch.  A negative or out-of-range counter (TQ_DEVERR_LENGTH), or a block
+ * any launch; more than 128 kv heads return TQ_ERR_UNSUPPORTED (a block holds
+ * one sequence's tokens in shared memory).  A negative or out-of-range counter (TQ_DEVERR_LENGTH), or a block
  * table entry outside [0, num_pages) (TQ_DEVERR_PAGE_RANGE), leaves that
  * sequence untouched and sets the bit in err_word.
  */
