@@ -952,23 +952,6 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         process(kb, v);
         if (++k == seg_tiles) break;
       }
-    } else if constexpr (tile_pipeline<KB>() == 3) {
-      // keys one tile ahead as in 2, with one copy of the tile body: the next
-      // tile's key registers are moved into the current ones after each tile
-      KR ka, kn;
-      VR v;
-      keys(ka);
-      kn.ok0 = kn.ok1 = false;
-#pragma unroll 1
-      for (int k = 0; k < seg_tiles; k++) {
-        vals(v);
-        if (k + 1 < seg_tiles) {
-          step_cursor();
-          keys(kn);
-        }
-        process(ka, v);
-        ka = kn;
-      }
     } else if constexpr (tile_pipeline<KB>() == 1) {
       // the next tile's loads are in flight while this one is computed
       KR ka, kb;
