@@ -334,12 +334,16 @@ def test_append_window_matches_oracle(kb, vb, qjl, W, kmix):
     if W:
         assert np.array_equal(g_lens.cpu().numpy(), lens) and np.array_equal(g_head.cpu().numpy(), head)
         assert np.array_equal(g_kw.cpu().numpy(), kw) and np.array_equal(g_vw.cpu().numpy(), vw)
-    # pages: the evicted tokens, field by field against a direct oracle encode
-    pool = g_pool.cpu().numpy()
+    _check_append_pages(fmt, g_pool.cpu().numpy(), pool_ref, lay, evicted, num_pages, ks, vs, kcb, vcb, S)
+
+
+def _check_append_pages(fmt, pool, pool_ref, lay, evicted, num_pages, ks, vs, kcb, vcb, S):
+    """Pages after appends: the evicted tokens, field by field against a direct
+    oracle encode of them (each kind in its own pass)."""
+    from tq_testlib import written_mask
     slots = np.array([e[1] for e in evicted], np.int32)
     assert len(slots) > 0
-    from tq_testlib import written_mask
-    for kind, bits in ((0, kb), (1, vb)):
+    for kind in (0, 1):
         X = np.stack([e[2 + kind] for e in evicted])
         scratch = np.zeros_like(pool_ref)
         rc, _, cm, sm = oracle.encode(fmt, kind, X, slots, scratch, num_pages, ks if kind == 0 else vs,
@@ -349,6 +353,52 @@ def test_append_window_matches_oracle(kb, vb, qjl, W, kmix):
         pg = pool.copy()
         pg[other] = pool_ref[other]  # the other kind is checked in its own pass
         compare_encoded(pg, pool_ref, lay, fmt, kind, slots, cm, sm)
+
+
+@pytest.mark.parametrize("B,H,W,kb,vb,qjl", [(400, 4, 8, 4, 4, 0), (301, 2, 0, 3, 2, 1), (3, 128, 4, 4, 3, 1), (2, 64, 6, 2, 4, 0)])
+def test_append_window_block_shapes(B, H, W, kb, vb, qjl):
+    """The append's block shapes: several sequences per block (more sequences
+    than SMs), a shorter last block, and the largest head counts (one
+    sequence of 64 or 128 heads per block, QJL matrix and both token buffers
+    in shared memory).  Random initial states; all pages valid."""
+    fmt = ti.Format(128, kb, vb, qjl, 128, 16, H)
+    d, P = fmt.head_dim, fmt.page_size
+    steps = 6
+    rng = np.random.default_rng(B * 7 + H)
+    max_pages = 4
+    num_pages = B * max_pages
+    bt = rng.permutation(num_pages).astype(np.int32).reshape(B, max_pages)
+    comp = rng.integers(0, max_pages * P - steps, B).astype(np.int32)
+    lens = np.where(rng.random(B) < 0.6, W, rng.integers(0, W + 1, B)).astype(np.int32) if W else None
+    head = (rng.integers(0, W, B) * (lens == W)).astype(np.int32) if W else None
+    kw = (rng.standard_normal((B, H, W, d)) * 3).astype(np.float16) if W else None
+    vw = (rng.standard_normal((B, H, W, d)) * 3).astype(np.float16) if W else None
+    K = ti.kv_history(steps, B, H, d, 3, 0).numpy()
+    V = ti.kv_history(steps, B, H, d, 3, 1).numpy()
+    lay = oracle.page_layout(fmt)
+    pool_ref = np.full(num_pages * lay["page_bytes"], 0x5A, np.uint8)
+    kcb, vcb = oracle.kind_codebook(fmt, 0), oracle.kind_codebook(fmt, 1)
+    ks, vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
+    S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if qjl else None
+    dev = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    g_kw, g_vw, g_lens, g_head, g_comp, g_bt = dev(kw), dev(vw), dev(lens), dev(head), dev(comp), dev(bt)
+    g_pool = torch.full((pool_ref.size,), 0x5A, dtype=torch.uint8, device="cuda")
+    g_ks, g_vs, g_S = dev(ks), dev(vs), dev(S)
+    assert tq.tq_append_window_workspace_size(fmt, B) == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    evicted = []
+    for t in range(steps):
+        tq.tq_append_window(fmt, dev(K[t]), dev(V[t]), g_kw, g_vw, g_lens, g_head, g_comp, g_bt, g_pool, num_pages, g_ks, g_vs,
+                            tq.kind_codebook(fmt, 0), tq.kind_codebook(fmt, 1), g_S, err_word=err)
+        assert oracle.append_window(fmt, K[t], V[t], kw, vw, lens, head, comp, bt, pool_ref, num_pages, ks, vs, kcb, vcb, S,
+                                    evicted=evicted) == []
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(g_comp.cpu().numpy(), comp)
+    if W:
+        assert np.array_equal(g_lens.cpu().numpy(), lens) and np.array_equal(g_head.cpu().numpy(), head)
+        assert np.array_equal(g_kw.cpu().numpy(), kw) and np.array_equal(g_vw.cpu().numpy(), vw)
+    _check_append_pages(fmt, g_pool.cpu().numpy(), pool_ref, lay, evicted, num_pages, ks, vs, kcb, vcb, S)
 
 
 @pytest.mark.parametrize("kind,qjl", [(0, 1), (1, 0)])
