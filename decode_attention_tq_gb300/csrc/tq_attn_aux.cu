@@ -7,7 +7,9 @@
 //            per 32-token chunk;
 //   merge  : log-sum-exp merge of the compressed partials of a (sequence,
 //            query head), one inverse rotation of their value accumulator
-//            (D_V . H acc / d), then the window partials, normalised.
+//            (D_V . H acc / d), then the window partials, normalised; one
+//            warp per (sequence, query head) when they have few partials, one
+//            128-thread block otherwise.
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -259,11 +261,12 @@ __device__ __forceinline__ float block_sum128(float v, float *s_red) {
   return r;
 }
 
-// Online log-sum-exp merge of n partials (max, sum, accumulator column j),
-// 32 at a time: the accumulator columns of a chunk are loaded into registers
-// together with the (max, sum) pairs, so a chunk costs one memory latency.
+// Block variant (rows with many partials): online log-sum-exp merge of n
+// partials (max, sum, accumulator column j = thread), 32 at a time: the
+// accumulator columns of a chunk are loaded into registers together with the
+// (max, sum) pairs, so a chunk costs one memory latency.
 template <class ML, class ACC>
-__device__ __forceinline__ void merge_partials(int64_t n, ML ml, ACC acc_of, float &M, float &L, float &A, float *s_w,
+__device__ __forceinline__ void merge_partials_block(int64_t n, ML ml, ACC acc_of, float &M, float &L, float &A, float *s_w,
                                                float *s_red) {
   constexpr int kChunk = 32;
   const int j = threadIdx.x;
@@ -299,7 +302,9 @@ __device__ __forceinline__ void merge_partials(int64_t n, ML ml, ACC acc_of, flo
   }
 }
 
-__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
+// Block variant: one 128-thread block per (sequence, query head) row, thread
+// = output coordinate.
+__global__ void __launch_bounds__(128) attn_merge_block_kernel(const AttnArgs a) {
   __shared__ float s_x[kD];
   __shared__ float s_w[128];
   __shared__ float s_red[4];
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
     const int64_t o = a.H * a.pre[b] + h * tb;
     const int64_t w0 = tile_owner(o, T, NW), w1 = tile_owner(o + tb - 1, T, NW);
     const int64_t unit = (int64_t)b * a.H + h;
-    merge_partials(
+    merge_partials_block(
         w1 - w0 + 1,
         [&](int64_t k) {
           const int64_t w = w0 + k;
@@ -370,11 +375,141 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a) {
     Lt = Lt * sold + lsum;
     M = Mn;
   } else if (nwin > kWinPre) {
-    merge_partials(
+    merge_partials_block(
         nwin, [&](int64_t k) { return make_float2(a.win_ml[(row * nch + k) * 2], a.win_ml[(row * nch + k) * 2 + 1]); },
         [&](int64_t k) { return a.win_acc + (row * nch + k) * kD; }, M, Lt, At, s_w, s_red);
   }
   a.out[row * kD + j] = (M != -INFINITY && Lt > 0.f) ? At / Lt : 0.f;
+}
+
+// Partials per chunk of the warp merge (32 float4 accumulators would spill).
+constexpr int kWarpMergeMaxPartials = 24;
+
+// One chunk of up to 32 partials merged into the running (M, L, A) of a
+// warp: lane i holds the (max m, sum l) of partial i, v[u] the accumulator
+// coordinates 4 lane .. 4 lane + 3 of partial i0 + u.
+__device__ __forceinline__ float chunk_weight(float m, float l, float &M, float &L, float4 &A, float &lsum) {
+  const float Mn = fmaxf(M, warp_max_xor(m, 31));
+  const float w = m == -INFINITY ? 0.f : exp2f(m - Mn);
+  lsum = warp_sum_xor(l * w, 31);
+  const float sold = Mn == -INFINITY ? 1.f : exp2f(M - Mn);
+  A.x *= sold;
+  A.y *= sold;
+  A.z *= sold;
+  A.w *= sold;
+  L *= sold;
+  M = Mn;
+  return w;
+}
+template <int N>
+__device__ __forceinline__ void chunk_accumulate(float w, int i0, const float4 (&v)[N], float4 &A) {
+#pragma unroll
+  for (int u = 0; u < N; u++) {
+    const float wu = __shfl_sync(0xffffffffu, w, (i0 + u) & 31);
+    A.x = fmaf(wu, v[u].x, A.x);
+    A.y = fmaf(wu, v[u].y, A.y);
+    A.z = fmaf(wu, v[u].z, A.z);
+    A.w = fmaf(wu, v[u].w, A.w);
+  }
+}
+
+// Online log-sum-exp merge of n partials (max, sum, accumulator) into the
+// running (M, L, A) of one warp; lane l holds accumulator coordinates
+// 4l .. 4l+3.  kChunk (<= 32) partials at a time: their accumulators
+// (kChunk float4 loads per lane) are issued together with their (max, sum)
+// pairs (one per lane), so a chunk costs one memory latency.
+template <int kChunk, class ML, class ACC>
+__device__ __forceinline__ void merge_partials(int64_t n, ML ml, ACC acc_of, float &M, float &L, float4 &A, int lane) {
+  for (int64_t c0 = 0; c0 < n; c0 += kChunk) {
+    const int cn = (int)min((int64_t)kChunk, n - c0);
+    float4 v[kChunk];
+#pragma unroll
+    for (int u = 0; u < kChunk; u++)
+      v[u] = u < cn ? reinterpret_cast<const float4 *>(acc_of(c0 + u))[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float m = -INFINITY, l = 0.f;
+    if (lane < cn) {
+      const float2 p = ml(c0 + lane);
+      m = p.x;
+      l = p.y;
+    }
+    float lsum;
+    const float w = chunk_weight(m, l, M, L, A, lsum);  // w = 0 past cn
+    chunk_accumulate(w, 0, v, A);
+    L += lsum;
+  }
+}
+
+// Warp variant (rows with few partials): one warp per (sequence, query head)
+// row, four rows per block; no shared memory and no block barriers.
+__global__ void __launch_bounds__(128) attn_merge_warp_kernel(const AttnArgs a) {
+  griddep_wait();  // the main kernel's partials
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);  // b * Hq + qh
+  if (row >= (int64_t)a.B * a.Hq) return;
+  const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
+  const int h = qh / a.G, g = qh % a.G;
+  const int64_t T = a.hdr->total_tiles, NW = a.hdr->active_warps;
+  // the window partials do not depend on the compressed merge: up to kWinPre
+  // chunks are loaded first (longer windows are merged from memory later)
+  constexpr int kWinPre = 8;
+  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
+  const int64_t nwin = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
+  float4 wv[kWinPre];
+  float wm = -INFINITY, wl = 0.f;
+  if (nwin <= kWinPre) {
+#pragma unroll
+    for (int u = 0; u < kWinPre; u++)
+      wv[u] = u < nwin ? reinterpret_cast<const float4 *>(a.win_acc + (row * nch + u) * kD)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < nwin) {
+      const float2 v = *reinterpret_cast<const float2 *>(a.win_ml + (row * nch + lane) * 2);
+      wm = v.x;
+      wl = v.y;
+    }
+  }
+  float M = -INFINITY, L = 0.f;
+  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t tb = a.pre[b + 1] - a.pre[b];
+  if (tb > 0 && NW > 0) {
+    const int64_t o = a.H * a.pre[b] + h * tb;
+    const int64_t w0 = tile_owner(o, T, NW), w1 = tile_owner(o + tb - 1, T, NW);
+    const int64_t unit = (int64_t)b * a.H + h;
+    merge_partials<kWarpMergeMaxPartials>(
+        w1 - w0 + 1,
+        [&](int64_t k) {
+          const int64_t w = w0 + k;
+          // a warp's range can only be empty when there are fewer tiles than warps
+          if (T < NW && T * w / NW >= T * (w + 1) / NW) return make_float2(-INFINITY, 0.f);
+          return *reinterpret_cast<const float2 *>(a.seg_ml + ((w + unit) * a.G + g) * 2);
+        },
+        [&](int64_t k) { return a.seg_acc + ((w0 + k + unit) * a.G + g) * kD; }, M, L, A, lane);
+  }
+  // inverse rotation of the rotated-domain accumulator: D_V . (H A) / d
+  float x[4] = {A.x, A.y, A.z, A.w};
+  fwht_local<4>(x);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) fwht_xlane<4>(x, m, (lane & m) != 0);
+#pragma unroll
+  for (int i = 0; i < 4; i++) x[i] = (a.v_signs[4 * lane + i] ? -x[i] : x[i]) * (1.0f / (float)kD);
+  A = make_float4(x[0], x[1], x[2], x[3]);
+
+  // window partials (raw domain), merged onto the compressed part
+  if (nwin > 0 && nwin <= kWinPre) {
+    float lsum;
+    const float w = chunk_weight(wm, wl, M, L, A, lsum);
+    chunk_accumulate(w, 0, wv, A);
+    L += lsum;
+  } else if (nwin > kWinPre) {
+    merge_partials<kWinPre>(
+        nwin, [&](int64_t k) { return *reinterpret_cast<const float2 *>(a.win_ml + (row * nch + k) * 2); },
+        [&](int64_t k) { return a.win_acc + (row * nch + k) * kD; }, M, L, A, lane);
+  }
+  const bool ok = M != -INFINITY && L > 0.f;
+  const float inv = ok ? 1.0f / L : 0.f;  // no token: a zero row
+  float *o = a.out + row * kD + 4 * lane;  // out is 4-byte aligned
+  o[0] = A.x * inv;
+  o[1] = A.y * inv;
+  o[2] = A.z * inv;
+  o[3] = A.w * inv;
 }
 
 cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
@@ -386,7 +521,13 @@ cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
 }
 
 cudaError_t launch_attn_merge(const AttnArgs &a, cudaStream_t st) {
-  const cudaError_t e = launch_maybe_dependent(attn_merge_kernel, dim3((unsigned)((int64_t)a.B * a.Hq)), dim3(128), 0, st, a.pdl, a);
+  // warp rows when a (sequence, kv head) averages at most 24 partials (one
+  // chunk of the warp merge); blocks of 128 threads per row otherwise
+  const int64_t rows = (int64_t)a.B * a.Hq, units = (int64_t)a.B * a.H;
+  const cudaError_t e =
+      (int64_t)a.nw_launch <= kWarpMergeMaxPartials * units
+          ? launch_maybe_dependent(attn_merge_warp_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, st, a.pdl, a)
+          : launch_maybe_dependent(attn_merge_block_kernel, dim3((unsigned)rows), dim3(128), 0, st, a.pdl, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
