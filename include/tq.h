@@ -220,9 +220,10 @@ tq_status tq_append_window_workspace_size(const tq_format *fmt, int batch, size_
  * windows of a group of sequences, encodes the keys and values that left
  * them and then advances their counters.  Host argument errors return before
  * any launch; more than 128 kv heads return TQ_ERR_UNSUPPORTED (a block holds
- * one sequence's tokens in shared memory).  A negative or out-of-range counter (TQ_DEVERR_LENGTH), or a block
- * table entry outside [0, num_pages) (TQ_DEVERR_PAGE_RANGE), leaves that
- * sequence untouched and sets the bit in err_word.
+ * one sequence's tokens in shared memory).  A negative or out-of-range
+ * counter (TQ_DEVERR_LENGTH), or a block table entry outside [0, num_pages)
+ * (TQ_DEVERR_PAGE_RANGE), leaves that sequence untouched and sets the bit in
+ * err_word.
  */
 tq_status tq_append_window(const tq_format *fmt, int batch, const void *k_new_f16, const void *v_new_f16,
                            void *k_win_f16, void *v_win_f16, int window, int32_t *win_lens, int32_t *win_head,
