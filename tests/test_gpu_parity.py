@@ -145,6 +145,11 @@ ATTN_CASES = {
     # GQA groups that are not powers of two (partly filled MMA columns)
     "k3v4_g3": (ti.Format(128, 3, 4, 0, 128, 64, 3), 2, 9, [333, 700], 16, [16, 1]),
     "k4qjl_v2_g7": (ti.Format(128, 4, 2, 1, 128, 64, 2), 1, 14, [515], 32, [20]),
+    # 4-bit keys without QJL (centroid tables shifted to 64 KB shared-window
+    # boundaries) with every value width and both column-tile counts
+    "k4v4_g8_w": (ti.Format(128, 4, 4, 0, 128, 64, 2), 2, 16, [800, 310], 24, [24, 7]),
+    "k4v3_g6": (ti.Format(128, 4, 3, 0, 128, 32, 2), 2, 12, [450, 1], 0, [0, 0]),
+    "k4v2_g4_w": (ti.Format(128, 4, 2, 0, 128, 64, 4), 2, 16, [390, 1025], 40, [40, 33]),
     # a page of 48 tokens (three tiles per page) and many short sequences
     "k4v4_p48_b24": (ti.Format(128, 4, 4, 0, 128, 48, 2), 24, 4, [int(x) for x in (np.arange(24) * 37) % 211], 8, [int(x) for x in np.arange(24) % 9]),
 }
