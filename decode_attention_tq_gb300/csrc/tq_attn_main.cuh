@@ -22,16 +22,18 @@
 //   online softmax in fp32 (log2 domain);
 //   acc[128 x G] += Vcodes^T[128 x 16] * W[16 x G], W = p_i * n_i / nu
 //        (nu = running max value norm) in fp16.  One MMA takes 8 tokens and
-//        two coordinate halves: its K index is (half h, token i), column
-//        4h + g of B holds head g's weights in the rows of half h and zeros
-//        in the other's, so the 8 columns carry 2 x 4 useful outputs and the
-//        accumulator needs no register for a zero column.  The value table
-//        maps a pair of codes to a pair of centroids, so the codes of the two
-//        tokens an A register pairs are interleaved and looked up once.
+//        32 coordinates, and column 4e + g of B holds head g's weights in
+//        the rows of part e and zeros in the others, so the 8 columns carry
+//        2 x 4 useful outputs, with no accumulator register for a zero
+//        column.  The K index of an MMA is (token slot i, coordinate parity
+//        e) for 3-bit values: an A register is one code pair of one token,
+//        one table lookup.  For 2- and 4-bit values it is (coordinate half
+//        e, token i): an A register pairs two tokens' codes at one
+//        coordinate, interleaved in registers and looked up once.
 // Thread (r = lane/4, t = lane%4) owns head 4*nt + t of n-tile nt and tokens r
 // and r+8 of a tile for the scores; for the values it reads the codes of
-// coordinates 16r..16r+15 and accumulates heads 4nt + 2(t&1), 4nt + 2(t&1) + 1
-// at coordinates 16r + 4mt + 2(t>>1) + {0, 1}, mt = 0..3.
+// coordinates 16r..16r+15 of tokens 2t, 2t+1, 2t+8, 2t+9 and accumulates
+// heads 4nt + 2(t&1) and 4nt + 2(t&1) + 1.
 #pragma once
 
 #include "tq_internal.cuh"
@@ -422,6 +424,18 @@ struct TileCursor {
 #ifndef TQ_TILE_PIPELINE
 #define TQ_TILE_PIPELINE -1
 #endif
+// Value MMA layouts.  Parity pairs (K index = token slot x coordinate
+// parity: an A register is one code pair of one token) for 3-bit values,
+// where they replace a gather of two tokens' 3-bit fields; coordinate halves
+// (K index = coordinate half x token: an A register pairs two tokens'
+// codes, interleaved in registers) for 2- and 4-bit values.  Measured at the
+// Llama-3-8B decode shape, 32K context: K3.5/V3 160.3 us with parity pairs
+// against 170.0; K4/V4 137.4 either way; long context K2+QJL/V2 176.3
+// against 170.0.
+template <int VB>
+__host__ __device__ constexpr bool val_parity_pairs() {
+  return VB == 3;
+}
 template <int KB>
 __host__ __device__ constexpr int tile_pipeline() {
   return TQ_TILE_PIPELINE >= 0 ? TQ_TILE_PIPELINE : (kb_mixed(KB) ? 0 : 2);
@@ -585,6 +599,9 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   const uint32_t laneK = (tbase + kKeyTableOff) | ((uint32_t)lane * 8u);
   const uint32_t laneKL = (tbase + key_lo_table_off<KB>()) | ((uint32_t)lane * 8u);  // mixed keys: low-channel table
   const uint32_t laneV = (tbase + kValTableOff) | ((uint32_t)lane * (VB == 2 ? 8u : 4u));
+  // value-weight operands: the low (tokens 2t, 2t+1) or high (2t+8, 2t+9)
+  // half of a weight pair into the half of this lane's parity column r/4
+  const uint32_t selW_lo = r < 4 ? 0x4410u : 0x1044u, selW_hi = r < 4 ? 0x4432u : 0x3244u;
 #if TQ_TMA_STAGING
   static_assert(!kb_mixed(KB), "the staging ring carries uniform key widths only");
   using SL = Stage<KB, VB, QJL>;
@@ -817,80 +834,137 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
           }
         }
       }
-      // wb[nt][s]: B operand of the value MMAs of token group s
-      uint32_t wb[NT][2][2];
+      if constexpr (val_parity_pairs<VB>()) {
+        // wb[nt][s][0 / 1]: B operand of token group s for the token slots t
+        // (token 2t + 8s) and t + 4 (token 2t + 1 + 8s); column r = (coordinate
+        // parity r/4, head 4nt + r%4): the token's weight in the half of its
+        // parity, 0 in the other half.  The lanes (2t, r%4) and (2t+1, r%4)
+        // own the weights.
+        uint32_t wb[NT][2][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; nt++) {
-        const float p0 = fast_exp2(lg0[nt] - mu[nt]), p1 = fast_exp2(lg1[nt] - mu[nt]);
-        lsum[nt] += p0 + p1;
-        const float w0 = p0 * vn0 * inv_nu, w1 = p1 * vn1 * inv_nu;
-        const uint32_t Wh = pack_half2(w0, w1);  // (token r, token r+8) of head 4nt + t
-        // column r = (coordinate half r/4, head 4nt + r%4): the weights of
-        // tokens 8s + 2t, 8s + 2t + 1 in the rows of half r/4, zeros in the
-        // other half's rows; the lanes (2t, r%4), (2t+1, r%4) own them
-        const int src0 = 4 * (2 * t) + (r & 3), src1 = src0 + 4;
-        const uint32_t h0 = __shfl_sync(0xffffffffu, Wh, src0);
-        const uint32_t h1 = __shfl_sync(0xffffffffu, Wh, src1);
-        const uint32_t e0 = __byte_perm(h0, h1, 0x5410), e1 = __byte_perm(h0, h1, 0x7632);
-        const bool half0 = r < 4;
-        wb[nt][0][0] = half0 ? e0 : 0u;
-        wb[nt][0][1] = half0 ? 0u : e0;
-        wb[nt][1][0] = half0 ? e1 : 0u;
-        wb[nt][1][1] = half0 ? 0u : e1;
-      }
-      // ---- values: interleave the codes of the token pairs (2t, 2t+1) and
-      // (2t+8, 2t+9) at each coordinate; one lookup gives an A register.
-      // Table offset = pair code << 8 | lane slot.
-      uint32_t ev[2][2][2];  // [token pair][even/odd coordinate][word]
+        for (int nt = 0; nt < NT; nt++) {
+          const float p0 = fast_exp2(lg0[nt] - mu[nt]), p1 = fast_exp2(lg1[nt] - mu[nt]);
+          lsum[nt] += p0 + p1;
+          const float w0 = p0 * vn0 * inv_nu, w1 = p1 * vn1 * inv_nu;
+          const uint32_t Wh = pack_half2(w0, w1);  // (token r, token r+8) of head 4nt + t
+          const int src0 = 4 * (2 * t) + (r & 3), src1 = src0 + 4;
+          const uint32_t h0 = __shfl_sync(0xffffffffu, Wh, src0);  // tokens 2t, 2t+8
+          const uint32_t h1 = __shfl_sync(0xffffffffu, Wh, src1);  // tokens 2t+1, 2t+9
+          wb[nt][0][0] = __byte_perm(h0, 0u, selW_lo);
+          wb[nt][0][1] = __byte_perm(h1, 0u, selW_lo);
+          wb[nt][1][0] = __byte_perm(h0, 0u, selW_hi);
+          wb[nt][1][1] = __byte_perm(h1, 0u, selW_hi);
+        }
+        // ---- values.  The K index of an MMA is (token slot i, coordinate
+        // parity e): an A register holds two consecutive coordinates of one
+        // token, i.e. one code pair of the token's own stream, looked up once.
+        // Token group s, m-tile mt: row r is the coordinate pair 2mt of this
+        // lane's chunk (coordinates 16r + 4mt, +1), row r+8 the pair 2mt + 1
+        // (16r + 4mt + 2, +3); slots t, t+4 are tokens 2t + 8s, 2t + 1 + 8s.
 #pragma unroll
-      for (int tp = 0; tp < 2; tp++) {
+        for (int s = 0; s < 2; s++) {
 #pragma unroll
-        for (int wi = 0; wi < 2; wi++) {
-          const uint32_t wa = wi ? V.vhi[2 * tp] : V.vlo[2 * tp];
-          const uint32_t wz = wi ? V.vhi[2 * tp + 1] : V.vlo[2 * tp + 1];
-          if constexpr (VB == 4) {
-            ev[tp][0][wi] = (wa & 0x0F0F0F0Fu) | ((wz << 4) & 0xF0F0F0F0u);  // byte k: coordinate 2k
-            ev[tp][1][wi] = ((wa >> 4) & 0x0F0F0F0Fu) | (wz & 0xF0F0F0F0u);  // byte k: coordinate 2k+1
-          } else if constexpr (VB == 2) {
-            ev[tp][0][wi] = (wa & 0x33333333u) | ((wz << 2) & 0xCCCCCCCCu);  // nibble k: coordinate 2k
-            ev[tp][1][wi] = ((wa >> 2) & 0x33333333u) | (wz & 0xCCCCCCCCu);  // nibble k: coordinate 2k+1
-          } else {
-            ev[tp][0][wi] = 0u;
-            ev[tp][1][wi] = 0u;
+          for (int mt = 0; mt < 4; mt++) {
+            uint32_t av[4];  // (token 2t+8s | 2t+1+8s) x (pair 2mt | 2mt+1)
+            if constexpr (VB == 2) {
+              // byte mt of a token's 2-bit word: pairs 2mt and 2mt + 1 in one 8-byte entry
+              const uint2 pa = lut64(__byte_perm(V.vlo[2 * s], laneV, 0x7604 | (mt << 4)));
+              const uint2 pb = lut64(__byte_perm(V.vlo[2 * s + 1], laneV, 0x7604 | (mt << 4)));
+              av[0] = pa.x; av[1] = pa.y; av[2] = pb.x; av[3] = pb.y;
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; q++) {
+                const int tok = 2 * s + (q >> 1), pair = 2 * mt + (q & 1);
+                uint32_t addr;
+                if constexpr (VB == 4) {  // byte `pair` of the token's 8-byte chunk
+                  addr = __byte_perm(pair < 4 ? V.vlo[tok] : V.vhi[tok], laneV, 0x7604 | ((pair & 3) << 4));
+                } else {  // 3-bit: the 6 bits of the pair in the token's 48-bit chunk
+                  addr = field_at<8>(V.vlo[tok], V.vhi[tok], 6 * pair, 6, laneV);
+                }
+                av[q] = lut32(addr);
+              }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++)
+              mma_16816(acc[mt][nt], av[0], av[1], av[2], av[3], wb[nt][s][0], wb[nt][s][1]);
           }
         }
-      }
-      // token group s (tokens 8s + 2t, 8s + 2t + 1 in this lane's A
-      // registers), m-tile mt: A rows r / r+8 of half h are coordinates
-      // 16r + 4mt + 2h / 16r + 4mt + 2h + 1, so av[q] is coordinate 16r + 4mt + q
+      } else {
+        // wb[nt][s]: B operand of the value MMAs of token group s
+        uint32_t wb[NT][2][2];
 #pragma unroll
-      for (int s = 0; s < 2; s++) {
+        for (int nt = 0; nt < NT; nt++) {
+          const float p0 = fast_exp2(lg0[nt] - mu[nt]), p1 = fast_exp2(lg1[nt] - mu[nt]);
+          lsum[nt] += p0 + p1;
+          const float w0 = p0 * vn0 * inv_nu, w1 = p1 * vn1 * inv_nu;
+          const uint32_t Wh = pack_half2(w0, w1);  // (token r, token r+8) of head 4nt + t
+          // column r = (coordinate half r/4, head 4nt + r%4): the weights of
+          // tokens 8s + 2t, 8s + 2t + 1 in the rows of half r/4, zeros in the
+          // other half's rows; the lanes (2t, r%4), (2t+1, r%4) own them
+          const int src0 = 4 * (2 * t) + (r & 3), src1 = src0 + 4;
+          const uint32_t h0 = __shfl_sync(0xffffffffu, Wh, src0);
+          const uint32_t h1 = __shfl_sync(0xffffffffu, Wh, src1);
+          const uint32_t e0 = __byte_perm(h0, h1, 0x5410), e1 = __byte_perm(h0, h1, 0x7632);
+          const bool half0 = r < 4;
+          wb[nt][0][0] = half0 ? e0 : 0u;
+          wb[nt][0][1] = half0 ? 0u : e0;
+          wb[nt][1][0] = half0 ? e1 : 0u;
+          wb[nt][1][1] = half0 ? 0u : e1;
+        }
+        // ---- values: interleave the codes of the token pairs (2t, 2t+1) and
+        // (2t+8, 2t+9) at each coordinate; one lookup gives an A register.
+        // Table offset = pair code << 8 | lane slot.
+        uint32_t ev[2][2][2];  // [token pair][even/odd coordinate][word]
 #pragma unroll
-        for (int mt = 0; mt < 4; mt++) {
-          uint32_t av[4];
-          if constexpr (VB == 2) {
-            // byte mt of ev[s][eo]: coordinates 4mt + eo and 4mt + 2 + eo
-            const uint2 pe = lut64(__byte_perm(ev[s][0][0], laneV, 0x7604 | (mt << 4)));
-            const uint2 po = lut64(__byte_perm(ev[s][1][0], laneV, 0x7604 | (mt << 4)));
-            av[0] = pe.x; av[1] = po.x; av[2] = pe.y; av[3] = po.y;
-          } else {
+        for (int tp = 0; tp < 2; tp++) {
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-              uint32_t addr;
-              if constexpr (VB == 4) {
-                // byte k of ev[s][eo][wi] is coordinate 8wi + 2k + eo
-                addr = __byte_perm(ev[s][q & 1][mt >> 1], laneV, 0x7604 | ((2 * (mt & 1) + (q >> 1)) << 4));
-              } else {  // 3-bit: gather the two codes of coordinate 16r + 4mt + q
-                const int p3 = 3 * (4 * mt + q);
-                addr = field_at<8>(V.vlo[2 * s], V.vhi[2 * s], p3, 3, laneV) |
-                       field_at<11>(V.vlo[2 * s + 1], V.vhi[2 * s + 1], p3, 3, 0u);
-              }
-              av[q] = lut32(addr);
+          for (int wi = 0; wi < 2; wi++) {
+            const uint32_t wa = wi ? V.vhi[2 * tp] : V.vlo[2 * tp];
+            const uint32_t wz = wi ? V.vhi[2 * tp + 1] : V.vlo[2 * tp + 1];
+            if constexpr (VB == 4) {
+              ev[tp][0][wi] = (wa & 0x0F0F0F0Fu) | ((wz << 4) & 0xF0F0F0F0u);  // byte k: coordinate 2k
+              ev[tp][1][wi] = ((wa >> 4) & 0x0F0F0F0Fu) | (wz & 0xF0F0F0F0u);  // byte k: coordinate 2k+1
+            } else if constexpr (VB == 2) {
+              ev[tp][0][wi] = (wa & 0x33333333u) | ((wz << 2) & 0xCCCCCCCCu);  // nibble k: coordinate 2k
+              ev[tp][1][wi] = ((wa >> 2) & 0x33333333u) | (wz & 0xCCCCCCCCu);  // nibble k: coordinate 2k+1
+            } else {
+              ev[tp][0][wi] = 0u;
+              ev[tp][1][wi] = 0u;
             }
           }
+        }
+        // token group s (tokens 8s + 2t, 8s + 2t + 1 in this lane's A
+        // registers), m-tile mt: A rows r / r+8 of half h are coordinates
+        // 16r + 4mt + 2h / 16r + 4mt + 2h + 1, so av[q] is coordinate 16r + 4mt + q
 #pragma unroll
-          for (int nt = 0; nt < NT; nt++)
-            mma_16816(acc[mt][nt], av[0], av[1], av[2], av[3], wb[nt][s][0], wb[nt][s][1]);
+        for (int s = 0; s < 2; s++) {
+#pragma unroll
+          for (int mt = 0; mt < 4; mt++) {
+            uint32_t av[4];
+            if constexpr (VB == 2) {
+              // byte mt of ev[s][eo]: coordinates 4mt + eo and 4mt + 2 + eo
+              const uint2 pe = lut64(__byte_perm(ev[s][0][0], laneV, 0x7604 | (mt << 4)));
+              const uint2 po = lut64(__byte_perm(ev[s][1][0], laneV, 0x7604 | (mt << 4)));
+              av[0] = pe.x; av[1] = po.x; av[2] = pe.y; av[3] = po.y;
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; q++) {
+                uint32_t addr;
+                if constexpr (VB == 4) {
+                  // byte k of ev[s][eo][wi] is coordinate 8wi + 2k + eo
+                  addr = __byte_perm(ev[s][q & 1][mt >> 1], laneV, 0x7604 | ((2 * (mt & 1) + (q >> 1)) << 4));
+                } else {  // 3-bit: gather the two codes of coordinate 16r + 4mt + q
+                  const int p3 = 3 * (4 * mt + q);
+                  addr = field_at<8>(V.vlo[2 * s], V.vhi[2 * s], p3, 3, laneV) |
+                         field_at<11>(V.vlo[2 * s + 1], V.vhi[2 * s + 1], p3, 3, 0u);
+                }
+                av[q] = lut32(addr);
+              }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++)
+              mma_16816(acc[mt][nt], av[0], av[1], av[2], av[3], wb[nt][s][0], wb[nt][s][1]);
+          }
         }
       }
     };
@@ -1030,16 +1104,25 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         a.seg_ml[(slot * G + g) * 2] = mu[nt];
         a.seg_ml[(slot * G + g) * 2 + 1] = ltot;
       }
-      // this lane's accumulator: heads gA, gA + 1 at coordinates
-      // 16r + 4mt + 2(t>>1) + {0, 1}
+      // this lane's accumulator: heads gA (i = 0, 2) and gA + 1 (i = 1, 3);
+      // parity pairs: coordinates 16r + 4mt + (t>>1) (i = 0, 1) and
+      // 16r + 4mt + 2 + (t>>1) (i = 2, 3); coordinate halves: 16r + 4mt +
+      // 2(t>>1) + {0, 1}
       const int gA = 4 * nt + 2 * (t & 1);
 #pragma unroll
       for (int hh = 0; hh < 2; hh++) {
         if (gA + hh < G) {
-          float *dst = a.seg_acc + (slot * G + gA + hh) * kD + 16 * r + 2 * (t >> 1);
+          float *row = a.seg_acc + (slot * G + gA + hh) * kD + 16 * r;
 #pragma unroll
-          for (int mt = 0; mt < 4; mt++)
-            *reinterpret_cast<float2 *>(dst + 4 * mt) = make_float2(acc[mt][nt][hh] * vscale, acc[mt][nt][hh + 2] * vscale);
+          for (int mt = 0; mt < 4; mt++) {
+            if constexpr (val_parity_pairs<VB>()) {
+              row[4 * mt + (t >> 1)] = acc[mt][nt][hh] * vscale;
+              row[4 * mt + 2 + (t >> 1)] = acc[mt][nt][hh + 2] * vscale;
+            } else {
+              *reinterpret_cast<float2 *>(row + 4 * mt + 2 * (t >> 1)) =
+                  make_float2(acc[mt][nt][hh] * vscale, acc[mt][nt][hh + 2] * vscale);
+            }
+          }
         }
       }
     }
