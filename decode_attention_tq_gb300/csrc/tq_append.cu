@@ -70,6 +70,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const RollArgs r
   __half *s_new = reinterpret_cast<__half *>(smem + append_cells_bytes(KQJL));
   __half *s_old = s_new + 2 * nsh * kD;
 
+  // A kernel launched after this one as a programmatic dependent (the
+  // attention's prep kernel) may start now: it waits for this grid to
+  // complete before it reads anything.
+  griddep_launch_dependents();
+
   // 1. counters, new tokens, tables
   if (tid < ns) {
     const int b = s0 + tid;

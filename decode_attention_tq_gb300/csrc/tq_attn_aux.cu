@@ -220,6 +220,9 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
 __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool qjl, int row_blocks) {
   __shared__ __align__(16) float s_q[8 * kQRow];
   __shared__ float s_p[8][kWinChunk];
+  // Launched as a programmatic dependent of whatever kernel precedes it in
+  // the stream: nothing is read before that kernel has completed.
+  griddep_wait();
   griddep_launch_dependents();  // the main kernel may start building its tables
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (blockIdx.x >= row_blocks) {  // window chunk blocks
@@ -516,7 +519,9 @@ cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
   const int64_t rows = (int64_t)a.B * a.Hq;
   const int64_t row_blocks = (rows + 3) / 4;
   const int64_t win_blocks = a.window > 0 ? (int64_t)a.B * a.H * ((a.window + kWinChunk - 1) / kWinChunk) : 0;
-  attn_prep_kernel<<<(unsigned)(row_blocks + win_blocks), 128, 0, st>>>(a, qjl, (int)row_blocks);
+  const cudaError_t e = launch_maybe_dependent(attn_prep_kernel, dim3((unsigned)(row_blocks + win_blocks)), dim3(128), 0,
+                                               st, a.pdl, a, qjl, (int)row_blocks);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
