@@ -514,8 +514,9 @@ static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_hea
   a.win_acc = reinterpret_cast<float *>(ws + p.off_winacc);
   a.nw_launch = p.nw_launch;
   a.min_tiles = kMinTilesPerWarp;
-  // main and merge start as programmatic dependents (their prologues overlap
-  // the previous kernel), except when the caller times the main kernel
+  // prep, main and merge start as programmatic dependents (their launches and
+  // prologues overlap the previous kernel; prep waits before it reads
+  // anything), except when the caller times the main kernel
   a.pdl = ev_begin == nullptr && ev_end == nullptr;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
