@@ -34,7 +34,7 @@
  *       the oracle instead materializes every token and takes the exact
  *       softmax, which is algebraically the same computation.
  *
- * Readings of points the pages leave open (each one is listed in the design doc):
+ * Readings of points the pages leave open:
  *   - Codebook: Lloyd-Max for N(0,1), fp64 fixed-point iteration from a
  *     symmetric start, symmetrized, then rounded to fp32.  Midpoints are the
  *     fp64 averages of neighbouring fp64 centroids, rounded to fp32.
