@@ -106,8 +106,8 @@ def _setup(fmt, B, Hq, comp_lens, W, win_lens, seed=0, q_zero=False):
     K = ti.kv_history(B, max(T, 1), H, d, layer=seed, kind=0).numpy()
     V = ti.kv_history(B, max(T, 1), H, d, layer=seed, kind=1).numpy()
     ks, vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
-    kc, kt = oracle.make_codebook(fmt.k_bits)
-    vc, vt = oracle.make_codebook(fmt.v_bits)
+    kc, kt = oracle.kind_codebook(fmt, 0)  # mixed keys: both widths' codebooks
+    vc, vt = oracle.kind_codebook(fmt, 1)
     S = ti.gaussian_matrix(ti.SEED_QJL, fmt.qjl_m, d) if fmt.k_qjl else None
     kwin = np.zeros((B, H, max(W, 1), d), np.float16)
     vwin = np.zeros((B, H, max(W, 1), d), np.float16)
@@ -171,6 +171,24 @@ def _unpack(buf, nbits, count):
     return (bits * (1 << np.arange(nbits))).sum(1)
 
 
+def _key_centroids(fmt, raw, d):
+    """Centroid of each channel of one key, from its code stream: uniform
+    keys at k_bits per channel; mixed keys with the channels j mod 16 < 8 at
+    k_bits + 1 bits first, then the others at k_bits (LSB-first)."""
+    if not fmt.k_mixed:
+        kc, _ = oracle.make_codebook(fmt.k_bits)
+        return kc.astype(np.float64)[_unpack(raw, fmt.k_bits, d)]
+    hi = (np.arange(d) % 16) < 8
+    bh, bl, nh = fmt.k_bits + 1, fmt.k_bits, int(hi.sum())
+    bits = np.unpackbits(raw, bitorder="little")
+    ih = (bits[: nh * bh].reshape(nh, bh) * (1 << np.arange(bh))).sum(1)
+    il = (bits[nh * bh: nh * bh + (d - nh) * bl].reshape(d - nh, bl) * (1 << np.arange(bl))).sum(1)
+    out = np.empty(d)
+    out[hi] = oracle.make_codebook(bh)[0].astype(np.float64)[ih]
+    out[~hi] = oracle.make_codebook(bl)[0].astype(np.float64)[il]
+    return out
+
+
 def _rotated_domain_attention(fmt, s, b, qh):
     """The README's fused form, from raw bytes: rotate q once, score codes via
     centroids (+ QJL term), weight values in the rotated domain, rotate back."""
@@ -191,12 +209,14 @@ def _rotated_domain_attention(fmt, s, b, qh):
         off = i % P
         slab = s["pool"][pg * L["page_bytes"] + h * L["slab_bytes"]:][: L["slab_bytes"]]
         nk = slab[L["k_norm"] + 4 * off:][:4].view(np.float32)[0]
-        idx = _unpack(slab[L["k_codes"] + off * L["k_code_bytes"]:][: L["k_code_bytes"]], fmt.k_bits, d)
-        score = q_rot @ s["kc"].astype(np.float64)[idx] / math.sqrt(d)
+        cent = _key_centroids(fmt, slab[L["k_codes"] + off * L["k_code_bytes"]:][: L["k_code_bytes"]], d)
+        score = q_rot @ cent / math.sqrt(d)
         if fmt.k_qjl:
             gam = slab[L["k_gamma"] + 4 * off:][:4].view(np.float32)[0]
             z = _unpack(slab[L["k_signs"] + off * L["k_sign_bytes"]:][: L["k_sign_bytes"]], 1, m)
-            score += math.sqrt(math.pi / 2) / m * float(gam) * (q_s @ (2.0 * z - 1.0))
+            # the format's coefficient: qjl_scale when given, else sqrt(pi/2) / m
+            coef = fmt.qjl_scale if fmt.qjl_scale > 0 else math.sqrt(math.pi / 2) / m
+            score += coef * float(gam) * (q_s @ (2.0 * z - 1.0))
         logits.append(float(nk) * score / math.sqrt(d))
         nv = slab[L["v_norm"] + 4 * off:][:4].view(np.float32)[0]
         vidx = _unpack(value_code_bytes(slab[L["v_codes"]:][: P * L["v_code_bytes"]], off, d, fmt.v_bits), fmt.v_bits, d)
@@ -217,6 +237,9 @@ def _rotated_domain_attention(fmt, s, b, qh):
         (ti.Format(128, 4, 4, 0, 128, 64, 2), 2, 8, [130, 64], 0, [0, 0]),
         (ti.Format(128, 3, 4, 1, 128, 64, 1), 1, 4, [200], 16, [16]),
         (ti.Format(128, 2, 2, 1, 128, 32, 2), 2, 4, [33, 95], 8, [8, 3]),
+        # mixed-rate keys (3.5 and 2.5 bits), one with a given QJL scale
+        (ti.Format(128, 3, 4, 0, 128, 64, 2, k_mixed=1), 2, 8, [150, 40], 8, [8, 2]),
+        (ti.Format(128, 2, 3, 1, 128, 32, 1, k_mixed=1, qjl_scale=0.05), 1, 4, [90], 0, [0]),
     ],
 )
 def test_materialized_equals_rotated_domain(fmt, B, Hq, comp, W, wl):
