@@ -240,6 +240,8 @@ def _rotated_domain_attention(fmt, s, b, qh):
         # mixed-rate keys (3.5 and 2.5 bits), one with a given QJL scale
         (ti.Format(128, 3, 4, 0, 128, 64, 2, k_mixed=1), 2, 8, [150, 40], 8, [8, 2]),
         (ti.Format(128, 2, 3, 1, 128, 32, 1, k_mixed=1, qjl_scale=0.05), 1, 4, [90], 0, [0]),
+        # norm-corrected keys and values (the stored norms are n / ||y_hat||)
+        (ti.Format(128, 4, 3, 0, 128, 64, 2, norm_correct=1), 1, 4, [77], 4, [4]),
     ],
 )
 def test_materialized_equals_rotated_domain(fmt, B, Hq, comp, W, wl):
