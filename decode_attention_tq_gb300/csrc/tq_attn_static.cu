@@ -3,37 +3,29 @@
 // workspace, for callers that have no allocator to draw a workspace from
 // (a plug-in handed bare tensor pointers by its host framework, or a loop
 // that must not enter any allocator).  Nothing here allocates: the array is
-// part of the loaded module, its address is looked up once per device, and
-// the call then runs the ordinary tq_decode_attn on it.
-#include <mutex>
-
+// part of the loaded module, its address is looked up on every call, and the
+// call then runs the ordinary tq_decode_attn on it.
 #include "tq.h"
 #include "tq_internal.cuh"
 
 namespace {
 
 constexpr size_t kScratchBytes = TQ_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // The scratch: every call on a device uses this one buffer (calls must not
 // overlap in time).  No word of it needs to start at zero.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-std::mutex g_setup_mu;
-void *g_scratch_ptr[kMaxDevices];  // device address of g_scratch, per device; null until set up
-
-// Set-up, once per device, with that device current.
+// Device address of g_scratch in the current context.  Looked up on every
+// call rather than cached per device: a context that is torn down and created
+// again (cudaDeviceReset) loads the module anew, possibly at another address.
+// Once the module is loaded in the context this is a host-side table lookup
+// that allocates nothing; the first call in a context may load the module,
+// which is why that first call must come before any stream capture.
 tq_status scratch_address(void **ptr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return TQ_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *ptr = g_scratch_ptr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
+  *ptr = p;
   return TQ_OK;
 }
 
