@@ -16,15 +16,13 @@ import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-# the in-tree build; TQ_LIBRARY may name another build of the same sources
-LIB_PATH = os.environ.get("TQ_LIBRARY") or os.path.join(_HERE, "libtq.so")
+LIB_PATH = os.path.join(_HERE, "libtq.so")  # the in-tree build
 
 TQ_KIND_K = 0
 TQ_KIND_V = 1
 TQ_DEVERR_SLOT_RANGE = 0x1
 TQ_DEVERR_PAGE_RANGE = 0x2
 TQ_DEVERR_LENGTH = 0x4
-TQ_DEVERR_TIMEOUT = 0x8
 
 STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_CUDA", 4: "TQ_ERR_DEVICE_FAULT",
           5: "TQ_ERR_TIMEOUT", 6: "TQ_ERR_WORKSPACE", 7: "TQ_ERR_SCRATCH_LIMIT"}
@@ -102,6 +100,19 @@ def _dev_ptr(t, dtype=None, name="tensor", allow_none=False):
     return C.c_void_p(t.data_ptr())
 
 
+def _device(*tensors) -> torch.device:
+    """The one CUDA device all given tensors live on (None entries skipped).
+    The library launches on the current device, so every call runs with this
+    device made current."""
+    devs = {t.device for t in tensors if isinstance(t, torch.Tensor)}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one CUDA device, got {sorted(str(d) for d in devs)}")
+    dev = devs.pop()
+    if dev.type != "cuda":
+        raise TypeError(f"tensors must be CUDA tensors, got {dev}")
+    return dev
+
+
 def _stream(stream):
     if stream is None:
         return C.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -154,12 +165,13 @@ def kind_codebook(fmt, kind: int, device="cuda") -> torch.Tensor:
 # ----------------------------------------------------------------- device --
 def tq_encode(fmt, kind: int, x, slot_mapping, page_pool, num_pages: int, signs, codebook, S=None, err_word=None, stream=None):
     F = _fmt(fmt)
-    rc = load_library().tq_encode(
-        C.byref(F), int(kind), _dev_ptr(x, torch.float16, "x"), int(x.shape[0]), _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
-        _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(signs, torch.uint8, "signs"),
-        _dev_ptr(codebook, torch.float32, "codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
-        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
-    )
+    with torch.cuda.device(_device(x, slot_mapping, page_pool, signs, codebook, S, err_word)):
+        rc = load_library().tq_encode(
+            C.byref(F), int(kind), _dev_ptr(x, torch.float16, "x"), int(x.shape[0]), _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
+            _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(signs, torch.uint8, "signs"),
+            _dev_ptr(codebook, torch.float32, "codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
+            _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+        )
     _check(rc, "tq_encode")
 
 
@@ -168,14 +180,15 @@ def tq_encode_kv(fmt, k, v, slot_mapping, page_pool, num_pages: int, k_signs, v_
     F = _fmt(fmt)
     if tuple(k.shape) != tuple(v.shape):
         raise ValueError("tq_encode_kv: k and v must have the same shape")
-    rc = load_library().tq_encode_kv(
-        C.byref(F), _dev_ptr(k, torch.float16, "k"), _dev_ptr(v, torch.float16, "v"), int(k.shape[0]),
-        _dev_ptr(slot_mapping, torch.int32, "slot_mapping"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
-        _dev_ptr(k_signs, torch.uint8, "k_signs"), _dev_ptr(v_signs, torch.uint8, "v_signs"),
-        _dev_ptr(k_codebook, torch.float32, "k_codebook"), _dev_ptr(v_codebook, torch.float32, "v_codebook"),
-        _dev_ptr(S, torch.float32, "S", allow_none=True), _dev_ptr(err_word, torch.int32, "err_word", allow_none=True),
-        _stream(stream),
-    )
+    with torch.cuda.device(_device(k, v, slot_mapping, page_pool, k_signs, v_signs, k_codebook, v_codebook, S, err_word)):
+        rc = load_library().tq_encode_kv(
+            C.byref(F), _dev_ptr(k, torch.float16, "k"), _dev_ptr(v, torch.float16, "v"), int(k.shape[0]),
+            _dev_ptr(slot_mapping, torch.int32, "slot_mapping"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
+            _dev_ptr(k_signs, torch.uint8, "k_signs"), _dev_ptr(v_signs, torch.uint8, "v_signs"),
+            _dev_ptr(k_codebook, torch.float32, "k_codebook"), _dev_ptr(v_codebook, torch.float32, "v_codebook"),
+            _dev_ptr(S, torch.float32, "S", allow_none=True), _dev_ptr(err_word, torch.int32, "err_word", allow_none=True),
+            _stream(stream),
+        )
     _check(rc, "tq_encode_kv")
 
 
@@ -195,17 +208,19 @@ def tq_append_window(fmt, k_new, v_new, k_win, v_win, win_lens, win_head, comp_l
     W = 0 if k_win is None else int(k_win.shape[2])
     if workspace is None:
         workspace = torch.empty(tq_append_window_workspace_size(F, B), dtype=torch.uint8, device=k_new.device)
-    rc = load_library().tq_append_window(
-        C.byref(F), B, _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
-        _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True), W,
-        _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), _dev_ptr(win_head, torch.int32, "win_head", allow_none=True),
-        _dev_ptr(comp_lens, torch.int32, "comp_lens"), _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
-        _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(k_signs, torch.uint8, "k_signs"),
-        _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
-        _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
-        _dev_ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()),
-        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
-    )
+    with torch.cuda.device(_device(k_new, v_new, k_win, v_win, win_lens, win_head, comp_lens, block_tables, page_pool, k_signs,
+                                   v_signs, k_codebook, v_codebook, S, workspace, err_word)):
+        rc = load_library().tq_append_window(
+            C.byref(F), B, _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
+            _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True), W,
+            _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), _dev_ptr(win_head, torch.int32, "win_head", allow_none=True),
+            _dev_ptr(comp_lens, torch.int32, "comp_lens"), _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
+            _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(k_signs, torch.uint8, "k_signs"),
+            _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
+            _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
+            _dev_ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()),
+            _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+        )
     _check(rc, "tq_append_window")
 
 
@@ -214,12 +229,13 @@ def tq_decode(fmt, kind: int, page_pool, num_pages: int, slot_mapping, signs, co
     n = int(slot_mapping.shape[0])
     if out is None:
         out = torch.empty((n, F.num_kv_heads, F.head_dim), dtype=torch.float32, device=slot_mapping.device)
-    rc = load_library().tq_decode(
-        C.byref(F), int(kind), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
-        n, _dev_ptr(signs, torch.uint8, "signs"), _dev_ptr(codebook, torch.float32, "codebook"),
-        _dev_ptr(S, torch.float32, "S", allow_none=True), _dev_ptr(out, torch.float32, "out"),
-        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
-    )
+    with torch.cuda.device(_device(page_pool, slot_mapping, signs, codebook, S, out, err_word)):
+        rc = load_library().tq_decode(
+            C.byref(F), int(kind), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
+            n, _dev_ptr(signs, torch.uint8, "signs"), _dev_ptr(codebook, torch.float32, "codebook"),
+            _dev_ptr(S, torch.float32, "S", allow_none=True), _dev_ptr(out, torch.float32, "out"),
+            _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+        )
     _check(rc, "tq_decode")
     return out
 
@@ -251,15 +267,18 @@ def tq_decode_attn_static(fmt, q, page_pool, num_pages: int, block_tables, comp_
     F = _fmt(fmt)
     B, Hq, _ = q.shape
     window = 0 if k_win is None else int(k_win.shape[2])
-    rc = load_library().tq_decode_attn_static(
-        C.byref(F), int(B), int(Hq), _dev_ptr(q, torch.float16, "q"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
-        _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]), _dev_ptr(comp_lens, torch.int32, "comp_lens"),
-        _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True),
-        _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), window, _dev_ptr(k_signs, torch.uint8, "k_signs"),
-        _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
-        _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
-        _dev_ptr(out, torch.float32, "out"), _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
-    )
+    dev = _device(q, page_pool, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs, k_codebook, v_codebook, S, out,
+                  err_word)
+    with torch.cuda.device(dev):  # the static scratch used is the current device's
+        rc = load_library().tq_decode_attn_static(
+            C.byref(F), int(B), int(Hq), _dev_ptr(q, torch.float16, "q"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
+            _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]), _dev_ptr(comp_lens, torch.int32, "comp_lens"),
+            _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True),
+            _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), window, _dev_ptr(k_signs, torch.uint8, "k_signs"),
+            _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
+            _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
+            _dev_ptr(out, torch.float32, "out"), _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+        )
     _check(rc, "tq_decode_attn_static")
     return out
 
@@ -278,15 +297,17 @@ def _decode_attn(fmt, q, page_pool, num_pages, block_tables, comp_lens, k_win, v
     lib = load_library()
     fn = lib.tq_decode_attn if events is None else lib.tq_decode_attn_timed
     extra = () if events is None else (_event(events[0]), _event(events[1]))
-    rc = fn(
-        C.byref(F), int(B), int(Hq), _dev_ptr(q, torch.float16, "q"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
-        _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]), _dev_ptr(comp_lens, torch.int32, "comp_lens"),
-        _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True),
-        _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), window, _dev_ptr(k_signs, torch.uint8, "k_signs"),
-        _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
-        _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
-        _dev_ptr(out, torch.float32, "out"), _dev_ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()),
-        _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), *extra, _stream(stream),
-    )
+    with torch.cuda.device(_device(q, page_pool, block_tables, comp_lens, k_win, v_win, win_lens, k_signs, v_signs, k_codebook,
+                                   v_codebook, S, out, workspace, err_word)):
+        rc = fn(
+            C.byref(F), int(B), int(Hq), _dev_ptr(q, torch.float16, "q"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
+            _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]), _dev_ptr(comp_lens, torch.int32, "comp_lens"),
+            _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True),
+            _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), window, _dev_ptr(k_signs, torch.uint8, "k_signs"),
+            _dev_ptr(v_signs, torch.uint8, "v_signs"), _dev_ptr(k_codebook, torch.float32, "k_codebook"),
+            _dev_ptr(v_codebook, torch.float32, "v_codebook"), _dev_ptr(S, torch.float32, "S", allow_none=True),
+            _dev_ptr(out, torch.float32, "out"), _dev_ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()),
+            _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), *extra, _stream(stream),
+        )
     _check(rc, "tq_decode_attn" if events is None else "tq_decode_attn_timed")
     return out
