@@ -17,7 +17,7 @@ import torch
 
 import oracle
 import tq_inputs as ti
-from tq_testlib import REL_ATTN, compare_encoded, rel_err
+from tq_testlib import REL_ATTN, check_exemption_reach, compare_encoded, merge_stats, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -80,14 +80,16 @@ def test_decode_workload_full_size(wl):
         # sampled tokens of this layer's cache, re-encoded by the oracle
         rng = np.random.default_rng(5 + li)
         comp, P = b.comp, f.page_size
+        totals = {0: {}, 1: {}}
         slots_all = b.bt[:, torch.arange(comp, device="cuda") // P] * P + (torch.arange(comp, device="cuda") % P)[None, :]
         for kind in (0, 1):
             x = ti.kv_history(B, wl.context, H, d, li, kind, device="cuda")[:, :comp]  # [B, comp, H, d]
             for bb in sorted({0, B - 1}):
                 pick = _sample_positions(comp, P, rng)
-                _check_encode_samples(f, kind, x[bb], slots_all[bb].to(torch.int32), pool, b.num_pages, pick,
-                                      f"{wl.name} layer {li} b{bb}")
+                merge_stats(totals[kind], _check_encode_samples(f, kind, x[bb], slots_all[bb].to(torch.int32), pool, b.num_pages,
+                                                                pick, f"{wl.name} layer {li} b{bb}"))
             del x
+            check_exemption_reach(totals[kind], f"{wl.name} layer {li} kind {kind}")
     del b
     torch.cuda.empty_cache()
 
@@ -119,4 +121,5 @@ def test_bulk_encode_full_size(bits, qjl):
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         pick = _sample_positions(N, P, rng, n_random=120)
-        _check_encode_samples(fmt, kind, x, slots, pool.cpu().numpy(), num_pages, pick, f"b{bits} qjl{qjl} kind{kind}")
+        st = _check_encode_samples(fmt, kind, x, slots, pool.cpu().numpy(), num_pages, pick, f"b{bits} qjl{qjl} kind{kind}")
+        check_exemption_reach(st, f"bulk encode b{bits} qjl{qjl} kind {kind}")

@@ -12,7 +12,7 @@ import tq_inputs as ti
 
 EXEMPT = 1e-4     # codes / sign bits may differ only this close to a decision boundary
 REL_ATTN = 2e-3   # attention outputs: max |o - o_ref| / max |o_ref| per (b, q head)
-REL_NORM = 1e-6   # stored fp32 norms and gammas
+REL_NORM = 1e-6   # stored fp32 norms and QJL gammas, relative (their summation order differs)
 
 
 def value_chunk_pos(off: int, r: int, d: int, vb: int) -> int:
@@ -122,20 +122,48 @@ def compare_encoded(pool_gpu, pool_ref, lay, fmt, kind, slots, code_margin, sign
     assert np.all(np.abs(ng - nr) <= REL_NORM * np.abs(nr) + 1e-30), np.max(np.abs(ng - nr) / np.maximum(np.abs(nr), 1e-30))
     code_diff = cg != cr
     assert np.all(cm[code_diff] < EXEMPT), "code mismatch outside the boundary exemption"
-    stats = dict(codes=cg.size, code_mismatch=int(code_diff.sum()), code_exempt=int((cm < EXEMPT).sum()))
+    stats = dict(codes=cg.size, code_mismatch=int(code_diff.sum()), code_exempt=int((cm < EXEMPT).sum()),
+                 norm_max_rel=float((np.abs(ng - nr) / np.maximum(np.abs(nr), 1e-30)).max(initial=0.0)))
     if kind == 0 and fmt.k_qjl:
-        vec_same = ~code_diff.any(-1)  # sign bits are compared where all codes agree
+        vec_same = ~code_diff.any(-1)  # gamma and sign bits are compared where all codes agree
         sm = sign_margin[live]
         gdiff = np.abs(gg - gr)
-        assert np.all(gdiff[vec_same] <= 1e-5 * np.abs(gr[vec_same]) + 1e-30), np.max(gdiff[vec_same])
+        assert np.all(gdiff[vec_same] <= REL_NORM * np.abs(gr[vec_same]) + 1e-30), np.max((gdiff / np.maximum(np.abs(gr), 1e-30))[vec_same])
         sdiff = (sg != sr) & vec_same[..., None]
         assert np.all(sm[sdiff] < EXEMPT), "sign-bit mismatch outside the boundary exemption"
+        rel = gdiff / np.maximum(np.abs(gr), 1e-30)
         stats.update(signs=int(vec_same.sum()) * fmt.qjl_m, sign_mismatch=int(sdiff.sum()),
-                     sign_exempt=int((sm[vec_same] < EXEMPT).sum()), vectors_skipped_for_signs=int((~vec_same).sum()))
+                     sign_exempt=int((sm[vec_same] < EXEMPT).sum()), vectors=int(vec_same.size),
+                     vectors_skipped_for_signs=int((~vec_same).sum()),
+                     gamma_max_abs=float(gdiff[vec_same].max(initial=0.0)),
+                     gamma_max_rel=float(rel[vec_same].max(initial=0.0)))
     # bytes the encode must not touch are identical (both pools start from the same canary)
     mask = written_mask(len(pool_ref), lay, fmt, kind, slots)
     assert np.array_equal(pool_gpu[~mask], pool_ref[~mask]), "bytes outside the written fields changed"
     return stats
+
+
+def merge_stats(total: dict, st: dict) -> dict:
+    """Accumulate compare_encoded statistics: counts add, maxima take the max."""
+    for k, v in st.items():
+        total[k] = max(total.get(k, 0.0), v) if k.endswith(("_max_abs", "_max_rel")) else total.get(k, 0) + v
+    return total
+
+
+def check_exemption_reach(total: dict, where: str = ""):
+    """Bounds on how far the boundary exemption reaches over many vectors.
+    A code may differ only within 1e-4 of a threshold, where the fp64 oracle
+    and the fp32 kernel can round to different sides; such differences need a
+    margin of a few fp32 ulps (|u| < 6, so ~1e-6), a small fraction of the
+    1e-4 band.  So mismatches stay a small fraction of the exempt coordinates
+    and of all codes, and the vectors whose sign bits and gamma are not
+    compared (those with a differing code) stay rare."""
+    print(f"exemption reach {where}: {total}")
+    assert total.get("code_mismatch", 0) <= max(2, 0.25 * total.get("code_exempt", 0)), total
+    assert total.get("code_mismatch", 0) <= 1e-4 * max(1, total.get("codes", 0)) + 2, total
+    if "vectors" in total:
+        assert total["vectors_skipped_for_signs"] <= 0.01 * total["vectors"] + 2, total
+        assert total["sign_mismatch"] <= max(2, 0.25 * total["sign_exempt"]), total
 
 
 def rel_err(out, ref):
