@@ -125,50 +125,6 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// ---- bulk-copy staging: mbarrier and cp.async.bulk (global -> shared)
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait for the phase with the given parity, giving up after ~0.5 s; the
-// verdict is made warp-uniform so that no lane runs ahead alone.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  bool ok = mbar_try_wait(bar, parity);
-  if (!ok) {
-    const uint64_t t0 = global_ns();
-    while (!ok) {
-      for (int i = 0; i < 64 && !ok; i++) ok = mbar_try_wait(bar, parity);
-      if (!ok && global_ns() - t0 > 500000000ull) break;
-    }
-  }
-  return __all_sync(0xffffffffu, ok);
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
 // Read-only streaming loads of the packed cache that do not allocate in L1
 // (the tile data is used once; L1 hit rates for it are ~3 %).
 __device__ __forceinline__ uint4 ldna(const uint4 *p) {
@@ -305,81 +261,6 @@ __device__ __forceinline__ void load_values(const AttnArgs &a, const uint8_t *sl
   }
 }
 
-// One staged tile in shared memory: key codes [16][16 KB], value codes (one
-// grouped 16-token run), key norms [16], value norms [16], then for QJL the
-// gammas [16] and sign words [16][4].  Every part is a whole number of
-// 16-byte units, as bulk copies need.
-template <int KB, int VB, bool QJL>
-struct Stage {
-  static constexpr uint32_t kc = 0, vc = 16 * 16 * KB, kn = vc + 16 * 16 * VB, vn = kn + 64, kg = vn + 64,
-                            ks = kg + 64, bytes = QJL ? ks + 256 : kg;
-};
-
-template <int KB, int VB, bool QJL>
-__device__ __forceinline__ void lds_keys(const uint8_t *st, int live, int r, int t, KeyRegs<KB, QJL> &R) {
-  using S = Stage<KB, VB, QJL>;
-  R.ok0 = r < live;
-  R.ok1 = r + 8 < live;
-  const uint8_t *kc = st + S::kc + t * 4 * KB;
-  if constexpr (KB == 4) {
-    const uint4 x = *reinterpret_cast<const uint4 *>(kc + r * 64), y = *reinterpret_cast<const uint4 *>(kc + (r + 8) * 64);
-    R.k0[0] = x.x; R.k0[1] = x.y; R.k0[2] = x.z; R.k0[3] = x.w;
-    R.k1[0] = y.x; R.k1[1] = y.y; R.k1[2] = y.z; R.k1[3] = y.w;
-  } else if constexpr (KB == 2) {
-    const uint2 x = *reinterpret_cast<const uint2 *>(kc + r * 32), y = *reinterpret_cast<const uint2 *>(kc + (r + 8) * 32);
-    R.k0[0] = x.x; R.k0[1] = x.y;
-    R.k1[0] = y.x; R.k1[1] = y.y;
-  } else {
-#pragma unroll
-    for (int i = 0; i < KB; i++) {
-      R.k0[i] = reinterpret_cast<const uint32_t *>(kc + r * 16 * KB)[i];
-      R.k1[i] = reinterpret_cast<const uint32_t *>(kc + (r + 8) * 16 * KB)[i];
-    }
-  }
-  const float *kn = reinterpret_cast<const float *>(st + S::kn);
-  R.nk0 = kn[r];
-  R.nk1 = kn[r + 8];
-  if constexpr (QJL) {
-    const float *kg = reinterpret_cast<const float *>(st + S::kg);
-    R.g0 = kg[r];
-    R.g1 = kg[r + 8];
-    const uint32_t *ks = reinterpret_cast<const uint32_t *>(st + S::ks);
-    R.s0 = ks[r * 4 + t];
-    R.s1 = ks[(r + 8) * 4 + t];
-  }
-}
-
-template <int KB, int VB, bool QJL>
-__device__ __forceinline__ void lds_values(const uint8_t *st, int r, int t, ValRegs<VB> &R) {
-  using S = Stage<KB, VB, QJL>;
-  const float *vn = reinterpret_cast<const float *>(st + S::vn);
-  R.nv0 = vn[r];
-  R.nv1 = vn[r + 8];
-  const int lane = 4 * r + t;
-  const uint8_t *vc = st + S::vc + lane * (4 * 2 * VB);
-  if constexpr (VB == 4) {
-    // the two 16-byte halves are read in the opposite order on odd r, so the
-    // eight lanes of each load phase cover eight different bank groups
-    const int sw = r & 1;
-    const uint4 xa = *reinterpret_cast<const uint4 *>(vc + 16 * sw), xb = *reinterpret_cast<const uint4 *>(vc + 16 * (sw ^ 1));
-    const uint4 x0 = sw ? xb : xa, x1 = sw ? xa : xb;
-    R.vlo[0] = x0.x; R.vhi[0] = x0.y; R.vlo[1] = x0.z; R.vhi[1] = x0.w;
-    R.vlo[2] = x1.x; R.vhi[2] = x1.y; R.vlo[3] = x1.z; R.vhi[3] = x1.w;
-  } else if constexpr (VB == 2) {
-    const uint4 x0 = *reinterpret_cast<const uint4 *>(vc);
-    R.vlo[0] = x0.x; R.vlo[1] = x0.y; R.vlo[2] = x0.z; R.vlo[3] = x0.w;
-#pragma unroll
-    for (int i = 0; i < 4; i++) R.vhi[i] = 0u;
-  } else {
-    const uint2 x0 = reinterpret_cast<const uint2 *>(vc)[0], x1 = reinterpret_cast<const uint2 *>(vc)[1],
-                x2 = reinterpret_cast<const uint2 *>(vc)[2];
-    R.vlo[0] = x0.x;                                  R.vhi[0] = x0.y & 0xFFFFu;
-    R.vlo[1] = __byte_perm(x0.y, x1.x, 0x5432);       R.vhi[1] = x1.x >> 16;
-    R.vlo[2] = x1.y;                                  R.vhi[2] = x2.x & 0xFFFFu;
-    R.vlo[3] = __byte_perm(x2.x, x2.y, 0x5432);       R.vhi[3] = x2.y >> 16;
-  }
-}
-
 // Walks the tiles of one segment page by page, without divisions.
 struct TileCursor {
   const uint8_t *pool;
@@ -415,15 +296,11 @@ struct TileCursor {
   }
 };
 
-// Register pipeline over tiles: 0 = load a tile, then compute it; 1 = the
-// whole next tile in flight while one is computed; 2 = the next tile's keys
-// in flight, a tile's values loaded as its keys are scored.  Default: 2 for
-// uniform key widths, 0 for mixed ones (measured at the Llama-3-8B decode
-// shape, 32K context: K4/V4 141.3 us with 2 against 146.4 with 0; K3.5/V3
-// 188.4 against 169.0).
-#ifndef TQ_TILE_PIPELINE
-#define TQ_TILE_PIPELINE -1
-#endif
+// Register pipeline over tiles: the next tile's keys in flight while a tile
+// is scored, its values loaded as its keys are scored, for uniform key
+// widths; mixed widths load a tile, then compute it (measured at the
+// Llama-3-8B decode shape, 32K context: K4/V4 141.3 us with keys in flight
+// against 146.4 without; K3.5/V3 188.4 against 169.0).
 // Value MMA layouts.  Parity pairs (K index = token slot x coordinate
 // parity: an A register is one code pair of one token) for 3-bit values,
 // where they replace a gather of two tokens' 3-bit fields; coordinate halves
@@ -437,22 +314,13 @@ __host__ __device__ constexpr bool val_parity_pairs() {
   return VB == 3;
 }
 template <int KB>
-__host__ __device__ constexpr int tile_pipeline() {
-  return TQ_TILE_PIPELINE >= 0 ? TQ_TILE_PIPELINE : (kb_mixed(KB) ? 0 : 2);
+__host__ __device__ constexpr bool keys_in_flight() {
+  return !kb_mixed(KB);
 }
 
-// Tile operands: 1 = bulk copies into a two-stage shared-memory ring per warp
-// (the next tile in flight while one is computed), 0 = loads into registers.
-// Measured at the Llama-3-8B decode shape, 32K context: 186 us per launch
-// with the ring against 166 us with register loads, so 0 is the default.
-#ifndef TQ_TMA_STAGING
-#define TQ_TMA_STAGING 0
-#endif
-
-// Pages of a segment staged in L2 ahead of the page being read.
-#ifndef TQ_L2_PREFETCH
-#define TQ_L2_PREFETCH 1
-#endif
+// Pages of a segment staged in L2 ahead of the page being read (0 and 2
+// measured slower at the Llama-3-8B decode shape).
+constexpr int kL2Ahead = 1;
 
 // Shared-memory placement of the two centroid tables, as offsets from the
 // start of dynamic shared memory: the value table ([EV] rows of 256 bytes,
@@ -461,8 +329,7 @@ __host__ __device__ constexpr int tile_pipeline() {
 // (table offset | pair code << 8 | lane slot), one prmt / lop3, and each lane
 // reads its own bank.
 constexpr uint32_t kValTableOff = 0, kKeyTableOff = 65536;
-// 2-bit keys use a key table indexed by a code byte (two pairs, 128 KB);
-// builds with the staging ring keep the pair-indexed table to leave room.
+// 2-bit keys use a key table indexed by a code byte (two pairs, 128 KB).
 //
 // Window-aligned tables (uniform 4-bit keys without QJL): the two tables are
 // placed, at run time, where their shared-window addresses are multiples of
@@ -475,14 +342,14 @@ constexpr uint32_t kValTableOff = 0, kKeyTableOff = 65536;
 // widths, the aligned lookups measured slower).
 template <int KB>
 __host__ __device__ constexpr bool byte_keys() {
-  return KB == 2 && !TQ_TMA_STAGING;
+  return KB == 2;
 }
 template <int KB, bool QJL>
 __host__ __device__ constexpr bool aligned_tables() {
-  return KB == 4 && !QJL && !TQ_TMA_STAGING;
+  return KB == 4 && !QJL;
 }
 template <int KB>
-__host__ __device__ constexpr uint32_t attn_stage_off() {
+__host__ __device__ constexpr uint32_t attn_tables_end() {
   return kKeyTableOff + (kb_mixed(KB) ? ((uint32_t(1) << (2 * kb_hi(KB))) + (uint32_t(1) << (2 * kb_lo(KB)))) * 256
                          : byte_keys<KB>() ? 2u * 256 * 256 : (uint32_t(1) << (2 * KB)) * 256);
 }
@@ -491,33 +358,18 @@ template <int KB>
 __host__ __device__ constexpr uint32_t key_lo_table_off() {
   return kKeyTableOff + (uint32_t(1) << (2 * kb_hi(KB))) * 256;
 }
-// Stages of the per-warp ring (TQ_TMA_STAGING=1).
-#ifndef TQ_TMA_STAGES
-#define TQ_TMA_STAGES 2
-#endif
-constexpr int kStages = TQ_TMA_STAGES;
-// Per warp: kStages stages of (tile, 16-byte slot holding the tile's live
-// token count), then kStages 8-byte mbarriers, padded to 16 bytes.
-template <int KB, int VB, bool QJL>
-__host__ __device__ constexpr uint32_t attn_stage_stride() {
-  return Stage<KB, VB, QJL>::bytes + 16;
-}
-template <int KB, int VB, bool QJL>
-__host__ __device__ constexpr uint32_t attn_warp_stage_bytes() {
-  return (kStages * attn_stage_stride<KB, VB, QJL>() + 8 * kStages + 15) / 16 * 16;
-}
 template <int KB, int VB, bool QJL, int NT>
 constexpr size_t attn_smem_bytes() {
   return aligned_tables<KB, QJL>()
-             ? 65536 + (size_t)attn_stage_off<KB>()  // room to shift the tables to a 64 KB window boundary
-             : attn_stage_off<KB>() + (TQ_TMA_STAGING ? (size_t)attn_warps(NT, QJL) * attn_warp_stage_bytes<KB, VB, QJL>() : 0);
+             ? 65536 + (size_t)attn_tables_end<KB>()  // room to shift the tables to a 64 KB window boundary
+             : (size_t)attn_tables_end<KB>();
 }
 
 template <int KB, int VB, bool QJL, int NT>
 __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(const AttnArgs a) {
   constexpr int EK = 1 << (2 * kb_hi(KB)), EV = 1 << (2 * VB);
   static_assert(EV * 256 <= (int)kKeyTableOff, "table sizes");
-  static_assert(attn_stage_off<KB>() <= 232448, "tables above the shared-memory limit");
+  static_assert(attn_tables_end<KB>() <= 232448, "tables above the shared-memory limit");
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr bool kAligned = aligned_tables<KB, QJL>();
   // aligned tables: the shift that puts them on a 64 KB window boundary and
@@ -602,23 +454,6 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   // value-weight operands: the low (tokens 2t, 2t+1) or high (2t+8, 2t+9)
   // half of a weight pair into the half of this lane's parity column r/4
   const uint32_t selW_lo = r < 4 ? 0x4410u : 0x1044u, selW_hi = r < 4 ? 0x4432u : 0x3244u;
-#if TQ_TMA_STAGING
-  static_assert(!kb_mixed(KB), "the staging ring carries uniform key widths only");
-  using SL = Stage<KB, VB, QJL>;
-  const uint32_t wst_off = attn_stage_off<KB>() + (threadIdx.x >> 5) * attn_warp_stage_bytes<KB, VB, QJL>();
-  constexpr uint32_t kStride = attn_stage_stride<KB, VB, QJL>();
-  uint8_t *wst = smem + wst_off;  // this warp's ring
-  const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(smem) + wst_off;
-  const uint32_t bar0 = wst_s + kStages * kStride;
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < kStages; i++) mbar_init(bar0 + 8 * i, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");  // visible to the bulk-copy unit
-    fence_proxy_async_smem();
-  }
-  __syncwarp();
-  uint32_t gk = 0;  // tiles this warp has consumed: stage gk % kStages, phase parity (gk / kStages) & 1
-#endif
   const int H = a.H, G = a.G, Hq = a.Hq;
   const int tpp = a.P >> 4;
   const uint32_t slab_bytes = (uint32_t)a.slab_bytes;
@@ -722,9 +557,9 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
     cur.tok0 = j * 16;
     cur.clen = a.clen[b];
     const int last_page = (j + seg_tiles - 1) / tpp;
-    if (TQ_L2_PREFETCH > 0 && lane == 0) {  // stage the first pages of the segment in L2
+    if (lane == 0) {  // stage the first pages of the segment in L2
 #pragma unroll
-      for (int d = 0; d <= TQ_L2_PREFETCH; d++)
+      for (int d = 0; d <= kL2Ahead; d++)
         if (cur.pidx + d <= last_page) {
           const uint8_t *sp = cur.slab_of(cur.pidx + d);
           if (sp) prefetch_l2(sp, slab_bytes);
@@ -969,12 +804,12 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
       }
     };
 
-    // next tile position: stage the page TQ_L2_PREFETCH ahead whenever a page starts
+    // next tile position: stage the page kL2Ahead ahead whenever a page starts
     auto step_cursor = [&]() {
       if (cur.advance()) {
         cur.enter_page(a.err_word, lane == 0);
-        if (TQ_L2_PREFETCH > 0 && lane == 0 && cur.pidx + TQ_L2_PREFETCH <= last_page) {
-          const uint8_t *sp = cur.slab_of(cur.pidx + TQ_L2_PREFETCH);
+        if (lane == 0 && cur.pidx + kL2Ahead <= last_page) {
+          const uint8_t *sp = cur.slab_of(cur.pidx + kL2Ahead);
           if (sp) prefetch_l2(sp, slab_bytes);
         }
       }
@@ -982,64 +817,9 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 
     using KR = KeyRegs<KB, QJL>;
     using VR = ValRegs<VB>;
-#if TQ_TMA_STAGING
-    // Lane 0 copies the tile under the cursor into stage s (or, for a page
-    // outside the pool, only arrives so the phase still completes) and notes
-    // the tile's live token count in the stage's slot.
-    auto issue = [&](uint32_t s) {
-      const int live = cur.live();
-      if (lane == 0) {
-        const uint32_t bar = bar0 + 8 * s, dst = wst_s + s * kStride;
-        *reinterpret_cast<int *>(wst + s * kStride + SL::bytes) = live;
-        if (cur.page_ok) {
-          mbar_arrive_expect_tx(bar, SL::bytes);
-          bulk_g2s(dst + SL::kc, cur.slab + a.k_codes_o + (int64_t)cur.o0 * (16 * KB), 16 * 16 * KB, bar);
-          bulk_g2s(dst + SL::vc, cur.slab + a.v_codes_o + (int64_t)cur.o0 * (16 * VB), 16 * 16 * VB, bar);
-          bulk_g2s(dst + SL::kn, cur.slab + a.k_norm_o + cur.o0 * 4, 64, bar);
-          bulk_g2s(dst + SL::vn, cur.slab + a.v_norm_o + cur.o0 * 4, 64, bar);
-          if constexpr (QJL) {
-            bulk_g2s(dst + SL::kg, cur.slab + a.k_gamma_o + cur.o0 * 4, 64, bar);
-            bulk_g2s(dst + SL::ks, cur.slab + a.k_signs_o + cur.o0 * 16, 256, bar);
-          }
-        } else {
-          mbar_arrive(bar);
-        }
-      }
-    };
-    // prologue: the first kStages - 1 tiles of the segment; their stages were
-    // last read at least one tile ago
-    const int ahead = kStages - 1 < seg_tiles ? kStages - 1 : seg_tiles;
-    __syncwarp();
-    if (lane == 0) fence_proxy_async_smem();
-    for (int i = 0; i < ahead; i++) {
-      if (i) step_cursor();
-      issue((gk + i) % kStages);
-    }
-    for (int k = 0; k < seg_tiles; k++, gk++) {
-      const uint32_t s = gk % kStages;
-      if (k + kStages - 1 < seg_tiles) {  // the stage of tile k - 1, now finished
-        step_cursor();
-        __syncwarp();
-        if (lane == 0) fence_proxy_async_smem();
-        issue((gk + kStages - 1) % kStages);
-      }
-      if (!mbar_wait_bounded(bar0 + 8 * s, (gk / kStages) & 1)) {
-        if (lane == 0) report(a.err_word, TQ_DEVERR_TIMEOUT);
-        for (int i = 1; i < kStages; i++)  // own copies still in flight
-          if (k + i < seg_tiles) mbar_wait_bounded(bar0 + 8 * ((gk + i) % kStages), ((gk + i) / kStages) & 1);
-        return;
-      }
-      const uint8_t *st = wst + s * kStride;
-      KR ka;
-      VR va;
-      lds_keys<KB, VB, QJL>(st, *reinterpret_cast<const int *>(st + SL::bytes), r, t, ka);
-      lds_values<KB, VB, QJL>(st, r, t, va);
-      process(ka, va);
-    }
-#else
     auto keys = [&](KR &R) { load_keys<KB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, R); };
     auto vals = [&](VR &R) { load_values<VB>(a, cur.slab, cur.o0, r, t, R); };
-    if constexpr (tile_pipeline<KB>() == 2) {
+    if constexpr (keys_in_flight<KB>()) {
       // keys one tile ahead (ping-pong ka / kb), values at the tile itself
       KR ka, kb;
       VR v;
@@ -1060,26 +840,6 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         process(kb, v);
         if (++k == seg_tiles) break;
       }
-    } else if constexpr (tile_pipeline<KB>() == 1) {
-      // the next tile's loads are in flight while this one is computed
-      KR ka, kb;
-      VR va, vb;
-      keys(ka);
-      vals(va);
-      int k = 0;
-      for (; k + 2 <= seg_tiles; k += 2) {
-        step_cursor();
-        keys(kb);
-        vals(vb);
-        process(ka, va);
-        if (k + 2 < seg_tiles) {
-          step_cursor();
-          keys(ka);
-          vals(va);
-        }
-        process(kb, vb);
-      }
-      if (k < seg_tiles) process(ka, va);
     } else {
       for (int k = 0; k < seg_tiles; k++) {
         KR ka;
@@ -1090,8 +850,6 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
         if (k + 1 < seg_tiles) step_cursor();
       }
     }
-
-#endif
 
     // ---- segment partial: slot = warp + unit
     const int64_t slot = wg + (int64_t)b * H + h;

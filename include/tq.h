@@ -18,11 +18,7 @@
  *     outside the pool, a length larger than its buffer) never trap: the
  *     kernel skips the offending token/page and ORs a TQ_DEVERR_* bit into
  *     the caller's optional int32 *err_word (device memory, may be NULL).
- *   - No kernel waits on another, and the default build has no wait inside
- *     a kernel.  A build with the bulk-copy staging option of the attention
- *     kernel (TQ_TMA_STAGING=1) has one: a warp waiting for its own copies
- *     into shared memory, which gives up after about 0.5 s, sets
- *     TQ_DEVERR_TIMEOUT and returns.
+ *   - No kernel waits on another, and no kernel spins on a flag or barrier.
  *
  * Format (tq_format): d = head_dim, b_K / b_V = bits per coordinate of the
  * Lloyd-Max codes, optional 1-bit QJL residual sketch of length m on keys,
@@ -61,7 +57,6 @@ enum { TQ_KIND_K = 0, TQ_KIND_V = 1 };
 #define TQ_DEVERR_SLOT_RANGE 0x1   /* slot_mapping[n] >= num_pages * page_size          */
 #define TQ_DEVERR_PAGE_RANGE 0x2   /* block_tables entry outside [0, num_pages)         */
 #define TQ_DEVERR_LENGTH 0x4       /* comp_lens[b] > max_pages*P, win_lens[b] > window, or a negative length */
-#define TQ_DEVERR_TIMEOUT 0x8      /* a staging wait in the attention kernel gave up after ~0.5 s: outputs invalid */
 
 typedef struct {
   int32_t head_dim;     /* d                                                   */
@@ -129,7 +124,10 @@ const char *tq_status_string(tq_status s);
  * iteration, rounded to fp32.  centroids: host float[2^bits], ascending;
  * midpoints: host float[2^bits - 1], ascending (decision thresholds).
  * bits in [1, 8].  The device codebook the other calls take is the
- * concatenation centroids || midpoints (2^(b+1) - 1 floats).
+ * concatenation centroids || midpoints (2^(b+1) - 1 floats).  There is no
+ * head_dim argument (build choice, no passage): the table quantizes the
+ * unit-variance coordinates u = H(D x)/||x||, whose N(0, 1) law is the same
+ * for every d, so one table serves every head size.
  */
 tq_status tq_make_codebook(int bits, float *centroids, float *midpoints);
 
@@ -234,10 +232,19 @@ tq_status tq_append_window(const tq_format *fmt, int batch, const void *k_new_f1
 
 /*
  * Decode N slots of one kind back to vectors (tests and offline use; never on
- * the attention path, which reads the packed pages directly):
+ * the attention path, which reads the packed pages directly).  Follows the
+ * aither-kvcache README, section 'Algorithm' (decoding runs the encode's
+ * steps backwards: centroid look-up, inverse rotation, rescale by the norm),
+ * with the QJL reconstruction of "From 0% to 100%: Debugging a KV Cache
+ * Compression Algorithm ...", section 'The QJL detective story':
  *   x_hat = n * D . (H y) / sqrt(d),
- *   y = c[code] / sqrt(d) + sqrt(pi/2)/m * gamma * S^T (2 bits - 1) (QJL keys).
- *   out  device fp32 [N][H][d].  A negative slot gives zeros.
+ *   y = c[code] / sqrt(d) + a * gamma * S^T (2 bits - 1)   (QJL keys),
+ *   a = fmt->qjl_scale, or sqrt(pi/2)/m when qjl_scale is 0.
+ *   page_pool    as for tq_encode; slot_mapping device int32 [N] (slot as in
+ *                tq_encode); signs, codebook, S as for tq_encode
+ *   out          device fp32 [N][H][d].  A negative slot gives zeros.
+ *   err_word     device int32 or NULL (TQ_DEVERR_SLOT_RANGE: that slot gives
+ *                zeros)
  */
 tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64_t num_pages,
                     const int32_t *slot_mapping, int64_t n_tokens, const uint8_t *signs,
@@ -245,7 +252,11 @@ tq_status tq_decode(const tq_format *fmt, int kind, const void *page_pool, int64
 
 /*
  * Bytes of device workspace tq_decode_attn needs for these sizes on the
- * current device (depends on its SM count).  Host only.
+ * current device (depends on its SM count).  Host only.  Build choice, no
+ * passage: the size is given by max_pages (block-table columns: the largest
+ * compressed context is max_pages * P) and window (its fp16 partials) rather
+ * than one max_ctx, because the two parts of the context have separate
+ * scratch sections and the caller sizes both anyway.
  */
 tq_status tq_decode_attn_workspace_size(const tq_format *fmt, int batch, int num_q_heads, int max_pages,
                                         int window, size_t *bytes);
@@ -309,9 +320,20 @@ tq_status tq_decode_attn_timed(const tq_format *fmt, int batch, int num_q_heads,
  * must not call into any allocator.
  *   - Arguments, layouts, results and device-side errors are those of
  *     tq_decode_attn, minus workspace / workspace_bytes.
- *   - The first call on a device (that device current) looks up the
- *     buffer's address with cudaGetSymbolAddress; make that first call
- *     before any stream capture.  A failed look-up returns TQ_ERR_CUDA.
+ *   - Every call looks up the buffer's address in the current context with
+ *     cudaGetSymbolAddress (a host-side lookup once the library's module is
+ *     loaded in that context, so a context created anew after
+ *     cudaDeviceReset is found too).  The first call on a device, that
+ *     device current, may load the module: make it before any stream
+ *     capture.  A failed look-up returns TQ_ERR_CUDA.
+ *   - The buffer is part of the library's device image: every device
+ *     context that loads the module holds its 16 MiB until the process
+ *     exits.  With lazy module loading (the CUDA default) that is a device
+ *     on which a libtq kernel has run; with CUDA_MODULE_LOADING=EAGER it is
+ *     every device the process touches after loading libtq.so, even if
+ *     tq_decode_attn_static is never called.
+ *   - The tensors must live on the device that is current on the calling
+ *     thread: the buffer used is that device's.
  *   - A shape whose tq_decode_attn_workspace_size exceeds
  *     TQ_STATIC_SCRATCH_BYTES returns TQ_ERR_SCRATCH_LIMIT before anything
  *     is launched (16 MiB covers, e.g., B 16 x 32/8 heads at 32K context).
