@@ -235,8 +235,18 @@ tq_status tq_make_codebook(int bits, float *centroids, float *midpoints) {
   double c[256], t[256];
   lloyd_max_thresholds(bits, c, t);
   const int levels = 1 << bits;
+  // stored at fp16: the nearest fp16 value of each centroid (ties to even);
+  // the thresholds are then the exact midpoints of the stored neighbours
+  for (int k = 0; k < levels; k++) {
+    const double x = c[k];
+    if (x != 0.0) {
+      const int e = ilogb(x) < -14 ? -14 : ilogb(x);  // fp16 binade (subnormals share -14)
+      const double quantum = ldexp(1.0, e - 10);      // 10 fraction bits
+      c[k] = rint(x / quantum) * quantum;
+    }
+  }
   for (int k = 0; k < levels; k++) centroids[k] = (float)c[k];
-  for (int k = 0; k + 1 < levels; k++) midpoints[k] = (float)t[k];
+  for (int k = 0; k + 1 < levels; k++) midpoints[k] = (float)(0.5 * (c[k] + c[k + 1]));
   return TQ_OK;
 }
 

@@ -23,17 +23,19 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "oracle.c")
+_SRCS = (os.path.join(_HERE, "oracle.c"), os.path.join(_HERE, "kivi.c"))
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so with gcc (-O2, no fast-math)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    """Compile oracle.c and kivi.c into liboracle.so with gcc (-O2, no
+    fast-math, no floating-point contraction)."""
+    newest = max(os.path.getmtime(p) for p in _SRCS)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"], check=True)
+        subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, *_SRCS, "-lm"], check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -61,6 +63,8 @@ def _load():
             lib.orc_half_to_double.restype = dbl
             lib.orc_lloyd_max_f64.argtypes = [C.c_int, P, P]
             lib.orc_make_codebook.argtypes = [C.c_int, P, P]
+            lib.orc_round_to_half.argtypes = [dbl]
+            lib.orc_round_to_half.restype = dbl
             lib.orc_quantize_scalar.argtypes = [C.c_int, P, dbl]
             lib.orc_fwht.argtypes = [P, C.c_int]
             lib.orc_fwht.restype = None
@@ -78,6 +82,13 @@ def _load():
             lib.orc_encode.argtypes = [P, C.c_int, P, i64, P, P, i64, P, P, P, P, P, P, P]
             lib.orc_decode.argtypes = [P, C.c_int, P, i64, P, i64, P, P, P, P]
             lib.orc_attention.argtypes = [P, C.c_int, C.c_int, P, P, i64, P, C.c_int, P, P, P, P, C.c_int, P, P, P, P, P, P, C.c_int, P]
+            lib.orc_kivi_layout.argtypes = [P, P]
+            lib.orc_kivi_quantize_group.argtypes = [C.c_int, P, i64, C.c_int, P, P, P]
+            lib.orc_kivi_quantize_group.restype = None
+            lib.orc_kivi_encode_keys.argtypes = [P, P, i64, P, P, i64]
+            lib.orc_kivi_encode_values.argtypes = [P, P, i64, P, P, i64]
+            lib.orc_kivi_decode.argtypes = [P, C.c_int, P, i64, P, i64, P]
+            lib.orc_kivi_attention.argtypes = [P, C.c_int, C.c_int, P, P, i64, P, C.c_int, P, P, P, P, C.c_int, P, C.c_int, P]
             _lib = lib
     return _lib
 
@@ -132,8 +143,15 @@ def kind_codebook(f, kind: int):
     return make_codebook(bits)
 
 
+def round_to_half(x: float) -> float:
+    """The nearest fp16 value of x (ties to even), as a float."""
+    return _load().orc_round_to_half(float(x))
+
+
 def make_codebook(bits: int):
-    """The stored codebook: fp32 centroids [2^b] and fp32 midpoints [2^b-1]."""
+    """The stored codebook as fp32 arrays: centroids [2^b] (the fp64 Lloyd-Max
+    fixed point rounded to fp16) and thresholds [2^b-1] (exact midpoints of
+    neighbouring stored centroids)."""
     L = 1 << bits
     c = np.zeros(L, np.float32)
     t = np.zeros(max(L - 1, 1), np.float32)
@@ -380,3 +398,82 @@ def append_window(f, k_new, v_new, k_win, v_win, win_lens, win_head, comp_lens, 
         assert rc == 0
         comp_lens[b] += 1
     return skipped
+
+
+# ------------------------------------------------------------------- KIVI --
+class _KiviFormat(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "page_size", "num_kv_heads")]
+
+
+class _KiviLayout(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("slab_bytes", "page_bytes", "k_params", "k_codes", "v_params", "v_codes")] + [
+        (n, C.c_int32) for n in ("k_code_bytes", "v_code_bytes")
+    ]
+
+
+def _kfmt(f) -> _KiviFormat:
+    return _KiviFormat(int(f.head_dim), int(f.k_bits), int(f.v_bits), int(f.page_size), int(f.num_kv_heads))
+
+
+def kivi_layout(f) -> dict:
+    """Page layout of the KIVI-style control arm (kivi.c)."""
+    L = _KiviLayout()
+    F = _kfmt(f)
+    if _load().orc_kivi_layout(C.byref(F), C.byref(L)) != 0:
+        raise ValueError("invalid KIVI format")
+    return {n: getattr(L, n) for n, _ in _KiviLayout._fields_}
+
+
+def kivi_quantize_group(x, bits: int):
+    """Asymmetric quantization of one group of fp16 values: (scale, zero) as
+    fp16 and the codes."""
+    xb = _c(_f16bits(np.asarray(x, np.float16)), np.uint16)
+    codes = np.zeros(len(xb), np.int32)
+    s = np.zeros(1, np.uint16)
+    z = np.zeros(1, np.uint16)
+    _load().orc_kivi_quantize_group(len(xb), _ptr(xb), 1, int(bits), _ptr(s), _ptr(z), _ptr(codes))
+    return s.view(np.float16)[0], z.view(np.float16)[0], codes
+
+
+def kivi_encode_keys(f, x, page_ids, pool: np.ndarray, num_pages: int) -> int:
+    """Keys x [N][H][d] fp16 in token order into pages page_ids[n // P]."""
+    xb = _f16bits(x)
+    pi = _c(page_ids, np.int32)
+    F = _kfmt(f)
+    return _load().orc_kivi_encode_keys(C.byref(F), _ptr(xb), int(xb.shape[0]), _ptr(pi), _ptr(pool), int(num_pages))
+
+
+def kivi_encode_values(f, x, slot_mapping, pool: np.ndarray, num_pages: int) -> int:
+    """Values x [N][H][d] fp16 into slots slot_mapping[n] (negative: skipped)."""
+    xb = _f16bits(x)
+    sl = _c(slot_mapping, np.int32)
+    F = _kfmt(f)
+    return _load().orc_kivi_encode_values(C.byref(F), _ptr(xb), int(xb.shape[0]), _ptr(sl), _ptr(pool), int(num_pages))
+
+
+def kivi_decode(f, kind: int, pool, num_pages: int, slot_mapping):
+    """Reconstructions [N][H][d] (fp64) of the given slots of one kind."""
+    sl = _c(slot_mapping, np.int32)
+    out = np.zeros((len(sl), int(f.num_kv_heads), int(f.head_dim)), np.float64)
+    F = _kfmt(f)
+    rc = _load().orc_kivi_decode(C.byref(F), int(kind), _ptr(_c(pool, np.uint8)), int(num_pages), _ptr(sl), len(sl), _ptr(out))
+    return rc, out
+
+
+def kivi_attention(f, q, pool, num_pages: int, block_tables, comp_lens, k_win, v_win, win_lens, heads=None):
+    """Exact-softmax decode attention over a KIVI cache plus the fp16 window."""
+    qb = _f16bits(q)
+    B, Hq, d = qb.shape
+    bt = _c(block_tables, np.int32)
+    cl = _c(comp_lens, np.int32)
+    W = 0 if k_win is None else int(k_win.shape[2])
+    kw = None if k_win is None else _f16bits(k_win)
+    vw = None if v_win is None else _f16bits(v_win)
+    wl = None if win_lens is None else _c(win_lens, np.int32)
+    hs = None if heads is None else _c(heads, np.int32)
+    n = B * Hq if hs is None else len(hs)
+    out = np.zeros((n, d), np.float64)
+    F = _kfmt(f)
+    rc = _load().orc_kivi_attention(C.byref(F), B, Hq, _ptr(qb), _ptr(_c(pool, np.uint8)), int(num_pages), _ptr(bt), int(bt.shape[1]),
+                                    _ptr(cl), _ptr(kw), _ptr(vw), _ptr(wl), W, _ptr(hs), 0 if hs is None else len(hs), _ptr(out))
+    return rc, (out.reshape(B, Hq, d) if hs is None else out)

@@ -36,8 +36,9 @@
  *
  * Readings of points the pages leave open:
  *   - Codebook: Lloyd-Max for N(0,1), fp64 fixed-point iteration from a
- *     symmetric start, symmetrized, then rounded to fp32.  Midpoints are the
- *     fp64 averages of neighbouring fp64 centroids, rounded to fp32.
+ *     symmetric start, symmetrized, then stored at fp16 (each centroid
+ *     rounded to the nearest fp16 value); the thresholds are the exact
+ *     midpoints of neighbouring stored centroids.
  *   - u-domain: u = H (D . x) / ||x||, H the unnormalized Sylvester Hadamard
  *     matrix, so ||u||^2 = d and each u_j is close to N(0,1).
  *   - Quantizer: idx_j = #{k : t_k <= u_j} (ties go to the upper code).
@@ -158,14 +159,39 @@ int orc_lloyd_max_f64(int bits, double *c, double *t) {
   return it;
 }
 
-/* The stored codebook: fp32 centroids [2^b] and fp32 midpoints [2^b - 1]. */
+/* The nearest IEEE binary16 value to x (ties to even), as a double; out of
+ * range gives an infinity.  11 significant bits for normal values, a fixed
+ * quantum of 2^-24 below 2^-14. */
+double orc_round_to_half(double x) {
+  if (x == 0.0 || !isfinite(x)) return x;
+  int e;
+  frexp(x, &e); /* |x| = m 2^e, m in [0.5, 1) */
+  int q = e - 11;
+  if (q < -24) q = -24;
+  double r = ldexp(nearbyint(ldexp(x, -q)), q);
+  if (fabs(r) > 65504.0) r = copysign(INFINITY, x);
+  return r;
+}
+
+/*
+ * The stored codebook: centroids [2^b] and decision thresholds [2^b - 1],
+ * held as fp32 arrays.  The pages fix no storage precision for the
+ * precomputed codebook; it is stored at fp16, the precision of the cache's
+ * own dense data (the fp16 K/V and window): each centroid is the fp64
+ * Lloyd-Max fixed point rounded to the nearest fp16 value, and each
+ * threshold is the exact midpoint of two stored neighbours (representable in
+ * fp32), so the quantizer stays the nearest-centroid rule of the table it
+ * stores.  The fp16 rounding moves a centroid by at most 2^-12 of itself,
+ * which changes the quantizer's MSE by about 1e-5 relative.
+ */
 int orc_make_codebook(int bits, float *centroids, float *midpoints) {
   double c[256], t[256];
   int it = orc_lloyd_max_f64(bits, c, t);
   if (it < 0) return it;
   int L = 1 << bits;
+  for (int k = 0; k < L; k++) c[k] = orc_round_to_half(c[k]);
   for (int k = 0; k < L; k++) centroids[k] = (float)c[k];
-  for (int k = 0; k + 1 < L; k++) midpoints[k] = (float)t[k];
+  for (int k = 0; k + 1 < L; k++) midpoints[k] = (float)(0.5 * (c[k] + c[k + 1]));
   return it;
 }
 

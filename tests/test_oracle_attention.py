@@ -215,7 +215,8 @@ def _rotated_domain_attention(fmt, s, b, qh):
             gam = slab[L["k_gamma"] + 4 * off:][:4].view(np.float32)[0]
             z = _unpack(slab[L["k_signs"] + off * L["k_sign_bytes"]:][: L["k_sign_bytes"]], 1, m)
             # the format's coefficient: qjl_scale when given, else sqrt(pi/2) / m
-            coef = fmt.qjl_scale if fmt.qjl_scale > 0 else math.sqrt(math.pi / 2) / m
+            # (the format field is an fp32 value)
+            coef = float(np.float32(fmt.qjl_scale)) if fmt.qjl_scale > 0 else math.sqrt(math.pi / 2) / m
             score += coef * float(gam) * (q_s @ (2.0 * z - 1.0))
         logits.append(float(nk) * score / math.sqrt(d))
         nv = slab[L["v_norm"] + 4 * off:][:4].view(np.float32)[0]

@@ -89,14 +89,46 @@ def test_distortion_matches_validated_mse(golden):
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
-def test_stored_codebook_is_fp32_rounding(bits):
-    c64, t64, _ = oracle.lloyd_max_f64(bits)
+def test_stored_codebook_is_fp16_rounding(bits):
+    """Stored centroids are numpy's (correctly rounded, ties-to-even) fp16
+    values of the fp64 fixed point; thresholds are the exact midpoints of
+    neighbouring stored centroids."""
+    c64, _, _ = oracle.lloyd_max_f64(bits)
     c32, t32 = oracle.make_codebook(bits)
     assert c32.dtype == np.float32 and t32.dtype == np.float32
-    assert np.array_equal(c32, c64.astype(np.float32))
-    assert np.array_equal(t32, t64.astype(np.float32))
+    c16 = c64.astype(np.float16)
+    assert np.array_equal(c32, c16.astype(np.float32))
+    mid = 0.5 * (c16[:-1].astype(np.float64) + c16[1:].astype(np.float64))
+    assert np.array_equal(t32.astype(np.float64), mid)  # exact in fp32
     assert np.array_equal(c32, -c32[::-1])
     assert np.all(np.diff(t32) > 0)
+    # the rounding moves a centroid by at most half an fp16 ulp
+    assert np.all(np.abs(c32 - c64) <= np.abs(c64) * 2.0 ** -11)
+
+
+def test_round_to_half_matches_numpy():
+    rng = np.random.default_rng(3)
+    xs = np.concatenate([rng.standard_normal(2000) * 3, rng.standard_normal(500) * 1e-5, [0.5 * (1 + 2 ** -10), 1 + 3 * 2 ** -11,
+                                                                                       6.103515625e-05, 2.0 ** -24 * 1.5, 65504.0, 65519.0, 65520.0]])
+    for x in xs:
+        with np.errstate(over="ignore"):
+            want = float(np.float16(x))
+        got = oracle.round_to_half(x)
+        assert got == want or (np.isinf(want) and np.isinf(got)), (x, got, want)
+
+
+def test_fp16_codebook_keeps_the_distortion(golden):
+    """Storing the table at fp16 changes the Gaussian distortion by < 1e-4
+    relative, so the validated MSE values still apply."""
+    g = golden("validated_mse.json")
+    for b in (2, 3, 4):
+        c64, t64, _ = oracle.lloyd_max_f64(b)
+        c32, t32 = oracle.make_codebook(b)
+        d64 = _distortion(c64, t64)
+        d16 = _distortion(c32.astype(np.float64), t32.astype(np.float64))
+        assert d16 >= d64 - 1e-15  # the fp64 fixed point is the optimum
+        assert (d16 - d64) / d64 < 1e-4, (b, d64, d16)
+        assert abs(d16 - g["mse"][str(b)]) / g["mse"][str(b)] < 0.02
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
