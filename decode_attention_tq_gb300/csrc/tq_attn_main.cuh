@@ -12,9 +12,9 @@
 // Per tile (16 tokens of one (b, h)) a warp runs, on the tensor cores
 // (mma.sync m16n8k16, fp16 operands, fp32 accumulation):
 //   scores[16 x 2G] = Kcodes[16 x 128] * Qrot[128 x 2G]
-//     A: centroids of each code pair from a shared-memory table, split into
-//        fp16 hi and lo parts that fill rows g and g+8 of one MMA (8 tokens
-//        per MMA, so one 8-byte table read gives two A registers);
+//     A: the fp16 centroids of each code pair from a shared-memory table (the
+//        stored codebook is fp16-exact, so each is an exact operand); rows
+//        are the 16 tokens of the tile, one 4-byte table read per register;
 //        B: the rotated query, hi/lo split over the 2G columns, so the
 //        product is exact to ~2^-22;
 //   QJL (keys): + signs[16 x 128] * (S q_rot)[128 x 2G], the +-1 operands are
@@ -322,64 +322,83 @@ __host__ __device__ constexpr bool keys_in_flight() {
 // measured slower at the Llama-3-8B decode shape).
 constexpr int kL2Ahead = 1;
 
-// Shared-memory placement of the two centroid tables, as offsets from the
-// start of dynamic shared memory: the value table ([EV] rows of 256 bytes,
-// lane l's 4-byte entry at 4l) at 0 and the key table ([EK] rows of 256 bytes,
-// lane l's 8-byte (hi, lo) entry at 8l) at 64 KB.  An entry offset is then
-// (table offset | pair code << 8 | lane slot), one prmt / lop3, and each lane
-// reads its own bank.
-constexpr uint32_t kValTableOff = 0, kKeyTableOff = 65536;
-// 2-bit keys use a key table indexed by a code byte (two pairs, 128 KB).
+// Shared-memory placement of the centroid tables, as offsets from the start
+// of dynamic shared memory.  Rows of 256 bytes indexed by a code pair (or a
+// code byte); lane l reads its own bank-private entry, so a warp's lookup is
+// conflict-free, and an entry offset is (table offset | code << 8 | lane slot),
+// one prmt / lop3.
+//   - Value table at 0: 4-byte entries (the two fp16 centroids of a code pair)
+//     in the first 128 bytes of a row; 2-bit values: 8-byte entries indexed by
+//     a byte of interleaved codes (two coordinates), whole rows.
+//   - Key table: 4-byte entries (two fp16 centroids; the stored codebook is
+//     fp16-exact, so a centroid is an exact tensor-core operand) in the second
+//     half of the same rows (offset 128) when both kinds use 4-byte entries;
+//     2-bit keys use 8-byte entries indexed by a code byte (two pairs) in rows
+//     of their own from 64 KB.  Mixed-rate keys: the low channels' table
+//     follows the high channels' rows.
 //
-// Window-aligned tables (uniform 4-bit keys without QJL): the two tables are
+// Window-aligned tables (uniform 4-bit keys without QJL): the tables are
 // placed, at run time, where their shared-window addresses are multiples of
 // 64 KB, so the prmt result is itself the address of an `ld.shared` and no
 // lookup adds the base of dynamic shared memory (which is not 0: the window
 // starts with reserved bytes).  The launch reserves 64 KB of room for the
-// shift.  Measured at the Llama-3-8B decode shape, 32K context: 135.2 us per
-// launch against 139.8 us.  The other key kinds keep offset lookups (the
-// mixed and byte-indexed tables would not fit; with QJL, or for the mixed
-// widths, the aligned lookups measured slower).
+// shift.
 template <int KB>
 __host__ __device__ constexpr bool byte_keys() {
   return KB == 2;
+}
+template <int VB>
+__host__ __device__ constexpr bool byte_values() {
+  return VB == 2;
+}
+template <int KB, int VB>
+__host__ __device__ constexpr bool shared_rows() {
+  return !byte_keys<KB>() && !byte_values<VB>();
 }
 template <int KB, bool QJL>
 __host__ __device__ constexpr bool aligned_tables() {
   return KB == 4 && !QJL;
 }
 template <int KB>
-__host__ __device__ constexpr uint32_t attn_tables_end() {
-  return kKeyTableOff + (kb_mixed(KB) ? ((uint32_t(1) << (2 * kb_hi(KB))) + (uint32_t(1) << (2 * kb_lo(KB)))) * 256
-                         : byte_keys<KB>() ? 2u * 256 * 256 : (uint32_t(1) << (2 * KB)) * 256);
+__host__ __device__ constexpr uint32_t key_rows() {
+  return kb_mixed(KB) ? (uint32_t(1) << (2 * kb_hi(KB))) + (uint32_t(1) << (2 * kb_lo(KB)))
+                      : byte_keys<KB>() ? 256u : (uint32_t(1) << (2 * KB));
 }
-// Mixed keys: the low channels' pair table follows the high channels' one.
-template <int KB>
+template <int KB, int VB>
+__host__ __device__ constexpr uint32_t key_table_off() {
+  return shared_rows<KB, VB>() ? 128u : 65536u;
+}
+// Mixed keys: the low channels' pair table follows the high channels' rows.
+template <int KB, int VB>
 __host__ __device__ constexpr uint32_t key_lo_table_off() {
-  return kKeyTableOff + (uint32_t(1) << (2 * kb_hi(KB))) * 256;
+  return key_table_off<KB, VB>() + (uint32_t(1) << (2 * kb_hi(KB))) * 256;
+}
+template <int KB, int VB>
+__host__ __device__ constexpr uint32_t attn_tables_end() {
+  return shared_rows<KB, VB>() ? 256u * (key_rows<KB>() > (1u << (2 * VB)) ? key_rows<KB>() : (1u << (2 * VB)))
+                               : 65536u + 256u * key_rows<KB>();
 }
 template <int KB, int VB, bool QJL, int NT>
 constexpr size_t attn_smem_bytes() {
   return aligned_tables<KB, QJL>()
-             ? 65536 + (size_t)attn_tables_end<KB>()  // room to shift the tables to a 64 KB window boundary
-             : (size_t)attn_tables_end<KB>();
+             ? 65536 + (size_t)attn_tables_end<KB, VB>()  // room to shift the tables to a 64 KB window boundary
+             : (size_t)attn_tables_end<KB, VB>();
 }
 
 template <int KB, int VB, bool QJL, int NT>
 __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(const AttnArgs a) {
   constexpr int EK = 1 << (2 * kb_hi(KB)), EV = 1 << (2 * VB);
-  static_assert(EV * 256 <= (int)kKeyTableOff, "table sizes");
-  static_assert(attn_tables_end<KB>() <= 232448, "tables above the shared-memory limit");
+  static_assert(byte_values<VB>() || EV * 256 <= 65536, "table sizes");
+  static_assert(attn_tables_end<KB, VB>() <= 232448, "tables above the shared-memory limit");
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr bool kAligned = aligned_tables<KB, QJL>();
+  constexpr uint32_t kKeyOff = key_table_off<KB, VB>();
   // aligned tables: the shift that puts them on a 64 KB window boundary and
   // that boundary (table offsets below are added to it); otherwise 0, 0
   const uint32_t win_base = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t tshift = kAligned ? (0u - win_base) & 0xFFFFu : 0u;
   const uint32_t tbase = kAligned ? win_base + tshift : 0u;
   uint8_t *const tables = smem + tshift;
-  uint32_t *lutV = reinterpret_cast<uint32_t *>(tables + kValTableOff);  // [EV][64], lanes in the first 32
-  uint2 *lutK = reinterpret_cast<uint2 *>(tables + kKeyTableOff);        // [EK][32] (hi, lo)
   // table reads: at a shared-window address (aligned tables) or at a byte
   // offset from the start of dynamic shared memory
   auto lut64 = [&](uint32_t off) {
@@ -395,44 +414,39 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
     return v;
   };
 
-  // Bank-private centroid-pair tables: lane l reads its own copy in bank l.
-  // (hi pair, lo pair) of the code pair e of a `bits`-bit codebook cb
-  auto key_pair_of = [&](const float *cb, int bits, int e) {
-    __half h0, l0, h1, l1;
-    split_half(__ldg(cb + (e & ((1 << bits) - 1))) * kCentScale, h0, l0);
-    split_half(__ldg(cb + (e >> bits)) * kCentScale, h1, l1);
-    return make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(l0, l1));
+  // Bank-private centroid-pair tables: lane l reads its own copy in bank l
+  // (8-byte entries: banks 2l, 2l+1 of its half-warp's wavefront).  The two
+  // fp16 centroids (x256) of code pair e of a `bits`-bit codebook cb:
+  auto pair_of = [&](const float *cb, int bits, int e) {
+    return pack_half2(__ldg(cb + (e & ((1 << bits) - 1))) * kCentScale, __ldg(cb + (e >> bits)) * kCentScale);
   };
-  auto key_pair = [&](int e) { return key_pair_of(a.k_cb, kb_hi(KB), e); };
-  auto val_pair = [&](int e) {
-    return pack_half2(__ldg(a.v_cb + (e & ((1 << VB) - 1))) * kCentScale, __ldg(a.v_cb + (e >> VB)) * kCentScale);
-  };
+  uint32_t *const tab32 = reinterpret_cast<uint32_t *>(tables);
+  uint2 *const tab64 = reinterpret_cast<uint2 *>(tables);
   if constexpr (byte_keys<KB>()) {
-    // 2-bit keys: indexed by a code byte (two pairs), entry halves 64 KB apart
+    // 2-bit keys: indexed by a code byte (pair 2k in the low nibble, 2k + 1 high)
     for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
       const int e = i >> 5;
-      lutK[i] = key_pair(e & 15);
-      lutK[i + 256 * 32] = key_pair(e >> 4);
+      tab64[kKeyOff / 8 + i] = make_uint2(pair_of(a.k_cb, 2, e & 15), pair_of(a.k_cb, 2, e >> 4));
     }
   } else {
-    for (int i = threadIdx.x; i < EK * 32; i += blockDim.x) lutK[i] = key_pair(i >> 5);
+    for (int i = threadIdx.x; i < EK * 32; i += blockDim.x)
+      tab32[kKeyOff / 4 + (i >> 5) * 64 + (i & 31)] = pair_of(a.k_cb, kb_hi(KB), i >> 5);
   }
   if constexpr (kb_mixed(KB)) {
     // low channels: the k_bits codebook follows the (k_bits + 1) one
     constexpr int HB = kb_hi(KB), LB = kb_lo(KB), EL = 1 << (2 * LB);
     const float *cb_lo = a.k_cb + (2 << HB) - 1;
-    uint2 *lutKL = reinterpret_cast<uint2 *>(tables + key_lo_table_off<KB>());
-    for (int i = threadIdx.x; i < EL * 32; i += blockDim.x) lutKL[i] = key_pair_of(cb_lo, LB, i >> 5);
+    for (int i = threadIdx.x; i < EL * 32; i += blockDim.x)
+      tab32[key_lo_table_off<KB, VB>() / 4 + (i >> 5) * 64 + (i & 31)] = pair_of(cb_lo, LB, i >> 5);
   }
-  if constexpr (VB == 2) {
+  if constexpr (byte_values<VB>()) {
     // 2-bit values: indexed by a byte of the interleaved codes (two coordinates)
-    uint2 *lutV2 = reinterpret_cast<uint2 *>(tables + kValTableOff);
     for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
       const int e = i >> 5;
-      lutV2[i] = make_uint2(val_pair(e & 15), val_pair(e >> 4));
+      tab64[i] = make_uint2(pair_of(a.v_cb, VB, e & 15), pair_of(a.v_cb, VB, e >> 4));
     }
   } else {
-    for (int i = threadIdx.x; i < EV * 32; i += blockDim.x) lutV[(i >> 5) * 64 + (i & 31)] = val_pair(i >> 5);
+    for (int i = threadIdx.x; i < EV * 32; i += blockDim.x) tab32[(i >> 5) * 64 + (i & 31)] = pair_of(a.v_cb, VB, i >> 5);
   }
   __syncthreads();
   // Up to here only the codebooks were read; launched as a dependent of the
@@ -448,9 +462,9 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   if (wg >= NW) return;
   const int64_t ts = T * wg / NW, te = T * (wg + 1) / NW;
   if (ts >= te) return;
-  const uint32_t laneK = (tbase + kKeyTableOff) | ((uint32_t)lane * 8u);
-  const uint32_t laneKL = (tbase + key_lo_table_off<KB>()) | ((uint32_t)lane * 8u);  // mixed keys: low-channel table
-  const uint32_t laneV = (tbase + kValTableOff) | ((uint32_t)lane * (VB == 2 ? 8u : 4u));
+  const uint32_t laneK = (tbase + kKeyOff) | ((uint32_t)lane * (byte_keys<KB>() ? 8u : 4u));
+  const uint32_t laneKL = (tbase + key_lo_table_off<KB, VB>()) | ((uint32_t)lane * 4u);  // mixed keys: low-channel table
+  const uint32_t laneV = tbase | ((uint32_t)lane * (byte_values<VB>() ? 8u : 4u));
   // value-weight operands: the low (tokens 2t, 2t+1) or high (2t+8, 2t+9)
   // half of a weight pair into the half of this lane's parity column r/4
   const uint32_t selW_lo = r < 4 ? 0x4410u : 0x1044u, selW_hi = r < 4 ? 0x4432u : 0x3244u;
@@ -571,47 +585,52 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
       if (!__any_sync(0xffffffffu, R.ok0)) return;  // token 0 of a tile is live iff any is
       // ---- scores: tokens 0-7, tokens 8-15 and QJL chains run independently.
       // sa rows r / r+8 = token r hi / lo part; sb likewise for token r+8.
-      float sa[NT][4], sbk[NT][4], sq[NT][4];
+      // scr[nt][c]: scores, rows r / r+8 = tokens r / r+8, columns 2t / 2t+1 =
+      // head t times the hi / lo part of the query.  One accumulation chain
+      // per n-tile for one n-tile, else two (even and odd k-steps): measured
+      // at the Llama-3-8B decode shape, 32K context, 127.2 against 129.2 us;
+      // at the Qwen2.5-3B shape (two n-tiles) 21.4 against 22.1 us.
+      constexpr int kChains = NT == 1 ? 1 : 2;
+      float scr[NT][2][4], sq[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-        for (int i = 0; i < 4; i++) { sa[nt][i] = 0.f; sbk[nt][i] = 0.f; sq[nt][i] = 0.f; }
+        for (int i = 0; i < 4; i++) { scr[nt][0][i] = 0.f; scr[nt][1][i] = 0.f; sq[nt][i] = 0.f; }
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) {
-        uint2 L00, L01, L10, L11;
+        // A operand: the fp16 centroids of code pairs 2kk (k slots 2t, 2t+1)
+        // and 2kk + 1 (slots 2t+8, 2t+9) of token r (A0, A2) and r+8 (A1, A3)
+        uint32_t A0, A1, A2, A3;
         if constexpr (kb_mixed(KB)) {
           // channels 32t + 4kk .. +3 are the 4-code group g of the lane's
           // high stream when kk mod 4 < 2, of its low stream otherwise
           const int g = (kk & 1) + 2 * (kk >> 2);
           if ((kk & 2) == 0) {
-            L00 = lut64(mixed_pair_addr<kb_hi(KB)>(R.k0[0], R.k0[1], 2 * g, laneK));
-            L01 = lut64(mixed_pair_addr<kb_hi(KB)>(R.k0[0], R.k0[1], 2 * g + 1, laneK));
-            L10 = lut64(mixed_pair_addr<kb_hi(KB)>(R.k1[0], R.k1[1], 2 * g, laneK));
-            L11 = lut64(mixed_pair_addr<kb_hi(KB)>(R.k1[0], R.k1[1], 2 * g + 1, laneK));
+            A0 = lut32(mixed_pair_addr<kb_hi(KB)>(R.k0[0], R.k0[1], 2 * g, laneK));
+            A2 = lut32(mixed_pair_addr<kb_hi(KB)>(R.k0[0], R.k0[1], 2 * g + 1, laneK));
+            A1 = lut32(mixed_pair_addr<kb_hi(KB)>(R.k1[0], R.k1[1], 2 * g, laneK));
+            A3 = lut32(mixed_pair_addr<kb_hi(KB)>(R.k1[0], R.k1[1], 2 * g + 1, laneK));
           } else {
-            L00 = lut64(mixed_pair_addr<kb_lo(KB)>(R.k0[2], R.k0[3], 2 * g, laneKL));
-            L01 = lut64(mixed_pair_addr<kb_lo(KB)>(R.k0[2], R.k0[3], 2 * g + 1, laneKL));
-            L10 = lut64(mixed_pair_addr<kb_lo(KB)>(R.k1[2], R.k1[3], 2 * g, laneKL));
-            L11 = lut64(mixed_pair_addr<kb_lo(KB)>(R.k1[2], R.k1[3], 2 * g + 1, laneKL));
+            A0 = lut32(mixed_pair_addr<kb_lo(KB)>(R.k0[2], R.k0[3], 2 * g, laneKL));
+            A2 = lut32(mixed_pair_addr<kb_lo(KB)>(R.k0[2], R.k0[3], 2 * g + 1, laneKL));
+            A1 = lut32(mixed_pair_addr<kb_lo(KB)>(R.k1[2], R.k1[3], 2 * g, laneKL));
+            A3 = lut32(mixed_pair_addr<kb_lo(KB)>(R.k1[2], R.k1[3], 2 * g + 1, laneKL));
           }
-        } else if constexpr (byte_keys<KB>()) {  // byte kk = pairs 2kk (low nibble), 2kk+1: one address, halves 64 KB apart
-          const uint32_t a0 = __byte_perm(R.k0[kk >> 2], laneK, 0x7604 | ((kk & 3) << 4));
-          const uint32_t a1 = __byte_perm(R.k1[kk >> 2], laneK, 0x7604 | ((kk & 3) << 4));
-          L00 = lut64(a0);
-          L01 = lut64(a0 + 65536);
-          L10 = lut64(a1);
-          L11 = lut64(a1 + 65536);
+        } else if constexpr (byte_keys<KB>()) {  // byte kk = pairs 2kk (low nibble), 2kk+1: one 8-byte entry
+          const uint2 L0 = lut64(__byte_perm(R.k0[kk >> 2], laneK, 0x7604 | ((kk & 3) << 4)));
+          const uint2 L1 = lut64(__byte_perm(R.k1[kk >> 2], laneK, 0x7604 | ((kk & 3) << 4)));
+          A0 = L0.x;
+          A2 = L0.y;
+          A1 = L1.x;
+          A3 = L1.y;
         } else {
-          L00 = lut64(key_addr<KB>(R.k0, 2 * kk, laneK));
-          L01 = lut64(key_addr<KB>(R.k0, 2 * kk + 1, laneK));
-          L10 = lut64(key_addr<KB>(R.k1, 2 * kk, laneK));
-          L11 = lut64(key_addr<KB>(R.k1, 2 * kk + 1, laneK));
+          A0 = lut32(key_addr<KB>(R.k0, 2 * kk, laneK));
+          A2 = lut32(key_addr<KB>(R.k0, 2 * kk + 1, laneK));
+          A1 = lut32(key_addr<KB>(R.k1, 2 * kk, laneK));
+          A3 = lut32(key_addr<KB>(R.k1, 2 * kk + 1, laneK));
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++) {
-          mma_16816(sa[nt], L00.x, L00.y, L01.x, L01.y, qb[nt][kk][0], qb[nt][kk][1]);
-          mma_16816(sbk[nt], L10.x, L10.y, L11.x, L11.y, qb[nt][kk][0], qb[nt][kk][1]);
-        }
+        for (int nt = 0; nt < NT; nt++) mma_16816(scr[nt][kChains == 1 ? 0 : (kk & 1)], A0, A1, A2, A3, qb[nt][kk][0], qb[nt][kk][1]);
         if constexpr (QJL) {
           const uint32_t a0 = sign_pair(R.s0, 2 * kk), a1 = sign_pair(R.s1, 2 * kk);
           const uint32_t a2 = sign_pair(R.s0, 2 * kk + 1), a3 = sign_pair(R.s1, 2 * kk + 1);
@@ -629,8 +648,12 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
       bool big = vn0 > kLazyNu * nu || vn1 > kLazyNu * nu;
 #pragma unroll
       for (int nt = 0; nt < NT; nt++) {
-        float l0 = ((sa[nt][0] + sa[nt][1]) + (sa[nt][2] + sa[nt][3])) * cK[nt];
-        float l1 = ((sbk[nt][0] + sbk[nt][1]) + (sbk[nt][2] + sbk[nt][3])) * cK[nt];
+        float l0 = (scr[nt][0][0] + scr[nt][0][1]) * cK[nt];
+        float l1 = (scr[nt][0][2] + scr[nt][0][3]) * cK[nt];
+        if constexpr (kChains == 2) {
+          l0 = fmaf(scr[nt][1][0] + scr[nt][1][1], cK[nt], l0);
+          l1 = fmaf(scr[nt][1][2] + scr[nt][1][3], cK[nt], l1);
+        }
         if constexpr (QJL) {
           l0 = fmaf(R.g0 * (sq[nt][0] + sq[nt][1]), cQ[nt], l0);
           l1 = fmaf(R.g1 * (sq[nt][2] + sq[nt][3]), cQ[nt], l1);
