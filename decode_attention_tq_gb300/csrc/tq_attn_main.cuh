@@ -270,8 +270,13 @@ struct TileCursor {
   const uint8_t *slab;
   bool page_ok;
 
-  __device__ __forceinline__ void enter_page(int32_t *err_word, bool reporter) {
-    int32_t page = __ldg(btrow + pidx);
+  __device__ __forceinline__ int live() const { return page_ok ? clen - tok0 : 0; }
+  // Block-table entries of the next two pages, loaded a page ahead of use, so
+  // that neither the page switch nor the L2 prefetch of the next page waits
+  // on a block-table load.
+  int last_page;
+  int32_t pg_next, pg_ahead;  // entries of pages pidx + 1, pidx + 2 (0 past last_page)
+  __device__ __forceinline__ void set_page(int32_t page, int32_t *err_word, bool reporter) {
     page_ok = page >= 0 && (int64_t)page < num_pages;
     if (!page_ok) {
       if (reporter) report(err_word, TQ_DEVERR_PAGE_RANGE);
@@ -279,11 +284,34 @@ struct TileCursor {
     }
     slab = pool + (int64_t)page * page_bytes + slab_off;
   }
-  __device__ __forceinline__ const uint8_t *slab_of(int pi) const {
-    const int32_t page = __ldg(btrow + pi);
+  __device__ __forceinline__ const uint8_t *slab_if_valid(int32_t page) const {
     return (page >= 0 && (int64_t)page < num_pages) ? pool + (int64_t)page * page_bytes + slab_off : nullptr;
   }
-  __device__ __forceinline__ int live() const { return page_ok ? clen - tok0 : 0; }
+  // first page of a segment (pidx, last_page set); lane 0 stages it and the
+  // next one in L2
+  __device__ __forceinline__ void begin(int32_t *err_word, bool lane0, uint32_t slab_bytes) {
+    const int32_t page = __ldg(btrow + pidx);
+    pg_next = pidx + 1 <= last_page ? __ldg(btrow + pidx + 1) : 0;
+    pg_ahead = pidx + 2 <= last_page ? __ldg(btrow + pidx + 2) : 0;
+    set_page(page, err_word, lane0);
+    if (lane0) {
+      if (page_ok) prefetch_l2(slab, slab_bytes);
+      const uint8_t *sp = pidx + 1 <= last_page ? slab_if_valid(pg_next) : nullptr;
+      if (sp) prefetch_l2(sp, slab_bytes);
+    }
+  }
+  // the next tile; at a page switch lane 0 stages the page after it in L2
+  __device__ __forceinline__ void step(int32_t *err_word, bool lane0, uint32_t slab_bytes) {
+    if (!advance()) return;
+    const int32_t page = pg_next;
+    pg_next = pg_ahead;
+    pg_ahead = pidx + 2 <= last_page ? __ldg(btrow + pidx + 2) : 0;
+    set_page(page, err_word, lane0);
+    if (lane0 && pidx + 1 <= last_page) {
+      const uint8_t *sp = slab_if_valid(pg_next);
+      if (sp) prefetch_l2(sp, slab_bytes);
+    }
+  }
   __device__ __forceinline__ bool advance() {  // true when a new page starts
     tok0 += 16;
     o0 += 16;
@@ -317,10 +345,17 @@ template <int KB>
 __host__ __device__ constexpr bool keys_in_flight() {
   return !kb_mixed(KB);
 }
+// The whole next tile in flight (values too) for 2-bit keys and values:
+// measured at the long-context shape (K2+QJL/V2, 128K) 159.8 against
+// 172.2 us per launch; at the Llama-3-8B K4/V4 shape 131.1 against 127.0.
+template <int KB, int VB>
+__host__ __device__ constexpr bool values_in_flight() {
+  return KB == 2 && VB == 2;
+}
 
-// Pages of a segment staged in L2 ahead of the page being read (0 and 2
-// measured slower at the Llama-3-8B decode shape).
-constexpr int kL2Ahead = 1;
+// Pages of a segment are staged in L2 one page ahead of the page being read
+// (no prefetch, and two pages ahead, measured slower at the Llama-3-8B decode
+// shape).
 
 // Shared-memory placement of the centroid tables, as offsets from the start
 // of dynamic shared memory.  Rows of 256 bytes indexed by a code pair (or a
@@ -570,16 +605,8 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
     cur.o0 = (j - cur.pidx * tpp) * 16;
     cur.tok0 = j * 16;
     cur.clen = a.clen[b];
-    const int last_page = (j + seg_tiles - 1) / tpp;
-    if (lane == 0) {  // stage the first pages of the segment in L2
-#pragma unroll
-      for (int d = 0; d <= kL2Ahead; d++)
-        if (cur.pidx + d <= last_page) {
-          const uint8_t *sp = cur.slab_of(cur.pidx + d);
-          if (sp) prefetch_l2(sp, slab_bytes);
-        }
-    }
-    cur.enter_page(a.err_word, lane == 0);
+    cur.last_page = (j + seg_tiles - 1) / tpp;
+    cur.begin(a.err_word, lane == 0, slab_bytes);
 
     auto process = [&](const KeyRegs<KB, QJL> &R, const ValRegs<VB> &V) {
       if (!__any_sync(0xffffffffu, R.ok0)) return;  // token 0 of a tile is live iff any is
@@ -827,22 +854,35 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
       }
     };
 
-    // next tile position: stage the page kL2Ahead ahead whenever a page starts
-    auto step_cursor = [&]() {
-      if (cur.advance()) {
-        cur.enter_page(a.err_word, lane == 0);
-        if (lane == 0 && cur.pidx + kL2Ahead <= last_page) {
-          const uint8_t *sp = cur.slab_of(cur.pidx + kL2Ahead);
-          if (sp) prefetch_l2(sp, slab_bytes);
-        }
-      }
-    };
+    auto step_cursor = [&]() { cur.step(a.err_word, lane == 0, slab_bytes); };
 
     using KR = KeyRegs<KB, QJL>;
     using VR = ValRegs<VB>;
     auto keys = [&](KR &R) { load_keys<KB, QJL>(a, cur.slab, cur.o0, cur.live(), r, t, R); };
     auto vals = [&](VR &R) { load_values<VB>(a, cur.slab, cur.o0, r, t, R); };
-    if constexpr (keys_in_flight<KB>()) {
+    if constexpr (values_in_flight<KB, VB>()) {
+      // the whole next tile one tile ahead (ping-pong)
+      KR ka, kb;
+      VR va, vb;
+      keys(ka);
+      vals(va);
+      for (int k = 0;;) {
+        if (k + 1 < seg_tiles) {
+          step_cursor();
+          keys(kb);
+          vals(vb);
+        }
+        process(ka, va);
+        if (++k == seg_tiles) break;
+        if (k + 1 < seg_tiles) {
+          step_cursor();
+          keys(ka);
+          vals(va);
+        }
+        process(kb, vb);
+        if (++k == seg_tiles) break;
+      }
+    } else if constexpr (keys_in_flight<KB>()) {
       // keys one tile ahead (ping-pong ka / kb), values at the tile itself
       KR ka, kb;
       VR v;
