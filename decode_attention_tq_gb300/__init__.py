@@ -24,6 +24,12 @@ from .tq import (  # noqa: F401
     tq_encode_kv,
     tq_append_window,
     tq_append_window_workspace_size,
+    tq_kivi_decode,
+    tq_kivi_decode_attn,
+    tq_kivi_decode_attn_workspace_size,
+    tq_kivi_encode_keys,
+    tq_kivi_encode_values,
+    tq_kivi_page_layout,
     tq_make_codebook,
     tq_page_layout,
     tq_status_string,

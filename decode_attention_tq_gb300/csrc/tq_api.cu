@@ -153,8 +153,10 @@ cudaError_t main_kernel_call(const tq_format *f, const AttnArgs &a, int nt, bool
 // Occupancy of each main-kernel instance, per device (queried once).
 std::mutex g_occ_mu;
 int g_occ[64][5][3][2][2];  // [device][key widths][vb-2][qjl][nt-1]; 0 = unknown
+int g_occ_kivi[64][5][3][2];  // KIVI main kernel: [device][kb-2][vb-2][nt-1]
 
-tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int window, AttnPlan *p) {
+tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int window, AttnPlan *p,
+                         bool kivi = false) {
   const int H = f->num_kv_heads;
   p->G = Hq / H;
   p->NT = p->G <= 4 ? 1 : 2;
@@ -164,21 +166,25 @@ tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int w
   int bps = 0;
   {
     std::lock_guard<std::mutex> lk(g_occ_mu);
-    const int kw = f->k_mixed ? 3 + (f->k_bits - 2) : f->k_bits - 2;  // 2, 3, 4, then 2.5, 3.5
-    int *slot = dev < 64 ? &g_occ[dev][kw][f->v_bits - 2][f->k_qjl][p->NT - 1] : nullptr;
+    // key kinds 2, 3, 4, then 2.5, 3.5; KIVI keys in the QJL slot of kinds 2 and 4
+    const int kw = f->k_mixed ? 3 + (f->k_bits - 2) : f->k_bits - 2;
+    int *slot = dev < 64 ? &g_occ[dev][kw][f->v_bits - 2][kivi ? 1 : f->k_qjl][p->NT - 1] : nullptr;
+    if (kivi && slot) slot = &g_occ_kivi[dev][kw][f->v_bits - 2][p->NT - 1];
     if (slot && *slot > 0) {
       bps = *slot;
     } else {
       AttnArgs dummy;
       memset(&dummy, 0, sizeof(dummy));
-      if (main_kernel_call(f, dummy, p->NT, true, &bps, 0, 0) != cudaSuccess) return TQ_ERR_CUDA;
+      const cudaError_t e = kivi ? kivi_main(dummy, f->k_bits, f->v_bits, p->NT, true, &bps, 0, 0)
+                                 : main_kernel_call(f, dummy, p->NT, true, &bps, 0, 0);
+      if (e != cudaSuccess) return TQ_ERR_CUDA;
       if (bps < 1) bps = 1;
       if (slot) *slot = bps;
     }
   }
   const int64_t tiles_max = (int64_t)B * H * max_pages * (f->page_size / kTile);
   int64_t warps = (tiles_max + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
-  const int wpb = attn_warps(p->NT, f->k_qjl != 0);
+  const int wpb = kivi ? kivi_threads(p->NT) / 32 : attn_warps(p->NT, f->k_qjl != 0);
   const int64_t cap = (int64_t)sms * bps * wpb;
   if (warps > cap) warps = cap;
   if (warps < 1) warps = 1;
@@ -560,6 +566,238 @@ tq_status tq_decode_attn_timed(const tq_format *fmt, int batch, int num_q_heads,
                           k_win_f16, v_win_f16, win_lens, window, k_signs, v_signs, k_codebook, v_codebook, S, out,
                           workspace, workspace_bytes, err_word, static_cast<cudaEvent_t>(main_begin_event),
                           static_cast<cudaEvent_t>(main_end_event), stream);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ KIVI --
+static bool kivi_format_valid(const tq_kivi_format *f) {
+  if (!f) return false;
+  const int d = f->head_dim;
+  if (d < 16 || d > 256 || d % 16 || f->page_size < 16 || f->page_size % 16 || f->num_kv_heads < 1) return false;
+  if (f->k_bits < 1 || f->k_bits > 8 || f->v_bits < 1 || f->v_bits > 8) return false;
+  return true;
+}
+static bool kivi_gpu_supported(const tq_kivi_format *f) {
+  return f->head_dim == kD && (f->k_bits == 2 || f->k_bits == 4) && (f->v_bits == 2 || f->v_bits == 4);
+}
+static void kivi_layout(const tq_kivi_format *f, tq_kivi_layout *L) {
+  const int64_t d = f->head_dim, P = f->page_size;
+  L->k_code_bytes = (int32_t)(d * f->k_bits / 8);
+  L->v_code_bytes = (int32_t)(d * f->v_bits / 8);
+  int64_t c = 0;
+  L->k_params = c;
+  c = round16(c + 4 * d);  // (scale, zero) fp16 pairs per channel
+  L->k_codes = c;
+  c = round16(c + P * L->k_code_bytes);
+  L->v_params = c;
+  c = round16(c + 4 * P);  // (scale, zero) fp16 pairs per token
+  L->v_codes = c;
+  c = round16(c + P * L->v_code_bytes);
+  L->slab_bytes = c;
+  L->page_bytes = c * f->num_kv_heads;
+}
+// The planner's view of a KIVI format (no QJL, no mixed rates).
+static tq_format kivi_as_format(const tq_kivi_format *f) {
+  tq_format g;
+  memset(&g, 0, sizeof(g));
+  g.head_dim = f->head_dim;
+  g.k_bits = f->k_bits;
+  g.v_bits = f->v_bits;
+  g.page_size = f->page_size;
+  g.num_kv_heads = f->num_kv_heads;
+  return g;
+}
+
+static tq_status kivi_attn_impl(const tq_kivi_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                                const void *page_pool, int64_t num_pages, const int32_t *block_tables, int max_pages,
+                                const int32_t *comp_lens, const void *k_win_f16, const void *v_win_f16,
+                                const int32_t *win_lens, int window, float *out, void *workspace,
+                                size_t workspace_bytes, int32_t *err_word, cudaEvent_t ev_begin, cudaEvent_t ev_end,
+                                void *stream) {
+  if (!kivi_format_valid(fmt) || batch < 1 || num_q_heads < 1 || max_pages < 1 || window < 0 ||
+      num_q_heads % fmt->num_kv_heads)
+    return TQ_ERR_INVALID_ARG;
+  if (!kivi_gpu_supported(fmt) || num_q_heads / fmt->num_kv_heads > 8) return TQ_ERR_UNSUPPORTED;
+  if (num_pages < 1 || !q_f16 || !page_pool || !block_tables || !comp_lens || !out || !workspace)
+    return TQ_ERR_INVALID_ARG;
+  if (window > 0 && (!k_win_f16 || !v_win_f16 || !win_lens)) return TQ_ERR_INVALID_ARG;
+  if (!aligned(q_f16, 8) || !aligned(page_pool, 32) || !aligned(workspace, 256) || !aligned(out, 4) ||
+      (window > 0 && (!aligned(k_win_f16, 16) || !aligned(v_win_f16, 16))))
+    return TQ_ERR_INVALID_ARG;
+  const tq_format pf = kivi_as_format(fmt);
+  AttnPlan p;
+  tq_status s = plan_attention(&pf, batch, num_q_heads, max_pages, window, &p, true);
+  if (s != TQ_OK) return s;
+  if (workspace_bytes < p.total) return TQ_ERR_WORKSPACE;
+  tq_kivi_layout L;
+  kivi_layout(fmt, &L);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.pool = static_cast<const uint8_t *>(page_pool);
+  a.num_pages = num_pages;
+  a.page_bytes = L.page_bytes;
+  a.slab_bytes = L.slab_bytes;
+  a.k_norm_o = L.k_params;  // (scale, zero) sections in the norm slots
+  a.k_codes_o = L.k_codes;
+  a.v_norm_o = L.v_params;
+  a.v_codes_o = L.v_codes;
+  a.k_code_bytes = L.k_code_bytes;
+  a.v_code_bytes = L.v_code_bytes;
+  a.B = batch;
+  a.Hq = num_q_heads;
+  a.H = fmt->num_kv_heads;
+  a.G = p.G;
+  a.P = fmt->page_size;
+  a.max_pages = max_pages;
+  a.window = window;
+  a.block_tables = block_tables;
+  a.comp_lens = comp_lens;
+  a.q = static_cast<const __half *>(q_f16);
+  a.k_win = static_cast<const __half *>(k_win_f16);
+  a.v_win = static_cast<const __half *>(v_win_f16);
+  a.win_lens = win_lens;
+  a.out = out;
+  a.err_word = err_word;
+  a.hdr = reinterpret_cast<AttnHeader *>(ws + p.off_hdr);
+  a.pre = reinterpret_cast<int64_t *>(ws + p.off_pre);
+  a.clen = reinterpret_cast<int32_t *>(ws + p.off_clen);
+  a.wlen = reinterpret_cast<int32_t *>(ws + p.off_wlen);
+  a.q_rot = reinterpret_cast<float *>(ws + p.off_qrot);
+  a.q_s = reinterpret_cast<float *>(ws + p.off_qs);
+  a.q_exp = reinterpret_cast<int32_t *>(ws + p.off_qexp);
+  a.seg_ml = reinterpret_cast<float *>(ws + p.off_segml);
+  a.seg_acc = reinterpret_cast<float *>(ws + p.off_segacc);
+  a.win_ml = reinterpret_cast<float *>(ws + p.off_winml);
+  a.win_acc = reinterpret_cast<float *>(ws + p.off_winacc);
+  a.nw_launch = p.nw_launch;
+  a.min_tiles = kMinTilesPerWarp;
+  a.pdl = ev_begin == nullptr && ev_end == nullptr;
+  a.raw = true;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_attn_prep(a, false, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (ev_begin && cudaEventRecord(ev_begin, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (kivi_main(a, fmt->k_bits, fmt->v_bits, p.NT, false, nullptr, p.blocks, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (ev_end && cudaEventRecord(ev_end, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (launch_attn_merge(a, st) != cudaSuccess) return TQ_ERR_CUDA;
+  return TQ_OK;
+}
+
+extern "C" {
+
+tq_status tq_kivi_page_layout(const tq_kivi_format *fmt, tq_kivi_layout *out) {
+  if (!kivi_format_valid(fmt) || !out) return TQ_ERR_INVALID_ARG;
+  kivi_layout(fmt, out);
+  return TQ_OK;
+}
+
+static tq_status kivi_encode(const tq_kivi_format *fmt, int kind, const void *x_f16, int64_t n_tokens,
+                             const int32_t *map, void *page_pool, int64_t num_pages, int32_t *err_word,
+                             void *stream) {
+  if (!kivi_format_valid(fmt) || n_tokens < 0 || num_pages < 1) return TQ_ERR_INVALID_ARG;
+  if (!kivi_gpu_supported(fmt)) return TQ_ERR_UNSUPPORTED;
+  if (!x_f16 || !map || !page_pool) return TQ_ERR_INVALID_ARG;
+  if (!aligned(x_f16, 16) || !aligned(page_pool, 16) || !aligned(map, 4)) return TQ_ERR_INVALID_ARG;
+  if (n_tokens == 0) return TQ_OK;
+  tq_kivi_layout L;
+  kivi_layout(fmt, &L);
+  KiviEncodeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = static_cast<const __half *>(x_f16);
+  a.n_tokens = n_tokens;
+  a.H = fmt->num_kv_heads;
+  a.P = fmt->page_size;
+  a.page_ids = kind == TQ_KIND_K ? map : nullptr;
+  a.slot_mapping = kind == TQ_KIND_V ? map : nullptr;
+  a.pool = static_cast<uint8_t *>(page_pool);
+  a.num_pages = num_pages;
+  a.page_bytes = L.page_bytes;
+  a.slab_bytes = L.slab_bytes;
+  a.params_off = kind == TQ_KIND_K ? L.k_params : L.v_params;
+  a.codes_off = kind == TQ_KIND_K ? L.k_codes : L.v_codes;
+  a.err_word = err_word;
+  return launch_kivi_encode(a, kind, kind == TQ_KIND_K ? fmt->k_bits : fmt->v_bits, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? TQ_OK
+             : TQ_ERR_CUDA;
+}
+
+tq_status tq_kivi_encode_keys(const tq_kivi_format *fmt, const void *k_f16, int64_t n_tokens, const int32_t *page_ids,
+                              void *page_pool, int64_t num_pages, int32_t *err_word, void *stream) {
+  return kivi_encode(fmt, TQ_KIND_K, k_f16, n_tokens, page_ids, page_pool, num_pages, err_word, stream);
+}
+
+tq_status tq_kivi_encode_values(const tq_kivi_format *fmt, const void *v_f16, int64_t n_tokens,
+                                const int32_t *slot_mapping, void *page_pool, int64_t num_pages, int32_t *err_word,
+                                void *stream) {
+  return kivi_encode(fmt, TQ_KIND_V, v_f16, n_tokens, slot_mapping, page_pool, num_pages, err_word, stream);
+}
+
+tq_status tq_kivi_decode(const tq_kivi_format *fmt, int kind, const void *page_pool, int64_t num_pages,
+                         const int32_t *slot_mapping, int64_t n_tokens, float *out, int32_t *err_word, void *stream) {
+  if (!kivi_format_valid(fmt) || (kind != TQ_KIND_K && kind != TQ_KIND_V) || n_tokens < 0 || num_pages < 1)
+    return TQ_ERR_INVALID_ARG;
+  if (!kivi_gpu_supported(fmt)) return TQ_ERR_UNSUPPORTED;
+  if (!page_pool || !slot_mapping || !out) return TQ_ERR_INVALID_ARG;
+  if (!aligned(page_pool, 16) || !aligned(out, 16)) return TQ_ERR_INVALID_ARG;
+  if (n_tokens == 0) return TQ_OK;
+  tq_kivi_layout L;
+  kivi_layout(fmt, &L);
+  KiviDecodeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.pool = static_cast<const uint8_t *>(page_pool);
+  a.n_tokens = n_tokens;
+  a.H = fmt->num_kv_heads;
+  a.P = fmt->page_size;
+  a.kind = kind;
+  a.slot_mapping = slot_mapping;
+  a.num_pages = num_pages;
+  a.page_bytes = L.page_bytes;
+  a.slab_bytes = L.slab_bytes;
+  a.params_off = kind == TQ_KIND_K ? L.k_params : L.v_params;
+  a.codes_off = kind == TQ_KIND_K ? L.k_codes : L.v_codes;
+  a.out = out;
+  a.err_word = err_word;
+  return launch_kivi_decode(a, kind == TQ_KIND_K ? fmt->k_bits : fmt->v_bits, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? TQ_OK
+             : TQ_ERR_CUDA;
+}
+
+tq_status tq_kivi_decode_attn_workspace_size(const tq_kivi_format *fmt, int batch, int num_q_heads, int max_pages,
+                                             int window, size_t *bytes) {
+  if (!bytes || !kivi_format_valid(fmt) || batch < 1 || num_q_heads < 1 || max_pages < 1 || window < 0 ||
+      num_q_heads % fmt->num_kv_heads)
+    return TQ_ERR_INVALID_ARG;
+  if (!kivi_gpu_supported(fmt) || num_q_heads / fmt->num_kv_heads > 8) return TQ_ERR_UNSUPPORTED;
+  const tq_format pf = kivi_as_format(fmt);
+  AttnPlan p;
+  const tq_status s = plan_attention(&pf, batch, num_q_heads, max_pages, window, &p, true);
+  if (s != TQ_OK) return s;
+  *bytes = p.total;
+  return TQ_OK;
+}
+
+tq_status tq_kivi_decode_attn(const tq_kivi_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                              const void *page_pool, int64_t num_pages, const int32_t *block_tables, int max_pages,
+                              const int32_t *comp_lens, const void *k_win_f16, const void *v_win_f16,
+                              const int32_t *win_lens, int window, float *out, void *workspace, size_t workspace_bytes,
+                              int32_t *err_word, void *stream) {
+  return kivi_attn_impl(fmt, batch, num_q_heads, q_f16, page_pool, num_pages, block_tables, max_pages, comp_lens,
+                        k_win_f16, v_win_f16, win_lens, window, out, workspace, workspace_bytes, err_word, nullptr,
+                        nullptr, stream);
+}
+
+tq_status tq_kivi_decode_attn_timed(const tq_kivi_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                                    const void *page_pool, int64_t num_pages, const int32_t *block_tables,
+                                    int max_pages, const int32_t *comp_lens, const void *k_win_f16,
+                                    const void *v_win_f16, const int32_t *win_lens, int window, float *out,
+                                    void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                    void *main_begin_event, void *main_end_event, void *stream) {
+  return kivi_attn_impl(fmt, batch, num_q_heads, q_f16, page_pool, num_pages, block_tables, max_pages, comp_lens,
+                        k_win_f16, v_win_f16, win_lens, window, out, workspace, workspace_bytes, err_word,
+                        static_cast<cudaEvent_t>(main_begin_event), static_cast<cudaEvent_t>(main_end_event), stream);
 }
 
 }  // extern "C"

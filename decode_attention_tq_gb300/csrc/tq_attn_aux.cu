@@ -66,18 +66,19 @@ __device__ void prep_query(const AttnArgs &a, bool qjl, int64_t row, int lane, f
   const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
   const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
   float x[4] = {f01.x, f01.y, f23.x, f23.y};
+  if (!a.raw) {  // a raw-domain (KIVI) cache takes the query as it is
 #pragma unroll
-  for (int i = 0; i < 4; i++)
-    if (a.k_signs[4 * lane + i]) x[i] = -x[i];
-  fwht_local<4>(x);
+    for (int i = 0; i < 4; i++)
+      if (a.k_signs[4 * lane + i]) x[i] = -x[i];
+    fwht_local<4>(x);
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) fwht_xlane<4>(x, m, (lane & m) != 0);
+    for (int m = 1; m < 32; m <<= 1) fwht_xlane<4>(x, m, (lane & m) != 0);
+#pragma unroll
+    for (int i = 0; i < 4; i++) x[i] *= 0.08838834764831845f;  // 1/sqrt(128)
+  }
   float mx = 0.f;
 #pragma unroll
-  for (int i = 0; i < 4; i++) {
-    x[i] *= 0.08838834764831845f;  // 1/sqrt(128)
-    mx = fmaxf(mx, fabsf(x[i]));
-  }
+  for (int i = 0; i < 4; i++) mx = fmaxf(mx, fabsf(x[i]));
   *reinterpret_cast<float4 *>(a.q_rot + row * kD + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
   mx = warp_max_xor(mx, 31);
   // largest |value| lands in [2^12, 2^13) after scaling by 2^e
@@ -347,21 +348,24 @@ __global__ void __launch_bounds__(128) attn_merge_block_kernel(const AttnArgs a)
         [&](int64_t k) { return a.seg_acc + ((w0 + k + unit) * a.G + g) * kD; }, mu, l, A, s_w, s_red);
   }
   // inverse rotation of the rotated-domain accumulator: D_V . (H A) / d
+  // (a raw-domain KIVI accumulator is used as it is)
   float x = A;
+  if (!a.raw) {
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const float o = __shfl_xor_sync(0xffffffffu, x, m);
-    x = (j & m) ? (o - x) : (x + o);
-  }
+    for (int m = 1; m < 32; m <<= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, x, m);
+      x = (j & m) ? (o - x) : (x + o);
+    }
 #pragma unroll
-  for (int m = 32; m < kD; m <<= 1) {
-    s_x[j] = x;
-    __syncthreads();
-    const float o = s_x[j ^ m];
-    __syncthreads();
-    x = (j & m) ? (o - x) : (x + o);
+    for (int m = 32; m < kD; m <<= 1) {
+      s_x[j] = x;
+      __syncthreads();
+      const float o = s_x[j ^ m];
+      __syncthreads();
+      x = (j & m) ? (o - x) : (x + o);
+    }
+    x = (a.v_signs[j] ? -x : x) * (1.0f / (float)kD);
   }
-  x = (a.v_signs[j] ? -x : x) * (1.0f / (float)kD);
 
   // window partials (raw domain): merged onto the compressed part
   float M = mu, Lt = l, At = x;
@@ -487,13 +491,16 @@ __global__ void __launch_bounds__(128) attn_merge_warp_kernel(const AttnArgs a) 
         [&](int64_t k) { return a.seg_acc + ((w0 + k + unit) * a.G + g) * kD; }, M, L, A, lane);
   }
   // inverse rotation of the rotated-domain accumulator: D_V . (H A) / d
-  float x[4] = {A.x, A.y, A.z, A.w};
-  fwht_local<4>(x);
+  // (a raw-domain KIVI accumulator is used as it is)
+  if (!a.raw) {
+    float x[4] = {A.x, A.y, A.z, A.w};
+    fwht_local<4>(x);
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) fwht_xlane<4>(x, m, (lane & m) != 0);
+    for (int m = 1; m < 32; m <<= 1) fwht_xlane<4>(x, m, (lane & m) != 0);
 #pragma unroll
-  for (int i = 0; i < 4; i++) x[i] = (a.v_signs[4 * lane + i] ? -x[i] : x[i]) * (1.0f / (float)kD);
-  A = make_float4(x[0], x[1], x[2], x[3]);
+    for (int i = 0; i < 4; i++) x[i] = (a.v_signs[4 * lane + i] ? -x[i] : x[i]) * (1.0f / (float)kD);
+    A = make_float4(x[0], x[1], x[2], x[3]);
+  }
 
   // window partials (raw domain), merged onto the compressed part
   if (nwin > 0 && nwin <= kWinPre) {

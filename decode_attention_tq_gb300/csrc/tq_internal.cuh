@@ -108,7 +108,40 @@ struct AttnArgs {
   int nw_launch;     // warps launched for the main kernel
   int min_tiles;     // fewest tiles a warp is given
   bool pdl;          // host: launch main and merge as programmatic dependents
+  bool raw;          // KIVI cache: no query rotation, the accumulators are raw-domain
 };
+
+// KIVI-style control arm (tq_kivi.cu): encode of keys (per-channel groups of
+// one page) or values (per token), and reconstruction for tests.  Section
+// offsets are those of tq_kivi_layout for the kind.
+struct KiviEncodeArgs {
+  const __half *x;             // [N][H][d]
+  int64_t n_tokens;
+  int H, P;
+  const int32_t *page_ids;     // keys: [ceil(N / P)]
+  const int32_t *slot_mapping; // values: [N]
+  uint8_t *pool;
+  int64_t num_pages, page_bytes, slab_bytes;
+  int64_t params_off, codes_off;
+  int32_t *err_word;
+};
+struct KiviDecodeArgs {
+  const uint8_t *pool;
+  int64_t n_tokens;
+  int H, P, kind;
+  const int32_t *slot_mapping;
+  int64_t num_pages, page_bytes, slab_bytes;
+  int64_t params_off, codes_off;
+  float *out;
+  int32_t *err_word;
+};
+cudaError_t launch_kivi_encode(const KiviEncodeArgs &a, int kind, int bits, cudaStream_t st);
+cudaError_t launch_kivi_decode(const KiviDecodeArgs &a, int bits, cudaStream_t st);
+// KIVI main attention kernel (AttnArgs with raw = true; k_norm_o / v_norm_o
+// hold the K and V (scale, zero) sections)
+cudaError_t kivi_main(const AttnArgs &a, int k_bits, int v_bits, int nt, bool query_only, int *blocks_per_sm,
+                      int blocks, cudaStream_t st);
+__host__ __device__ constexpr int kivi_threads(int nt) { return nt == 1 ? 512 : 256; }
 
 cudaError_t launch_encode(const EncodeArgs &a, int bits, bool qjl, bool mixed, int sms, cudaStream_t st);
 // One launch: window roll, encode of the staged keys and values, counters.

@@ -40,6 +40,16 @@ class tq_format(C.Structure):
                                          "norm_correct")] + [("qjl_scale", C.c_float), ("k_mixed", C.c_int32)]
 
 
+class tq_kivi_format(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("head_dim", "k_bits", "v_bits", "page_size", "num_kv_heads")]
+
+
+class tq_kivi_layout(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("slab_bytes", "page_bytes", "k_params", "k_codes", "v_params", "v_codes")] + [
+        (n, C.c_int32) for n in ("k_code_bytes", "v_code_bytes")
+    ]
+
+
 class tq_layout(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("slab_bytes", "page_bytes", "k_norm", "k_gamma", "k_codes", "k_signs", "v_norm", "v_codes")] + [
         (n, C.c_int32) for n in ("k_code_bytes", "k_sign_bytes", "v_code_bytes")
@@ -72,8 +82,17 @@ def load_library():
             lib.tq_decode_attn.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P]
             lib.tq_decode_attn_timed.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P, P, P, P]
             lib.tq_decode_attn_static.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, P]
+            lib.tq_kivi_page_layout.argtypes = [P, P]
+            lib.tq_kivi_encode_keys.argtypes = [P, P, i64, P, P, i64, P, P]
+            lib.tq_kivi_encode_values.argtypes = [P, P, i64, P, P, i64, P, P]
+            lib.tq_kivi_decode.argtypes = [P, i32, P, i64, P, i64, P, P, P]
+            lib.tq_kivi_decode_attn_workspace_size.argtypes = [P, i32, i32, i32, i32, C.POINTER(sz)]
+            lib.tq_kivi_decode_attn.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, sz, P, P]
+            lib.tq_kivi_decode_attn_timed.argtypes = [P, i32, i32, P, P, i64, P, i32, P, P, P, P, i32, P, P, sz, P, P, P, P]
             for f in ("tq_make_codebook", "tq_page_layout", "tq_encode", "tq_encode_kv", "tq_append_window_workspace_size", "tq_append_window", "tq_decode", "tq_decode_attn_workspace_size", "tq_decode_attn",
-                      "tq_decode_attn_timed", "tq_decode_attn_static"):
+                      "tq_decode_attn_timed", "tq_decode_attn_static", "tq_kivi_page_layout", "tq_kivi_encode_keys",
+                      "tq_kivi_encode_values", "tq_kivi_decode", "tq_kivi_decode_attn_workspace_size", "tq_kivi_decode_attn",
+                      "tq_kivi_decode_attn_timed"):
                 getattr(lib, f).restype = C.c_int
             _lib = lib
     return _lib
@@ -310,4 +329,89 @@ def _decode_attn(fmt, q, page_pool, num_pages, block_tables, comp_lens, k_win, v
             _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), *extra, _stream(stream),
         )
     _check(rc, "tq_decode_attn" if events is None else "tq_decode_attn_timed")
+    return out
+
+
+
+# ------------------------------------------------------------------ KIVI --
+def _kfmt(f) -> tq_kivi_format:
+    if isinstance(f, tq_kivi_format):
+        return f
+    g = (lambda k: f.get(k, 0)) if isinstance(f, dict) else (lambda k: getattr(f, k, 0))
+    return tq_kivi_format(*(int(g(n)) for n, _ in tq_kivi_format._fields_))
+
+
+def tq_kivi_page_layout(fmt) -> dict:
+    L = tq_kivi_layout()
+    F = _kfmt(fmt)
+    _check(load_library().tq_kivi_page_layout(C.byref(F), C.byref(L)), "tq_kivi_page_layout")
+    return {n: getattr(L, n) for n, _ in tq_kivi_layout._fields_}
+
+
+def tq_kivi_encode_keys(fmt, x, page_ids, page_pool, num_pages: int, err_word=None, stream=None):
+    """Keys x [N][H][d] fp16 in token order into pages page_ids[n // P]."""
+    F = _kfmt(fmt)
+    with torch.cuda.device(_device(x, page_ids, page_pool, err_word)):
+        rc = load_library().tq_kivi_encode_keys(
+            C.byref(F), _dev_ptr(x, torch.float16, "x"), int(x.shape[0]), _dev_ptr(page_ids, torch.int32, "page_ids"),
+            _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(err_word, torch.int32, "err_word", allow_none=True),
+            _stream(stream),
+        )
+    _check(rc, "tq_kivi_encode_keys")
+
+
+def tq_kivi_encode_values(fmt, x, slot_mapping, page_pool, num_pages: int, err_word=None, stream=None):
+    F = _kfmt(fmt)
+    with torch.cuda.device(_device(x, slot_mapping, page_pool, err_word)):
+        rc = load_library().tq_kivi_encode_values(
+            C.byref(F), _dev_ptr(x, torch.float16, "x"), int(x.shape[0]), _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
+            _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages), _dev_ptr(err_word, torch.int32, "err_word", allow_none=True),
+            _stream(stream),
+        )
+    _check(rc, "tq_kivi_encode_values")
+
+
+def tq_kivi_decode(fmt, kind: int, page_pool, num_pages: int, slot_mapping, out=None, err_word=None, stream=None):
+    F = _kfmt(fmt)
+    n = int(slot_mapping.shape[0])
+    if out is None:
+        out = torch.empty((n, F.num_kv_heads, F.head_dim), dtype=torch.float32, device=slot_mapping.device)
+    with torch.cuda.device(_device(page_pool, slot_mapping, out, err_word)):
+        rc = load_library().tq_kivi_decode(
+            C.byref(F), int(kind), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
+            _dev_ptr(slot_mapping, torch.int32, "slot_mapping"), n, _dev_ptr(out, torch.float32, "out"),
+            _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), _stream(stream),
+        )
+    _check(rc, "tq_kivi_decode")
+    return out
+
+
+def tq_kivi_decode_attn_workspace_size(fmt, batch: int, num_q_heads: int, max_pages: int, window: int) -> int:
+    F = _kfmt(fmt)
+    n = C.c_size_t(0)
+    _check(load_library().tq_kivi_decode_attn_workspace_size(C.byref(F), int(batch), int(num_q_heads), int(max_pages), int(window),
+                                                             C.byref(n)), "tq_kivi_decode_attn_workspace_size")
+    return int(n.value)
+
+
+def tq_kivi_decode_attn(fmt, q, page_pool, num_pages: int, block_tables, comp_lens, k_win, v_win, win_lens, out, workspace,
+                        err_word=None, stream=None, events=None):
+    """Decode attention over a KIVI cache plus the fp16 window; `events`
+    (begin, end) selects the timed entry point."""
+    F = _kfmt(fmt)
+    B, Hq, _ = q.shape
+    window = 0 if k_win is None else int(k_win.shape[2])
+    lib = load_library()
+    fn = lib.tq_kivi_decode_attn if events is None else lib.tq_kivi_decode_attn_timed
+    extra = () if events is None else (_event(events[0]), _event(events[1]))
+    with torch.cuda.device(_device(q, page_pool, block_tables, comp_lens, k_win, v_win, win_lens, out, workspace, err_word)):
+        rc = fn(
+            C.byref(F), int(B), int(Hq), _dev_ptr(q, torch.float16, "q"), _dev_ptr(page_pool, torch.uint8, "page_pool"), int(num_pages),
+            _dev_ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]), _dev_ptr(comp_lens, torch.int32, "comp_lens"),
+            _dev_ptr(k_win, torch.float16, "k_win", allow_none=True), _dev_ptr(v_win, torch.float16, "v_win", allow_none=True),
+            _dev_ptr(win_lens, torch.int32, "win_lens", allow_none=True), window, _dev_ptr(out, torch.float32, "out"),
+            _dev_ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()),
+            _dev_ptr(err_word, torch.int32, "err_word", allow_none=True), *extra, _stream(stream),
+        )
+    _check(rc, "tq_kivi_decode_attn" if events is None else "tq_kivi_decode_attn_timed")
     return out

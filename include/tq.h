@@ -352,6 +352,99 @@ tq_status tq_decode_attn_static(const tq_format *fmt, int batch, int num_q_heads
                                 const float *v_codebook, const float *S, float *out, int32_t *err_word,
                                 void *stream);
 
+/* ----------------------------------------------------------------------
+ * KIVI-style control arm: asymmetric integer quantization of keys per
+ * channel and of values per token, with the same fp16 recent window.
+ * "TurboQuant Family Design Study for CPU and Browser WASM KV Caches",
+ * section 'Candidate key and value algorithms', item 1 (Control baseline
+ * arm), and its summary of KIVI in 'Why keys and values need different
+ * treatment' (keys per channel, values per token).  No rotation: the cache
+ * holds the raw-domain vectors.
+ *
+ * Quantizer of a group of fp16 values x (the same on every path): zero
+ * z = min x, scale s = (max x - min x) / (2^b - 1), both stored as fp16 (s
+ * rounded to nearest); the code of x is floor((x - z) / s + 1/2), clamped to
+ * [0, 2^b - 1], decided in fp32 with the stored z and s; a zero scale gives
+ * code 0.  Reconstruction z + s * code.  Key groups: one channel of one head
+ * over the tokens of one page; value groups: one token-head over its d
+ * channels.  Non-finite inputs give unspecified (but in-range) codes.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t head_dim;     /* d                                     */
+  int32_t k_bits;       /* b_K, bits per key code                */
+  int32_t v_bits;       /* b_V, bits per value code              */
+  int32_t page_size;    /* P, tokens per page (a multiple of 16) */
+  int32_t num_kv_heads; /* H                                     */
+} tq_kivi_format;
+
+/* One pool per layer = [num_pages][H] head-slabs; per slab, each section
+ * 16-byte aligned: K (scale, zero) fp16 pairs [d] (this page's per-channel
+ * groups), K codes [P][d*b_K/8] (LSB-first per token), V (scale, zero) fp16
+ * pairs [P], V codes (P*d*b_V/8 bytes in the grouped order of tq_layout's
+ * value section). */
+typedef struct {
+  int64_t slab_bytes, page_bytes;
+  int64_t k_params, k_codes, v_params, v_codes;
+  int32_t k_code_bytes, v_code_bytes; /* per token */
+} tq_kivi_layout;
+
+/* Layout of a KIVI format (host only).  The GPU kernels support d = 128 and
+ * b_K, b_V in {2, 4}; other valid formats return TQ_ERR_UNSUPPORTED from the
+ * device calls. */
+tq_status tq_kivi_page_layout(const tq_kivi_format *fmt, tq_kivi_layout *out);
+
+/*
+ * Prefill keys into whole pages: x_f16 device fp16 [N][H][d] in token order;
+ * token n goes to page page_ids[n / P], offset n % P (page_ids: device int32
+ * [ceil(N / P)]).  Each page's tokens (the last page may hold N mod P) form
+ * the per-channel groups.  A page id outside [0, num_pages) skips its group
+ * and sets TQ_DEVERR_PAGE_RANGE in err_word (device int32 or NULL).
+ */
+tq_status tq_kivi_encode_keys(const tq_kivi_format *fmt, const void *k_f16, int64_t n_tokens, const int32_t *page_ids,
+                              void *page_pool, int64_t num_pages, int32_t *err_word, void *stream);
+
+/* Values, per token: v_f16 device fp16 [N][H][d], token n to slot
+ * slot_mapping[n] (as tq_encode: negative skips, beyond the pool sets
+ * TQ_DEVERR_SLOT_RANGE). */
+tq_status tq_kivi_encode_values(const tq_kivi_format *fmt, const void *v_f16, int64_t n_tokens,
+                                const int32_t *slot_mapping, void *page_pool, int64_t num_pages, int32_t *err_word,
+                                void *stream);
+
+/* Reconstruction z + s * code of N slots of one kind into out device fp32
+ * [N][H][d] (tests and offline use; a negative slot gives zeros). */
+tq_status tq_kivi_decode(const tq_kivi_format *fmt, int kind, const void *page_pool, int64_t num_pages,
+                         const int32_t *slot_mapping, int64_t n_tokens, float *out, int32_t *err_word, void *stream);
+
+/* Workspace bytes of tq_kivi_decode_attn (host only; depends on the current
+ * device's SM count). */
+tq_status tq_kivi_decode_attn_workspace_size(const tq_kivi_format *fmt, int batch, int num_q_heads, int max_pages,
+                                             int window, size_t *bytes);
+
+/*
+ * One decode step of attention over [KIVI pages U fp16 recent window]:
+ * l_i = q . k_hat_i / sqrt(d), o = sum_i softmax(l)_i v_hat_i, computed from
+ * the codes on the tensor cores (keys: q scaled per page by the channel
+ * scales against the integer codes, plus q . z; values: weights p * s against
+ * the integer codes, plus sum p * z), split-KV with a log-sum-exp merge.  No
+ * decoded copy of the cache is written.  Arguments, layouts and errors as
+ * for tq_decode_attn, without signs, codebooks or S; the page pool must be
+ * 32-byte aligned.
+ */
+tq_status tq_kivi_decode_attn(const tq_kivi_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                              const void *page_pool, int64_t num_pages, const int32_t *block_tables, int max_pages,
+                              const int32_t *comp_lens, const void *k_win_f16, const void *v_win_f16,
+                              const int32_t *win_lens, int window, float *out, void *workspace, size_t workspace_bytes,
+                              int32_t *err_word, void *stream);
+
+/* tq_kivi_decode_attn that also records two caller events (cudaEvent_t, may
+ * be NULL) around its main kernel on `stream`, as tq_decode_attn_timed. */
+tq_status tq_kivi_decode_attn_timed(const tq_kivi_format *fmt, int batch, int num_q_heads, const void *q_f16,
+                                    const void *page_pool, int64_t num_pages, const int32_t *block_tables,
+                                    int max_pages, const int32_t *comp_lens, const void *k_win_f16,
+                                    const void *v_win_f16, const int32_t *win_lens, int window, float *out,
+                                    void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                    void *main_begin_event, void *main_end_event, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -122,7 +122,7 @@ void orc_kivi_quantize_group(int n, const uint16_t *x, int64_t stride, int bits,
     if (sf > 0.0f) {
       float t = (v - zf) / sf; /* fp32 */
       float r = floorf(t + 0.5f);
-      code = r < 0.0f ? 0 : (r > (float)top ? top : (int)r);
+      code = r >= 0.0f ? (r > (float)top ? top : (int)r) : 0; /* NaN: 0 */
     }
     codes[i] = code;
   }

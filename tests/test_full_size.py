@@ -123,3 +123,56 @@ def test_bulk_encode_full_size(bits, qjl):
         pick = _sample_positions(N, P, rng, n_random=120)
         st = _check_encode_samples(fmt, kind, x, slots, pool.cpu().numpy(), num_pages, pick, f"b{bits} qjl{qjl} kind{kind}")
         check_exemption_reach(st, f"bulk encode b{bits} qjl{qjl} kind {kind}")
+
+
+@pytest.mark.parametrize("wl", ti.KIVI_WORKLOADS, ids=[w.name for w in ti.KIVI_WORKLOADS])
+def test_kivi_workload_full_size(wl):
+    """The KIVI control arm at the Llama-3-8B decode shape (two layers, the
+    benchmark's own cache builder): sampled attention rows against the
+    oracle over the same pool, and sampled page groups / tokens re-encoded by
+    the oracle byte for byte."""
+    import bench
+    import decode_attention_tq_gb300 as tq
+
+    two = dataclasses.replace(wl, layers=2)
+    b = bench.KiviDecodeBench(two, "cuda")
+    f = b.fmt
+    B, Hq, H, d, P = b.B, b.Hq, b.H, f.head_dim, f.page_size
+    lay = oracle.kivi_layout(f)
+    for li, L in enumerate(b.layers):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
+        tq.tq_kivi_decode_attn(f, L["q"], L["pool"], b.num_pages, b.bt, b.comp_lens, L["kwin"], L["vwin"], b.win_lens, out, b.ws,
+                               err_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        got = out.cpu().numpy()
+        assert np.isfinite(got).all()
+        pool = L["pool"].cpu().numpy()
+        rows = sorted({0, Hq - 1, (B - 1) * Hq, B * Hq - 1, (B // 2) * Hq + 3 + li})
+        rc, ref = oracle.kivi_attention(f, L["q"].cpu().numpy(), pool, b.num_pages, b.bt.cpu().numpy(), b.comp_lens.cpu().numpy(),
+                                        L["kwin"].cpu().numpy(), L["vwin"].cpu().numpy(), b.win_lens.cpu().numpy(), heads=rows)
+        assert rc == 0
+        e = rel_err(got.reshape(B * Hq, d)[rows], ref)
+        print(wl.name, li, "max rel err", e.max())
+        assert e.max() <= REL_ATTN, (wl.name, li, e)
+        # sampled page groups (keys) and tokens (values) re-encoded by the oracle
+        rng = np.random.default_rng(7 + li)
+        bt = b.bt.cpu().numpy()
+        for kind in (0, 1):
+            x = ti.kv_history(B, wl.context, H, d, li, kind, device="cuda")
+            for bb in sorted({0, B - 1}):
+                ref_pool = pool.copy()
+                if kind == 0:
+                    for g in sorted({0, b.pages_per_seq - 1, int(rng.integers(0, b.pages_per_seq))}):
+                        xs = x[bb, g * P:(g + 1) * P].cpu().numpy()
+                        assert oracle.kivi_encode_keys(f, xs, bt[bb, g:g + 1], ref_pool, b.num_pages) == 0
+                else:
+                    pick = _sample_positions(b.comp, P, rng)
+                    xs = x[bb, pick].cpu().numpy()
+                    sl = (bt[bb, np.array(pick) // P] * P + np.array(pick) % P).astype(np.int32)
+                    assert oracle.kivi_encode_values(f, xs, sl, ref_pool, b.num_pages) == 0
+                assert np.array_equal(ref_pool, pool), (wl.name, li, kind, bb)
+            del x
+    del b
+    torch.cuda.empty_cache()

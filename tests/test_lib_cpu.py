@@ -125,3 +125,34 @@ def test_host_validation_before_any_launch(lib):
     # window > 0 needs the window buffers
     assert lib.tq_decode_attn(C.byref(f), 1, 8, dummy, dummy, 4, dummy, 4, dummy, None, None, None, 16, dummy, dummy, dummy, dummy,
                               None, dummy, dummy, 1 << 20, None, None) == 1
+
+
+@pytest.mark.parametrize("fmt", [ti.KiviFormat(128, kb, vb, P, H) for kb in (2, 4) for vb in (2, 4) for P in (16, 64, 128) for H in (1, 8)]
+                         + [ti.KiviFormat(64, 3, 2, 32, 2), ti.KiviFormat(16, 1, 8, 16, 3)])
+def test_kivi_layout_equals_oracle(lib, fmt):
+    from decode_attention_tq_gb300 import tq_kivi_page_layout
+
+    assert tq_kivi_page_layout(fmt) == oracle.kivi_layout(fmt)
+
+
+def test_kivi_host_validation_before_any_launch(lib):
+    from decode_attention_tq_gb300.tq import tq_kivi_format
+
+    P = C.c_void_p
+    dummy = P(4096)  # never dereferenced
+    f = tq_kivi_format(128, 2, 2, 64, 8)
+    assert lib.tq_kivi_encode_keys(None, dummy, 1, dummy, dummy, 1, None, None) == 1
+    assert lib.tq_kivi_encode_keys(C.byref(tq_kivi_format(128, 2, 2, 24, 8)), dummy, 1, dummy, dummy, 1, None, None) == 1
+    assert lib.tq_kivi_encode_keys(C.byref(tq_kivi_format(128, 3, 2, 64, 8)), dummy, 1, dummy, dummy, 1, None, None) == 2
+    assert lib.tq_kivi_encode_values(C.byref(tq_kivi_format(64, 2, 2, 64, 8)), dummy, 1, dummy, dummy, 1, None, None) == 2
+    assert lib.tq_kivi_encode_values(C.byref(f), dummy, -1, dummy, dummy, 1, None, None) == 1
+    assert lib.tq_kivi_encode_values(C.byref(f), P(4098), 1, dummy, dummy, 1, None, None) == 1
+    assert lib.tq_kivi_encode_values(C.byref(f), dummy, 0, dummy, dummy, 1, None, None) == 0  # no-op
+    assert lib.tq_kivi_decode(C.byref(f), 2, dummy, 1, dummy, 1, dummy, None, None) == 1
+    n = C.c_size_t(0)
+    assert lib.tq_kivi_decode_attn_workspace_size(C.byref(f), 1, 12, 4, 0, C.byref(n)) == 1   # Hq % H
+    assert lib.tq_kivi_decode_attn_workspace_size(C.byref(f), 1, 8 * 16, 4, 0, C.byref(n)) == 2  # G = 16 > 8
+    assert lib.tq_kivi_decode_attn(C.byref(f), 1, 8, None, dummy, 4, dummy, 4, dummy, None, None, None, 0, dummy, dummy,
+                                   1 << 20, None, None) == 1
+    assert lib.tq_kivi_decode_attn(C.byref(f), 1, 8, dummy, dummy, 4, dummy, 4, dummy, None, None, None, 16, dummy, dummy,
+                                   1 << 20, None, None) == 1  # window buffers missing

@@ -150,6 +150,17 @@ class Format:
 
 
 @dataclasses.dataclass(frozen=True)
+class KiviFormat:
+    """Format of the KIVI-style control arm (mirrored by tq_kivi_format)."""
+
+    head_dim: int = 128
+    k_bits: int = 2
+    v_bits: int = 2
+    page_size: int = 64
+    num_kv_heads: int = 8
+
+
+@dataclasses.dataclass(frozen=True)
 class DecodeWorkload:
     name: str
     layers: int
@@ -203,6 +214,16 @@ LLAMA3_8B_T32K_K35V3 = DecodeWorkload("llama-3-8b_l32_b16_h32x8_t32768_k35v3_w12
                                       Format(128, 3, 3, 0, 128, 64, 8, k_mixed=1), 32768, 128)
 
 DECODE_WORKLOADS = (SINGLE_LAYER_T2K, QWEN25_3B_T16K, LLAMA3_8B_T32K, LONG_CTX_T128K, LLAMA3_8B_T32K_K35V3)
+
+# The KIVI-style control arm ('Candidate key and value algorithms', Control
+# baseline arm of the design study) at the Llama-3-8B decode shape: 2-bit
+# keys and values (KIVI's own width) and 4-bit (the width of the TurboQuant
+# workload it is compared with), the same 128-token fp16 window.
+LLAMA3_8B_T32K_KIVI2 = DecodeWorkload("llama-3-8b_l32_b16_h32x8_t32768_kivi_k2v2_w128", 32, 16, 32, KiviFormat(128, 2, 2, 64, 8),
+                                      32768, 128)
+LLAMA3_8B_T32K_KIVI4 = DecodeWorkload("llama-3-8b_l32_b16_h32x8_t32768_kivi_k4v4_w128", 32, 16, 32, KiviFormat(128, 4, 4, 64, 8),
+                                      32768, 128)
+KIVI_WORKLOADS = (LLAMA3_8B_T32K_KIVI2, LLAMA3_8B_T32K_KIVI4)
 
 
 def orthogonal_matrix(seed: int, m: int, d: int) -> np.ndarray:
