@@ -231,18 +231,80 @@ class DecodeBench:
         self.step_bytes = wl.layers * (self.main_bytes + self.window_bytes + B * Hq * d * (2 + 4))
         self.launches_per_step = wl.layers * 4  # append (roll + K and V encode), prep (with window chunks), main, merge
 
-    def step(self, events=None):
+    def step(self, events=None, append_only=False):
         tq, f = self.tq, self.fmt
         for i, L in enumerate(self.layers):
             tq.tq_append_window(f, L["knew"], L["vnew"], L["kwin"], L["vwin"], L["wlen"], L["whead"], L["comp"], self.bt, L["pool"],
                                 self.num_pages, self.ks, self.vs, self.kcb, self.vcb, self.S, workspace=self.ws_append,
                                 err_word=self.err)
+            if append_only:
+                continue
             args = (f, L["q"], L["pool"], self.num_pages, self.bt, L["comp"], L["kwin"], L["vwin"], L["wlen"],
                     self.ks, self.vs, self.kcb, self.vcb, self.S, L["out"], self.ws)
             if events is None:
                 tq.tq_decode_attn(*args, err_word=self.err)
             else:
                 tq.tq_decode_attn_timed(*args, events[i][0], events[i][1], err_word=self.err)
+
+
+class KiviDecodeBench:
+    """A resident multi-layer KIVI-style cache (the control arm: keys per
+    channel over each page, values per token) and its decode step: one
+    tq_kivi_decode_attn per layer over the compressed pages plus the fp16
+    window.  Keys are encoded a page group at a time (prefill), so this arm
+    has no per-token append."""
+
+    def __init__(self, wl: ti.DecodeWorkload, device: str):
+        import decode_attention_tq_gb300 as tq
+
+        self.tq = tq
+        self.wl = wl
+        f = wl.fmt
+        self.fmt = f
+        B, Hq, H, d, P, W, T = wl.batch, wl.q_heads, wl.kv_heads, f.head_dim, f.page_size, wl.window, wl.context
+        comp = wl.comp_tokens
+        self.B, self.Hq, self.H, self.W, self.T, self.comp = B, Hq, H, W, T, comp
+        self.pages_per_seq = wl.pages_per_seq
+        self.num_pages = B * self.pages_per_seq + 1
+        perm = ti.page_permutation(self.num_pages).to(device)
+        self.bt = perm[: B * self.pages_per_seq].reshape(B, self.pages_per_seq).contiguous()
+        pos = torch.arange(comp, device=device)
+        slots = self.bt[:, pos // P] * P + (pos % P)[None, :]
+        self.comp_lens = torch.full((B,), comp, dtype=torch.int32, device=device)
+        self.win_lens = torch.full((B,), wl.win_tokens, dtype=torch.int32, device=device)
+        lay = tq.tq_kivi_page_layout(f)
+        self.layers = []
+        for layer in range(wl.layers):
+            pool = torch.zeros(self.num_pages * lay["page_bytes"], dtype=torch.uint8, device=device)
+            ent = {"pool": pool}
+            for kind, name in ((0, "k"), (1, "v")):
+                x = ti.kv_history(B, T, H, d, layer, kind, device=device)
+                for b in range(B):
+                    xs = x[b, :comp].contiguous()
+                    if kind == 0:
+                        tq.tq_kivi_encode_keys(f, xs, self.bt[b].contiguous(), pool, self.num_pages)
+                    else:
+                        tq.tq_kivi_encode_values(f, xs, slots[b].to(torch.int32).contiguous(), pool, self.num_pages)
+                ent[name + "win"] = x[:, comp:].permute(0, 2, 1, 3).contiguous() if W else None
+                del x
+            ent["q"] = ti.query(B, Hq, d, device=device, seed=ti.SEED_QUERY + 7919 * layer)
+            ent["out"] = torch.empty((B, Hq, d), dtype=torch.float32, device=device)
+            self.layers.append(ent)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        self.ws = torch.empty(tq.tq_kivi_decode_attn_workspace_size(f, B, Hq, self.pages_per_seq, W), dtype=torch.uint8, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        per_tok = 4 * d / P + lay["k_code_bytes"] + 4 + lay["v_code_bytes"]  # K params amortised over the page
+        self.main_bytes = int(B * H * comp * per_tok) + B * self.pages_per_seq * 4
+        self.window_bytes = B * H * wl.win_tokens * d * 2 * 2
+        self.step_bytes = wl.layers * (self.main_bytes + self.window_bytes + B * Hq * d * (2 + 4))
+        self.launches_per_step = wl.layers * 3  # prep (with window chunks), main, merge
+
+    def step(self, events=None):
+        for i, L in enumerate(self.layers):
+            self.tq.tq_kivi_decode_attn(self.fmt, L["q"], L["pool"], self.num_pages, self.bt, self.comp_lens, L["kwin"], L["vwin"],
+                                        self.win_lens if self.W else None, L["out"], self.ws, err_word=self.err,
+                                        events=None if events is None else events[i])
 
 
 def time_steps(fn, steps: int, warmup: int, barrier):
@@ -283,23 +345,22 @@ def time_steps_flushed(fn, steps: int, warmup: int, barrier, flush):
     return statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
 
 
-def run_decode(args, device, barrier, reduce_max, rank, world):
-    wl = {w.name: w for w in ti.DECODE_WORKLOADS}[args.workload]
-    if args.layers:
-        import dataclasses
+def event_pairs(n):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:  # torch creates the CUDA event on its first record
+        a.record()
+        b.record()
+    return evs
 
-        wl = dataclasses.replace(wl, layers=args.layers, name=f"{wl.name}(first {args.layers} layers)")
-    t0 = time.time()
-    # every step appends one compressed token per sequence: room for all the
-    # steps this run makes (both timed arms, warm-ups, captures, event steps)
-    bench = DecodeBench(wl, device, spare_tokens=2 * (args.steps + args.warmup) + 32)
-    setup_s = time.time() - t0
 
-    # graph-captured step (launch-bound pieces replay without host overhead)
+def measure_decode(bench, steps, warmup, barrier, reduce_max, device, use_graph=True, event_steps=5):
+    """Step time (graph replay, L2 flushed per step when the working set is
+    under 4x L2), clocks during the timed region, and the main kernel's mean
+    CUDA-event duration over eager steps."""
     bench.step()
     torch.cuda.synchronize()
     graph = None
-    if not args.no_graph:
+    if use_graph:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
@@ -310,36 +371,54 @@ def run_decode(args, device, barrier, reduce_max, rank, world):
             bench.step()
         torch.cuda.synchronize()
     run = graph.replay if graph is not None else bench.step
-
     # a working set that L2 could hold is timed step by step with L2 flushed
     # before each step; larger ones stream from HBM anyway
     flush_l2 = bench.step_bytes < 4 * L2_BYTES
+    flush = None
     if flush_l2:
         scratch = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=device)
         flush = lambda: scratch.fill_(1)
     with ClockSampler(nvml_index(torch.cuda.current_device())) as clk:
         if flush_l2:
-            ms = time_steps_flushed(run, args.steps, args.warmup, barrier, flush)
+            ms = time_steps_flushed(run, steps, warmup, barrier, flush)
         else:
-            ms = time_steps(run, args.steps, args.warmup, barrier)
+            ms = time_steps(run, steps, warmup, barrier)
     ms = reduce_max(ms)
     clocks = clk.summary()
-
     # dominant kernel in place: eager steps with events around the main kernel
-    nl = wl.layers
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
-    for a, b in evs:  # torch creates the CUDA event on its first record
-        a.record()
-        b.record()
+    evs = event_pairs(bench.wl.layers)
     durs = []
-    for _ in range(max(1, min(args.steps, 5))):
+    for _ in range(max(1, min(steps, event_steps))):
         if flush_l2:
             flush()
         bench.step(events=evs)
         torch.cuda.synchronize()
         durs.extend(a.elapsed_time(b) for a, b in evs)
     main_ms = statistics.mean(durs)
-    err = int(bench.err.item())
+    del graph
+    return dict(ms=ms, clocks=clocks, main_ms=main_ms, err=int(bench.err.item()), cuda_graph=use_graph, flush_l2=flush_l2,
+                flush=flush)
+
+
+def l2_note(bench, flush_l2):
+    return ("working set %.1f MB < 4x L2: L2 flushed before every timed step, outside the timing" % (bench.step_bytes / 1e6)
+            if flush_l2 else "working set (cache %.1f GB) >> L2; no flush" % (bench.step_bytes / 1e9))
+
+
+def run_decode(args, device, barrier, reduce_max, rank, world):
+    wl = {w.name: w for w in ti.DECODE_WORKLOADS}[args.workload]
+    if args.layers:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, layers=args.layers, name=f"{wl.name}(first {args.layers} layers)")
+    t0 = time.time()
+    # every step appends one compressed token per sequence: room for all the
+    # steps this run makes (both timed arms, warm-ups, captures, event steps)
+    bench = DecodeBench(wl, device, spare_tokens=2 * (args.steps + args.warmup) + 80)
+    setup_s = time.time() - t0
+    m = measure_decode(bench, args.steps, args.warmup, barrier, reduce_max, device, use_graph=not args.no_graph)
+    ms, clocks, main_ms, err, flush_l2, flush = m["ms"], m["clocks"], m["main_ms"], m["err"], m["flush_l2"], m["flush"]
+    graph = True if not args.no_graph else None
 
     peak, peak_kind = measured_peaks()
     achieved = bench.main_bytes / (main_ms * 1e-3) / 1e9
@@ -364,8 +443,7 @@ def run_decode(args, device, barrier, reduce_max, rank, world):
             "workload": wl.name, "layers": wl.layers, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
             "head_dim": wl.fmt.head_dim, "context": wl.context, "window": wl.window, "page_size": wl.fmt.page_size,
             "k_bits": wl.fmt.k_bits + 0.5 * wl.fmt.k_mixed, "v_bits": wl.fmt.v_bits, "k_qjl": wl.fmt.k_qjl, "step": "per layer: append 1 token/seq + decode attention",
-            "l2": ("working set %.1f MB < 4x L2: L2 flushed before every timed step, outside the timing" % (bench.step_bytes / 1e6)
-                   if flush_l2 else "working set (cache %.1f GB) >> L2; no flush" % (bench.step_bytes / 1e9)),
+            "l2": l2_note(bench, flush_l2),
             "cuda_graph": graph is not None,
         },
         "hbm_gbs": bench.step_bytes / (ms * 1e-3) / 1e9,
@@ -379,6 +457,83 @@ def run_decode(args, device, barrier, reduce_max, rank, world):
         "err_word": err,
     }
     return res, bench
+
+
+def run_break_even(bench, ms_step, steps: int = 8):
+    """M7 of the design study ('Append cost and memory-bandwidth tradeoffs'):
+    G* = C_append tau_op / (dB_step / BW_eff), the number of future decode
+    steps whose bandwidth savings repay one step's append.  C_append tau_op is
+    the measured device time of one step's appends (every layer's
+    tq_append_window, replayed as one CUDA graph between two events),
+    dB_step = T L H d (4 - (b_K + b_V)/8) the bytes one decode step saves
+    against an fp16 cache, BW_eff the measured bytes per second of the
+    decode step."""
+    wl, f = bench.wl, bench.fmt
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        bench.step(append_only=True)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bench.step(append_only=True)
+    torch.cuda.synchronize()
+    g.replay()
+    per_step = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        per_step.append(e0.elapsed_time(e1))
+    del g
+    t_append_ms = statistics.median(per_step)
+    kbits = f.k_bits + 0.5 * f.k_mixed + (f.qjl_m / f.head_dim if f.k_qjl else 0.0)
+    d_bytes = wl.context * wl.layers * wl.kv_heads * f.head_dim * (4 - (kbits + f.v_bits) / 8)
+    bw_eff = bench.step_bytes / (ms_step * 1e-3)
+    saved_ms = d_bytes / bw_eff * 1e3
+    return {"append_ms_per_step": t_append_ms, "delta_bytes_per_step": d_bytes, "bw_eff_gbs": bw_eff / 1e9,
+            "saved_ms_per_step": saved_ms, "g_star_steps": t_append_ms / saved_ms,
+            "how": "append time: one step's appends (every layer) replayed as a CUDA graph between two events, median of 8; "
+                   "dB_step from the formula with the format's bits per coordinate (QJL sign bits included); "
+                   "BW_eff = step bytes / step time"}
+
+
+def workload_entry(wl, bench, m, kind: str):
+    peak, _ = measured_peaks()
+    achieved = bench.main_bytes / (m["main_ms"] * 1e-3) / 1e9
+    tokens = wl.batch * wl.layers * wl.context
+    f = wl.fmt
+    return {
+        "ms_per_step": m["ms"], "value": tokens / (m["ms"] * 1e-3), "unit": UNIT, "hbm_gbs": bench.step_bytes / (m["ms"] * 1e-3) / 1e9,
+        "main_kernel": kind, "main_us": m["main_ms"] * 1e3, "main_bytes": bench.main_bytes, "main_gbs": achieved, "frac": achieved / peak,
+        "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS, "clocks": m["clocks"], "l2": l2_note(bench, m["flush_l2"]),
+        "cuda_graph": m["cuda_graph"], "err_word": m["err"], "gpu_launches_per_step": bench.launches_per_step,
+        "shape": {"layers": wl.layers, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "context": wl.context,
+                  "window": wl.window, "page_size": f.page_size, "k_bits": f.k_bits + 0.5 * getattr(f, "k_mixed", 0), "v_bits": f.v_bits,
+                  "k_qjl": getattr(f, "k_qjl", 0)},
+        "step": "per layer: append 1 token/seq + decode attention" if kind == "attn_main_kernel" else
+                "per layer: decode attention (the KIVI arm encodes keys a page group at a time; no per-token append)",
+    }
+
+
+def run_workloads(args, device, barrier, reduce_max, skip_name: str):
+    """Every other decode workload (the five configurations' decode shapes,
+    the design study's K3.5/V3 mode and the KIVI control arm), each timed the
+    same way as the headline line, with fewer steps."""
+    out = {}
+    steps, warmup = max(3, min(args.steps, 10)), 3
+    for wl in ti.DECODE_WORKLOADS + ti.KIVI_WORKLOADS:
+        if wl.name == skip_name:
+            continue
+        kivi = wl in ti.KIVI_WORKLOADS
+        bench = KiviDecodeBench(wl, device) if kivi else DecodeBench(wl, device, spare_tokens=2 * (steps + warmup) + 48)
+        m = measure_decode(bench, steps, warmup, barrier, reduce_max, device)
+        out[wl.name] = workload_entry(wl, bench, m, "kivi_main_kernel" if kivi else "attn_main_kernel")
+        del bench, m
+        torch.cuda.empty_cache()
+    return out
 
 
 def load_traffic(kernel: str, workload: str):
@@ -501,15 +656,15 @@ def run_e2e(args, bench: DecodeBench, graph: bool = True):
 
 
 # --------------------------------------------------------------- oracle --
-def oracle_sample_setup(wl: ti.DecodeWorkload, n_seq: int, device: str | None):
-    """Host-side pages of `n_seq` sequences of layer 0, encoded by the oracle."""
+def oracle_sample_setup(wl: ti.DecodeWorkload, n_seq: int, device: str | None, layer: int = 0):
+    """Host-side pages of `n_seq` sequences of one layer, encoded by the oracle."""
     import oracle
 
     f = wl.fmt
     H, d, P, W, T, comp = wl.kv_heads, f.head_dim, f.page_size, wl.window, wl.context, wl.comp_tokens
     gen_dev = device if device else "cpu"
-    K = ti.kv_history(n_seq, T, H, d, 0, 0, device=gen_dev).cpu().numpy()
-    V = ti.kv_history(n_seq, T, H, d, 0, 1, device=gen_dev).cpu().numpy()
+    K = ti.kv_history(n_seq, T, H, d, layer, 0, device=gen_dev).cpu().numpy()
+    V = ti.kv_history(n_seq, T, H, d, layer, 1, device=gen_dev).cpu().numpy()
     pps = wl.pages_per_seq
     num_pages = n_seq * pps
     bt = np.arange(num_pages, dtype=np.int32).reshape(n_seq, pps)
@@ -571,6 +726,91 @@ def cpu_baseline(wl: ti.DecodeWorkload, device, target_cpu_s: float = 20.0):
                       f"(~{n_heads * probe:.0f} s of CPU work)"}
 
 
+def cpu_baseline_layers(wl: ti.DecodeWorkload, device, budget_s: float):
+    """The oracle on whole layers (every sequence and query head), layer after
+    layer until the budget is spent or the workload is done: the full step
+    when it fits, else the layers it reached (stated in `sample`)."""
+    cores = host_cores()
+    t_att, layers = 0.0, 0
+    t0 = time.perf_counter()
+    for layer in range(wl.layers):
+        s = oracle_sample_setup(wl, wl.batch, device, layer)
+        t_att += oracle_time(s, list(range(wl.batch * wl.q_heads)), cores)
+        layers += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    value = wl.batch * layers * wl.context / t_att
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{wl.name}: the full step ({layers} layers)" if layers == wl.layers else
+                       f"{wl.name}: {layers} of {wl.layers} layers, every sequence and query head") +
+                      f"; {t_att:.2f} s of attention wall time on {cores} threads (encode excluded)"}
+
+
+def cpu_baseline_slice(wl: ti.DecodeWorkload, device, budget_s: float):
+    """The oracle on (sequence, query head) rows of layer 0 of one sequence,
+    as many as fit the budget (the long-context shape's layer is minutes of
+    CPU work)."""
+    cores = host_cores()
+    s = oracle_sample_setup(wl, 1, device)
+    probe = oracle_time(s, [0], 1)
+    n = int(max(1, min(wl.q_heads, budget_s * cores / max(probe, 1e-3))))
+    dt = oracle_time(s, list(range(n)), cores)
+    return {"value": wl.context * n / wl.q_heads / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{wl.name}: layer 0, sequence 0, {n} of {wl.q_heads} query heads at context {wl.context}; "
+                      f"{dt:.2f} s wall on {cores} threads"}
+
+
+def cpu_baseline_encode(budget_s: float, device):
+    """The oracle's encode on vectors of one layer of the bulk-encode workload
+    (K with a QJL sketch and V, 3 bits), as many tokens as fit the budget."""
+    import oracle
+
+    cores = host_cores()
+    wl = ti.BULK_ENCODE_64K
+    H, d, P = wl.kv_heads, 128, wl.page_size
+    fmt = ti.Format(d, 3, 3, 1, wl.qjl_m, P, H)
+    c, t = oracle.make_codebook(3)
+    ks, vs = ti.sign_bits(ti.SEED_SIGNS_K, d), ti.sign_bits(ti.SEED_SIGNS_V, d)
+    S = ti.gaussian_matrix(ti.SEED_QJL, wl.qjl_m, d)
+    NMAX = wl.tokens
+    X = [ti.kv_history(1, NMAX, H, d, 0, kind, device=device if device else "cpu")[0].cpu().numpy() for kind in (0, 1)]
+    lay = oracle.page_layout(fmt)
+
+    def run(n):
+        pool = np.zeros((n // P + 1) * lay["page_bytes"], np.uint8)
+        chunks = [(kind, i0) for kind in (0, 1) for i0 in range(0, n, 64)]
+
+        def job(j):
+            kind, i0 = j
+            i1 = min(n, i0 + 64)
+            sl = np.arange(i0, i1, dtype=np.int32)
+            return oracle.encode(fmt, kind, X[kind][i0:i1], sl, pool, n // P + 1, ks if kind == 0 else vs, c, t, S if kind == 0 else None)
+
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+            list(ex.map(job, chunks))
+        return time.perf_counter() - t0
+
+    n0 = 64 * cores
+    dt0 = run(n0)
+    N = int(min(NMAX, max(n0, n0 * budget_s / max(dt0, 1e-3)))) // 64 * 64
+    dt = run(N)
+    vecs = 2 * N * H
+    return {"value": vecs / dt, "unit": "vectors/s", "cores": cores, "kind": "oracle",
+            "sample": f"{wl.name}: {N} tokens x {H} heads of K (3-bit + QJL) and V (3-bit), layer 0; {dt:.2f} s wall on {cores} threads"}
+
+
+def run_cpu_baselines(device):
+    """Oracle baselines beyond the headline slice: the single-layer and Qwen
+    decode shapes on whole layers, a long-context slice, and the encode."""
+    return {
+        ti.SINGLE_LAYER_T2K.name: cpu_baseline_layers(ti.SINGLE_LAYER_T2K, device, 10.0),
+        ti.QWEN25_3B_T16K.name: cpu_baseline_layers(ti.QWEN25_3B_T16K, device, 15.0),
+        ti.LONG_CTX_T128K.name: cpu_baseline_slice(ti.LONG_CTX_T128K, device, 10.0),
+        ti.BULK_ENCODE_64K.name: cpu_baseline_encode(8.0, device),
+    }
+
+
 def run_reference(args, rank, world):
     """The reference arm: the fp64 oracle, timed on the host cores."""
     wl = {w.name: w for w in ti.DECODE_WORKLOADS}[args.workload]
@@ -611,6 +851,7 @@ def main():
     ap.add_argument("--no-encode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="only the headline workload (no other decode shapes, no break-even)")
     ap.add_argument("--quick", action="store_true", help="fewer encode layers (development)")
     ap.add_argument("--layers", type=int, default=0, help="decode layers (profiling a small case; 0 = the workload's)")
     ap.add_argument("--encode-only", action="store_true", help="run only the bulk-encode part (profiling)")
@@ -670,13 +911,20 @@ def main():
         e2e_ms = reduce_max(e2e["ms_per_step"])
         e2e["value"] = job_throughput(bench.wl.batch * bench.wl.layers * bench.wl.context, e2e_ms, world)
         res["e2e"] = e2e
+    if not args.no_workloads:
+        res["break_even"] = run_break_even(bench, res["ms_per_step"])
+    main_name = bench.wl.name
     del bench
     torch.cuda.empty_cache()
+    if not args.no_workloads:
+        res["workloads"] = run_workloads(args, device, barrier, reduce_max, main_name)
     if not args.no_encode:
         res["encode"] = run_encode(args, device)
     if rank == 0 and world == 1 and not args.no_cpu:
         wl = {w.name: w for w in ti.DECODE_WORKLOADS}[args.workload]
         res["cpu_baseline"] = cpu_baseline(wl, device)
+        if not args.no_workloads:
+            res["cpu_baselines"] = run_cpu_baselines(device)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if pg:
