@@ -69,7 +69,11 @@ struct KeyRegs {
 template <int VB>
 struct ValRegs {
   float nv0, nv1;           // value norms of tokens r, r+8
-  uint32_t vlo[4], vhi[4];  // value code bits of coords 16r..16r+15 of tokens 2t, 2t+1, 2t+8, 2t+9
+  // value code bits of coords 16r..16r+15 of tokens 2t, 2t+1, 2t+8, 2t+9: for
+  // 3-bit codes word pairs (vlo[i], vhi[i]) of token i's chunk; for 2- and
+  // 4-bit codes, (vlo, vhi)[2tp + eo] = the even (eo = 0) or odd coordinate
+  // stream of token pair tp (value_pairs_interleaved), vhi unused at 2 bits
+  uint32_t vlo[4], vhi[4];
 };
 
 // `width` bits at compile-time bit `pos` of the 64-bit (hi:lo), moved to bit
@@ -237,7 +241,8 @@ __device__ __forceinline__ void load_values(const AttnArgs &a, const uint8_t *sl
   R.nv0 = ldna(vn + r);
   R.nv1 = ldna(vn + r + 8);
   // chunk r (coordinates 16r..16r+15) of tokens 2t, 2t+1, 2t+8, 2t+9: one
-  // contiguous run of 4 * 2VB bytes in the grouped value-code section
+  // contiguous run of 4 * 2VB bytes in the grouped value-code section (two
+  // pair-interleaved runs of 4VB bytes for 2- and 4-bit codes)
   const uint8_t *vc = slab + a.v_codes_o + (int64_t)o0 * VCB + r * (16 * 2 * VB) + t * (4 * 2 * VB);
   if constexpr (VB == 4) {
     // 32-byte aligned: sections are multiples of 64 bytes for P % 16 == 0 and
@@ -331,12 +336,11 @@ struct TileCursor {
 // against 146.4 without; K3.5/V3 188.4 against 169.0).
 // Value MMA layouts.  Parity pairs (K index = token slot x coordinate
 // parity: an A register is one code pair of one token) for 3-bit values,
-// where they replace a gather of two tokens' 3-bit fields; coordinate halves
-// (K index = coordinate half x token: an A register pairs two tokens'
-// codes, interleaved in registers) for 2- and 4-bit values.  Measured at the
-// Llama-3-8B decode shape, 32K context: K3.5/V3 160.3 us with parity pairs
-// against 170.0; K4/V4 137.4 either way; long context K2+QJL/V2 176.3
-// against 170.0.
+// where they replace a gather of two tokens' 3-bit fields (measured at the
+// Llama-3-8B decode shape, 32K context: K3.5/V3 160.3 us against 170.0);
+// coordinate halves (K index = coordinate half x token: an A register pairs
+// two tokens' codes of one coordinate, stored so in the pair-interleaved
+// layout) for 2- and 4-bit values.
 template <int VB>
 __host__ __device__ constexpr bool val_parity_pairs() {
   return VB == 3;
@@ -751,23 +755,11 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 #pragma unroll
           for (int mt = 0; mt < 4; mt++) {
             uint32_t av[4];  // (token 2t+8s | 2t+1+8s) x (pair 2mt | 2mt+1)
-            if constexpr (VB == 2) {
-              // byte mt of a token's 2-bit word: pairs 2mt and 2mt + 1 in one 8-byte entry
-              const uint2 pa = lut64(__byte_perm(V.vlo[2 * s], laneV, 0x7604 | (mt << 4)));
-              const uint2 pb = lut64(__byte_perm(V.vlo[2 * s + 1], laneV, 0x7604 | (mt << 4)));
-              av[0] = pa.x; av[1] = pa.y; av[2] = pb.x; av[3] = pb.y;
-            } else {
 #pragma unroll
-              for (int q = 0; q < 4; q++) {
-                const int tok = 2 * s + (q >> 1), pair = 2 * mt + (q & 1);
-                uint32_t addr;
-                if constexpr (VB == 4) {  // byte `pair` of the token's 8-byte chunk
-                  addr = __byte_perm(pair < 4 ? V.vlo[tok] : V.vhi[tok], laneV, 0x7604 | ((pair & 3) << 4));
-                } else {  // 3-bit: the 6 bits of the pair in the token's 48-bit chunk
-                  addr = field_at<8>(V.vlo[tok], V.vhi[tok], 6 * pair, 6, laneV);
-                }
-                av[q] = lut32(addr);
-              }
+            for (int q = 0; q < 4; q++) {
+              // the 6 bits of code pair 2mt + (q&1) in the token's 48-bit chunk
+              const int tok = 2 * s + (q >> 1), pair = 2 * mt + (q & 1);
+              av[q] = lut32(field_at<8>(V.vlo[tok], V.vhi[tok], 6 * pair, 6, laneV));
             }
 #pragma unroll
             for (int nt = 0; nt < NT; nt++)
@@ -796,28 +788,17 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
           wb[nt][1][0] = half0 ? e1 : 0u;
           wb[nt][1][1] = half0 ? 0u : e1;
         }
-        // ---- values: interleave the codes of the token pairs (2t, 2t+1) and
-        // (2t+8, 2t+9) at each coordinate; one lookup gives an A register.
-        // Table offset = pair code << 8 | lane slot.
+        // ---- values: the codes of the token pairs (2t, 2t+1) and (2t+8,
+        // 2t+9) come interleaved at each coordinate (value_pairs_interleaved);
+        // one lookup gives an A register.  Table offset = pair code << 8 | lane slot.
         uint32_t ev[2][2][2];  // [token pair][even/odd coordinate][word]
 #pragma unroll
-        for (int tp = 0; tp < 2; tp++) {
+        for (int tp = 0; tp < 2; tp++)
 #pragma unroll
-          for (int wi = 0; wi < 2; wi++) {
-            const uint32_t wa = wi ? V.vhi[2 * tp] : V.vlo[2 * tp];
-            const uint32_t wz = wi ? V.vhi[2 * tp + 1] : V.vlo[2 * tp + 1];
-            if constexpr (VB == 4) {
-              ev[tp][0][wi] = (wa & 0x0F0F0F0Fu) | ((wz << 4) & 0xF0F0F0F0u);  // byte k: coordinate 2k
-              ev[tp][1][wi] = ((wa >> 4) & 0x0F0F0F0Fu) | (wz & 0xF0F0F0F0u);  // byte k: coordinate 2k+1
-            } else if constexpr (VB == 2) {
-              ev[tp][0][wi] = (wa & 0x33333333u) | ((wz << 2) & 0xCCCCCCCCu);  // nibble k: coordinate 2k
-              ev[tp][1][wi] = ((wa >> 2) & 0x33333333u) | (wz & 0xCCCCCCCCu);  // nibble k: coordinate 2k+1
-            } else {
-              ev[tp][0][wi] = 0u;
-              ev[tp][1][wi] = 0u;
-            }
+          for (int eo = 0; eo < 2; eo++) {
+            ev[tp][eo][0] = V.vlo[2 * tp + eo];
+            ev[tp][eo][1] = V.vhi[2 * tp + eo];
           }
-        }
         // token group s (tokens 8s + 2t, 8s + 2t + 1 in this lane's A
         // registers), m-tile mt: A rows r / r+8 of half h are coordinates
         // 16r + 4mt + 2h / 16r + 4mt + 2h + 1, so av[q] is coordinate 16r + 4mt + q
@@ -834,16 +815,8 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
             } else {
 #pragma unroll
               for (int q = 0; q < 4; q++) {
-                uint32_t addr;
-                if constexpr (VB == 4) {
-                  // byte k of ev[s][eo][wi] is coordinate 8wi + 2k + eo
-                  addr = __byte_perm(ev[s][q & 1][mt >> 1], laneV, 0x7604 | ((2 * (mt & 1) + (q >> 1)) << 4));
-                } else {  // 3-bit: gather the two codes of coordinate 16r + 4mt + q
-                  const int p3 = 3 * (4 * mt + q);
-                  addr = field_at<8>(V.vlo[2 * s], V.vhi[2 * s], p3, 3, laneV) |
-                         field_at<11>(V.vlo[2 * s + 1], V.vhi[2 * s + 1], p3, 3, 0u);
-                }
-                av[q] = lut32(addr);
+                // 4-bit: byte k of ev[s][eo][wi] is coordinate 8wi + 2k + eo
+                av[q] = lut32(__byte_perm(ev[s][q & 1][mt >> 1], laneV, 0x7604 | ((2 * (mt & 1) + (q >> 1)) << 4)));
               }
             }
 #pragma unroll

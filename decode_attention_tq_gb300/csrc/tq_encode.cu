@@ -114,10 +114,12 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
       }
     } else {
       uint32_t w[BITS];
-      if (a.grouped)
-        load_codes_grouped<BITS>(slab + a.codes_off, off, q, w);
-      else
+      if (!a.grouped)
         load_codes<BITS>(slab + a.codes_off + off * a.code_bytes + q * 4 * BITS, w);
+      else if constexpr (value_pairs_interleaved(BITS))
+        load_codes_pair<BITS>(slab + a.codes_off, off, q, w);
+      else
+        load_codes_grouped<BITS>(slab + a.codes_off, off, q, w);
       int idx[32];
       unpack_codes<BITS>(w, idx);
 #pragma unroll

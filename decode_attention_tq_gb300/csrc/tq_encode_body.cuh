@@ -37,62 +37,58 @@ __device__ __forceinline__ void unpack_codes(const uint32_t (&w)[BITS], int (&id
   }
 }
 
-template <int BITS>
-__device__ __forceinline__ void store_codes(uint8_t *p, const uint32_t (&w)[BITS]) {
-  if constexpr (BITS == 4) {
-    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-  } else if constexpr (BITS == 2) {
-    *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
-  } else {
-#pragma unroll
-    for (int k = 0; k < BITS; k++) reinterpret_cast<uint32_t *>(p)[k] = w[k];
-  }
-}
-
-// The same 4*BITS bytes (chunks 2q and 2q+1 of a token) in a grouped
-// value-code section (value_chunk_offset).
-template <int BITS>
-__device__ __forceinline__ void store_codes_grouped(uint8_t *sec, int64_t off, int q, const uint32_t (&w)[BITS]) {
-  uint8_t *c0 = sec + value_chunk_offset(off, 2 * q, BITS);
-  uint8_t *c1 = sec + value_chunk_offset(off, 2 * q + 1, BITS);
-  if constexpr (BITS == 4) {
-    *reinterpret_cast<uint2 *>(c0) = make_uint2(w[0], w[1]);
-    *reinterpret_cast<uint2 *>(c1) = make_uint2(w[2], w[3]);
-  } else if constexpr (BITS == 2) {
-    *reinterpret_cast<uint32_t *>(c0) = w[0];
-    *reinterpret_cast<uint32_t *>(c1) = w[1];
-  } else {  // 6-byte chunks: 4-byte aligned for even offsets, 2 bytes past that for odd ones
-    const uint32_t lo0 = w[0], hi0 = w[1] & 0xFFFFu;                   // chunk 2q: bytes 0..5
-    const uint32_t lo1 = __byte_perm(w[1], w[2], 0x5432), hi1 = w[2] >> 16;  // chunk 2q+1: bytes 6..11
-    if ((off & 1) == 0) {
-      *reinterpret_cast<uint32_t *>(c0) = lo0;
-      *reinterpret_cast<uint16_t *>(c0 + 4) = (uint16_t)hi0;
-      *reinterpret_cast<uint32_t *>(c1) = lo1;
-      *reinterpret_cast<uint16_t *>(c1 + 4) = (uint16_t)hi1;
-    } else {
-      *reinterpret_cast<uint16_t *>(c0) = (uint16_t)lo0;
-      *reinterpret_cast<uint32_t *>(c0 + 2) = (lo0 >> 16) | (hi0 << 16);
-      *reinterpret_cast<uint16_t *>(c1) = (uint16_t)lo1;
-      *reinterpret_cast<uint32_t *>(c1 + 2) = (lo1 >> 16) | (hi1 << 16);
-    }
-  }
-}
-
+// Chunks 2q and 2q+1 of a token (4*BITS bytes of its stream) in a grouped
+// value-code section whose chunks are whole (3-bit codes: 6-byte chunks,
+// 4-byte aligned for even page offsets, 2 bytes past that for odd ones).
 template <int BITS>
 __device__ __forceinline__ void load_codes_grouped(const uint8_t *sec, int64_t off, int q, uint32_t (&w)[BITS]) {
-  const uint8_t *c0 = sec + value_chunk_offset(off, 2 * q, BITS);
-  const uint8_t *c1 = sec + value_chunk_offset(off, 2 * q + 1, BITS);
-  if constexpr (BITS == 4) {
-    const uint2 x = *reinterpret_cast<const uint2 *>(c0), y = *reinterpret_cast<const uint2 *>(c1);
-    w[0] = x.x; w[1] = x.y; w[2] = y.x; w[3] = y.y;
-  } else if constexpr (BITS == 2) {
-    w[0] = *reinterpret_cast<const uint32_t *>(c0);
-    w[1] = *reinterpret_cast<const uint32_t *>(c1);
-  } else {
-    const uint16_t *h0 = reinterpret_cast<const uint16_t *>(c0), *h1 = reinterpret_cast<const uint16_t *>(c1);
-    w[0] = (uint32_t)h0[0] | ((uint32_t)h0[1] << 16);
-    w[1] = (uint32_t)h0[2] | ((uint32_t)h1[0] << 16);
-    w[2] = (uint32_t)h1[1] | ((uint32_t)h1[2] << 16);
+  static_assert(BITS == 3, "2- and 4-bit value codes are pair-interleaved (load_codes_pair)");
+  const uint16_t *h0 = reinterpret_cast<const uint16_t *>(sec + value_chunk_offset(off, 2 * q, BITS));
+  const uint16_t *h1 = reinterpret_cast<const uint16_t *>(sec + value_chunk_offset(off, 2 * q + 1, BITS));
+  w[0] = (uint32_t)h0[0] | ((uint32_t)h0[1] << 16);
+  w[1] = (uint32_t)h0[2] | ((uint32_t)h1[0] << 16);
+  w[2] = (uint32_t)h1[1] | ((uint32_t)h1[2] << 16);
+}
+
+// Pair-interleaved value codes (value_pairs_interleaved): the bits of a
+// 32-bit word of the pair's even- or odd-coordinate stream that belong to
+// the token at offset parity m.
+template <int BITS>
+__host__ __device__ constexpr uint32_t pair_mask(int m) {
+  constexpr uint32_t lo = BITS == 4 ? 0x0F0F0F0Fu : 0x33333333u;
+  return m ? ~lo : lo;
+}
+// Word i of a token's own chunk stream (16 coordinates, LSB-first) from words
+// i of the pair's even (E) and odd (O) coordinate streams.
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_split(uint32_t E, uint32_t O, int m) {
+  constexpr uint32_t lo = pair_mask<BITS>(0);
+  return m ? (((E >> BITS) & lo) | (O & ~lo)) : ((E & lo) | ((O & lo) << BITS));
+}
+// The inverse: a token's chunk-stream word T to its bits of E and O.
+template <int BITS>
+__device__ __forceinline__ void pair_merge(uint32_t T, int m, uint32_t &e, uint32_t &o) {
+  constexpr uint32_t lo = pair_mask<BITS>(0);
+  e = m ? ((T << BITS) & ~lo) : (T & lo);
+  o = m ? (T & ~lo) : ((T >> BITS) & lo);
+}
+
+// Chunks 2q and 2q+1 of the token at page offset `off` (4*BITS bytes of its
+// own stream) from a pair-interleaved value-code section.
+template <int BITS>
+__device__ __forceinline__ void load_codes_pair(const uint8_t *sec, int64_t off, int q, uint32_t (&w)[BITS]) {
+  const int m = (int)(off & 1);
+#pragma unroll
+  for (int i = 0; i < 2; i++) {
+    const uint8_t *pr = sec + value_chunk_offset(off & ~(int64_t)1, 2 * q + i, BITS);
+    if constexpr (BITS == 4) {
+      const uint4 x = *reinterpret_cast<const uint4 *>(pr);  // E0 E1 O0 O1
+      w[2 * i] = pair_split<4>(x.x, x.z, m);
+      w[2 * i + 1] = pair_split<4>(x.y, x.w, m);
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2 *>(pr);  // E O
+      w[i] = pair_split<2>(x.x, x.y, m);
+    }
   }
 }
 
@@ -311,19 +307,38 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
       hb[ks][nt][1] = had_pair(8 * q + 4 * ks + 2, 8 * q + 4 * ks + 3, j);
     }
 
-  for (int64_t vb = (int64_t)warp * 8; vb < NH; vb += nwarps * 8) {
+  // Pair-interleaved value codes: vectors in pair-major order, quads 2i and
+  // 2i+1 of a warp holding tokens 2k and 2k+1 of one head, so that the two
+  // tokens of an offset pair, where they come in order, sit in neighbouring
+  // quads and one of them writes the words they share.
+  constexpr bool kPairCodes = !MIXED && value_pairs_interleaved(BITS);
+  const bool pairs = kPairCodes && a.grouped;
+  const int64_t NV = pairs ? ((a.n_tokens + 1) & ~(int64_t)1) * a.H : NH;
+  for (int64_t vb = (int64_t)warp * 8; vb < NV; vb += nwarps * 8) {
     const int64_t v = vb + quad_in_warp;
-    const bool in_range = v < NH;
-    const int64_t vv = in_range ? v : NH - 1;
     int64_t n;
     int h;
-    if (small) {  // 32-bit division for the common sizes
-      n = (uint32_t)vv / (uint32_t)a.H;
-      h = (int)((uint32_t)vv - (uint32_t)n * (uint32_t)a.H);
+    bool in_range;
+    if (pairs) {
+      const int64_t H2 = 2 * (int64_t)a.H;
+      const int64_t k = small ? (int64_t)((uint32_t)v / (uint32_t)H2) : v / H2;
+      const int rem = (int)(v - k * H2);
+      n = 2 * k + (rem & 1);
+      h = rem >> 1;
+      in_range = n < a.n_tokens;
+      if (!in_range) n = a.n_tokens - 1;
     } else {
-      n = vv / a.H;
-      h = (int)(vv % a.H);
+      in_range = v < NH;
+      const int64_t vc = in_range ? v : NH - 1;
+      if (small) {  // 32-bit division for the common sizes
+        n = (uint32_t)vc / (uint32_t)a.H;
+        h = (int)((uint32_t)vc - (uint32_t)n * (uint32_t)a.H);
+      } else {
+        n = vc / a.H;
+        h = (int)(vc % a.H);
+      }
     }
+    const int64_t vv = n * a.H + h;
     const int64_t slot = a.slot_mapping[n];
     bool ok = in_range && slot >= 0;
     if (ok && slot >= pool_slots) {
@@ -454,6 +469,46 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
         }
       }
       if (q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nstore;
+    } else if (kPairCodes && pairs) {
+      // this lane's 8 codes of block c are half q&1 of chunk 2c + q/2, i.e.
+      // BITS bytes at byte (q&1)*BITS of each of the pair's two streams.  The
+      // offset partner in the neighbouring quad: the even-offset token writes
+      // both tokens' words; otherwise each token sets its own bits atomically
+      // (its partner may be written by another warp of this launch).
+      const int64_t pslot = __shfl_xor_sync(0xffffffffu, ok ? slot : (int64_t)-1, 4);
+      const bool paired = ok && pslot == (slot ^ 1);
+      const int m = (int)(off & 1), hq = q & 1;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        uint32_t w = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; i++) w += (uint32_t)idx[8 * c + i] << (BITS * i);
+        if (zero) w = 0u;
+        uint32_t e, o;
+        pair_merge<BITS>(BITS == 4 ? w : w << (16 * hq), m, e, o);
+        const uint32_t pe = __shfl_xor_sync(0xffffffffu, e, 4), po = __shfl_xor_sync(0xffffffffu, o, 4);
+        uint8_t *pr = slab + a.codes_off + value_chunk_offset(off & ~(int64_t)1, 2 * c + (q >> 1), BITS);
+        if (paired) {
+          if (m == 0) {
+            if constexpr (BITS == 4) {
+              reinterpret_cast<uint32_t *>(pr)[hq] = e | pe;
+              reinterpret_cast<uint32_t *>(pr + 8)[hq] = o | po;
+            } else {
+              reinterpret_cast<uint16_t *>(pr)[hq] = (uint16_t)((e | pe) >> (16 * hq));
+              reinterpret_cast<uint16_t *>(pr + 4)[hq] = (uint16_t)((o | po) >> (16 * hq));
+            }
+          }
+        } else if (ok) {
+          unsigned *E = reinterpret_cast<unsigned *>(pr + (BITS == 4 ? 4 * hq : 0));
+          unsigned *O = reinterpret_cast<unsigned *>(pr + 2 * BITS + (BITS == 4 ? 4 * hq : 0));
+          const uint32_t own = pair_mask<BITS>(m) & (BITS == 4 ? 0xFFFFFFFFu : 0xFFFFu << (16 * hq));
+          atomicAnd(E, ~own);
+          atomicOr(E, e);
+          atomicAnd(O, ~own);
+          atomicOr(O, o);
+        }
+      }
+      if (ok && q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nstore;
     } else if (ok) {
 #pragma unroll
       for (int c = 0; c < 4; c++) {

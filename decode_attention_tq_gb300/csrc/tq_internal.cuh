@@ -19,7 +19,8 @@ struct EncodeArgs {
   int64_t num_pages, page_bytes, slab_bytes;
   int64_t norm_off, codes_off, gamma_off, signs_off;
   int code_bytes;
-  bool grouped;  // value-code stream: 16-token groups, chunk-major (value_chunk_offset)
+  bool grouped;  // value-code stream: 16-token groups, chunk-major (value_chunk_offset),
+                 // offset pairs interleaved for 2- and 4-bit codes (value_pairs_interleaved)
   bool norm_correct;  // store n / ||y_hat|| (no QJL)
   const uint8_t *signs;
   const float *codebook;
@@ -67,6 +68,15 @@ __host__ __device__ __forceinline__ int64_t value_chunk_offset(int64_t off, int 
   const int slot = 4 * ((i & 7) >> 1) + 2 * (i >> 3) + (i & 1);
   return (off >> 4) * (2 * kD * bits) + (int64_t)r * (16 * 2 * bits) + slot * (2 * bits);  // group = 16 * kD * bits / 8 bytes
 }
+
+// 2- and 4-bit value codes interleave the tokens of each page-offset pair
+// (2p, 2p+1) inside their two chunk slots: the pair's 4*bits bytes are two
+// LSB-first streams of bits-wide fields, the even coordinates c of the chunk
+// first, then the odd ones, field 2 (c div 2) + (offset mod 2) holding the
+// code of coordinate c of one of the two tokens.  The attention kernel then
+// reads, for a pair of tokens, one register of both tokens' codes per two
+// coordinates as stored.
+__host__ __device__ constexpr bool value_pairs_interleaved(int bits) { return bits == 2 || bits == 4; }
 
 // Workspace header written by the prep kernel and read by the others.
 struct AttnHeader {

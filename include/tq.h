@@ -106,7 +106,16 @@ typedef struct {
  *   s(i) = 4*((i mod 8) div 2) + 2*(i div 8) + (i mod 2)
  * (tokens in the order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15), so that the
  * attention kernel reads chunk r of the four tokens one thread multiplies in
- * one contiguous load. */
+ * one contiguous load.  For b_V = 2 and 4 the two tokens of an offset pair
+ * (2p, 2p+1) share their two chunk slots (4*b_V bytes from the slot of 2p):
+ * bit (c mod 2)*16*b_V + (c div 2)*2*b_V + (offset mod 2)*b_V + k holds bit k
+ * of the code of chunk coordinate c, i.e. the even coordinates first, then
+ * the odd ones, the pair's two codes of one coordinate side by side; the
+ * attention kernel takes one 32-bit word of that as a tensor-core operand
+ * register of both tokens.  Other widths keep each chunk as the token's own
+ * stream.  An encode of one token of a pair leaves the partner's bits as they
+ * were (the bits are set atomically unless both tokens come in one call in
+ * order). */
 typedef struct {
   int64_t slab_bytes, page_bytes;
   int64_t k_norm, k_gamma, k_codes, k_signs, v_norm, v_codes;
@@ -145,7 +154,11 @@ tq_status tq_page_layout(const tq_format *fmt, tq_layout *out);
  * story'.  An all-zero vector stores n = 0, gamma = 0, all codes/bits 0.
  *   x_f16        device fp16 [N][H][d]
  *   slot_mapping device int32 [N]; token n goes to page slot/P, offset slot%P;
- *                a negative slot skips the token
+ *                a negative slot skips the token; two tokens with one slot
+ *                in one call race (which one is stored is not defined).
+ *                2- and 4-bit values are written fastest when tokens 2k and
+ *                2k+1 go to offsets 2p and 2p+1 of one page (their shared
+ *                words in one store, see tq_layout)
  *   page_pool    device bytes [num_pages * page_bytes], 16-byte aligned
  *   signs        device uint8 [d], 1 = negate coordinate (the kind's D)
  *   codebook     device fp32 [2^b + 2^b - 1] for this kind's b
@@ -380,8 +393,9 @@ typedef struct {
 /* One pool per layer = [num_pages][H] head-slabs; per slab, each section
  * 16-byte aligned: K (scale, zero) fp16 pairs [d] (this page's per-channel
  * groups), K codes [P][d*b_K/8] (LSB-first per token), V (scale, zero) fp16
- * pairs [P], V codes (P*d*b_V/8 bytes in the grouped order of tq_layout's
- * value section). */
+ * pairs [P], V codes (P*d*b_V/8 bytes in the grouped chunk order of
+ * tq_layout's value section, each chunk the token's own LSB-first stream at
+ * every width). */
 typedef struct {
   int64_t slab_bytes, page_bytes;
   int64_t k_params, k_codes, v_params, v_codes;

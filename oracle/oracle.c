@@ -50,9 +50,11 @@
  *     bit l; byte k of the stream holds stream bits [8k, 8k+8).
  *   - Page body: the passage's section order, each section 16-byte aligned,
  *     pages of a multiple of 16 tokens and d a multiple of 16.  The value
- *     code stream keeps each token's bitstream whole in 16-coordinate chunks
- *     (2*b bytes) but stores a group of 16 tokens chunk by chunk, tokens in
- *     the order 0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15 (v_chunk_pos).
+ *     code section stores a group of 16 tokens chunk by chunk (16
+ *     coordinates, 2*b bytes of each token), tokens in the order 0,1,8,9,
+ *     2,3,10,11, 4,5,12,13, 6,7,14,15 (v_chunk_pos); for b = 2 and 4 the two
+ *     tokens of an offset pair interleave their codes coordinate by
+ *     coordinate inside their 4*b bytes (v_code_bit).
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared oracle.c -lm   (no fast-math)
  */
@@ -427,12 +429,42 @@ static int64_t v_chunk_pos(int64_t off, int r, int d, int vb) {
   return grp * 16 * token_bytes + (int64_t)r * 16 * chunk_bytes + (int64_t)slot * chunk_bytes;
 }
 
-static void put_v_codes(uint8_t *section, int64_t off, int d, int vb, const uint8_t *stream) {
-  for (int r = 0; r < d / 16; r++) memcpy(section + v_chunk_pos(off, r, d, vb), stream + 2 * vb * r, (size_t)(2 * vb));
+/*
+ * Bit position, inside the value-code section, of bit k of the code of
+ * coordinate j of the token at page offset `off`.  For 2- and 4-bit codes the
+ * tokens of an offset pair (2p, 2p+1) share the 4*vb bytes of their two chunk
+ * slots, as two bitstreams of vb-bit fields: the even coordinates first, then
+ * the odd ones, and in each the two tokens' codes of one coordinate side by
+ * side (even offset first).  Other widths keep each token's chunk whole.
+ */
+static int64_t v_code_bit(int64_t off, int j, int k, int d, int vb) {
+  int r = j / 16, c = j % 16;
+  if (vb == 2 || vb == 4) {
+    int64_t pair = v_chunk_pos(off - off % 2, r, d, vb);
+    return 8 * pair + (int64_t)(c % 2) * 16 * vb + (int64_t)(c / 2) * 2 * vb + (off % 2) * vb + k;
+  }
+  return 8 * v_chunk_pos(off, r, d, vb) + (int64_t)c * vb + k;
 }
 
-static void get_v_codes(const uint8_t *section, int64_t off, int d, int vb, uint8_t *stream) {
-  for (int r = 0; r < d / 16; r++) memcpy(stream + 2 * vb * r, section + v_chunk_pos(off, r, d, vb), (size_t)(2 * vb));
+/* Writes the token's d codes (bits of nothing else change). */
+static void put_v_codes(uint8_t *section, int64_t off, int d, int vb, const int32_t *idx) {
+  for (int j = 0; j < d; j++)
+    for (int k = 0; k < vb; k++) {
+      int64_t bit = v_code_bit(off, j, k, d, vb);
+      uint8_t m = (uint8_t)(1u << (bit % 8));
+      if ((idx[j] >> k) & 1) section[bit / 8] |= m;
+      else section[bit / 8] &= (uint8_t)~m;
+    }
+}
+
+static void get_v_codes(const uint8_t *section, int64_t off, int d, int vb, int32_t *idx) {
+  for (int j = 0; j < d; j++) {
+    idx[j] = 0;
+    for (int k = 0; k < vb; k++) {
+      int64_t bit = v_code_bit(off, j, k, d, vb);
+      idx[j] |= ((section[bit / 8] >> (bit % 8)) & 1) << k;
+    }
+  }
 }
 
 /*
@@ -440,7 +472,7 @@ static void get_v_codes(const uint8_t *section, int64_t off, int d, int vb, uint
  * the section order of the packed-format passage: K norms (fp32 [P]),
  * K QJL gammas (fp32 [P], QJL only), K codes ([P][d*kb/8]), K sign bits
  * ([P][m/8], QJL only), V norms (fp32 [P]), V codes (P*d*vb/8 bytes in
- * 16-token groups, see v_chunk_pos); every section starts on a 16-byte
+ * 16-token groups, see v_code_bit); every section starts on a 16-byte
  * boundary and the slab is padded to 16 bytes.  P and d are multiples of 16.
  */
 int orc_page_layout(const orc_format *f, orc_layout *L) {
@@ -503,12 +535,11 @@ int orc_encode(const orc_format *f, int kind, const uint16_t *x, int64_t N, cons
   const float *lo_t = mixed ? midpoints + (1 << bits) - 1 : NULL;
   int qjl = (kind == 0) && f->k_qjl;
   int m = qjl ? f->qjl_m : 0;
-  int code_bytes = kind == 0 ? L.k_code_bytes : L.v_code_bytes;
+  int code_bytes = L.k_code_bytes;
   double *xv = (double *)malloc(sizeof(double) * d);
   int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * d);
   uint8_t *z = (uint8_t *)malloc((size_t)(m > 0 ? m : 1));
   int32_t *zi = (int32_t *)malloc(sizeof(int32_t) * (m > 0 ? m : 1));
-  uint8_t *stream = (uint8_t *)malloc((size_t)code_bytes);
   int rc = ORC_OK;
   for (int64_t n = 0; n < N; n++) {
     int64_t slot = slot_mapping[n];
@@ -538,12 +569,10 @@ int orc_encode(const orc_format *f, int kind, const uint16_t *x, int64_t N, cons
         }
       } else {
         put_f32(slab + L.v_norm + 4 * off, (float)norm);
-        orc_pack_bits(d, bits, idx, stream);
-        put_v_codes(slab + L.v_codes, off, d, bits, stream);
+        put_v_codes(slab + L.v_codes, off, d, bits, idx);
       }
     }
   }
-  free(stream);
   free(xv);
   free(idx);
   free(z);
@@ -573,9 +602,7 @@ static void decode_slot(const orc_format *f, const orc_layout *L, int kind, cons
                       mixed ? centroids + (1 << bits) : NULL);
   } else {
     double norm = get_f32(slab + L->v_norm + 4 * off);
-    uint8_t stream[L->v_code_bytes];
-    get_v_codes(slab + L->v_codes, off, d, f->v_bits, stream);
-    orc_unpack_bits(d, f->v_bits, stream, idx);
+    get_v_codes(slab + L->v_codes, off, d, f->v_bits, idx);
     orc_decode_vector(d, f->v_bits, 0, 0, norm, 0.0, idx, NULL, signs, centroids, NULL, out, 0.0, 0, NULL);
   }
 }

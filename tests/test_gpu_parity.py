@@ -60,7 +60,7 @@ def test_encode_matches_oracle(bits, kind, qjl):
     print("encode", bits, kind, qjl, st)
 
 
-@pytest.mark.parametrize("bits,kind,qjl", [(2, 0, 1), (3, 1, 0), (4, 0, 0), (4, 0, 1)])
+@pytest.mark.parametrize("bits,kind,qjl", [(2, 0, 1), (3, 1, 0), (4, 0, 0), (4, 0, 1), (2, 1, 0), (4, 1, 0)])
 def test_decode_matches_oracle(bits, kind, qjl):
     fmt = ti.Format(128, bits, bits, qjl, 128, 32, 2)
     N = 150
@@ -345,7 +345,7 @@ def test_append_window_matches_oracle(kb, vb, qjl, W, kmix):
 def _check_append_pages(fmt, pool, pool_ref, lay, evicted, num_pages, ks, vs, kcb, vcb, S):
     """Pages after appends: the evicted tokens, field by field against a direct
     oracle encode of them (each kind in its own pass)."""
-    from tq_testlib import written_mask
+    from tq_testlib import merge_bits, written_mask
     slots = np.array([e[1] for e in evicted], np.int32)
     assert len(slots) > 0
     for kind in (0, 1):
@@ -355,8 +355,7 @@ def _check_append_pages(fmt, pool, pool_ref, lay, evicted, num_pages, ks, vs, kc
                                       *(kcb if kind == 0 else vcb), S if kind == 0 else None, diagnostics=True)
         assert rc == 0
         other = written_mask(len(pool_ref), lay, fmt, 1 - kind, slots)
-        pg = pool.copy()
-        pg[other] = pool_ref[other]  # the other kind is checked in its own pass
+        pg = merge_bits(pool, pool_ref, other)  # the other kind is checked in its own pass
         compare_encoded(pg, pool_ref, lay, fmt, kind, slots, cm, sm)
 
 
@@ -507,3 +506,49 @@ def test_encode_random_formats_match_oracle(case):
     neg = (N - 1,) if N > 3 else ()
     pool, pool_ref, lay, slots, cm, sm, *_ = _encode_case(fmt, kind, N, seed=seed, zero_rows=zero, neg_slots=neg)
     compare_encoded(pool, pool_ref, lay, fmt, kind, slots, cm, sm)
+
+
+@pytest.mark.parametrize("vb,H", [(4, 1), (4, 3), (2, 2)])
+def test_encode_value_pairs_every_store_path(vb, H):
+    """2- and 4-bit value codes share bytes between the tokens of an offset
+    pair (2p, 2p+1).  Two calls whose slots take every store path: pairs in
+    order (one store of both tokens' words), reversed and misaligned pairs,
+    a pair split over two pages, a live token whose partner is skipped, a
+    lone last token, partners that arrive in the second call, and tokens the
+    second call overwrites.  The pool after both calls equals the oracle's
+    after the same two calls (codes up to the boundary exemption), and no
+    bit outside the written codes changes."""
+    fmt = ti.Format(128, 4, vb, 0, 128, 64, H)
+    d, P = 128, 64
+    num_pages = 4
+    A, Bp = 1 * P, 3 * P  # slot bases of pages 1 and 3
+    s1 = ([A + i for i in range(20)]            # in order: pairs (0,1) .. (18,19)
+          + [A + 33, A + 32]                    # a reversed pair
+          + [A + 41, A + 42, A + 43, A + 44]    # misaligned: no two neighbours are partners
+          + [Bp + 2, A + 3 + 60]                # neighbours on different pages
+          + [A + 50, -1]                        # live token, skipped neighbour
+          + [A + 52])                           # lone last token (odd count)
+    s2 = [A + 51, A + 53, A + 0, A + 7, Bp + 3]  # partners of earlier tokens, overwrites of 0 and 7
+    lay = oracle.page_layout(fmt)
+    signs = ti.sign_bits(ti.SEED_SIGNS_V, d)
+    c, t = oracle.kind_codebook(fmt, 1)
+    x1 = ti.kv_history(1, len(s1), H, d, 3, 1)[0].numpy()
+    x2 = ti.kv_history(1, len(s2), H, d, 4, 1)[0].numpy()
+    s1, s2 = np.array(s1, np.int32), np.array(s2, np.int32)
+    pool_ref = np.full(num_pages * lay["page_bytes"], 0xA5, np.uint8)
+    r1 = oracle.encode(fmt, 1, x1, s1, pool_ref, num_pages, signs, c, t, diagnostics=True)
+    r2 = oracle.encode(fmt, 1, x2, s2, pool_ref, num_pages, signs, c, t, diagnostics=True)
+    assert r1[0] == 0 and r2[0] == 0
+    pool = torch.full((num_pages * lay["page_bytes"],), 0xA5, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cb = tq.kind_codebook(fmt, 1)
+    for x, s in ((x1, s1), (x2, s2)):
+        tq.tq_encode(fmt, 1, torch.from_numpy(x).cuda(), torch.from_numpy(s).cuda(), pool, num_pages,
+                     torch.from_numpy(signs).cuda(), cb, None, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    keep = ~np.isin(s1, s2)  # the final writer of each slot
+    slots = np.concatenate([s1[keep], s2])
+    cm = np.concatenate([r1[2][keep], r2[2]])
+    st = compare_encoded(pool.cpu().numpy(), pool_ref, lay, fmt, 1, slots, cm, None)
+    print("pairs", vb, H, st)

@@ -23,7 +23,7 @@ from scipy.special import softmax
 
 import oracle
 import tq_inputs as ti
-from tq_testlib import value_code_bytes
+from tq_testlib import value_codes
 
 
 # ---------------------------------------------------------------- bytes ----
@@ -220,7 +220,7 @@ def _rotated_domain_attention(fmt, s, b, qh):
             score += coef * float(gam) * (q_s @ (2.0 * z - 1.0))
         logits.append(float(nk) * score / math.sqrt(d))
         nv = slab[L["v_norm"] + 4 * off:][:4].view(np.float32)[0]
-        vidx = _unpack(value_code_bytes(slab[L["v_codes"]:][: P * L["v_code_bytes"]], off, d, fmt.v_bits), fmt.v_bits, d)
+        vidx = value_codes(slab[L["v_codes"]:][: P * L["v_code_bytes"]], off, d, fmt.v_bits)
         vrot.append(float(nv) * s["vc"].astype(np.float64)[vidx] / math.sqrt(d))
     nw = s["wl"][b] if s["kwin"] is not None else 0
     kw = s["kwin"][b, h, :nw].astype(np.float64) if nw else np.zeros((0, d))

@@ -233,3 +233,48 @@ def test_rotation_gaussianizes_heavy_tailed_vectors(golden):
     gs = rng.standard_normal((4000, d))
     kg = kurt(np.stack([oracle.rotate(v, s) for v in gs]))
     assert abs(kg.mean() + 6.0 / (d + 1)) < 4 * kg.std() / math.sqrt(len(kg))
+
+
+@pytest.mark.parametrize("vb", [2, 3, 4])
+def test_value_code_placement_by_hand(vb):
+    """Where the oracle puts value codes, written out byte by byte.  Section
+    rows of 16 coordinates hold 16 tokens of a group in the order 0,1,8,9,
+    2,3,10,11,...; 2- and 4-bit codes of an offset pair (2p, 2p+1) are
+    interleaved coordinate by coordinate, even coordinates first; 3-bit codes
+    keep each token's chunk as its own LSB-first stream.  Tokens at offsets 2
+    and 3 (a pair) and 9 (its partner 8 never written: zeros stay)."""
+    f = ti.Format(128, 4, vb, 0, 128, 16, 1)
+    lay = oracle.page_layout(f)
+    signs = ti.sign_bits(11, 128)
+    cen, mid = oracle.kind_codebook(f, 1)
+    X = ti.kv_history(1, 3, 1, 128, 0, 1).numpy()[0]
+    offs = [2, 3, 9]
+    pool = np.zeros(lay["page_bytes"], np.uint8)
+    assert oracle.encode(f, 1, X, np.array(offs, np.int32), pool, 1, signs, cen, mid) == 0
+    idx = [oracle.encode_vector(X[n, 0].astype(np.float64), vb, signs, cen, mid)["idx"] for n in range(3)]
+    sec = pool[lay["v_codes"]:lay["v_codes"] + 16 * 128 * vb // 8]
+    row = 16 * 2 * vb  # bytes of one 16-coordinate row of a token group
+    want = np.zeros_like(sec)
+    for r in range(8):
+        for c in range(16):
+            a, b, z = (int(idx[n][16 * r + c]) for n in range(3))
+            if vb == 4:
+                # tokens 2, 3 at slots 4, 5 (bytes 32..47 of the row): 8 bytes of
+                # even coordinates, then 8 of odd ones, one coordinate per byte,
+                # offset 2 in the low nibble; token 9 at slots 2, 3 (bytes 16..31)
+                # in the high nibbles
+                want[r * row + 32 + 8 * (c % 2) + c // 2] = a | (b << 4)
+                want[r * row + 16 + 8 * (c % 2) + c // 2] = z << 4
+            elif vb == 2:
+                # 4 bytes of even coordinates, then 4 of odd ones; a byte holds
+                # two coordinates, each as (even offset, odd offset) 2-bit codes
+                sh = 4 * ((c // 2) % 2)
+                want[r * row + 16 + 4 * (c % 2) + c // 4] |= (a | (b << 2)) << sh
+                want[r * row + 8 + 4 * (c % 2) + c // 4] |= (z << 2) << sh
+            else:
+                # 6-byte chunks: token 2 at slot 4, token 3 at 5, token 9 at 3
+                for tok, slot in ((a, 4), (b, 5), (z, 3)):
+                    for k in range(3):
+                        bit = 8 * (r * row + 6 * slot) + 3 * c + k
+                        want[bit // 8] |= ((tok >> k) & 1) << (bit % 8)
+    assert np.array_equal(sec, want)

@@ -16,17 +16,35 @@ REL_NORM = 1e-6   # stored fp32 norms and QJL gammas, relative (their summation 
 
 
 def value_chunk_pos(off: int, r: int, d: int, vb: int) -> int:
-    """Byte position in the value-code section of chunk r (coordinates
-    16r..16r+15) of the token at page offset `off`: 16-token groups stored
-    chunk by chunk, tokens in the order 0,1,8,9,2,3,10,11,..."""
+    """Byte position in the value-code section of the chunk slot r
+    (coordinates 16r..16r+15) of the token at page offset `off`: 16-token
+    groups stored chunk by chunk, tokens in the order 0,1,8,9,2,3,10,11,..."""
     g, i = divmod(off, 16)
     slot = 4 * ((i % 8) // 2) + 2 * (i // 8) + (i % 2)
     return g * 16 * (d * vb // 8) + r * 16 * (2 * vb) + slot * (2 * vb)
 
 
-def value_code_bytes(section: np.ndarray, off: int, d: int, vb: int) -> np.ndarray:
-    """The token's LSB-first code bitstream, gathered from a grouped section."""
-    return np.concatenate([section[value_chunk_pos(off, r, d, vb): value_chunk_pos(off, r, d, vb) + 2 * vb] for r in range(d // 16)])
+def value_code_bits(off: int, d: int, vb: int) -> np.ndarray:
+    """Bit positions [d, vb] in the value-code section of the token's codes
+    (bit k of coordinate j's code).  2- and 4-bit codes: the offset pair
+    (2p, 2p+1) shares its two chunk slots, even coordinates first, then the
+    odd ones, the pair's two codes of one coordinate side by side (even
+    offset first); other widths: the token's chunk holds its LSB-first codes."""
+    j = np.arange(d)[:, None]
+    k = np.arange(vb)[None, :]
+    r, c = j // 16, j % 16
+    if vb in (2, 4):
+        base = np.array([[8 * value_chunk_pos(off - off % 2, int(rr), d, vb)] for rr in r[:, 0]])
+        return base + (c % 2) * 16 * vb + (c // 2) * 2 * vb + (off % 2) * vb + k
+    base = np.array([[8 * value_chunk_pos(off, int(rr), d, vb)] for rr in r[:, 0]])
+    return base + c * vb + k
+
+
+def value_codes(section: np.ndarray, off: int, d: int, vb: int) -> np.ndarray:
+    """The token's d value codes read from a value-code section."""
+    pos = value_code_bits(off, d, vb)
+    bits = (section[pos // 8] >> (pos % 8).astype(np.uint8)) & 1
+    return (bits.astype(np.int64) << np.arange(vb)).sum(1)
 
 
 def unpack_field(pool: np.ndarray, lay: dict, fmt, kind: int, slots: np.ndarray):
@@ -48,13 +66,12 @@ def unpack_field(pool: np.ndarray, lay: dict, fmt, kind: int, slots: np.ndarray)
             no = lay["k_norm"] if kind == 0 else lay["v_norm"]
             co = lay["k_codes"] if kind == 0 else lay["v_codes"]
             norm[i, h] = pool[base + no + 4 * off: base + no + 4 * off + 4].view(np.float32)[0]
-            if kind == 0:
+            if kind == 1:
+                codes[i, h] = value_codes(pool[base + co: base + co + P * cb], off, d, bits)
+            elif getattr(fmt, "k_mixed", 0):
+                codes[i, h] = mixed_key_codes(pool[base + co + off * cb: base + co + (off + 1) * cb], d, bits)
+            else:
                 raw = pool[base + co + off * cb: base + co + (off + 1) * cb]
-            else:
-                raw = value_code_bytes(pool[base + co: base + co + P * cb], off, d, bits)
-            if kind == 0 and getattr(fmt, "k_mixed", 0):
-                codes[i, h] = mixed_key_codes(raw, d, bits)
-            else:
                 bitsarr = np.unpackbits(raw, bitorder="little").reshape(d, bits)
                 codes[i, h] = (bitsarr * (1 << np.arange(bits))).sum(1)
             if qjl:
@@ -79,9 +96,10 @@ def mixed_key_codes(raw: np.ndarray, d: int, b: int) -> np.ndarray:
 
 
 def written_mask(pool_len: int, lay: dict, fmt, kind: int, slots) -> np.ndarray:
-    """Boolean mask of the pool bytes an encode of `slots` may write."""
+    """Per pool byte, the mask (uint8) of the bits an encode of `slots` may
+    write (2- and 4-bit value codes share bytes with the offset partner)."""
     P, H = fmt.page_size, fmt.num_kv_heads
-    mask = np.zeros(pool_len, bool)
+    mask = np.zeros(pool_len, np.uint8)
     qjl = kind == 0 and fmt.k_qjl
     cb = lay["k_code_bytes"] if kind == 0 else lay["v_code_bytes"]
     for s in slots:
@@ -92,19 +110,22 @@ def written_mask(pool_len: int, lay: dict, fmt, kind: int, slots) -> np.ndarray:
             base = page * lay["page_bytes"] + h * lay["slab_bytes"]
             no = lay["k_norm"] if kind == 0 else lay["v_norm"]
             co = lay["k_codes"] if kind == 0 else lay["v_codes"]
-            mask[base + no + 4 * off: base + no + 4 * off + 4] = True
+            mask[base + no + 4 * off: base + no + 4 * off + 4] = 0xFF
             if kind == 0:
-                mask[base + co + off * cb: base + co + (off + 1) * cb] = True
+                mask[base + co + off * cb: base + co + (off + 1) * cb] = 0xFF
             else:
-                d, vb = fmt.head_dim, fmt.v_bits
-                for r in range(d // 16):
-                    pos = base + co + value_chunk_pos(off, r, d, vb)
-                    mask[pos: pos + 2 * vb] = True
+                pos = value_code_bits(off, fmt.head_dim, fmt.v_bits).ravel()
+                np.bitwise_or.at(mask, base + co + pos // 8, (1 << (pos % 8)).astype(np.uint8))
             if qjl:
-                mask[base + lay["k_gamma"] + 4 * off: base + lay["k_gamma"] + 4 * off + 4] = True
+                mask[base + lay["k_gamma"] + 4 * off: base + lay["k_gamma"] + 4 * off + 4] = 0xFF
                 sb = fmt.qjl_m // 8
-                mask[base + lay["k_signs"] + off * sb: base + lay["k_signs"] + (off + 1) * sb] = True
+                mask[base + lay["k_signs"] + off * sb: base + lay["k_signs"] + (off + 1) * sb] = 0xFF
     return mask
+
+
+def merge_bits(a: np.ndarray, b: np.ndarray, mask: np.ndarray) -> np.ndarray:
+    """Bytes of `a` with the bits in `mask` taken from `b`."""
+    return (a & ~mask) | (b & mask)
 
 
 def compare_encoded(pool_gpu, pool_ref, lay, fmt, kind, slots, code_margin, sign_margin):
@@ -139,7 +160,7 @@ def compare_encoded(pool_gpu, pool_ref, lay, fmt, kind, slots, code_margin, sign
                      gamma_max_rel=float(rel[vec_same].max(initial=0.0)))
     # bytes the encode must not touch are identical (both pools start from the same canary)
     mask = written_mask(len(pool_ref), lay, fmt, kind, slots)
-    assert np.array_equal(pool_gpu[~mask], pool_ref[~mask]), "bytes outside the written fields changed"
+    assert not np.any((pool_gpu ^ pool_ref) & ~mask), "bits outside the written fields changed"
     return stats
 
 
