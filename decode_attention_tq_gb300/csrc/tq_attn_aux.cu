@@ -2,14 +2,15 @@
 //   prep   : (one launch, three kinds of block) tile prefix sums and clamped
 //            lengths; each query rotated once into the key basis
 //            (q_rot = H (D_K . q)/sqrt(d)), projected for the QJL term
-//            (q_s = S q_rot), with power-of-two operand scales; and
+//            (q_s = S q_rot, one block per row), with power-of-two operand
+//            scales; and
 //            attention partials over the raw fp16 recent-token window, one
 //            per 32-token chunk;
 //   merge  : log-sum-exp merge of the compressed partials of a (sequence,
 //            query head), one inverse rotation of their value accumulator
 //            (D_V . H acc / d), then the window partials, normalised; one
-//            warp per (sequence, query head) when they have few partials, one
-//            128-thread block otherwise.
+//            warp per (sequence, query head) when they have few partials, a
+//            block of 16 warps sharing them otherwise.
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -59,14 +60,18 @@ __device__ void prep_lengths(const AttnArgs &a, int lane) {
   }
 }
 
-// One warp per query row: rotation, QJL projection, operand exponents.
-__device__ void prep_query(const AttnArgs &a, bool qjl, int64_t row, int lane, float *s_q) {
-  // lane holds coordinates 4*lane .. 4*lane+3
+// The query row rotated into the key basis, q_rot = H (D_K . q) / sqrt(d)
+// (a raw-domain KIVI cache takes the query as it is): lane holds
+// coordinates 4 lane .. 4 lane + 3.
+__device__ __forceinline__ void rotate_query(const AttnArgs &a, int64_t row, int lane, float (&x)[4]) {
   const uint2 raw = *reinterpret_cast<const uint2 *>(a.q + row * kD + 4 * lane);
   const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
   const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-  float x[4] = {f01.x, f01.y, f23.x, f23.y};
-  if (!a.raw) {  // a raw-domain (KIVI) cache takes the query as it is
+  x[0] = f01.x;
+  x[1] = f01.y;
+  x[2] = f23.x;
+  x[3] = f23.y;
+  if (!a.raw) {
 #pragma unroll
     for (int i = 0; i < 4; i++)
       if (a.k_signs[4 * lane + i]) x[i] = -x[i];
@@ -76,46 +81,65 @@ __device__ void prep_query(const AttnArgs &a, bool qjl, int64_t row, int lane, f
 #pragma unroll
     for (int i = 0; i < 4; i++) x[i] *= 0.08838834764831845f;  // 1/sqrt(128)
   }
+}
+
+// Power-of-two operand scale: the largest |value| lands in [2^12, 2^13).
+__device__ __forceinline__ int operand_exponent(float mx) { return mx > 0.f ? 12 - ilogbf(mx) : 0; }
+
+// Stores q_rot and its exponent (one warp).
+__device__ __forceinline__ void store_query(const AttnArgs &a, int64_t row, int lane, const float (&x)[4]) {
   float mx = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; i++) mx = fmaxf(mx, fabsf(x[i]));
   *reinterpret_cast<float4 *>(a.q_rot + row * kD + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
   mx = warp_max_xor(mx, 31);
-  // largest |value| lands in [2^12, 2^13) after scaling by 2^e
-  const int eq = mx > 0.f ? 12 - ilogbf(mx) : 0;
-  int es = 0;
-  if (qjl) {
+  if (lane == 0) a.q_exp[row * 2] = operand_exponent(mx);
+}
+
+// Without QJL: one warp per query row.
+__device__ void prep_query(const AttnArgs &a, int64_t row, int lane) {
+  float x[4];
+  rotate_query(a, row, lane, x);
+  store_query(a, row, lane, x);
+  if (lane == 0) a.q_exp[row * 2 + 1] = 0;
+}
+
+// With QJL: one 128-thread block per query row.  Every warp rotates the row
+// (a few shuffles); warp w projects it on S rows 32w .. 32w + 31, q_s = S q_rot:
+// lane holds coordinates 4 lane .. 4 lane + 3 and reads the same coordinates
+// of each S row (one coalesced 512-byte row per load, 16 rows in flight).
+// The 32 per-lane partial dots are summed over the warp by a transposing
+// butterfly (31 shuffles), after which lane l holds row 32w + l.
+__device__ void prep_query_qjl(const AttnArgs &a, int64_t row, int warp, int lane, float *s_red) {
+  float x[4];
+  rotate_query(a, row, lane, x);
+  if (warp == 0) store_query(a, row, lane, x);
+  float v[32];
+  const float4 *S4 = reinterpret_cast<const float4 *>(a.S + (int64_t)(32 * warp) * kD) + lane;
 #pragma unroll
-    for (int i = 0; i < 4; i++) s_q[4 * lane + i] = x[i];
-    __syncwarp();
-    // rows 4 lane .. 4 lane + 3 of S side by side, so that 16 loads are in
-    // flight per step instead of 4 rows one after another
-    float ys[4] = {0.f, 0.f, 0.f, 0.f};
-    const float4 *srow = reinterpret_cast<const float4 *>(a.S + (int64_t)(4 * lane) * kD);
-#pragma unroll 4
-    for (int k = 0; k < kD / 4; k++) {
-      float4 sv[4];
+  for (int half = 0; half < 2; half++) {
+    float4 sv[16];
 #pragma unroll
-      for (int i = 0; i < 4; i++) sv[i] = __ldg(srow + i * (kD / 4) + k);
+    for (int i = 0; i < 16; i++) sv[i] = __ldg(S4 + (16 * half + i) * (kD / 4));
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        ys[i] = fmaf(sv[i].x, s_q[4 * k], ys[i]);
-        ys[i] = fmaf(sv[i].y, s_q[4 * k + 1], ys[i]);
-        ys[i] = fmaf(sv[i].z, s_q[4 * k + 2], ys[i]);
-        ys[i] = fmaf(sv[i].w, s_q[4 * k + 3], ys[i]);
-      }
+    for (int i = 0; i < 16; i++) v[16 * half + i] = fmaf(sv[i].x, x[0], fmaf(sv[i].y, x[1], fmaf(sv[i].z, x[2], sv[i].w * x[3])));
+  }
+#pragma unroll
+  for (int m = 16, n = 16; m >= 1; m >>= 1, n >>= 1) {
+    // keep the half of the n pairs (v[i], v[i + n]) selected by lane bit m,
+    // add the partner's copy of it
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < n; i++) {
+      const float keep = up ? v[i + n] : v[i], send = up ? v[i] : v[i + n];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
     }
-    float my = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; i++) my = fmaxf(my, fabsf(ys[i]));
-    *reinterpret_cast<float4 *>(a.q_s + row * kM + 4 * lane) = make_float4(ys[0], ys[1], ys[2], ys[3]);
-    my = warp_max_xor(my, 31);
-    es = my > 0.f ? 12 - ilogbf(my) : 0;
   }
-  if (lane == 0) {
-    a.q_exp[row * 2] = eq;
-    a.q_exp[row * 2 + 1] = es;
-  }
+  a.q_s[row * kM + 32 * warp + lane] = v[0];
+  const float my = warp_max_xor(fabsf(v[0]), 31);
+  if (lane == 0) s_red[warp] = my;
+  __syncthreads();
+  if (threadIdx.x == 0) a.q_exp[row * 2 + 1] = operand_exponent(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
 }
 
 // Attention partial of the G query heads of (b, h) over window chunk c
@@ -236,8 +260,12 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
     return;
   }
   if (blockIdx.x == 0 && warp == 0) prep_lengths(a, lane);
-  const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // b * Hq + qh
-  if (row < (int64_t)a.B * a.Hq) prep_query(a, qjl, row, lane, s_q + warp * kQRow);
+  if (qjl) {
+    prep_query_qjl(a, blockIdx.x, warp, lane, s_q);  // one row per block (b * Hq + qh)
+  } else {
+    const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // b * Hq + qh
+    if (row < (int64_t)a.B * a.Hq) prep_query(a, row, lane);
+  }
 }
 
 // Warp that owns tile x: largest w in [0, NW) with floor(T*w/NW) <= x.
@@ -245,148 +273,6 @@ __device__ __forceinline__ int64_t tile_owner(int64_t x, int64_t T, int64_t NW) 
   const int64_t num = NW * (x + 1) + T - 1;
   const int64_t w = (num <= 0xffffffffll ? (int64_t)((uint32_t)num / (uint32_t)T) : num / T) - 1;  // 32-bit when it fits
   return w < NW - 1 ? w : NW - 1;
-}
-
-__device__ __forceinline__ float block_max128(float v, float *s_red) {
-  v = warp_max_xor(v, 31);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  const float r = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-  __syncthreads();
-  return r;
-}
-
-__device__ __forceinline__ float block_sum128(float v, float *s_red) {
-  v = warp_sum_xor(v, 31);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  const float r = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
-  __syncthreads();
-  return r;
-}
-
-// Block variant (rows with many partials): online log-sum-exp merge of n
-// partials (max, sum, accumulator column j = thread), 32 at a time: the
-// accumulator columns of a chunk are loaded into registers together with the
-// (max, sum) pairs, so a chunk costs one memory latency.
-template <class ML, class ACC>
-__device__ __forceinline__ void merge_partials_block(int64_t n, ML ml, ACC acc_of, float &M, float &L, float &A, float *s_w,
-                                               float *s_red) {
-  constexpr int kChunk = 32;
-  const int j = threadIdx.x;
-  for (int64_t c0 = 0; c0 < n; c0 += kChunk) {
-    const int cn = (int)min((int64_t)kChunk, n - c0);
-    float av[kChunk];
-#pragma unroll
-    for (int i = 0; i < kChunk; i++) av[i] = i < cn ? acc_of(c0 + i)[j] : 0.f;
-    float m = -INFINITY, l = 0.f;
-    if (j < cn) {
-      const float2 v = ml(c0 + j);
-      m = v.x;
-      l = v.y;
-    }
-    const float Mn = fmaxf(M, block_max128(m, s_red));
-    if (Mn == -INFINITY) continue;  // block-uniform
-    const float w = m == -INFINITY ? 0.f : exp2f(m - Mn);
-    if (j < kChunk) s_w[j] = w;
-    const float lsum = block_sum128(l * w, s_red);  // also publishes s_w
-    const float sold = exp2f(M - Mn);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-    for (int i = 0; i < kChunk; i += 4) {
-      a0 = fmaf(s_w[i], av[i], a0);
-      a1 = fmaf(s_w[i + 1], av[i + 1], a1);
-      a2 = fmaf(s_w[i + 2], av[i + 2], a2);
-      a3 = fmaf(s_w[i + 3], av[i + 3], a3);
-    }
-    A = A * sold + ((a0 + a1) + (a2 + a3));
-    L = L * sold + lsum;
-    M = Mn;
-    __syncthreads();  // s_w is rewritten by the next chunk
-  }
-}
-
-// Block variant: one 128-thread block per (sequence, query head) row, thread
-// = output coordinate.
-__global__ void __launch_bounds__(128) attn_merge_block_kernel(const AttnArgs a) {
-  __shared__ float s_x[kD];
-  __shared__ float s_w[128];
-  __shared__ float s_red[4];
-  griddep_wait();  // the main kernel's partials
-  const int64_t row = blockIdx.x;  // b * Hq + qh
-  const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
-  const int h = qh / a.G, g = qh % a.G;
-  const int j = threadIdx.x;
-  const int64_t T = a.hdr->total_tiles, NW = a.hdr->active_warps;
-  float mu = -INFINITY, l = 0.f, A = 0.f;
-  const int64_t tb = a.pre[b + 1] - a.pre[b];
-  // the window partials do not depend on the compressed merge: their loads
-  // are issued first (up to kWinPre chunks; longer windows read them later)
-  constexpr int kWinPre = 8;
-  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
-  const int64_t nwin = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
-  float wacc[kWinPre];
-  float2 wml = make_float2(-INFINITY, 0.f);
-  if (nwin <= kWinPre) {
-#pragma unroll
-    for (int i = 0; i < kWinPre; i++) wacc[i] = i < nwin ? a.win_acc[(row * nch + i) * kD + j] : 0.f;
-    if (j < nwin) wml = make_float2(a.win_ml[(row * nch + j) * 2], a.win_ml[(row * nch + j) * 2 + 1]);
-  }
-  if (tb > 0 && NW > 0) {
-    const int64_t o = a.H * a.pre[b] + h * tb;
-    const int64_t w0 = tile_owner(o, T, NW), w1 = tile_owner(o + tb - 1, T, NW);
-    const int64_t unit = (int64_t)b * a.H + h;
-    merge_partials_block(
-        w1 - w0 + 1,
-        [&](int64_t k) {
-          const int64_t w = w0 + k;
-          // a warp's range can only be empty when there are fewer tiles than warps
-          if (T < NW && T * w / NW >= T * (w + 1) / NW) return make_float2(-INFINITY, 0.f);
-          const int64_t base = (w + unit) * a.G + g;
-          return make_float2(a.seg_ml[base * 2], a.seg_ml[base * 2 + 1]);
-        },
-        [&](int64_t k) { return a.seg_acc + ((w0 + k + unit) * a.G + g) * kD; }, mu, l, A, s_w, s_red);
-  }
-  // inverse rotation of the rotated-domain accumulator: D_V . (H A) / d
-  // (a raw-domain KIVI accumulator is used as it is)
-  float x = A;
-  if (!a.raw) {
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, x, m);
-      x = (j & m) ? (o - x) : (x + o);
-    }
-#pragma unroll
-    for (int m = 32; m < kD; m <<= 1) {
-      s_x[j] = x;
-      __syncthreads();
-      const float o = s_x[j ^ m];
-      __syncthreads();
-      x = (j & m) ? (o - x) : (x + o);
-    }
-    x = (a.v_signs[j] ? -x : x) * (1.0f / (float)kD);
-  }
-
-  // window partials (raw domain): merged onto the compressed part
-  float M = mu, Lt = l, At = x;
-  if (nwin > 0 && nwin <= kWinPre) {
-    const float Mn = fmaxf(M, block_max128(wml.x, s_red));
-    const float w = wml.x == -INFINITY ? 0.f : exp2f(wml.x - Mn);
-    if (j < kWinPre) s_w[j] = w;
-    const float lsum = block_sum128(wml.y * w, s_red);  // also publishes s_w
-    const float sold = exp2f(M - Mn);
-    float aw = 0.f;
-#pragma unroll
-    for (int i = 0; i < kWinPre; i++) aw = fmaf(s_w[i], wacc[i], aw);
-    At = At * sold + aw;
-    Lt = Lt * sold + lsum;
-    M = Mn;
-  } else if (nwin > kWinPre) {
-    merge_partials_block(
-        nwin, [&](int64_t k) { return make_float2(a.win_ml[(row * nch + k) * 2], a.win_ml[(row * nch + k) * 2 + 1]); },
-        [&](int64_t k) { return a.win_acc + (row * nch + k) * kD; }, M, Lt, At, s_w, s_red);
-  }
-  a.out[row * kD + j] = (M != -INFINITY && Lt > 0.f) ? At / Lt : 0.f;
 }
 
 // Partials per chunk of the warp merge (32 float4 accumulators would spill).
@@ -446,50 +332,73 @@ __device__ __forceinline__ void merge_partials(int64_t n, ML ml, ACC acc_of, flo
   }
 }
 
-// Warp variant (rows with few partials): one warp per (sequence, query head)
-// row, four rows per block; no shared memory and no block barriers.
-__global__ void __launch_bounds__(128) attn_merge_warp_kernel(const AttnArgs a) {
-  griddep_wait();  // the main kernel's partials
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);  // b * Hq + qh
-  if (row >= (int64_t)a.B * a.Hq) return;
-  const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
-  const int h = qh / a.G, g = qh % a.G;
-  const int64_t T = a.hdr->total_tiles, NW = a.hdr->active_warps;
-  // the window partials do not depend on the compressed merge: up to kWinPre
-  // chunks are loaded first (longer windows are merged from memory later)
-  constexpr int kWinPre = 8;
-  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
-  const int64_t nwin = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
-  float4 wv[kWinPre];
-  float wm = -INFINITY, wl = 0.f;
-  if (nwin <= kWinPre) {
+// The compressed partials of (b, h): warps w0 .. w0 + n - 1 of the main
+// kernel, slot w + unit; n = 0 when the sequence has no compressed token.
+struct RowParts {
+  int64_t w0, n, unit, T, NW;
+};
+__device__ __forceinline__ RowParts row_parts(const AttnArgs &a, int b, int h) {
+  RowParts r;
+  r.T = a.hdr->total_tiles;
+  r.NW = a.hdr->active_warps;
+  r.unit = (int64_t)b * a.H + h;
+  r.w0 = 0;
+  r.n = 0;
+  const int64_t tb = a.pre[b + 1] - a.pre[b];
+  if (tb > 0 && r.NW > 0) {
+    const int64_t o = a.H * a.pre[b] + h * tb;
+    r.w0 = tile_owner(o, r.T, r.NW);
+    r.n = tile_owner(o + tb - 1, r.T, r.NW) - r.w0 + 1;
+  }
+  return r;
+}
+
+// Merge of partials k0 .. k1 - 1 of a row into the running (M, L, A) of a
+// warp, kChunk at a time.
+template <int kChunk>
+__device__ __forceinline__ void merge_row_range(const AttnArgs &a, const RowParts &r, int g, int64_t k0, int64_t k1, float &M,
+                                                float &L, float4 &A, int lane) {
+  merge_partials<kChunk>(
+      k1 - k0,
+      [&](int64_t k) {
+        const int64_t w = r.w0 + k0 + k;
+        // a warp's range can only be empty when there are fewer tiles than warps
+        if (r.T < r.NW && r.T * w / r.NW >= r.T * (w + 1) / r.NW) return make_float2(-INFINITY, 0.f);
+        return *reinterpret_cast<const float2 *>(a.seg_ml + ((w + r.unit) * a.G + g) * 2);
+      },
+      [&](int64_t k) { return a.seg_acc + ((r.w0 + k0 + k + r.unit) * a.G + g) * kD; }, M, L, A, lane);
+}
+
+// Window partials of a row: up to kWinPre chunks are loaded before the
+// compressed merge (they do not depend on it); longer windows are merged
+// from memory at the end.
+constexpr int kWinPre = 8;
+struct RowWindow {
+  float4 v[kWinPre];
+  float m, l;
+  int64_t n, nch;
+};
+__device__ __forceinline__ void row_window_load(const AttnArgs &a, int64_t row, int b, int lane, RowWindow &w) {
+  w.nch = (a.window + kWinChunk - 1) / kWinChunk;
+  w.n = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
+  w.m = -INFINITY;
+  w.l = 0.f;
+  if (w.n <= kWinPre) {
 #pragma unroll
     for (int u = 0; u < kWinPre; u++)
-      wv[u] = u < nwin ? reinterpret_cast<const float4 *>(a.win_acc + (row * nch + u) * kD)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane < nwin) {
-      const float2 v = *reinterpret_cast<const float2 *>(a.win_ml + (row * nch + lane) * 2);
-      wm = v.x;
-      wl = v.y;
+      w.v[u] = u < w.n ? reinterpret_cast<const float4 *>(a.win_acc + (row * w.nch + u) * kD)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < w.n) {
+      const float2 v = *reinterpret_cast<const float2 *>(a.win_ml + (row * w.nch + lane) * 2);
+      w.m = v.x;
+      w.l = v.y;
     }
   }
-  float M = -INFINITY, L = 0.f;
-  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int64_t tb = a.pre[b + 1] - a.pre[b];
-  if (tb > 0 && NW > 0) {
-    const int64_t o = a.H * a.pre[b] + h * tb;
-    const int64_t w0 = tile_owner(o, T, NW), w1 = tile_owner(o + tb - 1, T, NW);
-    const int64_t unit = (int64_t)b * a.H + h;
-    merge_partials<kWarpMergeMaxPartials>(
-        w1 - w0 + 1,
-        [&](int64_t k) {
-          const int64_t w = w0 + k;
-          // a warp's range can only be empty when there are fewer tiles than warps
-          if (T < NW && T * w / NW >= T * (w + 1) / NW) return make_float2(-INFINITY, 0.f);
-          return *reinterpret_cast<const float2 *>(a.seg_ml + ((w + unit) * a.G + g) * 2);
-        },
-        [&](int64_t k) { return a.seg_acc + ((w0 + k + unit) * a.G + g) * kD; }, M, L, A, lane);
-  }
+}
+
+// The end of a row's merge, one warp: inverse rotation of the compressed
+// accumulator, the window partials, normalisation, the output row.
+__device__ __forceinline__ void row_finish(const AttnArgs &a, int64_t row, int lane, const RowWindow &win, float M, float L,
+                                           float4 A) {
   // inverse rotation of the rotated-domain accumulator: D_V . (H A) / d
   // (a raw-domain KIVI accumulator is used as it is)
   if (!a.raw) {
@@ -501,16 +410,16 @@ __global__ void __launch_bounds__(128) attn_merge_warp_kernel(const AttnArgs a) 
     for (int i = 0; i < 4; i++) x[i] = (a.v_signs[4 * lane + i] ? -x[i] : x[i]) * (1.0f / (float)kD);
     A = make_float4(x[0], x[1], x[2], x[3]);
   }
-
   // window partials (raw domain), merged onto the compressed part
-  if (nwin > 0 && nwin <= kWinPre) {
+  if (win.n > 0 && win.n <= kWinPre) {
     float lsum;
-    const float w = chunk_weight(wm, wl, M, L, A, lsum);
-    chunk_accumulate(w, 0, wv, A);
+    const float w = chunk_weight(win.m, win.l, M, L, A, lsum);
+    chunk_accumulate(w, 0, win.v, A);
     L += lsum;
-  } else if (nwin > kWinPre) {
+  } else if (win.n > kWinPre) {
+    const int64_t nch = win.nch;
     merge_partials<kWinPre>(
-        nwin, [&](int64_t k) { return *reinterpret_cast<const float2 *>(a.win_ml + (row * nch + k) * 2); },
+        win.n, [&](int64_t k) { return *reinterpret_cast<const float2 *>(a.win_ml + (row * nch + k) * 2); },
         [&](int64_t k) { return a.win_acc + (row * nch + k) * kD; }, M, L, A, lane);
   }
   const bool ok = M != -INFINITY && L > 0.f;
@@ -522,9 +431,88 @@ __global__ void __launch_bounds__(128) attn_merge_warp_kernel(const AttnArgs a) 
   o[3] = A.w * inv;
 }
 
+// Warp variant (rows with few partials): one warp per (sequence, query head)
+// row, four rows per block; no shared memory and no block barriers.
+__global__ void __launch_bounds__(128) attn_merge_warp_kernel(const AttnArgs a) {
+  griddep_wait();  // the main kernel's partials
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);  // b * Hq + qh
+  if (row >= (int64_t)a.B * a.Hq) return;
+  const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
+  const int h = qh / a.G, g = qh % a.G;
+  RowWindow win;
+  row_window_load(a, row, b, lane, win);
+  const RowParts r = row_parts(a, b, h);
+  float M = -INFINITY, L = 0.f;
+  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  merge_row_range<kWarpMergeMaxPartials>(a, r, g, 0, r.n, M, L, A, lane);
+  row_finish(a, row, lane, win, M, L, A);
+}
+
+// Wide variant (rows with many partials): one block of kMergeWarps warps per
+// row; warp w merges the w-th share of the row's partials kWideChunk at a
+// time (a chunk's loads issued together: one memory latency), then warp 0
+// merges the warps' results from shared memory.  The window partials are
+// copied to shared memory asynchronously meanwhile.
+constexpr int kMergeWarps = 16, kWideChunk = 12;
+__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_wide_kernel(const AttnArgs a) {
+  __shared__ float4 s_acc[kMergeWarps][kD / 4];
+  __shared__ float2 s_ml[kMergeWarps];
+  __shared__ float4 s_wacc[kWinPre][kD / 4];
+  __shared__ float2 s_wml[32];
+  griddep_wait();  // the main kernel's partials
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t row = blockIdx.x;  // b * Hq + qh
+  const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
+  const int h = qh / a.G, g = qh % a.G;
+  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
+  const int64_t nwin = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
+  if (warp == kMergeWarps - 1 && nwin <= kWinPre) {
+    for (int u = 0; u < nwin; u++) cp_async16(&s_wacc[u][lane], a.win_acc + (row * nch + u) * kD + 4 * lane);
+    if (lane < nwin) cp_async8(&s_wml[lane], a.win_ml + (row * nch + lane) * 2);
+  }
+  const RowParts r = row_parts(a, b, h);
+  float M = -INFINITY, L = 0.f;
+  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  merge_row_range<kWideChunk>(a, r, g, r.n * warp / kMergeWarps, r.n * (warp + 1) / kMergeWarps, M, L, A, lane);
+  s_acc[warp][lane] = A;
+  if (lane == 0) s_ml[warp] = make_float2(M, L);
+  cp_async_wait_all();
+  __syncthreads();
+  if (warp != 0) return;
+  M = -INFINITY;
+  L = 0.f;
+  A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int h8 = 0; h8 < kMergeWarps; h8 += 8) {  // eight warps' results at a time
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) v[u] = s_acc[h8 + u][lane];
+    const float2 ml = lane < 8 ? s_ml[h8 + lane] : make_float2(-INFINITY, 0.f);
+    float lsum;
+    const float w = chunk_weight(ml.x, ml.y, M, L, A, lsum);
+    chunk_accumulate(w, 0, v, A);
+    L += lsum;
+  }
+  RowWindow win;
+  win.nch = nch;
+  win.n = nwin;
+  win.m = -INFINITY;
+  win.l = 0.f;
+  if (nwin <= kWinPre) {
+#pragma unroll
+    for (int u = 0; u < kWinPre; u++) win.v[u] = u < nwin ? s_wacc[u][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < nwin) {
+      win.m = s_wml[lane].x;
+      win.l = s_wml[lane].y;
+    }
+  }
+  row_finish(a, row, lane, win, M, L, A);
+}
+
 cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
   const int64_t rows = (int64_t)a.B * a.Hq;
-  const int64_t row_blocks = (rows + 3) / 4;
+  const int64_t row_blocks = qjl ? rows : (rows + 3) / 4;
   const int64_t win_blocks = a.window > 0 ? (int64_t)a.B * a.H * ((a.window + kWinChunk - 1) / kWinChunk) : 0;
   const cudaError_t e = launch_maybe_dependent(attn_prep_kernel, dim3((unsigned)(row_blocks + win_blocks)), dim3(128), 0,
                                                st, a.pdl, a, qjl, (int)row_blocks);
@@ -534,12 +522,12 @@ cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
 
 cudaError_t launch_attn_merge(const AttnArgs &a, cudaStream_t st) {
   // warp rows when a (sequence, kv head) averages at most 24 partials (one
-  // chunk of the warp merge); blocks of 128 threads per row otherwise
+  // chunk of the warp merge); blocks of kMergeWarps warps per row otherwise
   const int64_t rows = (int64_t)a.B * a.Hq, units = (int64_t)a.B * a.H;
   const cudaError_t e =
       (int64_t)a.nw_launch <= kWarpMergeMaxPartials * units
           ? launch_maybe_dependent(attn_merge_warp_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, st, a.pdl, a)
-          : launch_maybe_dependent(attn_merge_block_kernel, dim3((unsigned)rows), dim3(128), 0, st, a.pdl, a);
+          : launch_maybe_dependent(attn_merge_wide_kernel, dim3((unsigned)rows), dim3(kMergeWarps * 32), 0, st, a.pdl, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
