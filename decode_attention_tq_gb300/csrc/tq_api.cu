@@ -124,28 +124,37 @@ void lloyd_max_thresholds(int bits, double *cent, double *thr) {
 
 // ---------------------------------------------------------- attention plan --
 struct AttnPlan {
-  int G, NT, nw_launch, blocks;
-  size_t off_hdr, off_pre, off_clen, off_wlen, off_qrot, off_qs, off_qexp, off_segml, off_segacc, off_winml, off_winacc,
-      total;
+  int G, NT, nw_launch, blocks, slices;
+  bool qop_keys;
+  size_t off_hdr, off_pre, off_clen, off_wlen, off_qrot, off_qop, off_qcst, off_qexp, off_segml, off_segacc, off_winml, off_winacc,
+      off_mpart, off_mcnt, total;
 };
 
-constexpr int kMinTilesPerWarp = 4;
+// Fewest tiles per warp of the main kernel: one (a latency-bound shape gets
+// as many warps as the machine holds; the wide merge's slices absorb the
+// extra partials).
+constexpr int kMinTilesPerWarp = 1;
+// Up to this many tiles per warp (at the longest lengths the shape allows)
+// the main kernel takes its key-score query operands ready-made from the
+// prep kernel (the QOP instances); beyond it, it splits q_rot itself.
+constexpr int64_t kQopMaxTilesPerWarp = 8;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 cudaError_t main_kernel_call(const tq_format *f, const AttnArgs &a, int nt, bool query, int *bps, int blocks,
                              cudaStream_t st) {
+  const bool q = f->k_qjl != 0, o = a.qop_keys;
   if (f->k_mixed) {
     switch (f->k_bits) {
-      case 2: return attn_main_k23(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
-      case 3: return attn_main_k34(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
+      case 2: return (o ? attn_main_k23_qop : attn_main_k23)(a, f->v_bits, q, nt, query, bps, blocks, st);
+      case 3: return (o ? attn_main_k34_qop : attn_main_k34)(a, f->v_bits, q, nt, query, bps, blocks, st);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (f->k_bits) {
-    case 2: return attn_main_k2(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
-    case 3: return attn_main_k3(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
-    case 4: return attn_main_k4(a, f->v_bits, f->k_qjl != 0, nt, query, bps, blocks, st);
+    case 2: return (o ? attn_main_k2_qop : attn_main_k2)(a, f->v_bits, q, nt, query, bps, blocks, st);
+    case 3: return (o ? attn_main_k3_qop : attn_main_k3)(a, f->v_bits, q, nt, query, bps, blocks, st);
+    case 4: return (o ? attn_main_k4_qop : attn_main_k4)(a, f->v_bits, q, nt, query, bps, blocks, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -190,6 +199,7 @@ tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int w
   if (warps < 1) warps = 1;
   p->blocks = (int)((warps + wpb - 1) / wpb);
   p->nw_launch = p->blocks * wpb;
+  p->qop_keys = tiles_max <= kQopMaxTilesPerWarp * p->nw_launch;
 
   const int64_t rows = (int64_t)B * Hq;
   const int64_t slots = (int64_t)p->nw_launch + (int64_t)B * H;
@@ -199,13 +209,17 @@ tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int w
   p->off_clen = off;   off = align256(off + sizeof(int32_t) * B);
   p->off_wlen = off;   off = align256(off + sizeof(int32_t) * B);
   p->off_qrot = off;   off = align256(off + sizeof(float) * rows * kD);
-  p->off_qs = off;     off = align256(off + (f->k_qjl ? sizeof(float) * rows * kM : 0));
+  p->off_qop = off;    off = align256(off + sizeof(uint32_t) * rows * 4 * 64);
+  p->off_qcst = off;   off = align256(off + sizeof(float2) * rows);
   p->off_qexp = off;   off = align256(off + sizeof(int32_t) * rows * 2);
   p->off_segml = off;  off = align256(off + sizeof(float) * slots * p->G * 2);
   p->off_segacc = off; off = align256(off + sizeof(float) * slots * p->G * kD);
   const int64_t nch = (window + kWinChunk - 1) / kWinChunk;
   p->off_winml = off;  off = align256(off + sizeof(float) * rows * nch * 2);
   p->off_winacc = off; off = align256(off + sizeof(float) * rows * nch * kD);
+  p->slices = merge_slices(p->nw_launch, (int64_t)B * H);
+  p->off_mpart = off;  off = align256(off + (p->slices > 1 ? sizeof(float) * rows * p->slices * kMergePartStride : 0));
+  p->off_mcnt = off;   off = align256(off + sizeof(int32_t) * rows);
   p->total = off;
   return TQ_OK;
 }
@@ -522,7 +536,8 @@ static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_hea
   a.clen = reinterpret_cast<int32_t *>(ws + p.off_clen);
   a.wlen = reinterpret_cast<int32_t *>(ws + p.off_wlen);
   a.q_rot = reinterpret_cast<float *>(ws + p.off_qrot);
-  a.q_s = reinterpret_cast<float *>(ws + p.off_qs);
+  a.q_op = reinterpret_cast<uint32_t *>(ws + p.off_qop);
+  a.q_cst = reinterpret_cast<float2 *>(ws + p.off_qcst);
   a.q_exp = reinterpret_cast<int32_t *>(ws + p.off_qexp);
   a.seg_ml = reinterpret_cast<float *>(ws + p.off_segml);
   a.seg_acc = reinterpret_cast<float *>(ws + p.off_segacc);
@@ -530,6 +545,10 @@ static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_hea
   a.win_acc = reinterpret_cast<float *>(ws + p.off_winacc);
   a.nw_launch = p.nw_launch;
   a.min_tiles = kMinTilesPerWarp;
+  a.merge_slices = p.slices;
+  a.qop_keys = p.qop_keys;
+  a.merge_part = reinterpret_cast<float *>(ws + p.off_mpart);
+  a.merge_cnt = reinterpret_cast<int32_t *>(ws + p.off_mcnt);
   // prep, main and merge start as programmatic dependents (their launches and
   // prologues overlap the previous kernel; prep waits before it reads
   // anything), except when the caller times the main kernel
@@ -665,7 +684,8 @@ static tq_status kivi_attn_impl(const tq_kivi_format *fmt, int batch, int num_q_
   a.clen = reinterpret_cast<int32_t *>(ws + p.off_clen);
   a.wlen = reinterpret_cast<int32_t *>(ws + p.off_wlen);
   a.q_rot = reinterpret_cast<float *>(ws + p.off_qrot);
-  a.q_s = reinterpret_cast<float *>(ws + p.off_qs);
+  a.q_op = reinterpret_cast<uint32_t *>(ws + p.off_qop);
+  a.q_cst = reinterpret_cast<float2 *>(ws + p.off_qcst);
   a.q_exp = reinterpret_cast<int32_t *>(ws + p.off_qexp);
   a.seg_ml = reinterpret_cast<float *>(ws + p.off_segml);
   a.seg_acc = reinterpret_cast<float *>(ws + p.off_segacc);
@@ -673,6 +693,10 @@ static tq_status kivi_attn_impl(const tq_kivi_format *fmt, int batch, int num_q_
   a.win_acc = reinterpret_cast<float *>(ws + p.off_winacc);
   a.nw_launch = p.nw_launch;
   a.min_tiles = kMinTilesPerWarp;
+  a.merge_slices = p.slices;
+  a.qop_keys = p.qop_keys;
+  a.merge_part = reinterpret_cast<float *>(ws + p.off_mpart);
+  a.merge_cnt = reinterpret_cast<int32_t *>(ws + p.off_mcnt);
   a.pdl = ev_begin == nullptr && ev_end == nullptr;
   a.raw = true;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -157,7 +157,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const RollArgs r
     kl.x = x;
     kl.n_tokens = ns;
     kl.slot_mapping = s_slot;
-    encode_loop<KBITS, KQJL, KMIX>(tk, kl, warp, 4);
+    if (KQJL && nsh <= 8)  // one octet of key vectors: the four warps share its QJL projection
+      encode_loop<KBITS, KQJL, KMIX>(tk, kl, 0, 1, warp, 4);
+    else
+      encode_loop<KBITS, KQJL, KMIX>(tk, kl, warp, 4);
   } else {
     EncodeArgs vl = va;
     vl.x = x + nsh * kD;

@@ -2,15 +2,16 @@
 //   prep   : (one launch, three kinds of block) tile prefix sums and clamped
 //            lengths; each query rotated once into the key basis
 //            (q_rot = H (D_K . q)/sqrt(d)), projected for the QJL term
-//            (q_s = S q_rot, one block per row), with power-of-two operand
-//            scales; and
+//            (S q_rot, one block per row), with power-of-two operand scales,
+//            written as the main kernel's fp16 hi/lo operands; and
 //            attention partials over the raw fp16 recent-token window, one
 //            per 32-token chunk;
 //   merge  : log-sum-exp merge of the compressed partials of a (sequence,
 //            query head), one inverse rotation of their value accumulator
 //            (D_V . H acc / d), then the window partials, normalised; one
-//            warp per (sequence, query head) when they have few partials, a
-//            block of 16 warps sharing them otherwise.
+//            warp per (sequence, query head) when they have few partials,
+//            blocks of 16 warps sharing them otherwise (several blocks per
+//            row, the last one to finish merging their results).
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -86,14 +87,27 @@ __device__ __forceinline__ void rotate_query(const AttnArgs &a, int64_t row, int
 // Power-of-two operand scale: the largest |value| lands in [2^12, 2^13).
 __device__ __forceinline__ int operand_exponent(float mx) { return mx > 0.f ? 12 - ilogbf(mx) : 0; }
 
-// Stores q_rot and its exponent (one warp).
+// Stores q_rot, its exponent and (rotated-domain caches) its operand parts
+// and key score constant (one warp).
 __device__ __forceinline__ void store_query(const AttnArgs &a, int64_t row, int lane, const float (&x)[4]) {
   float mx = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; i++) mx = fmaxf(mx, fabsf(x[i]));
   *reinterpret_cast<float4 *>(a.q_rot + row * kD + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
   mx = warp_max_xor(mx, 31);
-  if (lane == 0) a.q_exp[row * 2] = operand_exponent(mx);
+  const int eq = operand_exponent(mx);
+  if (lane == 0) a.q_exp[row * 2] = eq;
+  if (!a.raw) {
+    // words 2 lane, 2 lane + 1 of parts 0 (hi) and 1 (lo): coordinates 4 lane .. 4 lane + 3
+    const float sc = ldexpf(1.0f, eq);
+    __half h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) split_half(x[i] * sc, h[i], l[i]);
+    uint32_t *op = a.q_op + row * 256;
+    *reinterpret_cast<uint2 *>(op + 2 * lane) = make_uint2(pack_half2_raw(h[0], h[1]), pack_half2_raw(h[2], h[3]));
+    *reinterpret_cast<uint2 *>(op + 64 + 2 * lane) = make_uint2(pack_half2_raw(l[0], l[1]), pack_half2_raw(l[2], l[3]));
+    if (lane == 0) a.q_cst[row].x = ldexpf(kLog2e / (float)kD, -(eq + 8));
+  }
 }
 
 // Without QJL: one warp per query row.
@@ -101,29 +115,32 @@ __device__ void prep_query(const AttnArgs &a, int64_t row, int lane) {
   float x[4];
   rotate_query(a, row, lane, x);
   store_query(a, row, lane, x);
-  if (lane == 0) a.q_exp[row * 2 + 1] = 0;
+  if (lane == 0) {
+    a.q_exp[row * 2 + 1] = 0;
+    a.q_cst[row].y = 0.f;
+    a.merge_cnt[row] = 0;
+  }
 }
 
 // With QJL: one 128-thread block per query row.  Every warp rotates the row
-// (a few shuffles); warp w projects it on S rows 32w .. 32w + 31, q_s = S q_rot:
+// (a few shuffles); warp w projects it on S rows 32w .. 32w + 31, S q_rot:
 // lane holds coordinates 4 lane .. 4 lane + 3 and reads the same coordinates
-// of each S row (one coalesced 512-byte row per load, 16 rows in flight).
+// of each S row (one coalesced 512-byte row per load, all 32 in flight).
 // The 32 per-lane partial dots are summed over the warp by a transposing
 // butterfly (31 shuffles), after which lane l holds row 32w + l.
 __device__ void prep_query_qjl(const AttnArgs &a, int64_t row, int warp, int lane, float *s_red) {
+  // the warp's 32 S rows are loaded first (they depend on nothing), together
+  // with the query row: one memory latency
+  float4 sv[32];
+  const float4 *S4 = reinterpret_cast<const float4 *>(a.S + (int64_t)(32 * warp) * kD) + lane;
+#pragma unroll
+  for (int i = 0; i < 32; i++) sv[i] = __ldg(S4 + i * (kD / 4));
   float x[4];
   rotate_query(a, row, lane, x);
   if (warp == 0) store_query(a, row, lane, x);
   float v[32];
-  const float4 *S4 = reinterpret_cast<const float4 *>(a.S + (int64_t)(32 * warp) * kD) + lane;
 #pragma unroll
-  for (int half = 0; half < 2; half++) {
-    float4 sv[16];
-#pragma unroll
-    for (int i = 0; i < 16; i++) sv[i] = __ldg(S4 + (16 * half + i) * (kD / 4));
-#pragma unroll
-    for (int i = 0; i < 16; i++) v[16 * half + i] = fmaf(sv[i].x, x[0], fmaf(sv[i].y, x[1], fmaf(sv[i].z, x[2], sv[i].w * x[3])));
-  }
+  for (int i = 0; i < 32; i++) v[i] = fmaf(sv[i].x, x[0], fmaf(sv[i].y, x[1], fmaf(sv[i].z, x[2], sv[i].w * x[3])));
 #pragma unroll
   for (int m = 16, n = 16; m >= 1; m >>= 1, n >>= 1) {
     // keep the half of the n pairs (v[i], v[i + n]) selected by lane bit m,
@@ -135,11 +152,22 @@ __device__ void prep_query_qjl(const AttnArgs &a, int64_t row, int warp, int lan
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
     }
   }
-  a.q_s[row * kM + 32 * warp + lane] = v[0];
   const float my = warp_max_xor(fabsf(v[0]), 31);
   if (lane == 0) s_red[warp] = my;
   __syncthreads();
-  if (threadIdx.x == 0) a.q_exp[row * 2 + 1] = operand_exponent(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
+  const int es = operand_exponent(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
+  // slice t = warp of parts 2 (hi) and 3 (lo), value i = lane (qop_qjl_half)
+  __half hi, lo;
+  split_half(v[0] * ldexpf(1.0f, es), hi, lo);
+  __half *op = reinterpret_cast<__half *>(a.q_op + row * 256);
+  op[2 * (128 + 16 * warp) + qop_qjl_half(lane)] = hi;
+  op[2 * (192 + 16 * warp) + qop_qjl_half(lane)] = lo;
+  if (threadIdx.x == 0) {
+    a.merge_cnt[row] = 0;
+    a.q_exp[row * 2 + 1] = es;
+    // qjl_coef / sqrt(d) (qjl_coef = sqrt(pi/2) / m for the paper's Gaussian S)
+    a.q_cst[row].y = ldexpf(kLog2e * a.qjl_coef / 11.313708498984761f, -es);
+  }
 }
 
 // Attention partial of the G query heads of (b, h) over window chunk c
@@ -275,8 +303,8 @@ __device__ __forceinline__ int64_t tile_owner(int64_t x, int64_t T, int64_t NW) 
   return w < NW - 1 ? w : NW - 1;
 }
 
-// Partials per chunk of the warp merge (32 float4 accumulators would spill).
-constexpr int kWarpMergeMaxPartials = 24;
+// kWarpMergeMaxPartials: partials per chunk of the warp merge (32 float4
+// accumulators would spill).
 
 // One chunk of up to 32 partials merged into the running (M, L, A) of a
 // warp: lane i holds the (max m, sum l) of partial i, v[u] the accumulator
@@ -449,12 +477,15 @@ __global__ void __launch_bounds__(128) attn_merge_warp_kernel(const AttnArgs a) 
   row_finish(a, row, lane, win, M, L, A);
 }
 
-// Wide variant (rows with many partials): one block of kMergeWarps warps per
-// row; warp w merges the w-th share of the row's partials kWideChunk at a
-// time (a chunk's loads issued together: one memory latency), then warp 0
-// merges the warps' results from shared memory.  The window partials are
-// copied to shared memory asynchronously meanwhile.
-constexpr int kMergeWarps = 16, kWideChunk = 12;
+// Wide variant (rows with many partials): blocks of kMergeWarps warps; a row
+// is cut into up to merge_slices slices of about kSlicePartials partials, one
+// block each.  Warp w of a block merges the w-th share of its slice
+// kWideChunk partials at a time (a chunk's loads issued together: one memory
+// latency), then warp 0 merges the warps' results from shared memory.  With
+// one slice it finishes the row; otherwise it stores the slice result, and
+// the block that completes a row's last slice (a per-row counter the prep
+// kernel zeroed) merges the slice results and finishes the row.  The window
+// partials are copied to shared memory asynchronously meanwhile.
 __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_wide_kernel(const AttnArgs a) {
   __shared__ float4 s_acc[kMergeWarps][kD / 4];
   __shared__ float2 s_ml[kMergeWarps];
@@ -462,19 +493,25 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_wide_kernel(const
   __shared__ float2 s_wml[32];
   griddep_wait();  // the main kernel's partials
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t row = blockIdx.x;  // b * Hq + qh
+  const int64_t row = blockIdx.x / a.merge_slices;  // b * Hq + qh
+  const int slice = (int)(blockIdx.x - row * a.merge_slices);
   const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
   const int h = qh / a.G, g = qh % a.G;
+  const RowParts r = row_parts(a, b, h);
+  // slices this row uses (the same in every block of the row)
+  int64_t ns = (r.n + kSlicePartials - 1) / kSlicePartials;
+  ns = ns < 1 ? 1 : (ns > a.merge_slices ? a.merge_slices : ns);
+  if (slice >= ns) return;  // block-uniform
   const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
   const int64_t nwin = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
   if (warp == kMergeWarps - 1 && nwin <= kWinPre) {
     for (int u = 0; u < nwin; u++) cp_async16(&s_wacc[u][lane], a.win_acc + (row * nch + u) * kD + 4 * lane);
     if (lane < nwin) cp_async8(&s_wml[lane], a.win_ml + (row * nch + lane) * 2);
   }
-  const RowParts r = row_parts(a, b, h);
+  const int64_t k0 = r.n * slice / ns, kn = r.n * (slice + 1) / ns - k0;
   float M = -INFINITY, L = 0.f;
   float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-  merge_row_range<kWideChunk>(a, r, g, r.n * warp / kMergeWarps, r.n * (warp + 1) / kMergeWarps, M, L, A, lane);
+  merge_row_range<kWideChunk>(a, r, g, k0 + kn * warp / kMergeWarps, k0 + kn * (warp + 1) / kMergeWarps, M, L, A, lane);
   s_acc[warp][lane] = A;
   if (lane == 0) s_ml[warp] = make_float2(M, L);
   cp_async_wait_all();
@@ -493,6 +530,34 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_wide_kernel(const
     const float w = chunk_weight(ml.x, ml.y, M, L, A, lsum);
     chunk_accumulate(w, 0, v, A);
     L += lsum;
+  }
+  if (ns > 1) {
+    float *part = a.merge_part + (row * a.merge_slices + slice) * kMergePartStride;
+    reinterpret_cast<float4 *>(part)[lane] = A;
+    if (lane == 0) *reinterpret_cast<float2 *>(part + kD) = make_float2(M, L);
+    __threadfence();
+    int done = 0;
+    if (lane == 0) done = atomicAdd(a.merge_cnt + row, 1);
+    done = __shfl_sync(0xffffffffu, done, 0);
+    if (done != ns - 1) return;  // another block finishes the row
+    __threadfence();
+    // the row's slice results (written by other blocks: read past L1)
+    M = -INFINITY;
+    L = 0.f;
+    A = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float *rp = a.merge_part + row * a.merge_slices * kMergePartStride;
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++)
+        v[u] = s0 + u < ns ? __ldcg(reinterpret_cast<const float4 *>(rp + (s0 + u) * kMergePartStride) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float2 ml = s0 + lane < ns && lane < 8 ? __ldcg(reinterpret_cast<const float2 *>(rp + (s0 + lane) * kMergePartStride + kD))
+                                                   : make_float2(-INFINITY, 0.f);
+      float lsum;
+      const float w = chunk_weight(ml.x, ml.y, M, L, A, lsum);
+      chunk_accumulate(w, 0, v, A);
+      L += lsum;
+    }
   }
   RowWindow win;
   win.nch = nch;
@@ -522,12 +587,14 @@ cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
 
 cudaError_t launch_attn_merge(const AttnArgs &a, cudaStream_t st) {
   // warp rows when a (sequence, kv head) averages at most 24 partials (one
-  // chunk of the warp merge); blocks of kMergeWarps warps per row otherwise
+  // chunk of the warp merge); blocks of kMergeWarps warps per row slice
+  // otherwise
   const int64_t rows = (int64_t)a.B * a.Hq, units = (int64_t)a.B * a.H;
   const cudaError_t e =
-      (int64_t)a.nw_launch <= kWarpMergeMaxPartials * units
+      merge_by_warps(a.nw_launch, units)
           ? launch_maybe_dependent(attn_merge_warp_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, st, a.pdl, a)
-          : launch_maybe_dependent(attn_merge_wide_kernel, dim3((unsigned)rows), dim3(kMergeWarps * 32), 0, st, a.pdl, a);
+          : launch_maybe_dependent(attn_merge_wide_kernel, dim3((unsigned)(rows * a.merge_slices)), dim3(kMergeWarps * 32), 0,
+                                   st, a.pdl, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

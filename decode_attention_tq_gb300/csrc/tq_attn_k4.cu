@@ -6,7 +6,7 @@ namespace tq {
 
 cudaError_t attn_main_k4(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
                          int blocks, cudaStream_t st) {
-  return attn_main_dispatch<4>(a, v_bits, qjl, nt, query_only, blocks_per_sm, blocks, st);
+  return attn_main_dispatch<4, false>(a, v_bits, qjl, nt, query_only, blocks_per_sm, blocks, st);
 }
 
 }  // namespace tq

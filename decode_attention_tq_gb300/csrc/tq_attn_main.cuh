@@ -424,7 +424,13 @@ constexpr size_t attn_smem_bytes() {
              : (size_t)attn_tables_end<KB, VB>();
 }
 
-template <int KB, int VB, bool QJL, int NT>
+// QOP: the key-score query operands are the prep kernel's ready-made words
+// (q_op); otherwise the kernel splits q_rot into them.  The host picks it per
+// shape: measured at the Llama-3-8B K4/V4 shape (108 tiles per warp) 118.8 us
+// per launch splitting in the kernel against 129.0 with loaded words; at the
+// Qwen2.5-3B shape (2 tiles per warp) 15.0 against 12.9.  (A run-time switch
+// between the two inside one kernel measured 131.0 at the Llama shape.)
+template <int KB, int VB, bool QJL, int NT, bool QOP>
 __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(const AttnArgs a) {
   constexpr int EK = 1 << (2 * kb_hi(KB)), EV = 1 << (2 * VB);
   static_assert(byte_values<VB>() || EV * 256 <= 65536, "table sizes");
@@ -529,60 +535,75 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   while (pos < te) {
     const int seg_tiles = (int)min(te - pos, (int64_t)(tb - j));
 
-    // ---- segment setup: query operands for the G heads of (b, h)
+    // ---- the segment's first page: block-table loads issued before the
+    // operand loads below, so that both wait on one memory latency
+    TileCursor cur;
+    cur.pool = a.pool;
+    cur.btrow = a.block_tables + (int64_t)b * a.max_pages;
+    cur.num_pages = a.num_pages;
+    cur.page_bytes = a.page_bytes;
+    cur.slab_off = (int64_t)h * a.slab_bytes;
+    cur.P = a.P;
+    cur.pidx = j / tpp;
+    cur.o0 = (j - cur.pidx * tpp) * 16;
+    cur.tok0 = j * 16;
+    cur.clen = a.clen[b];
+    cur.last_page = (j + seg_tiles - 1) / tpp;
+    cur.begin(a.err_word, lane == 0, slab_bytes);
+
+    // ---- segment setup: query operands for the G heads of (b, h), as the
+    // prep kernel wrote them (hi / lo fp16 words in register order, the
+    // score constants): loads only, all issued together
     uint32_t qb[NT][8][2];
     uint32_t sb[NT][QJL ? 8 : 1][2];
     float cK[NT], cQ[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
       const int gcol = 4 * nt + (r >> 1);
-      const bool lo_part = (r & 1) != 0;
+      const int part = r & 1;  // hi (even rows) or lo (odd rows) of head gcol
       const bool gval = gcol < G;
       const int64_t qrow = ((int64_t)b * Hq + (int64_t)h * G + (gval ? gcol : 0));
-      const int ecol = gval ? a.q_exp[qrow * 2] : 0;
-      const float sc = ldexpf(1.0f, ecol);
-      const float *qr = a.q_rot + qrow * kD + 32 * t;
+      const uint4 *op = reinterpret_cast<const uint4 *>(a.q_op + qrow * 256 + 16 * t);
+      if constexpr (QOP) {  // the prep kernel's operand words
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) {
-        float4 v = gval ? *reinterpret_cast<const float4 *>(qr + 4 * kk) : make_float4(0.f, 0.f, 0.f, 0.f);
-        __half hx, lx, hy, ly, hz, lz, hw, lw;
-        split_half(v.x * sc, hx, lx);
-        split_half(v.y * sc, hy, ly);
-        split_half(v.z * sc, hz, lz);
-        split_half(v.w * sc, hw, lw);
-        qb[nt][kk][0] = lo_part ? pack_half2_raw(lx, ly) : pack_half2_raw(hx, hy);
-        qb[nt][kk][1] = lo_part ? pack_half2_raw(lz, lw) : pack_half2_raw(hz, hw);
-      }
-      if constexpr (QJL) {
-        const int es = gval ? a.q_exp[qrow * 2 + 1] : 0;
-        const float ss = ldexpf(1.0f, es);
-        const float *qs = a.q_s + qrow * kM + 32 * t;
+        for (int u = 0; u < 4; u++) {
+          const uint4 v = gval ? op[16 * part + u] : make_uint4(0u, 0u, 0u, 0u);
+          qb[nt][2 * u][0] = v.x;
+          qb[nt][2 * u][1] = v.y;
+          qb[nt][2 * u + 1][0] = v.z;
+          qb[nt][2 * u + 1][1] = v.w;
+        }
+      } else {  // the hi / lo split of q_rot here
+        const int ecol = gval ? a.q_exp[qrow * 2] : 0;
+        const float sc = ldexpf(1.0f, ecol);
+        const float *qr = a.q_rot + qrow * kD + 32 * t;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
-          // b0 pairs sign bits (2kk, 2kk+16), b1 pairs (2kk+1, 2kk+17) of word t
-          const float v0 = gval ? qs[2 * kk] * ss : 0.f, v1 = gval ? qs[2 * kk + 16] * ss : 0.f;
-          const float v2 = gval ? qs[2 * kk + 1] * ss : 0.f, v3 = gval ? qs[2 * kk + 17] * ss : 0.f;
-          __half h0, l0, h1, l1, h2, l2, h3, l3;
-          split_half(v0, h0, l0);
-          split_half(v1, h1, l1);
-          split_half(v2, h2, l2);
-          split_half(v3, h3, l3);
-          sb[nt][kk][0] = lo_part ? pack_half2_raw(l0, l1) : pack_half2_raw(h0, h1);
-          sb[nt][kk][1] = lo_part ? pack_half2_raw(l2, l3) : pack_half2_raw(h2, h3);
+          const float4 v = gval ? *reinterpret_cast<const float4 *>(qr + 4 * kk) : make_float4(0.f, 0.f, 0.f, 0.f);
+          __half hx, lx, hy, ly, hz, lz, hw, lw;
+          split_half(v.x * sc, hx, lx);
+          split_half(v.y * sc, hy, ly);
+          split_half(v.z * sc, hz, lz);
+          split_half(v.w * sc, hw, lw);
+          qb[nt][kk][0] = part ? pack_half2_raw(lx, ly) : pack_half2_raw(hx, hy);
+          qb[nt][kk][1] = part ? pack_half2_raw(lz, lw) : pack_half2_raw(hz, hw);
+        }
+      }
+      if constexpr (QJL) {
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          const uint4 v = gval ? op[16 * (2 + part) + u] : make_uint4(0u, 0u, 0u, 0u);
+          sb[nt][2 * u][0] = v.x;
+          sb[nt][2 * u][1] = v.y;
+          sb[nt][2 * u + 1][0] = v.z;
+          sb[nt][2 * u + 1][1] = v.w;
         }
       }
       // score constants of this thread's own head g = 4nt + t (log2 domain)
       const int gown = 4 * nt + t;
-      const int64_t orow = ((int64_t)b * Hq + (int64_t)h * G + (gown < G ? gown : 0));
-      const int eq = a.q_exp[orow * 2];
-      cK[nt] = ldexpf(kLog2e / (float)kD, -(eq + 8));
-      if constexpr (QJL) {
-        const int es = a.q_exp[orow * 2 + 1];
-        // qjl_coef / sqrt(d) (qjl_coef = sqrt(pi/2) / m for the paper's Gaussian S)
-        cQ[nt] = ldexpf(kLog2e * a.qjl_coef / 11.313708498984761f, -es);
-      } else {
-        cQ[nt] = 0.f;
-      }
+      const float2 c = a.q_cst[(int64_t)b * Hq + (int64_t)h * G + (gown < G ? gown : 0)];
+      cK[nt] = c.x;
+      cQ[nt] = QJL ? c.y : 0.f;
     }
 
     float mu[NT], lsum[NT];
@@ -598,19 +619,6 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
     }
     float nu = 0.f, inv_nu = 0.f;
 
-    TileCursor cur;
-    cur.pool = a.pool;
-    cur.btrow = a.block_tables + (int64_t)b * a.max_pages;
-    cur.num_pages = a.num_pages;
-    cur.page_bytes = a.page_bytes;
-    cur.slab_off = (int64_t)h * a.slab_bytes;
-    cur.P = a.P;
-    cur.pidx = j / tpp;
-    cur.o0 = (j - cur.pidx * tpp) * 16;
-    cur.tok0 = j * 16;
-    cur.clen = a.clen[b];
-    cur.last_page = (j + seg_tiles - 1) / tpp;
-    cur.begin(a.err_word, lane == 0, slab_bytes);
 
     auto process = [&](const KeyRegs<KB, QJL> &R, const ValRegs<VB> &V) {
       if (!__any_sync(0xffffffffu, R.ok0)) return;  // token 0 of a tile is live iff any is
@@ -933,9 +941,9 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   }
 }
 
-template <int KB, int VB, bool QJL, int NT>
+template <int KB, int VB, bool QJL, int NT, bool QOP>
 cudaError_t attn_main_launch_t(const AttnArgs &a, bool query_only, int *blocks_per_sm, int blocks, cudaStream_t st) {
-  auto kern = attn_main_kernel<KB, VB, QJL, NT>;
+  auto kern = attn_main_kernel<KB, VB, QJL, NT, QOP>;
   constexpr size_t smem_bytes = attn_smem_bytes<KB, VB, QJL, NT>();
   static_assert(smem_bytes <= 232448, "dynamic shared memory above the per-CTA limit");
   static unsigned long long done = 0;
@@ -945,11 +953,11 @@ cudaError_t attn_main_launch_t(const AttnArgs &a, bool query_only, int *blocks_p
   return launch_maybe_dependent(kern, dim3(blocks), dim3(attn_threads(NT, QJL)), smem_bytes, st, a.pdl, a);
 }
 
-template <int KB>
+template <int KB, bool QOP>
 cudaError_t attn_main_dispatch(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *bps, int blocks,
                                cudaStream_t st) {
 #define TQ_CASE(VB, Q, N) \
-  if (v_bits == VB && qjl == Q && nt == N) return attn_main_launch_t<KB, VB, Q, N>(a, query_only, bps, blocks, st);
+  if (v_bits == VB && qjl == Q && nt == N) return attn_main_launch_t<KB, VB, Q, N, QOP>(a, query_only, bps, blocks, st);
   TQ_CASE(2, false, 1) TQ_CASE(2, false, 2) TQ_CASE(2, true, 1) TQ_CASE(2, true, 2)
   TQ_CASE(3, false, 1) TQ_CASE(3, false, 2) TQ_CASE(3, true, 1) TQ_CASE(3, true, 2)
   TQ_CASE(4, false, 1) TQ_CASE(4, false, 2) TQ_CASE(4, true, 1) TQ_CASE(4, true, 2)

@@ -214,21 +214,22 @@ __device__ __forceinline__ void encode_s_cells_load(const EncodeArgs &a) {
   extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells
   // cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
   // coordinates thread t contributes at k-step ks of the projection
-  // four consecutive coordinates share a cell: float4 loads, four per
-  // thread in flight, and one 8-byte store each for the hi and lo halves
-  constexpr int N4 = kM * kD / 4;
+  // four consecutive coordinates share a cell: float4 loads, sixteen per
+  // thread in flight (all of them for 256 threads: one memory latency), and
+  // one 8-byte store each for the hi and lo halves
+  constexpr int N4 = kM * kD / 4, kBatch = 16;
   const int tid = threadIdx.x;
   const float4 *S4 = reinterpret_cast<const float4 *>(a.S);
   uint2 *cells = reinterpret_cast<uint2 *>(s_Sq);
-  for (int i0 = tid; i0 < N4; i0 += 4 * blockDim.x) {
-    float4 v[4];
+  for (int i0 = tid; i0 < N4; i0 += kBatch * blockDim.x) {
+    float4 v[kBatch];
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
+    for (int u = 0; u < kBatch; u++) {
       const int i4 = i0 + u * blockDim.x;
       v[u] = i4 < N4 ? __ldg(S4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
+    for (int u = 0; u < kBatch; u++) {
       const int i4 = i0 + u * blockDim.x;
       if (i4 < N4) {
         const int l = (4 * i4) / kD, j = (4 * i4) % kD;
@@ -270,9 +271,13 @@ __device__ __forceinline__ void encode_tables_build(EncodeTables<MIXED> &T) {
 // The vectors [n_tokens][H] of a.x (global or shared memory), 8 per warp and
 // step: warps [warp0, warp0 + nwarps) of the grid share them (a grid-stride
 // loop); the default is every warp of the grid.
+// part / parts (QJL): several warps encoding the same vectors (a batch that
+// fills fewer octets than there are warps) share the projection: this warp
+// computes n-tiles [16 part / parts, 16 (part + 1) / parts) and stores only
+// the sign words they fill; part 0 stores codes, norm and gamma.
 template <int BITS, bool QJL, bool MIXED = false>
 __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const EncodeArgs &a, int64_t warp0 = -1,
-                                            int64_t nwarps_in = 0) {
+                                            int64_t nwarps_in = 0, int part = 0, int parts = 1) {
   extern __shared__ __align__(16) uint4 s_Sq[];  // QJL only
   constexpr int L = 1 << BITS;
   const int tid = threadIdx.x;
@@ -444,7 +449,8 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
     const int64_t page = ok ? slot / a.P : 0;
     const int64_t off = ok ? slot % a.P : 0;
     uint8_t *slab = a.pool + page * a.page_bytes + (int64_t)h * a.slab_bytes;
-    if (MIXED && ok) {
+    const bool okc = ok && part == 0;  // this warp stores the codes and the norm
+    if (MIXED && okc) {
       // high stream (channels j mod 16 < 8) at BITS bits, then the low stream
       // at BITS - 1: this lane's 8 codes of block c are group 2c + q/2 of its
       // stream
@@ -509,7 +515,7 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
         }
       }
       if (ok && q == 0) reinterpret_cast<float *>(slab + a.norm_off)[off] = nstore;
-    } else if (ok) {
+    } else if (okc) {
 #pragma unroll
       for (int c = 0; c < 4; c++) {
         // codes of coordinates 32c + 8q .. +7: 8 * BITS bits, LSB first
@@ -577,6 +583,7 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
       uint32_t words[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int nt = 0; nt < 16; nt++) {  // outputs l = 8nt .. 8nt+7; this lane gets 8nt+2q, 8nt+2q+1
+        if (parts > 1 && (nt < 16 * part / parts || nt >= 16 * (part + 1) / parts)) continue;  // warp-uniform
         float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f};
         const int l = 8 * nt + quad_in_warp;
 #pragma unroll
@@ -597,7 +604,8 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
       }
       uint32_t word = q == 0 ? words[0] : q == 1 ? words[1] : q == 2 ? words[2] : words[3];
       if (zero) word = 0u;
-      if (ok) {
+      // word q holds n-tiles 4q .. 4q + 3: stored by the warp that computed them
+      if (ok && (parts == 1 || (4 * q >= 16 * part / parts && 4 * q < 16 * (part + 1) / parts))) {
         reinterpret_cast<uint32_t *>(slab + a.signs_off + off * (kM / 8))[q] = word;
         if (q == 0) reinterpret_cast<float *>(slab + a.gamma_off)[off] = gamma;
       }

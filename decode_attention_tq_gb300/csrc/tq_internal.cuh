@@ -78,6 +78,17 @@ __host__ __device__ __forceinline__ int64_t value_chunk_offset(int64_t off, int 
 // coordinates as stored.
 __host__ __device__ constexpr bool value_pairs_interleaved(int bits) { return bits == 2 || bits == 4; }
 
+// Query operands of the split-KV main kernel, written by the prep kernel:
+// per query row four parts of 64 fp16x2 words, the rotated query scaled by
+// 2^q_exp[0] split into fp16 hi (part 0) and lo (part 1) and the QJL
+// projection scaled by 2^q_exp[1] likewise (parts 2, 3).  Word 16t + w of a
+// part holds coordinates of slice t (32t .. 32t + 31) as a main-kernel lane
+// of that slice takes them as B-operand registers (w = 0 .. 15): the query
+// words pair slice coordinates (2w, 2w + 1), the QJL words pair slice values
+// (w, w + 16), i.e. fp16 index 2 (i mod 16) + (i div 16) of the slice holds
+// QJL value i.
+__host__ __device__ __forceinline__ int qop_qjl_half(int i) { return 2 * (i & 15) + (i >> 4); }
+
 // Workspace header written by the prep kernel and read by the others.
 struct AttnHeader {
   int64_t total_tiles;  // sum over (b, h) of ceil(comp_len / 16)
@@ -109,16 +120,22 @@ struct AttnArgs {
   int32_t *clen;     // [B] clamped compressed lengths
   int32_t *wlen;     // [B] clamped window lengths
   float *q_rot;      // [B][Hq][d]
-  float *q_s;        // [B][Hq][m]
   int32_t *q_exp;    // [B][Hq][2] power-of-two exponents for the fp16 operands
+  uint32_t *q_op;    // [B][Hq][4][64] the main kernel's fp16x2 query operands (qop_word)
+  float2 *q_cst;     // [B][Hq] score constants (key part, QJL part) in the log2 domain
   float *seg_ml;     // [slots][G][2]  (max in log2 units, sum)
   float *seg_acc;    // [slots][G][d]  rotated-domain value accumulator
   float *win_ml;     // [B][Hq][window chunks][2]
   float *win_acc;    // [B][Hq][window chunks][d]  raw-domain window accumulators
+  float *merge_part; // [B][Hq][merge_slices][kMergePartStride] slice results of the wide merge
+                     // (accumulator [d], then max, sum; records 16-byte aligned)
+  int32_t *merge_cnt;  // [B][Hq] slices of a row done (zeroed by the prep kernel)
   int nw_launch;     // warps launched for the main kernel
   int min_tiles;     // fewest tiles a warp is given
+  int merge_slices;  // blocks per row of the wide merge (1: no slice results)
   bool pdl;          // host: launch main and merge as programmatic dependents
   bool raw;          // KIVI cache: no query rotation, the accumulators are raw-domain
+  bool qop_keys;     // host: launch the main kernel that loads its key-score query operands from q_op
 };
 
 // KIVI-style control arm (tq_kivi.cu): encode of keys (per-channel groups of
@@ -184,6 +201,19 @@ cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, bool mixed, i
 constexpr int kWinChunk = 32;  // window tokens per window partial
 cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st);
 cudaError_t launch_attn_merge(const AttnArgs &a, cudaStream_t st);
+// Merge geometry: rows whose (sequence, kv head) average at most
+// kWarpMergeMaxPartials partials are merged by one warp each, the others by
+// blocks of kMergeWarps warps, kSlicePartials partials per block (slices).
+constexpr int kWarpMergeMaxPartials = 24, kMergeWarps = 16, kWideChunk = 10;
+constexpr int kSlicePartials = kMergeWarps * kWideChunk, kMaxMergeSlices = 32;
+constexpr int kMergePartStride = kD + 4;  // floats per slice result: a multiple of 4 (float4 accesses)
+inline bool merge_by_warps(int64_t nw_launch, int64_t units) { return nw_launch <= kWarpMergeMaxPartials * units; }
+inline int merge_slices(int64_t nw_launch, int64_t units) {
+  if (merge_by_warps(nw_launch, units)) return 1;
+  const int64_t avg = (nw_launch + units - 1) / units;
+  const int64_t s = (avg + kSlicePartials - 1) / kSlicePartials;
+  return (int)(s < 1 ? 1 : (s > kMaxMergeSlices ? kMaxMergeSlices : s));
+}
 // Main split-KV kernel: returns its per-SM occupancy through *blocks_per_sm
 // when `query_only`, else launches `blocks` CTAs.
 cudaError_t attn_main_k2(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
@@ -196,6 +226,17 @@ cudaError_t attn_main_k34(const AttnArgs &a, int v_bits, bool qjl, int nt, bool 
                          int blocks, cudaStream_t st);
 cudaError_t attn_main_k23(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
                          int blocks, cudaStream_t st);
+// The same with the prep kernel's ready-made key-score query operands.
+cudaError_t attn_main_k2_qop(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                             int blocks, cudaStream_t st);
+cudaError_t attn_main_k3_qop(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                             int blocks, cudaStream_t st);
+cudaError_t attn_main_k4_qop(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                             int blocks, cudaStream_t st);
+cudaError_t attn_main_k34_qop(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                              int blocks, cudaStream_t st);
+cudaError_t attn_main_k23_qop(const AttnArgs &a, int v_bits, bool qjl, int nt, bool query_only, int *blocks_per_sm,
+                              int blocks, cudaStream_t st);
 
 // Set a kernel's dynamic shared-memory limit once per device (never inside a
 // stream capture after the first call on that device).
