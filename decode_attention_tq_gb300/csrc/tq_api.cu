@@ -125,7 +125,7 @@ void lloyd_max_thresholds(int bits, double *cent, double *thr) {
 // ---------------------------------------------------------- attention plan --
 struct AttnPlan {
   int G, NT, nw_launch, blocks, slices;
-  bool qop_keys;
+  bool qop_keys, win_apart;
   size_t off_hdr, off_pre, off_clen, off_wlen, off_qrot, off_qop, off_qcst, off_qexp, off_segml, off_segacc, off_winml, off_winacc,
       off_mpart, off_mcnt, total;
 };
@@ -200,6 +200,23 @@ tq_status plan_attention(const tq_format *f, int B, int Hq, int max_pages, int w
   p->blocks = (int)((warps + wpb - 1) / wpb);
   p->nw_launch = p->blocks * wpb;
   p->qop_keys = tiles_max <= kQopMaxTilesPerWarp * p->nw_launch;
+  if (!kivi && p->qop_keys && bps == 1) {
+    // Latency-bound shape: the main kernel is launched while the prep kernel
+    // runs, and a CTA of one per SM cannot start on an SM that holds a prep
+    // block until it completes; those CTAs would start late and set the
+    // kernel's end.  Leave the prep kernel's SMs to it.
+    const int64_t prep_blocks = (f->k_qjl ? (int64_t)B * Hq : ((int64_t)B * Hq + 3) / 4) +
+                                (window > 0 ? (int64_t)B * H * ((window + kWinChunk - 1) / kWinChunk) : 0);
+    const int64_t free_sms = sms - prep_blocks;
+    if (p->blocks > free_sms && free_sms >= sms / 2) {
+      p->blocks = (int)free_sms;
+      p->nw_launch = p->blocks * wpb;
+    }
+  }
+  // The window partials by their own kernel beside the main one when the
+  // main grid leaves SMs to run it (latency-bound shapes): the prep kernel,
+  // which the main kernel waits for, then only prepares the queries.
+  p->win_apart = !kivi && p->qop_keys && window > 0 && bps == 1 && p->blocks < sms;
 
   const int64_t rows = (int64_t)B * Hq;
   const int64_t slots = (int64_t)p->nw_launch + (int64_t)B * H;
@@ -547,6 +564,7 @@ static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_hea
   a.min_tiles = kMinTilesPerWarp;
   a.merge_slices = p.slices;
   a.qop_keys = p.qop_keys;
+  a.win_apart = p.win_apart;
   a.merge_part = reinterpret_cast<float *>(ws + p.off_mpart);
   a.merge_cnt = reinterpret_cast<int32_t *>(ws + p.off_mcnt);
   // prep, main and merge start as programmatic dependents (their launches and
@@ -559,6 +577,7 @@ static tq_status decode_attn_impl(const tq_format *fmt, int batch, int num_q_hea
   if (ev_begin && cudaEventRecord(ev_begin, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (main_kernel_call(fmt, a, p.NT, false, nullptr, p.blocks, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, st) != cudaSuccess) return TQ_ERR_CUDA;
+  if (launch_attn_window(a, st) != cudaSuccess) return TQ_ERR_CUDA;
   if (launch_attn_merge(a, st) != cudaSuccess) return TQ_ERR_CUDA;
   return TQ_OK;
 }
@@ -695,6 +714,7 @@ static tq_status kivi_attn_impl(const tq_kivi_format *fmt, int batch, int num_q_
   a.min_tiles = kMinTilesPerWarp;
   a.merge_slices = p.slices;
   a.qop_keys = p.qop_keys;
+  a.win_apart = false;
   a.merge_part = reinterpret_cast<float *>(ws + p.off_mpart);
   a.merge_cnt = reinterpret_cast<int32_t *>(ws + p.off_mcnt);
   a.pdl = ev_begin == nullptr && ev_end == nullptr;

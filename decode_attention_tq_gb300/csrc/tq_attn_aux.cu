@@ -190,7 +190,7 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
   wl = wl < 0 ? 0 : (wl > a.window ? a.window : wl);
   const int t0 = c * kWinChunk;
   const int n = min(kWinChunk, wl - t0);
-  if (n <= 0) return;  // block-uniform
+  if (n <= 0) return;  // block-uniform (the caller's barriers follow for all threads)
   const __half *kbase = a.k_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
   const __half *vbase = a.v_win + (((int64_t)b * a.H + h) * a.window + t0) * kD;
   // every load of the block is issued before the first barrier: this
@@ -294,6 +294,25 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
     const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // b * Hq + qh
     if (row < (int64_t)a.B * a.Hq) prep_query(a, row, lane);
   }
+}
+
+// Window partials in a launch of their own, after the main kernel as its
+// programmatic dependent: it starts once the main kernel is past its grid
+// wait (so the append before the prep kernel has completed and the window
+// rings are final) and runs beside it on the SMs the main grid leaves free.
+// Every thread waits for the main kernel before it exits, so the merge
+// launched after this kernel sees the main kernel's partials too.
+__global__ void __launch_bounds__(128) attn_window_kernel(const AttnArgs a) {
+  __shared__ __align__(16) float s_q[8 * kQRow];
+  __shared__ float s_p[8][kWinChunk];
+  griddep_launch_dependents();  // the merge may launch; it waits for this grid
+  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
+  const int64_t k = blockIdx.x;
+  if (a.G <= 4)
+    prep_window<4>(a, k / nch, (int)(k % nch), s_q, s_p);
+  else
+    prep_window<8>(a, k / nch, (int)(k % nch), s_q, s_p);
+  griddep_wait();
 }
 
 // Warp that owns tile x: largest w in [0, NW) with floor(T*w/NW) <= x.
@@ -578,9 +597,18 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_wide_kernel(const
 cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
   const int64_t rows = (int64_t)a.B * a.Hq;
   const int64_t row_blocks = qjl ? rows : (rows + 3) / 4;
-  const int64_t win_blocks = a.window > 0 ? (int64_t)a.B * a.H * ((a.window + kWinChunk - 1) / kWinChunk) : 0;
+  const int64_t win_blocks =
+      a.window > 0 && !a.win_apart ? (int64_t)a.B * a.H * ((a.window + kWinChunk - 1) / kWinChunk) : 0;
   const cudaError_t e = launch_maybe_dependent(attn_prep_kernel, dim3((unsigned)(row_blocks + win_blocks)), dim3(128), 0,
                                                st, a.pdl, a, qjl, (int)row_blocks);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_window(const AttnArgs &a, cudaStream_t st) {
+  if (!a.win_apart || a.window <= 0) return cudaSuccess;
+  const int64_t blocks = (int64_t)a.B * a.H * ((a.window + kWinChunk - 1) / kWinChunk);
+  const cudaError_t e = launch_maybe_dependent(attn_window_kernel, dim3((unsigned)blocks), dim3(128), 0, st, a.pdl, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -136,6 +136,7 @@ struct AttnArgs {
   bool pdl;          // host: launch main and merge as programmatic dependents
   bool raw;          // KIVI cache: no query rotation, the accumulators are raw-domain
   bool qop_keys;     // host: launch the main kernel that loads its key-score query operands from q_op
+  bool win_apart;    // window partials by their own kernel after the main kernel (else in the prep kernel)
 };
 
 // KIVI-style control arm (tq_kivi.cu): encode of keys (per-channel groups of
@@ -201,6 +202,9 @@ cudaError_t launch_decode(const DecodeArgs &a, int bits, bool qjl, bool mixed, i
 constexpr int kWinChunk = 32;  // window tokens per window partial
 cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st);
 cudaError_t launch_attn_merge(const AttnArgs &a, cudaStream_t st);
+// Window partials by their own launch (a.win_apart): after the main kernel,
+// as its programmatic dependent; no-op without a window.
+cudaError_t launch_attn_window(const AttnArgs &a, cudaStream_t st);
 // Merge geometry: rows whose (sequence, kv head) average at most
 // kWarpMergeMaxPartials partials are merged by one warp each, the others by
 // blocks of kMergeWarps warps, kSlicePartials partials per block (slices).
