@@ -70,6 +70,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const RollArgs r
   __half *s_new = reinterpret_cast<__half *>(smem + append_cells_bytes(KQJL));
   __half *s_old = s_new + 2 * nsh * kD;
 
+  // Launched as a programmatic dependent of the kernel before it: nothing is
+  // read before that kernel has completed (its launch and block scheduling
+  // overlap that kernel's end).
+  griddep_wait();
   // A kernel launched after this one as a programmatic dependent (the
   // attention's prep kernel) may start now: it waits for this grid to
   // complete before it reads anything.
@@ -185,7 +189,8 @@ cudaError_t launch_append_t(const RollArgs &r, const EncodeArgs &ka, const Encod
   static unsigned long long done = 0;
   const cudaError_t e = set_smem_once(kern, (int)append_smem_bytes(KQJL, kAppendMaxVecs, true), done);
   if (e != cudaSuccess) return e;
-  kern<<<blocks, kAppendThreads, smem, st>>>(r, ka, va, spb);
+  const cudaError_t le = launch_maybe_dependent(kern, dim3(blocks), dim3(kAppendThreads), smem, st, true, r, ka, va, spb);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

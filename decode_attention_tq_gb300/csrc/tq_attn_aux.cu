@@ -480,16 +480,23 @@ __device__ __forceinline__ void row_finish(const AttnArgs &a, int64_t row, int l
 
 // Warp variant (rows with few partials): one warp per (sequence, query head)
 // row, four rows per block; no shared memory and no block barriers.
+// Both merge kernels read the prep kernel's outputs (tile counts, clamped
+// lengths) before their grid wait: a merge block starts only after the main
+// kernel is past its own grid wait, i.e. after the prep kernel has completed.
+// The partials (main kernel) and the window partials are read after it.
 __global__ void __launch_bounds__(128) attn_merge_warp_kernel(const AttnArgs a) {
-  griddep_wait();  // the main kernel's partials
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);  // b * Hq + qh
-  if (row >= (int64_t)a.B * a.Hq) return;
-  const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
+  const bool live = row < (int64_t)a.B * a.Hq;
+  const int b = live ? (int)(row / a.Hq) : 0, qh = live ? (int)(row % a.Hq) : 0;
   const int h = qh / a.G, g = qh % a.G;
+  RowParts r;
+  if (live) r = row_parts(a, b, h);
+  griddep_wait();  // the main kernel's partials
+  griddep_launch_dependents();  // a dependent (the next append) may launch; it waits for this grid
+  if (!live) return;
   RowWindow win;
   row_window_load(a, row, b, lane, win);
-  const RowParts r = row_parts(a, b, h);
   float M = -INFINITY, L = 0.f;
   float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
   merge_row_range<kWarpMergeMaxPartials>(a, r, g, 0, r.n, M, L, A, lane);
@@ -510,19 +517,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_wide_kernel(const
   __shared__ float2 s_ml[kMergeWarps];
   __shared__ float4 s_wacc[kWinPre][kD / 4];
   __shared__ float2 s_wml[32];
-  griddep_wait();  // the main kernel's partials
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row = blockIdx.x / a.merge_slices;  // b * Hq + qh
   const int slice = (int)(blockIdx.x - row * a.merge_slices);
   const int b = (int)(row / a.Hq), qh = (int)(row % a.Hq);
   const int h = qh / a.G, g = qh % a.G;
-  const RowParts r = row_parts(a, b, h);
+  const RowParts r = row_parts(a, b, h);  // prep outputs: before the grid wait
+  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
+  const int64_t nwin = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
+  griddep_wait();  // the main kernel's partials
+  griddep_launch_dependents();  // a dependent (the next append) may launch; it waits for this grid
   // slices this row uses (the same in every block of the row)
   int64_t ns = (r.n + kSlicePartials - 1) / kSlicePartials;
   ns = ns < 1 ? 1 : (ns > a.merge_slices ? a.merge_slices : ns);
   if (slice >= ns) return;  // block-uniform
-  const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
-  const int64_t nwin = a.window > 0 ? (a.wlen[b] + kWinChunk - 1) / kWinChunk : 0;
   if (warp == kMergeWarps - 1 && nwin <= kWinPre) {
     for (int u = 0; u < nwin; u++) cp_async16(&s_wacc[u][lane], a.win_acc + (row * nch + u) * kD + 4 * lane);
     if (lane < nwin) cp_async8(&s_wml[lane], a.win_ml + (row * nch + lane) * 2);
