@@ -8,9 +8,12 @@ namespace tq {
 
 // Blocks per SM: 2 with QJL (S cells in shared memory), else 3 for 4-bit and
 // 4 for 2- and 3-bit codes (measured: 3-bit +6 %, 2-bit +2 % at 4 blocks).
+#ifndef TQ_ENCODE_MIN_BLOCKS_23
+#define TQ_ENCODE_MIN_BLOCKS_23 4
+#endif
 template <int BITS, bool QJL>
 constexpr int encode_min_blocks() {
-  return QJL ? 2 : (BITS == 4 ? TQ_ENCODE_MIN_BLOCKS : 4);
+  return QJL ? 2 : (BITS == 4 ? TQ_ENCODE_MIN_BLOCKS : TQ_ENCODE_MIN_BLOCKS_23);
 }
 
 template <int BITS, bool QJL, bool MIXED = false>

@@ -291,6 +291,12 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
   const float *cent = T.cent + 16 * set, *midp = T.mid + 16 * set;
   const uint2 *qlut = T.qlut + set * kQBuckets;
   const float2 *qcen = T.qcen + set * kQBuckets;
+  // shared-window addresses of the bucket tables, offset so that the bucket
+  // entry of the magic-number sum s (quant_bucket) is at base + 8 * bits(s)
+  // (one shift-add per coordinate; the sums wrap mod 2^32 as addresses do)
+  const uint32_t kMagicBits = (uint32_t)__float_as_int(12582912.0f);
+  const uint32_t qlut_at = (uint32_t)__cvta_generic_to_shared(qlut) - 8u * kMagicBits;
+  const uint32_t qcen_at = (uint32_t)__cvta_generic_to_shared(qcen) - 8u * kMagicBits;
   const bool lut_bad = (T.lut_bad >> set) & 1;
   const bool small = NH <= 0x7fffffff;
   // sign masks of this thread's fp16 pairs (coordinates 32c + 8q + 2p, +1)
@@ -353,26 +359,13 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
 
     // fp16 pairs of coordinates 32c + 8q + 2p, +1, sign-flipped by D
     uint32_t xw[4][4];
-    float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; c++) {
       const uint4 raw = *reinterpret_cast<const uint4 *>(a.x + vv * kD + 32 * c + 8 * q);
       const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int p = 0; p < 4; p++) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r4[p]));
-        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-        xw[c][p] = r4[p] ^ smask[c][p];
-      }
+      for (int p = 0; p < 4; p++) xw[c][p] = r4[p] ^ smask[c][p];
     }
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    const float nrm = sqrtf(ss);
-    // A NaN or infinite coordinate (finite fp16 vectors cannot overflow ss)
-    // stores the norm as computed and a zero block, and never reaches the
-    // quantizer's bucket table with a NaN.
-    const bool bad = !(ss <= 3.0e38f);
-    const bool zero = !(nrm > 0.f) || bad;
 
     // z = x_c H_32 on the tensor cores, then the H_4 butterfly over blocks
     float z[4][8];
@@ -398,6 +391,20 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
       x[16 + i] = s01 - s23;
       x[24 + i] = d01 - d23;
     }
+    // ||x||^2 from the rotated coordinates (||H y||^2 = d ||y||^2 for the
+    // unnormalised Sylvester H; the products of the transform are exact).
+    // A NaN or infinite coordinate (finite fp16 vectors cannot overflow ss)
+    // stores the norm as computed and a zero block, and never reaches the
+    // quantizer's bucket table with a NaN.
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; j++) ss = fmaf(x[j], x[j], ss);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss *= 1.0f / (float)kD;
+    const float nrm = sqrtf(ss);
+    const bool bad = !(ss <= 3.0e38f);
+    const bool zero = !(nrm > 0.f) || bad;
     if (bad) {
 #pragma unroll
       for (int j = 0; j < 32; j++) x[j] = 0.f;
@@ -409,12 +416,14 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
 #pragma unroll
       for (int j = 0; j < 32; j++) {
         const float u = x[j] * inv;
-        const int b = quant_bucket(u);
-        const uint2 e = qlut[b];
+        const uint32_t sb = (uint32_t)__float_as_int(fmaf(u, 4.0f, kQMagic)) << 3;  // 8 x bits of quant_bucket's sum
+        uint2 e;
+        asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(e.x), "=r"(e.y) : "r"(qlut_at + sb));
         const bool up = u >= __uint_as_float(e.y);
         idx[j] = (int)e.x + (up ? 1 : 0);  // a zero vector's codes are cleared when packed
         if constexpr (QJL) {
-          const float2 c = qcen[b];
+          float2 c;
+          asm("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(c.x), "=f"(c.y) : "r"(qcen_at + sb));
           x[j] = u - (up ? c.y : c.x);  // residual in u units (unused for a zero vector: gamma, bits 0)
         }
       }
