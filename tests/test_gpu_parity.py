@@ -152,6 +152,15 @@ ATTN_CASES = {
     "k4v2_g4_w": (ti.Format(128, 4, 2, 0, 128, 64, 4), 2, 16, [390, 1025], 40, [40, 33]),
     # a page of 48 tokens (three tiles per page) and many short sequences
     "k4v4_p48_b24": (ti.Format(128, 4, 4, 0, 128, 48, 2), 24, 4, [int(x) for x in (np.arange(24) * 37) % 211], 8, [int(x) for x in np.arange(24) % 9]),
+    # batch-1 shapes with one or two kv heads and long sequences: hundreds to
+    # over a thousand partials per (b, h), so the merge cuts a row into
+    # several slices (the block finishing a row's last slice merges them);
+    # the window partials come from their own kernel; the main kernel takes
+    # ready-made query operands
+    "k4v4_h1_g8_t24k_w": (ti.Format(128, 4, 4, 0, 128, 64, 1), 1, 8, [24000], 48, [48]),
+    "k3qjl_v4_h2_g8_t16k_w": (ti.Format(128, 3, 4, 1, 128, 64, 2), 1, 16, [16000], 128, [128]),
+    # rows with many partials beside rows with few (one slice, one chunk)
+    "k4v4_h1_g4_ragged": (ti.Format(128, 4, 4, 0, 128, 64, 1), 2, 4, [20000, 300], 16, [16, 5]),
 }
 
 
