@@ -8,12 +8,9 @@ namespace tq {
 
 // Blocks per SM: 2 with QJL (S cells in shared memory), else 3 for 4-bit and
 // 4 for 2- and 3-bit codes (measured: 3-bit +6 %, 2-bit +2 % at 4 blocks).
-#ifndef TQ_ENCODE_MIN_BLOCKS_23
-#define TQ_ENCODE_MIN_BLOCKS_23 4
-#endif
 template <int BITS, bool QJL>
 constexpr int encode_min_blocks() {
-  return QJL ? 2 : (BITS == 4 ? TQ_ENCODE_MIN_BLOCKS : TQ_ENCODE_MIN_BLOCKS_23);
+  return QJL ? 2 : (BITS == 4 ? kEncodeBlocks4 : 4);
 }
 
 template <int BITS, bool QJL, bool MIXED = false>
@@ -24,7 +21,7 @@ __global__ void __launch_bounds__(256, encode_min_blocks<BITS, QJL>()) encode_ke
 // Keys and values of the same tokens in one launch (same bits, keys without
 // QJL): blockIdx.y selects the kind.
 template <int BITS>
-__global__ void __launch_bounds__(256, TQ_ENCODE_MIN_BLOCKS) encode_kv_kernel(const EncodeArgs ka, const EncodeArgs va) {
+__global__ void __launch_bounds__(256, kEncodeBlocks4) encode_kv_kernel(const EncodeArgs ka, const EncodeArgs va) {
   if (blockIdx.y == 0)
     encode_body<BITS, false>(ka);
   else
