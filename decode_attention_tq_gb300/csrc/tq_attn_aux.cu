@@ -122,27 +122,29 @@ __device__ void prep_query(const AttnArgs &a, int64_t row, int lane) {
   }
 }
 
-// With QJL: one 128-thread block per query row.  Every warp rotates the row
-// (a few shuffles); warp w projects it on S rows 32w .. 32w + 31, S q_rot:
-// lane holds coordinates 4 lane .. 4 lane + 3 and reads the same coordinates
-// of each S row (one coalesced 512-byte row per load, all 32 in flight).
-// The 32 per-lane partial dots are summed over the warp by a transposing
-// butterfly (31 shuffles), after which lane l holds row 32w + l.
+// With QJL: one block of NW warps per query row (NW = 4 or 8).  Every warp
+// rotates the row (a few shuffles); warp w projects it on S rows R w ..
+// R w + R - 1 (R = 128 / NW), S q_rot: lane holds coordinates 4 lane ..
+// 4 lane + 3 and reads the same coordinates of each S row (one coalesced
+// 512-byte row per load, all R loads issued before the rotation).  The R
+// per-lane partial dots are summed over the warp by a transposing butterfly,
+// after which lane l holds row R w + l (R = 32), or lanes 2i, 2i+1 hold row
+// R w + i (R = 16).
+template <int NW>
 __device__ void prep_query_qjl(const AttnArgs &a, int64_t row, int warp, int lane, float *s_red) {
-  // the warp's 32 S rows are loaded first (they depend on nothing), together
-  // with the query row: one memory latency
-  float4 sv[32];
-  const float4 *S4 = reinterpret_cast<const float4 *>(a.S + (int64_t)(32 * warp) * kD) + lane;
+  constexpr int R = kM / NW;
+  float4 sv[R];
+  const float4 *S4 = reinterpret_cast<const float4 *>(a.S + (int64_t)(R * warp) * kD) + lane;
 #pragma unroll
-  for (int i = 0; i < 32; i++) sv[i] = __ldg(S4 + i * (kD / 4));
+  for (int i = 0; i < R; i++) sv[i] = __ldg(S4 + i * (kD / 4));
   float x[4];
   rotate_query(a, row, lane, x);
   if (warp == 0) store_query(a, row, lane, x);
-  float v[32];
+  float v[R];
 #pragma unroll
-  for (int i = 0; i < 32; i++) v[i] = fmaf(sv[i].x, x[0], fmaf(sv[i].y, x[1], fmaf(sv[i].z, x[2], sv[i].w * x[3])));
+  for (int i = 0; i < R; i++) v[i] = fmaf(sv[i].x, x[0], fmaf(sv[i].y, x[1], fmaf(sv[i].z, x[2], sv[i].w * x[3])));
 #pragma unroll
-  for (int m = 16, n = 16; m >= 1; m >>= 1, n >>= 1) {
+  for (int m = 16, n = R / 2; n >= 1; m >>= 1, n >>= 1) {
     // keep the half of the n pairs (v[i], v[i + n]) selected by lane bit m,
     // add the partner's copy of it
     const bool up = (lane & m) != 0;
@@ -152,16 +154,25 @@ __device__ void prep_query_qjl(const AttnArgs &a, int64_t row, int warp, int lan
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
     }
   }
+  constexpr int kRest = R == 32 ? 0 : 1;  // lane bits not yet summed (bit 0 for R = 16)
+  if (kRest) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+  const int i_row = R == 32 ? lane : (lane >> 1);  // this lane's row within the warp's R
   const float my = warp_max_xor(fabsf(v[0]), 31);
   if (lane == 0) s_red[warp] = my;
   __syncthreads();
-  const int es = operand_exponent(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
-  // slice t = warp of parts 2 (hi) and 3 (lo), value i = lane (qop_qjl_half)
+  float mx = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; w++) mx = fmaxf(mx, s_red[w]);
+  const int es = operand_exponent(mx);
+  // slice t of parts 2 (hi) and 3 (lo): S rows 32t .. 32t + 31, value i (qop_qjl_half)
   __half hi, lo;
   split_half(v[0] * ldexpf(1.0f, es), hi, lo);
-  __half *op = reinterpret_cast<__half *>(a.q_op + row * 256);
-  op[2 * (128 + 16 * warp) + qop_qjl_half(lane)] = hi;
-  op[2 * (192 + 16 * warp) + qop_qjl_half(lane)] = lo;
+  const int srow = R * warp + i_row, t = srow >> 5, i = srow & 31;
+  if (R == 32 || (lane & 1) == 0) {
+    __half *op = reinterpret_cast<__half *>(a.q_op + row * 256);
+    op[2 * (128 + 16 * t) + qop_qjl_half(i)] = hi;
+    op[2 * (192 + 16 * t) + qop_qjl_half(i)] = lo;
+  }
   if (threadIdx.x == 0) {
     a.merge_cnt[row] = 0;
     a.q_exp[row * 2 + 1] = es;
@@ -270,7 +281,7 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
   }
 }
 
-__global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool qjl, int row_blocks) {
+__global__ void __launch_bounds__(256) attn_prep_kernel(const AttnArgs a, bool qjl, int row_blocks) {
   __shared__ __align__(16) float s_q[8 * kQRow];
   __shared__ float s_p[8][kWinChunk];
   // Launched as a programmatic dependent of whatever kernel precedes it in
@@ -288,8 +299,11 @@ __global__ void __launch_bounds__(128) attn_prep_kernel(const AttnArgs a, bool q
     return;
   }
   if (blockIdx.x == 0 && warp == 0) prep_lengths(a, lane);
-  if (qjl) {
-    prep_query_qjl(a, blockIdx.x, warp, lane, s_q);  // one row per block (b * Hq + qh)
+  if (qjl) {  // one row per block (b * Hq + qh)
+    if (blockDim.x == 256)
+      prep_query_qjl<8>(a, blockIdx.x, warp, lane, s_q);
+    else
+      prep_query_qjl<4>(a, blockIdx.x, warp, lane, s_q);
   } else {
     const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // b * Hq + qh
     if (row < (int64_t)a.B * a.Hq) prep_query(a, row, lane);
@@ -607,8 +621,11 @@ cudaError_t launch_attn_prep(const AttnArgs &a, bool qjl, cudaStream_t st) {
   const int64_t row_blocks = qjl ? rows : (rows + 3) / 4;
   const int64_t win_blocks =
       a.window > 0 && !a.win_apart ? (int64_t)a.B * a.H * ((a.window + kWinChunk - 1) / kWinChunk) : 0;
-  const cudaError_t e = launch_maybe_dependent(attn_prep_kernel, dim3((unsigned)(row_blocks + win_blocks)), dim3(128), 0,
-                                               st, a.pdl, a, qjl, (int)row_blocks);
+  // QJL rows without window blocks in the launch: 8 warps per row (the window
+  // blocks need 128 threads: thread = coordinate)
+  const int threads = qjl && win_blocks == 0 ? 256 : 128;
+  const cudaError_t e = launch_maybe_dependent(attn_prep_kernel, dim3((unsigned)(row_blocks + win_blocks)), dim3(threads),
+                                               0, st, a.pdl, a, qjl, (int)row_blocks);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
