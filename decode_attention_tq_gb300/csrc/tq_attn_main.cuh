@@ -502,6 +502,12 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 
   const int lane = threadIdx.x & 31, r = lane >> 2, t = lane & 3;
   const int64_t wg = (int64_t)blockIdx.x * attn_warps(NT, QJL) + (threadIdx.x >> 5);
+  // QOP (short tile ranges) with at most 31 sequences: lane i loads pre[i]
+  // together with the header, so the first tile is located without a second
+  // dependent load (a ballot over the lanes instead of the binary search)
+  const bool pre_in_lanes = QOP && a.B <= 31;
+  int64_t pre_l = INT64_MAX;
+  if (pre_in_lanes && lane <= a.B) pre_l = a.pre[lane];
   const int64_t T = a.hdr->total_tiles;
   const int64_t NW = a.hdr->active_warps;
   if (wg >= NW) return;
@@ -519,17 +525,27 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
 
   // locate the first tile: largest b with H * pre[b] <= ts
   int b = 0;
-  {
+  int64_t pre_b, pre_b1;
+  if (pre_in_lanes) {
+    // pre is non-decreasing and pre[0] = 0: the lanes b < B with
+    // H * pre[b] <= ts are a prefix
+    const uint32_t le = __ballot_sync(0xffffffffu, lane < a.B && H * pre_l <= ts);
+    b = __popc(le) - 1;
+    pre_b = __shfl_sync(0xffffffffu, pre_l, b);
+    pre_b1 = __shfl_sync(0xffffffffu, pre_l, b + 1);
+  } else {
     int lo = 0, hi = a.B;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (H * a.pre[mid] <= ts) lo = mid; else hi = mid;
     }
     b = lo;
+    pre_b = a.pre[b];
+    pre_b1 = a.pre[b + 1];
   }
-  int tb = (int)(a.pre[b + 1] - a.pre[b]);
-  int h = (int)((ts - H * a.pre[b]) / tb);
-  int j = (int)((ts - H * a.pre[b]) - (int64_t)h * tb);
+  int tb = (int)(pre_b1 - pre_b);
+  int h = (int)((ts - H * pre_b) / tb);
+  int j = (int)((ts - H * pre_b) - (int64_t)h * tb);
   int64_t pos = ts;
 
   while (pos < te) {

@@ -161,6 +161,10 @@ ATTN_CASES = {
     "k3qjl_v4_h2_g8_t16k_w": (ti.Format(128, 3, 4, 1, 128, 64, 2), 1, 16, [16000], 128, [128]),
     # rows with many partials beside rows with few (one slice, one chunk)
     "k4v4_h1_g4_ragged": (ti.Format(128, 4, 4, 0, 128, 64, 1), 2, 4, [20000, 300], 16, [16, 5]),
+    # more than 31 short sequences (the first tile located by a binary search
+    # over the tile prefix sums, not by a lane ballot)
+    "k4v4_b40_short": (ti.Format(128, 4, 4, 0, 128, 16, 2), 40, 4, [int(x) for x in (np.arange(40) * 13) % 90 + 1], 8,
+                       [int(x) for x in np.arange(40) % 8]),
 }
 
 
