@@ -17,11 +17,11 @@
 // cross-block ordering and each phase waits on at most one memory latency:
 //   1. loads that depend on nothing: the sequences' counters, their new
 //      tokens (into shared memory), both kinds' codebooks and sign flips (and
-//      the QJL matrix);
+//      the QJL matrix, into registers);
 //   2. the action of each sequence from its counters; side by side, the block
 //      table entry of the compressed position it writes and the ring slot of
 //      the token that leaves (copied into shared memory); the quantizer
-//      tables are built meanwhile;
+//      tables and the QJL matrix's hi / lo cells are built meanwhile;
 //   3. the new tokens into the rings (every leaving token has been read),
 //      the counters, and the two encodes from shared memory at once: keys on
 //      warps 0-3, values on warps 4-7.
@@ -92,7 +92,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const RollArgs r
   }
   if (tid < kD) encode_tables_load<KBITS, KMIX>(tk, ka, tid);
   else if (tid < 2 * kD) encode_tables_load<VBITS, false>(tv, va, tid - kD);
-  if constexpr (KQJL) encode_s_cells_load(ka);
+  // the QJL matrix: loaded here (one memory latency beside the others),
+  // converted into its hi / lo cells in phase 2, where that work overlaps the
+  // block-table lookup (256 threads: one batch of kSCellBatch float4 each)
+  static_assert(kAppendThreads * kSCellBatch * 4 == kM * kD, "one batch of S per thread");
+  float4 sv[KQJL ? kSCellBatch : 1];
+  if constexpr (KQJL) encode_s_batch_load(ka, tid, sv);
   __syncthreads();
 
   // 2. actions, pages and leaving tokens, quantizer tables
@@ -131,6 +136,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const RollArgs r
   }
   encode_tables_build<KBITS, KMIX>(tk);
   encode_tables_build<VBITS, false>(tv);
+  if constexpr (KQJL) encode_s_batch_store(tid, sv);
   __syncthreads();
 
   // 3. rings, counters, encodes (slot -1: nothing to encode for that sequence)

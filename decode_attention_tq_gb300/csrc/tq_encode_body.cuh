@@ -211,39 +211,47 @@ __device__ __forceinline__ void encode_tables_load(EncodeTables<MIXED> &T, const
 
 // QJL: the matrix S staged as fp16 hi/lo cells in dynamic shared memory, by
 // every thread of the block.
-__device__ __forceinline__ void encode_s_cells_load(const EncodeArgs &a) {
-  extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells
-  // cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
-  // coordinates thread t contributes at k-step ks of the projection
-  // four consecutive coordinates share a cell: float4 loads, sixteen per
-  // thread in flight (all of them for 256 threads: one memory latency), and
-  // one 8-byte store each for the hi and lo halves
-  constexpr int N4 = kM * kD / 4, kBatch = 16;
-  const int tid = threadIdx.x;
+// cell (l, t, ks) holds S[l][32(ks/2) + 8t + 4(ks%2) + 0..3]: the
+// coordinates thread t contributes at k-step ks of the projection.  Four
+// consecutive coordinates share a cell: float4 loads, sixteen per thread in
+// flight (all of them for 256 threads: one memory latency), and one 8-byte
+// store each for the hi and lo halves.
+constexpr int kSCellBatch = 16;
+__device__ __forceinline__ void encode_s_batch_load(const EncodeArgs &a, int i0, float4 (&v)[kSCellBatch]) {
+  constexpr int N4 = kM * kD / 4;
   const float4 *S4 = reinterpret_cast<const float4 *>(a.S);
+#pragma unroll
+  for (int u = 0; u < kSCellBatch; u++) {
+    const int i4 = i0 + u * blockDim.x;
+    v[u] = i4 < N4 ? __ldg(S4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+__device__ __forceinline__ void encode_s_batch_store(int i0, const float4 (&v)[kSCellBatch]) {
+  extern __shared__ __align__(16) uint4 s_Sq[];  // [m][4][8] cells
+  constexpr int N4 = kM * kD / 4;
   uint2 *cells = reinterpret_cast<uint2 *>(s_Sq);
-  for (int i0 = tid; i0 < N4; i0 += kBatch * blockDim.x) {
-    float4 v[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; u++) {
-      const int i4 = i0 + u * blockDim.x;
-      v[u] = i4 < N4 ? __ldg(S4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = 0; u < kSCellBatch; u++) {
+    const int i4 = i0 + u * blockDim.x;
+    if (i4 < N4) {
+      const int l = (4 * i4) / kD, j = (4 * i4) % kD;
+      __half h0, l0, h1, l1, h2, l2, h3, l3;
+      split_half(v[u].x, h0, l0);
+      split_half(v[u].y, h1, l1);
+      split_half(v[u].z, h2, l2);
+      split_half(v[u].w, h3, l3);
+      const int cell = sq_cell(l, (j & 31) >> 3, 2 * (j >> 5) + ((j >> 2) & 1));
+      cells[2 * cell] = make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(h2, h3));
+      cells[2 * cell + 1] = make_uint2(pack_half2_raw(l0, l1), pack_half2_raw(l2, l3));
     }
-#pragma unroll
-    for (int u = 0; u < kBatch; u++) {
-      const int i4 = i0 + u * blockDim.x;
-      if (i4 < N4) {
-        const int l = (4 * i4) / kD, j = (4 * i4) % kD;
-        __half h0, l0, h1, l1, h2, l2, h3, l3;
-        split_half(v[u].x, h0, l0);
-        split_half(v[u].y, h1, l1);
-        split_half(v[u].z, h2, l2);
-        split_half(v[u].w, h3, l3);
-        const int cell = sq_cell(l, (j & 31) >> 3, 2 * (j >> 5) + ((j >> 2) & 1));
-        cells[2 * cell] = make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(h2, h3));
-        cells[2 * cell + 1] = make_uint2(pack_half2_raw(l0, l1), pack_half2_raw(l2, l3));
-      }
-    }
+  }
+}
+__device__ __forceinline__ void encode_s_cells_load(const EncodeArgs &a) {
+  constexpr int N4 = kM * kD / 4;
+  for (int i0 = threadIdx.x; i0 < N4; i0 += kSCellBatch * blockDim.x) {
+    float4 v[kSCellBatch];
+    encode_s_batch_load(a, i0, v);
+    encode_s_batch_store(i0, v);
   }
 }
 
