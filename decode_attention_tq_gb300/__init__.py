@@ -8,6 +8,7 @@ from .tq import (  # noqa: F401
     TQ_DEVERR_LENGTH,
     TQ_DEVERR_PAGE_RANGE,
     TQ_DEVERR_SLOT_RANGE,
+    TQ_DEVERR_TIMEOUT,
     TQ_KIND_K,
     TQ_KIND_V,
     TQ_STATIC_SCRATCH_BYTES,

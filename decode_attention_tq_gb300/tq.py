@@ -23,6 +23,7 @@ TQ_KIND_V = 1
 TQ_DEVERR_SLOT_RANGE = 0x1
 TQ_DEVERR_PAGE_RANGE = 0x2
 TQ_DEVERR_LENGTH = 0x4
+TQ_DEVERR_TIMEOUT = 0x8
 
 STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_CUDA", 4: "TQ_ERR_DEVICE_FAULT",
           5: "TQ_ERR_TIMEOUT", 6: "TQ_ERR_WORKSPACE", 7: "TQ_ERR_SCRATCH_LIMIT"}

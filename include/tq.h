@@ -57,6 +57,9 @@ enum { TQ_KIND_K = 0, TQ_KIND_V = 1 };
 #define TQ_DEVERR_SLOT_RANGE 0x1   /* slot_mapping[n] >= num_pages * page_size          */
 #define TQ_DEVERR_PAGE_RANGE 0x2   /* block_tables entry outside [0, num_pages)         */
 #define TQ_DEVERR_LENGTH 0x4       /* comp_lens[b] > max_pages*P, win_lens[b] > window, or a negative length */
+#define TQ_DEVERR_TIMEOUT 0x8      /* a bounded wait inside a kernel ran out (the tensor-core
+                                      completion of the QJL key encode); that launch's sign
+                                      words are incomplete                                 */
 
 typedef struct {
   int32_t head_dim;     /* d                                                   */
@@ -152,6 +155,10 @@ tq_status tq_page_layout(const tq_format *fmt, tq_layout *out);
  * structured rotation of the design study's 'Dense and structured transform
  * comparison' and the QJL sketch of the debugging post's 'The QJL detective
  * story'.  An all-zero vector stores n = 0, gamma = 0, all codes/bits 0.
+ * Keys with QJL compute S e on the tensor cores in batches of 128 vectors
+ * and wait for each batch's products with a time limit (one second); a wait
+ * that runs out sets TQ_DEVERR_TIMEOUT and leaves the later sign words of
+ * that launch unwritten.
  *   x_f16        device fp16 [N][H][d]
  *   slot_mapping device int32 [N]; token n goes to page slot/P, offset slot%P;
  *                a negative slot skips the token; two tokens with one slot
@@ -163,7 +170,8 @@ tq_status tq_page_layout(const tq_format *fmt, tq_layout *out);
  *   signs        device uint8 [d], 1 = negate coordinate (the kind's D)
  *   codebook     device fp32 [2^b + 2^b - 1] for this kind's b
  *   S            device fp32 [m][d] row-major (keys with QJL), else NULL
- *   err_word     device int32 or NULL (TQ_DEVERR_SLOT_RANGE)
+ *   err_word     device int32 or NULL (TQ_DEVERR_SLOT_RANGE; TQ_DEVERR_TIMEOUT
+ *                for keys with QJL, see above)
  */
 tq_status tq_encode(const tq_format *fmt, int kind, const void *x_f16, int64_t n_tokens,
                     const int32_t *slot_mapping, void *page_pool, int64_t num_pages,

@@ -156,3 +156,14 @@ def test_kivi_host_validation_before_any_launch(lib):
                                    1 << 20, None, None) == 1
     assert lib.tq_kivi_decode_attn(C.byref(f), 1, 8, dummy, dummy, 4, dummy, 4, dummy, None, None, None, 16, dummy, dummy,
                                    1 << 20, None, None) == 1  # window buffers missing
+
+
+def test_device_error_bits_match_header():
+    from decode_attention_tq_gb300 import tq
+
+    src = open(os.path.join(ROOT, "include", "tq.h")).read()
+    bits = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define (TQ_DEVERR_[A-Z_]+) 0x([0-9a-fA-F]+)", src)}
+    assert set(bits) == {"TQ_DEVERR_SLOT_RANGE", "TQ_DEVERR_PAGE_RANGE", "TQ_DEVERR_LENGTH", "TQ_DEVERR_TIMEOUT"}
+    for name, v in bits.items():
+        assert getattr(tq, name) == v, name
+    assert len(set(bits.values())) == len(bits) and all(v & (v - 1) == 0 for v in bits.values())
