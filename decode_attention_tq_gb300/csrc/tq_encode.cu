@@ -6,16 +6,69 @@
 
 namespace tq {
 
-// Blocks per SM: 2 with QJL (S cells in shared memory), else 3 for 4-bit and
-// 4 for 2- and 3-bit codes (measured: 3-bit +6 %, 2-bit +2 % at 4 blocks).
-template <int BITS, bool QJL>
+// Blocks per SM of the encode without QJL: 3 for 4-bit and 4 for 2- and
+// 3-bit codes (measured: 3-bit +6 %, 2-bit +2 % at 4 blocks).
+template <int BITS>
 constexpr int encode_min_blocks() {
-  return QJL ? 2 : (BITS == 4 ? kEncodeBlocks4 : 4);
+  return BITS == 4 ? kEncodeBlocks4 : 4;
 }
 
-template <int BITS, bool QJL, bool MIXED = false>
-__global__ void __launch_bounds__(256, encode_min_blocks<BITS, QJL>()) encode_kernel(const EncodeArgs a) {
-  encode_body<BITS, QJL, MIXED>(a);
+template <int BITS, bool MIXED = false>
+__global__ void __launch_bounds__(256, encode_min_blocks<BITS>()) encode_kernel(const EncodeArgs a) {
+  encode_body<BITS, false, MIXED>(a);
+}
+
+// Keys with QJL: the sketch products on tcgen05 (UmmaQjl in
+// tq_encode_body.cuh).  One block of 16 warps per SM: S hi/lo (64 KB) and
+// two residual buffers (2 x 64 KB) of 128-row operand tiles, 256 columns of
+// tensor memory for two fp32 accumulators.
+template <int BITS, bool MIXED>
+__global__ void __launch_bounds__(kUmmaThreads, 1) encode_qjl_kernel(const EncodeArgs a) {
+  __shared__ EncodeTables<MIXED> T;
+  __shared__ uint64_t s_info[4 * kUmmaRows];
+  __shared__ __align__(8) uint64_t s_mbar[4];  // full[0], full[1], done[0], done[1]
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  extern __shared__ __align__(16) uint4 s_Sq[];  // the operand tiles (1024-byte aligned below)
+  const int tid = threadIdx.x;
+  const uint32_t dyn = umma::smem_addr(s_Sq);
+  const uint32_t pad = (1024u - (dyn & 1023u)) & 1023u;
+  uint8_t *tiles = reinterpret_cast<uint8_t *>(s_Sq) + pad;
+  if (tid < kD) encode_tables_load<BITS, MIXED>(T, a, tid);
+  if (tid == 0) {
+    umma::mbar_init(umma::smem_addr(&s_mbar[0]), kUmmaThreads);
+    umma::mbar_init(umma::smem_addr(&s_mbar[1]), kUmmaThreads);
+    umma::mbar_init(umma::smem_addr(&s_mbar[2]), 1);
+    umma::mbar_init(umma::smem_addr(&s_mbar[3]), 1);
+    s_abort = 0;
+    umma::mbar_init_fence();
+  }
+  if (tid < 32) {
+    umma::tmem_alloc(umma::smem_addr(&s_tmem), kUmmaTmemCols);
+    umma::tmem_relinquish();
+  }
+  umma_s_tiles_load(a, tiles);
+  umma::fence_proxy_async_smem();
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  encode_tables_build<BITS, MIXED>(T);
+  __syncthreads();
+  UmmaQjl U;
+  U.s_tiles = dyn + pad;
+  U.r_tiles = dyn + pad + 2 * kUmmaTile;
+  U.r_ptr = tiles + 2 * kUmmaTile;
+  U.info = s_info;
+  U.mbar = umma::smem_addr(&s_mbar[0]);
+  U.tmem = s_tmem;
+  U.abort = &s_abort;
+  encode_loop<BITS, true, MIXED, true>(T, a, -1, 0, 0, 1, &U);
+  umma::fence_before_sync();
+  __syncthreads();
+  if (tid < 32) {
+    umma::fence_after_sync();
+    umma::tmem_dealloc(U.tmem, kUmmaTmemCols);
+  }
 }
 
 // Keys and values of the same tokens in one launch (same bits, keys without
@@ -169,18 +222,22 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeArgs a) {
 // ----------------------------------------------------------------- launch --
 template <int BITS, bool QJL, bool MIXED = false>
 static cudaError_t launch_encode_t(const EncodeArgs &a, int sms, cudaStream_t st) {
-  const size_t smem = QJL ? (size_t)kM * kD * sizeof(float) : 0;
-  if (QJL) {
+  const int64_t vectors = a.n_tokens * a.H;
+  if constexpr (QJL) {
     static unsigned long long done = 0;
-    cudaError_t e = set_smem_once(encode_kernel<BITS, QJL, MIXED>, (int)smem, done);
+    cudaError_t e = set_smem_once(encode_qjl_kernel<BITS, MIXED>, (int)kUmmaDynSmem, done);
     if (e != cudaSuccess) return e;
+    int64_t blocks = (vectors + kUmmaRows - 1) / kUmmaRows;  // one batch of 128 vectors per block and pass
+    if (blocks > sms) blocks = sms;
+    if (blocks < 1) blocks = 1;
+    encode_qjl_kernel<BITS, MIXED><<<(unsigned)blocks, kUmmaThreads, kUmmaDynSmem, st>>>(a);
+  } else {
+    int64_t blocks = (vectors + 63) / 64;
+    const int64_t cap = (int64_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    encode_kernel<BITS, MIXED><<<(unsigned)blocks, 256, 0, st>>>(a);
   }
-  const int64_t quads = a.n_tokens * a.H;
-  int64_t blocks = (quads + 63) / 64;
-  const int64_t cap = (int64_t)sms * (QJL ? 3 : 8);
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  encode_kernel<BITS, QJL, MIXED><<<(unsigned)blocks, 256, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -6,6 +6,7 @@
 #pragma once
 
 #include "tq_internal.cuh"
+#include "tq_umma.cuh"
 
 namespace tq {
 
@@ -277,6 +278,127 @@ __device__ __forceinline__ void encode_tables_build(EncodeTables<MIXED> &T) {
   }
 }
 
+// ------------------------------------------------ QJL sketch on tcgen05 --
+// The bulk key encode with QJL computes the sketch products (S e)_l of a
+// batch of 128 vectors as one 128 x 128 x 128 contraction on the tensor cores:
+// D[v][l] = sum_j e_v[j] S[l][j], A = the residuals (rows = vectors), B = S
+// (rows = l), both fp16 hi/lo split in shared memory (K-major, 128-byte
+// swizzle: two 16 KB column blocks of 64 coordinates per 128-row tile), the
+// fp32 accumulator in tensor memory.  Three products (hi.hi, lo.hi, hi.lo)
+// give the same precision as the register path (the lo.lo term, ~2^-22 of
+// the product, is left out).  A CTA of 16 warps encodes 128 vectors per
+// iteration (8 per warp); warp w's vector g is row 8w + kUmmaRowOfQuad[g],
+// which puts the two vectors of every 8-lane store phase 4 rows apart (so
+// their swizzled chunks fall in different banks).  The residual tiles and the
+// accumulator are double-buffered: batch t's MMAs (issued by one thread once
+// all 512 threads have arrived on full[t&1]) run while the warps encode batch
+// t+1, and batch t's sign words are read back during iteration t+1.
+constexpr int kUmmaThreads = 512;
+constexpr int kUmmaRows = 128;                         // vectors per batch (MMA M)
+constexpr uint32_t kUmmaTile = 32768;                  // one 128 x 128 fp16 operand tile
+constexpr uint32_t kUmmaDynSmem = 6 * kUmmaTile + 1024;  // S hi/lo, 2 x residual hi/lo, alignment
+constexpr uint32_t kUmmaTmemCols = 256;                // 2 accumulators of 128 fp32 columns
+constexpr uint64_t kUmmaWaitNs = 1000000000ull;        // bounded waits: one second
+
+__device__ __forceinline__ int umma_row(int warp_in_block, int g) { return 8 * warp_in_block + ((g >> 1) | ((g & 1) << 2)); }
+
+// Byte offset of coordinates j .. j+7 (j a multiple of 8) of row r inside a
+// 128 x 128 fp16 tile: column block j / 64, chunk (j mod 64) / 8 swizzled by r.
+__device__ __forceinline__ uint32_t umma_tile_off(int r, int j) {
+  return (uint32_t)((j >> 6) * 16384 + r * 128 + ((((j & 63) >> 3) ^ (r & 7)) << 4));
+}
+
+struct UmmaQjl {
+  uint32_t s_tiles;   // S hi at +0, S lo at +kUmmaTile (shared-window address)
+  uint32_t r_tiles;   // residual buffer b at +2 kUmmaTile b: hi at +0, lo at +kUmmaTile
+  uint8_t *r_ptr;     // generic pointer of r_tiles
+  uint64_t *info;     // [4][128]: sign-word address of each row | 1 for a zero vector; 0 = not stored
+  uint32_t mbar;      // four mbarriers, 8 bytes apart: full(b) = mbar + 8 b, 512 arrivals
+                      // when residual buffer b is written; done(b) = mbar + 16 + 8 b,
+                      // the MMAs reading buffer b completed (tcgen05.commit)
+  __device__ __forceinline__ uint32_t full(int b) const { return mbar + 8u * (uint32_t)b; }
+  __device__ __forceinline__ uint32_t done(int b) const { return mbar + 16u + 8u * (uint32_t)b; }
+  uint32_t tmem;      // accumulator base: buffer b at column 128 b
+  int *abort;         // set when a bounded wait ran out; every warp then stops
+};
+
+// S as fp16 hi/lo B-operand tiles (every thread of the block).
+__device__ __forceinline__ void umma_s_tiles_load(const EncodeArgs &a, uint8_t *tiles) {
+  constexpr int N4 = kM * kD / 4;
+  const float4 *S4 = reinterpret_cast<const float4 *>(a.S);
+  for (int i0 = threadIdx.x; i0 < N4; i0 += 8 * blockDim.x) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int i4 = i0 + u * blockDim.x;
+      v[u] = i4 < N4 ? __ldg(S4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int i4 = i0 + u * blockDim.x;
+      if (i4 < N4) {
+        const int l = i4 / (kD / 4), j = 4 * (i4 % (kD / 4));
+        __half h0, l0, h1, l1, h2, l2, h3, l3;
+        split_half(v[u].x, h0, l0);
+        split_half(v[u].y, h1, l1);
+        split_half(v[u].z, h2, l2);
+        split_half(v[u].w, h3, l3);
+        const uint32_t o = umma_tile_off(l, j & ~7) + 2 * (j & 7);
+        *reinterpret_cast<uint2 *>(tiles + o) = make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(h2, h3));
+        *reinterpret_cast<uint2 *>(tiles + kUmmaTile + o) = make_uint2(pack_half2_raw(l0, l1), pack_half2_raw(l2, l3));
+      }
+    }
+  }
+}
+
+// The 24 MMAs of one batch (K = 128 in 8 steps of 16, three hi/lo products),
+// then the commit that arrives on done[buf].  One thread.
+__device__ __forceinline__ void umma_qjl_issue(const UmmaQjl &U, int buf) {
+  constexpr uint32_t idesc = umma::idesc_f16_f32<kUmmaRows, kM>();
+  const uint32_t d = U.tmem + 128u * (uint32_t)buf;
+  const uint32_t ra = U.r_tiles + 2u * kUmmaTile * (uint32_t)buf;
+#pragma unroll
+  for (int part = 0; part < 3; part++) {
+    const uint32_t a0 = ra + (part == 1 ? kUmmaTile : 0u);           // e hi, e lo, e hi
+    const uint32_t b0 = U.s_tiles + (part == 2 ? kUmmaTile : 0u);    // S hi, S hi, S lo
+#pragma unroll
+    for (int ks = 0; ks < 8; ks++) {
+      const uint32_t ko = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);  // 16 coordinates = 32 bytes
+      umma::mma_f16_ss(d, umma::desc_sw128_kmajor(a0 + ko), umma::desc_sw128_kmajor(b0 + ko), idesc,
+                       (part | ks) ? 1u : 0u);
+    }
+  }
+  umma::commit(U.done(buf));
+}
+
+// Sign words of batch t: warp w reads accumulator lanes 32 (w mod 4) .. +31
+// (its sub-partition: one row = one vector per thread) and columns
+// 32 (w / 4) .. +31, i.e. sign word w / 4 of each of its 32 vectors: bit i
+// is [(S e)_{32 (w/4) + i} >= 0], gathered MSB first by funnel shifts of the
+// fp32 sign bits and inverted.  Returns false (warp-uniform) when the
+// completion wait ran out or another warp had already given up.
+__device__ __forceinline__ bool umma_qjl_epilogue(const UmmaQjl &U, int64_t t, int32_t *err_word) {
+  const int buf = (int)(t & 1);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool ok = *reinterpret_cast<volatile int *>(U.abort) == 0;
+  if (ok && !umma::mbar_wait_bounded(U.done(buf), (uint32_t)((t >> 1) & 1), kUmmaWaitNs)) {
+    *reinterpret_cast<volatile int *>(U.abort) = 1;
+    report(err_word, TQ_DEVERR_TIMEOUT);
+    ok = false;
+  }
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  umma::fence_after_sync();
+  uint32_t v[32];
+  umma::ld_32x32b_x32(U.tmem + ((uint32_t)(32 * (w & 3)) << 16) + 128u * (uint32_t)buf + 32u * (uint32_t)(w >> 2), v);
+  uint32_t neg = 0u;
+#pragma unroll
+  for (int i = 31; i >= 0; i--) neg = __funnelshift_l(v[i], neg, 1);
+  const uint64_t inf = U.info[(t & 3) * kUmmaRows + 32 * (w & 3) + lane];
+  if (inf) reinterpret_cast<uint32_t *>(inf & ~(uint64_t)1)[w >> 2] = (inf & 1) ? 0u : ~neg;
+  umma::fence_before_sync();
+  return true;
+}
+
 // The vectors [n_tokens][H] of a.x (global or shared memory), 8 per warp and
 // step: warps [warp0, warp0 + nwarps) of the grid share them (a grid-stride
 // loop); the default is every warp of the grid.
@@ -284,9 +406,14 @@ __device__ __forceinline__ void encode_tables_build(EncodeTables<MIXED> &T) {
 // fills fewer octets than there are warps) share the projection: this warp
 // computes n-tiles [16 part / parts, 16 (part + 1) / parts) and stores only
 // the sign words they fill; part 0 stores codes, norm and gamma.
-template <int BITS, bool QJL, bool MIXED = false>
+// UMMA (QJL, a block of kUmmaThreads, the default warp range): the
+// projection runs on tcgen05 through U (see UmmaQjl); every warp of the block
+// runs the same number of iterations (whole batches of 128 vectors).
+template <int BITS, bool QJL, bool MIXED = false, bool UMMA = false>
 __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const EncodeArgs &a, int64_t warp0 = -1,
-                                            int64_t nwarps_in = 0, int part = 0, int parts = 1) {
+                                            int64_t nwarps_in = 0, int part = 0, int parts = 1,
+                                            const UmmaQjl *U = nullptr) {
+  static_assert(!UMMA || QJL, "the tensor-core path is the QJL projection");
   extern __shared__ __align__(16) uint4 s_Sq[];  // QJL only
   constexpr int L = 1 << BITS;
   const int tid = threadIdx.x;
@@ -334,7 +461,11 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
   constexpr bool kPairCodes = !MIXED && value_pairs_interleaved(BITS);
   const bool pairs = kPairCodes && a.grouped;
   const int64_t NV = pairs ? ((a.n_tokens + 1) & ~(int64_t)1) * a.H : NH;
-  for (int64_t vb = (int64_t)warp * 8; vb < NV; vb += nwarps * 8) {
+  int64_t t = 0;  // iteration (UMMA: batch of the block)
+  for (int64_t vb = (int64_t)warp * 8; (UMMA ? (vb & ~(int64_t)(kUmmaRows - 1)) : vb) < NV; vb += nwarps * 8, t++) {
+    if constexpr (UMMA) {
+      if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int *>(U->abort) != 0)) break;
+    }
     const int64_t v = vb + quad_in_warp;
     int64_t n;
     int h;
@@ -580,6 +711,47 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
       g2 += __shfl_xor_sync(0xffffffffu, g2, 1);
       g2 += __shfl_xor_sync(0xffffffffu, g2, 2);
       const float gamma = zero ? 0.f : sqrtf(g2) * 0.08838834764831845f;
+      if constexpr (UMMA) {
+        // residual hi/lo into this batch's A tiles, row r; the sign-word
+        // address (and the zero-vector flag) for the epilogue
+        const int r = umma_row(tid >> 5, quad_in_warp);
+        const int buf = (int)(t & 1);
+        uint8_t *rt = U->r_ptr + 2 * kUmmaTile * buf;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int p = 0; p < 4; p++) {
+            __half h0, l0, h1, l1;
+            split_half(x[8 * c + 2 * p], h0, l0);
+            split_half(x[8 * c + 2 * p + 1], h1, l1);
+            hw[p] = pack_half2_raw(h0, h1);
+            lw[p] = pack_half2_raw(l0, l1);
+          }
+          const uint32_t o = umma_tile_off(r, 32 * c + 8 * q);
+          *reinterpret_cast<uint4 *>(rt + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4 *>(rt + kUmmaTile + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        if (q == 0) {
+          U->info[(t & 3) * kUmmaRows + r] =
+              ok ? ((uint64_t)(uintptr_t)(slab + a.signs_off + off * (kM / 8)) | (zero ? 1u : 0u)) : 0ull;
+          if (ok) reinterpret_cast<float *>(slab + a.gamma_off)[off] = gamma;
+        }
+        umma::fence_proxy_async_smem();
+        umma::mbar_arrive(U->full(buf));
+        if (tid == kUmmaThreads - 32) {
+          // the issuer: the last warp's lane 0, once the whole batch is written
+          if (umma::mbar_wait_bounded(U->full(buf), (uint32_t)((t >> 1) & 1), kUmmaWaitNs)) {
+            umma::fence_after_sync();
+            umma_qjl_issue(*U, buf);
+          } else {
+            *reinterpret_cast<volatile int *>(U->abort) = 1;
+            report(a.err_word, TQ_DEVERR_TIMEOUT);
+          }
+        }
+        __syncwarp();
+        if (t > 0 && !umma_qjl_epilogue(*U, t - 1, a.err_word)) break;
+      } else {
       // (S e)_l on the tensor cores: rows g / g+8 of the A operand are the fp16
       // hi / lo parts of this quad's residual (vector g of the warp), B is
       // S hi then S lo, so the fp32 sum misses only the lo*lo term (~2^-22).
@@ -627,7 +799,12 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
         reinterpret_cast<uint32_t *>(slab + a.signs_off + off * (kM / 8))[q] = word;
         if (q == 0) reinterpret_cast<float *>(slab + a.gamma_off)[off] = gamma;
       }
+      }  // register path
     }
+  }
+  if constexpr (UMMA) {
+    // the last batch's sign words
+    if (t > 0) umma_qjl_epilogue(*U, t - 1, a.err_word);
   }
 }
 

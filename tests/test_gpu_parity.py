@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import tq_inputs as ti
-from tq_testlib import REL_ATTN, Scenario, compare_encoded, gpu_attention, rel_err
+from tq_testlib import REL_ATTN, Scenario, check_exemption_reach, compare_encoded, gpu_attention, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -79,6 +79,21 @@ def test_decode_matches_oracle(bits, kind, qjl):
 
 
 ORTH_SHRINK = 0.7 * math.sqrt(math.pi / 2) / math.sqrt(128)  # orthogonal S, 0.7 damping
+
+
+@pytest.mark.parametrize("bits,kmix", [(2, 0), (4, 0), (3, 1)])
+def test_encode_qjl_many_batches_matches_oracle(bits, kmix):
+    """Keys with QJL over more 128-vector batches than the grid has blocks
+    (40,024 vectors: every block runs two or three batches through both
+    residual/accumulator buffers, the last batch ragged), with zero vectors
+    and skipped tokens; every field against the oracle."""
+    fmt = ti.Format(128, bits, 4, 1, 128, 64, 8, k_mixed=kmix)
+    N = 5003
+    pool, pool_ref, lay, slots, cm, sm, *_ = _encode_case(fmt, 0, N, seed=40 + bits + 5 * kmix,
+                                                          zero_rows=(0, 2500, N - 1), neg_slots=(7, 4099))
+    st = compare_encoded(pool, pool_ref, lay, fmt, 0, slots, cm, sm)
+    check_exemption_reach(st, f"qjl many batches b{bits} mixed {kmix}")
+    print("qjl many batches", bits, kmix, st)
 
 
 @pytest.mark.parametrize("b,qjl,nc", [(3, 0, 0), (2, 0, 0), (3, 1, 0), (2, 1, 0), (3, 0, 1)])
