@@ -26,7 +26,8 @@ template <int BITS, bool MIXED>
 __global__ void __launch_bounds__(kUmmaThreads, 1) encode_qjl_kernel(const EncodeArgs a) {
   __shared__ EncodeTables<MIXED> T;
   __shared__ uint64_t s_info[4 * kUmmaRows];
-  __shared__ __align__(8) uint64_t s_mbar[4];  // full[0], full[1], done[0], done[1]
+  __shared__ __align__(8) uint64_t s_mbar[2];  // done(0), done(1)
+  __shared__ unsigned s_count[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   extern __shared__ __align__(16) uint4 s_Sq[];  // the operand tiles (1024-byte aligned below)
@@ -36,10 +37,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1) encode_qjl_kernel(const Encod
   uint8_t *tiles = reinterpret_cast<uint8_t *>(s_Sq) + pad;
   if (tid < kD) encode_tables_load<BITS, MIXED>(T, a, tid);
   if (tid == 0) {
-    umma::mbar_init(umma::smem_addr(&s_mbar[0]), kUmmaThreads);
-    umma::mbar_init(umma::smem_addr(&s_mbar[1]), kUmmaThreads);
-    umma::mbar_init(umma::smem_addr(&s_mbar[2]), 1);
-    umma::mbar_init(umma::smem_addr(&s_mbar[3]), 1);
+    umma::mbar_init(umma::smem_addr(&s_mbar[0]), 1);
+    umma::mbar_init(umma::smem_addr(&s_mbar[1]), 1);
+    s_count[0] = s_count[1] = 0u;
     s_abort = 0;
     umma::mbar_init_fence();
   }
@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1) encode_qjl_kernel(const Encod
   U.r_ptr = tiles + 2 * kUmmaTile;
   U.info = s_info;
   U.mbar = umma::smem_addr(&s_mbar[0]);
+  U.count = s_count;
   U.tmem = s_tmem;
   U.abort = &s_abort;
   encode_loop<BITS, true, MIXED, true>(T, a, -1, 0, 0, 1, &U);

@@ -290,9 +290,10 @@ __device__ __forceinline__ void encode_tables_build(EncodeTables<MIXED> &T) {
 // iteration (8 per warp); warp w's vector g is row 8w + kUmmaRowOfQuad[g],
 // which puts the two vectors of every 8-lane store phase 4 rows apart (so
 // their swizzled chunks fall in different banks).  The residual tiles and the
-// accumulator are double-buffered: batch t's MMAs (issued by one thread once
-// all 512 threads have arrived on full[t&1]) run while the warps encode batch
-// t+1, and batch t's sign words are read back during iteration t+1.
+// accumulator are double-buffered: batch t's MMAs (issued by lane 0 of the
+// last warp to finish its rows of buffer t&1, so that no thread waits for
+// the others) run while the warps encode batch t+1, and batch t's sign words
+// are read back during iteration t+1.
 constexpr int kUmmaThreads = 512;
 constexpr int kUmmaRows = 128;                         // vectors per batch (MMA M)
 constexpr uint32_t kUmmaTile = 32768;                  // one 128 x 128 fp16 operand tile
@@ -313,11 +314,11 @@ struct UmmaQjl {
   uint32_t r_tiles;   // residual buffer b at +2 kUmmaTile b: hi at +0, lo at +kUmmaTile
   uint8_t *r_ptr;     // generic pointer of r_tiles
   uint64_t *info;     // [4][128]: sign-word address of each row | 1 for a zero vector; 0 = not stored
-  uint32_t mbar;      // four mbarriers, 8 bytes apart: full(b) = mbar + 8 b, 512 arrivals
-                      // when residual buffer b is written; done(b) = mbar + 16 + 8 b,
-                      // the MMAs reading buffer b completed (tcgen05.commit)
-  __device__ __forceinline__ uint32_t full(int b) const { return mbar + 8u * (uint32_t)b; }
-  __device__ __forceinline__ uint32_t done(int b) const { return mbar + 16u + 8u * (uint32_t)b; }
+  uint32_t mbar;      // two mbarriers, 8 bytes apart: done(b) = mbar + 8 b, the MMAs
+                      // reading residual buffer b completed (tcgen05.commit)
+  unsigned *count;    // [2]: warps that have written their rows of buffer b (a running
+                      // count; the warp that makes it a multiple of 16 issues the MMAs)
+  __device__ __forceinline__ uint32_t done(int b) const { return mbar + 8u * (uint32_t)b; }
   uint32_t tmem;      // accumulator base: buffer b at column 128 b
   int *abort;         // set when a bounded wait ran out; every warp then stops
 };
@@ -722,11 +723,13 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int p = 0; p < 4; p++) {
-            __half h0, l0, h1, l1;
-            split_half(x[8 * c + 2 * p], h0, l0);
-            split_half(x[8 * c + 2 * p + 1], h1, l1);
-            hw[p] = pack_half2_raw(h0, h1);
-            lw[p] = pack_half2_raw(l0, l1);
+            // split_half of a pair, with paired conversions
+            const float x0 = x[8 * c + 2 * p], x1 = x[8 * c + 2 * p + 1];
+            const __half2 h = __floats2half2_rn(x0, x1);
+            const float2 hf = __half22float2(h);
+            const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+            hw[p] = *reinterpret_cast<const uint32_t *>(&h);
+            lw[p] = *reinterpret_cast<const uint32_t *>(&l);
           }
           const uint32_t o = umma_tile_off(r, 32 * c + 8 * q);
           *reinterpret_cast<uint4 *>(rt + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -737,16 +740,18 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
               ok ? ((uint64_t)(uintptr_t)(slab + a.signs_off + off * (kM / 8)) | (zero ? 1u : 0u)) : 0ull;
           if (ok) reinterpret_cast<float *>(slab + a.gamma_off)[off] = gamma;
         }
+        // this warp's rows are written: the warp whose arrival completes the
+        // batch issues its MMAs (release / acquire through the shared counter;
+        // the proxy fence makes the rows visible to the tensor core's reads)
         umma::fence_proxy_async_smem();
-        umma::mbar_arrive(U->full(buf));
-        if (tid == kUmmaThreads - 32) {
-          // the issuer: the last warp's lane 0, once the whole batch is written
-          if (umma::mbar_wait_bounded(U->full(buf), (uint32_t)((t >> 1) & 1), kUmmaWaitNs)) {
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          const unsigned before = atomicAdd(U->count + buf, 1u);
+          if ((before & (kUmmaThreads / 32 - 1)) == kUmmaThreads / 32 - 1) {
+            __threadfence_block();
             umma::fence_after_sync();
             umma_qjl_issue(*U, buf);
-          } else {
-            *reinterpret_cast<volatile int *>(U->abort) = 1;
-            report(a.err_word, TQ_DEVERR_TIMEOUT);
           }
         }
         __syncwarp();

@@ -25,14 +25,6 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
 // arrives on the barrier) before the CTA barrier that follows it.
 __device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
-// One arrival of this thread (release at CTA scope).
-__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
-  asm volatile(
-      "{\n\t.reg .b64 st;\n\t"
-      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(mbar)
-      : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
