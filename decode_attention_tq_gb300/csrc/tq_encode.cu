@@ -20,12 +20,12 @@ __global__ void __launch_bounds__(256, encode_min_blocks<BITS>()) encode_kernel(
 
 // Keys with QJL: the sketch products on tcgen05 (UmmaQjl in
 // tq_encode_body.cuh).  One block of 16 warps per SM: S hi/lo (64 KB) and
-// two residual buffers (2 x 64 KB) of 128-row operand tiles, 256 columns of
-// tensor memory for two fp32 accumulators.
+// two residual buffers (2 x 64 KB) of 128-row operand tiles, 512 columns of
+// tensor memory for three fp32 accumulators.
 template <int BITS, bool MIXED>
 __global__ void __launch_bounds__(kUmmaThreads, 1) encode_qjl_kernel(const EncodeArgs a) {
   __shared__ EncodeTables<MIXED> T;
-  __shared__ uint64_t s_info[4 * kUmmaRows];
+  __shared__ uint64_t s_info[kUmmaInfoRing * kUmmaRows];
   __shared__ __align__(8) uint64_t s_mbar[2];  // done(0), done(1)
   __shared__ unsigned s_count[2];
   __shared__ uint32_t s_tmem;

@@ -287,18 +287,21 @@ __device__ __forceinline__ void encode_tables_build(EncodeTables<MIXED> &T) {
 // fp32 accumulator in tensor memory.  Three products (hi.hi, lo.hi, hi.lo)
 // give the same precision as the register path (the lo.lo term, ~2^-22 of
 // the product, is left out).  A CTA of 16 warps encodes 128 vectors per
-// iteration (8 per warp); warp w's vector g is row 8w + kUmmaRowOfQuad[g],
-// which puts the two vectors of every 8-lane store phase 4 rows apart (so
-// their swizzled chunks fall in different banks).  The residual tiles and the
-// accumulator are double-buffered: batch t's MMAs (issued by lane 0 of the
-// last warp to finish its rows of buffer t&1, so that no thread waits for
-// the others) run while the warps encode batch t+1, and batch t's sign words
-// are read back during iteration t+1.
+// iteration (8 per warp); warp w's vector g is row umma_row(w, g), which
+// puts the two vectors of every 8-lane store phase 4 rows apart (so their
+// swizzled chunks fall in different banks).  Batch t's MMAs are issued by
+// lane 0 of the last warp to finish its rows of residual buffer t&1 (so
+// that no thread waits for the others) into accumulator t mod 3, and run
+// while the warps encode batches t+1 and t+2.  In iteration t+2 each warp
+// waits for them (their residual buffer is then free again) and reads batch
+// t's sign words back: the warps of a block may drift up to two batches
+// apart before one waits.
 constexpr int kUmmaThreads = 512;
 constexpr int kUmmaRows = 128;                         // vectors per batch (MMA M)
 constexpr uint32_t kUmmaTile = 32768;                  // one 128 x 128 fp16 operand tile
 constexpr uint32_t kUmmaDynSmem = 6 * kUmmaTile + 1024;  // S hi/lo, 2 x residual hi/lo, alignment
-constexpr uint32_t kUmmaTmemCols = 256;                // 2 accumulators of 128 fp32 columns
+constexpr uint32_t kUmmaTmemCols = 512;                // 3 accumulators of 128 fp32 columns (a power of 2)
+constexpr int kUmmaInfoRing = 8;                       // batches of sign-word addresses kept
 constexpr uint64_t kUmmaWaitNs = 1000000000ull;        // bounded waits: one second
 
 __device__ __forceinline__ int umma_row(int warp_in_block, int g) { return 8 * warp_in_block + ((g >> 1) | ((g & 1) << 2)); }
@@ -313,13 +316,14 @@ struct UmmaQjl {
   uint32_t s_tiles;   // S hi at +0, S lo at +kUmmaTile (shared-window address)
   uint32_t r_tiles;   // residual buffer b at +2 kUmmaTile b: hi at +0, lo at +kUmmaTile
   uint8_t *r_ptr;     // generic pointer of r_tiles
-  uint64_t *info;     // [4][128]: sign-word address of each row | 1 for a zero vector; 0 = not stored
+  uint64_t *info;     // [kUmmaInfoRing][128]: sign-word address of each row | 1 for a zero
+                      // vector; 0 = not stored
   uint32_t mbar;      // two mbarriers, 8 bytes apart: done(b) = mbar + 8 b, the MMAs
                       // reading residual buffer b completed (tcgen05.commit)
   unsigned *count;    // [2]: warps that have written their rows of buffer b (a running
                       // count; the warp that makes it a multiple of 16 issues the MMAs)
   __device__ __forceinline__ uint32_t done(int b) const { return mbar + 8u * (uint32_t)b; }
-  uint32_t tmem;      // accumulator base: buffer b at column 128 b
+  uint32_t tmem;      // accumulator base: batch t at column 128 (t mod 3)
   int *abort;         // set when a bounded wait ran out; every warp then stops
 };
 
@@ -352,11 +356,14 @@ __device__ __forceinline__ void umma_s_tiles_load(const EncodeArgs &a, uint8_t *
   }
 }
 
-// The 24 MMAs of one batch (K = 128 in 8 steps of 16, three hi/lo products),
-// then the commit that arrives on done[buf].  One thread.
-__device__ __forceinline__ void umma_qjl_issue(const UmmaQjl &U, int buf) {
+__device__ __forceinline__ uint32_t umma_acc_col(int64_t t) { return 128u * (uint32_t)(t % 3); }
+
+// The 24 MMAs of batch t (K = 128 in 8 steps of 16, three hi/lo products),
+// then the commit that arrives on done(t & 1).  One thread.
+__device__ __forceinline__ void umma_qjl_issue(const UmmaQjl &U, int64_t t) {
   constexpr uint32_t idesc = umma::idesc_f16_f32<kUmmaRows, kM>();
-  const uint32_t d = U.tmem + 128u * (uint32_t)buf;
+  const int buf = (int)(t & 1);
+  const uint32_t d = U.tmem + umma_acc_col(t);
   const uint32_t ra = U.r_tiles + 2u * kUmmaTile * (uint32_t)buf;
 #pragma unroll
   for (int part = 0; part < 3; part++) {
@@ -372,32 +379,36 @@ __device__ __forceinline__ void umma_qjl_issue(const UmmaQjl &U, int buf) {
   umma::commit(U.done(buf));
 }
 
-// Sign words of batch t: warp w reads accumulator lanes 32 (w mod 4) .. +31
-// (its sub-partition: one row = one vector per thread) and columns
-// 32 (w / 4) .. +31, i.e. sign word w / 4 of each of its 32 vectors: bit i
-// is [(S e)_{32 (w/4) + i} >= 0], gathered MSB first by funnel shifts of the
-// fp32 sign bits and inverted.  Returns false (warp-uniform) when the
-// completion wait ran out or another warp had already given up.
-__device__ __forceinline__ bool umma_qjl_epilogue(const UmmaQjl &U, int64_t t, int32_t *err_word) {
-  const int buf = (int)(t & 1);
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Waits until batch t's MMAs have completed (its residual buffer is free and
+// its accumulator ready).  Warp-uniform; false when the wait ran out here or
+// another warp had already given up.
+__device__ __forceinline__ bool umma_qjl_wait(const UmmaQjl &U, int64_t t, int32_t *err_word) {
   bool ok = *reinterpret_cast<volatile int *>(U.abort) == 0;
-  if (ok && !umma::mbar_wait_bounded(U.done(buf), (uint32_t)((t >> 1) & 1), kUmmaWaitNs)) {
+  if (ok && !umma::mbar_wait_bounded(U.done((int)(t & 1)), (uint32_t)((t >> 1) & 1), kUmmaWaitNs)) {
     *reinterpret_cast<volatile int *>(U.abort) = 1;
     report(err_word, TQ_DEVERR_TIMEOUT);
     ok = false;
   }
-  if (!__all_sync(0xffffffffu, ok)) return false;
-  umma::fence_after_sync();
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok) umma::fence_after_sync();
+  return ok;
+}
+
+// Sign words of batch t (after umma_qjl_wait): warp w reads accumulator
+// lanes 32 (w mod 4) .. +31 (its sub-partition: one row = one vector per
+// thread) and columns 32 (w / 4) .. +31, i.e. sign word w / 4 of each of its
+// 32 vectors: bit i is [(S e)_{32 (w/4) + i} >= 0], gathered MSB first by
+// funnel shifts of the fp32 sign bits and inverted.
+__device__ __forceinline__ void umma_qjl_signs(const UmmaQjl &U, int64_t t) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t v[32];
-  umma::ld_32x32b_x32(U.tmem + ((uint32_t)(32 * (w & 3)) << 16) + 128u * (uint32_t)buf + 32u * (uint32_t)(w >> 2), v);
+  umma::ld_32x32b_x32(U.tmem + ((uint32_t)(32 * (w & 3)) << 16) + umma_acc_col(t) + 32u * (uint32_t)(w >> 2), v);
   uint32_t neg = 0u;
 #pragma unroll
   for (int i = 31; i >= 0; i--) neg = __funnelshift_l(v[i], neg, 1);
-  const uint64_t inf = U.info[(t & 3) * kUmmaRows + 32 * (w & 3) + lane];
+  const uint64_t inf = U.info[(t & (kUmmaInfoRing - 1)) * kUmmaRows + 32 * (w & 3) + lane];
   if (inf) reinterpret_cast<uint32_t *>(inf & ~(uint64_t)1)[w >> 2] = (inf & 1) ? 0u : ~neg;
   umma::fence_before_sync();
-  return true;
 }
 
 // The vectors [n_tokens][H] of a.x (global or shared memory), 8 per warp and
@@ -427,13 +438,15 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
   const int set = MIXED ? (q & 1) : 0;
   const float *cent = T.cent + 16 * set, *midp = T.mid + 16 * set;
   const uint2 *qlut = T.qlut + set * kQBuckets;
-  const float2 *qcen = T.qcen + set * kQBuckets;
   // shared-window addresses of the bucket tables, offset so that the bucket
   // entry of the magic-number sum s (quant_bucket) is at base + 8 * bits(s)
   // (one shift-add per coordinate; the sums wrap mod 2^32 as addresses do)
   const uint32_t kMagicBits = (uint32_t)__float_as_int(12582912.0f);
+  // (the centroid pairs qcen follow qlut: the same entry is kQcenOff bytes on)
   const uint32_t qlut_at = (uint32_t)__cvta_generic_to_shared(qlut) - 8u * kMagicBits;
-  const uint32_t qcen_at = (uint32_t)__cvta_generic_to_shared(qcen) - 8u * kMagicBits;
+  constexpr int kQcenOff = (int)(sizeof(uint2) * EncodeTables<MIXED>::NSET * kQBuckets);
+  static_assert(offsetof(EncodeTables<MIXED>, qcen) - offsetof(EncodeTables<MIXED>, qlut) == kQcenOff,
+                "qcen directly after qlut");
   const bool lut_bad = (T.lut_bad >> set) & 1;
   const bool small = NH <= 0x7fffffff;
   // sign masks of this thread's fp16 pairs (coordinates 32c + 8q + 2p, +1)
@@ -564,7 +577,7 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
         idx[j] = (int)e.x + (up ? 1 : 0);  // a zero vector's codes are cleared when packed
         if constexpr (QJL) {
           float2 c;
-          asm("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(c.x), "=f"(c.y) : "r"(qcen_at + sb));
+          asm("ld.shared.v2.f32 {%0,%1}, [%2+%3];" : "=f"(c.x), "=f"(c.y) : "r"(qlut_at + sb), "n"(kQcenOff));
           x[j] = u - (up ? c.y : c.x);  // residual in u units (unused for a zero vector: gamma, bits 0)
         }
       }
@@ -713,6 +726,8 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
       g2 += __shfl_xor_sync(0xffffffffu, g2, 2);
       const float gamma = zero ? 0.f : sqrtf(g2) * 0.08838834764831845f;
       if constexpr (UMMA) {
+        // batch t-2's MMAs done: its residual buffer is this batch's
+        if (t >= 2 && !umma_qjl_wait(*U, t - 2, a.err_word)) break;
         // residual hi/lo into this batch's A tiles, row r; the sign-word
         // address (and the zero-vector flag) for the epilogue
         const int r = umma_row(tid >> 5, quad_in_warp);
@@ -736,7 +751,7 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
           *reinterpret_cast<uint4 *>(rt + kUmmaTile + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         if (q == 0) {
-          U->info[(t & 3) * kUmmaRows + r] =
+          U->info[(t & (kUmmaInfoRing - 1)) * kUmmaRows + r] =
               ok ? ((uint64_t)(uintptr_t)(slab + a.signs_off + off * (kM / 8)) | (zero ? 1u : 0u)) : 0ull;
           if (ok) reinterpret_cast<float *>(slab + a.gamma_off)[off] = gamma;
         }
@@ -751,11 +766,11 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
           if ((before & (kUmmaThreads / 32 - 1)) == kUmmaThreads / 32 - 1) {
             __threadfence_block();
             umma::fence_after_sync();
-            umma_qjl_issue(*U, buf);
+            umma_qjl_issue(*U, t);
           }
         }
         __syncwarp();
-        if (t > 0 && !umma_qjl_epilogue(*U, t - 1, a.err_word)) break;
+        if (t >= 2) umma_qjl_signs(*U, t - 2);
       } else {
       // (S e)_l on the tensor cores: rows g / g+8 of the A operand are the fp16
       // hi / lo parts of this quad's residual (vector g of the warp), B is
@@ -808,8 +823,9 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
     }
   }
   if constexpr (UMMA) {
-    // the last batch's sign words
-    if (t > 0) umma_qjl_epilogue(*U, t - 1, a.err_word);
+    // the last two batches' sign words
+    for (int64_t s = t >= 2 ? t - 2 : 0; s < t; s++)
+      if (umma_qjl_wait(*U, s, a.err_word)) umma_qjl_signs(*U, s);
   }
 }
 

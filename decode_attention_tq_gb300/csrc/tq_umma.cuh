@@ -37,13 +37,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with a suspend-time hint: the thread may sleep up to hint_ns
+// (waking when the phase completes) instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t mbar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(mbar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete, for at most
 // limit_ns of wall-clock time; false when the time ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(mbar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-    if (mbar_try_wait(mbar, parity)) return true;
+    if (mbar_try_wait_sleep(mbar, parity, 20000u)) return true;
     if (globaltimer() - t0 > limit_ns) return false;
   }
 }
