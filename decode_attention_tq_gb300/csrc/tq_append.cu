@@ -75,8 +75,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const RollArgs r
   // overlap that kernel's end).
   griddep_wait();
   // A kernel launched after this one as a programmatic dependent (the
-  // attention's prep kernel) may start now: it waits for this grid to
-  // complete before it reads anything.
+  // attention's prep kernel) may start now: before it waits for this grid it
+  // reads only the attention call's inputs (query, S, sign flips).
   griddep_launch_dependents();
 
   // 1. counters, new tokens, tables

@@ -65,7 +65,7 @@ __device__ void prep_lengths(const AttnArgs &a, int lane) {
 // (a raw-domain KIVI cache takes the query as it is): lane holds
 // coordinates 4 lane .. 4 lane + 3.
 __device__ __forceinline__ void rotate_query(const AttnArgs &a, int64_t row, int lane, float (&x)[4]) {
-  const uint2 raw = *reinterpret_cast<const uint2 *>(a.q + row * kD + 4 * lane);
+  const uint2 raw = __ldcg(reinterpret_cast<const uint2 *>(a.q + row * kD + 4 * lane));
   const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
   const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
   x[0] = f01.x;
@@ -75,7 +75,7 @@ __device__ __forceinline__ void rotate_query(const AttnArgs &a, int64_t row, int
   if (!a.raw) {
 #pragma unroll
     for (int i = 0; i < 4; i++)
-      if (a.k_signs[4 * lane + i]) x[i] = -x[i];
+      if (__ldcg(a.k_signs + 4 * lane + i)) x[i] = -x[i];
     fwht_local<4>(x);
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) fwht_xlane<4>(x, m, (lane & m) != 0);
@@ -118,7 +118,6 @@ __device__ void prep_query(const AttnArgs &a, int64_t row, int lane) {
   if (lane == 0) {
     a.q_exp[row * 2 + 1] = 0;
     a.q_cst[row].y = 0.f;
-    a.merge_cnt[row] = 0;
   }
 }
 
@@ -136,7 +135,7 @@ __device__ void prep_query_qjl(const AttnArgs &a, int64_t row, int warp, int lan
   float4 sv[R];
   const float4 *S4 = reinterpret_cast<const float4 *>(a.S + (int64_t)(R * warp) * kD) + lane;
 #pragma unroll
-  for (int i = 0; i < R; i++) sv[i] = __ldg(S4 + i * (kD / 4));
+  for (int i = 0; i < R; i++) sv[i] = __ldcg(S4 + i * (kD / 4));
   float x[4];
   rotate_query(a, row, lane, x);
   if (warp == 0) store_query(a, row, lane, x);
@@ -174,7 +173,6 @@ __device__ void prep_query_qjl(const AttnArgs &a, int64_t row, int warp, int lan
     op[2 * (192 + 16 * t) + qop_qjl_half(i)] = lo;
   }
   if (threadIdx.x == 0) {
-    a.merge_cnt[row] = 0;
     a.q_exp[row * 2 + 1] = es;
     // qjl_coef / sqrt(d) (qjl_coef = sqrt(pi/2) / m for the paper's Gaussian S)
     a.q_cst[row].y = ldexpf(kLog2e * a.qjl_coef / 11.313708498984761f, -es);
@@ -284,12 +282,12 @@ __device__ void prep_window(const AttnArgs &a, int64_t unit, int c, float *s_q, 
 __global__ void __launch_bounds__(256) attn_prep_kernel(const AttnArgs a, bool qjl, int row_blocks) {
   __shared__ __align__(16) float s_q[8 * kQRow];
   __shared__ float s_p[8][kWinChunk];
-  // Launched as a programmatic dependent of whatever kernel precedes it in
-  // the stream: nothing is read before that kernel has completed.
-  griddep_wait();
-  griddep_launch_dependents();  // the main kernel may start building its tables
+  // Launched as a programmatic dependent of the kernel before it in the
+  // stream (the append).
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (blockIdx.x >= row_blocks) {  // window chunk blocks
+  if (blockIdx.x >= row_blocks) {  // window chunk blocks: they read the rings the append writes
+    griddep_wait();
+    griddep_launch_dependents();  // the main kernel may start building its tables
     const int64_t nch = (a.window + kWinChunk - 1) / kWinChunk;
     const int64_t k = blockIdx.x - row_blocks;
     if (a.G <= 4)
@@ -298,7 +296,12 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const AttnArgs a, bool q
       prep_window<8>(a, k / nch, (int)(k % nch), s_q, s_p);
     return;
   }
-  if (blockIdx.x == 0 && warp == 0) prep_lengths(a, lane);
+  // Query rows before the grid wait, beside the kernel before this one: they
+  // read only the call's inputs (q, S, the key sign flips, through L2), which
+  // no kernel of this library writes, and write q_rot, q_op, q_exp and q_cst,
+  // which only this call's main kernel reads (it waits for this grid; the
+  // previous call's main kernel completed before the kernel before this one
+  // let it launch).
   if (qjl) {  // one row per block (b * Hq + qh)
     if (blockDim.x == 256)
       prep_query_qjl<8>(a, blockIdx.x, warp, lane, s_q);
@@ -307,6 +310,19 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const AttnArgs a, bool q
   } else {
     const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // b * Hq + qh
     if (row < (int64_t)a.B * a.Hq) prep_query(a, row, lane);
+  }
+  // After the grid wait: the lengths the append updates, and the merge
+  // counters, which the previous call's merge may still be using until then.
+  // The main kernel launches from here (launched earlier, beside the
+  // append, its blocks measured slower once they ran).
+  griddep_wait();
+  griddep_launch_dependents();  // the main kernel may start building its tables
+  if (blockIdx.x == 0 && warp == 0) prep_lengths(a, lane);
+  if (qjl) {
+    if (threadIdx.x == 0) a.merge_cnt[blockIdx.x] = 0;
+  } else {
+    const int64_t row = (int64_t)blockIdx.x * 4 + warp;
+    if (lane == 0 && row < (int64_t)a.B * a.Hq) a.merge_cnt[row] = 0;
   }
 }
 

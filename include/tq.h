@@ -307,6 +307,12 @@ tq_status tq_decode_attn_workspace_size(const tq_format *fmt, int batch, int num
  *                bytes, 256-byte aligned; overwritten by every call, so calls
  *                that overlap on the GPU need separate workspaces
  *   err_word     device int32 or NULL (TQ_DEVERR_PAGE_RANGE / _LENGTH)
+ * Stream order: the call's kernels are launched as programmatic dependents
+ * of the kernel before them.  The first one reads q_f16, S and k_signs
+ * before that kernel has completed when that kernel lets its dependents
+ * launch early (as tq_append_window does once the work before it has
+ * completed); everything else waits for it.  A kernel of the caller that
+ * lets dependents launch early must have written those three by then.
  */
 tq_status tq_decode_attn(const tq_format *fmt, int batch, int num_q_heads, const void *q_f16,
                          const void *page_pool, int64_t num_pages, const int32_t *block_tables,
