@@ -467,31 +467,45 @@ __global__ void __launch_bounds__(attn_threads(NT, QJL), 1) attn_main_kernel(con
   };
   uint32_t *const tab32 = reinterpret_cast<uint32_t *>(tables);
   uint2 *const tab64 = reinterpret_cast<uint2 *>(tables);
+  // One thread per entry: its value once, stored to the 32 lane copies with
+  // 16-byte stores whose chunk order is rotated by the entry, so the eight
+  // stores of a wavefront fall in different banks.  fill32: entry e's copies
+  // are words w0 + 64 e .. + 31; fill64: 8-byte slots p0 + 32 e .. + 31.
+  auto fill32 = [&](uint32_t w0, int E, auto val) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const uint32_t v = val(e);
+      const uint4 q4 = make_uint4(v, v, v, v);
+      uint4 *d = reinterpret_cast<uint4 *>(tab32 + w0 + 64 * e);
+#pragma unroll
+      for (int k = 0; k < 8; k++) d[(k + e) & 7] = q4;
+    }
+  };
+  auto fill64 = [&](uint32_t p0, int E, auto val) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const uint2 v = val(e);
+      const uint4 q4 = make_uint4(v.x, v.y, v.x, v.y);
+      uint4 *d = reinterpret_cast<uint4 *>(tab64 + p0 + 32 * e);
+#pragma unroll
+      for (int k = 0; k < 16; k++) d[(k + e) & 15] = q4;
+    }
+  };
   if constexpr (byte_keys<KB>()) {
     // 2-bit keys: indexed by a code byte (pair 2k in the low nibble, 2k + 1 high)
-    for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
-      const int e = i >> 5;
-      tab64[kKeyOff / 8 + i] = make_uint2(pair_of(a.k_cb, 2, e & 15), pair_of(a.k_cb, 2, e >> 4));
-    }
+    fill64(kKeyOff / 8, 256, [&](int e) { return make_uint2(pair_of(a.k_cb, 2, e & 15), pair_of(a.k_cb, 2, e >> 4)); });
   } else {
-    for (int i = threadIdx.x; i < EK * 32; i += blockDim.x)
-      tab32[kKeyOff / 4 + (i >> 5) * 64 + (i & 31)] = pair_of(a.k_cb, kb_hi(KB), i >> 5);
+    fill32(kKeyOff / 4, EK, [&](int e) { return pair_of(a.k_cb, kb_hi(KB), e); });
   }
   if constexpr (kb_mixed(KB)) {
     // low channels: the k_bits codebook follows the (k_bits + 1) one
     constexpr int HB = kb_hi(KB), LB = kb_lo(KB), EL = 1 << (2 * LB);
     const float *cb_lo = a.k_cb + (2 << HB) - 1;
-    for (int i = threadIdx.x; i < EL * 32; i += blockDim.x)
-      tab32[key_lo_table_off<KB, VB>() / 4 + (i >> 5) * 64 + (i & 31)] = pair_of(cb_lo, LB, i >> 5);
+    fill32(key_lo_table_off<KB, VB>() / 4, EL, [&](int e) { return pair_of(cb_lo, LB, e); });
   }
   if constexpr (byte_values<VB>()) {
     // 2-bit values: indexed by a byte of the interleaved codes (two coordinates)
-    for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
-      const int e = i >> 5;
-      tab64[i] = make_uint2(pair_of(a.v_cb, VB, e & 15), pair_of(a.v_cb, VB, e >> 4));
-    }
+    fill64(0, 256, [&](int e) { return make_uint2(pair_of(a.v_cb, VB, e & 15), pair_of(a.v_cb, VB, e >> 4)); });
   } else {
-    for (int i = threadIdx.x; i < EV * 32; i += blockDim.x) tab32[(i >> 5) * 64 + (i & 31)] = pair_of(a.v_cb, VB, i >> 5);
+    fill32(0, EV, [&](int e) { return pair_of(a.v_cb, VB, e); });
   }
   __syncthreads();
   // Up to here only the codebooks were read; launched as a dependent of the
