@@ -15,7 +15,7 @@ constexpr int encode_min_blocks() {
 
 template <int BITS, bool MIXED = false>
 __global__ void __launch_bounds__(256, encode_min_blocks<BITS>()) encode_kernel(const EncodeArgs a) {
-  encode_body<BITS, false, MIXED>(a);
+  encode_body<BITS, MIXED>(a);
 }
 
 // Keys with QJL: the sketch products on tcgen05 (UmmaQjl in
@@ -77,9 +77,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1) encode_qjl_kernel(const Encod
 template <int BITS>
 __global__ void __launch_bounds__(256, kEncodeBlocks4) encode_kv_kernel(const EncodeArgs ka, const EncodeArgs va) {
   if (blockIdx.y == 0)
-    encode_body<BITS, false>(ka);
+    encode_body<BITS>(ka);
   else
-    encode_body<BITS, false>(va);
+    encode_body<BITS>(va);
 }
 
 // 16 codes of W bits from byte `off` of a key stream, as a 64-bit value.

@@ -178,9 +178,10 @@ constexpr int kEncodeBlocks4 = 3;
 // quantizes with one codebook set: set 0 (high) or set 1 (low).
 //
 // The encode runs in three parts: encode_tables_load (global loads of the
-// codebook and sign flips into shared memory, plus the QJL matrix cells),
-// then after a block barrier encode_tables_build (the quantizer's bucket
-// table), then after another barrier encode_loop (the vectors).  A kernel
+// codebook and sign flips into shared memory; the kernels with a QJL sketch
+// also stage S, as hi/lo cells or as tcgen05 operand tiles), then after a
+// block barrier encode_tables_build (the quantizer's bucket table), then
+// after another barrier encode_loop (the vectors).  A kernel
 // that encodes two kinds keeps two table sets and overlaps their loads.
 template <bool MIXED>
 struct EncodeTables {
@@ -245,14 +246,6 @@ __device__ __forceinline__ void encode_s_batch_store(int i0, const float4 (&v)[k
       cells[2 * cell] = make_uint2(pack_half2_raw(h0, h1), pack_half2_raw(h2, h3));
       cells[2 * cell + 1] = make_uint2(pack_half2_raw(l0, l1), pack_half2_raw(l2, l3));
     }
-  }
-}
-__device__ __forceinline__ void encode_s_cells_load(const EncodeArgs &a) {
-  constexpr int N4 = kM * kD / 4;
-  for (int i0 = threadIdx.x; i0 < N4; i0 += kSCellBatch * blockDim.x) {
-    float4 v[kSCellBatch];
-    encode_s_batch_load(a, i0, v);
-    encode_s_batch_store(i0, v);
   }
 }
 
@@ -830,16 +823,16 @@ __device__ __forceinline__ void encode_loop(const EncodeTables<MIXED> &T, const 
 }
 
 
-// Load, build and loop in one call (kernels that encode one kind).
-template <int BITS, bool QJL, bool MIXED = false>
+// Load, build and loop in one call (kernels that encode one kind without a
+// QJL sketch; keys with one run encode_qjl_kernel or the append).
+template <int BITS, bool MIXED = false>
 __device__ __forceinline__ void encode_body(const EncodeArgs &a, int64_t warp0 = -1, int64_t nwarps_in = 0) {
   __shared__ EncodeTables<MIXED> T;
   if (threadIdx.x < kD) encode_tables_load<BITS, MIXED>(T, a, threadIdx.x);
-  if constexpr (QJL) encode_s_cells_load(a);
   __syncthreads();
   encode_tables_build<BITS, MIXED>(T);
   __syncthreads();
-  encode_loop<BITS, QJL, MIXED>(T, a, warp0, nwarps_in);
+  encode_loop<BITS, false, MIXED>(T, a, warp0, nwarps_in);
 }
 
 }  // namespace tq
