@@ -110,6 +110,11 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32() {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The two encodings worked out by hand for the operands used here.
+static_assert(idesc_f16_f32<128, 128>() == 0x08200010u, "D f32 = 1 << 4, N / 8 = 16 << 17, M / 16 = 8 << 24");
+static_assert(desc_sw128_kmajor(0x400u) == 0x4000404000010040ull,
+              "start 0x400 >> 4, LBO 1 << 16, SBO 64 << 32, version 1 << 46, 128-byte swizzle 2 << 61");
+
 // --------------------------------------------------------------- the MMA
 // D[M x N] (tensor memory, fp32) = A[M x K] B[N x K]^T (+ D when accumulate),
 // K = 16, both operands in shared memory.  Issued by one thread.
