@@ -18,7 +18,9 @@
  *     outside the pool, a length larger than its buffer) never trap: the
  *     kernel skips the offending token/page and ORs a TQ_DEVERR_* bit into
  *     the caller's optional int32 *err_word (device memory, may be NULL).
- *   - No kernel waits on another, and no kernel spins on a flag or barrier.
+ *   - No kernel spins on another kernel or on a flag another block sets.  The
+ *     one polled wait is inside the QJL key encode: a block waits, with a
+ *     one-second limit, for its own tensor-core products (TQ_DEVERR_TIMEOUT).
  *
  * Format (tq_format): d = head_dim, b_K / b_V = bits per coordinate of the
  * Lloyd-Max codes, optional 1-bit QJL residual sketch of length m on keys,
